@@ -56,21 +56,68 @@ GEMM_RTOL, GEMM_ATOL = 5e-3, 1e-5   # tensor-core path (A rounded to bf16)
 # --------------------------------------------------------------------------
 # f32 <-> f16 (lattice-inference 0.1.2, metal_qwen35.rs, f32_to_f16)
 # --------------------------------------------------------------------------
-def _round_shift_right_even(value: np.ndarray, shift: np.ndarray) -> np.ndarray:
-    """value >> shift, rounded to nearest with ties to even (uint64 math)."""
-    value = value.astype(np.uint64)
-    shift = shift.astype(np.uint64)
-    out = np.zeros_like(value)
+def _round_shift_right_even(value: np.ndarray, shift) -> np.ndarray:
+    """value >> shift, rounded to nearest with ties to even (page's
+    ``round_shift_right_even``): shift 0 keeps the value, shift >= 32 gives 0."""
+    value = np.asarray(value).astype(np.uint64)
+    shift = np.broadcast_to(np.asarray(shift, dtype=np.int64), value.shape)
     big = shift >= 32
-    s = np.where(big, 1, np.maximum(shift, 1)).astype(np.uint64)
+    s = np.clip(shift, 1, 31).astype(np.uint64)
     base = value >> s
     rem = value & ((np.uint64(1) << s) - np.uint64(1))
     half = np.uint64(1) << (s - np.uint64(1))
     up = (rem > half) | ((rem == half) & ((base & np.uint64(1)) == 1))
     rounded = base + up.astype(np.uint64)
     out = np.where(shift == 0, value, rounded)
-    out = np.where(big, np.uint64(0), out)
-    return out
+    return np.where(big, np.uint64(0), out)
+
+
+_CHUNK = 1 << 22
+
+
+def _f32_to_f16_chunk(bits: np.ndarray) -> np.ndarray:
+    sign = ((bits >> 16) & 0x8000).astype(np.uint32)
+    exp = ((bits >> 23) & 0xFF).astype(np.int32)
+    frac = bits & np.uint32(0x7FFFFF)
+    e = exp - 127
+    out = sign.copy()                      # zero and f32 subnormals -> signed zero
+
+    # normal f16 range: round the 23-bit fraction to 10 bits, a carry bumps
+    # the exponent (possibly to infinity)
+    normal = (exp != 0) & (exp != 0xFF) & (e >= -14) & (e <= 15)
+    if normal.any():
+        f = frac[normal]
+        base = f >> 13
+        rem = f & np.uint32(0x1FFF)
+        up = (rem > 0x1000) | ((rem == 0x1000) & ((base & 1) == 1))
+        frac16 = base + up.astype(np.uint32)
+        exp16 = (e[normal] + 15).astype(np.uint32)
+        carry = frac16 == 0x400
+        exp16 = exp16 + carry.astype(np.uint32)
+        frac16 = np.where(carry, np.uint32(0), frac16)
+        val = np.where(exp16 >= 0x1F, np.uint32(0x7C00), (exp16 << 10) | frac16)
+        out[normal] = sign[normal] | val
+
+    # overflow to infinity
+    over = (exp != 0) & (exp != 0xFF) & (e > 15)
+    out[over] = sign[over] | 0x7C00
+
+    # subnormal f16 range: shift the 24-bit significand right by (-e - 1)
+    sub = (exp != 0) & (exp != 0xFF) & (e < -14)
+    if sub.any():
+        mant = frac[sub] | np.uint32(0x800000)
+        v = _round_shift_right_even(mant, (-e[sub] - 1)).astype(np.uint32)
+        # 0 stays signed zero; 0x400 is the smallest normal, both fit as-is
+        out[sub] = sign[sub] | v
+
+    # Inf / NaN (NaN keeps its top payload bits and gets the quiet bit)
+    special = exp == 0xFF
+    if special.any():
+        f = frac[special]
+        payload = (f >> 13) & 0x3FF
+        payload = np.where(payload == 0, np.uint32(1), payload) | 0x200
+        out[special] = sign[special] | 0x7C00 | np.where(f == 0, np.uint32(0), payload)
+    return out.astype(np.uint16)
 
 
 def f32_to_f16_bits(x) -> np.ndarray:
@@ -81,63 +128,27 @@ def f32_to_f16_bits(x) -> np.ndarray:
     exponents above 15 overflow to infinity, the normal range rounds the
     23-bit fraction to 10 bits (a carry bumps the exponent, possibly to
     infinity), and the subnormal range shifts the 24-bit significand right by
-    (-e - 1) with round-to-nearest-even.
+    (-e - 1) with round-to-nearest-even. Works through the input in chunks.
     """
-    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    sign = ((bits >> 16) & 0x8000).astype(np.uint64)
-    exp = ((bits >> 23) & 0xFF).astype(np.int64)
-    frac = bits & 0x7FFFFF
-    out = np.zeros(bits.shape, dtype=np.uint64)
-
-    # Inf / NaN
-    is_special = exp == 0xFF
-    payload = (frac >> 13) & 0x3FF
-    payload = np.where(payload == 0, 1, payload) | 0x200
-    out = np.where(is_special & (frac == 0), sign | 0x7C00, out)
-    out = np.where(is_special & (frac != 0), sign | 0x7C00 | payload, out)
-
-    # zero or f32 subnormal -> signed zero
-    is_zero = exp == 0
-    out = np.where(is_zero, sign, out)
-
-    e = exp - 127
-    ordinary = ~is_special & ~is_zero
-    overflow = ordinary & (e > 15)
-    out = np.where(overflow, sign | 0x7C00, out)
-
-    normal = ordinary & (e <= 15) & (e >= -14)
-    exp16 = (e + 15).astype(np.int64)
-    frac16 = _round_shift_right_even(frac, np.full(frac.shape, 13)).astype(np.int64)
-    carry = frac16 == 0x400
-    exp16 = np.where(carry, exp16 + 1, exp16)
-    frac16 = np.where(carry, 0, frac16)
-    norm_bits = np.where(exp16 >= 0x1F, sign | 0x7C00,
-                         sign | (exp16.astype(np.uint64) << 10) | frac16.astype(np.uint64))
-    out = np.where(normal, norm_bits, out)
-
-    sub = ordinary & (e < -14)
-    mant = frac | 0x800000
-    shift = np.where(sub, -e - 1, 0)
-    sub16 = _round_shift_right_even(mant, shift)
-    sub_bits = np.where(sub16 == 0, sign, np.where(sub16 == 0x400, sign | 0x400, sign | sub16))
-    out = np.where(sub, sub_bits, out)
-    return out.astype(np.uint16)
+    arr = np.ascontiguousarray(x, dtype=np.float32)
+    bits = arr.view(np.uint32).reshape(-1)
+    out = np.empty(bits.shape, dtype=np.uint16)
+    for i in range(0, bits.size, _CHUNK):
+        out[i:i + _CHUNK] = _f32_to_f16_chunk(bits[i:i + _CHUNK])
+    return out.reshape(arr.shape)
 
 
-def f16_bits_to_f32(h) -> np.ndarray:
-    """binary16 bits -> binary32 value, exact (page's ``f16_to_f32``)."""
-    h = np.asarray(h, dtype=np.uint16).astype(np.uint32)
+def _f16_to_f32_codes(h: np.ndarray) -> np.ndarray:
+    """binary16 bits -> binary32 bits, exact (page's ``f16_to_f32``)."""
+    h = h.astype(np.uint32)
     sign = (h >> 15) & 1
     exp = (h >> 10) & 0x1F
     frac = h & 0x3FF
     out = np.zeros(h.shape, dtype=np.uint32)
-    # normal
     normal = (exp != 0) & (exp != 0x1F)
     out = np.where(normal, (sign << 31) | ((exp - 15 + 127) << 23) | (frac << 13), out)
-    # inf / nan
     special = exp == 0x1F
     out = np.where(special, (sign << 31) | 0x7F800000 | (frac << 13), out)
-    # zero
     out = np.where((exp == 0) & (frac == 0), sign << 31, out)
     # subnormal: value = frac * 2^-24; normalise the leading one
     sub = (exp == 0) & (frac != 0)
@@ -148,8 +159,16 @@ def f16_bits_to_f32(h) -> np.ndarray:
         mant = np.where(need, mant << 1, mant)
         e = np.where(need, e - 1, e)
     sub_bits = (sign << 31) | (((e + 127).astype(np.uint32)) << 23) | ((mant & 0x3FF).astype(np.uint32) << 13)
-    out = np.where(sub, sub_bits, out)
-    return out.view(np.float32)
+    return np.where(sub, sub_bits, out)
+
+
+# The widening evaluated once for every one of the 2^16 codes.
+_F16_TABLE = _f16_to_f32_codes(np.arange(1 << 16, dtype=np.uint32)).view(np.float32)
+
+
+def f16_bits_to_f32(h) -> np.ndarray:
+    """binary16 bits -> binary32 value, exact (page's ``f16_to_f32``)."""
+    return _F16_TABLE[np.asarray(h, dtype=np.uint16)]
 
 
 def f32_to_bf16_rne(x) -> np.ndarray:
