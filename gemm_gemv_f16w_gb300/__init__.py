@@ -1,0 +1,203 @@
+"""Python binding of liblq, the GB300 weight-only matmul library.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``liblq.so`` (built in-tree by ``gemm_gemv_f16w_gb300.build``).
+The names match the C-ABI in ``include/lq.h``:
+
+    lq_gemv_{f16,q8_0,q4_0}, lq_gemm_{f16,q8_0,q4_0}, lq_matmul_{f16,q8_0,q4_0}
+    lq_pack_{f16,q8_0,q4_0}, lq_packed_bytes, lq_last_device_error, ...
+
+Compute calls take torch CUDA tensors (A float32 [M,K], W packed bytes,
+C float32 [M,N]) or raw device addresses; the stream defaults to torch's
+current stream. A non-OK status raises ``LQError``. If the library is
+missing, the first call fails loudly: there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblq.so")
+
+LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_CUDA, LQ_ERR_DEVICE_TIMEOUT = range(5)
+FMT = {"f16": 0, "q8_0": 1, "q4_0": 2}
+ROUTE_AUTO, ROUTE_STREAM, ROUTE_TENSOR_CORE, ROUTE_GENERIC = range(4)
+
+# every symbol include/lq.h declares
+EXPORTS = [
+    "lq_gemv_f16", "lq_gemv_q8_0", "lq_gemv_q4_0",
+    "lq_gemm_f16", "lq_gemm_q8_0", "lq_gemm_q4_0",
+    "lq_matmul_f16", "lq_matmul_q8_0", "lq_matmul_q4_0",
+    "lq_packed_bytes", "lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0",
+    "lq_status_string", "lq_last_device_error", "lq_version",
+    "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
+    "lq_debug_set_wait_limit_ns",
+]
+_COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
+
+
+class LQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded liblq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        i64, vp, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+        for n in _COMPUTE:
+            f = getattr(L, n)
+            f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+            f.restype = st
+        L.lq_packed_bytes.argtypes = [ctypes.c_int, i64, i64]
+        L.lq_packed_bytes.restype = ctypes.c_size_t
+        for n in ("lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0"):
+            f = getattr(L, n)
+            f.argtypes = [vp, i64, i64, vp]
+            f.restype = st
+        L.lq_status_string.argtypes = [st]
+        L.lq_status_string.restype = ctypes.c_char_p
+        L.lq_last_device_error.argtypes = []
+        L.lq_last_device_error.restype = st
+        L.lq_version.restype = ctypes.c_char_p
+        L.lq_debug_force_route.argtypes = [st]
+        L.lq_debug_force_route.restype = st
+        L.lq_debug_route_count.argtypes = [st]
+        L.lq_debug_route_count.restype = ctypes.c_uint64
+        L.lq_debug_reset_counts.argtypes = []
+        L.lq_debug_reset_counts.restype = None
+        L.lq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        L.lq_debug_set_wait_limit_ns.restype = None
+        _lib = L
+    return _lib
+
+
+def status_string(s: int) -> str:
+    return lib().lq_status_string(int(s)).decode()
+
+
+def _check(s: int, what: str) -> None:
+    if s != LQ_OK:
+        raise LQError(s, what)
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _call(name, A, W, C, M, N, K, stream=None) -> None:
+    _check(getattr(lib(), name)(_ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K), _stream(stream)),
+           name)
+
+
+def _make(name):
+    def f(A, W, C, M, N, K, stream=None):
+        _call(name, A, W, C, M, N, K, stream)
+    f.__name__ = name
+    f.__doc__ = f"{name}(A, W, C, M, N, K, stream=None): see include/lq.h."
+    return f
+
+
+for _n in _COMPUTE:
+    globals()[_n] = _make(_n)
+
+
+def matmul(fmt: str, A, W, N: int, K: int, out=None, kind: str = "matmul", stream=None):
+    """C = A @ W^T for packed W of format ``fmt``; A is float32 CUDA [M, K].
+
+    ``kind`` picks the entry point: "matmul" (router), "gemv" or "gemm".
+    """
+    import torch
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    _call(f"lq_{kind}_{fmt}", A, W, out, M, N, K, stream)
+    return out
+
+
+# ---- host packers --------------------------------------------------------
+def packed_bytes(fmt: str, N: int, K: int) -> int:
+    return int(lib().lq_packed_bytes(FMT[fmt], int(N), int(K)))
+
+
+def pack(fmt: str, W) -> np.ndarray:
+    """Pack f32 weights [N, K] (numpy or CPU torch) on the host.
+
+    Returns uint16 [N, K] for f16 and uint8 [N, K/32*34 or *18] otherwise.
+    """
+    if hasattr(W, "detach"):
+        W = W.detach().cpu().numpy()
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    N, K = W.shape
+    nbytes = packed_bytes(fmt, N, K)
+    if nbytes == 0 and N * K > 0:
+        raise LQError(LQ_ERR_INVALID_ARG, f"lq_pack_{fmt}")
+    if fmt == "f16":
+        out = np.empty((N, K), dtype=np.uint16)
+    else:
+        out = np.empty((N, nbytes // max(N, 1)), dtype=np.uint8)
+    _check(getattr(lib(), f"lq_pack_{fmt}")(W.ctypes.data, N, K, out.ctypes.data), f"lq_pack_{fmt}")
+    return out
+
+
+def lq_pack_f16(W) -> np.ndarray:
+    return pack("f16", W)
+
+
+def lq_pack_q8_0(W) -> np.ndarray:
+    return pack("q8_0", W)
+
+
+def lq_pack_q4_0(W) -> np.ndarray:
+    return pack("q4_0", W)
+
+
+# ---- status and test hooks -----------------------------------------------
+def last_device_error() -> int:
+    return int(lib().lq_last_device_error())
+
+
+def version() -> str:
+    return lib().lq_version().decode()
+
+
+def force_route(route: int) -> None:
+    _check(lib().lq_debug_force_route(int(route)), "lq_debug_force_route")
+
+
+def route_count(route: int) -> int:
+    return int(lib().lq_debug_route_count(int(route)))
+
+
+def reset_counts() -> None:
+    lib().lq_debug_reset_counts()
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    lib().lq_debug_set_wait_limit_ns(int(ns))

@@ -1,0 +1,197 @@
+// C-ABI entry points: argument validation, the M==1 / M>1 router and the
+// route hooks used by the tests.
+//
+// The router mirrors dispatch_gemm_q8 / dispatch_gemm_q4 / dispatch_matmul_half
+// (lattice-inference, src/forward/metal_qwen35/inner/dispatch.rs): M == 0 or
+// N == 0 returns without launching; quantised formats need K > 0 and
+// K % 32 == 0 (the page asserts, this library returns LQ_ERR_INVALID_ARG);
+// M == 1 goes to the GEMV; M > 1 goes to a GEMM, the tensor-core kernel when
+// it can take the shape and the CUDA-core kernel otherwise.
+#include <atomic>
+#include <mutex>
+
+#include "lq_internal.h"
+
+namespace lq {
+
+namespace {
+std::atomic<int> g_force_route{0};
+std::atomic<uint64_t> g_route_count[4];
+std::atomic<unsigned long long> g_wait_ns{0};
+std::mutex g_info_mu;
+DeviceInfo g_info[kMaxDevices];
+bool g_info_valid[kMaxDevices];
+}  // namespace
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+const DeviceInfo& device_info() {
+  static DeviceInfo empty;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return empty;
+  std::lock_guard<std::mutex> lk(g_info_mu);
+  if (!g_info_valid[dev]) {
+    DeviceInfo d;
+    cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_info[dev] = d;
+    g_info_valid[dev] = true;
+  }
+  return g_info[dev];
+}
+
+unsigned long long wait_limit_ns() {
+  const unsigned long long v = g_wait_ns.load();
+  return v ? v : kDefaultWaitNsHost;
+}
+
+unsigned wait_limit_iters() {
+  const unsigned long long v = g_wait_ns.load();
+  if (v == 0 || v >= 1000000ull) return 1u << 30;
+  const unsigned long long it = v / 1000ull;
+  return it < 1 ? 1u : static_cast<unsigned>(it);
+}
+
+void count_route(int route) {
+  if (route >= 0 && route < 4) g_route_count[route].fetch_add(1);
+}
+
+bool use_pdl() { return true; }
+
+lq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LQ_OK : LQ_ERR_CUDA; }
+
+namespace {
+
+bool aligned_to(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared argument checks. Returns LQ_OK to proceed, or the status to return;
+// `*noop` is set when the call is a valid no-op.
+lq_status validate(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N,
+                   int64_t K, bool* noop) {
+  *noop = false;
+  if (M < 0 || N < 0 || K < 0) return LQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    *noop = true;
+    return LQ_OK;
+  }
+  if (fmt != LQ_FMT_F16 && (K == 0 || K % 32 != 0)) return LQ_ERR_INVALID_ARG;
+  if (K == 0) return LQ_ERR_INVALID_ARG;
+  if (!A || !W || !C) return LQ_ERR_INVALID_ARG;
+  if (!aligned_to(A, 4) || !aligned_to(C, 4)) return LQ_ERR_INVALID_ARG;
+  if (fmt == LQ_FMT_F16 && !aligned_to(W, 2)) return LQ_ERR_INVALID_ARG;
+  // 32-bit indexing inside the kernels
+  if (M > (1LL << 31) - 1 || N > (1LL << 30) || K > (1LL << 30)) return LQ_ERR_UNSUPPORTED;
+  return LQ_OK;
+}
+
+lq_status do_gemv(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
+                  void* stream) {
+  bool noop;
+  lq_status st = validate(fmt, A, W, C, M, N, K, &noop);
+  if (st != LQ_OK || noop) return st;
+  if (M != 1) return LQ_ERR_INVALID_ARG;
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  if (g_force_route.load() == 3) return launch_gemv_generic(a);
+  return launch_gemv(a);
+}
+
+lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
+                  void* stream) {
+  bool noop;
+  lq_status st = validate(fmt, A, W, C, M, N, K, &noop);
+  if (st != LQ_OK || noop) return st;
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  switch (g_force_route.load()) {
+    case 1: return launch_gemm_stream(a);
+    case 2: return gemm_tc_eligible(a) ? launch_gemm_tc(a) : LQ_ERR_UNSUPPORTED;
+    case 3: return launch_gemv_generic(a);
+    default: break;
+  }
+  if (gemm_tc_eligible(a)) return launch_gemm_tc(a);
+  return launch_gemm_stream(a);
+}
+
+lq_status do_matmul(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N,
+                    int64_t K, void* stream) {
+  if (M == 1) return do_gemv(fmt, A, W, C, M, N, K, stream);
+  return do_gemm(fmt, A, W, C, M, N, K, stream);
+}
+
+}  // namespace
+}  // namespace lq
+
+using namespace lq;
+
+extern "C" {
+
+lq_status lq_gemv_f16(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemv(LQ_FMT_F16, A, W, C, M, N, K, s);
+}
+lq_status lq_gemv_q8_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemv(LQ_FMT_Q8_0, A, W, C, M, N, K, s);
+}
+lq_status lq_gemv_q4_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemv(LQ_FMT_Q4_0, A, W, C, M, N, K, s);
+}
+lq_status lq_gemm_f16(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemm(LQ_FMT_F16, A, W, C, M, N, K, s);
+}
+lq_status lq_gemm_q8_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemm(LQ_FMT_Q8_0, A, W, C, M, N, K, s);
+}
+lq_status lq_gemm_q4_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemm(LQ_FMT_Q4_0, A, W, C, M, N, K, s);
+}
+lq_status lq_matmul_f16(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_matmul(LQ_FMT_F16, A, W, C, M, N, K, s);
+}
+lq_status lq_matmul_q8_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_matmul(LQ_FMT_Q8_0, A, W, C, M, N, K, s);
+}
+lq_status lq_matmul_q4_0(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_matmul(LQ_FMT_Q4_0, A, W, C, M, N, K, s);
+}
+
+const char* lq_status_string(lq_status s) {
+  switch (s) {
+    case LQ_OK: return "LQ_OK";
+    case LQ_ERR_INVALID_ARG: return "LQ_ERR_INVALID_ARG: bad pointer, size or alignment";
+    case LQ_ERR_UNSUPPORTED: return "LQ_ERR_UNSUPPORTED: no kernel for this request";
+    case LQ_ERR_CUDA: return "LQ_ERR_CUDA: a CUDA call or launch failed";
+    case LQ_ERR_DEVICE_TIMEOUT: return "LQ_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+  }
+  return "unknown lq_status";
+}
+
+lq_status lq_last_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return LQ_ERR_CUDA;
+  const unsigned a = read_clear_gemv_error();
+  const unsigned b = read_clear_gemm_error();
+  const unsigned v = a ? a : b;
+  if (v == 0) return LQ_OK;
+  return static_cast<lq_status>(v);
+}
+
+const char* lq_version(void) { return "lq 0.1.0 (sm_103a)"; }
+
+lq_status lq_debug_force_route(int route) {
+  if (route < 0 || route > 3) return LQ_ERR_INVALID_ARG;
+  g_force_route.store(route);
+  return LQ_OK;
+}
+uint64_t lq_debug_route_count(int route) {
+  if (route < 0 || route > 3) return 0;
+  return g_route_count[route].load();
+}
+void lq_debug_reset_counts(void) {
+  for (auto& c : g_route_count) c.store(0);
+}
+void lq_debug_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+
+}  // extern "C"

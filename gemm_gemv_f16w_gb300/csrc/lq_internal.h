@@ -1,0 +1,57 @@
+// Host-side declarations shared by the translation units of liblq.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lq.h"
+
+namespace lq {
+
+// Problem handed from the C-ABI layer (already validated) to a launcher.
+struct MatmulArgs {
+  const float* A;
+  const void* W;
+  float* C;
+  int64_t M, N, K;
+  int fmt;            // lq_format
+  cudaStream_t stream;
+};
+
+// Per-device facts cached on first use.
+struct DeviceInfo {
+  int sm_count = 0;
+  int max_smem_optin = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+const DeviceInfo& device_info();
+constexpr int kMaxDevices = 64;
+int current_device();
+
+constexpr unsigned long long kDefaultWaitNsHost = 2000000000ull;
+unsigned long long wait_limit_ns();
+// Poll budget of a device wait: unlimited by default; with an overridden
+// limit below 1 ms, one non-blocking poll per microsecond (at least one).
+unsigned wait_limit_iters();
+void count_route(int route);
+bool use_pdl();
+
+// Bytes of one packed W row.
+inline int64_t row_bytes(int fmt, int64_t K) {
+  return fmt == LQ_FMT_F16 ? 2 * K : (fmt == LQ_FMT_Q8_0 ? K / 32 * 34 : K / 32 * 18);
+}
+
+// Launchers (return LQ_OK, LQ_ERR_CUDA or LQ_ERR_UNSUPPORTED; arguments were
+// checked by the C-ABI layer).
+lq_status launch_gemv(const MatmulArgs& a);            // M == 1, picks fast or generic
+lq_status launch_gemv_generic(const MatmulArgs& a);    // any M, K, alignment
+lq_status launch_gemm_stream(const MatmulArgs& a);     // CUDA-core, small M
+lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05
+bool gemm_tc_eligible(const MatmulArgs& a);
+
+// Device status words of each translation unit (read-and-clear).
+unsigned read_clear_gemv_error();
+unsigned read_clear_gemm_error();
+
+lq_status cuda_status(cudaError_t e);
+
+}  // namespace lq

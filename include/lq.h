@@ -1,0 +1,145 @@
+/*
+ * lq.h - weight-only mixed-precision matmul for GB300 (sm_103a).
+ *
+ *     C[M,N] (f32) = A[M,K] (f32) @ W[N,K]^T,   W in {f16, Q8_0, Q4_0}
+ *
+ * Operation and formats follow the docs.rs source pages of lattice-inference
+ * (src/forward/metal_qwen35.rs: kernels gemv_decode_m1, gemv_q8_decode,
+ * gemv_q4_decode, gemm_q8, gemm_q4, gemm_q4_tiled; host packers f32_to_f16,
+ * quantize_row_q8_0; src/forward/metal_qwen35/inner/dispatch.rs: routers
+ * dispatch_matmul_half, dispatch_gemm_q8, dispatch_gemm_q4) and ferrum-kernels
+ * (src/attention/metal/pipelines.rs: gemm_f32a_f16w_v2, gemv_f32a_f16w).
+ *
+ * Layouts (all row-major, tightly packed, little-endian):
+ *   A : float[M*K]                      activations, row m at A + m*K
+ *   C : float[M*N]                      outputs, row m at C + m*N
+ *   W f16  : uint16_t[N*K]              IEEE binary16 bits, row n at W + n*K
+ *   W q8_0 : uint8_t[N*(K/32)*34]       per 32-element block: f16 scale d
+ *                                       (2 bytes) then 32 x int8 q; x = d*q
+ *   W q4_0 : uint8_t[N*(K/32)*18]       per block: f16 scale d then 16 bytes;
+ *                                       byte j holds q_j (low nibble) and
+ *                                       q_{j+16} (high nibble); x = d*(q-8)
+ *
+ * Conventions shared by every compute entry point:
+ *   - A, W and C are DEVICE pointers on the current CUDA device; the caller
+ *     owns them. C must not overlap A or W.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are
+ *     asynchronous: nothing is synchronised, results are ready when the
+ *     stream reaches them.
+ *   - M == 0 or N == 0: LQ_OK, nothing is launched (as the page's routers
+ *     return early).
+ *   - Quantised formats need K > 0 and K % 32 == 0, else LQ_ERR_INVALID_ARG
+ *     (the page's routers assert this). f16 takes any K >= 1.
+ *   - NULL pointers, negative sizes, pointers not aligned to their element
+ *     size (4 bytes for A and C, 2 for f16 W) -> LQ_ERR_INVALID_ARG, before
+ *     any launch.
+ *   - Shapes or alignments that the fastest kernel cannot take run on a
+ *     slower, correct kernel; no call silently computes less.
+ *   - A launch failure returns LQ_ERR_CUDA (cudaGetLastError after launch).
+ *   - Kernels never trap: every wait inside a kernel is bounded; a wait that
+ *     runs out records LQ_ERR_DEVICE_TIMEOUT in a per-device status word,
+ *     read and cleared by lq_last_device_error().
+ *   - Sub-matrices (e.g. the gate or up half of a fused weight) are addressed
+ *     by pointer offsets; a W row offset is always block-aligned.
+ *   - Kernels launched on a stream may begin streaming W before the previous
+ *     kernel on that stream has finished (programmatic dependent launch); A
+ *     and C are touched only after it has. Do not write W on the same stream
+ *     with a kernel that itself allows early launch of its successors.
+ */
+#ifndef LQ_H
+#define LQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LQ_OK = 0,
+  LQ_ERR_INVALID_ARG = 1,    /* bad pointer, size or alignment; nothing ran   */
+  LQ_ERR_UNSUPPORTED = 2,    /* no kernel exists for this request             */
+  LQ_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed          */
+  LQ_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait ran out            */
+} lq_status;
+
+typedef enum { LQ_FMT_F16 = 0, LQ_FMT_Q8_0 = 1, LQ_FMT_Q4_0 = 2 } lq_format;
+
+/* ---- decode GEMV, M == 1 (M != 1 -> LQ_ERR_INVALID_ARG) -----------------
+ * One pass over W: each output C[0,n] = sum_k A[0,k] * w(n,k), accumulated
+ * in f32 (Q formats: sum of q*a per block slice, times d, as gemv_q8_decode /
+ * gemv_q4_decode do). Bound by HBM bandwidth, as the page notes for decode
+ * (dispatch.rs, dispatch_gemm_q3: "decode is weight-bandwidth-bound"). */
+lq_status lq_gemv_f16 (const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_gemv_q8_0(const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+
+/* ---- prefill GEMM, any M >= 1 -----------------------------------------
+ * Counterparts: gemm_q8 / gemm_q4 / gemm_q4_tiled (metal_qwen35.rs),
+ * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). Small M streams W on the
+ * CUDA cores in f32 (GEMV accuracy); larger M runs on the tensor cores
+ * (tcgen05, TMEM accumulators) with A rounded to bf16 and W dequantised to
+ * bf16, products accumulated in f32. */
+lq_status lq_gemm_f16 (const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_gemm_q8_0(const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_gemm_q4_0(const float* A, const void* W, float* C,
+                       int64_t M, int64_t N, int64_t K, void* stream);
+
+/* ---- dispatcher: M == 1 -> GEMV, M > 1 -> GEMM ---------------------------
+ * The matmul entry point model code calls (dispatch_matmul / dispatch_gemm
+ * in dispatch.rs). */
+lq_status lq_matmul_f16 (const float* A, const void* W, float* C,
+                         int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_matmul_q8_0(const float* A, const void* W, float* C,
+                         int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_matmul_q4_0(const float* A, const void* W, float* C,
+                         int64_t M, int64_t N, int64_t K, void* stream);
+
+/* ---- host-side packers (HOST memory in, HOST memory out) ----------------
+ * make_buffer_f16 / quantize_row_q8_0 (metal_qwen35.rs) and the Q4_0 rule:
+ *   f16 : RNE narrowing of every element.
+ *   q8_0: per 32-block d = max|x|/127 (f32), q = round(x/d) halves away from
+ *         zero, clamped to [-127,127]; d == 0 -> q = 0.
+ *   q4_0: per block m = first element of largest |x|, d = m/-8 (f32),
+ *         q = min(15, (int)(x/d + 8.5)); d == 0 -> q = 8.
+ * `out` must hold lq_packed_bytes(fmt, N, K) bytes. Non-finite input or a
+ * bad shape -> LQ_ERR_INVALID_ARG (out may be partly written). The packers
+ * are plain CPU code and need no GPU. */
+size_t    lq_packed_bytes(int fmt, int64_t N, int64_t K); /* 0 if invalid */
+lq_status lq_pack_f16 (const float* W_host, int64_t N, int64_t K, void* out_host);
+lq_status lq_pack_q8_0(const float* W_host, int64_t N, int64_t K, void* out_host);
+lq_status lq_pack_q4_0(const float* W_host, int64_t N, int64_t K, void* out_host);
+
+/* ---- status ---------------------------------------------------------- */
+const char* lq_status_string(lq_status s);
+/* Synchronises the current device, then reads and clears its device status
+ * word. LQ_OK if no kernel recorded an error. */
+lq_status   lq_last_device_error(void);
+/* Library version string. */
+const char* lq_version(void);
+
+/* ---- test hooks (the forced-route idea of the page's
+ * force_q4_gemm_fallback_for_test and its fallback dispatch counter) ------
+ * route: 0 = automatic, 1 = CUDA-core streaming GEMM (any M),
+ *        2 = tensor-core GEMM, 3 = generic fallback kernels (any shape).
+ * lq_debug_route_count(r) counts launches taken by route r (r = 0 counts
+ * the fast GEMV); counters are process-wide. */
+lq_status lq_debug_force_route(int route);
+uint64_t  lq_debug_route_count(int route);
+void      lq_debug_reset_counts(void);
+/* Overrides the device-side wait limit in nanoseconds (0 = default, 2 s).
+ * Below one millisecond the waits also stop blocking and give up after
+ * ns/1000 polls (at least one), which exercises the LQ_ERR_DEVICE_TIMEOUT
+ * path deterministically without any real hang. */
+void      lq_debug_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LQ_H */

@@ -1,0 +1,134 @@
+"""Host-side checks of the C-ABI library that need no GPU: the exported
+symbols, the host packers (bit-exact against the oracle) and the argument
+checks that return before any launch."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_header_declarations_are_all_exported(lq):
+    with open(os.path.join(ROOT, "include", "lq.h")) as f:
+        text = f.read()
+    declared = set(re.findall(r"\b(lq_[a-z0-9_]+)\s*\(", text))
+    assert declared == set(lq.EXPORTS)
+    L = lq.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(lq):
+    assert "sm_103a" in lq.version()
+    for s in range(5):
+        assert lq.status_string(s).startswith("LQ_")
+
+
+@pytest.mark.parametrize("fmt,N,K", [("f16", 3, 7), ("q8_0", 5, 64), ("q4_0", 2, 96)])
+def test_packed_bytes(lq, fmt, N, K):
+    assert lq.packed_bytes(fmt, N, K) == N * O.packed_row_bytes(fmt, K)
+    assert lq.packed_bytes("q8_0", 1, 33) == 0
+    assert lq.packed_bytes("q4_0", -1, 32) == 0
+
+
+def _adversarial(K=256):
+    rows = []
+    z = np.zeros(K, np.float32)
+    rows.append(z)                                   # all-zero blocks
+    r = z.copy(); r[3] = 1.0; r[7] = -1.0            # +a/-a tie (first wins)
+    rows.append(r)
+    r = z.copy(); r[5] = -1.0; r[9] = 1.0
+    rows.append(r)
+    rows.append(np.full(K, 0.37, np.float32))        # constant blocks
+    rows.append(np.full(K, -2.5e-3, np.float32))
+    t = (np.arange(K) % 32 - 16).astype(np.float32) * np.float32(2**-6) * np.float32(127 / 16)
+    rows.append(t.astype(np.float32))                # ramps
+    rows.append((np.arange(K) % 32 - 16).astype(np.float32) * np.float32(0.5))  # exact halves
+    rows.append(np.full(K, 1e-6, np.float32))        # d in the f16 subnormal range
+    rows.append(np.full(K, 3e-9, np.float32))        # d underflows to 0 in f16
+    r = np.full(K, 1e-3, np.float32); r[::32] = 1e7  # d overflows f16 (inf)
+    rows.append(r)
+    r = np.full(K, 0.01, np.float32); r[1::32] = -0.02
+    rows.append(r)
+    rng = np.random.default_rng(0)
+    rows.append((rng.standard_normal(K) * 0.02).astype(np.float32))
+    rows.append(-z)                                  # -0.0 everywhere
+    return np.stack(rows)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_packer_bit_exact_adversarial(lq, fmt):
+    W = _adversarial()
+    assert np.array_equal(lq.pack(fmt, W).view(np.uint8), O.pack(fmt, W).view(np.uint8))
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_packer_bit_exact_random(lq, fmt, seed):
+    rng = np.random.default_rng(seed)
+    N, K = 37, 32 * (1 + seed * 5)
+    W = (rng.standard_normal((N, K)) * rng.choice([0.02, 1.0, 300.0])).astype(np.float32)
+    W[rng.integers(0, N)] *= 20
+    assert np.array_equal(lq.pack(fmt, W).view(np.uint8), O.pack(fmt, W).view(np.uint8))
+
+
+@pytest.mark.parametrize("name", ["gemv_q8_0_4096x4096", "gemv_q4_0_11008x4096_outliers",
+                                  "gemm_q8_0_512x6144x2048", "gemm_q4_0_512x6144x2048",
+                                  "gemm_f16_512x6144x2048"])
+def test_packer_bit_exact_on_workload_weights(lq, name):
+    w = synthetic.WORKLOADS[name]
+    W, _ = synthetic.draw_workload(w, M=1)
+    Wn = W.numpy()
+    assert np.array_equal(lq.pack(w.fmt, Wn).view(np.uint8), O.pack(w.fmt, Wn).view(np.uint8))
+
+
+def test_packer_rejects_bad_input(lq):
+    with pytest.raises(lq.LQError):
+        lq.pack("q8_0", np.zeros((2, 48), np.float32))
+    bad = np.zeros((1, 32), np.float32)
+    bad[0, 4] = np.inf
+    for fmt in ("f16", "q8_0", "q4_0"):
+        with pytest.raises(lq.LQError):
+            lq.pack(fmt, bad)
+
+
+def _raw(lq, name, A, W, C, M, N, K):
+    return getattr(lq.lib(), name)(A, W, C, M, N, K, 0)
+
+
+@pytest.mark.parametrize("kind", ["gemv", "gemm", "matmul"])
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_argument_errors_return_before_launch(lq, kind, fmt):
+    name = f"lq_{kind}_{fmt}"
+    # never dereferenced: every call below fails validation or is a no-op
+    a, w, c = 0x10000, 0x20000, 0x30000
+    assert _raw(lq, name, a, w, c, 0, 8, 64) == lq.LQ_OK
+    assert _raw(lq, name, a, w, c, 1, 0, 64) == lq.LQ_OK
+    assert _raw(lq, name, None, None, None, 0, 0, 64) == lq.LQ_OK
+    assert _raw(lq, name, a, w, c, -1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a, w, c, 1, 8, -64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, None, w, c, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a, None, c, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a, w, None, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a, w, c, 1, 8, 0) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a + 2, w, c, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    assert _raw(lq, name, a, w, c + 1, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    if fmt == "f16":
+        assert _raw(lq, name, a, w + 1, c, 1, 8, 64) == lq.LQ_ERR_INVALID_ARG
+    else:
+        assert _raw(lq, name, a, w, c, 1, 8, 48) == lq.LQ_ERR_INVALID_ARG
+    if kind == "gemv":
+        assert _raw(lq, name, a, w, c, 2, 8, 64) == lq.LQ_ERR_INVALID_ARG
+
+
+def test_route_hooks(lq):
+    with pytest.raises(lq.LQError):
+        lq.force_route(9)
+    lq.force_route(0)
+    lq.reset_counts()
+    assert all(lq.route_count(r) == 0 for r in range(4))
