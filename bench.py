@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the weight-only matmul C = A @ W^T on GB300.
+
+Headline workload: the Q8_0 decode GEMV, M=1, N=4096, K=4096 (metric: achieved
+HBM GB/s on the algorithmic bytes W + A + C, as a fraction of the measured
+HBM peak). One step is one decode pass over a stack of R such weight matrices
+(R copies whose total exceeds twice the L2), each multiplied by its own
+activation row through the library's router; the step is captured once as a
+CUDA graph and replayed, so the GPU never waits on the host. The other
+workload families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and
+the M = 2 / 16 / 64 crossover) are timed the same way under "workloads".
+
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload (rank 0 only) and prints the same JSON line with "impl": "reference".
+
+Inputs are synthetic and seeded (synthetic.py); nothing is read from disk
+except the measured peaks and the committed ncu summaries.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+HEADLINE = "gemv_q8_0_4096x4096"
+METRIC = "decode GEMV achieved HBM GB/s (% of peak); prefill GEMM TFLOP/s (% peak)"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+
+
+# ---------------------------------------------------------------- helpers
+def algorithmic_bytes(fmt, M, N, K) -> int:
+    row = {"f16": 2 * K, "q8_0": K // 32 * 34, "q4_0": K // 32 * 18}[fmt]
+    return N * row + 4 * M * K + 4 * M * N
+
+
+def flops(M, N, K) -> int:
+    return 2 * M * N * K
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch of the dominant kernel, from the committed ncu
+    summary of this workload (profiles/<workload>.md, line
+    'traffic_bytes_per_launch: <int>'), or None."""
+    path = os.path.join(ROOT, "profiles", f"{workload}.md")
+    try:
+        with open(path) as f:
+            m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", f.read())
+        return int(m.group(1)) if m else None
+    except OSError:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = ""
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+class Workbench:
+    """R device copies of one workload's packed weights (R chosen so that the
+    copies together exceed twice the L2), R activation blocks and R outputs;
+    step() runs the library's router once per copy."""
+
+    def __init__(self, lq, w: synthetic.Workload, dev, copies=None, max_bytes=3 * 2**30):
+        self.lq, self.w, self.dev = lq, w, dev
+        W, A = synthetic.draw_workload(w)
+        packed = lq.pack(w.fmt, W).reshape(-1).view(np.uint8)
+        self.wbytes = packed.nbytes
+        R = copies or max(1, math.ceil(2 * L2_BYTES / (self.wbytes + 4 * w.M * (w.K + w.N))))
+        R = max(1, min(R, max_bytes // max(self.wbytes, 1)))
+        self.R = R
+        base = torch.from_numpy(packed).to(dev)
+        self.Wd = [base] + [base.clone() for _ in range(R - 1)]
+        self.A_host = A.unsqueeze(0).expand(R, -1, -1).contiguous().pin_memory()
+        self.Ad = self.A_host.to(dev)
+        self.Cd = torch.empty((R, w.M, w.N), dtype=torch.float32, device=dev)
+        self.C_host = torch.empty((R, w.M, w.N), dtype=torch.float32).pin_memory()
+        self.fn = getattr(lq, f"lq_matmul_{w.fmt}")
+        self.bytes_per_launch = algorithmic_bytes(w.fmt, w.M, w.N, w.K)
+        self.flops_per_launch = flops(w.M, w.N, w.K)
+        self.graph = None
+
+    def step(self, stream=None):
+        w = self.w
+        for r in range(self.R):
+            self.fn(self.Ad[r], self.Wd[r], self.Cd[r], w.M, w.N, w.K, stream)
+
+    def capture(self):
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self.step()          # eager warm-up (sets kernel attributes)
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        self.graph = g
+        st = self.lq.last_device_error()
+        if st != self.lq.LQ_OK:
+            raise RuntimeError(f"device status after warm-up: {self.lq.status_string(st)}")
+
+    def time_graph(self, steps: int, warmup: int, barrier=None):
+        """Device time in seconds of `steps` graph replays (CUDA events on
+        the replay stream), after `warmup` replays."""
+        stream = torch.cuda.current_stream(self.dev)
+        for _ in range(warmup):
+            self.graph.replay()
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            self.graph.replay()
+        t1.record(stream)
+        torch.cuda.synchronize(self.dev)
+        if barrier:
+            barrier()
+        return t0.elapsed_time(t1) / 1e3
+
+    def time_e2e(self, steps: int):
+        """Through the public API with host buffers: per step the pinned A
+        goes to the device, the router runs on every copy, C comes back to
+        the host and is read."""
+        stream = torch.cuda.current_stream(self.dev)
+        torch.cuda.synchronize(self.dev)
+        t0 = time.perf_counter()
+        checksum = 0.0
+        for _ in range(steps):
+            self.Ad.copy_(self.A_host, non_blocking=True)
+            self.step()
+            self.C_host.copy_(self.Cd, non_blocking=True)
+            stream.synchronize()
+            checksum += float(self.C_host[0, 0, 0])
+        dt = time.perf_counter() - t0
+        return dt, self.A_host.numel() * 4, self.C_host.numel() * 4, checksum
+
+    def free(self):
+        self.graph = None
+        self.Wd = self.Ad = self.Cd = None
+        torch.cuda.empty_cache()
+
+
+def rate(wb: Workbench, seconds_per_launch: float):
+    """(value, unit, roofline bound) of one launch of this workload."""
+    if wb.w.M >= 128:
+        return wb.flops_per_launch / seconds_per_launch / 1e12, "TFLOP/s", "tensor"
+    return wb.bytes_per_launch / seconds_per_launch / 1e9, "GB/s", "hbm"
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_rate(w: synthetic.Workload, seconds: float, rows=None):
+    """Time the CPU oracle (dequantise + float64 matmul, as it stands) on the
+    workload's inputs, restricted to `rows` weight rows, for about `seconds`.
+    Returns (bytes/s of algorithmic traffic, sample description, calls, s)."""
+    import oracle as O
+    W, A = synthetic.draw_workload(w)
+    Wn, An = W.numpy(), A.numpy()
+    n = w.N if rows is None else min(rows, w.N)
+    packed = O.pack(w.fmt, Wn[:n])
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        O.reference(w.fmt, An, packed, n, w.K, tensor_core=w.M >= 128)
+        calls += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(w.fmt, w.M, n, w.K)
+    return (b * calls / dt, f"{calls} oracle call(s) of M={w.M}, N={n} of {w.N}, K={w.K} ({w.fmt})",
+            calls, dt)
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ---------------------------------------------------------------- main
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() and args.impl != "reference" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The oracle on the headline workload's config, as it stands, on the
+    host cores: each step is one oracle call on a row sample sized so that
+    the whole run takes about a minute."""
+    if rank != 0:
+        return
+    import oracle as O
+    w = synthetic.WORKLOADS[args.workload]
+    steps, warmup = args.steps or 20, args.warmup
+    _, _, _, dt1 = oracle_rate(w, 0.0, rows=64)
+    per_row = dt1 / 64
+    rows = int(max(8, min(w.N, 60.0 / max(steps + warmup, 1) / max(per_row, 1e-9))))
+    W, A = synthetic.draw_workload(w)
+    packed = O.pack(w.fmt, W.numpy()[:rows])
+    An = A.numpy()
+    for _ in range(warmup):
+        O.reference(w.fmt, An, packed, rows, w.K, tensor_core=w.M >= 128)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        O.reference(w.fmt, An, packed, rows, w.K, tensor_core=w.M >= 128)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(w.fmt, w.M, rows, w.K)
+    val = b * steps / dt / 1e9
+    sample = f"each step: oracle on M={w.M}, N={rows} of {w.N} rows, K={w.K} ({w.fmt})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": dt / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                                         "format": w.fmt},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+EXTRA = ["gemv_f16_256x512", "gemv_q4_0_11008x4096_outliers", "gemv_f16_lmhead_151936x2048",
+         "gemm_f16_512x6144x2048", "gemm_q8_0_512x6144x2048", "gemm_q4_0_512x6144x2048"] + \
+        [f"gemm_{f}_m{m}_6144x2048" for m in (2, 16, 64) for f in ("f16", "q8_0", "q4_0")]
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s of device time)")
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--extras", default="all",
+                    help="comma-separated extra workloads to time, 'all' or 'none'")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = init_dist(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import gemm_gemv_f16w_gb300 as lq
+    from gemm_gemv_f16w_gb300 import build as lqbuild
+    if rank == 0 or not os.path.exists(lq.LIB_PATH):
+        lqbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    lq.lib()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    hbm_peak, tc_peak, _, peak_src = peaks()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---- headline workload
+    w = synthetic.WORKLOADS[args.workload]
+    wb = Workbench(lq, w, dev)
+    wb.capture()
+    probe = wb.time_graph(3, 1)
+    steps = args.steps or max(20, int(1.5 / max(probe / 3, 1e-7)))
+    lq.reset_counts()
+    with ClockSampler(local) as clk:
+        dt = wb.time_graph(steps, args.warmup, barrier)
+    dt = max_over_ranks(dt)
+    clocks = clk.summary()
+    launches_per_step = wb.R
+    per_launch = dt / (steps * launches_per_step)
+    val1, unit, bound = rate(wb, per_launch)
+    value = val1 * world  # every rank runs the same per-GPU work (weak scaling)
+    peak = hbm_peak if bound == "hbm" else tc_peak
+    roofline = {"bound": bound, "achieved": val1, "peak": peak, "unit": unit,
+                "frac": val1 / peak, "traffic": ncu_traffic(w.name),
+                "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
+                "algorithmic_per_launch": wb.bytes_per_launch if bound == "hbm" else wb.flops_per_launch,
+                "us_per_launch": per_launch * 1e6}
+    e2e_dt, h2d, d2h, _ = wb.time_e2e(steps)
+    e2e_dt = max_over_ranks(e2e_dt)
+    e2e_val = wb.bytes_per_launch * wb.R * steps / e2e_dt / 1e9 * world
+    wb.free()
+
+    # ---- the other workload families (same method, shorter runs)
+    extras = {}
+    names = EXTRA if args.extras == "all" else ([] if args.extras == "none" else args.extras.split(","))
+    for name in names:
+        if name == w.name:
+            continue
+        x = synthetic.WORKLOADS[name]
+        xb = Workbench(lq, x, dev)
+        xb.capture()
+        p = xb.time_graph(2, 1)
+        n = max(5, int(0.25 / max(p / 2, 1e-7)))
+        d = max_over_ranks(xb.time_graph(n, 3, barrier))
+        pl = d / (n * xb.R)
+        v, u, b = rate(xb, pl)
+        pk = hbm_peak if b == "hbm" else tc_peak
+        extras[name] = {"value": v, "unit": u, "bound": b, "frac": v / pk, "us_per_launch": pl * 1e6,
+                        "copies": xb.R, "launches": n * xb.R,
+                        "gb_per_s": xb.bytes_per_launch / pl / 1e9,
+                        "tflop_per_s": xb.flops_per_launch / pl / 1e12}
+        xb.free()
+
+    # ---- CPU oracle baseline (rank 0 at N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bps, sample, calls, cdt = oracle_rate(w, 10.0)
+        cpu = {"value": bps / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{sample}; {cdt:.1f} s; numpy float64 (BLAS matmul, multi-threaded)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded torch.randn, recipe in synthetic.py)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "format": w.fmt,
+                       "launches_per_step": launches_per_step,
+                       "l2": f"inputs larger than L2: {wb.R} weight copies, "
+                             f"{wb.R * wb.wbytes / 2**20:.0f} MiB > {L2_BYTES // 2**20} MiB",
+                       "step": "one decode pass over the weight-copy stack, CUDA-graph replay",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": steps * launches_per_step,
+            "clocks": clocks,
+            "workloads": extras,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
