@@ -62,7 +62,11 @@ void count_route(int route) {
   if (route >= 0 && route < 4) g_route_count[route].fetch_add(1);
 }
 
-bool use_pdl() { return true; }
+namespace {
+std::atomic<bool> g_use_pdl{true};
+}
+bool use_pdl() { return g_use_pdl.load(); }
+void set_use_pdl(bool on) { g_use_pdl.store(on); }
 
 lq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LQ_OK : LQ_ERR_CUDA; }
 

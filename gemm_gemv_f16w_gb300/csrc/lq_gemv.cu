@@ -288,7 +288,7 @@ __device__ __forceinline__ float transpose_reduce8(const float (&acc)[8], int la
 // has read the slot's reduction buffer.
 // ---------------------------------------------------------------------------
 template <int FMT, int CPW>
-__global__ void __launch_bounds__(kGemvThreads, 1) gemv_stream_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_stream_kernel(const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Header& hd = *reinterpret_cast<Header*>(smem);
   float* As = reinterpret_cast<float*>(smem + kHeaderBytes);
@@ -551,7 +551,18 @@ lq_status launch_gemv_generic(const MatmulArgs& a) {
   return cuda_status(e);
 }
 
-lq_status launch_gemv(const MatmulArgs& a) {
+// Launch plan of the streaming kernel: grid, ring geometry and shared memory.
+struct GemvPlan {
+  GemvParams p;
+  int grid = 0, cpw = 0;
+  size_t smem = 0;
+  bool ok = false;
+};
+
+// `ctas_per_sm` CTAs share an SM (each gets 1/ctas_per_sm of the usable
+// shared memory); stages hold up to `max_rows` rows.
+GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows) {
+  GemvPlan pl;
   const int K = static_cast<int>(a.K);
   const int rb = static_cast<int>(row_bytes(a.fmt, a.K));
   // Fast path: every stage start and A are 16-byte aligned for the bulk
@@ -559,22 +570,24 @@ lq_status launch_gemv(const MatmulArgs& a) {
   const bool shape_ok = a.K <= kGemvFastMaxK &&
                         (a.fmt == LQ_FMT_F16 ? (K % 8 == 0) : (K % 256 == 0)) && a.N < (1LL << 30);
   const bool align_ok = aligned(a.W, 16) && aligned(a.A, 16);
-  const int cpw = shape_ok ? pick_cpw(a.fmt, K) : 0;
-  if (!shape_ok || !align_ok || cpw == 0) return launch_gemv_generic(a);
+  pl.cpw = shape_ok ? pick_cpw(a.fmt, K) : 0;
+  if (!shape_ok || !align_ok || pl.cpw == 0) return pl;
 
   const DeviceInfo& di = device_info();
-  const int G = static_cast<int>(std::min<int64_t>(a.N, di.sm_count));
+  const int G = static_cast<int>(std::min<int64_t>(a.N, static_cast<int64_t>(di.sm_count) * ctas_per_sm));
   const int a_bytes = K * 4;  // a multiple of 16 on this path
-  const int budget = std::min(di.max_smem_optin, 200 * 1024) - kHeaderBytes - a_bytes;
+  const int per_cta = std::min(di.max_smem_optin, (226 * 1024) / ctas_per_sm - 1024);
+  const int budget = per_cta - kHeaderBytes - a_bytes;
   const int rows_per_cta = static_cast<int>((a.N + G - 1) / G);
-  // up to 8 rows per bulk copy, and room for at least two stages
-  const int rs = std::min({kRowsPerStage, std::max(1, budget / (2 * rb)), std::max(1, rows_per_cta)});
+  // up to max_rows rows per bulk copy, and room for at least two stages
+  const int rs = std::min({max_rows, kRowsPerStage, std::max(1, budget / (2 * rb)),
+                           std::max(1, rows_per_cta)});
   const int stage_bytes = rs * rb;
   const int need_stages = (rows_per_cta + rs - 1) / rs;
   const int stages = std::min({kMaxStages, budget / std::max(stage_bytes, 1), std::max(need_stages, 2)});
-  if (G < 1 || budget <= 0 || stages < 2) return launch_gemv_generic(a);
+  if (G < 1 || budget <= 0 || stages < 2) return pl;
 
-  GemvParams p;
+  GemvParams& p = pl.p;
   p.A = a.A;
   p.W = static_cast<const uint8_t*>(a.W);
   p.C = a.C;
@@ -586,14 +599,26 @@ lq_status launch_gemv(const MatmulArgs& a) {
   p.a_bytes = a_bytes;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
-  const size_t smem = kHeaderBytes + a_bytes + static_cast<size_t>(stages) * stage_bytes;
-  lq_status st;
-  if (a.fmt == LQ_FMT_F16)
-    st = launch_stream_fmt<LQ_FMT_F16>(a, cpw, p, G, smem);
-  else if (a.fmt == LQ_FMT_Q8_0)
-    st = launch_stream_fmt<LQ_FMT_Q8_0>(a, cpw, p, G, smem);
-  else
-    st = launch_stream_fmt<LQ_FMT_Q4_0>(a, cpw, p, G, smem);
+  pl.grid = G;
+  pl.smem = kHeaderBytes + a_bytes + static_cast<size_t>(stages) * stage_bytes;
+  pl.ok = true;
+  return pl;
+}
+
+lq_status launch_plan(const MatmulArgs& a, const GemvPlan& pl) {
+  if (a.fmt == LQ_FMT_F16) return launch_stream_fmt<LQ_FMT_F16>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  if (a.fmt == LQ_FMT_Q8_0) return launch_stream_fmt<LQ_FMT_Q8_0>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  return launch_stream_fmt<LQ_FMT_Q4_0>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+}
+
+lq_status launch_gemv(const MatmulArgs& a) {
+  // Two CTAs per SM: twice the warps to hide shared-memory and ALU latency,
+  // and room for the next kernel's CTAs to start while this one drains
+  // (programmatic dependent launch). Measured on GB300 against one CTA per
+  // SM: LM head 4.45 -> 6.57 TB/s, Q8_0 4096x4096 1.79 -> 2.49 TB/s.
+  const GemvPlan pl = plan_gemv(a, 2, kRowsPerStage);
+  if (!pl.ok) return launch_gemv_generic(a);
+  const lq_status st = launch_plan(a, pl);
   if (st == LQ_ERR_UNSUPPORTED) return launch_gemv_generic(a);
   if (st == LQ_OK) count_route(0);
   return st;

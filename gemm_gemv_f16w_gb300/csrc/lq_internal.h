@@ -34,6 +34,7 @@ unsigned long long wait_limit_ns();
 unsigned wait_limit_iters();
 void count_route(int route);
 bool use_pdl();
+void set_use_pdl(bool on);  // kernels may overlap their predecessor (default on)
 
 // Bytes of one packed W row.
 inline int64_t row_bytes(int fmt, int64_t K) {
