@@ -288,7 +288,7 @@ __device__ __forceinline__ float transpose_reduce8(const float (&acc)[8], int la
 // has read the slot's reduction buffer.
 // ---------------------------------------------------------------------------
 template <int FMT, int CPW>
-__global__ void __launch_bounds__(kGemvThreads, 2) gemv_stream_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_kernel(const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Header& hd = *reinterpret_cast<Header*>(smem);
   float* As = reinterpret_cast<float*>(smem + kHeaderBytes);

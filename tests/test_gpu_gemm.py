@@ -1,0 +1,110 @@
+"""GPU parity of the prefill GEMM (M > 1) through the C-ABI, against the oracle.
+
+The tensor-core route rounds A to bf16 and accumulates bf16 x bf16 products
+in f32; the oracle rounds A to bf16 the same way and the tolerance is
+5e-3 * sum|a*w| + 1e-5 per element. Output buffers start as NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from helpers import check, nan_filled, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lq, dev, fmt, W, A, kind="gemm"):
+    N, K = W.shape
+    M = A.shape[0]
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
+    C = nan_filled(M, N, dev)
+    getattr(lq, f"lq_{kind}_{fmt}")(A.to(dev), Wd, C, M, N, K)
+    torch.cuda.synchronize()
+    assert lq.last_device_error() == lq.LQ_OK
+    return C.cpu().numpy()
+
+
+def _ref(fmt, W, A):
+    N, K = W.shape
+    return O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_tc_single_tile_single_kstep(lq, cuda_dev, fmt):
+    W, A = synthetic.draw(16, 128, 64, seed=1)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} 16x128x64")
+    assert lq.route_count(2) == 1
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("M,N,K", [(2, 128, 128), (5, 200, 512), (16, 1000, 1024), (33, 384, 256),
+                                   (100, 130, 2048), (256, 256, 640), (300, 515, 512)])
+def test_tc_shapes(lq, cuda_dev, fmt, M, N, K):
+    W, A = synthetic.draw(M, N, K, seed=M + N + K, outlier_frac=0.05)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} {M}x{N}x{K}")
+    assert lq.route_count(2) == 1
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_gemm_router_and_generic_route_agree(lq, cuda_dev, fmt):
+    """Every route gives the oracle's answer (forced-route test hook)."""
+    W, A = synthetic.draw(24, 192, 320, seed=3)
+    y, tol = _ref(fmt, W, A)
+    try:
+        for route in (lq.ROUTE_AUTO, lq.ROUTE_TENSOR_CORE, lq.ROUTE_GENERIC, lq.ROUTE_STREAM):
+            lq.force_route(route)
+            C = _run(lq, cuda_dev, fmt, W, A, kind="matmul")
+            check(C, y, tol, f"route {route}")
+    finally:
+        lq.force_route(0)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_gemm_k_not_multiple_of_64_uses_generic(lq, cuda_dev, fmt):
+    W, A = synthetic.draw(8, 96, 96, seed=4)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol)
+    assert lq.route_count(2) == 0
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_gemm_config_512x6144x2048(lq, cuda_dev, fmt):
+    w = synthetic.WORKLOADS[f"gemm_{fmt}_512x6144x2048"]
+    W, A = synthetic.draw_workload(w)
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, w.name)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("M", [2, 16, 64])
+def test_gemm_config_crossover(lq, cuda_dev, fmt, M):
+    w = synthetic.WORKLOADS[f"gemm_{fmt}_m{M}_6144x2048"]
+    W, A = synthetic.draw_workload(w)
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, w.name)
+
+
+def test_gemm_row_equals_gemv(lq, cuda_dev):
+    """Row m of the GEMM equals the GEMV on row m of A (within the GEMM
+    tolerance)."""
+    W, A = synthetic.draw(8, 512, 1024, seed=6)
+    C = _run(lq, cuda_dev, "q8_0", W, A)
+    Wd = to_dev(lq.pack("q8_0", W).reshape(-1).view(np.uint8), cuda_dev)
+    _, tol = _ref("q8_0", W, A)
+    for m in range(8):
+        g = nan_filled(1, 512, cuda_dev)
+        lq.lq_gemv_q8_0(A[m:m + 1].contiguous().to(cuda_dev), Wd, g, 1, 512, 1024)
+        torch.cuda.synchronize()
+        assert np.all(np.abs(g.cpu().numpy()[0] - C[m]) <= tol[m])
