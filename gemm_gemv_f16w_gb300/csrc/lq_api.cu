@@ -113,10 +113,13 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
   MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
   switch (g_force_route.load()) {
     case 1: return launch_gemm_stream(a);
-    case 2: return gemm_tc_eligible(a) ? launch_gemm_tc(a) : LQ_ERR_UNSUPPORTED;
+    case 2:
+      if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
+      return gemm_tc_eligible(a) ? launch_gemm_tc(a) : LQ_ERR_UNSUPPORTED;
     case 3: return launch_gemv_generic(a);
     default: break;
   }
+  if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
   if (gemm_tc_eligible(a)) return launch_gemm_tc(a);
   return launch_gemm_stream(a);
 }
@@ -177,7 +180,8 @@ lq_status lq_last_device_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return LQ_ERR_CUDA;
   const unsigned a = read_clear_gemv_error();
   const unsigned b = read_clear_gemm_error();
-  const unsigned v = a ? a : b;
+  const unsigned c = read_clear_gemm_tma_error();
+  const unsigned v = a ? a : (b ? b : c);
   if (v == 0) return LQ_OK;
   return static_cast<lq_status>(v);
 }

@@ -1,0 +1,587 @@
+// Prefill GEMM, fast path: TMA-fed tcgen05 kernel with the weight operand in
+// tensor memory.
+//
+// Counterparts on the source pages: gemm_q4_tiled / gemm_q8_tiled
+// (lattice-inference, metal_qwen35.rs and dispatch.rs: W dequantised inside
+// the tile loop) and gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs: f16
+// weights widened on load). The GB300 design:
+//
+//  1. a pre-pass turns A (f32) into f16 with an exact per-token power-of-two
+//     scale s_m, so the largest |a| of row m lands in [2^14, 2^15): no
+//     overflow, 11 significant bits (3 more than bf16), and the scale is
+//     undone exactly in the epilogue;
+//  2. the GEMM kernel, one CTA per SM, owns 128 rows of W and a tile of BT
+//     tokens. A producer thread moves raw W (f16 / Q8_0 / Q4_0 bytes) with
+//     TMA as 16-byte "slabs" (slab s of all 128 rows contiguous), so that a
+//     thread reading its own row does so with conflict-free 16-byte loads,
+//     and moves the f16 A tile with TMA straight into the 128-byte-swizzled
+//     K-major layout of the MMA's B operand;
+//  3. eight converter warps (thread = W row = TMEM lane) dequantise 64 K of
+//     their row at a time with half2 arithmetic (Q8_0: q*d, Q4_0: (q-8)*d,
+//     computed in f16 with W scaled by 2^8 to stay clear of f16 subnormals)
+//     and write the f16 operand into tensor memory with tcgen05.st;
+//  4. one thread issues tcgen05.mma kind::f16 with A (= W) from tensor
+//     memory and B (= tokens) from shared memory, accumulating f32 in TMEM;
+//  5. four warps read the accumulator (tcgen05.ld), multiply by s_m * 2^-8
+//     (f16 weights: s_m) and store C with coalesced stores.
+// Every wait is bounded; on timeout the kernel records LQ_ERR_DEVICE_TIMEOUT,
+// lets its copies and MMAs finish, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "lq_device.cuh"
+#include "lq_internal.h"
+#include "lq_tcgen05.cuh"
+
+namespace lq {
+namespace {
+
+__device__ unsigned g_tma_err;
+
+constexpr int kNumConv = 8;                        // converter warps (2 groups of 4)
+constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
+constexpr int kBN = 128;                           // W rows per CTA
+constexpr int kAStages = 4, kWStages = 4, kRawStages = 2;
+constexpr int kSlabBytes = 16 * kBN;               // one 16-byte slab of 128 rows
+constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 384)
+constexpr uint32_t kWCol0 = 256;
+constexpr float kWScale = 256.0f;                  // Q formats: W is computed as 2^8 * w
+
+// 64-K steps per raw stage and 16-byte slabs per row per raw stage.
+template <int FMT> constexpr int kSub = FMT == LQ_FMT_F16 ? 2 : 4;
+template <int FMT> constexpr int kSlabs = FMT == LQ_FMT_F16 ? 16 : (FMT == LQ_FMT_Q8_0 ? 17 : 9);
+
+struct TmaGemmParams {
+  float* C;
+  const float* scale;  // s_m per token (from the pre-pass)
+  int M, N, K;
+  int bt;              // tokens per CTA (multiple of 16, <= 256)
+  unsigned long long wait_ns;
+  unsigned wait_iters;
+};
+
+struct Bars {
+  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t a_full[kAStages], a_empty[kAStages];
+  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t tmem_full;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+__device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_tma_err, 0u, code); }
+
+// ---------------------------------------------------------------------------
+// Pre-pass: A f32 [M,K] -> f16 [M,K] scaled by 1/s_m, s_m = 2^(e-15) where
+// max|a_m| < 2^e (frexp), so max|a_m/s_m| lies in [2^14, 2^15).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) a_to_f16_kernel(const float* __restrict__ A,
+                                                        __half* __restrict__ A16,
+                                                        float* __restrict__ scale, int M, int K) {
+  __shared__ float red[8];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x;
+  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+    const float4* a = reinterpret_cast<const float4*>(A + static_cast<long long>(m) * K);
+    float amax = 0.f;
+    for (int i = tid; i < K / 4; i += 256) {
+      const float4 v = a[i];
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if ((tid & 31) == 0) red[tid >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+    __syncthreads();
+    int e = 0;
+    float inv = 1.f, s = 1.f;
+    if (amax > 0.f && amax <= 3.4e38f) {
+      frexpf(amax, &e);
+      s = ldexpf(1.f, e - 15);
+      inv = ldexpf(1.f, 15 - e);
+    }
+    __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
+    for (int i = tid; i < K / 4; i += 256) {
+      const float4 v = a[i];
+      out[2 * i] = __floats2half2_rn(v.x * inv, v.y * inv);
+      out[2 * i + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
+    }
+    if (tid == 0) scale[m] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Converters: 64 K of one W row (raw slabs in shared memory, this thread's
+// row at `row` = ring base + 16 * row) -> 32 words of packed f16 pairs
+// (word j = elements 2j, 2j+1; low half = even element).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+template <int FMT, int SUB>
+__device__ __forceinline__ void convert64(uint32_t row, uint32_t (&out)[32]) {
+  if constexpr (FMT == LQ_FMT_F16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint4 v = lds128(row + static_cast<uint32_t>(SUB * 8 + i) * kSlabBytes);
+      out[4 * i] = v.x;
+      out[4 * i + 1] = v.y;
+      out[4 * i + 2] = v.z;
+      out[4 * i + 3] = v.w;
+    }
+  } else if constexpr (FMT == LQ_FMT_Q8_0) {
+    // two 34-byte blocks at byte 68*SUB of the row's 272 raw bytes
+    constexpr int s0 = (68 * SUB) / 16, off = SUB;  // first slab, word offset in it
+    uint32_t w[20];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * kSlabBytes);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    const __half2 bias = __float2half2_rn(1152.0f);  // 1024 + 128
+    const __half2 d0 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off] & 0xFFFFu))),
+                               __float2half2_rn(kWScale));
+    const __half2 d1 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off + 8] >> 16))),
+                               __float2half2_rn(kWScale));
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      // block 0: bytes 2+2p, 3+2p; block 1: bytes 36+2p, 37+2p
+      const int b0 = 2 + 2 * p, b1 = 36 + 2 * p;
+      const uint32_t x0 = w[off + (b0 >> 2)] ^ 0x80808080u;
+      const uint32_t x1 = w[off + (b1 >> 2)] ^ 0x80808080u;
+      const uint32_t v0 = __byte_perm(x0, 0x64646464u, (b0 & 2) ? 0x4342u : 0x4140u);
+      const uint32_t v1 = __byte_perm(x1, 0x64646464u, (b1 & 2) ? 0x4342u : 0x4140u);
+      out[p] = h2_bits(__hmul2(__hsub2(bits_h2(v0), bias), d0));
+      out[16 + p] = h2_bits(__hmul2(__hsub2(bits_h2(v1), bias), d1));
+    }
+  } else {
+    // two 18-byte blocks at byte 36*SUB of the row's 144 raw bytes
+    constexpr int s0 = (36 * SUB) / 16, off = SUB;
+    uint32_t w[12];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * kSlabBytes);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    const __half2 bias = __float2half2_rn(1032.0f);  // 1024 + 8
+    const __half2 d0 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off] & 0xFFFFu))),
+                               __float2half2_rn(kWScale));
+    const __half2 d1 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off + 4] >> 16))),
+                               __float2half2_rn(kWScale));
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      // bytes j = 2+2p, 3+2p of block 0 (and 20+2p.. of block 1) hold
+      // q_{2p}, q_{2p+1} (low nibbles) and q_{16+2p}, q_{17+2p} (high)
+      const int b0 = 2 + 2 * p, b1 = 20 + 2 * p;
+      const uint32_t x0 = w[off + (b0 >> 2)], x1 = w[off + (b1 >> 2)];
+      const uint32_t s0sel = (b0 & 2) ? 0x4342u : 0x4140u, s1sel = (b1 & 2) ? 0x4342u : 0x4140u;
+      const uint32_t lo0 = __byte_perm(x0 & 0x0F0F0F0Fu, 0x64646464u, s0sel);
+      const uint32_t hi0 = __byte_perm((x0 >> 4) & 0x0F0F0F0Fu, 0x64646464u, s0sel);
+      const uint32_t lo1 = __byte_perm(x1 & 0x0F0F0F0Fu, 0x64646464u, s1sel);
+      const uint32_t hi1 = __byte_perm((x1 >> 4) & 0x0F0F0F0Fu, 0x64646464u, s1sel);
+      out[p] = h2_bits(__hmul2(__hsub2(bits_h2(lo0), bias), d0));
+      out[8 + p] = h2_bits(__hmul2(__hsub2(bits_h2(hi0), bias), d0));
+      out[16 + p] = h2_bits(__hmul2(__hsub2(bits_h2(lo1), bias), d1));
+      out[24 + p] = h2_bits(__hmul2(__hsub2(bits_h2(hi1), bias), d1));
+    }
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ void convert64_dyn(int sub, uint32_t row, uint32_t (&out)[32]) {
+  switch (sub) {
+    case 0: convert64<FMT, 0>(row, out); break;
+    case 1: convert64<FMT, 1>(row, out); break;
+    case 2: convert64<FMT, 2>(row, out); break;
+    default: convert64<FMT, 3>(row, out); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
+// Warps 2..9: converters in two groups of four (group g converts the 64-K
+// steps with ks % 2 == g into W stage ks % 4); warps 2..5 then run the
+// epilogue. Ring phases: every barrier below is waited on by one party that
+// sees all of its phases in order (the producer for raw_empty / a_empty, the
+// owning converter group for raw_full / w_empty, the MMA thread for a_full /
+// w_full), so no waiter can mistake an older phase.
+// ---------------------------------------------------------------------------
+template <int FMT>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    gemm_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                    const TmaGemmParams p) {
+  constexpr int SUB = kSub<FMT>, SLABS = kSlabs<FMT>;
+  constexpr int kRawBytes = SLABS * kSlabBytes;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  const uint32_t base_u = (raw_u + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u - raw_u);
+  const int bt = p.bt;
+  const uint32_t a_tile_bytes = static_cast<uint32_t>(bt) * 128u;
+  uint8_t* a_ring = base;                                  // kAStages x bt x 128 B (swizzled)
+  uint8_t* w_ring = base + kAStages * a_tile_bytes;        // kRawStages x raw slabs
+  Bars& b = *reinterpret_cast<Bars*>(w_ring + kRawStages * kRawBytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bt;
+  const int nk = p.K / 64, nraw = nk / SUB;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(&b.raw_full[i], 1);
+      mbar_init(&b.raw_empty[i], kNumConv);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&b.a_full[i], 1);
+      mbar_init(&b.a_empty[i], 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&b.w_full[i], 4);
+      mbar_init(&b.w_empty[i], 1);
+    }
+    mbar_init(&b.tmem_full, 1);
+    b.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&b.tmem_base, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = b.tmem_base;
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- producer ----------------
+      tc::prefetch_tmap(&tmW);
+      tc::prefetch_tmap(&tmA);
+      auto issue_raw = [&](int j) {
+        const int slot = j % kRawStages;
+        mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
+        for (int s = 0; s < SLABS; ++s)
+          tc::tma_load_2d(w_ring + slot * kRawBytes + s * kSlabBytes, &tmW, 4 * (j * SLABS + s), n0,
+                          &b.raw_full[slot]);
+      };
+      int raw_issued = 0, a_issued = 0;
+      bool ok = true;
+      // W does not depend on the previous kernel: start it before waiting.
+      for (; raw_issued < nraw && raw_issued < kRawStages; ++raw_issued) issue_raw(raw_issued);
+      pdl_wait();
+      for (int ks = 0; ks < nk && ok; ++ks) {
+        const int j = ks / SUB;
+        if (ks % SUB == 0 && j >= raw_issued) {
+          if (!mbar_wait(&b.raw_empty[j % kRawStages], ((j / kRawStages) - 1) & 1, p.wait_ns, p.wait_iters) ||
+              b.abort) {
+            ok = false;
+            break;
+          }
+          issue_raw(j);
+          ++raw_issued;
+        }
+        const int as = ks % kAStages;
+        if (ks >= kAStages &&
+            (!mbar_wait(&b.a_empty[as], ((ks / kAStages) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&b.a_full[as], a_tile_bytes);
+        tc::tma_load_2d(a_ring + as * a_tile_bytes, &tmA, 64 * ks, m0, &b.a_full[as]);
+        ++a_issued;
+      }
+      if (!ok) {
+        record_error(kDevErrTimeout);
+        b.abort = 1;
+      }
+      // never leave copies in flight
+      for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
+        mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, kDrainWaitNs);
+      for (int ks = max(0, a_issued - kAStages); ks < a_issued; ++ks)
+        mbar_wait(&b.a_full[ks % kAStages], (ks / kAStages) & 1, kDrainWaitNs);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
+      for (int ks = 0; ks < nk; ++ks) {
+        const int st = ks % kAStages;
+        const uint32_t ph = (ks / kAStages) & 1;
+        if (!mbar_wait(&b.a_full[st], ph, p.wait_ns, p.wait_iters) ||
+            !mbar_wait(&b.w_full[st], ph, p.wait_ns, p.wait_iters) || b.abort) {
+          record_error(kDevErrTimeout);
+          b.abort = 1;
+          break;
+        }
+        tc::fence_after_sync();
+        const uint64_t bdesc = tc::desc_sw128_kmajor(smem_u32(a_ring + st * a_tile_bytes));
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc::mma_f16_ts(tmem, tmem + kWCol0 + 32u * st + 8u * kk, bdesc + 2u * kk, idesc,
+                         (ks > 0 || kk > 0) ? 1u : 0u);
+        tc::commit(&b.a_empty[st]);
+        tc::commit(&b.w_empty[st]);
+      }
+      tc::commit(&b.tmem_full);
+      if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
+    }
+  } else {
+    // ---------------- converters ----------------
+    const int cw = warp - 2, g = cw >> 2, q4 = warp & 3;
+    const int r = 32 * q4 + lane;  // W row in the tile = TMEM lane
+    const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
+    bool ok = true;
+    for (int ks = g; ks < nk && ok; ks += 2) {
+      const int j = ks / SUB, sub = ks % SUB, ws = ks % kWStages;
+      if (sub == g &&
+          (!mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+        ok = false;
+        break;
+      }
+      if (ks >= kWStages &&
+          (!mbar_wait(&b.w_empty[ws], ((ks / kWStages) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+        ok = false;
+        break;
+      }
+      uint32_t out[32];
+      convert64_dyn<FMT>(sub, smem_u32(w_ring + (j % kRawStages) * kRawBytes) + 16u * r, out);
+      tc::st_32x32b_x32(tmem + tlane + kWCol0 + 32u * ws, out);
+      tc::wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&b.w_full[ws]);
+        if (sub == SUB - 2 + g) mbar_arrive(&b.raw_empty[j % kRawStages]);
+      }
+    }
+    if (!ok) {
+      record_error(kDevErrTimeout);
+      b.abort = 1;
+    }
+    if (g == 0) {
+      // ---------------- epilogue ----------------
+      const bool have = mbar_wait(&b.tmem_full, 0, p.wait_ns, p.wait_iters);
+      tc::fence_after_sync();
+      if (!have) {
+        record_error(kDevErrTimeout);
+        b.abort = 1;
+      }
+      if (have && !b.abort) {
+        const int n = n0 + r;
+        const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
+#pragma unroll 1
+        for (int c = 0; c < (bt + 31) / 32; ++c) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
+          tc::wait_ld();
+          if (n < p.N) {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int m = m0 + 32 * c + jj;
+              if (32 * c + jj < bt && m < p.M)
+                p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * (__ldg(p.scale + m) * wunscale);
+            }
+          }
+        }
+      }
+    }
+  }
+  // ---------------- teardown ----------------
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+bool aligned(const void* p, unsigned al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
+
+int kstep_multiple(int fmt) { return fmt == LQ_FMT_F16 ? 128 : 256; }
+
+// Token-tile width: enough tiles to put about one CTA on every SM, at most
+// 256 tokens (the MMA's N limit) and at least 16.
+int pick_bt(int64_t M, int64_t N) {
+  const DeviceInfo& di = device_info();
+  const int64_t ntn = (N + kBN - 1) / kBN;
+  int64_t t = std::max<int64_t>(1, (di.sm_count + ntn / 2) / ntn);
+  t = std::max<int64_t>(t, (M + 255) / 256);
+  t = std::min<int64_t>(t, (M + 15) / 16);
+  const int64_t per = (M + t - 1) / t;
+  return static_cast<int>(std::min<int64_t>(256, (per + 15) / 16 * 16));
+}
+
+size_t tma_smem_bytes(int fmt, int bt) {
+  const int slabs = fmt == LQ_FMT_F16 ? 16 : (fmt == LQ_FMT_Q8_0 ? 17 : 9);
+  const size_t need = 1024 + static_cast<size_t>(kAStages) * bt * 128 +
+                      static_cast<size_t>(kRawStages) * slabs * kSlabBytes + sizeof(Bars) + 64;
+  // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
+  return std::max<size_t>(need, 116 * 1024);
+}
+
+template <int FMT>
+lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
+                             const TmaGemmParams& p) {
+  auto kern = gemm_tma_kernel<FMT>;
+  const size_t smem = tma_smem_bytes(FMT, p.bt);
+  static int configured[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
+  if (configured[dev] < static_cast<int>(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_status(e);
+    configured[dev] = static_cast<int>(smem);
+  }
+  const dim3 grid(static_cast<unsigned>((a.N + kBN - 1) / kBN), static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
+  cudaError_t e = launch_pdl(kern, grid, dim3(kTmaThreads), smem, a.stream, tmW, tmA, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+}  // namespace
+
+unsigned read_clear_gemm_tma_error() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tma_err, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_tma_err, &z, sizeof(z));
+  return v;
+}
+
+bool gemm_tma_eligible(const MatmulArgs& a) {
+  if (a.M < 2 || a.K % kstep_multiple(a.fmt) != 0) return false;
+  if (!aligned(a.A, 16) || !aligned(a.W, 16)) return false;
+  if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
+  if (!encode_fn()) return false;
+  const DeviceInfo& di = device_info();
+  return di.cc_major >= 10 && di.max_smem_optin >= static_cast<int>(tma_smem_bytes(a.fmt, 256));
+}
+
+// The operands of the tensor-core kernel (f16 copy of A and its per-token
+// scales) live in a stream-ordered workspace taken from the device's default
+// memory pool for the duration of the call.
+lq_status launch_gemm_tma(const MatmulArgs& a) {
+  const int bt = pick_bt(a.M, a.N);
+  const size_t a16_bytes = static_cast<size_t>(a.M) * a.K * 2;
+  const size_t ws_bytes = (a16_bytes + 255) / 256 * 256 + static_cast<size_t>(a.M) * 4;
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocAsync(&ws, ws_bytes, a.stream);
+  if (e != cudaSuccess) return LQ_ERR_CUDA;
+  __half* A16 = static_cast<__half*>(ws);
+  float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (a16_bytes + 255) / 256 * 256);
+  lq_status st = launch_gemm_tma_ws(a, A16, scale, bt);
+  cudaError_t ef = cudaFreeAsync(ws, a.stream);
+  if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
+  if (st == LQ_OK) count_route(2);
+  return st;
+}
+
+// Pre-pass + GEMM given a workspace of M*K halves (A16) and M floats (scale).
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt) {
+  const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
+  const DeviceInfo& di = device_info();
+  // 1. A -> f16 with per-token power-of-two scales
+  const int pre_grid = std::min(M, 4 * std::max(di.sm_count, 1));
+  cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(pre_grid), dim3(256), 0, a.stream, a.A,
+                             static_cast<__half*>(a16), scale, M, K);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return LQ_ERR_CUDA;
+
+  // 2. tensor maps: raw W as [N][row_bytes/4] 32-bit words, boxes of
+  //    4 words x 128 rows (one 16-byte slab); A16 as [M][K] halves, boxes of
+  //    64 x bt with the 128-byte swizzle of the MMA operand.
+  EncodeTiled enc = encode_fn();
+  if (!enc) return LQ_ERR_UNSUPPORTED;
+  const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
+  CUtensorMap tmW, tmA;
+  {
+    cuuint64_t dims[2] = {rb / 4, static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {rb};
+    cuuint32_t box[2] = {4, kBN};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a.W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bt)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a16, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  }
+  TmaGemmParams p;
+  p.C = a.C;
+  p.scale = scale;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.bt = bt;
+  p.wait_ns = wait_limit_ns();
+  p.wait_iters = wait_limit_iters();
+  lq_status st;
+  if (a.fmt == LQ_FMT_F16)
+    st = launch_gemm_kernel<LQ_FMT_F16>(a, tmW, tmA, p);
+  else if (a.fmt == LQ_FMT_Q8_0)
+    st = launch_gemm_kernel<LQ_FMT_Q8_0>(a, tmW, tmA, p);
+  else
+    st = launch_gemm_kernel<LQ_FMT_Q4_0>(a, tmW, tmA, p);
+  return st;
+}
+
+}  // namespace lq

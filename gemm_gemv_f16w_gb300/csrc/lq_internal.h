@@ -46,12 +46,18 @@ inline int64_t row_bytes(int fmt, int64_t K) {
 lq_status launch_gemv(const MatmulArgs& a);            // M == 1, picks fast or generic
 lq_status launch_gemv_generic(const MatmulArgs& a);    // any M, K, alignment
 lq_status launch_gemm_stream(const MatmulArgs& a);     // CUDA-core, small M
-lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05
+lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via shared memory
 bool gemm_tc_eligible(const MatmulArgs& a);
+// tcgen05 with TMA loads and W in tensor memory; allocates its workspace
+lq_status launch_gemm_tma(const MatmulArgs& a);
+// the same given a workspace: M*K halves at a16 (16-byte aligned), M floats at scale
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt);
+bool gemm_tma_eligible(const MatmulArgs& a);
 
 // Device status words of each translation unit (read-and-clear).
 unsigned read_clear_gemv_error();
 unsigned read_clear_gemm_error();
+unsigned read_clear_gemm_tma_error();
 
 lq_status cuda_status(cudaError_t e);
 
