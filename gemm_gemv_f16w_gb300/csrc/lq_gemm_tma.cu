@@ -44,7 +44,7 @@ __device__ unsigned g_tma_err;
 constexpr int kNumConv = 8;                        // converter warps (2 groups of 4)
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
-constexpr int kAStages = 4, kWStages = 4, kRawStages = 2;
+constexpr int kAStages = 6, kWStages = 4, kRawStages = 2;  // A ring: up to kAStages
 constexpr int kSlabBytes = 16 * kBN;               // one 16-byte slab of 128 rows
 constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 384)
 constexpr uint32_t kWCol0 = 256;
@@ -59,6 +59,7 @@ struct TmaGemmParams {
   const float* scale;  // s_m per token (from the pre-pass)
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
+  int a_stages;        // depth of the A-tile ring (2..kAStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
@@ -81,25 +82,37 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_tma_e
 __global__ void __launch_bounds__(256) a_to_f16_kernel(const float* __restrict__ A,
                                                         __half* __restrict__ A16,
                                                         float* __restrict__ scale, int M, int K) {
-  __shared__ float red[8];
   pdl_launch_dependents();
   pdl_wait();
-  const int tid = threadIdx.x;
-  for (int m = blockIdx.x; m < M; m += gridDim.x) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), nw = gridDim.x * 8;
+  constexpr int kChunk = 32 * 4 * 8;  // floats one warp keeps in registers per pass
+  for (int m = gw; m < M; m += nw) {
     const float4* a = reinterpret_cast<const float4*>(A + static_cast<long long>(m) * K);
+    __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
+    // pass 1: row maximum (rows up to kChunk floats stay in registers)
+    float4 keep[8];
     float amax = 0.f;
-    for (int i = tid; i < K / 4; i += 256) {
-      const float4 v = a[i];
-      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int idx = lane + 32 * i;
+      keep[i] = idx < K / 4 ? a[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    for (int base = 0; base < K / 4; base += 256) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if ((tid & 31) == 0) red[tid >> 5] = amax;
-    __syncthreads();
-    amax = red[0];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
-    __syncthreads();
+      for (int i = 0; i < 8; ++i) {
+        const int idx = base + lane + 32 * i;
+        if (idx < K / 4) {
+          const float4 v = base == 0 ? keep[i] : a[idx];
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+      }
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     int e = 0;
     float inv = 1.f, s = 1.f;
     if (amax > 0.f && amax <= 3.4e38f) {
@@ -107,14 +120,21 @@ __global__ void __launch_bounds__(256) a_to_f16_kernel(const float* __restrict__
       s = ldexpf(1.f, e - 15);
       inv = ldexpf(1.f, 15 - e);
     }
-    __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
-    for (int i = tid; i < K / 4; i += 256) {
-      const float4 v = a[i];
-      out[2 * i] = __floats2half2_rn(v.x * inv, v.y * inv);
-      out[2 * i + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
+    // pass 2: scale (exact) and round to f16
+    for (int base = 0; base < K / 4; base += 256) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int idx = base + lane + 32 * i;
+        if (idx < K / 4) {
+          const float4 v = base == 0 ? keep[i] : a[idx];
+          out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
+          out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
+        }
+      }
     }
-    if (tid == 0) scale[m] = s;
+    if (lane == 0) scale[m] = s;
   }
+  (void)kChunk;
 }
 
 // ---------------------------------------------------------------------------
@@ -230,9 +250,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
   const int bt = p.bt;
+  const int AS = p.a_stages;
   const uint32_t a_tile_bytes = static_cast<uint32_t>(bt) * 128u;
-  uint8_t* a_ring = base;                                  // kAStages x bt x 128 B (swizzled)
-  uint8_t* w_ring = base + kAStages * a_tile_bytes;        // kRawStages x raw slabs
+  uint8_t* a_ring = base;                                  // AS x bt x 128 B (swizzled)
+  uint8_t* w_ring = base + AS * a_tile_bytes;        // kRawStages x raw slabs
   Bars& b = *reinterpret_cast<Bars*>(w_ring + kRawStages * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,7 +265,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(&b.raw_full[i], 1);
       mbar_init(&b.raw_empty[i], kNumConv);
     }
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = 0; i < AS; ++i) {
       mbar_init(&b.a_full[i], 1);
       mbar_init(&b.a_empty[i], 1);
     }
@@ -294,9 +315,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           issue_raw(j);
           ++raw_issued;
         }
-        const int as = ks % kAStages;
-        if (ks >= kAStages &&
-            (!mbar_wait(&b.a_empty[as], ((ks / kAStages) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+        const int as = ks % AS;
+        if (ks >= AS &&
+            (!mbar_wait(&b.a_empty[as], ((ks / AS) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
           ok = false;
           break;
         }
@@ -311,30 +332,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       // never leave copies in flight
       for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
         mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, kDrainWaitNs);
-      for (int ks = max(0, a_issued - kAStages); ks < a_issued; ++ks)
-        mbar_wait(&b.a_full[ks % kAStages], (ks / kAStages) & 1, kDrainWaitNs);
+      for (int ks = max(0, a_issued - AS); ks < a_issued; ++ks)
+        mbar_wait(&b.a_full[ks % AS], (ks / AS) & 1, kDrainWaitNs);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
       for (int ks = 0; ks < nk; ++ks) {
-        const int st = ks % kAStages;
-        const uint32_t ph = (ks / kAStages) & 1;
-        if (!mbar_wait(&b.a_full[st], ph, p.wait_ns, p.wait_iters) ||
-            !mbar_wait(&b.w_full[st], ph, p.wait_ns, p.wait_iters) || b.abort) {
+        const int as = ks % AS, ws = ks % kWStages;
+        if (!mbar_wait(&b.a_full[as], (ks / AS) & 1, p.wait_ns, p.wait_iters) ||
+            !mbar_wait(&b.w_full[ws], (ks / kWStages) & 1, p.wait_ns, p.wait_iters) || b.abort) {
           record_error(kDevErrTimeout);
           b.abort = 1;
           break;
         }
         tc::fence_after_sync();
-        const uint64_t bdesc = tc::desc_sw128_kmajor(smem_u32(a_ring + st * a_tile_bytes));
+        const uint64_t bdesc = tc::desc_sw128_kmajor(smem_u32(a_ring + as * a_tile_bytes));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc::mma_f16_ts(tmem, tmem + kWCol0 + 32u * st + 8u * kk, bdesc + 2u * kk, idesc,
+          tc::mma_f16_ts(tmem, tmem + kWCol0 + 32u * ws + 8u * kk, bdesc + 2u * kk, idesc,
                          (ks > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&b.a_empty[st]);
-        tc::commit(&b.w_empty[st]);
+        tc::commit(&b.a_empty[as]);
+        tc::commit(&b.w_empty[ws]);
       }
       tc::commit(&b.tmem_full);
       if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
@@ -463,10 +483,20 @@ int pick_bt(int64_t M, int64_t N) {
   return static_cast<int>(std::min<int64_t>(256, (per + 15) / 16 * 16));
 }
 
-size_t tma_smem_bytes(int fmt, int bt) {
-  const int slabs = fmt == LQ_FMT_F16 ? 16 : (fmt == LQ_FMT_Q8_0 ? 17 : 9);
-  const size_t need = 1024 + static_cast<size_t>(kAStages) * bt * 128 +
-                      static_cast<size_t>(kRawStages) * slabs * kSlabBytes + sizeof(Bars) + 64;
+int raw_slabs(int fmt) { return fmt == LQ_FMT_F16 ? 16 : (fmt == LQ_FMT_Q8_0 ? 17 : 9); }
+
+// Depth of the A-tile ring that fits next to the raw-W ring.
+int a_stages_for(int fmt, int bt) {
+  const DeviceInfo& di = device_info();
+  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - 256 -
+                           static_cast<long long>(kRawStages) * raw_slabs(fmt) * kSlabBytes;
+  const long long n = budget / (static_cast<long long>(bt) * 128);
+  return static_cast<int>(std::min<long long>(kAStages, n));
+}
+
+size_t tma_smem_bytes(int fmt, int bt, int a_stages) {
+  const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 128 +
+                      static_cast<size_t>(kRawStages) * raw_slabs(fmt) * kSlabBytes + sizeof(Bars) + 64;
   // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
   return std::max<size_t>(need, 116 * 1024);
 }
@@ -475,7 +505,7 @@ template <int FMT>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              const TmaGemmParams& p) {
   auto kern = gemm_tma_kernel<FMT>;
-  const size_t smem = tma_smem_bytes(FMT, p.bt);
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.a_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -505,18 +535,43 @@ bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
   if (!encode_fn()) return false;
   const DeviceInfo& di = device_info();
-  return di.cc_major >= 10 && di.max_smem_optin >= static_cast<int>(tma_smem_bytes(a.fmt, 256));
+  return di.cc_major >= 10 && a_stages_for(a.fmt, 256) >= 3;
+}
+
+// The library's own stream-ordered memory pool on the current device: freed
+// blocks stay in the pool (release threshold = max), so repeated calls and
+// CUDA-graph replays do not map and unmap memory each time.
+cudaMemPool_t workspace_pool() {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t thr = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    pools[dev] = pool;
+  }
+  return pools[dev];
 }
 
 // The operands of the tensor-core kernel (f16 copy of A and its per-token
-// scales) live in a stream-ordered workspace taken from the device's default
-// memory pool for the duration of the call.
+// scales) live in a stream-ordered workspace from the library's pool for the
+// duration of the call.
 lq_status launch_gemm_tma(const MatmulArgs& a) {
   const int bt = pick_bt(a.M, a.N);
   const size_t a16_bytes = static_cast<size_t>(a.M) * a.K * 2;
   const size_t ws_bytes = (a16_bytes + 255) / 256 * 256 + static_cast<size_t>(a.M) * 4;
   void* ws = nullptr;
-  cudaError_t e = cudaMallocAsync(&ws, ws_bytes, a.stream);
+  cudaMemPool_t pool = workspace_pool();
+  if (!pool) return LQ_ERR_CUDA;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
   if (e != cudaSuccess) return LQ_ERR_CUDA;
   __half* A16 = static_cast<__half*>(ws);
   float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (a16_bytes + 255) / 256 * 256);
@@ -532,7 +587,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
   const DeviceInfo& di = device_info();
   // 1. A -> f16 with per-token power-of-two scales
-  const int pre_grid = std::min(M, 4 * std::max(di.sm_count, 1));
+  const int pre_grid = std::max(1, std::min((M + 7) / 8, 8 * std::max(di.sm_count, 1)));
   cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(pre_grid), dim3(256), 0, a.stream, a.A,
                              static_cast<__half*>(a16), scale, M, K);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -572,6 +627,8 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   p.N = N;
   p.K = K;
   p.bt = bt;
+  p.a_stages = a_stages_for(a.fmt, bt);
+  if (p.a_stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   lq_status st;
