@@ -19,12 +19,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 // ---- mbarrier -------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
@@ -65,11 +59,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase with the given parity to complete, for at most
+// Waits for the phase with the given parity to complete, for at most about
 // `limit_ns` nanoseconds and `max_iters` polls. Returns false on timeout.
-// A small poll budget (a debugging override) polls without blocking, so that
-// the wait gives up deterministically; otherwise the hardware's potentially
-// blocking try_wait is used.
+// The deadline is kept in SM clock cycles (clock64 is cheap to read; the
+// limit is converted at 4 cycles per ns, so at clocks up to 4 GHz the wait
+// lasts at least `limit_ns`). A small poll budget (a debugging override)
+// polls without blocking, so that the wait gives up deterministically;
+// otherwise the hardware's potentially blocking try_wait is used.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           unsigned long long limit_ns,
                                           uint32_t max_iters = (1u << 30)) {
@@ -79,10 +75,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return false;
   }
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
+  const long long t0 = clock64();
+  const long long limit = static_cast<long long>(limit_ns) * 4;
   for (uint32_t it = 1; it < max_iters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 15u && globaltimer() - t0 > limit_ns) return false;
+    if ((it & 15u) == 15u && clock64() - t0 > limit) return false;
   }
   return false;
 }

@@ -12,10 +12,12 @@
 //     undone exactly in the epilogue;
 //  2. the GEMM kernel, one CTA per SM, owns 128 rows of W and a tile of BT
 //     tokens. A producer thread moves raw W (f16 / Q8_0 / Q4_0 bytes) with
-//     TMA as 16-byte "slabs" (slab s of all 128 rows contiguous), so that a
-//     thread reading its own row does so with conflict-free 16-byte loads,
-//     and moves the f16 A tile with TMA straight into the 128-byte-swizzled
-//     K-major layout of the MMA's B operand;
+//     one TMA box of full-width rows per stage: Q8_0 rows of 256 K are 272
+//     bytes and Q4_0 rows 144 bytes, both odd multiples of 16, so eight
+//     threads reading 16-byte chunks of eight consecutive rows hit eight
+//     different bank groups; f16 rows (64 K = 128 bytes per box) use the
+//     TMA's 128-byte swizzle for the same effect. The f16 A tile arrives the
+//     same way in the swizzled K-major layout of the MMA's B operand;
 //  3. eight converter warps (thread = W row = TMEM lane) dequantise 64 K of
 //     their row at a time with half2 arithmetic (Q8_0: q*d, Q4_0: (q-8)*d,
 //     computed in f16 with W scaled by 2^8 to stay clear of f16 subnormals)
@@ -44,36 +46,44 @@ __device__ unsigned g_tma_err;
 constexpr int kNumConv = 8;                        // converter warps (2 groups of 4)
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
-constexpr int kAStages = 6, kWStages = 4, kRawStages = 2;  // A ring: up to kAStages
-constexpr int kSlabBytes = 16 * kBN;               // one 16-byte slab of 128 rows
-constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 384)
+constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
+constexpr int kMaxStages = 4, kRawStages = 2;
+constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
 constexpr uint32_t kWCol0 = 256;
 constexpr float kWScale = 256.0f;                  // Q formats: W is computed as 2^8 * w
 
-// 64-K steps per raw stage and 16-byte slabs per row per raw stage.
-template <int FMT> constexpr int kSub = FMT == LQ_FMT_F16 ? 2 : 4;
-template <int FMT> constexpr int kSlabs = FMT == LQ_FMT_F16 ? 16 : (FMT == LQ_FMT_Q8_0 ? 17 : 9);
+// Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
+// formats: 256 K in one box; f16: 128 K as two boxes of 64 K, each 128 rows
+// x 128 bytes, swizzled).
+template <int FMT> constexpr int kSub = FMT == LQ_FMT_F16 ? 1 : 2;
+template <int FMT> constexpr int kRowBytes = FMT == LQ_FMT_F16 ? 256 : (FMT == LQ_FMT_Q8_0 ? 272 : 144);
 
 struct TmaGemmParams {
   float* C;
   const float* scale;  // s_m per token (from the pre-pass)
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
-  int a_stages;        // depth of the A-tile ring (2..kAStages)
+  int stages;          // pipeline depth (2..kMaxStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
 
 struct Bars {
   uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  uint64_t a_full[kAStages], a_empty[kAStages];
-  uint64_t w_full[kWStages], w_empty[kWStages];
+  uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
+  uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
   uint64_t tmem_full;
   uint32_t tmem_base;
   volatile int abort;
 };
 
 __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_tma_err, 0u, code); }
+
+// Bounded wait by all 32 lanes of a warp, with one outcome for the warp.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const TmaGemmParams& p) {
+  const bool ok = mbar_wait(bar, parity, p.wait_ns, p.wait_iters);
+  return __all_sync(0xffffffffu, ok);
+}
 
 // ---------------------------------------------------------------------------
 // Pre-pass: A f32 [M,K] -> f16 [M,K] scaled by 1/s_m, s_m = 2^(e-15) where
@@ -138,19 +148,21 @@ __global__ void __launch_bounds__(256) a_to_f16_kernel(const float* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// Converters: 64 K of one W row (raw slabs in shared memory, this thread's
-// row at `row` = ring base + 16 * row) -> 32 words of packed f16 pairs
-// (word j = elements 2j, 2j+1; low half = even element).
+// Converters: 64 K of W row r (raw stage in shared memory at `stage`) ->
+// 32 words of packed f16 pairs (word j = elements 2j, 2j+1; low half = even
+// element).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 template <int FMT, int SUB>
-__device__ __forceinline__ void convert64(uint32_t row, uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
   if constexpr (FMT == LQ_FMT_F16) {
+    // box SUB: 128 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)
+    const uint32_t row = stage + SUB * (kBN * 128u) + r * 128u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const uint4 v = lds128(row + static_cast<uint32_t>(SUB * 8 + i) * kSlabBytes);
+      const uint4 v = lds128(row + ((static_cast<uint32_t>(i) ^ (r & 7u)) << 4));
       out[4 * i] = v.x;
       out[4 * i + 1] = v.y;
       out[4 * i + 2] = v.z;
@@ -158,11 +170,12 @@ __device__ __forceinline__ void convert64(uint32_t row, uint32_t (&out)[32]) {
     }
   } else if constexpr (FMT == LQ_FMT_Q8_0) {
     // two 34-byte blocks at byte 68*SUB of the row's 272 raw bytes
-    constexpr int s0 = (68 * SUB) / 16, off = SUB;  // first slab, word offset in it
+    constexpr int s0 = (68 * SUB) / 16, off = SUB;  // first 16-byte chunk, word offset in it
+    const uint32_t row = stage + r * 272u;
     uint32_t w[20];
 #pragma unroll
     for (int i = 0; i < 5; ++i) {
-      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * kSlabBytes);
+      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * 16u);
       w[4 * i] = v.x;
       w[4 * i + 1] = v.y;
       w[4 * i + 2] = v.z;
@@ -187,10 +200,11 @@ __device__ __forceinline__ void convert64(uint32_t row, uint32_t (&out)[32]) {
   } else {
     // two 18-byte blocks at byte 36*SUB of the row's 144 raw bytes
     constexpr int s0 = (36 * SUB) / 16, off = SUB;
+    const uint32_t row = stage + r * 144u;
     uint32_t w[12];
 #pragma unroll
     for (int i = 0; i < 3; ++i) {
-      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * kSlabBytes);
+      const uint4 v = lds128(row + static_cast<uint32_t>(s0 + i) * 16u);
       w[4 * i] = v.x;
       w[4 * i + 1] = v.y;
       w[4 * i + 2] = v.z;
@@ -221,57 +235,55 @@ __device__ __forceinline__ void convert64(uint32_t row, uint32_t (&out)[32]) {
 }
 
 template <int FMT>
-__device__ __forceinline__ void convert64_dyn(int sub, uint32_t row, uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
   switch (sub) {
-    case 0: convert64<FMT, 0>(row, out); break;
-    case 1: convert64<FMT, 1>(row, out); break;
-    case 2: convert64<FMT, 2>(row, out); break;
-    default: convert64<FMT, 3>(row, out); break;
+    case 0: convert64<FMT, 0>(stage, r, out); break;
+    case 1: convert64<FMT, 1>(stage, r, out); break;
+    case 2: convert64<FMT, 2>(stage, r, out); break;
+    default: convert64<FMT, 3>(stage, r, out); break;
   }
 }
 
 // ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
-// Warps 2..9: converters in two groups of four (group g converts the 64-K
-// steps with ks % 2 == g into W stage ks % 4); warps 2..5 then run the
-// epilogue. Ring phases: every barrier below is waited on by one party that
-// sees all of its phases in order (the producer for raw_empty / a_empty, the
-// owning converter group for raw_full / w_empty, the MMA thread for a_full /
-// w_full), so no waiter can mistake an older phase.
+// Warps 2..9: converters in two groups of four (group g converts the
+// pipeline stages ks with ks % 2 == g: 128 K of its W rows into the stage's
+// 64 TMEM columns); warps 2..5 then run the epilogue. Per stage one barrier
+// says "A tile and W operand ready" (1 arrival with the TMA bytes + 4
+// converter warps) and one commit says "the stage's MMAs are done". The
+// producer and MMA warps run their loops with all 32 lanes (every lane
+// waits, lane 0 issues); a lone active lane beside parked lanes issues very
+// slowly. Every waiter sees the phases of the barriers it waits on in order.
 // ---------------------------------------------------------------------------
 template <int FMT>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemm_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const TmaGemmParams p) {
-  constexpr int SUB = kSub<FMT>, SLABS = kSlabs<FMT>;
-  constexpr int kRawBytes = SLABS * kSlabBytes;
+  constexpr int SUB = kSub<FMT>;
+  constexpr int kRawBytes = kRowBytes<FMT> * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
-  const int bt = p.bt;
-  const int AS = p.a_stages;
-  const uint32_t a_tile_bytes = static_cast<uint32_t>(bt) * 128u;
-  uint8_t* a_ring = base;                                  // AS x bt x 128 B (swizzled)
-  uint8_t* w_ring = base + AS * a_tile_bytes;        // kRawStages x raw slabs
+  const int bt = p.bt, S = p.stages;
+  const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
+  const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
+  uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
+  uint8_t* w_ring = base + S * a_stage_bytes;                      // kRawStages x raw W stages
   Bars& b = *reinterpret_cast<Bars*>(w_ring + kRawStages * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bt;
-  const int nk = p.K / 64, nraw = nk / SUB;
+  const int nk = p.K / kKS, nraw = nk / SUB;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       mbar_init(&b.raw_full[i], 1);
-      mbar_init(&b.raw_empty[i], kNumConv);
+      mbar_init(&b.raw_empty[i], 4 * SUB);
     }
-    for (int i = 0; i < AS; ++i) {
-      mbar_init(&b.a_full[i], 1);
-      mbar_init(&b.a_empty[i], 1);
-    }
-    for (int i = 0; i < kWStages; ++i) {
-      mbar_init(&b.w_full[i], 4);
-      mbar_init(&b.w_empty[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&b.full[i], 1 + 4);
+      mbar_init(&b.empty[i], 1);
     }
     mbar_init(&b.tmem_full, 1);
     b.abort = 0;
@@ -288,115 +300,134 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   pdl_launch_dependents();
 
   if (warp == 0) {
+    // ---------------- producer ----------------
     if (lane == 0) {
-      // ---------------- producer ----------------
       tc::prefetch_tmap(&tmW);
       tc::prefetch_tmap(&tmA);
-      auto issue_raw = [&](int j) {
-        const int slot = j % kRawStages;
-        mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
-        for (int s = 0; s < SLABS; ++s)
-          tc::tma_load_2d(w_ring + slot * kRawBytes + s * kSlabBytes, &tmW, 4 * (j * SLABS + s), n0,
+    }
+    auto issue_raw = [&](int j, int slot) {
+      mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
+      if (FMT == LQ_FMT_F16) {
+        for (int h = 0; h < 2; ++h)  // two boxes of 64 halves x 128 rows (128B-swizzled)
+          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * j + 64 * h, n0,
                           &b.raw_full[slot]);
-      };
-      int raw_issued = 0, a_issued = 0;
-      bool ok = true;
-      // W does not depend on the previous kernel: start it before waiting.
-      for (; raw_issued < nraw && raw_issued < kRawStages; ++raw_issued) issue_raw(raw_issued);
-      pdl_wait();
-      for (int ks = 0; ks < nk && ok; ++ks) {
-        const int j = ks / SUB;
-        if (ks % SUB == 0 && j >= raw_issued) {
-          if (!mbar_wait(&b.raw_empty[j % kRawStages], ((j / kRawStages) - 1) & 1, p.wait_ns, p.wait_iters) ||
-              b.abort) {
-            ok = false;
-            break;
-          }
-          issue_raw(j);
-          ++raw_issued;
-        }
-        const int as = ks % AS;
-        if (ks >= AS &&
-            (!mbar_wait(&b.a_empty[as], ((ks / AS) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+      } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
+        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * j, n0, &b.raw_full[slot]);
+      }
+    };
+    int raw_issued = 0, issued = 0;
+    bool ok = true;
+    // W does not depend on the previous kernel: start it before waiting.
+    for (; raw_issued < nraw && raw_issued < kRawStages; ++raw_issued)
+      if (lane == 0) issue_raw(raw_issued, raw_issued);
+    __syncwarp();
+    pdl_wait();
+    int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
+    for (int ks = 0; ks < nk; ++ks) {
+      if (ks % SUB == 0 && ks / SUB >= kRawStages) {
+        const int j = ks / SUB;  // reuse raw slot j % 2 after both of its users finished
+        if (!warp_wait(&b.raw_empty[rslot], rlap & 1, p) || b.abort) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&b.a_full[as], a_tile_bytes);
-        tc::tma_load_2d(a_ring + as * a_tile_bytes, &tmA, 64 * ks, m0, &b.a_full[as]);
-        ++a_issued;
+        if (lane == 0) issue_raw(j, rslot);
+        __syncwarp();
+        ++raw_issued;
+        if (++rslot == kRawStages) { rslot = 0; ++rlap; }
       }
-      if (!ok) {
-        record_error(kDevErrTimeout);
-        b.abort = 1;
+      if (ks >= S && (!warp_wait(&b.empty[st], (lap - 1) & 1, p) || b.abort)) {
+        ok = false;
+        break;
       }
-      // never leave copies in flight
-      for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
-        mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, kDrainWaitNs);
-      for (int ks = max(0, a_issued - AS); ks < a_issued; ++ks)
-        mbar_wait(&b.a_full[ks % AS], (ks / AS) & 1, kDrainWaitNs);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * ks, m0, &b.full[st]);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * ks + 64, m0, &b.full[st]);
+      }
+      __syncwarp();
+      ++issued;
+      if (++st == S) { st = 0; ++lap; }
     }
+    if (!ok && lane == 0) {
+      record_error(kDevErrTimeout);
+      b.abort = 1;
+    }
+    // never leave copies in flight (waits for the last use of every slot)
+    for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
+      mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, kDrainWaitNs);
+    for (int ks = max(0, issued - S); ks < issued; ++ks)
+      mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
-      for (int ks = 0; ks < nk; ++ks) {
-        const int as = ks % AS, ws = ks % kWStages;
-        if (!mbar_wait(&b.a_full[as], (ks / AS) & 1, p.wait_ns, p.wait_iters) ||
-            !mbar_wait(&b.w_full[ws], (ks / kWStages) & 1, p.wait_ns, p.wait_iters) || b.abort) {
-          record_error(kDevErrTimeout);
-          b.abort = 1;
-          break;
-        }
-        tc::fence_after_sync();
-        const uint64_t bdesc = tc::desc_sw128_kmajor(smem_u32(a_ring + as * a_tile_bytes));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc::mma_f16_ts(tmem, tmem + kWCol0 + 32u * ws + 8u * kk, bdesc + 2u * kk, idesc,
-                         (ks > 0 || kk > 0) ? 1u : 0u);
-        tc::commit(&b.a_empty[as]);
-        tc::commit(&b.w_empty[ws]);
+    // ---------------- MMA issuer ----------------
+    const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
+    bool ok = true;
+    int st = 0, lap = 0;
+    for (int ks = 0; ks < nk; ++ks) {
+      if (!warp_wait(&b.full[st], lap & 1, p) || b.abort) {
+        ok = false;
+        break;
       }
-      tc::commit(&b.tmem_full);
-      if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
+      tc::fence_after_sync();
+      if (lane == 0) {
+        const uint32_t abase = smem_u32(a_ring + st * a_stage_bytes);
+        const uint32_t wcol = tmem + kWCol0 + 64u * st;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
+          tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit(&b.empty[st]);
+      }
+      __syncwarp();
+      if (++st == S) { st = 0; ++lap; }
     }
+    if (!ok && lane == 0) {
+      record_error(kDevErrTimeout);
+      b.abort = 1;
+    }
+    if (lane == 0) tc::commit(&b.tmem_full);
+    __syncwarp();
+    if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
   } else {
     // ---------------- converters ----------------
     const int cw = warp - 2, g = cw >> 2, q4 = warp & 3;
     const int r = 32 * q4 + lane;  // W row in the tile = TMEM lane
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
-    for (int ks = g; ks < nk && ok; ks += 2) {
-      const int j = ks / SUB, sub = ks % SUB, ws = ks % kWStages;
-      if (sub == g &&
-          (!mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+    for (int ks = g; ks < nk; ks += 2) {
+      const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % kRawStages;
+      if (!warp_wait(&b.raw_full[rslot], (j / kRawStages) & 1, p) || b.abort) {
         ok = false;
         break;
       }
-      if (ks >= kWStages &&
-          (!mbar_wait(&b.w_empty[ws], ((ks / kWStages) - 1) & 1, p.wait_ns, p.wait_iters) || b.abort)) {
+      if (ks >= S && (!warp_wait(&b.empty[st], ((ks / S) - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
+      const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
+      const uint32_t tcol = tmem + tlane + kWCol0 + 64u * st;
       uint32_t out[32];
-      convert64_dyn<FMT>(sub, smem_u32(w_ring + (j % kRawStages) * kRawBytes) + 16u * r, out);
-      tc::st_32x32b_x32(tmem + tlane + kWCol0 + 32u * ws, out);
+      convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
+      tc::st_32x32b_x32(tcol, out);
+      convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
+      tc::st_32x32b_x32(tcol + 32u, out);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&b.w_full[ws]);
-        if (sub == SUB - 2 + g) mbar_arrive(&b.raw_empty[j % kRawStages]);
+        mbar_arrive(&b.full[st]);
+        mbar_arrive(&b.raw_empty[rslot]);
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
       b.abort = 1;
     }
     if (g == 0) {
       // ---------------- epilogue ----------------
-      const bool have = mbar_wait(&b.tmem_full, 0, p.wait_ns, p.wait_iters);
+      const bool have = warp_wait(&b.tmem_full, 0, p);
       tc::fence_after_sync();
-      if (!have) {
+      if (!have && lane == 0) {
         record_error(kDevErrTimeout);
         b.abort = 1;
       }
@@ -469,7 +500,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 bool aligned(const void* p, unsigned al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
 
-int kstep_multiple(int fmt) { return fmt == LQ_FMT_F16 ? 128 : 256; }
+int kstep_multiple(int fmt) { return fmt == LQ_FMT_F16 ? 128 : 256; }  // one raw stage
 
 // Token-tile width: enough tiles to put about one CTA on every SM, at most
 // 256 tokens (the MMA's N limit) and at least 16.
@@ -483,20 +514,21 @@ int pick_bt(int64_t M, int64_t N) {
   return static_cast<int>(std::min<int64_t>(256, (per + 15) / 16 * 16));
 }
 
-int raw_slabs(int fmt) { return fmt == LQ_FMT_F16 ? 16 : (fmt == LQ_FMT_Q8_0 ? 17 : 9); }
+int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
 
-// Depth of the A-tile ring that fits next to the raw-W ring.
+// Pipeline depth that fits next to the raw-W ring (A tile of a stage: bt
+// rows x 128 K halves).
 int a_stages_for(int fmt, int bt) {
   const DeviceInfo& di = device_info();
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - 256 -
-                           static_cast<long long>(kRawStages) * raw_slabs(fmt) * kSlabBytes;
-  const long long n = budget / (static_cast<long long>(bt) * 128);
-  return static_cast<int>(std::min<long long>(kAStages, n));
+                           static_cast<long long>(kRawStages) * raw_stage_bytes(fmt);
+  const long long n = budget / (static_cast<long long>(bt) * 256);
+  return static_cast<int>(std::min<long long>(kMaxStages, n));
 }
 
 size_t tma_smem_bytes(int fmt, int bt, int a_stages) {
-  const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 128 +
-                      static_cast<size_t>(kRawStages) * raw_slabs(fmt) * kSlabBytes + sizeof(Bars) + 64;
+  const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 256 +
+                      static_cast<size_t>(kRawStages) * raw_stage_bytes(fmt) + sizeof(Bars) + 64;
   // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
   return std::max<size_t>(need, 116 * 1024);
 }
@@ -505,7 +537,7 @@ template <int FMT>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              const TmaGemmParams& p) {
   auto kern = gemm_tma_kernel<FMT>;
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.a_stages);
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -535,7 +567,7 @@ bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
   if (!encode_fn()) return false;
   const DeviceInfo& di = device_info();
-  return di.cc_major >= 10 && a_stages_for(a.fmt, 256) >= 3;
+  return di.cc_major >= 10 && a_stages_for(a.fmt, 256) >= 2;
 }
 
 // The library's own stream-ordered memory pool on the current device: freed
@@ -593,17 +625,27 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return LQ_ERR_CUDA;
 
-  // 2. tensor maps: raw W as [N][row_bytes/4] 32-bit words, boxes of
-  //    4 words x 128 rows (one 16-byte slab); A16 as [M][K] halves, boxes of
-  //    64 x bt with the 128-byte swizzle of the MMA operand.
+  // 2. tensor maps. Q formats: raw W as [N][row_bytes/4] 32-bit words, one
+  //    box = the bytes of 256 K (68 or 36 words) x 128 rows. f16: W as
+  //    [N][K] halves, boxes of 64 x 128 with the 128-byte swizzle. A16 as
+  //    [M][K] halves, boxes of 64 x bt with the 128-byte swizzle.
   EncodeTiled enc = encode_fn();
   if (!enc) return LQ_ERR_UNSUPPORTED;
   const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
   CUtensorMap tmW, tmA;
-  {
+  if (a.fmt == LQ_FMT_F16) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    cuuint64_t strides[1] = {rb};
+    cuuint32_t box[2] = {64, kBN};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(a.W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  } else {
     cuuint64_t dims[2] = {rb / 4, static_cast<cuuint64_t>(N)};
     cuuint64_t strides[1] = {rb};
-    cuuint32_t box[2] = {4, kBN};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(a.fmt == LQ_FMT_Q8_0 ? 68 : 36), kBN};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a.W), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -627,8 +669,8 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   p.N = N;
   p.K = K;
   p.bt = bt;
-  p.a_stages = a_stages_for(a.fmt, bt);
-  if (p.a_stages < 2) return LQ_ERR_UNSUPPORTED;
+  p.stages = a_stages_for(a.fmt, bt);
+  if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   lq_status st;
