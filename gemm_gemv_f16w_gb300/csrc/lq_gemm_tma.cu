@@ -362,24 +362,41 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
     int st = 0, lap = 0;
-    for (int ks = 0; ks < nk; ++ks) {
-      if (!warp_wait(&b.full[st], lap & 1, p) || b.abort) {
+    auto issue_stage = [&](int ks, int sst) {
+      const uint32_t abase = smem_u32(a_ring + sst * a_stage_bytes);
+      const uint32_t wcol = tmem + kWCol0 + 64u * sst;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
+        tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc::commit(&b.empty[sst]);
+    };
+    for (int ks = 0; ks < nk;) {
+      if (!warp_wait(&b.full[st], lap & 1, p)) {
         ok = false;
         break;
       }
+      // Issue this stage and, without a blocking wait, any following stages
+      // that are already complete (the pipeline usually runs ahead).
+      int cnt = 1;
+      int st2 = st + 1 == S ? 0 : st + 1, lap2 = st + 1 == S ? lap + 1 : lap;
+      while (ks + cnt < nk && cnt < S - 1 && __all_sync(0xffffffffu, mbar_test_wait(&b.full[st2], lap2 & 1))) {
+        ++cnt;
+        if (++st2 == S) { st2 = 0; ++lap2; }
+      }
       tc::fence_after_sync();
       if (lane == 0) {
-        const uint32_t abase = smem_u32(a_ring + st * a_stage_bytes);
-        const uint32_t wcol = tmem + kWCol0 + 64u * st;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
-          tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        int sst = st;
+        for (int i = 0; i < cnt; ++i) {
+          issue_stage(ks + i, sst);
+          if (++sst == S) sst = 0;
         }
-        tc::commit(&b.empty[st]);
       }
       __syncwarp();
-      if (++st == S) { st = 0; ++lap; }
+      ks += cnt;
+      for (int i = 0; i < cnt; ++i)
+        if (++st == S) { st = 0; ++lap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
@@ -438,14 +455,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         for (int c = 0; c < (bt + 31) / 32; ++c) {
           uint32_t v[32];
           tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
+          // lane j holds the scale of token m0 + 32c + j
+          const int ml = m0 + 32 * c + lane;
+          const float sc = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
           tc::wait_ld();
-          if (n < p.N) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int m = m0 + 32 * c + jj;
-              if (32 * c + jj < bt && m < p.M)
-                p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * (__ldg(p.scale + m) * wunscale);
-            }
+          for (int jj = 0; jj < 32; ++jj) {
+            const int m = m0 + 32 * c + jj;
+            const float f = __shfl_sync(0xffffffffu, sc, jj);
+            if (n < p.N && 32 * c + jj < bt && m < p.M)
+              p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * f;
           }
         }
       }
