@@ -616,7 +616,9 @@ lq_status launch_gemv(const MatmulArgs& a) {
   // and room for the next kernel's CTAs to start while this one drains
   // (programmatic dependent launch). Measured on GB300 against one CTA per
   // SM: LM head 4.45 -> 6.57 TB/s, Q8_0 4096x4096 1.79 -> 2.49 TB/s.
-  const GemvPlan pl = plan_gemv(a, 2, kRowsPerStage);
+  GemvPlan pl = plan_gemv(a, 2, kRowsPerStage);
+  // very long rows: half the shared memory cannot hold two stages
+  if (!pl.ok) pl = plan_gemv(a, 1, kRowsPerStage);
   if (!pl.ok) return launch_gemv_generic(a);
   const lq_status st = launch_plan(a, pl);
   if (st == LQ_ERR_UNSUPPORTED) return launch_gemv_generic(a);
