@@ -34,7 +34,7 @@ EXPORTS = [
     "lq_packed_bytes", "lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0",
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
-    "lq_debug_set_wait_limit_ns",
+    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.lq_debug_reset_counts.restype = None
         L.lq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.lq_debug_set_wait_limit_ns.restype = None
+        L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
+        L.lq_gemm_noalloc.restype = st
         _lib = L
     return _lib
 
@@ -139,6 +141,14 @@ def matmul(fmt: str, A, W, N: int, K: int, out=None, kind: str = "matmul", strea
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _call(f"lq_{kind}_{fmt}", A, W, out, M, N, K, stream)
     return out
+
+
+def lq_gemm_noalloc(fmt, A, W, C, M, N, K, stream=None):
+    """Tensor-core GEMM on the library's fixed workspace (no device
+    allocation during the call); see include/lq.h for the limits."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib().lq_gemm_noalloc(f, _ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K),
+                                 _stream(stream)), "lq_gemm_noalloc")
 
 
 # ---- host packers --------------------------------------------------------

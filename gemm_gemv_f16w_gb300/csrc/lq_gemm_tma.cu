@@ -580,6 +580,8 @@ unsigned read_clear_gemm_tma_error() {
   return v;
 }
 
+int pick_gemm_bt(int64_t M, int64_t N) { return pick_bt(M, N); }
+
 bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M < 2 || a.K % kstep_multiple(a.fmt) != 0) return false;
   if (!aligned(a.A, 16) || !aligned(a.W, 16)) return false;

@@ -53,6 +53,7 @@ lq_status launch_gemm_tma(const MatmulArgs& a);
 // the same given a workspace: M*K halves at a16 (16-byte aligned), M floats at scale
 lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt);
 bool gemm_tma_eligible(const MatmulArgs& a);
+int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 
 // Device status words of each translation unit (read-and-clear).
 unsigned read_clear_gemv_error();

@@ -1,0 +1,71 @@
+// lq_gemm_noalloc: the tensor-core GEMM for callers that must not allocate
+// device memory.
+//
+// The regular tensor-core GEMM takes a short-lived workspace (an f16 copy of
+// A and one scale per token) from a stream-ordered memory pool on every call.
+// Some callers cannot allow that: runtimes that own all device memory
+// themselves and give the library none, services whose memory budget is fixed
+// at start-up, and hard real-time paths where an allocation (and the pool
+// growth behind it) is an unacceptable latency or failure point. For them
+// this entry point runs the same two
+// kernels on a workspace that is a fixed array in this library's device
+// memory, allocated once when the library is loaded on a device and held
+// until the process exits.
+#include <mutex>
+
+#include "lq_internal.h"
+
+namespace lq {
+namespace {
+
+// 8 MiB: enough for M*K*2 bytes of f16 activations plus M floats of scales
+// when M*K is at most about 4 million (e.g. 512 x 8192 or 2048 x 2048).
+constexpr size_t kNoAllocBytes = 8u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
+
+std::mutex g_mu;
+void* g_ws_ptr[kMaxDevices];  // device address of g_noalloc_ws, per device
+
+// Device address of the array on the current device. The array's name in
+// host code is only a host-side handle, so the address is looked up once per
+// device (with that device current) and cached.
+lq_status workspace_address(void** out) {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_ws_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_ws) != cudaSuccess || !p) return LQ_ERR_CUDA;
+    g_ws_ptr[dev] = p;
+  }
+  *out = g_ws_ptr[dev];
+  return LQ_OK;
+}
+
+}  // namespace
+}  // namespace lq
+
+using namespace lq;
+
+extern "C" lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, float* C, int64_t M,
+                                     int64_t N, int64_t K, void* stream) {
+  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return LQ_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return LQ_OK;
+  if (!A || !W || !C) return LQ_ERR_INVALID_ARG;
+  if (fmt != LQ_FMT_F16 && K % 32 != 0) return LQ_ERR_INVALID_ARG;
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  // Only the tensor-core kernel that needs the workspace is offered here.
+  if (!gemm_tma_eligible(a)) return LQ_ERR_UNSUPPORTED;
+  // Beyond the fixed workspace: a clear refusal, never a larger allocation.
+  const size_t a16 = (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
+  if (a16 + static_cast<size_t>(M) * 4 > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  const lq_status st = workspace_address(&ws);
+  if (st != LQ_OK) return st;
+  // Every byte the kernels read from the workspace is written earlier in the
+  // same call (the f16 rows and scales of the M tokens), so nothing needs
+  // clearing between calls.
+  auto* base = static_cast<unsigned char*>(ws);
+  return launch_gemm_tma_ws(a, base, reinterpret_cast<float*>(base + a16), pick_gemm_bt(M, N));
+}

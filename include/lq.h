@@ -116,6 +116,28 @@ lq_status lq_pack_f16 (const float* W_host, int64_t N, int64_t K, void* out_host
 lq_status lq_pack_q8_0(const float* W_host, int64_t N, int64_t K, void* out_host);
 lq_status lq_pack_q4_0(const float* W_host, int64_t N, int64_t K, void* out_host);
 
+/* ---- tensor-core GEMM without device allocation ---------------------------
+ * (An addition of this library; the source pages have no counterpart.)
+ * Same result as lq_gemm_<fmt> on its tensor-core route (fmt: LQ_FMT_*), for
+ * callers that must not allocate device memory during the call: runtimes
+ * that own all device memory and hand the library none, services that fix
+ * their memory budget at start-up, real-time paths where an allocation is a
+ * stall or a failure point they cannot accept. Its
+ * workspace is a fixed 8 MiB array inside this library, held on every GPU
+ * that loads the library until the process exits; it needs
+ * round_up(M*K*2, 256) + 4*M bytes, so M*K up to about 4 million elements.
+ *   - LQ_ERR_UNSUPPORTED: larger than the fixed workspace, or a shape or
+ *     alignment the tensor-core kernel does not take (K % 256 for Q8_0/Q4_0,
+ *     K % 128 for f16, A and W 16-byte aligned, M >= 2). Nothing runs.
+ *   - Other argument errors as for lq_gemm_<fmt>.
+ *   - The first call on a device looks up the array's device address (a
+ *     CUDA runtime query); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose executions overlap on the
+ *     GPU (different streams or host threads) race and give wrong
+ *     results; serialise them. Nothing carries over between calls. */
+lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, float* C,
+                          int64_t M, int64_t N, int64_t K, void* stream);
+
 /* ---- status ---------------------------------------------------------- */
 const char* lq_status_string(lq_status s);
 /* Synchronises the current device, then reads and clears its device status
