@@ -19,6 +19,8 @@ except the measured peaks and the committed ncu summaries.
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import math
 import os
@@ -65,15 +67,25 @@ def peaks():
 
 def ncu_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel, from the committed ncu
-    summary of this workload (profiles/<workload>.md, line
-    'traffic_bytes_per_launch: <int>'), or None."""
-    path = os.path.join(ROOT, "profiles", f"{workload}.md")
-    try:
+    summary of this workload (profiles/<kernel>.<workload>.md, line
+    'traffic_bytes_per_launch: <int>'); None when there is no summary or when
+    a kernel source it lists ('source: <path> <sha256 prefix>') has changed
+    since the capture."""
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*.{workload}.md"))):
         with open(path) as f:
-            m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", f.read())
-        return int(m.group(1)) if m else None
-    except OSError:
-        return None
+            text = f.read()
+        m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+        if not m:
+            continue
+        for src, digest in re.findall(r"source:\s*(\S+)\s+([0-9a-f]{16})", text):
+            try:
+                with open(os.path.join(ROOT, src), "rb") as g:
+                    if hashlib.sha256(g.read()).hexdigest()[:16] != digest:
+                        return None
+            except OSError:
+                return None
+        return int(m.group(1))
+    return None
 
 
 class ClockSampler:
