@@ -34,7 +34,7 @@ EXPORTS = [
     "lq_packed_bytes", "lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0",
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
-    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc",
+    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.lq_debug_reset_counts.restype = None
         L.lq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.lq_debug_set_wait_limit_ns.restype = None
+        L.lq_debug_gemv_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        L.lq_debug_gemv_plan.restype = st
         L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
         L.lq_gemm_noalloc.restype = st
         _lib = L
@@ -211,3 +213,9 @@ def reset_counts() -> None:
 
 def set_wait_limit_ns(ns: int) -> None:
     lib().lq_debug_set_wait_limit_ns(int(ns))
+
+
+def gemv_plan(ctas_per_sm: int = 0, rows_per_stage: int = 0, smem_bytes: int = 0) -> None:
+    """Override the decode GEMV's launch plan (0 = automatic); tuning only."""
+    _check(lib().lq_debug_gemv_plan(int(ctas_per_sm), int(rows_per_stage), int(smem_bytes)),
+           "lq_debug_gemv_plan")

@@ -8,23 +8,30 @@
 // stream has to keep ~7 TB/s of HBM busy, so this kernel is built around the
 // copy engine instead:
 //
-//  * one persistent CTA per SM owns a contiguous range of W rows;
+//  * persistent CTAs (one or two per SM) each own a contiguous range of W
+//    rows; a CTA stays within half an SM (<= 112 KB of shared memory, 288
+//    threads of <= 112 registers) so that the next GEMV on the stream can be
+//    resident beside it and start streaming its own weights while this one
+//    finishes (programmatic dependent launch; weights never depend on the
+//    previous kernel, activations and outputs are touched only after it
+//    completed);
 //  * a producer thread moves stages of up to 8 whole rows into a ring of
 //    shared-memory slots, one 1-D bulk copy (cp.async.bulk) per stage, with
 //    mbarrier transaction counts; small copies are slow, so stages are large;
-//  * eight consumer warps each cover a K-slice of every row of a stage, so a
-//    lane holds only its few activations in registers and has eight
-//    independent rows of work per stage;
+//  * eight consumer warps form a grid of K-groups x row-groups: a warp
+//    covers its K-slice of every row of its stages, keeps that slice of A in
+//    registers, and has up to eight independent rows of work per stage;
 //  * dequantisation happens in registers without int->float conversions:
 //    a quantised value is dropped into the mantissa of 2^23 and unbiased with
 //    one exact add/fma; dot products use packed f32x2 fma;
-//  * each warp reduces its eight row partials across lanes with one
-//    transposed shuffle tree; the stage's finisher warp adds the eight warps'
-//    partials in a fixed order and writes C.
+//  * each warp reduces its row partials across lanes with one transposed
+//    shuffle tree; the stage's finisher warp adds the K-groups' partials in a
+//    fixed order and writes C.
 //
 // Every wait is bounded (lq_device.cuh); on timeout the kernel records
 // LQ_ERR_DEVICE_TIMEOUT, its producer drains its own copies and it returns.
 #include <algorithm>
+#include <atomic>
 
 #include "lq_device.cuh"
 #include "lq_internal.h"
@@ -34,12 +41,13 @@ namespace {
 
 __device__ unsigned g_gemv_err;
 
-constexpr int kConsumerWarps = 8;              // each owns a K-slice of every row
+constexpr int kConsumerWarps = 8;              // K-groups x row-groups
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;
 constexpr int kRowsPerStage = 8;               // rows moved by one bulk copy
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 12;
 constexpr int kGemvFastMaxK = 16384;
-constexpr int kHeaderBytes = 5120;             // barriers + reduction buffers
+constexpr int kHalfSmSmem = 112 * 1024;        // two CTAs fit on one SM
+constexpr int64_t kL2PrefetchMaxBytes = 32LL << 20;
 
 struct GemvParams {
   const float* A;
@@ -49,7 +57,10 @@ struct GemvParams {
   int row_bytes;
   int rows_per_stage;        // <= kRowsPerStage
   int stages;                // ring depth
-  int a_bytes;               // K * 4 (a multiple of 16)
+  int nk, nr;                // consumer warp grid: nk K-groups x nr row-groups
+  int a_region;              // bytes of shared memory for A (a multiple of 128)
+  int a_stage;               // bytes of the staging area for A (0 for f16)
+  int l2_prefetch;           // prefetch the rows beyond the first ring-full into L2
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
@@ -58,19 +69,20 @@ struct Header {
   uint64_t full[kMaxStages];       // stage landed (TMA transaction bytes)
   uint64_t empty[kMaxStages];      // every consumer warp is done with the stage
   uint64_t red_full[kMaxStages];   // every consumer warp wrote its row partials
-  uint64_t a_bar;
+  uint64_t a_bar;                  // A landed in the staging area
   volatile int abort;
-  float red[kMaxStages][kConsumerWarps][kRowsPerStage];  // per ring slot
+  float red[kMaxStages][kRowsPerStage][kConsumerWarps];  // [slot][row][K-group]
 };
-static_assert(sizeof(Header) <= kHeaderBytes, "header too large");
+constexpr int kHeaderBytes = (static_cast<int>(sizeof(Header)) + 127) / 128 * 128;
 
 __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_gemv_err, 0u, code); }
 
 // ---------------------------------------------------------------------------
 // Per-format slices. A "chunk" is the part of a row that one warp covers in
 // one pass: 32 lanes x 8 elements (f16, Q8_0) or 32 lanes x 16 elements
-// (Q4_0). Warp w takes chunks w, w+8, w+16, ... of every row; a lane holds
-// the activations of its part of each of its chunks in registers.
+// (Q4_0). The warp of K-group kg (of nk) takes chunks kg, kg+nk, kg+2nk, ...
+// of each of its rows; a lane holds the activations of its part of each of
+// its chunks in registers (read once from global memory).
 // ---------------------------------------------------------------------------
 
 // f16: chunk = 256 halves = 512 bytes; lane l reads bytes [16l, 16l+16).
@@ -79,16 +91,17 @@ struct F16Slice {
   float2 a[CPW][4];
   uint32_t off[CPW];  // byte offset of the lane's 16 bytes within a row
   bool ok[CPW];
-  __device__ __forceinline__ void init(uint32_t As, int warp, int lane, int K) {
+  // sA: the activations in shared memory, in order (a_layout_f16).
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
     const int nch = (K + 255) / 256;
 #pragma unroll
     for (int i = 0; i < CPW; ++i) {
-      const int c = warp + kConsumerWarps * i;
+      const int c = kg + nk * i;
       const int e = 256 * c + 8 * lane;
       ok[i] = c < nch && e < K;
       off[i] = 2u * static_cast<uint32_t>(e);
       if (ok[i]) {
-        const float4 x = lds128f(As + 4u * e), y = lds128f(As + 4u * e + 16u);
+        const float4 x = lds128f(sA + 4u * e), y = lds128f(sA + 4u * e + 16u);
         a[i][0] = make_float2(x.x, x.y);
         a[i][1] = make_float2(x.z, x.w);
         a[i][2] = make_float2(y.x, y.y);
@@ -113,109 +126,110 @@ struct F16Slice {
   }
 };
 
-// Q8_0: chunk = 8 blocks = 272 bytes. Lane l takes block l/4 of the chunk
-// and its 8 values 8*(l%4) .. 8*(l%4)+7 (bytes 2+8*(l%4) .. of the block).
-// Those 8 bytes start 2 bytes past a word boundary for even blocks, so such
-// a lane reads 3 words and realigns them with one byte-permute each.
+// Quantised formats, one whole block per lane. K-group kg covers segments
+// kg/2 + (nk/2)*c (c < CPW; 64 blocks = 2048 values each) and, of them, the
+// blocks of parity kg%2: lane l takes block 64*seg + 2l + parity, so a
+// warp's 32 blocks of a segment are every other block of it. Their activations sit in shared memory
+// at slot (2*seg + parity)*32 + l, 144 bytes apart (a_slot_q): 144 is an odd
+// multiple of 16, so the lanes' 16-byte loads fall in eight different bank
+// groups.
+__host__ __device__ __forceinline__ int a_slot_q(int b) { return (2 * (b >> 6) + (b & 1)) * 32 + ((b & 63) >> 1); }
+constexpr int kASlotBytes = 144;
+
+// Q8_0 (34-byte blocks): the lane's block spans nine 32-bit words starting
+// at word 17l of the segment (+8 for odd blocks, whose scale sits in the
+// upper half of that first word). 17 is odd, so for each of the nine loads
+// the 32 lanes hit 32 different banks: every byte is read once, with no bank
+// conflicts. Even blocks start with their scale, so their quants are 2 bytes
+// past a word boundary and are realigned with one byte-permute per word;
+// odd blocks' quants are word-aligned (the parity is the same for the whole
+// warp, so the two cases are separate loops, not a divergent branch).
 template <int CPW>
 struct Q8Slice {
-  float2 a[CPW][4];
-  uint32_t qoff[CPW], doff[CPW];  // word-aligned byte offsets of quants / scale word
-  uint32_t sel, dshift, w2off;
+  float2 a[CPW][16];       // the blocks' activations
+  uint32_t woff[CPW];      // byte offset of the lane's first word in the row
+  bool odd;                // block parity (warp-uniform)
   bool ok[CPW];
-  __device__ __forceinline__ void init(uint32_t As, int warp, int lane, int K) {
-    const int nb = K / 32;
-    const int bl = lane >> 2, seg = lane & 3;
-    const uint32_t qb = 34u * bl + 2u + 8u * seg;   // byte offset within the chunk
-    sel = (qb & 2u) ? 0x5432u : 0x3210u;
-    w2off = (qb & 2u) ? 8u : 4u;  // aligned lanes re-read word 1: never past the block
-    dshift = (bl & 1) ? 16u : 0u;
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
+    const int par = kg & 1;
+    odd = par != 0;
 #pragma unroll
-    for (int i = 0; i < CPW; ++i) {
-      const int c = warp + kConsumerWarps * i;
-      const int b = 8 * c + bl;
-      ok[i] = b < nb;
-      qoff[i] = 272u * c + (qb & ~3u);
-      doff[i] = 272u * c + ((34u * bl) & ~3u);
-      const int e = 32 * b + 8 * seg;
-      if (ok[i]) {
-        const float4 x = lds128f(As + 4u * e), y = lds128f(As + 4u * e + 16u);
-        a[i][0] = make_float2(x.x, x.y);
-        a[i][1] = make_float2(x.z, x.w);
-        a[i][2] = make_float2(y.x, y.y);
-        a[i][3] = make_float2(y.z, y.w);
-      } else {
+    for (int c = 0; c < CPW; ++c) {
+      const int seg = (kg >> 1) + (nk >> 1) * c;
+      const int b = 64 * seg + 2 * lane + par;
+      ok[c] = b < K / 32;
+      woff[c] = 2176u * seg + 68u * lane + (par ? 32u : 0u);
+      const uint32_t src = sA + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) a[i][t] = make_float2(0.f, 0.f);
+      for (int t = 0; t < 8; ++t) {
+        const float4 x = ok[c] ? lds128f(src + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[c][2 * t] = make_float2(x.x, x.y);
+        a[c][2 * t + 1] = make_float2(x.z, x.w);
       }
     }
   }
-  __device__ __forceinline__ float dot(uint32_t row, int i) const {
-    const uint32_t w0 = lds32(row + qoff[i]), w1 = lds32(row + qoff[i] + 4u),
-                   w2 = lds32(row + qoff[i] + w2off);
-    const uint32_t dw = lds32(row + doff[i]);
-    const uint32_t x0 = __byte_perm(w0, w1, sel) ^ 0x80808080u;
-    const uint32_t x1 = __byte_perm(w1, w2, sel) ^ 0x80808080u;
-    const float d = f16_lo(dw >> dshift);
+  template <bool ODD>
+  __device__ __forceinline__ float dot_par(uint32_t row, int c) const {
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = lds32(row + woff[c] + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
     const float2 mb = make_float2(-kMagicS8, -kMagicS8);
-    const float2 q0 = fadd2(make_float2(s8_to_magic(x0, 0), s8_to_magic(x0, 1)), mb);
-    const float2 q1 = fadd2(make_float2(s8_to_magic(x0, 2), s8_to_magic(x0, 3)), mb);
-    const float2 q2 = fadd2(make_float2(s8_to_magic(x1, 0), s8_to_magic(x1, 1)), mb);
-    const float2 q3 = fadd2(make_float2(s8_to_magic(x1, 2), s8_to_magic(x1, 3)), mb);
-    float2 acc = ffma2(q0, a[i][0], make_float2(0.f, 0.f));
-    float2 acc1 = ffma2(q1, a[i][1], make_float2(0.f, 0.f));
-    acc = ffma2(q2, a[i][2], acc);
-    acc1 = ffma2(q3, a[i][3], acc1);
-    return d * ((acc.x + acc1.x) + (acc.y + acc1.y));
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // q_{4i..4i+3}, sign bits flipped
+      const uint32_t x = (ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u)) ^ 0x80808080u;
+      const float2 q01 = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
+      const float2 q23 = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
+      acc[(2 * i) & 3] = ffma2(q01, a[c][2 * i], acc[(2 * i) & 3]);
+      acc[(2 * i + 1) & 3] = ffma2(q23, a[c][2 * i + 1], acc[(2 * i + 1) & 3]);
+    }
+    const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return d * (s.x + s.y);
+  }
+  __device__ __forceinline__ float dot(uint32_t row, int c) const {
+    return odd ? dot_par<true>(row, c) : dot_par<false>(row, c);
   }
 };
 
-// Q4_0: chunk = 16 blocks = 288 bytes = 512 values. Lane l takes block l/2
-// of the chunk and nibble bytes 8*(l%2) .. 8*(l%2)+7 of it, i.e. values
-// q_{8s+j} (low nibbles) and q_{16+8s+j} (high nibbles), s = l%2, j < 8.
+// Q4_0 (18-byte blocks): the lane's block spans five words starting at word
+// 9l of the segment (+4 for odd blocks); 9 is odd, so again conflict-free.
+// Byte j of the 16 nibble bytes holds q_j (low nibble) and q_{j+16} (high).
 // Taking each word as two half-words of two bytes (B0, B1), the nibble at
 // bit 4p of a half-word is, for p = 0..3: B0.lo, B0.hi, B1.lo, B1.hi. A
 // nibble at bit 4p dropped into the mantissa of 2^23 gives 2^23 + q*16^p; one
 // fma with (16^-p, -(2^(23-4p)+8)) turns that into q - 8 exactly.
 template <int CPW>
 struct Q4Slice {
-  float2 a[CPW][8];  // pair j: (a_{8s+j}, a_{16+8s+j})
-  uint32_t qoff[CPW], doff[CPW];
-  uint32_t sel, dshift, w2off;
+  float2 a[CPW][16];       // pair j: (a_j, a_{16+j})
+  uint32_t woff[CPW];
+  bool odd;
   bool ok[CPW];
-  __device__ __forceinline__ void init(uint32_t As, int warp, int lane, int K) {
-    const int nb = K / 32;
-    const int bl = lane >> 1, hs = lane & 1;
-    const uint32_t qb = 18u * bl + 2u + 8u * hs;
-    sel = (qb & 2u) ? 0x5432u : 0x3210u;
-    w2off = (qb & 2u) ? 8u : 4u;
-    dshift = (bl & 1) ? 16u : 0u;
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
+    const int par = kg & 1;
+    odd = par != 0;
 #pragma unroll
-    for (int i = 0; i < CPW; ++i) {
-      const int c = warp + kConsumerWarps * i;
-      const int b = 16 * c + bl;
-      ok[i] = b < nb;
-      qoff[i] = 288u * c + (qb & ~3u);
-      doff[i] = 288u * c + ((18u * bl) & ~3u);
-      const int e = 32 * b + 8 * hs;
-      if (ok[i]) {
-        const float4 l0 = lds128f(As + 4u * e), l1 = lds128f(As + 4u * e + 16u);
-        const float4 h0 = lds128f(As + 4u * (e + 16)), h1 = lds128f(As + 4u * (e + 16) + 16u);
-        a[i][0] = make_float2(l0.x, h0.x);
-        a[i][1] = make_float2(l0.y, h0.y);
-        a[i][2] = make_float2(l0.z, h0.z);
-        a[i][3] = make_float2(l0.w, h0.w);
-        a[i][4] = make_float2(l1.x, h1.x);
-        a[i][5] = make_float2(l1.y, h1.y);
-        a[i][6] = make_float2(l1.z, h1.z);
-        a[i][7] = make_float2(l1.w, h1.w);
-      } else {
+    for (int c = 0; c < CPW; ++c) {
+      const int seg = (kg >> 1) + (nk >> 1) * c;
+      const int b = 64 * seg + 2 * lane + par;
+      ok[c] = b < K / 32;
+      woff[c] = 1152u * seg + 36u * lane + (par ? 16u : 0u);
+      const uint32_t src = sA + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) a[i][t] = make_float2(0.f, 0.f);
+      for (int t = 0; t < 4; ++t) {
+        const float4 lo = ok[c] ? lds128f(src + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 hi = ok[c] ? lds128f(src + 64u + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[c][4 * t] = make_float2(lo.x, hi.x);
+        a[c][4 * t + 1] = make_float2(lo.y, hi.y);
+        a[c][4 * t + 2] = make_float2(lo.z, hi.z);
+        a[c][4 * t + 3] = make_float2(lo.w, hi.w);
       }
     }
   }
-  // One half-word (bytes j, j+1 of the lane's eight) into two f32x2 sums.
+  // One half-word (bytes j, j+1) into two f32x2 sums.
   __device__ __forceinline__ static void halfword(uint32_t x, float2 a01, float2 a23, float2& acc0,
                                                   float2& acc1) {
     const float2 s01 = make_float2(1.0f, 0.0625f);
@@ -226,23 +240,31 @@ struct Q4Slice {
                              __uint_as_float((x & 0x00F0u) | 0x4B000000u));
     float2 v23 = make_float2(__uint_as_float((x & 0x0F00u) | 0x4B000000u),
                              __uint_as_float((x & 0xF000u) | 0x4B000000u));
-    v01 = ffma2(v01, s01, c01);  // (q_{8s+j} - 8, q_{16+8s+j} - 8)
-    v23 = ffma2(v23, s23, c23);  // (q_{8s+j+1} - 8, q_{16+8s+j+1} - 8)
+    v01 = ffma2(v01, s01, c01);  // (q_j - 8, q_{16+j} - 8)
+    v23 = ffma2(v23, s23, c23);  // (q_{j+1} - 8, q_{17+j} - 8)
     acc0 = ffma2(v01, a01, acc0);
     acc1 = ffma2(v23, a23, acc1);
   }
-  __device__ __forceinline__ float dot(uint32_t row, int i) const {
-    const uint32_t w0 = lds32(row + qoff[i]), w1 = lds32(row + qoff[i] + 4u),
-                   w2 = lds32(row + qoff[i] + w2off);
-    const uint32_t dw = lds32(row + doff[i]);
-    const uint32_t x0 = __byte_perm(w0, w1, sel), x1 = __byte_perm(w1, w2, sel);
-    const float d = f16_lo(dw >> dshift);
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    halfword(x0, a[i][0], a[i][1], acc0, acc1);
-    halfword(x0 >> 16, a[i][2], a[i][3], acc0, acc1);
-    halfword(x1, a[i][4], a[i][5], acc0, acc1);
-    halfword(x1 >> 16, a[i][6], a[i][7], acc0, acc1);
-    return d * ((acc0.x + acc1.x) + (acc0.y + acc1.y));
+  template <bool ODD>
+  __device__ __forceinline__ float dot_par(uint32_t row, int c) const {
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff[c] + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
+      halfword(x, a[c][4 * i], a[c][4 * i + 1], acc[0], acc[1]);
+      halfword(x >> 16, a[c][4 * i + 2], a[c][4 * i + 3], acc[2], acc[3]);
+    }
+    const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return d * (s.x + s.y);
+  }
+  __device__ __forceinline__ float dot(uint32_t row, int c) const {
+    return odd ? dot_par<true>(row, c) : dot_par<false>(row, c);
   }
 };
 
@@ -281,18 +303,23 @@ __device__ __forceinline__ float transpose_reduce8(const float (&acc)[8], int la
 }
 
 // ---------------------------------------------------------------------------
-// The streaming kernel. Ring slot s holds stage st (st % S == s); the full
-// barrier of a slot completes once per stage and every consumer warp waits
-// for every stage in order, so no waiter can mistake an older phase. A slot
-// is released (empty barrier, 8 arrivals) only after the stage's finisher
-// has read the slot's reduction buffer.
+// The streaming kernel. Consumer warp w < nk*nr is K-group kg = w % nk of
+// row-group rg = w / nk; row-group rg takes stages rg, rg + nr, rg + 2nr,
+// ..., all rows of each. Ring slot s holds stage st (st % S == s), and S is
+// a multiple of nr, so each slot serves one row-group only. Its full barrier
+// completes once per stage, and a slot is refilled only after the nk warps
+// of its stage released it (empty barrier, after the stage's finisher read
+// the slot's reduction buffer), so a waiter sees either the phase it waits
+// for or the one before it, never an older one.
 // ---------------------------------------------------------------------------
 template <int FMT, int CPW>
-__global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
+    gemv_stream_kernel(const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Header& hd = *reinterpret_cast<Header*>(smem);
-  float* As = reinterpret_cast<float*>(smem + kHeaderBytes);
-  uint8_t* ring = smem + kHeaderBytes + p.a_bytes;
+  uint8_t* sA = smem + kHeaderBytes;            // A as the slices read it
+  uint8_t* stage_a = sA + p.a_region;           // A as copied (quantised formats)
+  uint8_t* ring = stage_a + p.a_stage;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x;
@@ -300,14 +327,20 @@ __global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_ke
   const int r1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G);
   const int nrows = r1 - r0;
   const int RS = p.rows_per_stage, S = p.stages;
+  const int nk = p.nk, nr = p.nr, active = nk * nr;
   const int nst = (nrows + RS - 1) / RS;
   const uint32_t stage_bytes = static_cast<uint32_t>(RS) * p.row_bytes;
+  // The host plans S as a multiple of nr (see plan_gemv); refuse anything else.
+  if (S % nr != 0 || S > kMaxStages || active > kConsumerWarps) {
+    if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&hd.full[s], 1);
-      mbar_init(&hd.empty[s], kConsumerWarps);
-      mbar_init(&hd.red_full[s], kConsumerWarps);
+      mbar_init(&hd.empty[s], nk);
+      mbar_init(&hd.red_full[s], nk);
     }
     mbar_init(&hd.a_bar, 1);
     hd.abort = 0;
@@ -318,35 +351,46 @@ __global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_ke
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
-    if (lane != 0) return;
     const uint64_t pol = policy_evict_first();
     const uint8_t* wbase = p.W + static_cast<long long>(r0) * p.row_bytes;
-    int issued = 0;
-    bool a_issued = false, ok = true;
-    for (int st = 0; st < nst; ++st) {
+    auto issue = [&](int st) {
       const int s = st % S;
-      if (st >= S) {
-        if (!mbar_wait(&hd.empty[s], ((st / S) - 1) & 1, p.wait_ns, p.wait_iters) || hd.abort) {
-          ok = false;
-          break;
-        }
-      }
       const int rows = min(RS, nrows - st * RS);
       const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
       mbar_arrive_expect_tx(&hd.full[s], bytes);
       bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes,
                wbase + static_cast<long long>(st) * RS * p.row_bytes, bytes, &hd.full[s], pol);
-      ++issued;
-      if (st == 0) {
-        // A may come from the previous kernel on the stream: wait for it only
-        // now, with the first weight stage already on its way.
-        pdl_wait();
-        mbar_arrive_expect_tx(&hd.a_bar, p.a_bytes);
-        bulk_g2s(As, p.A, p.a_bytes, &hd.a_bar, policy_evict_last());
-        a_issued = true;
-      }
+    };
+    // W never depends on the previous kernel: fill the ring at once. The
+    // rows that do not fit in it are prefetched into L2 at the same time, so
+    // that the refills later hit L2 (only when the whole matrix is small next
+    // to L2; otherwise the prefetched lines would not survive).
+    if (lane != 0) return;
+    const int first = min(nst, S);
+    for (int st = 0; st < first; ++st) issue(st);
+    if (p.l2_prefetch && nst > S) {
+      const long long done = static_cast<long long>(S) * RS * p.row_bytes;
+      const long long rest = static_cast<long long>(nrows) * p.row_bytes - done;
+      bulk_prefetch_l2(wbase + done, static_cast<uint32_t>(rest));
     }
-    if (nst == 0) pdl_wait();
+    // A may come from the previous kernel: one bulk copy once that one has
+    // completed (f16 straight into place; quantised formats into the staging
+    // area, which the consumers spread into the block slots).
+    pdl_wait();
+    mbar_arrive_expect_tx(&hd.a_bar, static_cast<uint32_t>(p.K) * 4u);
+    bulk_g2s(FMT == LQ_FMT_F16 ? sA : stage_a, p.A, static_cast<uint32_t>(p.K) * 4u, &hd.a_bar,
+             policy_evict_last());
+    int issued = first;
+    bool ok = true;
+    for (int st = first; st < nst; ++st) {
+      if (st >= S && (!mbar_wait(&hd.empty[st % S], ((st / S) - 1) & 1, p.wait_ns, p.wait_iters) ||
+                      hd.abort)) {
+        ok = false;
+        break;
+      }
+      issue(st);
+      ++issued;
+    }
     if (!ok) {
       record_error(kDevErrTimeout);
       hd.abort = 1;
@@ -354,22 +398,36 @@ __global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_ke
     // Never leave copies in flight: consumers may have given up already.
     for (int st = max(0, issued - S); st < issued; ++st)
       mbar_wait(&hd.full[st % S], (st / S) & 1, kDrainWaitNs);
-    if (a_issued) mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
+    mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
     return;
   }
+  if (warp >= active) return;
 
   // ---------------- consumers ----------------
-  pdl_wait();
+  // A arrives through the producer, which copies it only after the previous
+  // kernel on the stream completed; C is written after that too.
   if (nrows == 0) return;
   if (!mbar_wait(&hd.a_bar, 0, p.wait_ns, p.wait_iters)) {
     record_error(kDevErrTimeout);
     hd.abort = 1;
     return;
   }
+  pdl_wait();  // returns at once: the previous kernel has completed
+  if (FMT != LQ_FMT_F16) {
+    // staging area -> block slots: each warp moves 512 contiguous bytes per
+    // step, and the four blocks they hold land in different bank groups
+    const uint32_t sa = smem_u32(sA), sg = smem_u32(stage_a);
+    for (int q = warp * 32 + lane; q < p.K / 4; q += active * 32) {
+      const uint4 v = lds128(sg + 16u * q);
+      sts128(sa + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes + 16u * (q & 7), v);
+    }
+    named_barrier(1, static_cast<uint32_t>(active) * 32u);
+  }
+  const int kg = warp % nk, rg = warp / nk;
   typename SliceOf<FMT, CPW>::T sl;
-  sl.init(smem_u32(As), warp, lane, p.K);
+  sl.init(smem_u32(sA), kg, nk, lane, p.K);
   const uint32_t ring_u = smem_u32(ring);
-  for (int st = 0; st < nst; ++st) {
+  for (int st = rg; st < nst; st += nr) {
     const int s = st % S;
     const uint32_t ph = (st / S) & 1;
     if (!mbar_wait(&hd.full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
@@ -390,13 +448,13 @@ __global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_ke
           if (r < rows) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, i);
       }
     }
-    int row;
-    const float v = transpose_reduce8(acc, lane, row);
-    if ((lane & 3) == 0) hd.red[s][warp][row] = v;
+    int r;
+    const float v = transpose_reduce8(acc, lane, r);
+    if ((lane & 3) == 0) hd.red[s][r][kg] = v;
     __syncwarp();
     if (lane == 0) mbar_arrive(&hd.red_full[s]);
-    if (warp == st % kConsumerWarps) {
-      // finisher of this stage: the eight warps' partials, in a fixed order
+    if (kg == (st / nr) % nk) {
+      // finisher of this stage: the K-groups' partials, in a fixed order
       if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
         record_error(kDevErrTimeout);
         hd.abort = 1;
@@ -404,8 +462,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW >= 4 ? 1 : 2) gemv_stream_ke
       }
       if (lane < rows) {
         float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) sum += hd.red[s][w][lane];
+        for (int g = 0; g < nk; ++g) sum += hd.red[s][lane][g];
         p.C[r0 + st * RS + lane] = sum;
       }
       __syncwarp();
@@ -486,14 +543,34 @@ cudaError_t launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, c
 
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Chunks per warp (template set 1, 2, 4, 8) that cover K for this format.
-int pick_cpw(int fmt, int K) {
-  const int chunk = fmt == LQ_FMT_Q4_0 ? 512 : 256;
-  const int nch = (K + chunk - 1) / chunk;
-  const int need = (nch + kConsumerWarps - 1) / kConsumerWarps;
-  for (int c : {1, 2, 4, 8})
-    if (c >= need) return c;
-  return 0;
+// Consumer warp grid for this format and K: nk K-groups x nr row-groups
+// (nk * nr <= 8) and cpw chunks per warp. f16: chunks of 256 values, nk a
+// power of two up to 8, cpw 1, 2, 4 or 8. Q8_0 / Q4_0: two K-groups (even and
+// odd blocks) per segment of 64 blocks, up to four segments at a time, cpw
+// 1 or 2.
+struct WarpGrid {
+  int nk = 0, nr = 0, cpw = 0;
+};
+WarpGrid pick_grid(int fmt, int K) {
+  WarpGrid g;
+  if (fmt == LQ_FMT_F16) {
+    const int nch = (K + 255) / 256;
+    g.nk = 1;
+    while (g.nk < nch && g.nk < kConsumerWarps) g.nk *= 2;
+    const int need = (nch + g.nk - 1) / g.nk;
+    for (int c : {1, 2, 4, 8})
+      if (c >= need) {
+        g.cpw = c;
+        break;
+      }
+  } else {
+    const int nseg = (K / 32 + 63) / 64;
+    g.nk = 2 * std::min(nseg, kConsumerWarps / 2);
+    const int need = (nseg + g.nk / 2 - 1) / (g.nk / 2);
+    g.cpw = need <= 1 ? 1 : (need <= 2 ? 2 : 0);
+  }
+  g.nr = g.cpw ? kConsumerWarps / g.nk : 0;
+  return g;
 }
 
 template <int FMT, int CPW>
@@ -515,12 +592,17 @@ lq_status launch_stream_t(const MatmulArgs& a, const GemvParams& p, int G, size_
 
 template <int FMT>
 lq_status launch_stream_fmt(const MatmulArgs& a, int cpw, const GemvParams& p, int G, size_t smem) {
-  switch (cpw) {
-    case 1: return launch_stream_t<FMT, 1>(a, p, G, smem);
-    case 2: return launch_stream_t<FMT, 2>(a, p, G, smem);
-    case 4: return launch_stream_t<FMT, 4>(a, p, G, smem);
-    case 8: return launch_stream_t<FMT, 8>(a, p, G, smem);
-    default: return LQ_ERR_UNSUPPORTED;
+  if constexpr (FMT != LQ_FMT_F16) {
+    return cpw == 1 ? launch_stream_t<FMT, 1>(a, p, G, smem)
+                    : (cpw == 2 ? launch_stream_t<FMT, 2>(a, p, G, smem) : LQ_ERR_UNSUPPORTED);
+  } else {
+    switch (cpw) {
+      case 1: return launch_stream_t<FMT, 1>(a, p, G, smem);
+      case 2: return launch_stream_t<FMT, 2>(a, p, G, smem);
+      case 4: return launch_stream_t<FMT, 4>(a, p, G, smem);
+      case 8: return launch_stream_t<FMT, 8>(a, p, G, smem);
+      default: return LQ_ERR_UNSUPPORTED;
+    }
   }
 }
 
@@ -551,7 +633,10 @@ lq_status launch_gemv_generic(const MatmulArgs& a) {
   return cuda_status(e);
 }
 
-// Launch plan of the streaming kernel: grid, ring geometry and shared memory.
+namespace {
+
+// Launch plan of the streaming kernel: grid, warp grid, ring geometry and
+// shared memory.
 struct GemvPlan {
   GemvParams p;
   int grid = 0, cpw = 0;
@@ -559,33 +644,56 @@ struct GemvPlan {
   bool ok = false;
 };
 
-// `ctas_per_sm` CTAs share an SM (each gets 1/ctas_per_sm of the usable
-// shared memory); stages hold up to `max_rows` rows.
-GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows) {
+// `ctas_per_sm` CTAs per SM, each with at most `smem_cap` bytes of shared
+// memory; stages hold up to `max_rows` rows.
+GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_cap) {
   GemvPlan pl;
   const int K = static_cast<int>(a.K);
   const int rb = static_cast<int>(row_bytes(a.fmt, a.K));
-  // Fast path: every stage start and A are 16-byte aligned for the bulk
-  // copies (rows a multiple of 16 bytes), and the per-lane slices cover K.
+  // Fast path: every stage start is 16-byte aligned for the bulk copies
+  // (rows a multiple of 16 bytes), A is 16-byte aligned for vector loads,
+  // and the per-lane slices cover K.
   const bool shape_ok = a.K <= kGemvFastMaxK &&
                         (a.fmt == LQ_FMT_F16 ? (K % 8 == 0) : (K % 256 == 0)) && a.N < (1LL << 30);
   const bool align_ok = aligned(a.W, 16) && aligned(a.A, 16);
-  pl.cpw = shape_ok ? pick_cpw(a.fmt, K) : 0;
-  if (!shape_ok || !align_ok || pl.cpw == 0) return pl;
+  if (!shape_ok || !align_ok) return pl;
+  const WarpGrid wg = pick_grid(a.fmt, K);
+  if (wg.cpw == 0) return pl;
 
   const DeviceInfo& di = device_info();
   const int G = static_cast<int>(std::min<int64_t>(a.N, static_cast<int64_t>(di.sm_count) * ctas_per_sm));
-  const int a_bytes = K * 4;  // a multiple of 16 on this path
-  const int per_cta = std::min(di.max_smem_optin, (226 * 1024) / ctas_per_sm - 1024);
-  const int budget = per_cta - kHeaderBytes - a_bytes;
+  const int per_cta = std::min(di.max_smem_optin, smem_cap);
+  // A in shared memory: in order for f16; for the quantised formats one
+  // 144-byte slot per block, two parities x 32 slots per 64-block segment.
+  const int a_bytes = a.fmt == LQ_FMT_F16 ? K * 4 : ((K / 32 + 63) / 64) * 64 * kASlotBytes;
+  const int a_region = (a_bytes + 127) / 128 * 128;
+  const int a_stage = a.fmt == LQ_FMT_F16 ? 0 : (K * 4 + 127) / 128 * 128;
+  const int budget = per_cta - kHeaderBytes - a_region - a_stage;
   const int rows_per_cta = static_cast<int>((a.N + G - 1) / G);
+  if (G < 1 || budget < 2 * rb) return pl;
   // up to max_rows rows per bulk copy, and room for at least two stages
-  const int rs = std::min({max_rows, kRowsPerStage, std::max(1, budget / (2 * rb)),
-                           std::max(1, rows_per_cta)});
+  const int rs_max = std::max(1, std::min({max_rows, kRowsPerStage, budget / (2 * rb), rows_per_cta}));
+  int stages = std::min({kMaxStages, budget / (rs_max * rb), std::max((rows_per_cta + rs_max - 1) / rs_max, 2)});
+  if (stages < 2) return pl;
+  // Row-groups take whole stages, and every ring slot must serve a single
+  // row-group (stage st goes to slot st % S and to row-group st % nr): with
+  // S a multiple of nr the warps of a slot see each of its phases in turn.
+  // Otherwise a warp could wait on a slot whose previous use belonged to
+  // another row-group, and with copies landing out of order the parity of
+  // an older phase would satisfy its wait.
+  // Prefer all eight warps; give up row-groups rather than drop below
+  // three stages in flight.
+  const int need_max = (rows_per_cta + rs_max - 1) / rs_max;
+  int nr = std::max(1, std::min({wg.nr, need_max, stages}));
+  while (nr > 1 && stages - stages % nr < std::min(3, stages)) --nr;
+  // Even out the row-groups: a multiple of nr stages, rows spread over them.
+  const int total = nr * ((need_max + nr - 1) / nr);
+  const int rs = std::max(1, (rows_per_cta + total - 1) / total);
   const int stage_bytes = rs * rb;
   const int need_stages = (rows_per_cta + rs - 1) / rs;
-  const int stages = std::min({kMaxStages, budget / std::max(stage_bytes, 1), std::max(need_stages, 2)});
-  if (G < 1 || budget <= 0 || stages < 2) return pl;
+  stages = std::min({kMaxStages, budget / stage_bytes, std::max(need_stages, 2)});
+  const int ring = stages - stages % nr;
+  if (ring < 1) return pl;
 
   GemvParams& p = pl.p;
   p.A = a.A;
@@ -595,12 +703,18 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows) {
   p.K = K;
   p.row_bytes = rb;
   p.rows_per_stage = rs;
-  p.stages = stages;
-  p.a_bytes = a_bytes;
+  p.stages = ring;
+  p.nk = wg.nk;
+  p.nr = nr;
+  p.a_region = a_region;
+  p.a_stage = a_stage;
+  // L2 keeps a whole weight matrix of up to a quarter of its size
+  p.l2_prefetch = static_cast<int64_t>(a.N) * rb <= kL2PrefetchMaxBytes ? 1 : 0;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
+  pl.cpw = wg.cpw;
   pl.grid = G;
-  pl.smem = kHeaderBytes + a_bytes + static_cast<size_t>(stages) * stage_bytes;
+  pl.smem = kHeaderBytes + a_region + a_stage + static_cast<size_t>(ring) * stage_bytes;
   pl.ok = true;
   return pl;
 }
@@ -611,14 +725,36 @@ lq_status launch_plan(const MatmulArgs& a, const GemvPlan& pl) {
   return launch_stream_fmt<LQ_FMT_Q4_0>(a, pl.cpw, pl.p, pl.grid, pl.smem);
 }
 
+std::atomic<int> g_tune_ctas{0}, g_tune_rows{0}, g_tune_smem{0};
+
+}  // namespace
+
+void set_gemv_tuning(int ctas_per_sm, int rows_per_stage, int smem_cap) {
+  g_tune_ctas.store(ctas_per_sm);
+  g_tune_rows.store(rows_per_stage);
+  g_tune_smem.store(smem_cap);
+}
+
 lq_status launch_gemv(const MatmulArgs& a) {
-  // Two CTAs per SM: twice the warps to hide shared-memory and ALU latency,
-  // and room for the next kernel's CTAs to start while this one drains
-  // (programmatic dependent launch). Measured on GB300 against one CTA per
-  // SM: LM head 4.45 -> 6.57 TB/s, Q8_0 4096x4096 1.79 -> 2.49 TB/s.
-  GemvPlan pl = plan_gemv(a, 2, kRowsPerStage);
-  // very long rows: half the shared memory cannot hold two stages
-  if (!pl.ok) pl = plan_gemv(a, 1, kRowsPerStage);
+  const WarpGrid wg = pick_grid(a.fmt, static_cast<int>(std::min<int64_t>(a.K, kGemvFastMaxK)));
+  const DeviceInfo& di = device_info();
+  // Kernels with one or two chunks per warp fit in half an SM (registers
+  // and shared memory): two CTAs per SM, each streaming its own rows, give
+  // the SM sixteen consumer warps and twice the bytes in flight (measured
+  // faster than one CTA per SM that leaves room for the next kernel). With
+  // fewer rows than that, one CTA per SM.
+  int ctas = 1, smem_cap = di.max_smem_optin;
+  if (wg.cpw <= 2) {
+    smem_cap = kHalfSmSmem;
+    ctas = a.N >= 2LL * kRowsPerStage * std::max(di.sm_count, 1) ? 2 : 1;
+  }
+  int rows = kRowsPerStage;
+  if (const int c = g_tune_ctas.load()) ctas = c;
+  if (const int r = g_tune_rows.load()) rows = r;
+  if (const int m = g_tune_smem.load()) smem_cap = m;
+  GemvPlan pl = plan_gemv(a, ctas, rows, smem_cap);
+  // very long rows: two stages need more than half an SM
+  if (!pl.ok) pl = plan_gemv(a, 1, kRowsPerStage, di.max_smem_optin);
   if (!pl.ok) return launch_gemv_generic(a);
   const lq_status st = launch_plan(a, pl);
   if (st == LQ_ERR_UNSUPPORTED) return launch_gemv_generic(a);

@@ -45,6 +45,9 @@ inline int64_t row_bytes(int fmt, int64_t K) {
 // checked by the C-ABI layer).
 lq_status launch_gemv(const MatmulArgs& a);            // M == 1, picks fast or generic
 lq_status launch_gemv_generic(const MatmulArgs& a);    // any M, K, alignment
+// GEMV launch-plan override (0 = automatic): CTAs per SM, rows per stage,
+// shared memory per CTA.
+void set_gemv_tuning(int ctas_per_sm, int rows_per_stage, int smem_cap);
 lq_status launch_gemm_stream(const MatmulArgs& a);     // CUDA-core, small M
 lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via shared memory
 bool gemm_tc_eligible(const MatmulArgs& a);

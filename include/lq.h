@@ -160,6 +160,11 @@ void      lq_debug_reset_counts(void);
  * ns/1000 polls (at least one), which exercises the LQ_ERR_DEVICE_TIMEOUT
  * path deterministically without any real hang. */
 void      lq_debug_set_wait_limit_ns(uint64_t ns);
+/* Overrides the decode GEMV's launch plan (0 = automatic for each field):
+ * CTAs per SM (1 or 2), rows per bulk-copy stage (1..8), shared memory per
+ * CTA in bytes. For tuning sweeps; results do not change. Returns
+ * LQ_ERR_INVALID_ARG for values out of range. */
+lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes);
 
 #ifdef __cplusplus
 }
