@@ -34,7 +34,7 @@ EXPORTS = [
     "lq_packed_bytes", "lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0",
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
-    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan",
+    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
         L.lq_debug_reset_counts.restype = None
         L.lq_debug_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
         L.lq_debug_set_wait_limit_ns.restype = None
+        L.lq_gemv_chain.argtypes = [st, ctypes.POINTER(GemvProblem), ctypes.c_int, vp]
+        L.lq_gemv_chain.restype = st
         L.lq_debug_gemv_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.lq_debug_gemv_plan.restype = st
         L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
@@ -143,6 +145,32 @@ def matmul(fmt: str, A, W, N: int, K: int, out=None, kind: str = "matmul", strea
         out = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _call(f"lq_{kind}_{fmt}", A, W, out, M, N, K, stream)
     return out
+
+
+class GemvProblem(ctypes.Structure):
+    """One problem of lq_gemv_chain (the lq_gemv_problem struct of lq.h)."""
+    _fields_ = [("A", ctypes.c_void_p), ("W", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("after", ctypes.c_int32)]
+
+
+def gemv_problems(items):
+    """ctypes array of lq_gemv_problem from (A, W, C, N, K, after) tuples."""
+    arr = (GemvProblem * len(items))()
+    for i, (A, W, C, N, K, after) in enumerate(items):
+        arr[i] = GemvProblem(_ptr(A), _ptr(W), _ptr(C), int(N), int(K), int(after))
+    return arr
+
+
+def lq_gemv_chain(fmt, problems, stream=None) -> int:
+    """Runs lq_gemv_chain on a ctypes array from gemv_problems (or a list of
+    tuples); returns the lq_status (LQ_ERR_UNSUPPORTED is not an exception:
+    the caller falls back to one lq_gemv_<fmt> per problem)."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    arr = problems if isinstance(problems, ctypes.Array) else gemv_problems(problems)
+    st = lib().lq_gemv_chain(f, arr, len(arr), _stream(stream))
+    if st not in (LQ_OK, LQ_ERR_UNSUPPORTED):
+        _check(st, "lq_gemv_chain")
+    return st
 
 
 def lq_gemm_noalloc(fmt, A, W, C, M, N, K, stream=None):

@@ -16,7 +16,7 @@ namespace lq {
 
 namespace {
 std::atomic<int> g_force_route{0};
-std::atomic<uint64_t> g_route_count[4];
+std::atomic<uint64_t> g_route_count[5];
 std::atomic<unsigned long long> g_wait_ns{0};
 std::mutex g_info_mu;
 DeviceInfo g_info[kMaxDevices];
@@ -59,7 +59,7 @@ unsigned wait_limit_iters() {
 }
 
 void count_route(int route) {
-  if (route >= 0 && route < 4) g_route_count[route].fetch_add(1);
+  if (route >= 0 && route < 5) g_route_count[route].fetch_add(1);
 }
 
 namespace {
@@ -181,9 +181,22 @@ lq_status lq_last_device_error(void) {
   const unsigned a = read_clear_gemv_error();
   const unsigned b = read_clear_gemm_error();
   const unsigned c = read_clear_gemm_tma_error();
-  const unsigned v = a ? a : (b ? b : c);
+  const unsigned d = read_clear_chain_error();
+  const unsigned v = a ? a : (b ? b : (c ? c : d));
   if (v == 0) return LQ_OK;
   return static_cast<lq_status>(v);
+}
+
+lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, void* stream) {
+  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (!problems || count < 1) return LQ_ERR_INVALID_ARG;
+  for (int j = 0; j < count; ++j) {
+    const lq_gemv_problem& q = problems[j];
+    if (q.N < 0 || q.K < 1) return LQ_ERR_INVALID_ARG;
+    if (fmt != LQ_FMT_F16 && q.K % 32 != 0) return LQ_ERR_INVALID_ARG;
+    if (!q.A || !q.W || !q.C) return LQ_ERR_INVALID_ARG;
+  }
+  return lq::launch_gemv_chain(fmt, problems, count, static_cast<cudaStream_t>(stream));
 }
 
 const char* lq_version(void) { return "lq 0.1.0 (sm_103a)"; }
@@ -194,7 +207,7 @@ lq_status lq_debug_force_route(int route) {
   return LQ_OK;
 }
 uint64_t lq_debug_route_count(int route) {
-  if (route < 0 || route > 3) return 0;
+  if (route < 0 || route > 4) return 0;
   return g_route_count[route].load();
 }
 void lq_debug_reset_counts(void) {

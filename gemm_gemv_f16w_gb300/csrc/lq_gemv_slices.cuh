@@ -1,0 +1,237 @@
+// Per-format GEMV slices and the warp reduction, shared by the streaming
+// GEMV (lq_gemv.cu) and the persistent chain engine (lq_gemv_chain.cu).
+#pragma once
+
+#include "lq.h"
+#include "lq_device.cuh"
+
+namespace lq {
+namespace gemv {
+
+// ---------------------------------------------------------------------------
+// Per-format slices. A "chunk" is the part of a row that one warp covers in
+// one pass: 32 lanes x 8 elements (f16, Q8_0) or 32 lanes x 16 elements
+// (Q4_0). The warp of K-group kg (of nk) takes chunks kg, kg+nk, kg+2nk, ...
+// of each of its rows; a lane holds the activations of its part of each of
+// its chunks in registers (read once from global memory).
+// ---------------------------------------------------------------------------
+
+// f16: chunk = 256 halves = 512 bytes; lane l reads bytes [16l, 16l+16).
+template <int CPW>
+struct F16Slice {
+  float2 a[CPW][4];
+  uint32_t off[CPW];  // byte offset of the lane's 16 bytes within a row
+  bool ok[CPW];
+  // sA: the activations in shared memory, in order (a_layout_f16).
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
+    const int nch = (K + 255) / 256;
+#pragma unroll
+    for (int i = 0; i < CPW; ++i) {
+      const int c = kg + nk * i;
+      const int e = 256 * c + 8 * lane;
+      ok[i] = c < nch && e < K;
+      off[i] = 2u * static_cast<uint32_t>(e);
+      if (ok[i]) {
+        const float4 x = lds128f(sA + 4u * e), y = lds128f(sA + 4u * e + 16u);
+        a[i][0] = make_float2(x.x, x.y);
+        a[i][1] = make_float2(x.z, x.w);
+        a[i][2] = make_float2(y.x, y.y);
+        a[i][3] = make_float2(y.z, y.w);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) a[i][t] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+  __device__ __forceinline__ float dot(uint32_t row, int i) const {
+    const uint4 v = lds128(row + off[i]);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+    const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+    const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+    float2 acc = ffma2(f0, a[i][0], make_float2(0.f, 0.f));
+    float2 acc1 = ffma2(f1, a[i][1], make_float2(0.f, 0.f));
+    acc = ffma2(f2, a[i][2], acc);
+    acc1 = ffma2(f3, a[i][3], acc1);
+    return (acc.x + acc1.x) + (acc.y + acc1.y);
+  }
+};
+
+// Quantised formats, one whole block per lane. K-group kg covers segments
+// kg/2 + (nk/2)*c (c < CPW; 64 blocks = 2048 values each) and, of them, the
+// blocks of parity kg%2: lane l takes block 64*seg + 2l + parity, so a
+// warp's 32 blocks of a segment are every other block of it. Their activations sit in shared memory
+// at slot (2*seg + parity)*32 + l, 144 bytes apart (a_slot_q): 144 is an odd
+// multiple of 16, so the lanes' 16-byte loads fall in eight different bank
+// groups.
+__host__ __device__ __forceinline__ int a_slot_q(int b) { return (2 * (b >> 6) + (b & 1)) * 32 + ((b & 63) >> 1); }
+constexpr int kASlotBytes = 144;
+
+// Q8_0 (34-byte blocks): the lane's block spans nine 32-bit words starting
+// at word 17l of the segment (+8 for odd blocks, whose scale sits in the
+// upper half of that first word). 17 is odd, so for each of the nine loads
+// the 32 lanes hit 32 different banks: every byte is read once, with no bank
+// conflicts. Even blocks start with their scale, so their quants are 2 bytes
+// past a word boundary and are realigned with one byte-permute per word;
+// odd blocks' quants are word-aligned (the parity is the same for the whole
+// warp, so the two cases are separate loops, not a divergent branch).
+template <int CPW>
+struct Q8Slice {
+  float2 a[CPW][16];       // the blocks' activations
+  uint32_t woff[CPW];      // byte offset of the lane's first word in the row
+  bool odd;                // block parity (warp-uniform)
+  bool ok[CPW];
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
+    const int par = kg & 1;
+    odd = par != 0;
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) {
+      const int seg = (kg >> 1) + (nk >> 1) * c;
+      const int b = 64 * seg + 2 * lane + par;
+      ok[c] = b < K / 32;
+      woff[c] = 2176u * seg + 68u * lane + (par ? 32u : 0u);
+      const uint32_t src = sA + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float4 x = ok[c] ? lds128f(src + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[c][2 * t] = make_float2(x.x, x.y);
+        a[c][2 * t + 1] = make_float2(x.z, x.w);
+      }
+    }
+  }
+  template <bool ODD>
+  __device__ __forceinline__ float dot_par(uint32_t row, int c) const {
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = lds32(row + woff[c] + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    const float2 mb = make_float2(-kMagicS8, -kMagicS8);
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // q_{4i..4i+3}, sign bits flipped
+      const uint32_t x = (ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u)) ^ 0x80808080u;
+      const float2 q01 = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
+      const float2 q23 = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
+      acc[(2 * i) & 3] = ffma2(q01, a[c][2 * i], acc[(2 * i) & 3]);
+      acc[(2 * i + 1) & 3] = ffma2(q23, a[c][2 * i + 1], acc[(2 * i + 1) & 3]);
+    }
+    const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return d * (s.x + s.y);
+  }
+  __device__ __forceinline__ float dot(uint32_t row, int c) const {
+    return odd ? dot_par<true>(row, c) : dot_par<false>(row, c);
+  }
+};
+
+// Q4_0 (18-byte blocks): the lane's block spans five words starting at word
+// 9l of the segment (+4 for odd blocks); 9 is odd, so again conflict-free.
+// Byte j of the 16 nibble bytes holds q_j (low nibble) and q_{j+16} (high).
+// Taking each word as two half-words of two bytes (B0, B1), the nibble at
+// bit 4p of a half-word is, for p = 0..3: B0.lo, B0.hi, B1.lo, B1.hi. A
+// nibble at bit 4p dropped into the mantissa of 2^23 gives 2^23 + q*16^p; one
+// fma with (16^-p, -(2^(23-4p)+8)) turns that into q - 8 exactly.
+template <int CPW>
+struct Q4Slice {
+  float2 a[CPW][16];       // pair j: (a_j, a_{16+j})
+  uint32_t woff[CPW];
+  bool odd;
+  bool ok[CPW];
+  __device__ __forceinline__ void init(uint32_t sA, int kg, int nk, int lane, int K) {
+    const int par = kg & 1;
+    odd = par != 0;
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) {
+      const int seg = (kg >> 1) + (nk >> 1) * c;
+      const int b = 64 * seg + 2 * lane + par;
+      ok[c] = b < K / 32;
+      woff[c] = 1152u * seg + 36u * lane + (par ? 16u : 0u);
+      const uint32_t src = sA + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float4 lo = ok[c] ? lds128f(src + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 hi = ok[c] ? lds128f(src + 64u + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[c][4 * t] = make_float2(lo.x, hi.x);
+        a[c][4 * t + 1] = make_float2(lo.y, hi.y);
+        a[c][4 * t + 2] = make_float2(lo.z, hi.z);
+        a[c][4 * t + 3] = make_float2(lo.w, hi.w);
+      }
+    }
+  }
+  // One half-word (bytes j, j+1) into two f32x2 sums.
+  __device__ __forceinline__ static void halfword(uint32_t x, float2 a01, float2 a23, float2& acc0,
+                                                  float2& acc1) {
+    const float2 s01 = make_float2(1.0f, 0.0625f);
+    const float2 c01 = make_float2(-8388616.0f, -524296.0f);
+    const float2 s23 = make_float2(0.00390625f, 0.000244140625f);
+    const float2 c23 = make_float2(-32776.0f, -2056.0f);
+    float2 v01 = make_float2(__uint_as_float((x & 0x000Fu) | 0x4B000000u),
+                             __uint_as_float((x & 0x00F0u) | 0x4B000000u));
+    float2 v23 = make_float2(__uint_as_float((x & 0x0F00u) | 0x4B000000u),
+                             __uint_as_float((x & 0xF000u) | 0x4B000000u));
+    v01 = ffma2(v01, s01, c01);  // (q_j - 8, q_{16+j} - 8)
+    v23 = ffma2(v23, s23, c23);  // (q_{j+1} - 8, q_{17+j} - 8)
+    acc0 = ffma2(v01, a01, acc0);
+    acc1 = ffma2(v23, a23, acc1);
+  }
+  template <bool ODD>
+  __device__ __forceinline__ float dot_par(uint32_t row, int c) const {
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff[c] + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    float2 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
+      halfword(x, a[c][4 * i], a[c][4 * i + 1], acc[0], acc[1]);
+      halfword(x >> 16, a[c][4 * i + 2], a[c][4 * i + 3], acc[2], acc[3]);
+    }
+    const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    return d * (s.x + s.y);
+  }
+  __device__ __forceinline__ float dot(uint32_t row, int c) const {
+    return odd ? dot_par<true>(row, c) : dot_par<false>(row, c);
+  }
+};
+
+template <int FMT, int CPW>
+struct SliceOf;
+template <int CPW> struct SliceOf<LQ_FMT_F16, CPW> { using T = F16Slice<CPW>; };
+template <int CPW> struct SliceOf<LQ_FMT_Q8_0, CPW> { using T = Q8Slice<CPW>; };
+template <int CPW> struct SliceOf<LQ_FMT_Q4_0, CPW> { using T = Q4Slice<CPW>; };
+
+// Sums acc[0..7] over the 32 lanes with 9 shuffles: after the three halving
+// steps lane l holds row ((l>>4)&1)*4 + ((l>>3)&1)*2 + ((l>>2)&1) summed over
+// 8 lanes, and the last two steps finish the sum. Returns the value; `row`
+// receives the row it belongs to.
+__device__ __forceinline__ float transpose_reduce8(const float (&acc)[8], int lane, int& row) {
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float v4[4], v2[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = b4 ? acc[i] : acc[i + 4];
+    const float keep = b4 ? acc[i + 4] : acc[i];
+    v4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = b3 ? v4[i] : v4[i + 2];
+    const float keep = b3 ? v4[i + 2] : v4[i];
+    v2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  const float send = b2 ? v2[0] : v2[1];
+  const float keep = b2 ? v2[1] : v2[0];
+  float v = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  row = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
+  return v;
+}
+
+}  // namespace gemv
+}  // namespace lq

@@ -58,10 +58,15 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
 bool gemm_tma_eligible(const MatmulArgs& a);
 int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 
+// Decode chain (lq_gemv_chain); LQ_ERR_UNSUPPORTED when the problems do not
+// fit its fast path.
+lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, cudaStream_t stream);
+
 // Device status words of each translation unit (read-and-clear).
 unsigned read_clear_gemv_error();
 unsigned read_clear_gemm_error();
 unsigned read_clear_gemm_tma_error();
+unsigned read_clear_chain_error();
 
 lq_status cuda_status(cudaError_t e);
 

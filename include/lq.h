@@ -116,6 +116,33 @@ lq_status lq_pack_f16 (const float* W_host, int64_t N, int64_t K, void* out_host
 lq_status lq_pack_q8_0(const float* W_host, int64_t N, int64_t K, void* out_host);
 lq_status lq_pack_q4_0(const float* W_host, int64_t N, int64_t K, void* out_host);
 
+/* ---- decode chain: many M = 1 GEMVs in one launch ------------------------
+ * (An addition of this library for the decode step the source pages run as
+ * a sequence of gemv_decode_m1 / gemv_q8_decode / gemv_q4_decode
+ * dispatches, one per projection; the pages have no such engine.)
+ * Computes, for j = 0 .. count-1 in order, C_j[n] = sum_k A_j[k] w_j(n, k)
+ * with every W_j in format `fmt`; W_j, A_j, C_j are device pointers laid
+ * out as for lq_gemv_<fmt> (M = 1). If problems[j].after is non-zero,
+ * problem j reads A_j only after problems 0 .. j-1 are complete, so A_j may
+ * be (or depend on) an earlier C; otherwise A_j must not be written by this
+ * call. Weights are streamed ahead of the computation in every case. One
+ * cooperative launch of one CTA per SM; the problems array is read during
+ * the call (host memory, caller-owned).
+ *   - count in 1..64; N_j >= 0; K_j in 1..16384 with K_j % 8 == 0 (f16) or
+ *     K_j % 256 == 0 (quantised); A_j and W_j 16-byte aligned. Anything else
+ *     returns LQ_ERR_UNSUPPORTED without launching (use lq_gemv_<fmt>).
+ *   - Device-side waits are bounded; lq_last_device_error reports a
+ *     timeout. At most 64 calls may be in flight at once across streams. */
+typedef struct {
+  const float* A;
+  const void*  W;
+  float*       C;
+  int64_t      N;
+  int64_t      K;
+  int32_t      after;
+} lq_gemv_problem;
+lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, void* stream);
+
 /* ---- tensor-core GEMM without device allocation ---------------------------
  * (An addition of this library; the source pages have no counterpart.)
  * Same result as lq_gemm_<fmt> on its tensor-core route (fmt: LQ_FMT_*), for
@@ -151,7 +178,7 @@ const char* lq_version(void);
  * route: 0 = automatic, 1 = CUDA-core streaming GEMM (any M),
  *        2 = tensor-core GEMM, 3 = generic fallback kernels (any shape).
  * lq_debug_route_count(r) counts launches taken by route r (r = 0 counts
- * the fast GEMV); counters are process-wide. */
+ * the fast GEMV, r = 4 the decode chain); counters are process-wide. */
 lq_status lq_debug_force_route(int route);
 uint64_t  lq_debug_route_count(int route);
 void      lq_debug_reset_counts(void);

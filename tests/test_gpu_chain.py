@@ -1,0 +1,113 @@
+"""lq_gemv_chain (the decode chain) against the oracle, problem by problem.
+
+A dependent chain feeds every problem the previous problem's output (after
+= 1), so each C_j is checked against the oracle on the GPU's own C_{j-1}
+(read back), with the GEMV tolerance. Independent problems, CTAs that own no
+rows (N < number of SMs), N = 0 and the refusal of shapes outside the fast
+path are covered as well.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from helpers import check, nan_filled, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(lq, fmt, N, K, seed, dev):
+    W, _ = synthetic.draw(1, N, K, seed=seed, outlier_frac=0.05 if K % 32 == 0 else 0.0)
+    Wn = W.numpy()
+    return Wn, to_dev(lq.pack(fmt, Wn).reshape(-1).view(np.uint8), dev)
+
+
+def _run_chain(lq, fmt, items):
+    st = lq.lq_gemv_chain(fmt, items)
+    torch.cuda.synchronize()
+    return st
+
+
+@pytest.mark.parametrize("fmt,dims", [
+    ("q8_0", [4096, 4096, 2048, 4096, 1024]),
+    ("q4_0", [4096, 11008 // 256 * 256, 4096, 512]),
+    ("f16", [2048, 1000 // 8 * 8, 2048, 256]),
+])
+def test_chain_dependent_matches_oracle_step_by_step(lq, cuda_dev, fmt, dims):
+    # problem j: K = dims[j], N = dims[j + 1]; A_j = C_{j-1} for j > 0
+    torch.manual_seed(0)
+    A0 = torch.randn(dims[0], dtype=torch.float32)
+    Ws, items, Cs = [], [], []
+    A = A0.to(cuda_dev)
+    for j in range(len(dims) - 1):
+        K, N = dims[j], dims[j + 1]
+        Wn, Wd = _weights(lq, fmt, N, K, 100 + j, cuda_dev)
+        C = nan_filled(1, N, cuda_dev)[0]
+        items.append((A, Wd, C, N, K, 1 if j > 0 else 0))
+        Ws.append(Wn)
+        Cs.append(C)
+        A = C
+    lq.reset_counts()
+    assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    assert lq.last_device_error() == lq.LQ_OK
+    assert lq.route_count(4) == 1
+    a_prev = A0.numpy()
+    for j, (Wn, C) in enumerate(zip(Ws, Cs)):
+        N, K = Wn.shape
+        c = C.cpu().numpy()
+        y, tol = O.reference(fmt, a_prev[None, :], O.pack(fmt, Wn), N, K)
+        check(torch.from_numpy(c[None, :]), y, tol, f"{fmt} chain step {j} N={N} K={K}")
+        a_prev = c
+
+
+def test_chain_independent_problems_and_small_n(lq, cuda_dev):
+    fmt = "q8_0"
+    shapes = [(4096, 4096), (100, 2048), (7, 256), (0, 512), (3000, 4096), (152, 1024)]
+    items, refs = [], []
+    for j, (N, K) in enumerate(shapes):
+        Wn, Wd = _weights(lq, fmt, max(N, 1), K, 200 + j, cuda_dev)
+        Wn = Wn[:N]
+        A = torch.randn(K, generator=torch.Generator().manual_seed(300 + j), dtype=torch.float32)
+        C = nan_filled(1, max(N, 1), cuda_dev)[0]
+        items.append((A.to(cuda_dev), Wd, C, N, K, 0))
+        refs.append((Wn, A.numpy(), C, N, K))
+    assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    assert lq.last_device_error() == lq.LQ_OK
+    for Wn, a, C, N, K in refs:
+        if N == 0:
+            assert torch.isnan(C).all()  # nothing written
+            continue
+        y, tol = O.reference(fmt, a[None, :], O.pack(fmt, Wn), N, K)
+        check(C[None, :N].cpu().numpy(), y, tol, f"independent N={N} K={K}")
+
+
+def test_chain_runs_twice_in_a_row(lq, cuda_dev):
+    # the completion counter is reset for every call: the second call's
+    # dependent problem must wait for its own first problem again
+    fmt = "q4_0"
+    K = N = 2048
+    Wn, Wd = _weights(lq, fmt, N, K, 400, cuda_dev)
+    A = torch.randn(K, generator=torch.Generator().manual_seed(401), dtype=torch.float32)
+    Ad = A.to(cuda_dev)
+    for _ in range(2):
+        C1, C2 = nan_filled(1, N, cuda_dev)[0], nan_filled(1, N, cuda_dev)[0]
+        assert lq.lq_gemv_chain(fmt, [(Ad, Wd, C1, N, K, 0), (C1, Wd, C2, N, N, 1)]) == lq.LQ_OK
+        torch.cuda.synchronize()
+        assert lq.last_device_error() == lq.LQ_OK
+        c1 = C1.cpu().numpy()
+        y1, tol1 = O.reference(fmt, A.numpy()[None, :], O.pack(fmt, Wn), N, K)
+        check(c1[None, :], y1, tol1, "first problem")
+        y2, tol2 = O.reference(fmt, c1[None, :], O.pack(fmt, Wn), N, N)
+        check(C2.cpu().numpy()[None, :], y2, tol2, "second problem (reads the first's output)")
+
+
+def test_chain_refuses_shapes_outside_its_path(lq, cuda_dev):
+    fmt = "q8_0"
+    K, N = 96, 64  # K % 256 != 0
+    Wn, Wd = _weights(lq, fmt, N, K, 500, cuda_dev)
+    A = torch.randn(K, dtype=torch.float32, device=cuda_dev)
+    C = nan_filled(1, N, cuda_dev)[0]
+    assert lq.lq_gemv_chain(fmt, [(A, Wd, C, N, K, 0)]) == lq.LQ_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.isnan(C).all()
