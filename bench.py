@@ -5,10 +5,13 @@ Headline workload: the Q8_0 decode GEMV, M=1, N=4096, K=4096 (metric: achieved
 HBM GB/s on the algorithmic bytes W + A + C, as a fraction of the measured
 HBM peak). One step is one decode pass over a stack of R such weight matrices
 (R copies whose total exceeds twice the L2), each multiplied by its own
-activation row through the library's router; the step is captured once as a
-CUDA graph and replayed, so the GPU never waits on the host. The other
-workload families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and
-the M = 2 / 16 / 64 crossover) are timed the same way under "workloads".
+activation row. For M = 1 the pass is one lq_gemv_chain call (the R GEMVs are
+independent: each has its own A and C); the same pass as R separate
+lq_matmul calls, and as a chain whose every problem waits for the previous
+one, is reported under "workloads" too. Steps are captured once as a CUDA
+graph and replayed, so the GPU never waits on the host. The other workload
+families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and the
+M = 2 / 16 / 64 crossover) are timed the same way under "workloads".
 
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload (rank 0 only) and prints the same JSON line with "impl": "reference".
@@ -39,6 +42,8 @@ import torch  # noqa: E402
 import synthetic  # noqa: E402
 
 HEADLINE = "gemv_q8_0_4096x4096"
+KERNEL_OF_MODE = {"chain": "gemv_chain_kernel", "chain-dependent": "gemv_chain_kernel",
+                  "calls": "gemv_stream_kernel"}
 METRIC = "decode GEMV achieved HBM GB/s (% of peak); prefill GEMM TFLOP/s (% peak)"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -65,13 +70,13 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
-def ncu_traffic(workload: str):
+def ncu_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel, from the committed ncu
-    summary of this workload (profiles/<kernel>.<workload>.md, line
+    summary of this kernel and workload (profiles/<kernel>.<workload>.md, line
     'traffic_bytes_per_launch: <int>'); None when there is no summary or when
     a kernel source it lists ('source: <path> <sha256 prefix>') has changed
     since the capture."""
-    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"*.{workload}.md"))):
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", f"{kernel}.{workload}.md"))):
         with open(path) as f:
             text = f.read()
         m = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
@@ -146,7 +151,11 @@ class Workbench:
     copies together exceed twice the L2), R activation blocks and R outputs;
     step() runs the library's router once per copy."""
 
-    def __init__(self, lq, w: synthetic.Workload, dev, copies=None, max_bytes=3 * 2**30):
+    def __init__(self, lq, w: synthetic.Workload, dev, copies=None, max_bytes=3 * 2**30,
+                 mode="auto"):
+        """mode: "calls" (one lq_matmul per copy), "chain" (one lq_gemv_chain
+        over the independent copies), "chain-dependent" (every problem waits
+        for the previous one), or "auto" (chain for M = 1, else calls)."""
         self.lq, self.w, self.dev = lq, w, dev
         W, A = synthetic.draw_workload(w)
         packed = lq.pack(w.fmt, W).reshape(-1).view(np.uint8)
@@ -164,9 +173,30 @@ class Workbench:
         self.bytes_per_launch = algorithmic_bytes(w.fmt, w.M, w.N, w.K)
         self.flops_per_launch = flops(w.M, w.N, w.K)
         self.graph = None
+        if mode == "auto":
+            mode = "chain" if w.M == 1 else "calls"
+        self.problems = None
+        if mode.startswith("chain") and w.M == 1:
+            # one chain call per 64 problems (the call's limit)
+            after = 1 if mode == "chain-dependent" else 0
+            self.problems = [
+                lq.gemv_problems([(self.Ad[r], self.Wd[r], self.Cd[r], w.N, w.K, after if r > r0 else 0)
+                                  for r in range(r0, min(R, r0 + 64))])
+                for r0 in range(0, R, 64)]
+            if any(lq.lq_gemv_chain(w.fmt, arr) != lq.LQ_OK for arr in self.problems):
+                self.problems = None  # outside the chain's path: separate calls
+            torch.cuda.synchronize(dev)
+        self.mode = mode if self.problems is not None else "calls"
+        # kernels of ours per step
+        self.kernels_per_step = (len(self.problems) if self.problems is not None
+                                 else R * (2 if w.M >= 2 else 1))
 
     def step(self, stream=None):
         w = self.w
+        if self.problems is not None:
+            for arr in self.problems:
+                self.lq.lq_gemv_chain(w.fmt, arr, stream)
+            return
         for r in range(self.R):
             self.fn(self.Ad[r], self.Wd[r], self.Cd[r], w.M, w.N, w.K, stream)
 
@@ -331,6 +361,8 @@ def main():
     ap.add_argument("--extras", default="all",
                     help="comma-separated extra workloads to time, 'all' or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="auto", choices=["auto", "calls", "chain", "chain-dependent"],
+                    help="how the headline step runs its matmuls (auto: chain for M = 1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -367,7 +399,7 @@ def main():
 
     # ---- headline workload
     w = synthetic.WORKLOADS[args.workload]
-    wb = Workbench(lq, w, dev)
+    wb = Workbench(lq, w, dev, mode=args.mode)
     wb.capture()
     probe = wb.time_graph(3, 1)
     steps = args.steps or max(20, int(1.5 / max(probe / 3, 1e-7)))
@@ -376,15 +408,19 @@ def main():
         dt = wb.time_graph(steps, args.warmup, barrier)
     dt = max_over_ranks(dt)
     clocks = clk.summary()
-    launches_per_step = wb.R
-    per_launch = dt / (steps * launches_per_step)
-    val1, unit, bound = rate(wb, per_launch)
+    kernel = KERNEL_OF_MODE[wb.mode] if w.M == 1 else "gemm_tma_kernel"
+    launches_per_step = wb.kernels_per_step
+    per_gemv = dt / (steps * wb.R)          # one matmul of the workload
+    val1, unit, bound = rate(wb, per_gemv)
     value = val1 * world  # every rank runs the same per-GPU work (weak scaling)
     peak = hbm_peak if bound == "hbm" else tc_peak
+    # the dominant kernel's launches: the step's work divided evenly
+    per_launch = dt / (steps * launches_per_step)
+    work_per_launch = (wb.bytes_per_launch if bound == "hbm" else wb.flops_per_launch) * wb.R / launches_per_step
     roofline = {"bound": bound, "achieved": val1, "peak": peak, "unit": unit,
-                "frac": val1 / peak, "traffic": ncu_traffic(w.name),
+                "frac": val1 / peak, "traffic": ncu_traffic(w.name, kernel),
                 "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops'})",
-                "algorithmic_per_launch": wb.bytes_per_launch if bound == "hbm" else wb.flops_per_launch,
+                "kernel": kernel, "algorithmic_per_launch": work_per_launch,
                 "us_per_launch": per_launch * 1e6}
     e2e_dt, h2d, d2h, _ = wb.time_e2e(steps)
     e2e_dt = max_over_ranks(e2e_dt)
@@ -394,11 +430,12 @@ def main():
     # ---- the other workload families (same method, shorter runs)
     extras = {}
     names = EXTRA if args.extras == "all" else ([] if args.extras == "none" else args.extras.split(","))
-    for name in names:
-        if name == w.name:
-            continue
+    runs = [(name, "auto") for name in names if name != w.name]
+    if w.M == 1 and args.extras != "none":
+        runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
+    for name, mode in runs:
         x = synthetic.WORKLOADS[name]
-        xb = Workbench(lq, x, dev)
+        xb = Workbench(lq, x, dev, mode=mode)
         xb.capture()
         p = xb.time_graph(2, 1)
         n = max(5, int(0.25 / max(p / 2, 1e-7)))
@@ -406,8 +443,9 @@ def main():
         pl = d / (n * xb.R)
         v, u, b = rate(xb, pl)
         pk = hbm_peak if b == "hbm" else tc_peak
-        extras[name] = {"value": v, "unit": u, "bound": b, "frac": v / pk, "us_per_launch": pl * 1e6,
-                        "copies": xb.R, "launches": n * xb.R,
+        key = name if mode == "auto" else f"{name} [{mode}]"
+        extras[key] = {"value": v, "unit": u, "bound": b, "frac": v / pk, "us_per_matmul": pl * 1e6,
+                        "mode": xb.mode, "copies": xb.R, "launches": n * xb.kernels_per_step,
                         "gb_per_s": xb.bytes_per_launch / pl / 1e9,
                         "tflop_per_s": xb.flops_per_launch / pl / 1e12}
         xb.free()
@@ -426,10 +464,10 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch.randn, recipe in synthetic.py)",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "format": w.fmt,
-                       "launches_per_step": launches_per_step,
+                       "launches_per_step": launches_per_step, "matmuls_per_step": wb.R,
                        "l2": f"inputs larger than L2: {wb.R} weight copies, "
                              f"{wb.R * wb.wbytes / 2**20:.0f} MiB > {L2_BYTES // 2**20} MiB",
-                       "step": "one decode pass over the weight-copy stack, CUDA-graph replay",
+                       "step": f"one decode pass over the weight-copy stack ({wb.mode}), CUDA-graph replay",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "cpu_baseline": cpu,
