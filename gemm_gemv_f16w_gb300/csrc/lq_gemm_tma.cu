@@ -32,7 +32,9 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "lq_device.cuh"
 #include "lq_internal.h"
@@ -47,7 +49,7 @@ constexpr int kNumConv = 8;                        // converter warps (2 groups 
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
-constexpr int kMaxStages = 4, kRawStages = 2;
+constexpr int kMaxStages = 4, kMaxRawStages = 8;
 constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
 constexpr uint32_t kWCol0 = 256;
 constexpr float kWScale = 256.0f;                  // Q formats: W is computed as 2^8 * w
@@ -63,13 +65,15 @@ struct TmaGemmParams {
   const float* scale;  // s_m per token (from the pre-pass)
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
+  int split;           // CTAs of a cluster splitting K (1: no split)
   int stages;          // pipeline depth (2..kMaxStages)
+  int raw_stages;      // raw W ring depth (2..kMaxRawStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
 
 struct Bars {
-  uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+  uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
   uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
   uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
   uint64_t tmem_full;
@@ -245,10 +249,68 @@ __device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t 
 }
 
 // ---------------------------------------------------------------------------
+// Split-K support: cluster barrier and loads from a peer CTA's shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
+
+// Epilogue of one TMEM lane (W row r of the tile): the accumulator columns
+// of 32-column chunks c0, c0 + dc, ..., plus the partial tiles of peers
+// 1 .. split-1 (token-major f32 at `red` in their shared memory) when
+// split > 1, scaled by s_m (and 2^-8 for the quantised formats) and stored
+// to C[m0 + j, n0 + r].
+template <int FMT>
+__device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
+                                           int bt, int lane, uint32_t red, int split, int c0, int dc) {
+  const int n = n0 + r;
+  const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
+#pragma unroll 1
+  for (int c = c0; c < (bt + 31) / 32; c += dc) {
+    uint32_t v[32];
+    tc::ld_32x32b_x32(tcol + 32u * c, v);
+    // lane j holds the scale of token m0 + 32c + j
+    const int ml = m0 + 32 * c + lane;
+    const float sc = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
+    tc::wait_ld();
+#pragma unroll 1
+    for (int q = 1; q < split; ++q) {
+      // all 32 loads first, so that they are in flight together
+      float t[32];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj)
+        t[jj] = 32 * c + jj < bt ? ld_peer_f32(red + 4u * static_cast<uint32_t>((32 * c + jj) * kBN + r),
+                                               static_cast<uint32_t>(q))
+                                 : 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + t[jj]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      const int m = m0 + 32 * c + jj;
+      const float f = __shfl_sync(0xffffffffu, sc, jj);
+      if (n < p.N && 32 * c + jj < bt && m < p.M)
+        p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
 // Warps 2..9: converters in two groups of four (group g converts the
 // pipeline stages ks with ks % 2 == g: 128 K of its W rows into the stage's
-// 64 TMEM columns); warps 2..5 then run the epilogue. Per stage one barrier
+// 64 TMEM columns); then both groups run the epilogue, group g taking the
+// 32-column chunks g, g + 2, ... With split K (a cluster of CTAs sharing one
+// output tile), the other ranks leave their partial tiles in their own
+// shared memory and the leader adds them over distributed shared memory
+// before storing C. Per stage one barrier
 // says "A tile and W operand ready" (1 arrival with the TMA bytes + 4
 // converter warps) and one commit says "the stage's MMAs are done". The
 // producer and MMA warps run their loops with all 32 lanes (every lane
@@ -269,15 +331,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
   uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
-  uint8_t* w_ring = base + S * a_stage_bytes;                      // kRawStages x raw W stages
-  Bars& b = *reinterpret_cast<Bars*>(w_ring + kRawStages * kRawBytes);
+  const int RR = p.raw_stages;
+  uint8_t* w_ring = base + S * a_stage_bytes;                      // RR x raw W stages
+  Bars& b = *reinterpret_cast<Bars*>(w_ring + RR * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * bt;
-  const int nk = p.K / kKS, nraw = nk / SUB;
+  // Split K: the `split` CTAs of a cluster share one output tile, rank r
+  // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
+  // the CTA, the K coordinates of its loads add ks0.
+  const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
+  const int n0 = (static_cast<int>(blockIdx.x) / split) * kBN, m0 = blockIdx.y * bt;
+  const int nraw_all = p.K / kKS / SUB;
+  const int jr0 = rank * nraw_all / split;
+  const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
+  bool epi = false;  // this CTA's accumulator is complete and may be used
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRawStages; ++i) {
+    for (int i = 0; i < RR; ++i) {
       mbar_init(&b.raw_full[i], 1);
       mbar_init(&b.raw_empty[i], 4 * SUB);
     }
@@ -309,22 +379,23 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
       if (FMT == LQ_FMT_F16) {
         for (int h = 0; h < 2; ++h)  // two boxes of 64 halves x 128 rows (128B-swizzled)
-          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * j + 64 * h, n0,
+          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
                           &b.raw_full[slot]);
       } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
-        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * j, n0, &b.raw_full[slot]);
+        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
+                        &b.raw_full[slot]);
       }
     };
     int raw_issued = 0, issued = 0;
     bool ok = true;
     // W does not depend on the previous kernel: start it before waiting.
-    for (; raw_issued < nraw && raw_issued < kRawStages; ++raw_issued)
+    for (; raw_issued < nraw && raw_issued < RR; ++raw_issued)
       if (lane == 0) issue_raw(raw_issued, raw_issued);
     __syncwarp();
     pdl_wait();
     int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
     for (int ks = 0; ks < nk; ++ks) {
-      if (ks % SUB == 0 && ks / SUB >= kRawStages) {
+      if (ks % SUB == 0 && ks / SUB >= RR) {
         const int j = ks / SUB;  // reuse raw slot j % 2 after both of its users finished
         if (!warp_wait(&b.raw_empty[rslot], rlap & 1, p) || b.abort) {
           ok = false;
@@ -333,7 +404,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (lane == 0) issue_raw(j, rslot);
         __syncwarp();
         ++raw_issued;
-        if (++rslot == kRawStages) { rslot = 0; ++rlap; }
+        if (++rslot == RR) { rslot = 0; ++rlap; }
       }
       if (ks >= S && (!warp_wait(&b.empty[st], (lap - 1) & 1, p) || b.abort)) {
         ok = false;
@@ -341,8 +412,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       if (lane == 0) {
         mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * ks, m0, &b.full[st]);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * ks + 64, m0, &b.full[st]);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.full[st]);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, m0,
+                        &b.full[st]);
       }
       __syncwarp();
       ++issued;
@@ -353,8 +425,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       b.abort = 1;
     }
     // never leave copies in flight (waits for the last use of every slot)
-    for (int j = max(0, raw_issued - kRawStages); j < raw_issued; ++j)
-      mbar_wait(&b.raw_full[j % kRawStages], (j / kRawStages) & 1, kDrainWaitNs);
+    for (int j = max(0, raw_issued - RR); j < raw_issued; ++j)
+      mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
     for (int ks = max(0, issued - S); ks < issued; ++ks)
       mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
   } else if (warp == 1) {
@@ -412,8 +484,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
     for (int ks = g; ks < nk; ks += 2) {
-      const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % kRawStages;
-      if (!warp_wait(&b.raw_full[rslot], (j / kRawStages) & 1, p) || b.abort) {
+      const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % RR;
+      if (!warp_wait(&b.raw_full[rslot], (j / RR) & 1, p) || b.abort) {
         ok = false;
         break;
       }
@@ -440,32 +512,29 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       record_error(kDevErrTimeout);
       b.abort = 1;
     }
-    if (g == 0) {
-      // ---------------- epilogue ----------------
+    {
+      // ---------------- epilogue (both groups: 32-column chunks g, g + 2, ...) ----------------
       const bool have = warp_wait(&b.tmem_full, 0, p);
       tc::fence_after_sync();
       if (!have && lane == 0) {
         record_error(kDevErrTimeout);
         b.abort = 1;
       }
-      if (have && !b.abort) {
-        const int n = n0 + r;
-        const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
+      epi = have && !b.abort;
+      if (epi && split == 1) {
+        store_tile<FMT>(p, tmem + tlane, r, n0, m0, bt, lane, 0u, 1, g, 2);
+      } else if (epi && rank != 0) {
+        // this rank's partial tile -> its own shared memory (the A ring is
+        // idle now), token-major so that the 32 lanes write 32 rows in a row
+        float* red = reinterpret_cast<float*>(a_ring);
 #pragma unroll 1
-        for (int c = 0; c < (bt + 31) / 32; ++c) {
+        for (int c = g; c < (bt + 31) / 32; c += 2) {
           uint32_t v[32];
           tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
-          // lane j holds the scale of token m0 + 32c + j
-          const int ml = m0 + 32 * c + lane;
-          const float sc = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
           tc::wait_ld();
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int m = m0 + 32 * c + jj;
-            const float f = __shfl_sync(0xffffffffu, sc, jj);
-            if (n < p.N && 32 * c + jj < bt && m < p.M)
-              p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * f;
-          }
+          for (int jj = 0; jj < 32; ++jj)
+            if (32 * c + jj < bt) red[(32 * c + jj) * kBN + r] = __uint_as_float(v[jj]);
         }
       }
     }
@@ -473,6 +542,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // ---------------- teardown ----------------
   tc::fence_before_sync();
   __syncthreads();
+  if (split > 1) {
+    // the peers' partial tiles are in their shared memory; the leader adds
+    // them to its own (rank order: a fixed summation order) and stores C
+    cluster_sync();
+    if (rank == 0 && epi && warp >= 2) {
+      tc::fence_after_sync();
+      const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
+      store_tile<FMT>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, lane,
+                      smem_u32(a_ring), split, g, 2);
+    }
+    cluster_sync();  // the peers keep their shared memory until the leader read it
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -501,29 +582,45 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
+// Launch with programmatic dependent launch and, when cluster_x > 1,
+// clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               unsigned cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
-  cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  return launch_pdl_cluster(kern, grid, block, smem, st, 1u, std::forward<Args>(args)...);
 }
 
 bool aligned(const void* p, unsigned al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
 
 int kstep_multiple(int fmt) { return fmt == LQ_FMT_F16 ? 128 : 256; }  // one raw stage
 
-// Token-tile width: enough tiles to put about one CTA on every SM, at most
-// 256 tokens (the MMA's N limit) and at least 16.
+// Token-tile width. Up to 256 tokens: one tile (W is streamed once; the SMs
+// are filled by splitting K). Beyond: enough tiles to put about one CTA on
+// every SM, at most 256 tokens (the MMA's N limit).
 int pick_bt(int64_t M, int64_t N) {
+  if (M <= 256) return static_cast<int>((M + 15) / 16 * 16);
   const DeviceInfo& di = device_info();
   const int64_t ntn = (N + kBN - 1) / kBN;
   int64_t t = std::max<int64_t>(1, (di.sm_count + ntn / 2) / ntn);
@@ -535,28 +632,87 @@ int pick_bt(int64_t M, int64_t N) {
 
 int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
 
-// Pipeline depth that fits next to the raw-W ring (A tile of a stage: bt
-// rows x 128 K halves).
-int a_stages_for(int fmt, int bt) {
+// Ring depths for a token tile of bt: the raw W ring first (W comes from
+// HBM: up to 6 raw stages of f16, 4 of Q8_0 / Q4_0, i.e. 6 to 8 pipeline
+// stages of lookahead), then as many A stages (bt rows x 128 K halves, from
+// L2) as fit, at least two of each.
+struct RingPlan {
+  int a_stages = 0, raw_stages = 0;
+};
+RingPlan ring_plan(int fmt, int bt) {
   const DeviceInfo& di = device_info();
-  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - 256 -
-                           static_cast<long long>(kRawStages) * raw_stage_bytes(fmt);
-  const long long n = budget / (static_cast<long long>(bt) * 256);
-  return static_cast<int>(std::min<long long>(kMaxStages, n));
+  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
+                           static_cast<long long>(sizeof(Bars)) - 64;
+  const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt);
+  RingPlan rp;
+  const int raw_cap = fmt == LQ_FMT_F16 ? 6 : 4;
+  rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 2 * a_stage) / raw));
+  if (rp.raw_stages < 2) return RingPlan{};
+  rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
+  if (rp.a_stages < 2) return RingPlan{};
+  return rp;
 }
 
-size_t tma_smem_bytes(int fmt, int bt, int a_stages) {
+size_t tma_smem_bytes(int fmt, int bt, int a_stages, int raw_stages) {
   const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 256 +
-                      static_cast<size_t>(kRawStages) * raw_stage_bytes(fmt) + sizeof(Bars) + 64;
+                      static_cast<size_t>(raw_stages) * raw_stage_bytes(fmt) + sizeof(Bars) + 64;
   // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
   return std::max<size_t>(need, 116 * 1024);
 }
 
+// Clusters of `split` CTAs along K: the largest split (up to 8, the portable
+// cluster size) whose clusters all fit on the GPU at once, or 1.
+template <int FMT>
+int pick_split_query(int64_t tiles, int nraw_all, size_t smem);
+
+template <int FMT>
+int pick_split(int64_t tiles, int nraw_all, size_t smem) {
+  const DeviceInfo& di = device_info();
+  if (2 * tiles > di.sm_count) return 1;
+  // the answer depends on (tiles, K, shared memory) only: remember it
+  static std::mutex mu;
+  static std::map<std::tuple<int, int64_t, int, size_t>, int> cache;
+  const auto key = std::make_tuple(current_device(), tiles, nraw_all, smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int s = pick_split_query<FMT>(tiles, nraw_all, smem);
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = s;
+  return s;
+}
+
+template <int FMT>
+int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
+  const DeviceInfo& di = device_info();
+  int s = static_cast<int>(std::min<int64_t>({8, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all}));
+  for (; s >= 2; --s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * s));
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT>, &cfg) == cudaSuccess && active >= tiles)
+      return s;
+    cudaGetLastError();  // a refused query is not an error of the call
+  }
+  return 1;
+}
+
 template <int FMT>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
-                             const TmaGemmParams& p) {
+                             TmaGemmParams p) {
   auto kern = gemm_tma_kernel<FMT>;
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages);
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -565,8 +721,12 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
     if (e != cudaSuccess) return cuda_status(e);
     configured[dev] = static_cast<int>(smem);
   }
-  const dim3 grid(static_cast<unsigned>((a.N + kBN - 1) / kBN), static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
-  cudaError_t e = launch_pdl(kern, grid, dim3(kTmaThreads), smem, a.stream, tmW, tmA, p);
+  const int64_t tiles = ((a.N + kBN - 1) / kBN) * ((a.M + p.bt - 1) / p.bt);
+  p.split = pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
+  const dim3 grid(static_cast<unsigned>((a.N + kBN - 1) / kBN * p.split),
+                  static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
+  cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
+                                     static_cast<unsigned>(p.split), tmW, tmA, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
 }
@@ -588,7 +748,7 @@ bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
   if (!encode_fn()) return false;
   const DeviceInfo& di = device_info();
-  return di.cc_major >= 10 && a_stages_for(a.fmt, 256) >= 2;
+  return di.cc_major >= 10 && ring_plan(a.fmt, 256).a_stages >= 2;
 }
 
 // The library's own stream-ordered memory pool on the current device: freed
@@ -690,7 +850,12 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   p.N = N;
   p.K = K;
   p.bt = bt;
-  p.stages = a_stages_for(a.fmt, bt);
+  p.split = 1;  // chosen at launch (pick_split)
+  {
+    const RingPlan rp = ring_plan(a.fmt, bt);
+    p.stages = rp.a_stages;
+    p.raw_stages = rp.raw_stages;
+  }
   if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
