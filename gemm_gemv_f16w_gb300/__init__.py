@@ -34,7 +34,7 @@ EXPORTS = [
     "lq_packed_bytes", "lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0",
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
-    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain",
+    "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
         L.lq_debug_set_wait_limit_ns.restype = None
         L.lq_gemv_chain.argtypes = [st, ctypes.POINTER(GemvProblem), ctypes.c_int, vp]
         L.lq_gemv_chain.restype = st
+        L.lq_debug_gemm_rings.argtypes = [ctypes.c_int, ctypes.c_int]
+        L.lq_debug_gemm_rings.restype = st
         L.lq_debug_gemv_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.lq_debug_gemv_plan.restype = st
         L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
@@ -247,3 +249,8 @@ def gemv_plan(ctas_per_sm: int = 0, rows_per_stage: int = 0, smem_bytes: int = 0
     """Override the decode GEMV's launch plan (0 = automatic); tuning only."""
     _check(lib().lq_debug_gemv_plan(int(ctas_per_sm), int(rows_per_stage), int(smem_bytes)),
            "lq_debug_gemv_plan")
+
+
+def gemm_rings(a_stages: int = 0, raw_stages: int = 0) -> None:
+    """Override the tensor-core GEMM's ring depths (0 = automatic); tuning only."""
+    _check(lib().lq_debug_gemm_rings(int(a_stages), int(raw_stages)), "lq_debug_gemm_rings")

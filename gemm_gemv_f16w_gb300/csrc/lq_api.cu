@@ -214,6 +214,11 @@ void lq_debug_reset_counts(void) {
   for (auto& c : g_route_count) c.store(0);
 }
 void lq_debug_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
+lq_status lq_debug_gemm_rings(int a_stages, int raw_stages) {
+  if (a_stages < 0 || a_stages > 4 || raw_stages < 0 || raw_stages > 8) return LQ_ERR_INVALID_ARG;
+  lq::set_gemm_rings(a_stages, raw_stages);
+  return LQ_OK;
+}
 lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes) {
   if (ctas_per_sm < 0 || ctas_per_sm > 2 || rows_per_stage < 0 || rows_per_stage > 8 ||
       smem_bytes < 0)

@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -91,64 +92,65 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // ---------------------------------------------------------------------------
 // Pre-pass: A f32 [M,K] -> f16 [M,K] scaled by 1/s_m, s_m = 2^(e-15) where
-// max|a_m| < 2^e (frexp), so max|a_m/s_m| lies in [2^14, 2^15).
+// max|a_m| < 2^e (frexp), so max|a_m/s_m| lies in [2^14, 2^15). One CTA of
+// 128 threads per token row; rows of up to 4096 values stay in registers
+// between the two passes (longer rows are read twice).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) a_to_f16_kernel(const float* __restrict__ A,
-                                                        __half* __restrict__ A16,
-                                                        float* __restrict__ scale, int M, int K) {
+constexpr int kPreThreads = 128, kPreKeep = 8;  // float4 per thread kept in registers
+__global__ void __launch_bounds__(kPreThreads) a_to_f16_kernel(const float* __restrict__ A,
+                                                               __half* __restrict__ A16,
+                                                               float* __restrict__ scale, int M, int K) {
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5), nw = gridDim.x * 8;
-  constexpr int kChunk = 32 * 4 * 8;  // floats one warp keeps in registers per pass
-  for (int m = gw; m < M; m += nw) {
-    const float4* a = reinterpret_cast<const float4*>(A + static_cast<long long>(m) * K);
-    __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
-    // pass 1: row maximum (rows up to kChunk floats stay in registers)
-    float4 keep[8];
-    float amax = 0.f;
+  __shared__ float wmax[kPreThreads / 32];
+  const int m = blockIdx.x, t = threadIdx.x, K4 = K / 4;
+  const float4* a = reinterpret_cast<const float4*>(A + static_cast<long long>(m) * K);
+  __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
+  float4 keep[kPreKeep];
+  float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int idx = lane + 32 * i;
-      keep[i] = idx < K / 4 ? a[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int base = 0; base < K / 4; base += 256) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = base + lane + 32 * i;
-        if (idx < K / 4) {
-          const float4 v = base == 0 ? keep[i] : a[idx];
-          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-        }
-      }
-    }
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    int e = 0;
-    float inv = 1.f, s = 1.f;
-    if (amax > 0.f && amax <= 3.4e38f) {
-      frexpf(amax, &e);
-      s = ldexpf(1.f, e - 15);
-      inv = ldexpf(1.f, 15 - e);
-    }
-    // pass 2: scale (exact) and round to f16
-    for (int base = 0; base < K / 4; base += 256) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int idx = base + lane + 32 * i;
-        if (idx < K / 4) {
-          const float4 v = base == 0 ? keep[i] : a[idx];
-          out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
-          out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
-        }
-      }
-    }
-    if (lane == 0) scale[m] = s;
+  for (int i = 0; i < kPreKeep; ++i) {
+    const int idx = t + kPreThreads * i;
+    keep[i] = idx < K4 ? __ldg(a + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(keep[i].x), fabsf(keep[i].y)), fmaxf(fabsf(keep[i].z), fabsf(keep[i].w))));
   }
-  (void)kChunk;
+  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads) {
+    const float4 v = __ldg(a + idx);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  if ((t & 31) == 0) wmax[t >> 5] = amax;
+  __syncthreads();
+  amax = wmax[0];
+#pragma unroll
+  for (int w = 1; w < kPreThreads / 32; ++w) amax = fmaxf(amax, wmax[w]);
+  int e = 0;
+  float inv = 1.f, s = 1.f;
+  if (amax > 0.f && amax <= 3.4e38f) {
+    frexpf(amax, &e);
+    s = ldexpf(1.f, e - 15);
+    inv = ldexpf(1.f, 15 - e);
+  }
+  // scale (exact) and round to f16
+#pragma unroll
+  for (int i = 0; i < kPreKeep; ++i) {
+    const int idx = t + kPreThreads * i;
+    if (idx < K4) {
+      out[2 * idx] = __floats2half2_rn(keep[i].x * inv, keep[i].y * inv);
+      out[2 * idx + 1] = __floats2half2_rn(keep[i].z * inv, keep[i].w * inv);
+    }
+  }
+  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads) {
+    const float4 v = __ldg(a + idx);
+    out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
+    out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
+  }
+  if (t == 0) scale[m] = s;
+  (void)M;
 }
 
 // ---------------------------------------------------------------------------
@@ -269,16 +271,15 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer)
 // to C[m0 + j, n0 + r].
 template <int FMT>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
-                                           int bt, int lane, uint32_t red, int split, int c0, int dc) {
+                                           int bt, uint32_t red, int split, int c0, const float (&scp)[4]) {
   const int n = n0 + r;
-  const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
-#pragma unroll 1
-  for (int c = c0; c < (bt + 31) / 32; c += dc) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + 2 * i;
+    if (c >= (bt + 31) / 32) break;
     uint32_t v[32];
     tc::ld_32x32b_x32(tcol + 32u * c, v);
-    // lane j holds the scale of token m0 + 32c + j
-    const int ml = m0 + 32 * c + lane;
-    const float sc = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
+    const float sc = scp[i];  // lane j: the scale of token m0 + 32c + j
     tc::wait_ld();
 #pragma unroll 1
     for (int q = 1; q < split; ++q) {
@@ -345,6 +346,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int jr0 = rank * nraw_all / split;
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
   bool epi = false;  // this CTA's accumulator is complete and may be used
+  float scp[4] = {0.f, 0.f, 0.f, 0.f};  // epilogue: scales of chunks g, g + 2, g + 4, g + 6
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RR; ++i) {
@@ -514,6 +516,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     {
       // ---------------- epilogue (both groups: 32-column chunks g, g + 2, ...) ----------------
+      // The token scales of this group's chunks, fetched while the last MMAs
+      // run (they come from the pre-pass, complete once griddepcontrol.wait
+      // returns; by now it returns at once).
+      pdl_wait();
+      {
+        const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = g + 2 * i, ml = m0 + 32 * c + lane;
+          scp[i] = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
+        }
+      }
       const bool have = warp_wait(&b.tmem_full, 0, p);
       tc::fence_after_sync();
       if (!have && lane == 0) {
@@ -522,7 +536,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       epi = have && !b.abort;
       if (epi && split == 1) {
-        store_tile<FMT>(p, tmem + tlane, r, n0, m0, bt, lane, 0u, 1, g, 2);
+        store_tile<FMT>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g, scp);
       } else if (epi && rank != 0) {
         // this rank's partial tile -> its own shared memory (the A ring is
         // idle now), token-major so that the 32 lanes write 32 rows in a row
@@ -549,8 +563,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (rank == 0 && epi && warp >= 2) {
       tc::fence_after_sync();
       const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
-      store_tile<FMT>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, lane,
-                      smem_u32(a_ring), split, g, 2);
+      store_tile<FMT>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
+                      split, g, scp);
     }
     cluster_sync();  // the peers keep their shared memory until the leader read it
   }
@@ -639,6 +653,8 @@ int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == L
 struct RingPlan {
   int a_stages = 0, raw_stages = 0;
 };
+std::atomic<int> g_ring_a{0}, g_ring_raw{0};  // debug override (0 = automatic)
+
 RingPlan ring_plan(int fmt, int bt) {
   const DeviceInfo& di = device_info();
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
@@ -650,6 +666,12 @@ RingPlan ring_plan(int fmt, int bt) {
   if (rp.raw_stages < 2) return RingPlan{};
   rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
   if (rp.a_stages < 2) return RingPlan{};
+  const int oa = g_ring_a.load(), orr = g_ring_raw.load();
+  if (oa || orr) {
+    const int a2 = oa ? oa : rp.a_stages, r2 = orr ? orr : rp.raw_stages;
+    if (a2 >= 2 && a2 <= kMaxStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
+      return RingPlan{a2, r2};
+  }
   return rp;
 }
 
@@ -742,6 +764,11 @@ unsigned read_clear_gemm_tma_error() {
 
 int pick_gemm_bt(int64_t M, int64_t N) { return pick_bt(M, N); }
 
+void set_gemm_rings(int a_stages, int raw_stages) {
+  g_ring_a.store(a_stages);
+  g_ring_raw.store(raw_stages);
+}
+
 bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M < 2 || a.K % kstep_multiple(a.fmt) != 0) return false;
   if (!aligned(a.A, 16) || !aligned(a.W, 16)) return false;
@@ -798,10 +825,8 @@ lq_status launch_gemm_tma(const MatmulArgs& a) {
 // Pre-pass + GEMM given a workspace of M*K halves (A16) and M floats (scale).
 lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
-  const DeviceInfo& di = device_info();
   // 1. A -> f16 with per-token power-of-two scales
-  const int pre_grid = std::max(1, std::min((M + 7) / 8, 8 * std::max(di.sm_count, 1)));
-  cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(pre_grid), dim3(256), 0, a.stream, a.A,
+  cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(static_cast<unsigned>(M)), dim3(kPreThreads), 0, a.stream, a.A,
                              static_cast<__half*>(a16), scale, M, K);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return LQ_ERR_CUDA;

@@ -57,6 +57,8 @@ lq_status launch_gemm_tma(const MatmulArgs& a);
 lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt);
 bool gemm_tma_eligible(const MatmulArgs& a);
 int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
+// TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
+void set_gemm_rings(int a_stages, int raw_stages);
 
 // Decode chain (lq_gemv_chain); LQ_ERR_UNSUPPORTED when the problems do not
 // fit its fast path.
