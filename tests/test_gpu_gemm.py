@@ -54,6 +54,22 @@ def test_tc_shapes(lq, cuda_dev, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("M,N,K", [(300, 6144, 1024), (400, 2048, 1024), (511, 1536, 512)])
+def test_tc_shapes_that_fill_the_gpu(lq, cuda_dev, fmt, M, N, K):
+    """Enough output tiles for every SM (K is not split), several token tiles
+    of different heights; checked on every 97th W row against the oracle."""
+    W, A = synthetic.draw(M, N, K, seed=M + N, outlier_frac=0.05)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    rows = np.arange(0, N, 97)
+    Wr = W[rows]
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, Wr.numpy()), len(rows), K, tensor_core=True)
+    check(C[:, rows], y, tol, f"{fmt} {M}x{N}x{K}")
+    assert np.all(np.isfinite(C))
+    assert lq.route_count(2) == 1
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
 def test_gemm_router_and_generic_route_agree(lq, cuda_dev, fmt):
     """Every route gives the oracle's answer (forced-route test hook)."""
     W, A = synthetic.draw(24, 192, 320, seed=3)
