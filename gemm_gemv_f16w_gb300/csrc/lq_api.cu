@@ -112,12 +112,20 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
   if (st != LQ_OK || noop) return st;
   MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
   switch (g_force_route.load()) {
-    case 1: return launch_gemm_stream(a);
+    case 1:
+      st = launch_gemv_batch(a);
+      return st == LQ_ERR_UNSUPPORTED ? launch_gemm_stream(a) : st;
     case 2:
       if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
       return gemm_tc_eligible(a) ? launch_gemm_tc(a) : LQ_ERR_UNSUPPORTED;
     case 3: return launch_gemv_generic(a);
     default: break;
+  }
+  // M = 2..4: one pass over W on the CUDA cores beats the tensor-core
+  // kernel's fixed latencies
+  if (M <= 4) {
+    st = launch_gemv_batch(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
   }
   if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
   if (gemm_tc_eligible(a)) return launch_gemm_tc(a);
@@ -182,7 +190,8 @@ lq_status lq_last_device_error(void) {
   const unsigned b = read_clear_gemm_error();
   const unsigned c = read_clear_gemm_tma_error();
   const unsigned d = read_clear_chain_error();
-  const unsigned v = a ? a : (b ? b : (c ? c : d));
+  const unsigned e = read_clear_batch_error();
+  const unsigned v = a ? a : (b ? b : (c ? c : (d ? d : e)));
   if (v == 0) return LQ_OK;
   return static_cast<lq_status>(v);
 }

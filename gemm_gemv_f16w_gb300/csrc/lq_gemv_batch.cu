@@ -1,0 +1,359 @@
+// Batched decode: C[m, n] = sum_k A[m, k] * w(n, k) for M = 2..4 rows of A
+// (several sequences decoded together; route 1, the CUDA-core streaming
+// GEMM). The pages' counterpart is the NR x NM multi-row GEMV pattern of
+// gemm_q4 / gemm_q8 (lattice-inference 0.1.2, src/forward/metal_qwen35.rs),
+// which reads each weight block once for several rows of A.
+//
+// The streaming GEMV (lq_gemv.cu) with the weights dequantised once per lane
+// and multiplied with all M activation rows:
+//
+//  * one CTA per SM owns a contiguous range of W rows, streamed in stages of
+//    up to 8 rows through a ring of shared-memory slots (one bulk copy per
+//    stage, mbarrier transaction counts);
+//  * A (all M rows) arrives with one bulk copy after the previous kernel on
+//    the stream completed; the consumers spread each row into the 144-byte
+//    block slots of the quantised slices. The copy lands in the top ring
+//    slots, whose weight stages are issued once A has been spread out;
+//  * the warps form the K-groups x row-groups grid of the GEMV, a row-group
+//    taking whole stages (ring depth a multiple of the row-group count);
+//    every lane holds its chunk of all M activation rows;
+//  * per stage each warp reduces its row partials per token with the
+//    transposed shuffle tree; the stage's finisher adds the K-groups in a
+//    fixed order and writes the M outputs of each row.
+//
+// f32 activations and exact dequantisation: the results meet the GEMV
+// tolerance. Every wait is bounded (LQ_ERR_DEVICE_TIMEOUT on expiry).
+#include <algorithm>
+
+#include "lq_device.cuh"
+#include "lq_gemv_slices.cuh"
+#include "lq_internal.h"
+
+namespace lq {
+namespace {
+
+using namespace gemv;
+
+__device__ unsigned g_batch_err;
+
+constexpr int kBKGroups = 8;   // K-groups at most (reduction buffer width)
+constexpr int kBRows = 8;      // rows per stage at most
+constexpr int kBMaxStages = 16;
+constexpr int kBMaxTokens = 4;
+
+// Warps per CTA, all of them consumers. The f16 slices and the two-token
+// quantised slices fit in 128 registers, so 16 warps; the quantised
+// four-token slices need up to 255, so 8 (two per SM sub-partition).
+__host__ __device__ constexpr int batch_warps(int fmt, int mt) {
+  return fmt == LQ_FMT_F16 || mt == 2 ? 16 : 8;
+}
+
+struct BatchParams {
+  const float* A;
+  const uint8_t* W;
+  float* C;
+  int M, N, K;
+  int row_bytes;
+  int rows_per_stage;     // at most kBRows
+  int stages;             // ring depth, a multiple of nr
+  int early;              // slots below the A staging area (issued at once)
+  int stage_off;          // byte offset of the A staging area in the ring
+  int nk, nr;             // K-groups x row-groups
+  int a_slot;             // bytes of one token's A as the slices read it
+  unsigned long long wait_ns;
+  unsigned wait_iters;
+};
+
+template <int MT>
+struct BatchHeader {
+  uint64_t full[kBMaxStages];
+  uint64_t red_full[kBMaxStages];
+  uint64_t a_bar;
+  int last[kBMaxStages];  // last stage issued into each slot (-1: none)
+  volatile int abort;
+  float red[kBMaxStages][MT][kBRows][kBKGroups];
+};
+template <int MT>
+__host__ __device__ constexpr int batch_header_bytes() {
+  return (static_cast<int>(sizeof(BatchHeader<MT>)) + 127) / 128 * 128;
+}
+
+__device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_batch_err, 0u, code); }
+
+// No producer warp. The ring is refilled by the finisher of a stage: once
+// every K-group has posted its partials for slot s no warp reads the slot's
+// weights any more, and once the finisher has summed the partials its lane 0
+// issues the stage S further on into the slot.
+template <int FMT, int MT>
+__global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kernel(const BatchParams p) {
+  constexpr int NW = batch_warps(FMT, MT);
+  extern __shared__ __align__(1024) uint8_t smem[];
+  BatchHeader<MT>& hd = *reinterpret_cast<BatchHeader<MT>*>(smem);
+  uint8_t* sA = smem + batch_header_bytes<MT>();  // MT x a_slot
+  uint8_t* ring = sA + MT * p.a_slot;
+  uint8_t* stage_a = ring + p.stage_off;          // M x K floats (quantised formats)
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+  const int r0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.N) / G);
+  const int r1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G);
+  const int nrows = r1 - r0;
+  const int RS = p.rows_per_stage, S = p.stages, nk = p.nk, nr = p.nr, active = nk * nr;
+  const int nst = (nrows + RS - 1) / RS;
+  const uint32_t stage_bytes = static_cast<uint32_t>(RS) * p.row_bytes;
+  if (S % nr != 0 || S > kBMaxStages || nk > kBKGroups || active > NW || RS > kBRows || p.M > MT ||
+      p.early > S) {
+    if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
+    return;
+  }
+  const uint8_t* wbase = p.W + static_cast<long long>(r0) * p.row_bytes;
+  auto issue = [&](int st, uint64_t pol) {
+    const int s = st % S;
+    const uint32_t bytes = static_cast<uint32_t>(min(RS, nrows - st * RS)) * p.row_bytes;
+    hd.last[s] = st;
+    mbar_arrive_expect_tx(&hd.full[s], bytes);
+    bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes,
+             wbase + static_cast<long long>(st) * RS * p.row_bytes, bytes, &hd.full[s], pol);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&hd.full[s], 1);
+      mbar_init(&hd.red_full[s], nk);
+      hd.last[s] = -1;
+    }
+    mbar_init(&hd.a_bar, 1);
+    hd.abort = 0;
+    fence_barrier_init();
+    const uint64_t pol = policy_evict_first();
+    for (int st = 0; st < min(nst, p.early); ++st) issue(st, pol);  // weights depend on nothing
+    // A (M rows, contiguous) once the previous kernel on the stream completed
+    pdl_wait();
+    const uint32_t a_bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(p.K) * 4u;
+    mbar_arrive_expect_tx(&hd.a_bar, a_bytes);
+    bulk_g2s(FMT == LQ_FMT_F16 ? sA : stage_a, p.A, a_bytes, &hd.a_bar, policy_evict_last());
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  if (warp < active && nrows > 0) {
+    // One lead thread waits for A under the time limit; the other consumers
+    // follow its verdict (a named barrier has no time limit, so every
+    // consumer has to reach it) and then observe the landed copy themselves.
+    if (threadIdx.x == 0 && !mbar_wait(&hd.a_bar, 0, p.wait_ns, p.wait_iters)) {
+      record_error(kDevErrTimeout);
+      hd.abort = 1;
+    }
+    named_barrier(1, static_cast<uint32_t>(active) * 32u);
+    if (!hd.abort) {
+      if (threadIdx.x != 0) mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
+      pdl_wait();  // returns at once: the previous kernel has completed
+      const uint64_t pol = policy_evict_first();
+      if (FMT != LQ_FMT_F16) {
+        // staging (M rows) -> block slots, token by token
+        const uint32_t sa = smem_u32(sA), sg = smem_u32(stage_a);
+        const int per = p.K / 4;
+        for (int c = warp * 32 + lane; c < p.M * per; c += active * 32) {
+          const int t = c / per, q = c - t * per;
+          const uint4 v = lds128(sg + 16u * c);
+          sts128(sa + static_cast<uint32_t>(t * p.a_slot) +
+                     static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes + 16u * (q & 7),
+                 v);
+        }
+        named_barrier(2, static_cast<uint32_t>(active) * 32u);
+        if (threadIdx.x == 0) {
+          // the staging area is free: the slots it covered get their stages
+          fence_proxy_async_smem();
+          for (int st = p.early; st < min(nst, S); ++st) issue(st, pol);
+        }
+      }
+      const int kg = warp % nk, rg = warp / nk;
+      typename SliceM<FMT, MT>::T sl;
+      sl.init(smem_u32(sA), static_cast<uint32_t>(p.a_slot), kg, lane, p.K);
+      const uint32_t ring_u = smem_u32(ring);
+      for (int st = rg; st < nst; st += nr) {
+        const int s = st % S;
+        const uint32_t ph = (st / S) & 1;
+        if (!mbar_wait(&hd.full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
+          record_error(kDevErrTimeout);
+          hd.abort = 1;
+          break;
+        }
+        const int rows = min(RS, nrows - st * RS);
+        const uint32_t base = ring_u + static_cast<uint32_t>(s) * stage_bytes;
+        float acc[MT][kBRows];
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int r = 0; r < kBRows; ++r) acc[t][r] = 0.f;
+        if (sl.ok) {
+#pragma unroll
+          for (int r = 0; r < kBRows; ++r) {
+            if (r < rows) {
+              float o[MT];
+              sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, o);
+#pragma unroll
+              for (int t = 0; t < MT; ++t) acc[t][r] = o[t];
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          int r;
+          const float v = transpose_reduce8(acc[t], lane, r);
+          if ((lane & 3) == 0) hd.red[s][t][r][kg] = v;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&hd.red_full[s]);
+        if (kg == (st / nr) % nk) {
+          // finisher: adds the K-groups' partials in a fixed order, one
+          // output per token, then refills slot s. The refill comes last: its
+          // landing releases the row-group's next stage in this slot, whose
+          // partials overwrite red[s].
+          if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
+            record_error(kDevErrTimeout);
+            hd.abort = 1;
+            break;
+          }
+          if (lane < rows) {
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+              if (t < p.M) {
+                float sum = 0.f;
+                for (int g = 0; g < nk; ++g) sum += hd.red[s][t][lane][g];
+                p.C[static_cast<long long>(t) * p.N + r0 + st * RS + lane] = sum;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0 && st + S < nst) issue(st + S, pol);
+        }
+      }
+    }
+  }
+  // Every warp gets here (all waits are bounded); no copy may still be in
+  // flight when the CTA exits.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s)
+      if (hd.last[s] >= 0) mbar_wait(&hd.full[s], (hd.last[s] / S) & 1, kDrainWaitNs);
+    mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
+  }
+}
+
+template <int FMT, int MT>
+lq_status launch_batch_t(const MatmulArgs& a, const BatchParams& p, int G, size_t smem) {
+  auto kern = gemv_batch_kernel<FMT, MT>;
+  static int configured[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
+  if (configured[dev] < static_cast<int>(smem)) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return cuda_status(e);
+    configured[dev] = static_cast<int>(smem);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(G));
+  cfg.blockDim = dim3(static_cast<unsigned>(batch_warps(FMT, MT) * 32));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+}  // namespace
+
+unsigned read_clear_batch_error() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_batch_err, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_batch_err, &z, sizeof(z));
+  return v;
+}
+
+lq_status launch_gemv_batch(const MatmulArgs& a) {
+  const int64_t M = a.M, N = a.N, K = a.K;
+  // the streaming GEMV's shapes, one chunk per warp
+  const bool shape_ok = M >= 2 && M <= kBMaxTokens && K <= 16384 && N < (1LL << 30) &&
+                        (a.fmt == LQ_FMT_F16 ? (K % 8 == 0) : (K % 256 == 0));
+  if (!shape_ok || !aligned16(a.A) || !aligned16(a.W)) return LQ_ERR_UNSUPPORTED;
+  int nk;
+  if (a.fmt == LQ_FMT_F16) {
+    const int nch = static_cast<int>((K + 255) / 256);
+    if (nch > kBKGroups) return LQ_ERR_UNSUPPORTED;
+    nk = 1;
+    while (nk < nch) nk *= 2;
+  } else {
+    const int nseg = static_cast<int>((K / 32 + 63) / 64);
+    if (2 * nseg > kBKGroups) return LQ_ERR_UNSUPPORTED;
+    nk = 2 * nseg;
+  }
+  const int MT = M <= 2 ? 2 : 4;
+  const int NW = batch_warps(a.fmt, MT);
+  const DeviceInfo& di = device_info();
+  const int G = static_cast<int>(std::min<int64_t>(N, di.sm_count));
+  const int rb = static_cast<int>(row_bytes(a.fmt, K));
+  const int a_slot = a.fmt == LQ_FMT_F16 ? static_cast<int>(K * 4)
+                                         : static_cast<int>((K / 32 + 63) / 64) * 64 * kASlotBytes;
+  const int a_stage = a.fmt == LQ_FMT_F16 ? 0 : static_cast<int>((M * K * 4 + 127) / 128 * 128);
+  const int hdr = MT == 2 ? batch_header_bytes<2>() : batch_header_bytes<4>();
+  const int budget = std::min(di.max_smem_optin, 227 * 1024) - hdr - MT * a_slot;
+  const int rows_per_cta = static_cast<int>((N + G - 1) / G);
+  if (budget < 2 * rb || budget < a_stage) return LQ_ERR_UNSUPPORTED;
+  // Stage height: as large as 8 rows while two stages fit; then as many
+  // row-groups as there are stages (up to the warps over the K-groups), and
+  // the height balanced so that every row-group gets the same number of
+  // stages. The ring takes as many slots as fit, a multiple of nr and never
+  // more than the CTA's stages rounded up to nr.
+  const int rs_max = std::max(1, std::min({kBRows, budget / (2 * rb), rows_per_cta}));
+  const int need_max = (rows_per_cta + rs_max - 1) / rs_max;
+  int nr = std::max(1, std::min(NW / nk, need_max));
+  const int cap_slots = std::min(kBMaxStages, budget / (rs_max * rb));
+  while (nr > 1 && cap_slots < nr) --nr;
+  const int total = nr * ((need_max + nr - 1) / nr);
+  const int RS = std::max(1, (rows_per_cta + total - 1) / total);
+  const int need = (rows_per_cta + RS - 1) / RS;
+  int S = std::min(kBMaxStages, budget / (RS * rb));
+  S -= S % nr;
+  S = std::min(S, nr * ((need + nr - 1) / nr));
+  if (S < 1) return LQ_ERR_UNSUPPORTED;
+  const int ring = std::max(S * RS * rb, a_stage);
+  BatchParams p = {};
+  p.A = a.A;
+  p.W = static_cast<const uint8_t*>(a.W);
+  p.C = a.C;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.K = static_cast<int>(K);
+  p.row_bytes = rb;
+  p.rows_per_stage = RS;
+  p.nk = nk;
+  p.nr = nr;
+  p.stages = S;
+  p.a_slot = a_slot;
+  // A staging at the top of the ring (128-byte aligned): the slots wholly
+  // below it are issued at once, the others after A has been spread out
+  p.stage_off = a_stage ? (ring - a_stage) / 128 * 128 : 0;
+  p.early = a_stage ? std::min(S, p.stage_off / (RS * rb)) : S;
+  p.wait_ns = wait_limit_ns();
+  p.wait_iters = wait_limit_iters();
+  const size_t smem = static_cast<size_t>(hdr) + MT * static_cast<size_t>(a_slot) + ring;
+  lq_status st;
+  if (a.fmt == LQ_FMT_F16)
+    st = MT == 2 ? launch_batch_t<LQ_FMT_F16, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_F16, 4>(a, p, G, smem);
+  else if (a.fmt == LQ_FMT_Q8_0)
+    st = MT == 2 ? launch_batch_t<LQ_FMT_Q8_0, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_Q8_0, 4>(a, p, G, smem);
+  else
+    st = MT == 2 ? launch_batch_t<LQ_FMT_Q4_0, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_Q4_0, 4>(a, p, G, smem);
+  if (st == LQ_OK) count_route(1);
+  return st;
+}
+
+}  // namespace lq

@@ -1,0 +1,131 @@
+"""The batched decode kernel (M = 2..4 rows of A, route 1) against the oracle.
+
+The kernel keeps f32 activations and dequantises W exactly, so every element
+is held to the GEMV tolerance (1e-4 * sum|a*w| + 1e-6), not the tensor-core
+one. Shapes cover several stages per CTA with a ragged last stage, fewer rows
+than SMs, the K limits of the kernel and the fallbacks beyond them (shapes it
+refuses go to the tensor-core or the generic kernel and still match).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synthetic
+from helpers import check, nan_filled, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(lq, dev, fmt, W, A, A_dev=None):
+    N, K = W.shape
+    M = A.shape[0]
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
+    C = nan_filled(M, N, dev)
+    getattr(lq, f"lq_gemm_{fmt}")(A.to(dev) if A_dev is None else A_dev, Wd, C, M, N, K)
+    torch.cuda.synchronize()
+    assert lq.last_device_error() == lq.LQ_OK
+    return C.cpu().numpy()
+
+
+def _ref(fmt, W, A):
+    N, K = W.shape
+    return O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K)
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("N,K", [(5, 512), (1000, 256), (4133, 2048), (2437, 1024)])
+def test_batch_matches_oracle(lq, cuda_dev, fmt, M, N, K):
+    W, A = synthetic.draw(M, N, K, seed=7 * M + N + K, outlier_frac=0.05)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} {M}x{N}x{K}")
+    assert lq.route_count(1) == 1
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 4, 20000, 2048), ("q4_0", 4, 16000, 4096),
+                                       ("f16", 4, 20000, 2048), ("q8_0", 2, 8192, 8192),
+                                       ("q4_0", 3, 30000, 1024)])
+def test_batch_ring_refills(lq, cuda_dev, fmt, M, N, K):
+    """More stages per CTA than ring slots: slots are refilled by the stage's
+    finisher while other row-groups compute, and each refill's partials reuse
+    the slot's reduction buffer."""
+    W, A = synthetic.draw(M, N, K, seed=N + K, outlier_frac=0.05)
+    lq.reset_counts()
+    for _ in range(3):  # the same result on every run
+        C = _run(lq, cuda_dev, fmt, W, A)
+        y, tol = _ref(fmt, W, A)
+        check(C, y, tol, f"{fmt} {M}x{N}x{K}")
+    assert lq.route_count(1) == 3
+
+
+@pytest.mark.parametrize("fmt,K", [("f16", 1000), ("f16", 2048), ("q8_0", 4096), ("q4_0", 4096),
+                                   ("q8_0", 8192), ("q4_0", 8192)])
+def test_batch_k_limits(lq, cuda_dev, fmt, K):
+    # M = 2 fits up to the limit; K = 8192 with four rows of A does not fit
+    # shared memory (activations kept twice) and falls back to the tensor cores
+    for M in (2, 4):
+        W, A = synthetic.draw(M, 1536, K, seed=K + M, outlier_frac=0.05 if K % 32 == 0 else 0.0)
+        lq.reset_counts()
+        C = _run(lq, cuda_dev, fmt, W, A)
+        fits = not (M == 4 and K == 8192)
+        if fits:
+            y, tol = _ref(fmt, W, A)
+            assert lq.route_count(1) == 1
+        else:
+            N = W.shape[0]
+            y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+            assert lq.route_count(1) == 0
+        check(C, y, tol, f"{fmt} {M}x1536x{K}")
+
+
+@pytest.mark.parametrize("fmt,K", [("f16", 4096), ("q8_0", 16384), ("q4_0", 320)])
+def test_batch_refused_shapes_fall_back(lq, cuda_dev, fmt, K):
+    W, A = synthetic.draw(3, 640, K, seed=K, outlier_frac=0.0)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    N = W.shape[0]
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+    check(C, y, tol, f"{fmt} 3x640x{K}")
+    assert lq.route_count(1) == 0
+
+
+def test_batch_unaligned_a_falls_back(lq, cuda_dev):
+    fmt, M, N, K = "q8_0", 2, 700, 1024
+    W, A = synthetic.draw(M, N, K, seed=11)
+    buf = torch.empty(M * K + 1, dtype=torch.float32, device=cuda_dev)
+    buf[1:] = A.reshape(-1).to(cuda_dev)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A, A_dev=buf[1:])
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+    check(C, y, tol, "A at a 4-byte offset")
+    assert lq.route_count(1) == 0
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_batch_crossover_config_m2(lq, cuda_dev, fmt):
+    w = synthetic.WORKLOADS[f"gemm_{fmt}_m2_6144x2048"]
+    W, A = synthetic.draw_workload(w)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, w.name)
+    assert lq.route_count(1) == 1
+
+
+def test_batch_rows_equal_gemv(lq, cuda_dev):
+    """Each row of the batched result agrees with the GEMV of that row of A
+    within twice the GEMV tolerance (the two kernels add in different
+    orders)."""
+    fmt, M, N, K = "q4_0", 4, 1200, 2048
+    W, A = synthetic.draw(M, N, K, seed=12)
+    C = _run(lq, cuda_dev, fmt, W, A)
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), cuda_dev)
+    _, tol = _ref(fmt, W, A)
+    for m in range(M):
+        g = nan_filled(1, N, cuda_dev)
+        lq.lq_gemv_q4_0(A[m:m + 1].contiguous().to(cuda_dev), Wd, g, 1, N, K)
+        torch.cuda.synchronize()
+        assert np.all(np.abs(g.cpu().numpy()[0] - C[m]) <= 2 * tol[m])

@@ -47,7 +47,11 @@ def test_tc_single_tile_single_kstep(lq, cuda_dev, fmt):
 def test_tc_shapes(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=M + N + K, outlier_frac=0.05)
     lq.reset_counts()
-    C = _run(lq, cuda_dev, fmt, W, A)
+    lq.force_route(lq.ROUTE_TENSOR_CORE)  # M <= 4 would take the batched decode kernel
+    try:
+        C = _run(lq, cuda_dev, fmt, W, A)
+    finally:
+        lq.force_route(0)
     y, tol = _ref(fmt, W, A)
     check(C, y, tol, f"{fmt} {M}x{N}x{K}")
     assert lq.route_count(2) == 1
