@@ -43,7 +43,8 @@ import synthetic  # noqa: E402
 
 HEADLINE = "gemv_q8_0_4096x4096"
 KERNEL_OF_MODE = {"chain": "gemv_chain_kernel", "chain-dependent": "gemv_chain_kernel",
-                  "calls": "gemv_stream_kernel"}
+                  "calls": "gemv_stream_kernel", "argmax": "gemv_stream_kernel",
+                  "argmax-unfused": "gemv_stream_kernel"}
 METRIC = "decode GEMV achieved HBM GB/s (% of peak); prefill GEMM TFLOP/s (% peak)"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -155,7 +156,9 @@ class Workbench:
                  mode="auto"):
         """mode: "calls" (one lq_matmul per copy), "chain" (one lq_gemv_chain
         over the independent copies), "chain-dependent" (every problem waits
-        for the previous one), or "auto" (chain for M = 1, else calls)."""
+        for the previous one), "argmax" (M = 1: one lq_gemv_argmax per copy,
+        logits not stored), "argmax-unfused" (M = 1: lq_matmul into C, then
+        lq_argmax_f32 on C), or "auto" (chain for M = 1, else calls)."""
         self.lq, self.w, self.dev = lq, w, dev
         W, A = synthetic.draw_workload(w)
         packed = lq.pack(w.fmt, W).reshape(-1).view(np.uint8)
@@ -187,9 +190,17 @@ class Workbench:
                 self.problems = None  # outside the chain's path: separate calls
             torch.cuda.synchronize(dev)
         self.mode = mode if self.problems is not None else "calls"
+        self.res = None
+        if mode.startswith("argmax") and w.M == 1:
+            self.mode = mode
+            self.res = torch.zeros((R, 3), dtype=torch.int64, device=dev)
         # kernels of ours per step
-        self.kernels_per_step = (len(self.problems) if self.problems is not None
-                                 else R * (2 if w.M >= 2 else 1))
+        if self.problems is not None:
+            self.kernels_per_step = len(self.problems)
+        elif self.mode == "argmax-unfused" or w.M >= 2:
+            self.kernels_per_step = 2 * R
+        else:
+            self.kernels_per_step = R
 
     def step(self, stream=None):
         w = self.w
@@ -197,8 +208,14 @@ class Workbench:
             for arr in self.problems:
                 self.lq.lq_gemv_chain(w.fmt, arr, stream)
             return
+        if self.mode == "argmax":
+            for r in range(self.R):
+                self.lq.lq_gemv_argmax(w.fmt, self.Ad[r], self.Wd[r], None, w.N, w.K, self.res[r], stream)
+            return
         for r in range(self.R):
             self.fn(self.Ad[r], self.Wd[r], self.Cd[r], w.M, w.N, w.K, stream)
+            if self.mode == "argmax-unfused":
+                self.lq.lq_argmax_f32(self.Cd[r], w.N, self.res[r], stream)
 
     def capture(self):
         s = torch.cuda.Stream(device=self.dev)
@@ -433,6 +450,9 @@ def main():
     runs = [(name, "auto") for name in names if name != w.name]
     if w.M == 1 and args.extras != "none":
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
+    lmhead = "gemv_f16_lmhead_151936x2048"
+    if lmhead in names or (w.name == lmhead and args.extras != "none"):
+        runs += [(lmhead, "argmax"), (lmhead, "argmax-unfused")]
     for name, mode in runs:
         x = synthetic.WORKLOADS[name]
         xb = Workbench(lq, x, dev, mode=mode)

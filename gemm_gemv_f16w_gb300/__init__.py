@@ -35,6 +35,7 @@ EXPORTS = [
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
+    "lq_gemv_argmax", "lq_argmax_f32",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -89,6 +90,10 @@ def lib() -> ctypes.CDLL:
         L.lq_debug_gemv_plan.restype = st
         L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
         L.lq_gemm_noalloc.restype = st
+        L.lq_gemv_argmax.argtypes = [st, vp, vp, vp, i64, i64, vp, vp]
+        L.lq_gemv_argmax.restype = st
+        L.lq_argmax_f32.argtypes = [vp, i64, vp, vp]
+        L.lq_argmax_f32.restype = st
         _lib = L
     return _lib
 
@@ -181,6 +186,35 @@ def lq_gemm_noalloc(fmt, A, W, C, M, N, K, stream=None):
     f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
     _check(lib().lq_gemm_noalloc(f, _ptr(A), _ptr(W), _ptr(C), int(M), int(N), int(K),
                                  _stream(stream)), "lq_gemm_noalloc")
+
+
+# ---- argmax ---------------------------------------------------------------
+ARGMAX_RESULT_BYTES = 24  # sizeof(lq_argmax_result): value, index, 16 bytes of work
+
+
+def argmax_result(dev=None):
+    """A device buffer for one lq_argmax_result (int64 x 3, 8-byte aligned)."""
+    import torch
+    return torch.zeros(3, dtype=torch.int64, device=dev or "cuda")
+
+
+def read_argmax(res):
+    """(value, index) of an lq_argmax_result buffer (synchronises)."""
+    raw = res.detach().cpu().numpy().view(np.uint8)
+    return float(raw[0:4].view(np.float32)[0]), int(raw[4:8].view(np.int32)[0])
+
+
+def lq_gemv_argmax(fmt, A, W, C, N, K, out, stream=None):
+    """Fused GEMV (M = 1) + argmax into the device lq_argmax_result `out`
+    (argmax_result()); C may be None. See include/lq.h."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib().lq_gemv_argmax(f, _ptr(A), _ptr(W), _ptr(C), int(N), int(K), _ptr(out),
+                                _stream(stream)), "lq_gemv_argmax")
+
+
+def lq_argmax_f32(x, n, out, stream=None):
+    """Argmax of n device floats into the device lq_argmax_result `out`."""
+    _check(lib().lq_argmax_f32(_ptr(x), int(n), _ptr(out), _stream(stream)), "lq_argmax_f32")
 
 
 # ---- host packers --------------------------------------------------------

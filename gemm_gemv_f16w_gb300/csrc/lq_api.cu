@@ -208,6 +208,33 @@ lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, voi
   return lq::launch_gemv_chain(fmt, problems, count, static_cast<cudaStream_t>(stream));
 }
 
+lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C, int64_t N, int64_t K,
+                         lq_argmax_result* out, void* stream) {
+  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (N < 1 || N >= (1LL << 30)) return LQ_ERR_INVALID_ARG;
+  if (!out || !aligned_to(out, 8)) return LQ_ERR_INVALID_ARG;
+  float* C_check = C ? C : reinterpret_cast<float*>(out);  // C may be null
+  bool noop;
+  lq_status st = validate(fmt, A, W, C_check, 1, N, K, &noop);
+  if (st != LQ_OK) return st;
+  MatmulArgs a{A, W, C, 1, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  if (g_force_route.load() != 3) {
+    st = launch_gemv_argmax(a, out);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
+  // unfused: the GEMV into C, then the argmax of C
+  if (!C) return LQ_ERR_UNSUPPORTED;
+  st = g_force_route.load() == 3 ? launch_gemv_generic(a) : launch_gemv(a);
+  if (st != LQ_OK) return st;
+  return launch_argmax_f32(C, N, out, a.stream);
+}
+
+lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* stream) {
+  if (!x || !aligned_to(x, 4) || n < 1 || n >= (1LL << 31)) return LQ_ERR_INVALID_ARG;
+  if (!out || !aligned_to(out, 8)) return LQ_ERR_INVALID_ARG;
+  return launch_argmax_f32(x, n, out, static_cast<cudaStream_t>(stream));
+}
+
 const char* lq_version(void) { return "lq 0.1.0 (sm_103a)"; }
 
 lq_status lq_debug_force_route(int route) {

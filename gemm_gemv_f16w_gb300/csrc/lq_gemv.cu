@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <atomic>
 
+#include "lq_argmax.cuh"
 #include "lq_device.cuh"
 #include "lq_gemv_slices.cuh"
 #include "lq_internal.h"
@@ -66,6 +67,8 @@ struct GemvParams {
   int l2_prefetch;           // prefetch the rows beyond the first ring-full into L2
   unsigned long long wait_ns;
   unsigned wait_iters;
+  lq_argmax_result* amax;    // argmax variant: the result (C may then be null)
+  unsigned amax_warps;       // argmax variant: consumer warps of the grid
 };
 
 struct Header {
@@ -89,8 +92,12 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_gemv_
 // of its stage released it (empty barrier, after the stage's finisher read
 // the slot's reduction buffer), so a waiter sees either the phase it waits
 // for or the one before it, never an older one.
+//
+// AMAX adds the argmax of the outputs (lq_gemv_argmax): a finisher lane
+// ranks each row it writes, and every consumer warp merges its best row into
+// the result once its stages are done (lq_argmax.cuh).
 // ---------------------------------------------------------------------------
-template <int FMT, int CPW>
+template <int FMT, int CPW, bool AMAX>
 __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     gemv_stream_kernel(const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -205,6 +212,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
   typename SliceOf<FMT, CPW>::T sl;
   sl.init(smem_u32(sA), kg, nk, lane, p.K);
   const uint32_t ring_u = smem_u32(ring);
+  unsigned long long best = 0ull;  // argmax variant: this lane's best row
   for (int st = rg; st < nst; st += nr) {
     const int s = st % S;
     const uint32_t ph = (st / S) & 1;
@@ -241,12 +249,20 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       if (lane < rows) {
         float sum = 0.f;
         for (int g = 0; g < nk; ++g) sum += hd.red[s][lane][g];
-        p.C[r0 + st * RS + lane] = sum;
+        const int row = r0 + st * RS + lane;
+        if constexpr (AMAX) {
+          const unsigned long long key = amax::make_key(sum, static_cast<unsigned>(row));
+          best = key > best ? key : best;
+          if (p.C) p.C[row] = sum;
+        } else {
+          p.C[row] = sum;
+        }
       }
       __syncwarp();
     }
     if (lane == 0) mbar_arrive(&hd.empty[s]);
   }
+  if constexpr (AMAX) amax::warp_done(best, p.amax, p.amax_warps, lane);
 }
 
 // ---------------------------------------------------------------------------
@@ -351,9 +367,9 @@ WarpGrid pick_grid(int fmt, int K) {
   return g;
 }
 
-template <int FMT, int CPW>
+template <int FMT, int CPW, bool AMAX>
 lq_status launch_stream_t(const MatmulArgs& a, const GemvParams& p, int G, size_t smem) {
-  auto kern = gemv_stream_kernel<FMT, CPW>;
+  auto kern = gemv_stream_kernel<FMT, CPW, AMAX>;
   static int configured_smem[kMaxDevices] = {};  // per instantiation and device
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -368,17 +384,17 @@ lq_status launch_stream_t(const MatmulArgs& a, const GemvParams& p, int G, size_
   return cuda_status(e);
 }
 
-template <int FMT>
+template <int FMT, bool AMAX>
 lq_status launch_stream_fmt(const MatmulArgs& a, int cpw, const GemvParams& p, int G, size_t smem) {
   if constexpr (FMT != LQ_FMT_F16) {
-    return cpw == 1 ? launch_stream_t<FMT, 1>(a, p, G, smem)
-                    : (cpw == 2 ? launch_stream_t<FMT, 2>(a, p, G, smem) : LQ_ERR_UNSUPPORTED);
+    return cpw == 1 ? launch_stream_t<FMT, 1, AMAX>(a, p, G, smem)
+                    : (cpw == 2 ? launch_stream_t<FMT, 2, AMAX>(a, p, G, smem) : LQ_ERR_UNSUPPORTED);
   } else {
     switch (cpw) {
-      case 1: return launch_stream_t<FMT, 1>(a, p, G, smem);
-      case 2: return launch_stream_t<FMT, 2>(a, p, G, smem);
-      case 4: return launch_stream_t<FMT, 4>(a, p, G, smem);
-      case 8: return launch_stream_t<FMT, 8>(a, p, G, smem);
+      case 1: return launch_stream_t<FMT, 1, AMAX>(a, p, G, smem);
+      case 2: return launch_stream_t<FMT, 2, AMAX>(a, p, G, smem);
+      case 4: return launch_stream_t<FMT, 4, AMAX>(a, p, G, smem);
+      case 8: return launch_stream_t<FMT, 8, AMAX>(a, p, G, smem);
       default: return LQ_ERR_UNSUPPORTED;
     }
   }
@@ -497,10 +513,11 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_
   return pl;
 }
 
+template <bool AMAX>
 lq_status launch_plan(const MatmulArgs& a, const GemvPlan& pl) {
-  if (a.fmt == LQ_FMT_F16) return launch_stream_fmt<LQ_FMT_F16>(a, pl.cpw, pl.p, pl.grid, pl.smem);
-  if (a.fmt == LQ_FMT_Q8_0) return launch_stream_fmt<LQ_FMT_Q8_0>(a, pl.cpw, pl.p, pl.grid, pl.smem);
-  return launch_stream_fmt<LQ_FMT_Q4_0>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  if (a.fmt == LQ_FMT_F16) return launch_stream_fmt<LQ_FMT_F16, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  if (a.fmt == LQ_FMT_Q8_0) return launch_stream_fmt<LQ_FMT_Q8_0, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  return launch_stream_fmt<LQ_FMT_Q4_0, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
 }
 
 std::atomic<int> g_tune_ctas{0}, g_tune_rows{0}, g_tune_smem{0};
@@ -513,7 +530,11 @@ void set_gemv_tuning(int ctas_per_sm, int rows_per_stage, int smem_cap) {
   g_tune_smem.store(smem_cap);
 }
 
-lq_status launch_gemv(const MatmulArgs& a) {
+namespace {
+
+// The launch plan launch_gemv uses (ok == false: the shape or the alignment
+// is outside the streaming kernel's fast path).
+GemvPlan plan_for(const MatmulArgs& a) {
   const WarpGrid wg = pick_grid(a.fmt, static_cast<int>(std::min<int64_t>(a.K, kGemvFastMaxK)));
   const DeviceInfo& di = device_info();
   // Kernels with one or two chunks per warp fit in half an SM (registers
@@ -533,9 +554,30 @@ lq_status launch_gemv(const MatmulArgs& a) {
   GemvPlan pl = plan_gemv(a, ctas, rows, smem_cap);
   // very long rows: two stages need more than half an SM
   if (!pl.ok) pl = plan_gemv(a, 1, kRowsPerStage, di.max_smem_optin);
+  return pl;
+}
+
+}  // namespace
+
+lq_status launch_gemv(const MatmulArgs& a) {
+  const GemvPlan pl = plan_for(a);
   if (!pl.ok) return launch_gemv_generic(a);
-  const lq_status st = launch_plan(a, pl);
+  const lq_status st = launch_plan<false>(a, pl);
   if (st == LQ_ERR_UNSUPPORTED) return launch_gemv_generic(a);
+  if (st == LQ_OK) count_route(0);
+  return st;
+}
+
+lq_status launch_gemv_argmax(const MatmulArgs& a, lq_argmax_result* out) {
+  GemvPlan pl = plan_for(a);
+  if (!pl.ok) return LQ_ERR_UNSUPPORTED;
+  // every CTA owns at least one row (grid <= N), so every consumer warp of
+  // the grid reaches the merge
+  pl.p.amax = out;
+  pl.p.amax_warps = static_cast<unsigned>(pl.grid) * static_cast<unsigned>(pl.p.nk * pl.p.nr);
+  cudaError_t e = cudaMemsetAsync(out->work, 0, sizeof(out->work), a.stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  const lq_status st = launch_plan<true>(a, pl);
   if (st == LQ_OK) count_route(0);
   return st;
 }

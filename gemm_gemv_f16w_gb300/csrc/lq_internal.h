@@ -63,6 +63,12 @@ int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
 void set_gemm_rings(int a_stages, int raw_stages);
 
+// Argmax (lq_gemv_argmax, lq_argmax_f32). launch_gemv_argmax returns
+// LQ_ERR_UNSUPPORTED, launching nothing, outside the streaming GEMV's fast
+// path. Both zero out->work on the stream first.
+lq_status launch_gemv_argmax(const MatmulArgs& a, lq_argmax_result* out);
+lq_status launch_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, cudaStream_t stream);
+
 // Decode chain (lq_gemv_chain); LQ_ERR_UNSUPPORTED when the problems do not
 // fit its fast path.
 lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, cudaStream_t stream);

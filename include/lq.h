@@ -165,6 +165,45 @@ lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, voi
 lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, float* C,
                           int64_t M, int64_t N, int64_t K, void* stream);
 
+/* ---- argmax: LM-head GEMV fused with the selection of its best row --------
+ * lm_head block-top-k stage 1 and 2 (lattice-inference, src/forward/
+ * metal_qwen35/inner/dispatch.rs: dispatch_lm_head_block_stage1_enc,
+ * dispatch_block_topk_merge_enc) for k = 1, with the candidate order of
+ * topk_better and the merge of logits_argmax_first / logits_argmax_merge
+ * (lattice-inference 0.1.2, src/forward/metal_qwen35.rs):
+ *   index = the n with the largest y[n]; equal values -> the lowest n;
+ *   NaN is never chosen; -0 and +0 are equal (a winning zero is reported
+ *   as +0). If every y[n] is NaN the result is the pages' sentinel:
+ *   value = -inf, index = -1.
+ * `out` is a DEVICE pointer to one caller-owned lq_argmax_result, 8-byte
+ * aligned. The call zeroes its work words on `stream` before the kernel and
+ * writes value and index when the kernel completes; work is undefined
+ * afterwards. Calls in flight at the same time need distinct results. */
+typedef struct {
+  float    value;    /* y[index], or -inf when nothing was chosen */
+  int32_t  index;    /* the chosen row, or -1 */
+  uint64_t work[2];  /* scratch of the call */
+} lq_argmax_result;
+
+/* y = A W^T for M = 1 (A: K floats; W: N rows in format `fmt`, as for
+ * lq_gemv_<fmt>), then the argmax of y, in one kernel: each row's output is
+ * ranked where it is produced and the per-warp winners are merged with one
+ * 64-bit atomic each. C (N floats, device) receives y when non-NULL; with C
+ * NULL the logits are never stored.
+ *   - N >= 1 and N < 2^30, else LQ_ERR_INVALID_ARG; K as for lq_gemv_<fmt>.
+ *   - Shapes outside the streaming GEMV's fast path (K or alignment) run the
+ *     GEMV into C followed by lq_argmax_f32 on C; with C NULL they return
+ *     LQ_ERR_UNSUPPORTED and launch nothing.
+ *   - A device-side timeout (lq_last_device_error) leaves `out` unwritten. */
+lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C,
+                         int64_t N, int64_t K, lq_argmax_result* out, void* stream);
+
+/* The argmax of x[0 .. n-1] (device floats), the same order and result as
+ * lq_gemv_argmax: the unfused pair logits_argmax_first + logits_argmax_merge
+ * of the pages as one launch. n >= 1 and n < 2^31, else LQ_ERR_INVALID_ARG;
+ * x 4-byte aligned. */
+lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* stream);
+
 /* ---- status ---------------------------------------------------------- */
 const char* lq_status_string(lq_status s);
 /* Synchronises the current device, then reads and clears its device status

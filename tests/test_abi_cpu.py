@@ -132,3 +132,22 @@ def test_route_hooks(lq):
     lq.force_route(0)
     lq.reset_counts()
     assert all(lq.route_count(r) == 0 for r in range(4))
+
+
+def test_argmax_argument_errors_return_before_launch(lq):
+    L = lq.lib()
+    a, w, c, out = 0x10000, 0x20000, 0x30000, 0x40000
+    # never dereferenced: every call below fails validation
+    assert L.lq_gemv_argmax(0, a, w, c, 0, 64, out, 0) == lq.LQ_ERR_INVALID_ARG      # N == 0
+    assert L.lq_gemv_argmax(0, a, w, c, 1 << 30, 64, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_argmax(7, a, w, c, 8, 64, out, 0) == lq.LQ_ERR_INVALID_ARG      # format
+    assert L.lq_gemv_argmax(0, a, w, c, 8, 64, None, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_argmax(0, a, w, c, 8, 64, out + 4, 0) == lq.LQ_ERR_INVALID_ARG  # 8-byte alignment
+    assert L.lq_gemv_argmax(1, a, w, c, 8, 48, out, 0) == lq.LQ_ERR_INVALID_ARG      # K % 32
+    assert L.lq_gemv_argmax(0, None, w, c, 8, 64, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_argmax(0, a, w, c + 2, 8, 64, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_argmax_f32(c, 0, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_argmax_f32(c, 1 << 31, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_argmax_f32(None, 8, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_argmax_f32(c + 2, 8, out, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_argmax_f32(c, 8, out + 4, 0) == lq.LQ_ERR_INVALID_ARG
