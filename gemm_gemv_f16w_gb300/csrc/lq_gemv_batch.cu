@@ -26,7 +26,7 @@
 #include <algorithm>
 
 #include "lq_device.cuh"
-#include "lq_gemv_slices.cuh"
+#include "lq_gemv_slices_batch.cuh"
 #include "lq_internal.h"
 
 namespace lq {

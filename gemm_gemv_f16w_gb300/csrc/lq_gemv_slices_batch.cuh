@@ -1,0 +1,186 @@
+// Multi-token slices of the batched decode kernel (lq_gemv_batch.cu): the
+// lane mapping of the one-token slices in lq_gemv_slices.cuh, with the weights
+// dequantised once and multiplied with up to four activation rows.
+#pragma once
+#include "lq_gemv_slices.cuh"
+
+namespace lq {
+namespace gemv {
+
+// ---------------------------------------------------------------------------
+// Multi-token slices for the batched decode kernel (M = 2..4 activation
+// rows): the lane mapping of the one-token slices, one chunk per warp, the
+// weights dequantised once and multiplied with MT activation rows. Token t's
+// activations sit at sA + t * a_stride in the layout of the one-token slice.
+// ---------------------------------------------------------------------------
+template <int MT>
+struct F16SliceM {
+  float2 a[MT][4];
+  uint32_t off;
+  bool ok;
+  __device__ __forceinline__ void init(uint32_t sA, uint32_t a_stride, int kg, int lane, int K) {
+    const int nch = (K + 255) / 256;
+    const int e = 256 * kg + 8 * lane;
+    ok = kg < nch && e < K;
+    off = 2u * static_cast<uint32_t>(e);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const uint32_t src = sA + a_stride * t + 4u * e;
+      const float4 x = ok ? lds128f(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 y = ok ? lds128f(src + 16u) : make_float4(0.f, 0.f, 0.f, 0.f);
+      a[t][0] = make_float2(x.x, x.y);
+      a[t][1] = make_float2(x.z, x.w);
+      a[t][2] = make_float2(y.x, y.y);
+      a[t][3] = make_float2(y.z, y.w);
+    }
+  }
+  __device__ __forceinline__ void dot(uint32_t row, float (&out)[MT]) const {
+    const uint4 v = lds128(row + off);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+    const float2 f2 = __half22float2(*reinterpret_cast<const __half2*>(&v.z));
+    const float2 f3 = __half22float2(*reinterpret_cast<const __half2*>(&v.w));
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float2 acc = ffma2(f0, a[t][0], make_float2(0.f, 0.f));
+      float2 acc1 = ffma2(f1, a[t][1], make_float2(0.f, 0.f));
+      acc = ffma2(f2, a[t][2], acc);
+      acc1 = ffma2(f3, a[t][3], acc1);
+      out[t] = (acc.x + acc1.x) + (acc.y + acc1.y);
+    }
+  }
+};
+
+// Q8_0 / Q4_0: one whole block per lane (see Q8Slice / Q4Slice for the
+// mapping and the bank argument); the block's 32 values are dequantised into
+// registers once, then dotted with each token's 32 activations.
+template <int MT>
+struct Q8SliceM {
+  float2 a[MT][16];
+  uint32_t woff;
+  bool odd, ok;
+  __device__ __forceinline__ void init(uint32_t sA, uint32_t a_stride, int kg, int lane, int K) {
+    const int seg = kg >> 1, par = kg & 1;
+    const int b = 64 * seg + 2 * lane + par;
+    ok = b < K / 32;
+    odd = par != 0;
+    woff = 2176u * seg + 68u * lane + (par ? 32u : 0u);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const uint32_t src = sA + a_stride * t + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = ok ? lds128f(src + 16u * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[t][2 * u] = make_float2(x.x, x.y);
+        a[t][2 * u + 1] = make_float2(x.z, x.w);
+      }
+    }
+  }
+  template <bool ODD>
+  __device__ __forceinline__ void dot_par(uint32_t row, float (&out)[MT]) const {
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = lds32(row + woff + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    const float2 mb = make_float2(-kMagicS8, -kMagicS8);
+    float2 q[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t x = (ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u)) ^ 0x80808080u;
+      q[2 * i] = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
+      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i & 3] = ffma2(q[i], a[t][i], acc[i & 3]);
+      const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+      out[t] = d * (s.x + s.y);
+    }
+  }
+  __device__ __forceinline__ void dot(uint32_t row, float (&out)[MT]) const {
+    if (odd)
+      dot_par<true>(row, out);
+    else
+      dot_par<false>(row, out);
+  }
+};
+
+template <int MT>
+struct Q4SliceM {
+  float2 a[MT][16];  // pair j: (a_j, a_{16+j})
+  uint32_t woff;
+  bool odd, ok;
+  __device__ __forceinline__ void init(uint32_t sA, uint32_t a_stride, int kg, int lane, int K) {
+    const int seg = kg >> 1, par = kg & 1;
+    const int b = 64 * seg + 2 * lane + par;
+    ok = b < K / 32;
+    odd = par != 0;
+    woff = 1152u * seg + 36u * lane + (par ? 16u : 0u);
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      const uint32_t src = sA + a_stride * t + static_cast<uint32_t>(a_slot_q(b)) * kASlotBytes;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 lo = ok ? lds128f(src + 16u * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 hi = ok ? lds128f(src + 64u + 16u * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+        a[t][4 * u] = make_float2(lo.x, hi.x);
+        a[t][4 * u + 1] = make_float2(lo.y, hi.y);
+        a[t][4 * u + 2] = make_float2(lo.z, hi.z);
+        a[t][4 * u + 3] = make_float2(lo.w, hi.w);
+      }
+    }
+  }
+  template <bool ODD>
+  __device__ __forceinline__ void dot_par(uint32_t row, float (&out)[MT]) const {
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff + 4u * i);
+    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    const float2 s01 = make_float2(1.0f, 0.0625f), c01 = make_float2(-8388616.0f, -524296.0f);
+    const float2 s23 = make_float2(0.00390625f, 0.000244140625f), c23 = make_float2(-32776.0f, -2056.0f);
+    float2 q[16];  // pair j: (q_j - 8, q_{16+j} - 8)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t y = x >> (16 * h);
+        q[4 * i + 2 * h] = ffma2(make_float2(__uint_as_float((y & 0x000Fu) | 0x4B000000u),
+                                             __uint_as_float((y & 0x00F0u) | 0x4B000000u)),
+                                 s01, c01);
+        q[4 * i + 2 * h + 1] = ffma2(make_float2(__uint_as_float((y & 0x0F00u) | 0x4B000000u),
+                                                 __uint_as_float((y & 0xF000u) | 0x4B000000u)),
+                                     s23, c23);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i & 3] = ffma2(q[i], a[t][i], acc[i & 3]);
+      const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+      out[t] = d * (s.x + s.y);
+    }
+  }
+  __device__ __forceinline__ void dot(uint32_t row, float (&out)[MT]) const {
+    if (odd)
+      dot_par<true>(row, out);
+    else
+      dot_par<false>(row, out);
+  }
+};
+
+template <int FMT, int MT>
+struct SliceM;
+template <int MT> struct SliceM<LQ_FMT_F16, MT> { using T = F16SliceM<MT>; };
+template <int MT> struct SliceM<LQ_FMT_Q8_0, MT> { using T = Q8SliceM<MT>; };
+template <int MT> struct SliceM<LQ_FMT_Q4_0, MT> { using T = Q4SliceM<MT>; };
+
+}  // namespace gemv
+}  // namespace lq
