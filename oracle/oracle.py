@@ -38,7 +38,8 @@ its reason in the design notes):
 * The f16 scale is stored little-endian.
 
 Parity pins: every function here is pinned by ``tests/test_oracle_*.py`` to
-closed forms, hand-derived golden bytes, library conversions and brute force.
+closed forms, hand-derived golden bytes, library conversions and brute force
+(the epilogues against scipy's logistic function and exact integer cases).
 No function is "parity unpinned".
 """
 from __future__ import annotations
@@ -371,6 +372,60 @@ def reference(fmt: str, A, packed, N: int, K: int, tensor_core: bool = False):
         rtol, atol = GEMV_RTOL, GEMV_ATOL
     y, B = matmul_ref(A, W_hat)
     return y, rtol * B + atol
+
+
+# --------------------------------------------------------------------------
+# epilogues: residual add and gate/up SwiGLU
+# (oxibonsai-kernels 0.1.4, src/gpu_backend/metal_prefill/functions.rs:
+# gemm_q1_v7_residual writes W x + hidden back into hidden;
+# fused_gate_up_swiglu_gemm runs on the gate_up weight of 2 * inter rows and
+# expands, without the fused kernel, to a GEMM with n_rows = 2 * inter and
+# batched_swiglu. lattice-inference 0.1.2, metal_qwen35.rs: silu_mul, the
+# product silu(gate) * up with silu(g) = g / (1 + exp(-g)); lattice-inference
+# dispatch.rs: dispatch_silu_mul_fused over [gate | up] of one token, and
+# dispatch_gemm_at, gate rows first and up rows after them in gate_up.)
+# --------------------------------------------------------------------------
+F32_EPS = 2.0 ** -24          # unit roundoff of float32
+SILU_LIPSCHITZ = 1.0999       # max over x of |d silu(x) / dx| (1.0998 near x = 2.40)
+
+
+def silu(x):
+    """silu(x) = x / (1 + exp(-x)) in float64, as silu_mul writes it; for
+    x below about -709 exp overflows and the quotient is -0, the limit."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def residual_reference(y, tol, R):
+    """(c_ref, tol) for C = A W^T + R given the matmul's (y_ref, tol).
+
+    The kernel adds R in float32 to its float32 sum: one more rounding, half
+    an ulp of the result."""
+    R64 = np.asarray(R, dtype=np.float32).astype(np.float64)
+    c = y + R64
+    return c, tol + F32_EPS * (np.abs(c) + tol)
+
+
+def swiglu_reference(y, tol, I: int):
+    """(h_ref, tol) for the gate/up SwiGLU over y = A [gate; up]^T (2I
+    columns, gate first): h[m, j] = silu(g) * u with g = y[m, j] and
+    u = y[m, I + j].
+
+    Bound: the kernel's g' and u' are within tg and tu of g and u (the
+    matmul tolerance of the two rows); silu is Lipschitz with constant
+    SILU_LIPSCHITZ, so |silu(g') u' - silu(g) u| <= L tg (|u| + tu) +
+    |silu(g)| tu. The float32 evaluation adds at most 3.5 ulp relative (exp
+    within 2 ulp, then an add, a divide and a multiply of half an ulp each),
+    taken as 8 F32_EPS of |h| plus that bound."""
+    y = np.asarray(y, dtype=np.float64)
+    tol = np.asarray(tol, dtype=np.float64)
+    g, u = y[:, :I], y[:, I:2 * I]
+    tg, tu = tol[:, :I], tol[:, I:2 * I]
+    sg = silu(g)
+    h = sg * u
+    prop = SILU_LIPSCHITZ * tg * (np.abs(u) + tu) + np.abs(sg) * tu
+    return h, prop + 8 * F32_EPS * (np.abs(h) + prop) + 1e-30
 
 
 def argmax_first(y) -> int:
