@@ -35,7 +35,7 @@ EXPORTS = [
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
-    "lq_gemv_argmax", "lq_argmax_f32",
+    "lq_gemv_argmax", "lq_argmax_f32", "lq_matmul_residual", "lq_matmul_swiglu",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -94,6 +94,10 @@ def lib() -> ctypes.CDLL:
         L.lq_gemv_argmax.restype = st
         L.lq_argmax_f32.argtypes = [vp, i64, vp, vp]
         L.lq_argmax_f32.restype = st
+        L.lq_matmul_residual.argtypes = [st, vp, vp, vp, vp, i64, i64, i64, vp]
+        L.lq_matmul_residual.restype = st
+        L.lq_matmul_swiglu.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
+        L.lq_matmul_swiglu.restype = st
         _lib = L
     return _lib
 
@@ -215,6 +219,22 @@ def lq_gemv_argmax(fmt, A, W, C, N, K, out, stream=None):
 def lq_argmax_f32(x, n, out, stream=None):
     """Argmax of n device floats into the device lq_argmax_result `out`."""
     _check(lib().lq_argmax_f32(_ptr(x), int(n), _ptr(out), _stream(stream)), "lq_argmax_f32")
+
+
+# ---- epilogue fusions ----------------------------------------------------
+def lq_matmul_residual(fmt, A, W, R, C, M, N, K, stream=None):
+    """C = A W^T + R (R may be C); see include/lq.h."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib().lq_matmul_residual(f, _ptr(A), _ptr(W), _ptr(R), _ptr(C), int(M), int(N), int(K),
+                                    _stream(stream)), "lq_matmul_residual")
+
+
+def lq_matmul_swiglu(fmt, A, W, H, M, I, K, stream=None):
+    """H = silu(A gate^T) * (A up^T) for W = [gate; up] (2I rows); see
+    include/lq.h."""
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib().lq_matmul_swiglu(f, _ptr(A), _ptr(W), _ptr(H), int(M), int(I), int(K), _stream(stream)),
+           "lq_matmul_swiglu")
 
 
 # ---- host packers --------------------------------------------------------

@@ -10,6 +10,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "lq_epilogue.cuh"
 #include "lq_internal.h"
 
 namespace lq {
@@ -132,6 +133,38 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
   return launch_gemm_stream(a);
 }
 
+// The matmul with an epilogue (residual add or gate/up SwiGLU): the same
+// routes as do_matmul, each kernel applying the epilogue before its store;
+// the tensor-core kernel of lq_gemm.cu and the small-M stream kernel do not
+// take epilogues, so those shapes go to the generic kernel.
+lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, float* C, int64_t M,
+                      int64_t N, int64_t K, int epi_kind, void* stream) {
+  bool noop;
+  lq_status st = validate(fmt, A, W, C, M, N, K, &noop);
+  if (st != LQ_OK || noop) return st;
+  if (epi_kind == epi::kResidual && (!R || !aligned_to(R, 4))) return LQ_ERR_INVALID_ARG;
+  if (epi_kind == epi::kSwiglu && 2 * N >= (1LL << 30)) return LQ_ERR_UNSUPPORTED;
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  a.epi = epi_kind;
+  a.R = R;
+  switch (g_force_route.load()) {
+    case 1:
+      st = launch_gemv_batch(a);
+      return st == LQ_ERR_UNSUPPORTED ? launch_gemv_generic(a) : st;
+    case 2:
+      return gemm_tma_eligible(a) ? launch_gemm_tma(a) : LQ_ERR_UNSUPPORTED;
+    case 3: return launch_gemv_generic(a);
+    default: break;
+  }
+  if (M == 1) return launch_gemv(a);  // falls back to the generic kernel itself
+  if (M <= 4) {
+    st = launch_gemv_batch(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
+  if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
+  return launch_gemv_generic(a);
+}
+
 lq_status do_matmul(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N,
                     int64_t K, void* stream) {
   if (M == 1) return do_gemv(fmt, A, W, C, M, N, K, stream);
@@ -227,6 +260,18 @@ lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C, int64
   st = g_force_route.load() == 3 ? launch_gemv_generic(a) : launch_gemv(a);
   if (st != LQ_OK) return st;
   return launch_argmax_f32(C, N, out, a.stream);
+}
+
+lq_status lq_matmul_residual(int fmt, const float* A, const void* W, const float* R, float* C, int64_t M,
+                             int64_t N, int64_t K, void* stream) {
+  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  return do_epilogue(fmt, A, W, R, C, M, N, K, epi::kResidual, stream);
+}
+
+lq_status lq_matmul_swiglu(int fmt, const float* A, const void* W, float* H, int64_t M, int64_t I, int64_t K,
+                           void* stream) {
+  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  return do_epilogue(fmt, A, W, nullptr, H, M, I, K, epi::kSwiglu, stream);
 }
 
 lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* stream) {

@@ -38,6 +38,7 @@
 #include <tuple>
 
 #include "lq_device.cuh"
+#include "lq_epilogue.cuh"
 #include "lq_internal.h"
 #include "lq_tcgen05.cuh"
 
@@ -63,6 +64,7 @@ template <int FMT> constexpr int kRowBytes = FMT == LQ_FMT_F16 ? 256 : (FMT == L
 
 struct TmaGemmParams {
   float* C;
+  const float* R;      // residual epilogue: added to every output
   const float* scale;  // s_m per token (from the pre-pass)
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
@@ -269,7 +271,7 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer)
 // 1 .. split-1 (token-major f32 at `red` in their shared memory) when
 // split > 1, scaled by s_m (and 2^-8 for the quantised formats) and stored
 // to C[m0 + j, n0 + r].
-template <int FMT>
+template <int FMT, int EPI>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
                                            int bt, uint32_t red, int split, int c0, const float (&scp)[4]) {
   const int n = n0 + r;
@@ -297,8 +299,13 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
     for (int jj = 0; jj < 32; ++jj) {
       const int m = m0 + 32 * c + jj;
       const float f = __shfl_sync(0xffffffffu, sc, jj);
-      if (n < p.N && 32 * c + jj < bt && m < p.M)
-        p.C[static_cast<long long>(m) * p.N + n] = __uint_as_float(v[jj]) * f;
+      if (n < p.N && 32 * c + jj < bt && m < p.M) {
+        const long long o = static_cast<long long>(m) * p.N + n;
+        if constexpr (EPI == epi::kResidual)
+          p.C[o] = __uint_as_float(v[jj]) * f + p.R[o];
+        else
+          p.C[o] = __uint_as_float(v[jj]) * f;
+      }
     }
   }
 }
@@ -318,11 +325,20 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 // waits, lane 0 issues); a lone active lane beside parked lanes issues very
 // slowly. Every waiter sees the phases of the barriers it waits on in order.
 // ---------------------------------------------------------------------------
-template <int FMT>
+//
+// EPI (lq_epilogue.cuh): kResidual adds R in the store. kSwiglu: tmW views W
+// as [2][N][row] (gate rows, then up rows) and one box brings 64 gate rows
+// and the 64 matching up rows (tile rows 0-63 and 64-127, the same bytes and
+// layout as a 128-row box), so a tile covers 64 outputs; in the epilogue the
+// warps of TMEM lanes 64-127 hand their (up) accumulators to the warps of
+// lanes 0-63 through the idle A ring, which store swiglu(gate, up). No K
+// split with kSwiglu.
+template <int FMT, int EPI>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemm_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const TmaGemmParams p) {
   constexpr int SUB = kSub<FMT>;
+  constexpr bool SWIGLU = EPI == epi::kSwiglu;
   constexpr int kRawBytes = kRowBytes<FMT> * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
   // the CTA, the K coordinates of its loads add ks0.
   const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
-  const int n0 = (static_cast<int>(blockIdx.x) / split) * kBN, m0 = blockIdx.y * bt;
+  const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : kBN), m0 = blockIdx.y * bt;
   const int nraw_all = p.K / kKS / SUB;
   const int jr0 = rank * nraw_all / split;
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
@@ -380,12 +396,21 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     auto issue_raw = [&](int j, int slot) {
       mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
       if (FMT == LQ_FMT_F16) {
-        for (int h = 0; h < 2; ++h)  // two boxes of 64 halves x 128 rows (128B-swizzled)
-          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
-                          &b.raw_full[slot]);
+        for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
+          if constexpr (SWIGLU)
+            tc::tma_load_3d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
+                            &b.raw_full[slot]);
+          else
+            tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
+                            &b.raw_full[slot]);
+        }
       } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
-        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
-                        &b.raw_full[slot]);
+        if constexpr (SWIGLU)
+          tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
+                          &b.raw_full[slot]);
+        else
+          tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
+                          &b.raw_full[slot]);
       }
     };
     int raw_issued = 0, issued = 0;
@@ -535,8 +560,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         b.abort = 1;
       }
       epi = have && !b.abort;
-      if (epi && split == 1) {
-        store_tile<FMT>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g, scp);
+      if constexpr (SWIGLU) {
+        // up accumulators (lanes 64-127) -> the A ring, token-major 64 wide;
+        // then the gate warps (lanes 0-63) combine and store
+        float* xch = reinterpret_cast<float*>(a_ring);
+        if (epi && q4 >= 2) {
+#pragma unroll 1
+          for (int c = g; c < (bt + 31) / 32; c += 2) {
+            uint32_t v[32];
+            tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
+            tc::wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (32 * c + jj < bt) xch[(32 * c + jj) * 64 + (r - 64)] = __uint_as_float(v[jj]);
+          }
+        }
+        named_barrier(3, 8u * 32u);  // the eight epilogue warps, whatever their outcome
+        if (epi && q4 < 2) {
+          const int n = n0 + r;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = g + 2 * i;
+            if (c >= (bt + 31) / 32) break;
+            uint32_t v[32];
+            tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
+            const float sc = scp[i];
+            tc::wait_ld();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int m = m0 + 32 * c + jj;
+              const float f = __shfl_sync(0xffffffffu, sc, jj);
+              if (n < p.N && 32 * c + jj < bt && m < p.M) {
+                const float up = xch[(32 * c + jj) * 64 + r] * f;
+                p.C[static_cast<long long>(m) * p.N + n] = epi::swiglu(__uint_as_float(v[jj]) * f, up);
+              }
+            }
+          }
+        }
+      } else if (epi && split == 1) {
+        store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g, scp);
       } else if (epi && rank != 0) {
         // this rank's partial tile -> its own shared memory (the A ring is
         // idle now), token-major so that the 32 lanes write 32 rows in a row
@@ -563,8 +625,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (rank == 0 && epi && warp >= 2) {
       tc::fence_after_sync();
       const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
-      store_tile<FMT>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
-                      split, g, scp);
+      store_tile<FMT, EPI>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
+                           split, g, scp);
     }
     cluster_sync();  // the peers keep their shared memory until the leader read it
   }
@@ -723,17 +785,41 @@ int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT>, &cfg) == cudaSuccess && active >= tiles)
+    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT, epi::kPlain>, &cfg) == cudaSuccess &&
+        active >= tiles)
       return s;
     cudaGetLastError();  // a refused query is not an error of the call
   }
   return 1;
 }
 
+template <int FMT, int EPI>
+lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
+                             TmaGemmParams p);
+
 template <int FMT>
+lq_status launch_gemm_fmt(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
+                          const TmaGemmParams& p) {
+  switch (a.epi) {
+    case epi::kPlain: return launch_gemm_kernel<FMT, epi::kPlain>(a, tmW, tmA, p);
+    case epi::kResidual: return launch_gemm_kernel<FMT, epi::kResidual>(a, tmW, tmA, p);
+    case epi::kSwiglu: return launch_gemm_kernel<FMT, epi::kSwiglu>(a, tmW, tmA, p);
+    default: return LQ_ERR_UNSUPPORTED;
+  }
+}
+
+lq_status launch_gemm_epi(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
+                          const TmaGemmParams& p) {
+  if (a.fmt == LQ_FMT_F16) return launch_gemm_fmt<LQ_FMT_F16>(a, tmW, tmA, p);
+  if (a.fmt == LQ_FMT_Q8_0) return launch_gemm_fmt<LQ_FMT_Q8_0>(a, tmW, tmA, p);
+  return launch_gemm_fmt<LQ_FMT_Q4_0>(a, tmW, tmA, p);
+}
+
+template <int FMT, int EPI>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              TmaGemmParams p) {
-  auto kern = gemm_tma_kernel<FMT>;
+  auto kern = gemm_tma_kernel<FMT, EPI>;
+  const int bn = EPI == epi::kSwiglu ? kBN / 2 : kBN;  // outputs per tile
   const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
@@ -743,9 +829,9 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
     if (e != cudaSuccess) return cuda_status(e);
     configured[dev] = static_cast<int>(smem);
   }
-  const int64_t tiles = ((a.N + kBN - 1) / kBN) * ((a.M + p.bt - 1) / p.bt);
-  p.split = pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
-  const dim3 grid(static_cast<unsigned>((a.N + kBN - 1) / kBN * p.split),
+  const int64_t tiles = ((a.N + bn - 1) / bn) * ((a.M + p.bt - 1) / p.bt);
+  p.split = EPI == epi::kSwiglu ? 1 : pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
+  const dim3 grid(static_cast<unsigned>((a.N + bn - 1) / bn * p.split),
                   static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
   cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
                                      static_cast<unsigned>(p.split), tmW, tmA, p);
@@ -839,22 +925,20 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   if (!enc) return LQ_ERR_UNSUPPORTED;
   const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
   CUtensorMap tmW, tmA;
-  if (a.fmt == LQ_FMT_F16) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {rb};
-    cuuint32_t box[2] = {64, kBN};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(a.W), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return LQ_ERR_UNSUPPORTED;
-  } else {
-    cuuint64_t dims[2] = {rb / 4, static_cast<cuuint64_t>(N)};
-    cuuint64_t strides[1] = {rb};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(a.fmt == LQ_FMT_Q8_0 ? 68 : 36), kBN};
-    cuuint32_t es[2] = {1, 1};
-    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(a.W), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  {
+    // swiglu: a third dimension of 2 (gate rows, up rows N rows further on)
+    // and boxes of 64 + 64 rows; otherwise boxes of 128 rows
+    const bool sw = a.epi == epi::kSwiglu;
+    const cuuint32_t rank = sw ? 3 : 2;
+    const bool f16 = a.fmt == LQ_FMT_F16;
+    cuuint64_t dims[3] = {f16 ? static_cast<cuuint64_t>(K) : rb / 4, static_cast<cuuint64_t>(N), 2};
+    cuuint64_t strides[2] = {rb, rb * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(f16 ? 64 : (a.fmt == LQ_FMT_Q8_0 ? 68 : 36)),
+                         static_cast<cuuint32_t>(sw ? kBN / 2 : kBN), 2};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tmW, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, rank,
+            const_cast<void*>(a.W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            f16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return LQ_ERR_UNSUPPORTED;
   }
@@ -870,6 +954,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   }
   TmaGemmParams p;
   p.C = a.C;
+  p.R = a.R;
   p.scale = scale;
   p.M = M;
   p.N = N;
@@ -884,14 +969,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
-  lq_status st;
-  if (a.fmt == LQ_FMT_F16)
-    st = launch_gemm_kernel<LQ_FMT_F16>(a, tmW, tmA, p);
-  else if (a.fmt == LQ_FMT_Q8_0)
-    st = launch_gemm_kernel<LQ_FMT_Q8_0>(a, tmW, tmA, p);
-  else
-    st = launch_gemm_kernel<LQ_FMT_Q4_0>(a, tmW, tmA, p);
-  return st;
+  return launch_gemm_epi(a, tmW, tmA, p);
 }
 
 }  // namespace lq

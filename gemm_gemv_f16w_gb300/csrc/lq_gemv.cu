@@ -32,9 +32,11 @@
 // LQ_ERR_DEVICE_TIMEOUT, its producer drains its own copies and it returns.
 #include <algorithm>
 #include <atomic>
+#include <type_traits>
 
 #include "lq_argmax.cuh"
 #include "lq_device.cuh"
+#include "lq_epilogue.cuh"
 #include "lq_gemv_slices.cuh"
 #include "lq_internal.h"
 
@@ -69,6 +71,8 @@ struct GemvParams {
   unsigned wait_iters;
   lq_argmax_result* amax;    // argmax variant: the result (C may then be null)
   unsigned amax_warps;       // argmax variant: consumer warps of the grid
+  const float* R;            // residual variant: added to every output
+  long long up_off;          // swiglu variant: bytes from a gate row to its up row
 };
 
 struct Header {
@@ -93,11 +97,17 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_gemv_
 // the slot's reduction buffer), so a waiter sees either the phase it waits
 // for or the one before it, never an older one.
 //
-// AMAX adds the argmax of the outputs (lq_gemv_argmax): a finisher lane
-// ranks each row it writes, and every consumer warp merges its best row into
-// the result once its stages are done (lq_argmax.cuh).
+// EPI (lq_epilogue.cuh) picks what the finisher does with a row's sum:
+//  * kArgmax (lq_gemv_argmax): a finisher lane ranks each row it writes, and
+//    every consumer warp merges its best row into the result once its stages
+//    are done (lq_argmax.cuh);
+//  * kResidual: adds R[n];
+//  * kSwiglu: a stage holds rows_per_stage gate rows and then the same
+//    number of up rows (two bulk copies, the up rows up_off bytes further
+//    on in W); output j of the stage is swiglu(sum of slot row j, sum of
+//    slot row rows_per_stage + j).
 // ---------------------------------------------------------------------------
-template <int FMT, int CPW, bool AMAX>
+template <int FMT, int CPW, int EPI>
 __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     gemv_stream_kernel(const GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -113,10 +123,11 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
   const int nrows = r1 - r0;
   const int RS = p.rows_per_stage, S = p.stages;
   const int nk = p.nk, nr = p.nr, active = nk * nr;
+  constexpr bool AMAX = EPI == epi::kArgmax, SWIGLU = EPI == epi::kSwiglu;
   const int nst = (nrows + RS - 1) / RS;
-  const uint32_t stage_bytes = static_cast<uint32_t>(RS) * p.row_bytes;
+  const uint32_t stage_bytes = static_cast<uint32_t>(SWIGLU ? 2 * RS : RS) * p.row_bytes;
   // The host plans S as a multiple of nr (see plan_gemv); refuse anything else.
-  if (S % nr != 0 || S > kMaxStages || active > kConsumerWarps) {
+  if (S % nr != 0 || S > kMaxStages || active > kConsumerWarps || (SWIGLU && 2 * RS > kRowsPerStage)) {
     if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
     return;
   }
@@ -142,9 +153,16 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       const int s = st % S;
       const int rows = min(RS, nrows - st * RS);
       const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
-      mbar_arrive_expect_tx(&hd.full[s], bytes);
-      bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes,
-               wbase + static_cast<long long>(st) * RS * p.row_bytes, bytes, &hd.full[s], pol);
+      uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
+      const uint8_t* src = wbase + static_cast<long long>(st) * RS * p.row_bytes;
+      if constexpr (SWIGLU) {
+        mbar_arrive_expect_tx(&hd.full[s], 2u * bytes);
+        bulk_g2s(dst, src, bytes, &hd.full[s], pol);
+        bulk_g2s(dst + static_cast<size_t>(RS) * p.row_bytes, src + p.up_off, bytes, &hd.full[s], pol);
+      } else {
+        mbar_arrive_expect_tx(&hd.full[s], bytes);
+        bulk_g2s(dst, src, bytes, &hd.full[s], pol);
+      }
     };
     // W never depends on the previous kernel: fill the ring at once. The
     // rows that do not fit in it are prefetched into L2 at the same time, so
@@ -230,8 +248,11 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     for (int i = 0; i < CPW; ++i) {
       if (sl.ok[i]) {
 #pragma unroll
-        for (int r = 0; r < kRowsPerStage; ++r)
-          if (r < rows) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, i);
+        for (int r = 0; r < kRowsPerStage; ++r) {
+          // swiglu: slot rows 0 .. RS-1 are gate rows, RS .. 2RS-1 up rows
+          const bool valid = SWIGLU ? (r < RS ? r < rows : (r < 2 * RS && r - RS < rows)) : r < rows;
+          if (valid) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, i);
+        }
       }
     }
     int r;
@@ -254,6 +275,12 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
           const unsigned long long key = amax::make_key(sum, static_cast<unsigned>(row));
           best = key > best ? key : best;
           if (p.C) p.C[row] = sum;
+        } else if constexpr (EPI == epi::kResidual) {
+          p.C[row] = sum + p.R[row];
+        } else if constexpr (SWIGLU) {
+          float up = 0.f;
+          for (int g = 0; g < nk; ++g) up += hd.red[s][RS + lane][g];
+          p.C[row] = epi::swiglu(sum, up);
         } else {
           p.C[row] = sum;
         }
@@ -275,11 +302,44 @@ __device__ __forceinline__ float load_f16_bytes(const uint8_t* p) {
   return __half2float(__ushort_as_half(b));
 }
 
+// The dot product of one W row with one row of A, summed over the warp.
 template <int FMT>
+__device__ __forceinline__ float generic_row_dot(const float* a, const uint8_t* w, int K, int lane) {
+  float acc = 0.f;
+  if (FMT == LQ_FMT_F16) {
+    const __half* wh = reinterpret_cast<const __half*>(w);
+    for (int k = lane; k < K; k += 32) acc = fmaf(a[k], __half2float(wh[k]), acc);
+  } else if (FMT == LQ_FMT_Q8_0) {
+    for (int b = lane; b < K / 32; b += 32) {
+      const uint8_t* blk = w + 34LL * b;
+      float s = 0.f;
+      for (int i = 0; i < 32; ++i)
+        s = fmaf(static_cast<float>(static_cast<int8_t>(blk[2 + i])), a[32 * b + i], s);
+      acc = fmaf(load_f16_bytes(blk), s, acc);
+    }
+  } else {
+    for (int b = lane; b < K / 32; b += 32) {
+      const uint8_t* blk = w + 18LL * b;
+      float s = 0.f;
+      for (int i = 0; i < 16; ++i) {
+        const int byte = blk[2 + i];
+        s = fmaf(static_cast<float>((byte & 0xF) - 8), a[32 * b + i], s);
+        s = fmaf(static_cast<float>((byte >> 4) - 8), a[32 * b + 16 + i], s);
+      }
+      acc = fmaf(load_f16_bytes(blk), s, acc);
+    }
+  }
+  return warp_sum(acc);
+}
+
+// EPI as in the streaming kernel (no argmax here): residual adds R[m, n];
+// swiglu reads rows n (gate) and N + n (up) of W.
+template <int FMT, int EPI>
 __global__ void __launch_bounds__(256) generic_matmul_kernel(const float* __restrict__ A,
                                                              const uint8_t* __restrict__ W,
                                                              float* __restrict__ C, int M, int N,
-                                                             int K, long long row_bytes) {
+                                                             int K, long long row_bytes,
+                                                             const float* __restrict__ R) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   pdl_wait();
@@ -287,32 +347,16 @@ __global__ void __launch_bounds__(256) generic_matmul_kernel(const float* __rest
   const uint8_t* w = W + static_cast<long long>(n) * row_bytes;
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     const float* a = A + static_cast<long long>(m) * K;
-    float acc = 0.f;
-    if (FMT == LQ_FMT_F16) {
-      const __half* wh = reinterpret_cast<const __half*>(w);
-      for (int k = lane; k < K; k += 32) acc = fmaf(a[k], __half2float(wh[k]), acc);
-    } else if (FMT == LQ_FMT_Q8_0) {
-      for (int b = lane; b < K / 32; b += 32) {
-        const uint8_t* blk = w + 34LL * b;
-        float s = 0.f;
-        for (int i = 0; i < 32; ++i)
-          s = fmaf(static_cast<float>(static_cast<int8_t>(blk[2 + i])), a[32 * b + i], s);
-        acc = fmaf(load_f16_bytes(blk), s, acc);
-      }
+    const long long o = static_cast<long long>(m) * N + n;
+    const float acc = generic_row_dot<FMT>(a, w, K, lane);
+    if constexpr (EPI == epi::kSwiglu) {
+      const float up = generic_row_dot<FMT>(a, w + static_cast<long long>(N) * row_bytes, K, lane);
+      if (lane == 0) C[o] = epi::swiglu(acc, up);
+    } else if constexpr (EPI == epi::kResidual) {
+      if (lane == 0) C[o] = acc + R[o];
     } else {
-      for (int b = lane; b < K / 32; b += 32) {
-        const uint8_t* blk = w + 18LL * b;
-        float s = 0.f;
-        for (int i = 0; i < 16; ++i) {
-          const int byte = blk[2 + i];
-          s = fmaf(static_cast<float>((byte & 0xF) - 8), a[32 * b + i], s);
-          s = fmaf(static_cast<float>((byte >> 4) - 8), a[32 * b + 16 + i], s);
-        }
-        acc = fmaf(load_f16_bytes(blk), s, acc);
-      }
+      if (lane == 0) C[o] = acc;
     }
-    acc = warp_sum(acc);
-    if (lane == 0) C[static_cast<long long>(m) * N + n] = acc;
   }
 }
 
@@ -367,9 +411,9 @@ WarpGrid pick_grid(int fmt, int K) {
   return g;
 }
 
-template <int FMT, int CPW, bool AMAX>
+template <int FMT, int CPW, int EPI>
 lq_status launch_stream_t(const MatmulArgs& a, const GemvParams& p, int G, size_t smem) {
-  auto kern = gemv_stream_kernel<FMT, CPW, AMAX>;
+  auto kern = gemv_stream_kernel<FMT, CPW, EPI>;
   static int configured_smem[kMaxDevices] = {};  // per instantiation and device
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -384,17 +428,17 @@ lq_status launch_stream_t(const MatmulArgs& a, const GemvParams& p, int G, size_
   return cuda_status(e);
 }
 
-template <int FMT, bool AMAX>
+template <int FMT, int EPI>
 lq_status launch_stream_fmt(const MatmulArgs& a, int cpw, const GemvParams& p, int G, size_t smem) {
   if constexpr (FMT != LQ_FMT_F16) {
-    return cpw == 1 ? launch_stream_t<FMT, 1, AMAX>(a, p, G, smem)
-                    : (cpw == 2 ? launch_stream_t<FMT, 2, AMAX>(a, p, G, smem) : LQ_ERR_UNSUPPORTED);
+    return cpw == 1 ? launch_stream_t<FMT, 1, EPI>(a, p, G, smem)
+                    : (cpw == 2 ? launch_stream_t<FMT, 2, EPI>(a, p, G, smem) : LQ_ERR_UNSUPPORTED);
   } else {
     switch (cpw) {
-      case 1: return launch_stream_t<FMT, 1, AMAX>(a, p, G, smem);
-      case 2: return launch_stream_t<FMT, 2, AMAX>(a, p, G, smem);
-      case 4: return launch_stream_t<FMT, 4, AMAX>(a, p, G, smem);
-      case 8: return launch_stream_t<FMT, 8, AMAX>(a, p, G, smem);
+      case 1: return launch_stream_t<FMT, 1, EPI>(a, p, G, smem);
+      case 2: return launch_stream_t<FMT, 2, EPI>(a, p, G, smem);
+      case 4: return launch_stream_t<FMT, 4, EPI>(a, p, G, smem);
+      case 8: return launch_stream_t<FMT, 8, EPI>(a, p, G, smem);
       default: return LQ_ERR_UNSUPPORTED;
     }
   }
@@ -415,13 +459,23 @@ lq_status launch_gemv_generic(const MatmulArgs& a) {
   const long long rb = row_bytes(a.fmt, a.K);
   const auto* W = static_cast<const uint8_t*>(a.W);
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
+  if (a.epi != epi::kPlain && a.epi != epi::kResidual && a.epi != epi::kSwiglu) return LQ_ERR_UNSUPPORTED;
+  auto go = [&](auto kern) {
+    return launch(kern, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb, a.R);
+  };
+  auto by_epi = [&](auto fmt_tag) {
+    constexpr int F = decltype(fmt_tag)::value;
+    if (a.epi == epi::kResidual) return go(generic_matmul_kernel<F, epi::kResidual>);
+    if (a.epi == epi::kSwiglu) return go(generic_matmul_kernel<F, epi::kSwiglu>);
+    return go(generic_matmul_kernel<F, epi::kPlain>);
+  };
   cudaError_t e;
   if (a.fmt == LQ_FMT_F16)
-    e = launch(generic_matmul_kernel<LQ_FMT_F16>, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb);
+    e = by_epi(std::integral_constant<int, LQ_FMT_F16>{});
   else if (a.fmt == LQ_FMT_Q8_0)
-    e = launch(generic_matmul_kernel<LQ_FMT_Q8_0>, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb);
+    e = by_epi(std::integral_constant<int, LQ_FMT_Q8_0>{});
   else
-    e = launch(generic_matmul_kernel<LQ_FMT_Q4_0>, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb);
+    e = by_epi(std::integral_constant<int, LQ_FMT_Q4_0>{});
   if (e == cudaSuccess) e = cudaGetLastError();
   count_route(3);
   return cuda_status(e);
@@ -443,7 +497,11 @@ struct GemvPlan {
 GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_cap) {
   GemvPlan pl;
   const int K = static_cast<int>(a.K);
-  const int rb = static_cast<int>(row_bytes(a.fmt, a.K));
+  // a swiglu "row" is a gate row and its up row, moved together
+  const bool swiglu = a.epi == epi::kSwiglu;
+  const int wrb = static_cast<int>(row_bytes(a.fmt, a.K));
+  const int rb = swiglu ? 2 * wrb : wrb;
+  if (swiglu) max_rows = std::min(max_rows, kRowsPerStage / 2);
   // Fast path: every stage start is 16-byte aligned for the bulk copies
   // (rows a multiple of 16 bytes), A is 16-byte aligned for vector loads,
   // and the per-lane slices cover K.
@@ -495,7 +553,7 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_
   p.C = a.C;
   p.N = static_cast<int>(a.N);
   p.K = K;
-  p.row_bytes = rb;
+  p.row_bytes = wrb;
   p.rows_per_stage = rs;
   p.stages = ring;
   p.nk = wg.nk;
@@ -503,7 +561,9 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_
   p.a_region = a_region;
   p.a_stage = a_stage;
   // L2 keeps a whole weight matrix of up to a quarter of its size
-  p.l2_prefetch = static_cast<int64_t>(a.N) * rb <= kL2PrefetchMaxBytes ? 1 : 0;
+  p.l2_prefetch = !swiglu && static_cast<int64_t>(a.N) * rb <= kL2PrefetchMaxBytes ? 1 : 0;
+  p.R = a.R;
+  p.up_off = static_cast<long long>(a.N) * wrb;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   pl.cpw = wg.cpw;
@@ -513,11 +573,21 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_
   return pl;
 }
 
-template <bool AMAX>
-lq_status launch_plan(const MatmulArgs& a, const GemvPlan& pl) {
-  if (a.fmt == LQ_FMT_F16) return launch_stream_fmt<LQ_FMT_F16, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
-  if (a.fmt == LQ_FMT_Q8_0) return launch_stream_fmt<LQ_FMT_Q8_0, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
-  return launch_stream_fmt<LQ_FMT_Q4_0, AMAX>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+template <int EPI>
+lq_status launch_plan_epi(const MatmulArgs& a, const GemvPlan& pl) {
+  if (a.fmt == LQ_FMT_F16) return launch_stream_fmt<LQ_FMT_F16, EPI>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  if (a.fmt == LQ_FMT_Q8_0) return launch_stream_fmt<LQ_FMT_Q8_0, EPI>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+  return launch_stream_fmt<LQ_FMT_Q4_0, EPI>(a, pl.cpw, pl.p, pl.grid, pl.smem);
+}
+
+lq_status launch_plan(const MatmulArgs& a, const GemvPlan& pl, int epi_kind) {
+  switch (epi_kind) {
+    case epi::kPlain: return launch_plan_epi<epi::kPlain>(a, pl);
+    case epi::kArgmax: return launch_plan_epi<epi::kArgmax>(a, pl);
+    case epi::kResidual: return launch_plan_epi<epi::kResidual>(a, pl);
+    case epi::kSwiglu: return launch_plan_epi<epi::kSwiglu>(a, pl);
+    default: return LQ_ERR_UNSUPPORTED;
+  }
 }
 
 std::atomic<int> g_tune_ctas{0}, g_tune_rows{0}, g_tune_smem{0};
@@ -562,7 +632,7 @@ GemvPlan plan_for(const MatmulArgs& a) {
 lq_status launch_gemv(const MatmulArgs& a) {
   const GemvPlan pl = plan_for(a);
   if (!pl.ok) return launch_gemv_generic(a);
-  const lq_status st = launch_plan<false>(a, pl);
+  const lq_status st = launch_plan(a, pl, a.epi);
   if (st == LQ_ERR_UNSUPPORTED) return launch_gemv_generic(a);
   if (st == LQ_OK) count_route(0);
   return st;
@@ -577,7 +647,7 @@ lq_status launch_gemv_argmax(const MatmulArgs& a, lq_argmax_result* out) {
   pl.p.amax_warps = static_cast<unsigned>(pl.grid) * static_cast<unsigned>(pl.p.nk * pl.p.nr);
   cudaError_t e = cudaMemsetAsync(out->work, 0, sizeof(out->work), a.stream);
   if (e != cudaSuccess) return cuda_status(e);
-  const lq_status st = launch_plan<true>(a, pl);
+  const lq_status st = launch_plan(a, pl, epi::kArgmax);
   if (st == LQ_OK) count_route(0);
   return st;
 }

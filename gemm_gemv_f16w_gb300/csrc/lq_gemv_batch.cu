@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "lq_device.cuh"
+#include "lq_epilogue.cuh"
 #include "lq_gemv_slices_batch.cuh"
 #include "lq_internal.h"
 
@@ -62,6 +63,8 @@ struct BatchParams {
   int a_slot;             // bytes of one token's A as the slices read it
   unsigned long long wait_ns;
   unsigned wait_iters;
+  const float* R;         // residual epilogue: added to every output
+  long long up_off;       // swiglu epilogue: bytes from a gate row to its up row
 };
 
 template <int MT>
@@ -84,9 +87,14 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_batch
 // every K-group has posted its partials for slot s no warp reads the slot's
 // weights any more, and once the finisher has summed the partials its lane 0
 // issues the stage S further on into the slot.
-template <int FMT, int MT>
+//
+// EPI (lq_epilogue.cuh): kResidual adds R[m, n]; kSwiglu stages hold
+// rows_per_stage gate rows followed by the same number of up rows (two bulk
+// copies), and output j of the stage is swiglu(gate sum j, up sum j).
+template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kernel(const BatchParams p) {
   constexpr int NW = batch_warps(FMT, MT);
+  constexpr bool SWIGLU = EPI == epi::kSwiglu;
   extern __shared__ __align__(1024) uint8_t smem[];
   BatchHeader<MT>& hd = *reinterpret_cast<BatchHeader<MT>*>(smem);
   uint8_t* sA = smem + batch_header_bytes<MT>();  // MT x a_slot
@@ -100,9 +108,9 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   const int nrows = r1 - r0;
   const int RS = p.rows_per_stage, S = p.stages, nk = p.nk, nr = p.nr, active = nk * nr;
   const int nst = (nrows + RS - 1) / RS;
-  const uint32_t stage_bytes = static_cast<uint32_t>(RS) * p.row_bytes;
-  if (S % nr != 0 || S > kBMaxStages || nk > kBKGroups || active > NW || RS > kBRows || p.M > MT ||
-      p.early > S) {
+  const uint32_t stage_bytes = static_cast<uint32_t>(SWIGLU ? 2 * RS : RS) * p.row_bytes;
+  if (S % nr != 0 || S > kBMaxStages || nk > kBKGroups || active > NW || (SWIGLU ? 2 * RS : RS) > kBRows ||
+      p.M > MT || p.early > S) {
     if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
     return;
   }
@@ -110,10 +118,17 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   auto issue = [&](int st, uint64_t pol) {
     const int s = st % S;
     const uint32_t bytes = static_cast<uint32_t>(min(RS, nrows - st * RS)) * p.row_bytes;
+    uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
+    const uint8_t* src = wbase + static_cast<long long>(st) * RS * p.row_bytes;
     hd.last[s] = st;
-    mbar_arrive_expect_tx(&hd.full[s], bytes);
-    bulk_g2s(ring + static_cast<size_t>(s) * stage_bytes,
-             wbase + static_cast<long long>(st) * RS * p.row_bytes, bytes, &hd.full[s], pol);
+    if constexpr (SWIGLU) {
+      mbar_arrive_expect_tx(&hd.full[s], 2u * bytes);
+      bulk_g2s(dst, src, bytes, &hd.full[s], pol);
+      bulk_g2s(dst + static_cast<size_t>(RS) * p.row_bytes, src + p.up_off, bytes, &hd.full[s], pol);
+    } else {
+      mbar_arrive_expect_tx(&hd.full[s], bytes);
+      bulk_g2s(dst, src, bytes, &hd.full[s], pol);
+    }
   };
 
   if (threadIdx.x == 0) {
@@ -189,7 +204,9 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
         if (sl.ok) {
 #pragma unroll
           for (int r = 0; r < kBRows; ++r) {
-            if (r < rows) {
+            // swiglu: slot rows 0 .. RS-1 are gate rows, RS .. 2RS-1 up rows
+            const bool valid = SWIGLU ? (r < RS ? r < rows : (r < 2 * RS && r - RS < rows)) : r < rows;
+            if (valid) {
               float o[MT];
               sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, o);
 #pragma unroll
@@ -221,7 +238,16 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
               if (t < p.M) {
                 float sum = 0.f;
                 for (int g = 0; g < nk; ++g) sum += hd.red[s][t][lane][g];
-                p.C[static_cast<long long>(t) * p.N + r0 + st * RS + lane] = sum;
+                const long long o = static_cast<long long>(t) * p.N + r0 + st * RS + lane;
+                if constexpr (EPI == epi::kResidual) {
+                  p.C[o] = sum + p.R[o];
+                } else if constexpr (SWIGLU) {
+                  float up = 0.f;
+                  for (int g = 0; g < nk; ++g) up += hd.red[s][t][RS + lane][g];
+                  p.C[o] = epi::swiglu(sum, up);
+                } else {
+                  p.C[o] = sum;
+                }
               }
             }
           }
@@ -241,9 +267,9 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   }
 }
 
-template <int FMT, int MT>
+template <int FMT, int MT, int EPI>
 lq_status launch_batch_t(const MatmulArgs& a, const BatchParams& p, int G, size_t smem) {
-  auto kern = gemv_batch_kernel<FMT, MT>;
+  auto kern = gemv_batch_kernel<FMT, MT, EPI>;
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -265,6 +291,21 @@ lq_status launch_batch_t(const MatmulArgs& a, const BatchParams& p, int G, size_
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
+}
+
+template <int FMT, int EPI>
+lq_status launch_batch_mt(const MatmulArgs& a, const BatchParams& p, int G, size_t smem, int MT) {
+  return MT == 2 ? launch_batch_t<FMT, 2, EPI>(a, p, G, smem) : launch_batch_t<FMT, 4, EPI>(a, p, G, smem);
+}
+
+template <int FMT>
+lq_status launch_batch_fmt(const MatmulArgs& a, const BatchParams& p, int G, size_t smem, int MT) {
+  switch (a.epi) {
+    case epi::kPlain: return launch_batch_mt<FMT, epi::kPlain>(a, p, G, smem, MT);
+    case epi::kResidual: return launch_batch_mt<FMT, epi::kResidual>(a, p, G, smem, MT);
+    case epi::kSwiglu: return launch_batch_mt<FMT, epi::kSwiglu>(a, p, G, smem, MT);
+    default: return LQ_ERR_UNSUPPORTED;
+  }
 }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
@@ -299,7 +340,12 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   const int NW = batch_warps(a.fmt, MT);
   const DeviceInfo& di = device_info();
   const int G = static_cast<int>(std::min<int64_t>(N, di.sm_count));
-  const int rb = static_cast<int>(row_bytes(a.fmt, K));
+  // a swiglu "row" is a gate row and its up row, moved together
+  const bool swiglu = a.epi == epi::kSwiglu;
+  if (a.epi != epi::kPlain && a.epi != epi::kResidual && !swiglu) return LQ_ERR_UNSUPPORTED;
+  const int wrb = static_cast<int>(row_bytes(a.fmt, K));
+  const int rb = swiglu ? 2 * wrb : wrb;
+  const int max_rows = swiglu ? kBRows / 2 : kBRows;
   const int a_slot = a.fmt == LQ_FMT_F16 ? static_cast<int>(K * 4)
                                          : static_cast<int>((K / 32 + 63) / 64) * 64 * kASlotBytes;
   const int a_stage = a.fmt == LQ_FMT_F16 ? 0 : static_cast<int>((M * K * 4 + 127) / 128 * 128);
@@ -312,7 +358,7 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   // the height balanced so that every row-group gets the same number of
   // stages. The ring takes as many slots as fit, a multiple of nr and never
   // more than the CTA's stages rounded up to nr.
-  const int rs_max = std::max(1, std::min({kBRows, budget / (2 * rb), rows_per_cta}));
+  const int rs_max = std::max(1, std::min({max_rows, budget / (2 * rb), rows_per_cta}));
   const int need_max = (rows_per_cta + rs_max - 1) / rs_max;
   int nr = std::max(1, std::min(NW / nk, need_max));
   const int cap_slots = std::min(kBMaxStages, budget / (rs_max * rb));
@@ -332,8 +378,10 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.K = static_cast<int>(K);
-  p.row_bytes = rb;
+  p.row_bytes = wrb;
   p.rows_per_stage = RS;
+  p.R = a.R;
+  p.up_off = static_cast<long long>(N) * wrb;
   p.nk = nk;
   p.nr = nr;
   p.stages = S;
@@ -347,11 +395,11 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   const size_t smem = static_cast<size_t>(hdr) + MT * static_cast<size_t>(a_slot) + ring;
   lq_status st;
   if (a.fmt == LQ_FMT_F16)
-    st = MT == 2 ? launch_batch_t<LQ_FMT_F16, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_F16, 4>(a, p, G, smem);
+    st = launch_batch_fmt<LQ_FMT_F16>(a, p, G, smem, MT);
   else if (a.fmt == LQ_FMT_Q8_0)
-    st = MT == 2 ? launch_batch_t<LQ_FMT_Q8_0, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_Q8_0, 4>(a, p, G, smem);
+    st = launch_batch_fmt<LQ_FMT_Q8_0>(a, p, G, smem, MT);
   else
-    st = MT == 2 ? launch_batch_t<LQ_FMT_Q4_0, 2>(a, p, G, smem) : launch_batch_t<LQ_FMT_Q4_0, 4>(a, p, G, smem);
+    st = launch_batch_fmt<LQ_FMT_Q4_0>(a, p, G, smem, MT);
   if (st == LQ_OK) count_route(1);
   return st;
 }

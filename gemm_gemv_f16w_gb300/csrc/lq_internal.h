@@ -8,6 +8,9 @@
 namespace lq {
 
 // Problem handed from the C-ABI layer (already validated) to a launcher.
+// With epilogue kSwiglu (lq_epilogue.cuh) W holds 2N rows (gate, then up)
+// and C receives the N SwiGLU outputs of each row of A; with kResidual C =
+// A W^T + R.
 struct MatmulArgs {
   const float* A;
   const void* W;
@@ -15,6 +18,8 @@ struct MatmulArgs {
   int64_t M, N, K;
   int fmt;            // lq_format
   cudaStream_t stream;
+  int epi = 0;        // lq::epi kind (0: plain)
+  const float* R = nullptr;
 };
 
 // Per-device facts cached on first use.

@@ -204,6 +204,34 @@ lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C,
  * x 4-byte aligned. */
 lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* stream);
 
+/* ---- epilogue fusions -----------------------------------------------------
+ * The matmul with its output combined before it is stored, for any M (the
+ * M = 1, M = 2..4 and tensor-core kernels apply it in their store; shapes
+ * outside their fast paths use the generic kernel with the same epilogue).
+ *
+ * lq_matmul_residual: C = A W^T + R (R: M*N floats, device), as
+ *   gemm_q1_v7_residual adds the hidden state to the output projection
+ *   (oxibonsai-kernels 0.1.4, src/gpu_backend/metal_prefill/functions.rs).
+ *   R may be C itself (in-place update of the residual stream); any other
+ *   overlap of R with C is not allowed. Arguments otherwise as lq_matmul_<fmt>;
+ *   R NULL or not 4-byte aligned -> LQ_ERR_INVALID_ARG.
+ *
+ * lq_matmul_swiglu: W is gate_up, 2*I rows in format `fmt` (gate rows
+ *   0 .. I-1, then up rows I .. 2I-1, as the pages lay out gate_up and index
+ *   it by offset); H (M*I floats, device) receives
+ *       H[m, j] = silu(g) * u,  g = (A W^T)[m, j],  u = (A W^T)[m, I + j],
+ *       silu(g) = g / (1 + exp(-g)),
+ *   fused_gate_up_swiglu_gemm (same page) and silu_mul / silu_mul_fused
+ *   (lattice-inference). The 2I x K gate/up products are never stored.
+ *   Arguments as lq_matmul_<fmt> with N = I; 2I >= 2^30 -> LQ_ERR_UNSUPPORTED.
+ *
+ * Tolerances: as the underlying matmul route for the products, then the
+ * float32 epilogue (one add; silu with CUDA's expf, a divide and a multiply). */
+lq_status lq_matmul_residual(int fmt, const float* A, const void* W, const float* R, float* C,
+                             int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_matmul_swiglu(int fmt, const float* A, const void* W, float* H,
+                           int64_t M, int64_t I, int64_t K, void* stream);
+
 /* ---- status ---------------------------------------------------------- */
 const char* lq_status_string(lq_status s);
 /* Synchronises the current device, then reads and clears its device status

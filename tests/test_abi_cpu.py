@@ -151,3 +151,21 @@ def test_argmax_argument_errors_return_before_launch(lq):
     assert L.lq_argmax_f32(None, 8, out, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_argmax_f32(c + 2, 8, out, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_argmax_f32(c, 8, out + 4, 0) == lq.LQ_ERR_INVALID_ARG
+
+
+def test_epilogue_argument_errors_return_before_launch(lq):
+    L = lq.lib()
+    a, w, r, c = 0x10000, 0x20000, 0x30000, 0x40000
+    for fmt in (0, 1, 2):
+        # no-ops and refusals, never dereferenced
+        assert L.lq_matmul_residual(fmt, a, w, r, c, 0, 8, 64, 0) == lq.LQ_OK
+        assert L.lq_matmul_swiglu(fmt, a, w, c, 3, 0, 64, 0) == lq.LQ_OK
+        assert L.lq_matmul_residual(fmt, a, w, None, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+        assert L.lq_matmul_residual(fmt, a, w, r + 2, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+        assert L.lq_matmul_residual(fmt, a, w, r, None, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+        assert L.lq_matmul_swiglu(fmt, a, None, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+        assert L.lq_matmul_swiglu(fmt, a, w, c, -1, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+        assert L.lq_matmul_swiglu(fmt, a, w, c, 2, 1 << 29, 64, 0) == lq.LQ_ERR_UNSUPPORTED
+    assert L.lq_matmul_residual(5, a, w, r, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_matmul_swiglu(5, a, w, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_matmul_swiglu(1, a, w, c, 2, 8, 48, 0) == lq.LQ_ERR_INVALID_ARG  # K % 32
