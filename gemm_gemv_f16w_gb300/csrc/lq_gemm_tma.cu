@@ -258,6 +258,11 @@ __device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t 
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
@@ -295,6 +300,16 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + t[jj]);
     }
+    // residual: the chunk's 32 values of R first (R may be C, so no load
+    // could move past a store), then the stores
+    float rv[32];
+    if constexpr (EPI == epi::kResidual) {
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) {
+        const int m = m0 + 32 * c + jj;
+        rv[jj] = (n < p.N && 32 * c + jj < bt && m < p.M) ? p.R[static_cast<long long>(m) * p.N + n] : 0.f;
+      }
+    }
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const int m = m0 + 32 * c + jj;
@@ -302,7 +317,7 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
       if (n < p.N && 32 * c + jj < bt && m < p.M) {
         const long long o = static_cast<long long>(m) * p.N + n;
         if constexpr (EPI == epi::kResidual)
-          p.C[o] = __uint_as_float(v[jj]) * f + p.R[o];
+          p.C[o] = __uint_as_float(v[jj]) * f + rv[jj];
         else
           p.C[o] = __uint_as_float(v[jj]) * f;
       }
@@ -329,10 +344,10 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 // EPI (lq_epilogue.cuh): kResidual adds R in the store. kSwiglu: tmW views W
 // as [2][N][row] (gate rows, then up rows) and one box brings 64 gate rows
 // and the 64 matching up rows (tile rows 0-63 and 64-127, the same bytes and
-// layout as a 128-row box), so a tile covers 64 outputs; in the epilogue the
-// warps of TMEM lanes 64-127 hand their (up) accumulators to the warps of
-// lanes 0-63 through the idle A ring, which store swiglu(gate, up). No K
-// split with kSwiglu.
+// layout as a 128-row box), so a tile covers 64 outputs; the epilogue warps
+// put the scaled accumulators into the idle A ring and then combine gate and
+// up pairs in one short loop (a fully unrolled combine made the kernel's
+// code large enough to stall on instruction fetch). No K split with kSwiglu.
 template <int FMT, int EPI>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     gemm_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
@@ -561,23 +576,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       epi = have && !b.abort;
       if constexpr (SWIGLU) {
-        // up accumulators (lanes 64-127) -> the A ring, token-major 64 wide;
-        // then the gate warps (lanes 0-63) combine and store
+        // gate (lanes 0-63) and up (lanes 64-127) accumulators, scaled,
+        // -> the A ring as [token][gate 64 | up 64]; then all eight warps
+        // combine (token, output) pairs in one rolled loop and store 64
+        // consecutive outputs of a token together
         float* xch = reinterpret_cast<float*>(a_ring);
-        if (epi && q4 >= 2) {
-#pragma unroll 1
-          for (int c = g; c < (bt + 31) / 32; c += 2) {
-            uint32_t v[32];
-            tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
-            tc::wait_ld();
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              if (32 * c + jj < bt) xch[(32 * c + jj) * 64 + (r - 64)] = __uint_as_float(v[jj]);
-          }
-        }
-        named_barrier(3, 8u * 32u);  // the eight epilogue warps, whatever their outcome
-        if (epi && q4 < 2) {
-          const int n = n0 + r;
+        if (epi) {
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = g + 2 * i;
@@ -588,13 +592,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             tc::wait_ld();
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
-              const int m = m0 + 32 * c + jj;
               const float f = __shfl_sync(0xffffffffu, sc, jj);
-              if (n < p.N && 32 * c + jj < bt && m < p.M) {
-                const float up = xch[(32 * c + jj) * 64 + r] * f;
-                p.C[static_cast<long long>(m) * p.N + n] = epi::swiglu(__uint_as_float(v[jj]) * f, up);
-              }
+              if (32 * c + jj < bt) xch[(32 * c + jj) * 128 + r] = __uint_as_float(v[jj]) * f;
             }
+          }
+        }
+        named_barrier(3, 8u * 32u);  // the eight epilogue warps, whatever their outcome
+        if (epi) {
+          const int t0 = static_cast<int>(threadIdx.x) - 64;  // 0 .. 255 over warps 2..9
+          const int rows = min(bt, p.M - m0);
+#pragma unroll 1
+          for (int idx = t0; idx < rows * 64; idx += 256) {
+            const int tok = idx >> 6, j = idx & 63, n = n0 + j;
+            if (n < p.N)
+              p.C[static_cast<long long>(m0 + tok) * p.N + n] = epi::swiglu(xch[tok * 128 + j], xch[tok * 128 + 64 + j]);
           }
         }
       } else if (epi && split == 1) {
@@ -891,7 +902,8 @@ cudaMemPool_t workspace_pool() {
 // scales) live in a stream-ordered workspace from the library's pool for the
 // duration of the call.
 lq_status launch_gemm_tma(const MatmulArgs& a) {
-  const int bt = pick_bt(a.M, a.N);
+  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
+  const int bt = pick_bt(a.M, a.epi == epi::kSwiglu ? 2 * a.N : a.N);
   const size_t a16_bytes = static_cast<size_t>(a.M) * a.K * 2;
   const size_t ws_bytes = (a16_bytes + 255) / 256 * 256 + static_cast<size_t>(a.M) * 4;
   void* ws = nullptr;

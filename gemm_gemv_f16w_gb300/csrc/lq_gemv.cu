@@ -102,10 +102,10 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_gemv_
 //    every consumer warp merges its best row into the result once its stages
 //    are done (lq_argmax.cuh);
 //  * kResidual: adds R[n];
-//  * kSwiglu: a stage holds rows_per_stage gate rows and then the same
-//    number of up rows (two bulk copies, the up rows up_off bytes further
-//    on in W); output j of the stage is swiglu(sum of slot row j, sum of
-//    slot row rows_per_stage + j).
+//  * kSwiglu: a stage of n outputs holds their n gate rows followed by their
+//    n up rows (two bulk copies, the up rows up_off bytes further on in W);
+//    output j of the stage is swiglu(sum of slot row j, sum of slot row
+//    n + j).
 // ---------------------------------------------------------------------------
 template <int FMT, int CPW, int EPI>
 __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       if constexpr (SWIGLU) {
         mbar_arrive_expect_tx(&hd.full[s], 2u * bytes);
         bulk_g2s(dst, src, bytes, &hd.full[s], pol);
-        bulk_g2s(dst + static_cast<size_t>(RS) * p.row_bytes, src + p.up_off, bytes, &hd.full[s], pol);
+        bulk_g2s(dst + bytes, src + p.up_off, bytes, &hd.full[s], pol);  // up rows right after
       } else {
         mbar_arrive_expect_tx(&hd.full[s], bytes);
         bulk_g2s(dst, src, bytes, &hd.full[s], pol);
@@ -249,9 +249,8 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       if (sl.ok[i]) {
 #pragma unroll
         for (int r = 0; r < kRowsPerStage; ++r) {
-          // swiglu: slot rows 0 .. RS-1 are gate rows, RS .. 2RS-1 up rows
-          const bool valid = SWIGLU ? (r < RS ? r < rows : (r < 2 * RS && r - RS < rows)) : r < rows;
-          if (valid) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, i);
+          // swiglu: slot rows 0 .. rows-1 are gate rows, rows .. 2rows-1 up rows
+          if (r < (SWIGLU ? 2 * rows : rows)) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, i);
         }
       }
     }
@@ -262,6 +261,10 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     if (lane == 0) mbar_arrive(&hd.red_full[s]);
     if (kg == (st / nr) % nk) {
       // finisher of this stage: the K-groups' partials, in a fixed order
+      // (residual: R is fetched while the other K-groups finish)
+      float rres = 0.f;
+      if constexpr (EPI == epi::kResidual)
+        if (lane < rows) rres = p.R[r0 + st * RS + lane];
       if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
         record_error(kDevErrTimeout);
         hd.abort = 1;
@@ -276,10 +279,10 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
           best = key > best ? key : best;
           if (p.C) p.C[row] = sum;
         } else if constexpr (EPI == epi::kResidual) {
-          p.C[row] = sum + p.R[row];
+          p.C[row] = sum + rres;
         } else if constexpr (SWIGLU) {
           float up = 0.f;
-          for (int g = 0; g < nk; ++g) up += hd.red[s][RS + lane][g];
+          for (int g = 0; g < nk; ++g) up += hd.red[s][rows + lane][g];
           p.C[row] = epi::swiglu(sum, up);
         } else {
           p.C[row] = sum;

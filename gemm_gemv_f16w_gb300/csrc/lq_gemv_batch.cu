@@ -88,8 +88,8 @@ __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_batch
 // weights any more, and once the finisher has summed the partials its lane 0
 // issues the stage S further on into the slot.
 //
-// EPI (lq_epilogue.cuh): kResidual adds R[m, n]; kSwiglu stages hold
-// rows_per_stage gate rows followed by the same number of up rows (two bulk
+// EPI (lq_epilogue.cuh): kResidual adds R[m, n]; a kSwiglu stage of n
+// outputs holds their n gate rows followed by their n up rows (two bulk
 // copies), and output j of the stage is swiglu(gate sum j, up sum j).
 template <int FMT, int MT, int EPI>
 __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kernel(const BatchParams p) {
@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
     if constexpr (SWIGLU) {
       mbar_arrive_expect_tx(&hd.full[s], 2u * bytes);
       bulk_g2s(dst, src, bytes, &hd.full[s], pol);
-      bulk_g2s(dst + static_cast<size_t>(RS) * p.row_bytes, src + p.up_off, bytes, &hd.full[s], pol);
+      bulk_g2s(dst + bytes, src + p.up_off, bytes, &hd.full[s], pol);  // up rows right after
     } else {
       mbar_arrive_expect_tx(&hd.full[s], bytes);
       bulk_g2s(dst, src, bytes, &hd.full[s], pol);
@@ -204,9 +204,8 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
         if (sl.ok) {
 #pragma unroll
           for (int r = 0; r < kBRows; ++r) {
-            // swiglu: slot rows 0 .. RS-1 are gate rows, RS .. 2RS-1 up rows
-            const bool valid = SWIGLU ? (r < RS ? r < rows : (r < 2 * RS && r - RS < rows)) : r < rows;
-            if (valid) {
+            // swiglu: slot rows 0 .. rows-1 are gate rows, rows .. 2rows-1 up rows
+            if (r < (SWIGLU ? 2 * rows : rows)) {
               float o[MT];
               sl.dot(base + static_cast<uint32_t>(r) * p.row_bytes, o);
 #pragma unroll
@@ -226,13 +225,31 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
           // finisher: adds the K-groups' partials in a fixed order, one
           // output per token, then refills slot s. The refill comes last: its
           // landing releases the row-group's next stage in this slot, whose
-          // partials overwrite red[s].
+          // partials overwrite red[s]. (Residual: R is fetched while the
+          // other K-groups finish.)
+          float rres[MT];
+#pragma unroll
+          for (int t = 0; t < MT; ++t)
+            rres[t] = EPI == epi::kResidual && lane < rows && t < p.M
+                          ? p.R[static_cast<long long>(t) * p.N + r0 + st * RS + lane]
+                          : 0.f;
           if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
             record_error(kDevErrTimeout);
             hd.abort = 1;
             break;
           }
-          if (lane < rows) {
+          if (SWIGLU && lane < rows) {
+            // one token at a time: a copy of silu per token would bloat the loop
+#pragma unroll 1
+            for (int t = 0; t < p.M; ++t) {
+              float sum = 0.f, up = 0.f;
+              for (int g = 0; g < nk; ++g) {
+                sum += hd.red[s][t][lane][g];
+                up += hd.red[s][t][rows + lane][g];
+              }
+              p.C[static_cast<long long>(t) * p.N + r0 + st * RS + lane] = epi::swiglu(sum, up);
+            }
+          } else if (lane < rows) {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
               if (t < p.M) {
@@ -240,11 +257,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
                 for (int g = 0; g < nk; ++g) sum += hd.red[s][t][lane][g];
                 const long long o = static_cast<long long>(t) * p.N + r0 + st * RS + lane;
                 if constexpr (EPI == epi::kResidual) {
-                  p.C[o] = sum + p.R[o];
-                } else if constexpr (SWIGLU) {
-                  float up = 0.f;
-                  for (int g = 0; g < nk; ++g) up += hd.red[s][t][RS + lane][g];
-                  p.C[o] = epi::swiglu(sum, up);
+                  p.C[o] = sum + rres[t];
                 } else {
                   p.C[o] = sum;
                 }
