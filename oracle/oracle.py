@@ -210,7 +210,7 @@ def _round_half_away(v32: np.ndarray) -> np.ndarray:
     return np.sign(v) * np.floor(np.abs(v) + 0.5)
 
 
-def quantize_q8_0(W) -> np.ndarray:
+def quantize_q8_0(W, reciprocal: bool = False) -> np.ndarray:
     """Q8_0 packing of W f32 [N, K] (K % 32 == 0) -> uint8 [N, K/32*34].
 
     Per 32-element block (quantize_row_q8_0, with the division of the matmul
@@ -220,6 +220,8 @@ def quantize_q8_0(W) -> np.ndarray:
       3. q_i = 0 if d == 0 else round(x_i / d)   (float32 divide, halves away
          from zero), clamped to [-127, 127]
       4. bytes 0-1: f16(d) little-endian; bytes 2..33: q_0..q_31 as int8.
+    With ``reciprocal`` step 3 is the page's own expression: id = 1 / d
+    (float32, 0 when d == 0), q_i = round(x_i * id) (float32 multiply).
     """
     W = np.ascontiguousarray(W, dtype=np.float32)
     _check_finite(W)
@@ -231,7 +233,11 @@ def quantize_q8_0(W) -> np.ndarray:
     amax = np.max(np.abs(x), axis=2)                          # f32
     d = (amax / np.float32(127.0)).astype(np.float32)         # f32
     with np.errstate(divide="ignore", invalid="ignore"):
-        v = (x / d[:, :, None]).astype(np.float32)            # f32 divide
+        if reciprocal:
+            inv = np.where(d != 0, np.float32(1.0) / d, np.float32(0.0)).astype(np.float32)
+            v = (x * inv[:, :, None]).astype(np.float32)      # f32 multiply
+        else:
+            v = (x / d[:, :, None]).astype(np.float32)        # f32 divide
     q = _round_half_away(v)
     q = np.clip(q, -127, 127)
     q = np.where(d[:, :, None] == 0, 0, q).astype(np.int8)
@@ -243,7 +249,7 @@ def quantize_q8_0(W) -> np.ndarray:
     return out.reshape(N, nb * Q8_0_BLOCK_BYTES)
 
 
-def quantize_q4_0(W) -> np.ndarray:
+def quantize_q4_0(W, interleaved: bool = False) -> np.ndarray:
     """Q4_0 packing of W f32 [N, K] (K % 32 == 0) -> uint8 [N, K/32*18].
 
     Per 32-element block:
@@ -253,6 +259,9 @@ def quantize_q4_0(W) -> np.ndarray:
          the argument is >= 0.5 so truncation is floor)
       4. bytes 0-1: f16(d) little-endian; byte 2+j = q_j | q_{j+16} << 4 for
          j = 0..15 (low nibbles: elements 0-15, high nibbles: 16-31).
+    With ``interleaved`` step 4 stores the order the pages' Q4 kernels read
+    (gemv_q4_decode and gemm_q4: low nibble of byte j = element 2j, high
+    nibble = element 2j+1): byte 2+j = q_{2j} | q_{2j+1} << 4.
     """
     W = np.ascontiguousarray(W, dtype=np.float32)
     _check_finite(W)
@@ -271,7 +280,10 @@ def quantize_q4_0(W) -> np.ndarray:
     d16 = f32_to_f16_bits(d)
     out[:, :, 0] = (d16 & 0xFF).astype(np.uint8)
     out[:, :, 1] = (d16 >> 8).astype(np.uint8)
-    out[:, :, 2:] = (qi[:, :, :16] & 0xF) | ((qi[:, :, 16:] & 0xF) << 4)
+    if interleaved:
+        out[:, :, 2:] = (qi[:, :, 0::2] & 0xF) | ((qi[:, :, 1::2] & 0xF) << 4)
+    else:
+        out[:, :, 2:] = (qi[:, :, :16] & 0xF) | ((qi[:, :, 16:] & 0xF) << 4)
     return out.reshape(N, nb * Q4_0_BLOCK_BYTES)
 
 
@@ -282,6 +294,8 @@ def pack(fmt: str, W) -> np.ndarray:
         return quantize_q8_0(W)
     if fmt == "q4_0":
         return quantize_q4_0(W)
+    if fmt == "q4_0i":
+        return quantize_q4_0(W, interleaved=True)
     raise ValueError(fmt)
 
 
@@ -301,19 +315,22 @@ def dequantize_q8_0(packed, N: int, K: int) -> np.ndarray:
     return (d[:, :, None] * q).astype(np.float32).reshape(N, K)
 
 
-def unpack_q4_0_codes(packed, N: int, K: int) -> np.ndarray:
-    """uint8 [N, K/32*18] -> the 4-bit codes q in 0..15, shape [N, K]."""
+def unpack_q4_0_codes(packed, N: int, K: int, interleaved: bool = False) -> np.ndarray:
+    """uint8 [N, K/32*18] -> the 4-bit codes q in 0..15, shape [N, K]
+    (``interleaved``: byte j holds elements 2j (low) and 2j+1 (high))."""
     b = np.asarray(packed, dtype=np.uint8).reshape(N, K // QK, Q4_0_BLOCK_BYTES)
     lo = b[:, :, 2:] & 0xF
     hi = b[:, :, 2:] >> 4
+    if interleaved:
+        return np.stack([lo, hi], axis=3).reshape(N, K)
     return np.concatenate([lo, hi], axis=2).reshape(N, K)
 
 
-def dequantize_q4_0(packed, N: int, K: int) -> np.ndarray:
+def dequantize_q4_0(packed, N: int, K: int, interleaved: bool = False) -> np.ndarray:
     """uint8 [N, K/32*18] -> f32 [N, K]; each value d*(q-8) is exact in float32."""
     b = np.asarray(packed, dtype=np.uint8).reshape(N, K // QK, Q4_0_BLOCK_BYTES)
     d = _scales(b)
-    q = unpack_q4_0_codes(packed, N, K).reshape(N, K // QK, QK).astype(np.float32) - np.float32(8)
+    q = unpack_q4_0_codes(packed, N, K, interleaved).reshape(N, K // QK, QK).astype(np.float32) - np.float32(8)
     return (d[:, :, None] * q).astype(np.float32).reshape(N, K)
 
 
@@ -328,6 +345,8 @@ def dequantize(fmt: str, packed, N: int, K: int) -> np.ndarray:
         return dequantize_q8_0(packed, N, K)
     if fmt == "q4_0":
         return dequantize_q4_0(packed, N, K)
+    if fmt == "q4_0i":
+        return dequantize_q4_0(packed, N, K, interleaved=True)
     raise ValueError(fmt)
 
 
@@ -336,7 +355,7 @@ def packed_row_bytes(fmt: str, K: int) -> int:
         return 2 * K
     if fmt == "q8_0":
         return K // QK * Q8_0_BLOCK_BYTES
-    if fmt == "q4_0":
+    if fmt in ("q4_0", "q4_0i"):
         return K // QK * Q4_0_BLOCK_BYTES
     raise ValueError(fmt)
 

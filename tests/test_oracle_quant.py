@@ -175,7 +175,7 @@ def test_planted_half_even_rounding_is_caught(monkeypatch):
 def test_planted_interleaved_nibbles_are_caught(monkeypatch):
     """A dequantiser that reads the page's interleaved nibble order (byte j =
     elements 2j, 2j+1) must fail the ramp golden's round trip."""
-    def interleaved(packed, N, K):
+    def interleaved(packed, N, K, interleaved=False):
         b = np.asarray(packed, dtype=np.uint8).reshape(N, K // 32, 18)[:, :, 2:]
         out = np.empty((N, K // 32, 32), dtype=np.uint8)
         out[:, :, 0::2] = b & 0xF
@@ -188,3 +188,43 @@ def test_planted_interleaved_nibbles_are_caught(monkeypatch):
     assert np.array_equal(O.dequantize_q4_0(p, 1, 32), x)
     monkeypatch.setattr(O.oracle, "unpack_q4_0_codes", interleaved)
     assert not np.array_equal(O.dequantize_q4_0(p, 1, 32), x)
+
+
+# ---- the pages' own layouts: interleaved Q4_0 nibbles, Q8_0 via 1/d --------
+def test_q4_0i_golden_ramp_interleaved_nibbles():
+    g = _golden("q4_0i_ramp.json")
+    x = (np.array(g["k"], dtype=np.float64) * g["x_scale"]).astype(np.float32)[None, :]
+    got = O.quantize_q4_0(x, interleaved=True)[0]
+    assert list(got) == g["bytes"]
+    assert list(O.pack("q4_0i", x)[0]) == g["bytes"]
+
+
+def test_q4_0i_holds_the_same_values_as_q4_0():
+    """The two layouts store the same codes and scale: dequantised they are
+    identical element for element, while the bytes differ."""
+    rng = np.random.default_rng(7)
+    W = (rng.standard_normal((9, 256)) * 0.05).astype(np.float32)
+    a, b = O.pack("q4_0", W), O.pack("q4_0i", W)
+    assert not np.array_equal(a, b)
+    assert np.array_equal(O.dequantize("q4_0", a, 9, 256), O.dequantize("q4_0i", b, 9, 256))
+    # a planted mistake: reading interleaved bytes in the standard order
+    assert not np.array_equal(O.dequantize("q4_0", b, 9, 256), O.dequantize("q4_0i", b, 9, 256))
+
+
+def test_q8_0_golden_reciprocal_rounding():
+    g = _golden("q8_0_reciprocal.json")
+    x = np.array(g["x_bits"], dtype=np.uint32).view(np.float32)[None, :]
+    assert list(O.quantize_q8_0(x)[0]) == g["bytes_divide"]
+    assert list(O.quantize_q8_0(x, reciprocal=True)[0]) == g["bytes_reciprocal"]
+
+
+def test_q8_0_reciprocal_differs_from_divide_only_at_ties():
+    """On random blocks the two rules agree except where x/d lies within an
+    ulp of a half: the codes differ by one there."""
+    rng = np.random.default_rng(8)
+    W = (rng.standard_normal((200, 1024)) * 0.02).astype(np.float32)
+    a = O.quantize_q8_0(W).reshape(200, 32, 34)[:, :, 2:].view(np.int8).astype(int)
+    b = O.quantize_q8_0(W, reciprocal=True).reshape(200, 32, 34)[:, :, 2:].view(np.int8).astype(int)
+    diff = np.abs(a - b)
+    assert diff.max() <= 1
+    assert (diff > 0).mean() < 1e-3
