@@ -23,7 +23,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblq.so")
 
 LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_CUDA, LQ_ERR_DEVICE_TIMEOUT = range(5)
-FMT = {"f16": 0, "q8_0": 1, "q4_0": 2}
+FMT = {"f16": 0, "q8_0": 1, "q4_0": 2, "q4_0i": 3}  # q4_0i: the pages' interleaved nibbles
 ROUTE_AUTO, ROUTE_STREAM, ROUTE_TENSOR_CORE, ROUTE_GENERIC = range(4)
 
 # every symbol include/lq.h declares
@@ -36,6 +36,7 @@ EXPORTS = [
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
     "lq_gemv_argmax", "lq_argmax_f32", "lq_matmul_residual", "lq_matmul_swiglu",
+    "lq_gemv_q4_0i", "lq_gemm_q4_0i", "lq_matmul_q4_0i", "lq_pack_q4_0i", "lq_pack_q8_0_rcp",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -65,7 +66,7 @@ def lib() -> ctypes.CDLL:
             f.restype = st
         L.lq_packed_bytes.argtypes = [ctypes.c_int, i64, i64]
         L.lq_packed_bytes.restype = ctypes.c_size_t
-        for n in ("lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0"):
+        for n in ("lq_pack_f16", "lq_pack_q8_0", "lq_pack_q4_0", "lq_pack_q4_0i", "lq_pack_q8_0_rcp"):
             f = getattr(L, n)
             f.argtypes = [vp, i64, i64, vp]
             f.restype = st
@@ -242,10 +243,12 @@ def packed_bytes(fmt: str, N: int, K: int) -> int:
     return int(lib().lq_packed_bytes(FMT[fmt], int(N), int(K)))
 
 
-def pack(fmt: str, W) -> np.ndarray:
+def pack(fmt: str, W, reciprocal: bool = False) -> np.ndarray:
     """Pack f32 weights [N, K] (numpy or CPU torch) on the host.
 
     Returns uint16 [N, K] for f16 and uint8 [N, K/32*34 or *18] otherwise.
+    fmt "q4_0i" stores the pages' interleaved nibble order; reciprocal=True
+    packs Q8_0 with the pages' q = round(x * (1/d)).
     """
     if hasattr(W, "detach"):
         W = W.detach().cpu().numpy()
@@ -258,12 +261,21 @@ def pack(fmt: str, W) -> np.ndarray:
         out = np.empty((N, K), dtype=np.uint16)
     else:
         out = np.empty((N, nbytes // max(N, 1)), dtype=np.uint8)
-    _check(getattr(lib(), f"lq_pack_{fmt}")(W.ctypes.data, N, K, out.ctypes.data), f"lq_pack_{fmt}")
+    name = "lq_pack_q8_0_rcp" if (reciprocal and fmt == "q8_0") else f"lq_pack_{fmt}"
+    _check(getattr(lib(), name)(W.ctypes.data, N, K, out.ctypes.data), name)
     return out
 
 
 def lq_pack_f16(W) -> np.ndarray:
     return pack("f16", W)
+
+
+def lq_pack_q4_0i(W) -> np.ndarray:
+    return pack("q4_0i", W)
+
+
+def lq_pack_q8_0_rcp(W) -> np.ndarray:
+    return pack("q8_0", W, reciprocal=True)
 
 
 def lq_pack_q8_0(W) -> np.ndarray:

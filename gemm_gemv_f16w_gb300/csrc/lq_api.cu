@@ -75,6 +75,22 @@ namespace {
 
 bool aligned_to(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Arguments for the launchers: LQ_FMT_Q4_0I runs the Q4_0 kernels with A
+// reordered within each block (lq_q4i.cuh).
+MatmulArgs make_args(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
+                     void* stream) {
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  if (fmt == LQ_FMT_Q4_0I) {
+    a.fmt = LQ_FMT_Q4_0;
+    a.a_perm = true;
+  }
+  return a;
+}
+
+bool known_format(int fmt) {
+  return fmt == LQ_FMT_F16 || fmt == LQ_FMT_Q8_0 || fmt == LQ_FMT_Q4_0 || fmt == LQ_FMT_Q4_0I;
+}
+
 // Shared argument checks. Returns LQ_OK to proceed, or the status to return;
 // `*noop` is set when the call is a valid no-op.
 lq_status validate(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N,
@@ -101,7 +117,7 @@ lq_status do_gemv(int fmt, const float* A, const void* W, float* C, int64_t M, i
   lq_status st = validate(fmt, A, W, C, M, N, K, &noop);
   if (st != LQ_OK || noop) return st;
   if (M != 1) return LQ_ERR_INVALID_ARG;
-  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  MatmulArgs a = make_args(fmt, A, W, C, M, N, K, stream);
   if (g_force_route.load() == 3) return launch_gemv_generic(a);
   return launch_gemv(a);
 }
@@ -111,7 +127,7 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
   bool noop;
   lq_status st = validate(fmt, A, W, C, M, N, K, &noop);
   if (st != LQ_OK || noop) return st;
-  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  MatmulArgs a = make_args(fmt, A, W, C, M, N, K, stream);
   switch (g_force_route.load()) {
     case 1:
       st = launch_gemv_batch(a);
@@ -144,7 +160,7 @@ lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, fl
   if (st != LQ_OK || noop) return st;
   if (epi_kind == epi::kResidual && (!R || !aligned_to(R, 4))) return LQ_ERR_INVALID_ARG;
   if (epi_kind == epi::kSwiglu && 2 * N >= (1LL << 30)) return LQ_ERR_UNSUPPORTED;
-  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  MatmulArgs a = make_args(fmt, A, W, C, M, N, K, stream);
   a.epi = epi_kind;
   a.R = R;
   switch (g_force_route.load()) {
@@ -206,6 +222,16 @@ lq_status lq_matmul_q4_0(const float* A, const void* W, float* C, int64_t M, int
   return do_matmul(LQ_FMT_Q4_0, A, W, C, M, N, K, s);
 }
 
+lq_status lq_gemv_q4_0i(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemv(LQ_FMT_Q4_0I, A, W, C, M, N, K, s);
+}
+lq_status lq_gemm_q4_0i(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_gemm(LQ_FMT_Q4_0I, A, W, C, M, N, K, s);
+}
+lq_status lq_matmul_q4_0i(const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K, void* s) {
+  return do_matmul(LQ_FMT_Q4_0I, A, W, C, M, N, K, s);
+}
+
 const char* lq_status_string(lq_status s) {
   switch (s) {
     case LQ_OK: return "LQ_OK";
@@ -230,6 +256,7 @@ lq_status lq_last_device_error(void) {
 }
 
 lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, void* stream) {
+  if (fmt == LQ_FMT_Q4_0I) return LQ_ERR_UNSUPPORTED;  // the chain keeps A in the standard order
   if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
   if (!problems || count < 1) return LQ_ERR_INVALID_ARG;
   for (int j = 0; j < count; ++j) {
@@ -243,14 +270,14 @@ lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, voi
 
 lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C, int64_t N, int64_t K,
                          lq_argmax_result* out, void* stream) {
-  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (!known_format(fmt)) return LQ_ERR_INVALID_ARG;
   if (N < 1 || N >= (1LL << 30)) return LQ_ERR_INVALID_ARG;
   if (!out || !aligned_to(out, 8)) return LQ_ERR_INVALID_ARG;
   float* C_check = C ? C : reinterpret_cast<float*>(out);  // C may be null
   bool noop;
   lq_status st = validate(fmt, A, W, C_check, 1, N, K, &noop);
   if (st != LQ_OK) return st;
-  MatmulArgs a{A, W, C, 1, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  MatmulArgs a = make_args(fmt, A, W, C, 1, N, K, stream);
   if (g_force_route.load() != 3) {
     st = launch_gemv_argmax(a, out);
     if (st != LQ_ERR_UNSUPPORTED) return st;
@@ -264,13 +291,13 @@ lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C, int64
 
 lq_status lq_matmul_residual(int fmt, const float* A, const void* W, const float* R, float* C, int64_t M,
                              int64_t N, int64_t K, void* stream) {
-  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (!known_format(fmt)) return LQ_ERR_INVALID_ARG;
   return do_epilogue(fmt, A, W, R, C, M, N, K, epi::kResidual, stream);
 }
 
 lq_status lq_matmul_swiglu(int fmt, const float* A, const void* W, float* H, int64_t M, int64_t I, int64_t K,
                            void* stream) {
-  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (!known_format(fmt)) return LQ_ERR_INVALID_ARG;
   return do_epilogue(fmt, A, W, nullptr, H, M, I, K, epi::kSwiglu, stream);
 }
 

@@ -342,6 +342,7 @@ unsigned read_clear_gemm_error() {
 }
 
 bool gemm_tc_eligible(const MatmulArgs& a) {
+  if (a.a_perm || a.epi != 0) return false;  // neither interleaved Q4_0 nor epilogues here
   if (a.M < 2 || a.K % kBK != 0) return false;
   if (!aligned(a.A, 16)) return false;
   // W rows: 16-byte loads for f16, 4-byte loads for the block formats
@@ -351,6 +352,7 @@ bool gemm_tc_eligible(const MatmulArgs& a) {
 }
 
 lq_status launch_gemm_tc(const MatmulArgs& a) {
+  if (!gemm_tc_eligible(a)) return LQ_ERR_UNSUPPORTED;
   lq_status st;
   if (a.fmt == LQ_FMT_F16)
     st = launch_tc_fmt<LQ_FMT_F16>(a);

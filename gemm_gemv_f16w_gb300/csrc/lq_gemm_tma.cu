@@ -40,6 +40,7 @@
 #include "lq_device.cuh"
 #include "lq_epilogue.cuh"
 #include "lq_internal.h"
+#include "lq_q4i.cuh"
 #include "lq_tcgen05.cuh"
 
 namespace lq {
@@ -99,9 +100,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // between the two passes (longer rows are read twice).
 // ---------------------------------------------------------------------------
 constexpr int kPreThreads = 128, kPreKeep = 8;  // float4 per thread kept in registers
+
+// Elements 4 idx .. 4 idx + 3 of a row, scaled and rounded to f16. With perm
+// (Q4_0 with interleaved nibbles) they go to the slots of lq_q4i.cuh within
+// their block of 32: chunk i of block b puts (x, z) at halves 32b + 2i, 2i+1
+// and (y, w) at halves 32b + 16 + 2i, 17 + 2i.
+__device__ __forceinline__ void store_f16_chunk(__half2* out, int idx, float4 v, float inv, int perm) {
+  if (perm) {
+    const int b = idx >> 3, i = idx & 7;
+    out[16 * b + i] = __floats2half2_rn(v.x * inv, v.z * inv);
+    out[16 * b + 8 + i] = __floats2half2_rn(v.y * inv, v.w * inv);
+  } else {
+    out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
+    out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
+  }
+}
 __global__ void __launch_bounds__(kPreThreads) a_to_f16_kernel(const float* __restrict__ A,
                                                                __half* __restrict__ A16,
-                                                               float* __restrict__ scale, int M, int K) {
+                                                               float* __restrict__ scale, int M, int K,
+                                                               int perm) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float wmax[kPreThreads / 32];
@@ -141,16 +158,10 @@ __global__ void __launch_bounds__(kPreThreads) a_to_f16_kernel(const float* __re
 #pragma unroll
   for (int i = 0; i < kPreKeep; ++i) {
     const int idx = t + kPreThreads * i;
-    if (idx < K4) {
-      out[2 * idx] = __floats2half2_rn(keep[i].x * inv, keep[i].y * inv);
-      out[2 * idx + 1] = __floats2half2_rn(keep[i].z * inv, keep[i].w * inv);
-    }
+    if (idx < K4) store_f16_chunk(out, idx, keep[i], inv, perm);
   }
-  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads) {
-    const float4 v = __ldg(a + idx);
-    out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
-    out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
-  }
+  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads)
+    store_f16_chunk(out, idx, __ldg(a + idx), inv, perm);
   if (t == 0) scale[m] = s;
   (void)M;
 }
@@ -925,7 +936,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
   // 1. A -> f16 with per-token power-of-two scales
   cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(static_cast<unsigned>(M)), dim3(kPreThreads), 0, a.stream, a.A,
-                             static_cast<__half*>(a16), scale, M, K);
+                             static_cast<__half*>(a16), scale, M, K, a.a_perm ? 1 : 0);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return LQ_ERR_CUDA;
 

@@ -39,6 +39,7 @@
 #include "lq_epilogue.cuh"
 #include "lq_gemv_slices.cuh"
 #include "lq_internal.h"
+#include "lq_q4i.cuh"
 
 namespace lq {
 namespace {
@@ -73,6 +74,7 @@ struct GemvParams {
   unsigned amax_warps;       // argmax variant: consumer warps of the grid
   const float* R;            // residual variant: added to every output
   long long up_off;          // swiglu variant: bytes from a gate row to its up row
+  int a_perm;                // Q4_0 with interleaved nibbles: A reordered per block
 };
 
 struct Header {
@@ -222,7 +224,11 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     const uint32_t sa = smem_u32(sA), sg = smem_u32(stage_a);
     for (int q = warp * 32 + lane; q < p.K / 4; q += active * 32) {
       const uint4 v = lds128(sg + 16u * q);
-      sts128(sa + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes + 16u * (q & 7), v);
+      const uint32_t blk = sa + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes;
+      if (p.a_perm)
+        q4i::store_chunk(blk, q & 7, v);
+      else
+        sts128(blk + 16u * (q & 7), v);
     }
     named_barrier(1, static_cast<uint32_t>(active) * 32u);
   }
@@ -305,9 +311,10 @@ __device__ __forceinline__ float load_f16_bytes(const uint8_t* p) {
   return __half2float(__ushort_as_half(b));
 }
 
-// The dot product of one W row with one row of A, summed over the warp.
+// The dot product of one W row with one row of A, summed over the warp
+// (il: Q4_0 with interleaved nibbles, byte j = elements 2j and 2j+1).
 template <int FMT>
-__device__ __forceinline__ float generic_row_dot(const float* a, const uint8_t* w, int K, int lane) {
+__device__ __forceinline__ float generic_row_dot(const float* a, const uint8_t* w, int K, int lane, bool il) {
   float acc = 0.f;
   if (FMT == LQ_FMT_F16) {
     const __half* wh = reinterpret_cast<const __half*>(w);
@@ -326,8 +333,8 @@ __device__ __forceinline__ float generic_row_dot(const float* a, const uint8_t* 
       float s = 0.f;
       for (int i = 0; i < 16; ++i) {
         const int byte = blk[2 + i];
-        s = fmaf(static_cast<float>((byte & 0xF) - 8), a[32 * b + i], s);
-        s = fmaf(static_cast<float>((byte >> 4) - 8), a[32 * b + 16 + i], s);
+        s = fmaf(static_cast<float>((byte & 0xF) - 8), a[32 * b + (il ? 2 * i : i)], s);
+        s = fmaf(static_cast<float>((byte >> 4) - 8), a[32 * b + (il ? 2 * i + 1 : 16 + i)], s);
       }
       acc = fmaf(load_f16_bytes(blk), s, acc);
     }
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(256) generic_matmul_kernel(const float* __rest
                                                              const uint8_t* __restrict__ W,
                                                              float* __restrict__ C, int M, int N,
                                                              int K, long long row_bytes,
-                                                             const float* __restrict__ R) {
+                                                             const float* __restrict__ R, int il) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = blockIdx.x * 8 + warp;
   pdl_wait();
@@ -351,9 +358,9 @@ __global__ void __launch_bounds__(256) generic_matmul_kernel(const float* __rest
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     const float* a = A + static_cast<long long>(m) * K;
     const long long o = static_cast<long long>(m) * N + n;
-    const float acc = generic_row_dot<FMT>(a, w, K, lane);
+    const float acc = generic_row_dot<FMT>(a, w, K, lane, il != 0);
     if constexpr (EPI == epi::kSwiglu) {
-      const float up = generic_row_dot<FMT>(a, w + static_cast<long long>(N) * row_bytes, K, lane);
+      const float up = generic_row_dot<FMT>(a, w + static_cast<long long>(N) * row_bytes, K, lane, il != 0);
       if (lane == 0) C[o] = epi::swiglu(acc, up);
     } else if constexpr (EPI == epi::kResidual) {
       if (lane == 0) C[o] = acc + R[o];
@@ -464,7 +471,7 @@ lq_status launch_gemv_generic(const MatmulArgs& a) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
   if (a.epi != epi::kPlain && a.epi != epi::kResidual && a.epi != epi::kSwiglu) return LQ_ERR_UNSUPPORTED;
   auto go = [&](auto kern) {
-    return launch(kern, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb, a.R);
+    return launch(kern, grid, dim3(256), 0, a.stream, a.A, W, a.C, M, N, K, rb, a.R, a.a_perm ? 1 : 0);
   };
   auto by_epi = [&](auto fmt_tag) {
     constexpr int F = decltype(fmt_tag)::value;
@@ -567,6 +574,7 @@ GemvPlan plan_gemv(const MatmulArgs& a, int ctas_per_sm, int max_rows, int smem_
   p.l2_prefetch = !swiglu && static_cast<int64_t>(a.N) * rb <= kL2PrefetchMaxBytes ? 1 : 0;
   p.R = a.R;
   p.up_off = static_cast<long long>(a.N) * wrb;
+  p.a_perm = a.a_perm ? 1 : 0;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   pl.cpw = wg.cpw;

@@ -29,6 +29,7 @@
 #include "lq_epilogue.cuh"
 #include "lq_gemv_slices_batch.cuh"
 #include "lq_internal.h"
+#include "lq_q4i.cuh"
 
 namespace lq {
 namespace {
@@ -65,6 +66,7 @@ struct BatchParams {
   unsigned wait_iters;
   const float* R;         // residual epilogue: added to every output
   long long up_off;       // swiglu epilogue: bytes from a gate row to its up row
+  int a_perm;             // Q4_0 with interleaved nibbles: A reordered per block
 };
 
 template <int MT>
@@ -171,9 +173,12 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
         for (int c = warp * 32 + lane; c < p.M * per; c += active * 32) {
           const int t = c / per, q = c - t * per;
           const uint4 v = lds128(sg + 16u * c);
-          sts128(sa + static_cast<uint32_t>(t * p.a_slot) +
-                     static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes + 16u * (q & 7),
-                 v);
+          const uint32_t blk =
+              sa + static_cast<uint32_t>(t * p.a_slot) + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes;
+          if (p.a_perm)
+            q4i::store_chunk(blk, q & 7, v);
+          else
+            sts128(blk + 16u * (q & 7), v);
         }
         named_barrier(2, static_cast<uint32_t>(active) * 32u);
         if (threadIdx.x == 0) {
@@ -395,6 +400,7 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   p.rows_per_stage = RS;
   p.R = a.R;
   p.up_off = static_cast<long long>(N) * wrb;
+  p.a_perm = a.a_perm ? 1 : 0;
   p.nk = nk;
   p.nr = nr;
   p.stages = S;

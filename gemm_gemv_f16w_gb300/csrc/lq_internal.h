@@ -20,6 +20,10 @@ struct MatmulArgs {
   cudaStream_t stream;
   int epi = 0;        // lq::epi kind (0: plain)
   const float* R = nullptr;
+  // Q4_0 weights with interleaved nibbles (LQ_FMT_Q4_0I, fmt is then
+  // LQ_FMT_Q4_0): the kernels read A reordered within each block of 32
+  // (lq_q4i.cuh); launchers that cannot do so return LQ_ERR_UNSUPPORTED
+  bool a_perm = false;
 };
 
 // Per-device facts cached on first use.

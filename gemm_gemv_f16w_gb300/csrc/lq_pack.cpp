@@ -35,15 +35,18 @@ inline void put_d(uint8_t* dst, float d) {
   dst[1] = static_cast<uint8_t>(b >> 8);
 }
 
-void q8_0_block(const float* x, uint8_t* out) {
+// reciprocal: q = round(x * (1/d)) as quantize_row_q8_0 computes it;
+// otherwise q = round(x / d) as the matmul statement writes it
+void q8_0_block(const float* x, uint8_t* out, bool reciprocal) {
   float amax = 0.0f;
   for (int i = 0; i < 32; ++i) amax = std::fmax(amax, std::fabs(x[i]));
   const float d = amax / 127.0f;
+  const float id = d != 0.0f ? 1.0f / d : 0.0f;
   put_d(out, d);
   for (int i = 0; i < 32; ++i) {
     int q = 0;
     if (d != 0.0f) {
-      const float v = x[i] / d;
+      const float v = reciprocal ? x[i] * id : x[i] / d;
       float r = std::round(v);  // halves away from zero
       if (r > 127.0f) r = 127.0f;
       if (r < -127.0f) r = -127.0f;
@@ -53,7 +56,9 @@ void q8_0_block(const float* x, uint8_t* out) {
   }
 }
 
-void q4_0_block(const float* x, uint8_t* out) {
+// interleaved: byte j holds elements 2j (low nibble) and 2j+1 (high), the
+// order gemv_q4_decode reads; otherwise elements j and j+16
+void q4_0_block(const float* x, uint8_t* out, bool interleaved) {
   float m = x[0], amax = std::fabs(x[0]);
   for (int i = 1; i < 32; ++i) {
     const float a = std::fabs(x[i]);
@@ -75,7 +80,10 @@ void q4_0_block(const float* x, uint8_t* out) {
       q[i] = static_cast<uint8_t>(v);
     }
   }
-  for (int j = 0; j < 16; ++j) out[2 + j] = static_cast<uint8_t>((q[j] & 0xF) | ((q[j + 16] & 0xF) << 4));
+  for (int j = 0; j < 16; ++j) {
+    const int lo = interleaved ? q[2 * j] : q[j], hi = interleaved ? q[2 * j + 1] : q[j + 16];
+    out[2 + j] = static_cast<uint8_t>((lo & 0xF) | ((hi & 0xF) << 4));
+  }
 }
 
 bool all_finite(const float* W, int64_t n) {
@@ -113,12 +121,38 @@ bool shape_ok(int64_t N, int64_t K, bool quant) {
 
 }  // namespace
 
+namespace {
+lq_status pack_q8(const float* W, int64_t N, int64_t K, void* out, bool reciprocal) {
+  if (!shape_ok(N, K, true) || (N > 0 && (!W || !out))) return LQ_ERR_INVALID_ARG;
+  if (!all_finite(W, N * K)) return LQ_ERR_INVALID_ARG;
+  const int64_t nb = K / 32;
+  auto* o = static_cast<uint8_t*>(out);
+  parallel_rows(N, K, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n)
+      for (int64_t j = 0; j < nb; ++j) q8_0_block(W + n * K + 32 * j, o + (n * nb + j) * 34, reciprocal);
+  });
+  return LQ_OK;
+}
+
+lq_status pack_q4(const float* W, int64_t N, int64_t K, void* out, bool interleaved) {
+  if (!shape_ok(N, K, true) || (N > 0 && (!W || !out))) return LQ_ERR_INVALID_ARG;
+  if (!all_finite(W, N * K)) return LQ_ERR_INVALID_ARG;
+  const int64_t nb = K / 32;
+  auto* o = static_cast<uint8_t*>(out);
+  parallel_rows(N, K, [&](int64_t b, int64_t e) {
+    for (int64_t n = b; n < e; ++n)
+      for (int64_t j = 0; j < nb; ++j) q4_0_block(W + n * K + 32 * j, o + (n * nb + j) * 18, interleaved);
+  });
+  return LQ_OK;
+}
+}  // namespace
+
 extern "C" {
 
 size_t lq_packed_bytes(int fmt, int64_t N, int64_t K) {
   if (fmt == LQ_FMT_F16) return shape_ok(N, K, false) ? static_cast<size_t>(N * K * 2) : 0;
   if (fmt == LQ_FMT_Q8_0) return shape_ok(N, K, true) ? static_cast<size_t>(N * (K / 32) * 34) : 0;
-  if (fmt == LQ_FMT_Q4_0) return shape_ok(N, K, true) ? static_cast<size_t>(N * (K / 32) * 18) : 0;
+  if (fmt == LQ_FMT_Q4_0 || fmt == LQ_FMT_Q4_0I) return shape_ok(N, K, true) ? static_cast<size_t>(N * (K / 32) * 18) : 0;
   return 0;
 }
 
@@ -136,28 +170,10 @@ lq_status lq_pack_f16(const float* W, int64_t N, int64_t K, void* out) {
   return LQ_OK;
 }
 
-lq_status lq_pack_q8_0(const float* W, int64_t N, int64_t K, void* out) {
-  if (!shape_ok(N, K, true) || (N > 0 && (!W || !out))) return LQ_ERR_INVALID_ARG;
-  if (!all_finite(W, N * K)) return LQ_ERR_INVALID_ARG;
-  const int64_t nb = K / 32;
-  auto* o = static_cast<uint8_t*>(out);
-  parallel_rows(N, K, [&](int64_t b, int64_t e) {
-    for (int64_t n = b; n < e; ++n)
-      for (int64_t j = 0; j < nb; ++j) q8_0_block(W + n * K + 32 * j, o + (n * nb + j) * 34);
-  });
-  return LQ_OK;
-}
 
-lq_status lq_pack_q4_0(const float* W, int64_t N, int64_t K, void* out) {
-  if (!shape_ok(N, K, true) || (N > 0 && (!W || !out))) return LQ_ERR_INVALID_ARG;
-  if (!all_finite(W, N * K)) return LQ_ERR_INVALID_ARG;
-  const int64_t nb = K / 32;
-  auto* o = static_cast<uint8_t*>(out);
-  parallel_rows(N, K, [&](int64_t b, int64_t e) {
-    for (int64_t n = b; n < e; ++n)
-      for (int64_t j = 0; j < nb; ++j) q4_0_block(W + n * K + 32 * j, o + (n * nb + j) * 18);
-  });
-  return LQ_OK;
-}
+lq_status lq_pack_q8_0(const float* W, int64_t N, int64_t K, void* out) { return pack_q8(W, N, K, out, false); }
+lq_status lq_pack_q8_0_rcp(const float* W, int64_t N, int64_t K, void* out) { return pack_q8(W, N, K, out, true); }
+lq_status lq_pack_q4_0(const float* W, int64_t N, int64_t K, void* out) { return pack_q4(W, N, K, out, false); }
+lq_status lq_pack_q4_0i(const float* W, int64_t N, int64_t K, void* out) { return pack_q4(W, N, K, out, true); }
 
 }  // extern "C"

@@ -64,7 +64,12 @@ typedef enum {
   LQ_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait ran out            */
 } lq_status;
 
-typedef enum { LQ_FMT_F16 = 0, LQ_FMT_Q8_0 = 1, LQ_FMT_Q4_0 = 2 } lq_format;
+/* Weight formats. LQ_FMT_Q4_0I is Q4_0 with the nibble order the pages' own
+ * Q4 kernels read (gemv_q4_decode, gemm_q4: the low nibble of byte j is
+ * element 2j, the high nibble element 2j+1); LQ_FMT_Q4_0 keeps elements
+ * 0-15 in the low nibbles and 16-31 in the high ones. Same 18-byte blocks,
+ * same scale, same values. */
+typedef enum { LQ_FMT_F16 = 0, LQ_FMT_Q8_0 = 1, LQ_FMT_Q4_0 = 2, LQ_FMT_Q4_0I = 3 } lq_format;
 
 /* ---- decode GEMV, M == 1 (M != 1 -> LQ_ERR_INVALID_ARG) -----------------
  * One pass over W: each output C[0,n] = sum_k A[0,k] * w(n,k), accumulated
@@ -101,6 +106,19 @@ lq_status lq_matmul_q8_0(const float* A, const void* W, float* C,
 lq_status lq_matmul_q4_0(const float* A, const void* W, float* C,
                          int64_t M, int64_t N, int64_t K, void* stream);
 
+/* ---- Q4_0 with interleaved nibbles (LQ_FMT_Q4_0I) -----------------------
+ * As lq_gemv_q4_0 / lq_gemm_q4_0 / lq_matmul_q4_0, for weights packed by
+ * lq_pack_q4_0i (byte j of a block: element 2j low, 2j+1 high). Same routes,
+ * results and tolerances; A is read in the reordered sequence the nibble
+ * order needs. lq_gemm_noalloc and lq_gemv_chain do not take this format
+ * (LQ_ERR_INVALID_ARG and LQ_ERR_UNSUPPORTED). */
+lq_status lq_gemv_q4_0i(const float* A, const void* W, float* C,
+                        int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_gemm_q4_0i(const float* A, const void* W, float* C,
+                        int64_t M, int64_t N, int64_t K, void* stream);
+lq_status lq_matmul_q4_0i(const float* A, const void* W, float* C,
+                          int64_t M, int64_t N, int64_t K, void* stream);
+
 /* ---- host-side packers (HOST memory in, HOST memory out) ----------------
  * make_buffer_f16 / quantize_row_q8_0 (metal_qwen35.rs) and the Q4_0 rule:
  *   f16 : RNE narrowing of every element.
@@ -115,6 +133,12 @@ size_t    lq_packed_bytes(int fmt, int64_t N, int64_t K); /* 0 if invalid */
 lq_status lq_pack_f16 (const float* W_host, int64_t N, int64_t K, void* out_host);
 lq_status lq_pack_q8_0(const float* W_host, int64_t N, int64_t K, void* out_host);
 lq_status lq_pack_q4_0(const float* W_host, int64_t N, int64_t K, void* out_host);
+/* The pages' own variants: Q4_0 with interleaved nibbles (LQ_FMT_Q4_0I), and
+ * Q8_0 rounded as quantize_row_q8_0 computes it, q = round(x * (1/d)) with
+ * 1/d in float32 (ordinary Q8_0 bytes; a code can differ by one from
+ * lq_pack_q8_0's where x/d is within an ulp of a half). */
+lq_status lq_pack_q4_0i(const float* W_host, int64_t N, int64_t K, void* out_host);
+lq_status lq_pack_q8_0_rcp(const float* W_host, int64_t N, int64_t K, void* out_host);
 
 /* ---- decode chain: many M = 1 GEMVs in one launch ------------------------
  * (An addition of this library for the decode step the source pages run as

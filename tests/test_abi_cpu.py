@@ -61,13 +61,13 @@ def _adversarial(K=256):
     return np.stack(rows)
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
 def test_packer_bit_exact_adversarial(lq, fmt):
     W = _adversarial()
     assert np.array_equal(lq.pack(fmt, W).view(np.uint8), O.pack(fmt, W).view(np.uint8))
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_packer_bit_exact_random(lq, fmt, seed):
     rng = np.random.default_rng(seed)
@@ -75,6 +75,23 @@ def test_packer_bit_exact_random(lq, fmt, seed):
     W = (rng.standard_normal((N, K)) * rng.choice([0.02, 1.0, 300.0])).astype(np.float32)
     W[rng.integers(0, N)] *= 20
     assert np.array_equal(lq.pack(fmt, W).view(np.uint8), O.pack(fmt, W).view(np.uint8))
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_packer_q8_0_reciprocal_bit_exact(lq, seed):
+    """The pages' round(x * (1/d)): byte for byte with the oracle, on random
+    weights and on the golden block where it differs from round(x / d)."""
+    rng = np.random.default_rng(seed)
+    W = (rng.standard_normal((64, 512)) * rng.choice([0.02, 1.0, 300.0])).astype(np.float32)
+    W = np.concatenate([W, _adversarial(512)])
+    got = lq.pack("q8_0", W, reciprocal=True)
+    assert np.array_equal(got, O.quantize_q8_0(W, reciprocal=True))
+    import json
+    with open(os.path.join(ROOT, "tests", "golden", "q8_0_reciprocal.json")) as f:
+        g = json.load(f)
+    x = np.array(g["x_bits"], dtype=np.uint32).view(np.float32)[None, :]
+    assert list(lq.pack("q8_0", x, reciprocal=True)[0]) == g["bytes_reciprocal"]
+    assert list(lq.pack("q8_0", x)[0]) == g["bytes_divide"]
 
 
 @pytest.mark.parametrize("name", ["gemv_q8_0_4096x4096", "gemv_q4_0_11008x4096_outliers",
@@ -102,7 +119,7 @@ def _raw(lq, name, A, W, C, M, N, K):
 
 
 @pytest.mark.parametrize("kind", ["gemv", "gemm", "matmul"])
-@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
 def test_argument_errors_return_before_launch(lq, kind, fmt):
     name = f"lq_{kind}_{fmt}"
     # never dereferenced: every call below fails validation or is a no-op
