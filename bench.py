@@ -190,6 +190,7 @@ class Workbench:
                 self.problems = None  # outside the chain's path: separate calls
             torch.cuda.synchronize(dev)
         self.mode = mode if self.problems is not None else "calls"
+        self.route = None
         self.res = None
         if mode.startswith("argmax") and w.M == 1:
             self.mode = mode
@@ -220,10 +221,15 @@ class Workbench:
     def capture(self):
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
+        self.lq.reset_counts()
         with torch.cuda.stream(s):
             self.step()          # eager warm-up (sets kernel attributes)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)
+        if self.w.M >= 2 and self.lq.route_count(1) >= self.R:
+            # M = 2..4 on the batched decode kernel: one launch a matmul
+            self.route = "batch"
+            self.kernels_per_step = self.R
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step()
@@ -378,8 +384,10 @@ def main():
     ap.add_argument("--extras", default="all",
                     help="comma-separated extra workloads to time, 'all' or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", default="auto", choices=["auto", "calls", "chain", "chain-dependent"],
-                    help="how the headline step runs its matmuls (auto: chain for M = 1)")
+    ap.add_argument("--mode", default="auto",
+                    choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused"],
+                    help="how the headline step runs its matmuls (auto: chain for M = 1; argmax modes: "
+                         "M = 1, the GEMV with its argmax)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -425,7 +433,10 @@ def main():
         dt = wb.time_graph(steps, args.warmup, barrier)
     dt = max_over_ranks(dt)
     clocks = clk.summary()
-    kernel = KERNEL_OF_MODE[wb.mode] if w.M == 1 else "gemm_tma_kernel"
+    if w.M == 1:
+        kernel = KERNEL_OF_MODE[wb.mode]
+    else:
+        kernel = "gemv_batch_kernel" if wb.route == "batch" else "gemm_tma_kernel"
     launches_per_step = wb.kernels_per_step
     per_gemv = dt / (steps * wb.R)          # one matmul of the workload
     val1, unit, bound = rate(wb, per_gemv)
