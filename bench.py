@@ -318,6 +318,17 @@ def cpu_cores():
 
 
 # ---------------------------------------------------------------- main
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of the ranks' values (the job is as slow as its slowest
+    rank); the value itself with one rank."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def init_dist(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -342,7 +353,7 @@ def run_reference(args, world, rank):
     steps, warmup = args.steps or 20, args.warmup
     _, _, _, dt1 = oracle_rate(w, 0.0, rows=64)
     per_row = dt1 / 64
-    rows = int(max(8, min(w.N, 60.0 / max(steps + warmup, 1) / max(per_row, 1e-9))))
+    rows = int(max(8, min(w.N, args.ref_seconds / max(steps + warmup, 1) / max(per_row, 1e-9))))
     W, A = synthetic.draw_workload(w)
     packed = O.pack(w.fmt, W.numpy()[:rows])
     An = A.numpy()
@@ -384,6 +395,8 @@ def main():
     ap.add_argument("--extras", default="all",
                     help="comma-separated extra workloads to time, 'all' or 'none'")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: seconds of oracle work the whole run aims at")
     ap.add_argument("--mode", default="auto",
                     choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused"],
                     help="how the headline step runs its matmuls (auto: chain for M = 1; argmax modes: "
@@ -414,13 +427,8 @@ def main():
             import torch.distributed as dist
             dist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def ranks_max(x: float) -> float:
+        return max_over_ranks(x, world, dev)
 
     # ---- headline workload
     w = synthetic.WORKLOADS[args.workload]
@@ -431,7 +439,7 @@ def main():
     lq.reset_counts()
     with ClockSampler(local) as clk:
         dt = wb.time_graph(steps, args.warmup, barrier)
-    dt = max_over_ranks(dt)
+    dt = ranks_max(dt)
     clocks = clk.summary()
     if w.M == 1:
         kernel = KERNEL_OF_MODE[wb.mode]
@@ -451,7 +459,7 @@ def main():
                 "kernel": kernel, "algorithmic_per_launch": work_per_launch,
                 "us_per_launch": per_launch * 1e6}
     e2e_dt, h2d, d2h, _ = wb.time_e2e(steps)
-    e2e_dt = max_over_ranks(e2e_dt)
+    e2e_dt = ranks_max(e2e_dt)
     e2e_val = wb.bytes_per_launch * wb.R * steps / e2e_dt / 1e9 * world
     wb.free()
 
@@ -470,7 +478,7 @@ def main():
         xb.capture()
         p = xb.time_graph(2, 1)
         n = max(5, int(0.25 / max(p / 2, 1e-7)))
-        d = max_over_ranks(xb.time_graph(n, 3, barrier))
+        d = ranks_max(xb.time_graph(n, 3, barrier))
         pl = d / (n * xb.R)
         v, u, b = rate(xb, pl)
         pk = hbm_peak if b == "hbm" else tc_peak
