@@ -258,6 +258,20 @@ class Workbench:
             barrier()
         return t0.elapsed_time(t1) / 1e3
 
+    def replay_spread(self, n: int):
+        """p10 / p50 / p90 of the device time of single graph replays, per
+        matmul, in µs (each replay bracketed by its own CUDA events)."""
+        stream = torch.cuda.current_stream(self.dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            self.graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize(self.dev)
+        us = sorted(a.elapsed_time(b) * 1e3 / self.R for a, b in ev)
+        q = lambda f: us[min(len(us) - 1, int(f * len(us)))]
+        return {"unit": "us_per_matmul", "p10": q(0.1), "p50": q(0.5), "p90": q(0.9), "replays": n}
+
     def time_e2e(self, steps: int):
         """Through the public API with host buffers: per step the pinned A
         goes to the device, the router runs on every copy, C comes back to
@@ -441,6 +455,7 @@ def main():
         dt = wb.time_graph(steps, args.warmup, barrier)
     dt = ranks_max(dt)
     clocks = clk.summary()
+    spread = wb.replay_spread(100)  # outside the timed region
     if w.M == 1:
         kernel = KERNEL_OF_MODE[wb.mode]
     else:
@@ -514,6 +529,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": steps * launches_per_step,
             "clocks": clocks,
+            "spread": spread,
             "workloads": extras,
         }
         print(json.dumps(line), flush=True)
