@@ -733,7 +733,8 @@ int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == L
 // Ring depths for a token tile of bt: the raw W ring first (W comes from
 // HBM: up to 6 raw stages of f16, 4 of Q8_0 / Q4_0, i.e. 6 to 8 pipeline
 // stages of lookahead), then as many A stages (bt rows x 128 K halves, from
-// L2) as fit, at least two of each.
+// L2) as fit, at least two of each; where that leaves two A stages, three A
+// stages over fewer raw stages.
 struct RingPlan {
   int a_stages = 0, raw_stages = 0;
 };
@@ -750,6 +751,12 @@ RingPlan ring_plan(int fmt, int bt) {
   if (rp.raw_stages < 2) return RingPlan{};
   rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
   if (rp.a_stages < 2) return RingPlan{};
+  // Large token tiles leave room for two A stages only: three A stages over
+  // two raw stages measured about 5 % faster at M = 512 (f16 and Q8_0).
+  if (rp.a_stages == 2 && 3 * a_stage + 2 * raw <= budget) {
+    rp.a_stages = 3;
+    rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 3 * a_stage) / raw));
+  }
   const int oa = g_ring_a.load(), orr = g_ring_raw.load();
   if (oa || orr) {
     const int a2 = oa ? oa : rp.a_stages, r2 = orr ? orr : rp.raw_stages;
