@@ -447,6 +447,21 @@ def swiglu_reference(y, tol, I: int):
     return h, prop + 8 * F32_EPS * (np.abs(h) + prop) + 1e-30
 
 
+def topk_first(y, k: int):
+    """The k best entries of y as (values, indices), best first: larger value
+    first, equal values by the lower index, NaN never chosen (topk_better and
+    the k candidates logits_topk_first_pass / logits_topk_merge_pass keep,
+    lattice-inference 0.1.2, metal_qwen35.rs). Fewer than k non-NaN entries:
+    the rest are the pages' sentinel, value -inf and index -1 (UINT_MAX)."""
+    y = np.asarray(y, dtype=np.float64).reshape(-1)
+    idx = [i for i in range(y.size) if not np.isnan(y[i])]
+    # -0 and +0 compare equal, as the pages' float comparison does
+    idx.sort(key=lambda i: (-(y[i] + 0.0), i))
+    idx = idx[:k]
+    vals = [float(y[i]) for i in idx] + [-np.inf] * (k - len(idx))
+    return np.array(vals, dtype=np.float64), np.array(idx + [-1] * (k - len(idx)), dtype=np.int64)
+
+
 def argmax_first(y) -> int:
     """Index of the largest value; ties go to the lowest index, NaN never wins."""
     y = np.asarray(y, dtype=np.float64)

@@ -175,3 +175,31 @@ def test_synthetic_recipe():
     big = torch.isclose(ratio, torch.tensor(20.0))
     assert int(big.sum()) == synthetic.n_outlier_blocks(64, 128, 0.05)
     assert abs(float(W0.std()) - 0.02) < 0.002
+
+
+def test_topk_first_against_lexsort_and_brute_force():
+    """topk_first against numpy's lexsort (an independent ordering routine)
+    on random data with planted ties and NaN, and against argmax_first."""
+    rng = np.random.default_rng(3)
+    for n, k in [(1, 1), (7, 3), (100, 64), (1000, 50), (5, 9)]:
+        y = rng.standard_normal(n)
+        if n > 10:
+            y[rng.choice(n, n // 10, replace=False)] = np.nan
+            y[rng.choice(n, 5, replace=False)] = np.nanmax(y)     # a tie at the top
+            y[rng.choice(n, 3, replace=False)] = -np.inf
+        v, i = O.topk_first(y, k)
+        ok = np.nonzero(~np.isnan(y))[0]
+        order = ok[np.lexsort((ok, -y[ok]))][:k]
+        assert list(i[:len(order)]) == list(order)
+        assert np.all(i[len(order):] == -1) and np.all(np.isneginf(v[len(order):]))
+        assert np.array_equal(v[:len(order)], y[order])
+        assert i[0] == O.argmax_first(y)
+
+
+def test_topk_first_special_values():
+    v, i = O.topk_first([0.0, -0.0, 1.0, np.nan, -0.0], 4)
+    assert list(i) == [2, 0, 1, 4]          # -0 and +0 tie: by index
+    v, i = O.topk_first([np.nan, np.nan], 2)
+    assert list(i) == [-1, -1] and np.all(np.isneginf(v))
+    v, i = O.topk_first([-np.inf, 3.0, -np.inf], 3)
+    assert list(i) == [1, 0, 2]             # real -inf entries come before the sentinel
