@@ -37,6 +37,7 @@ EXPORTS = [
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
     "lq_gemv_argmax", "lq_argmax_f32", "lq_matmul_residual", "lq_matmul_swiglu",
     "lq_gemv_q4_0i", "lq_gemm_q4_0i", "lq_matmul_q4_0i", "lq_pack_q4_0i", "lq_pack_q8_0_rcp",
+    "lq_topk_work_bytes", "lq_topk_f32", "lq_gemv_topk",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -99,6 +100,12 @@ def lib() -> ctypes.CDLL:
         L.lq_matmul_residual.restype = st
         L.lq_matmul_swiglu.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
         L.lq_matmul_swiglu.restype = st
+        L.lq_topk_work_bytes.argtypes = [i64, ctypes.c_int]
+        L.lq_topk_work_bytes.restype = ctypes.c_size_t
+        L.lq_topk_f32.argtypes = [vp, i64, ctypes.c_int, vp, vp, vp, vp]
+        L.lq_topk_f32.restype = st
+        L.lq_gemv_topk.argtypes = [st, vp, vp, vp, i64, i64, ctypes.c_int, vp, vp, vp, vp]
+        L.lq_gemv_topk.restype = st
         _lib = L
     return _lib
 
@@ -220,6 +227,29 @@ def lq_gemv_argmax(fmt, A, W, C, N, K, out, stream=None):
 def lq_argmax_f32(x, n, out, stream=None):
     """Argmax of n device floats into the device lq_argmax_result `out`."""
     _check(lib().lq_argmax_f32(_ptr(x), int(n), _ptr(out), _stream(stream)), "lq_argmax_f32")
+
+
+# ---- top-k ----------------------------------------------------------------
+def topk_buffers(n, k, dev=None):
+    """(values, indices, work) device buffers for a top-k of n entries."""
+    import torch
+    dev = dev or "cuda"
+    nbytes = int(lib().lq_topk_work_bytes(int(n), int(k)))
+    if nbytes == 0:
+        raise LQError(LQ_ERR_INVALID_ARG, "lq_topk_work_bytes")
+    return (torch.empty(k, dtype=torch.float32, device=dev), torch.empty(k, dtype=torch.int32, device=dev),
+            torch.empty(nbytes // 8, dtype=torch.int64, device=dev))
+
+
+def lq_topk_f32(x, n, k, values, indices, work, stream=None):
+    _check(lib().lq_topk_f32(_ptr(x), int(n), int(k), _ptr(values), _ptr(indices), _ptr(work),
+                             _stream(stream)), "lq_topk_f32")
+
+
+def lq_gemv_topk(fmt, A, W, C, N, K, k, values, indices, work, stream=None):
+    f = FMT[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(lib().lq_gemv_topk(f, _ptr(A), _ptr(W), _ptr(C), int(N), int(K), int(k), _ptr(values),
+                              _ptr(indices), _ptr(work), _stream(stream)), "lq_gemv_topk")
 
 
 # ---- epilogue fusions ----------------------------------------------------

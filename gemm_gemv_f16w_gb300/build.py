@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblq.so")
 
-CUDA_SOURCES = ["lq_api.cu", "lq_gemv.cu", "lq_gemv_chain.cu", "lq_gemv_batch.cu", "lq_argmax.cu", "lq_gemm.cu", "lq_gemm_tma.cu",
+CUDA_SOURCES = ["lq_api.cu", "lq_gemv.cu", "lq_gemv_chain.cu", "lq_gemv_batch.cu", "lq_argmax.cu", "lq_topk.cu", "lq_gemm.cu", "lq_gemm_tma.cu",
                 "lq_noalloc.cu"]
 CXX_SOURCES = ["lq_pack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -307,6 +307,30 @@ lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* 
   return launch_argmax_f32(x, n, out, static_cast<cudaStream_t>(stream));
 }
 
+size_t lq_topk_work_bytes(int64_t n, int k) {
+  if (n < 1 || n >= (1LL << 31) || k < 1 || k > 64) return 0;
+  return static_cast<size_t>(topk_ctas(n)) * static_cast<size_t>(k) * 8u;
+}
+
+lq_status lq_topk_f32(const float* x, int64_t n, int k, float* values, int32_t* indices, void* work,
+                      void* stream) {
+  if (!x || !aligned_to(x, 4) || n < 1 || n >= (1LL << 31) || k < 1 || k > 64) return LQ_ERR_INVALID_ARG;
+  if (!values || !aligned_to(values, 4) || !indices || !aligned_to(indices, 4)) return LQ_ERR_INVALID_ARG;
+  if (!work || !aligned_to(work, 8)) return LQ_ERR_INVALID_ARG;
+  return launch_topk_f32(x, n, k, values, indices, work, static_cast<cudaStream_t>(stream));
+}
+
+lq_status lq_gemv_topk(int fmt, const float* A, const void* W, float* C, int64_t N, int64_t K, int k,
+                       float* values, int32_t* indices, void* work, void* stream) {
+  if (!known_format(fmt) || !C) return LQ_ERR_INVALID_ARG;
+  if (N < 1 || N >= (1LL << 30) || k < 1 || k > 64) return LQ_ERR_INVALID_ARG;
+  if (!values || !aligned_to(values, 4) || !indices || !aligned_to(indices, 4)) return LQ_ERR_INVALID_ARG;
+  if (!work || !aligned_to(work, 8)) return LQ_ERR_INVALID_ARG;
+  const lq_status st = do_gemv(fmt, A, W, C, 1, N, K, stream);
+  if (st != LQ_OK) return st;
+  return launch_topk_f32(C, N, k, values, indices, work, static_cast<cudaStream_t>(stream));
+}
+
 const char* lq_version(void) { return "lq 0.1.0 (sm_103a)"; }
 
 lq_status lq_debug_force_route(int route) {

@@ -78,6 +78,12 @@ void set_gemm_rings(int a_stages, int raw_stages);
 lq_status launch_gemv_argmax(const MatmulArgs& a, lq_argmax_result* out);
 lq_status launch_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, cudaStream_t stream);
 
+// Top-k (lq_topk_f32): CTAs of the first pass for n inputs, and the launch
+// (work holds topk_ctas(n) * k keys of 8 bytes).
+int64_t topk_ctas(int64_t n);
+lq_status launch_topk_f32(const float* x, int64_t n, int k, float* values, int32_t* indices, void* work,
+                          cudaStream_t stream);
+
 // Decode chain (lq_gemv_chain); LQ_ERR_UNSUPPORTED when the problems do not
 // fit its fast path.
 lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, cudaStream_t stream);

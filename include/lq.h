@@ -228,6 +228,26 @@ lq_status lq_gemv_argmax(int fmt, const float* A, const void* W, float* C,
  * x 4-byte aligned. */
 lq_status lq_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, void* stream);
 
+/* ---- top-k --------------------------------------------------------------
+ * The k best entries (1 <= k <= 64), best first, in the order of the argmax
+ * above (larger value first, equal values by the lower index, NaN never
+ * chosen); when fewer than k entries are not NaN the rest are the pages'
+ * sentinel (value -inf, index -1). logits_topk_first_pass /
+ * logits_topk_merge_pass (lattice-inference 0.1.2, src/forward/
+ * metal_qwen35.rs), as two launches: per-CTA candidates, then one merge.
+ * values (k floats), indices (k int32) and work (lq_topk_work_bytes(n, k)
+ * bytes, 8-byte aligned) are caller-owned device buffers; work is scratch.
+ *
+ * lq_topk_f32: over x[0 .. n-1] (device floats), 1 <= n < 2^31.
+ * lq_gemv_topk: the GEMV (M = 1, as lq_gemv_<fmt>) into C (required, N
+ *   floats), then the top-k of C.
+ * lq_topk_work_bytes: 0 for arguments out of range. */
+size_t    lq_topk_work_bytes(int64_t n, int k);
+lq_status lq_topk_f32(const float* x, int64_t n, int k, float* values, int32_t* indices,
+                      void* work, void* stream);
+lq_status lq_gemv_topk(int fmt, const float* A, const void* W, float* C, int64_t N, int64_t K,
+                       int k, float* values, int32_t* indices, void* work, void* stream);
+
 /* ---- epilogue fusions -----------------------------------------------------
  * The matmul with its output combined before it is stored, for any M (the
  * M = 1, M = 2..4 and tensor-core kernels apply it in their store; shapes

@@ -186,3 +186,21 @@ def test_epilogue_argument_errors_return_before_launch(lq):
     assert L.lq_matmul_residual(5, a, w, r, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_matmul_swiglu(5, a, w, c, 2, 8, 64, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_matmul_swiglu(1, a, w, c, 2, 8, 48, 0) == lq.LQ_ERR_INVALID_ARG  # K % 32
+
+
+def test_topk_argument_errors_return_before_launch(lq):
+    L = lq.lib()
+    x, v, i, w = 0x10000, 0x20000, 0x30000, 0x40000
+    assert L.lq_topk_work_bytes(0, 5) == 0 and L.lq_topk_work_bytes(10, 0) == 0
+    assert L.lq_topk_work_bytes(10, 65) == 0 and L.lq_topk_work_bytes(1 << 31, 5) == 0
+    assert L.lq_topk_work_bytes(1, 1) == 8
+    assert L.lq_topk_work_bytes(151936, 50) > 0
+    assert L.lq_topk_f32(x, 0, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_topk_f32(x, 10, 0, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_topk_f32(x, 10, 65, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_topk_f32(None, 10, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_topk_f32(x, 10, 5, v, i, w + 4, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_topk_f32(x, 10, 5, None, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_topk(0, x, x, None, 10, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG  # C required
+    assert L.lq_gemv_topk(9, x, x, x, 10, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemv_topk(0, x, x, x, 0, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
