@@ -44,7 +44,7 @@ import synthetic  # noqa: E402
 HEADLINE = "gemv_q8_0_4096x4096"
 KERNEL_OF_MODE = {"chain": "gemv_chain_kernel", "chain-dependent": "gemv_chain_kernel",
                   "calls": "gemv_stream_kernel", "argmax": "gemv_stream_kernel",
-                  "argmax-unfused": "gemv_stream_kernel"}
+                  "argmax-unfused": "gemv_stream_kernel", "topk": "gemv_stream_kernel"}
 METRIC = "decode GEMV achieved HBM GB/s (% of peak); prefill GEMM TFLOP/s (% peak)"
 L2_BYTES = 129 * 2**20
 FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
@@ -158,7 +158,8 @@ class Workbench:
         over the independent copies), "chain-dependent" (every problem waits
         for the previous one), "argmax" (M = 1: one lq_gemv_argmax per copy,
         logits not stored), "argmax-unfused" (M = 1: lq_matmul into C, then
-        lq_argmax_f32 on C), or "auto" (chain for M = 1, else calls)."""
+        lq_argmax_f32 on C), "topk" (M = 1: lq_gemv_topk with k = 50), or
+        "auto" (chain for M = 1, else calls)."""
         self.lq, self.w, self.dev = lq, w, dev
         W, A = synthetic.draw_workload(w)
         packed = lq.pack(w.fmt, W).reshape(-1).view(np.uint8)
@@ -195,9 +196,14 @@ class Workbench:
         if mode.startswith("argmax") and w.M == 1:
             self.mode = mode
             self.res = torch.zeros((R, 3), dtype=torch.int64, device=dev)
+        if mode == "topk" and w.M == 1:
+            self.mode = mode
+            self.topk = [lq.topk_buffers(w.N, 50, dev) for _ in range(R)]
         # kernels of ours per step
         if self.problems is not None:
             self.kernels_per_step = len(self.problems)
+        elif self.mode == "topk":
+            self.kernels_per_step = 3 * R
         elif self.mode == "argmax-unfused" or w.M >= 2:
             self.kernels_per_step = 2 * R
         else:
@@ -212,6 +218,11 @@ class Workbench:
         if self.mode == "argmax":
             for r in range(self.R):
                 self.lq.lq_gemv_argmax(w.fmt, self.Ad[r], self.Wd[r], None, w.N, w.K, self.res[r], stream)
+            return
+        if self.mode == "topk":
+            for r in range(self.R):
+                v, i, wk = self.topk[r]
+                self.lq.lq_gemv_topk(w.fmt, self.Ad[r], self.Wd[r], self.Cd[r], w.N, w.K, 50, v, i, wk, stream)
             return
         for r in range(self.R):
             self.fn(self.Ad[r], self.Wd[r], self.Cd[r], w.M, w.N, w.K, stream)
@@ -412,7 +423,7 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: seconds of oracle work the whole run aims at")
     ap.add_argument("--mode", default="auto",
-                    choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused"],
+                    choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused", "topk"],
                     help="how the headline step runs its matmuls (auto: chain for M = 1; argmax modes: "
                          "M = 1, the GEMV with its argmax)")
     args = ap.parse_args()
@@ -486,7 +497,7 @@ def main():
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
     lmhead = "gemv_f16_lmhead_151936x2048"
     if lmhead in names or (w.name == lmhead and args.extras != "none"):
-        runs += [(lmhead, "argmax"), (lmhead, "argmax-unfused")]
+        runs += [(lmhead, "argmax"), (lmhead, "argmax-unfused"), (lmhead, "topk")]
     for name, mode in runs:
         x = synthetic.WORKLOADS[name]
         xb = Workbench(lq, x, dev, mode=mode)

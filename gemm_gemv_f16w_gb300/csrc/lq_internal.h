@@ -78,8 +78,8 @@ void set_gemm_rings(int a_stages, int raw_stages);
 lq_status launch_gemv_argmax(const MatmulArgs& a, lq_argmax_result* out);
 lq_status launch_argmax_f32(const float* x, int64_t n, lq_argmax_result* out, cudaStream_t stream);
 
-// Top-k (lq_topk_f32): CTAs of the first pass for n inputs, and the launch
-// (work holds topk_ctas(n) * k keys of 8 bytes).
+// Top-k (lq_topk_f32): the work buffer holds topk_ctas(n) * k keys of 8
+// bytes (two regions for the first pass's CTAs), and the launches.
 int64_t topk_ctas(int64_t n);
 lq_status launch_topk_f32(const float* x, int64_t n, int k, float* values, int32_t* indices, void* work,
                           cudaStream_t stream);

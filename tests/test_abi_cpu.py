@@ -193,7 +193,7 @@ def test_topk_argument_errors_return_before_launch(lq):
     x, v, i, w = 0x10000, 0x20000, 0x30000, 0x40000
     assert L.lq_topk_work_bytes(0, 5) == 0 and L.lq_topk_work_bytes(10, 0) == 0
     assert L.lq_topk_work_bytes(10, 65) == 0 and L.lq_topk_work_bytes(1 << 31, 5) == 0
-    assert L.lq_topk_work_bytes(1, 1) == 8
+    assert L.lq_topk_work_bytes(1, 1) == 16  # two regions of one key
     assert L.lq_topk_work_bytes(151936, 50) > 0
     assert L.lq_topk_f32(x, 0, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_topk_f32(x, 10, 0, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
