@@ -13,9 +13,9 @@
 //  1. a grid of CTAs (one tile of the input each, as many CTAs as tiles up
 //     to a cap) keeps a running top-64 of its tiles in shared memory: slots
 //     0..63 hold the best keys so far, slots 64..2047 take the next 1984
-//     inputs, and a bitonic sort of the 2048 keys (1024 threads, two keys
-//     each in registers; shared memory only for strides of 64 and more)
-//     brings the best 64 back to the front;
+//     inputs, and a partial bitonic sort (runs of 64 sorted in registers,
+//     then rounds that keep the best half of each pair of runs) brings the
+//     best 64 of the 2048 keys back to the front;
 //     each CTA writes its best k keys to the work buffer;
 //  2. merge passes, each CTA sorting up to 1984 / k groups of k candidates
 //     into one group, until one group is left; the last pass writes the k
@@ -36,56 +36,63 @@ constexpr int kTopkMaxK = 64;                   // kept between tiles
 constexpr int kTopkNew = kTopkTile - kTopkMaxK; // fresh keys per tile
 constexpr int kTopkMaxCtas = 512;
 
-// Bitonic sort of s[0 .. 2048) into descending order. Thread t holds
-// positions 2t and 2t+1 in registers; a step of stride 1 compares the two,
-// strides 2..32 pair the thread with lane t ^ (stride / 2) of its warp by
-// shuffles, and only strides of 64 and more go through shared memory (pair
-// t joins lo and lo + stride, lo = t with a zero bit inserted at
-// log2(stride)). Blocks of `size` with (lo & size) == 0 run descending, so
-// the last merge sorts the whole array descending. Reads s after a barrier
-// and leaves it written, followed by one.
-__device__ void sort_desc(unsigned long long* s) {
-  const int t = threadIdx.x, p0 = 2 * t;
-  unsigned long long e0 = s[p0], e1 = s[p0 + 1];
-  for (int ls = 1; ls <= kTopkLog; ++ls) {
-    const int size = 1 << ls;
-    int lst = ls - 1;
-    if ((1 << lst) >= 64) {
-      s[p0] = e0;  // this thread's own positions: nobody else reads them now
-      s[p0 + 1] = e1;
-      __syncthreads();
-      for (; (1 << lst) >= 64; --lst) {
-        const int stride = 1 << lst;
-        const int lo = ((t >> lst) << (lst + 1)) | (t & (stride - 1)), hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long a = s[lo], b = s[hi];
-        if (desc ? a < b : a > b) {
-          s[lo] = b;
-          s[hi] = a;
-        }
-        __syncthreads();
-      }
-      e0 = s[p0];
-      e1 = s[p0 + 1];
-    }
-    for (; lst >= 1; --lst) {
-      const int stride = 1 << lst;
-      const unsigned long long q0 = __shfl_xor_sync(0xffffffffu, e0, stride >> 1);
-      const unsigned long long q1 = __shfl_xor_sync(0xffffffffu, e1, stride >> 1);
-      // both positions share bit lst (stride >= 2) and bit ls (size >= 4)
-      const bool keep_max = ((p0 & stride) == 0) == (((p0 & ~stride) & size) == 0);
-      e0 = keep_max ? (e0 > q0 ? e0 : q0) : (e0 < q0 ? e0 : q0);
-      e1 = keep_max ? (e1 > q1 ? e1 : q1) : (e1 < q1 ? e1 : q1);
-    }
-    const bool desc = (p0 & size) == 0;  // stride 1, inside the thread
+// One compare-exchange step of a bitonic network on the warp's keys, thread
+// holding positions p and p + 1 (p even): strides 2..32 pair lanes by
+// shuffles, stride 1 is inside the thread. keep_max for the lower position
+// of each pair is decided by the caller's direction.
+__device__ __forceinline__ void cx_step(unsigned long long& e0, unsigned long long& e1, int p, int stride,
+                                        bool desc) {
+  if (stride == 1) {
     if (desc ? e0 < e1 : e0 > e1) {
       const unsigned long long x = e0;
       e0 = e1;
       e1 = x;
     }
+    return;
   }
-  s[p0] = e0;
-  s[p0 + 1] = e1;
+  const unsigned long long q0 = __shfl_xor_sync(0xffffffffu, e0, stride >> 1);
+  const unsigned long long q1 = __shfl_xor_sync(0xffffffffu, e1, stride >> 1);
+  const bool keep_max = ((p & stride) == 0) == desc;  // both positions share bit log2(stride)
+  e0 = keep_max ? (e0 > q0 ? e0 : q0) : (e0 < q0 ? e0 : q0);
+  e1 = keep_max ? (e1 > q1 ? e1 : q1) : (e1 < q1 ? e1 : q1);
+}
+
+// The best 64 of s[0 .. 2048), sorted descending into s[0 .. 64) (the rest
+// of s is left undefined). Warp w holds the run of positions 64w .. 64w+63,
+// two keys a lane. (1) Each run is sorted by the bitonic network on the
+// global positions, which leaves even runs descending and odd runs
+// ascending. (2) Five rounds halve the runs: warp w, a multiple of 2^(r+1),
+// takes the elementwise maximum of its run and the run of warp w + 2^r
+// (read through shared memory): a descending run against an ascending one,
+// this is the half-cleaner of their bitonic concatenation and keeps the best
+// 64 as a bitonic sequence, which six steps sort in the direction the next
+// round needs (descending when w / 2^(r+1) is even).
+__device__ void top64_desc(unsigned long long* s) {
+  const int t = threadIdx.x, w = t >> 5, p0 = 2 * t;
+  unsigned long long e0 = s[p0], e1 = s[p0 + 1];
+  for (int ls = 1; ls <= 6; ++ls)
+    for (int lst = ls - 1; lst >= 0; --lst) {
+      const int stride = 1 << lst;
+      cx_step(e0, e1, p0, stride, (((p0 & ~stride) & (1 << ls)) == 0));
+    }
+  for (int r = 0; r < 5; ++r) {
+    s[p0] = e0;  // this thread's own positions
+    s[p0 + 1] = e1;
+    __syncthreads();
+    if ((w & ((2 << r) - 1)) == 0) {
+      const int q = p0 + (64 << r);  // the same lane of warp w + 2^r
+      const unsigned long long b0 = s[q], b1 = s[q + 1];
+      e0 = e0 > b0 ? e0 : b0;
+      e1 = e1 > b1 ? e1 : b1;
+      const bool desc = ((w >> (r + 1)) & 1) == 0;
+      for (int lst = 5; lst >= 0; --lst) cx_step(e0, e1, p0 & 63, 1 << lst, desc);
+    }
+    __syncthreads();
+  }
+  if (w == 0) {
+    s[p0] = e0;
+    s[p0 + 1] = e1;
+  }
   __syncthreads();
 }
 
@@ -100,7 +107,7 @@ __device__ void running_topk(unsigned long long* s, long long count, long long f
     for (int j = threadIdx.x; j < kTopkNew; j += kTopkThreads)
       s[kTopkMaxK + j] = base + j < count ? key(base + j) : 0ull;
     __syncthreads();
-    sort_desc(s);
+    top64_desc(s);
   }
 }
 
