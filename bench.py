@@ -492,7 +492,13 @@ def main():
     # ---- the other workload families (same method, shorter runs)
     extras = {}
     names = EXTRA if args.extras == "all" else ([] if args.extras == "none" else args.extras.split(","))
-    runs = [(name, "auto") for name in names if name != w.name]
+    runs = []
+    for name in names:
+        if name == w.name:
+            continue
+        runs.append((name, "auto"))
+        if synthetic.WORKLOADS[name].M == 1:
+            runs.append((name, "calls"))  # the decode GEMVs both as a chain and as separate calls
     if w.M == 1 and args.extras != "none":
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
     lmhead = "gemv_f16_lmhead_151936x2048"
