@@ -256,8 +256,7 @@ lq_status lq_last_device_error(void) {
 }
 
 lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, void* stream) {
-  if (fmt == LQ_FMT_Q4_0I) return LQ_ERR_UNSUPPORTED;  // the chain keeps A in the standard order
-  if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
+  if (!known_format(fmt)) return LQ_ERR_INVALID_ARG;
   if (!problems || count < 1) return LQ_ERR_INVALID_ARG;
   for (int j = 0; j < count; ++j) {
     const lq_gemv_problem& q = problems[j];

@@ -31,6 +31,7 @@
 #include "lq_device.cuh"
 #include "lq_gemv_slices.cuh"
 #include "lq_internal.h"
+#include "lq_q4i.cuh"
 
 namespace lq {
 namespace {
@@ -73,6 +74,7 @@ struct ChainParams {
   int publish;            // some problem waits for an earlier one
   unsigned long long wait_ns;
   unsigned wait_iters;
+  int a_perm;             // Q4_0 with interleaved nibbles: A reordered per block
 };
 
 struct ChainHeader {
@@ -255,7 +257,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         const uint32_t sg = smem_u32(stage_a), sa = smem_u32(slots_a + b * p.a_slots);
         for (int c = at; c < q.K / 4; c += static_cast<int>(nthr)) {
           const uint4 v = lds128(sg + 16u * c);
-          sts128(sa + static_cast<uint32_t>(a_slot_q(c >> 3)) * kASlotBytes + 16u * (c & 7), v);
+          const uint32_t blk = sa + static_cast<uint32_t>(a_slot_q(c >> 3)) * kASlotBytes;
+          if (p.a_perm)
+            q4i::store_chunk(blk, c & 7, v);
+          else
+            sts128(blk + 16u * (c & 7), v);
         }
         named_barrier(2, nthr);
         if (lead) mbar_arrive(&hd.a_full[b]);
@@ -419,6 +425,10 @@ unsigned read_clear_chain_error() {
 lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, cudaStream_t stream) {
   if (count < 1 || count > kChainMax) return LQ_ERR_UNSUPPORTED;
   ChainParams p = {};
+  if (fmt == LQ_FMT_Q4_0I) {  // the Q4_0 kernel with A reordered per block (lq_q4i.cuh)
+    fmt = LQ_FMT_Q4_0;
+    p.a_perm = 1;
+  }
   int kmax = 0, rb_max = 0;
   for (int j = 0; j < count; ++j) {
     const lq_gemv_problem& u = problems[j];

@@ -110,8 +110,8 @@ lq_status lq_matmul_q4_0(const float* A, const void* W, float* C,
  * As lq_gemv_q4_0 / lq_gemm_q4_0 / lq_matmul_q4_0, for weights packed by
  * lq_pack_q4_0i (byte j of a block: element 2j low, 2j+1 high). Same routes,
  * results and tolerances; A is read in the reordered sequence the nibble
- * order needs. lq_gemm_noalloc and lq_gemv_chain do not take this format
- * (LQ_ERR_INVALID_ARG and LQ_ERR_UNSUPPORTED). */
+ * order needs (lq_gemv_chain takes the format too). lq_gemm_noalloc does not
+ * (LQ_ERR_INVALID_ARG). */
 lq_status lq_gemv_q4_0i(const float* A, const void* W, float* C,
                         int64_t M, int64_t N, int64_t K, void* stream);
 lq_status lq_gemm_q4_0i(const float* A, const void* W, float* C,

@@ -100,17 +100,42 @@ def test_q4_0i_fused_argmax(lq, cuda_dev):
     check(c[None, :], y, tol, "q4_0i argmax logits")
 
 
-def test_q4_0i_refused_where_not_supported(lq, cuda_dev):
+def test_q4_0i_in_the_decode_chain(lq, cuda_dev):
+    """A dependent chain of interleaved-Q4_0 GEMVs, each against the oracle
+    on the GPU's own previous output."""
+    dims = [4096, 2048, 4096, 1024]
+    torch.manual_seed(1)
+    A0 = torch.randn(dims[0], dtype=torch.float32)
+    items, Ws, Cs = [], [], []
+    A = A0.to(cuda_dev)
+    for j in range(len(dims) - 1):
+        K, N = dims[j], dims[j + 1]
+        W, _ = synthetic.draw(1, N, K, seed=90 + j, outlier_frac=0.05)
+        Wd = to_dev(lq.pack("q4_0i", W.numpy()).reshape(-1).view(np.uint8), cuda_dev)
+        C = nan_filled(1, N, cuda_dev)[0]
+        items.append((A, Wd, C, N, K, 1 if j > 0 else 0))
+        Ws.append((W.numpy(), Wd))
+        Cs.append(C)
+        A = C
+    assert lq.lq_gemv_chain("q4_0i", items) == lq.LQ_OK
+    torch.cuda.synchronize()
+    assert lq.last_device_error() == lq.LQ_OK
+    a_prev = A0.numpy()
+    for (Wn, _), C in zip(Ws, Cs):
+        N, K = Wn.shape
+        c = C.cpu().numpy()
+        y, tol = O.reference("q4_0i", a_prev[None, :], O.pack("q4_0i", Wn), N, K)
+        check(c[None, :], y, tol, f"q4_0i chain N={N} K={K}")
+        a_prev = c
+
+
+def test_q4_0i_refused_by_the_fixed_workspace_gemm(lq, cuda_dev):
     N, K = 256, 256
     W, A = synthetic.draw(2, N, K, seed=80)
     Wd = to_dev(lq.pack("q4_0i", W.numpy()).reshape(-1).view(np.uint8), cuda_dev)
-    Ad = A.to(cuda_dev)
     C = nan_filled(2, N, cuda_dev)
-    # the decode chain keeps A in the standard order
-    assert lq.lq_gemv_chain("q4_0i", [(Ad[0], Wd, C[0], N, K, 0)]) == lq.LQ_ERR_UNSUPPORTED
-    # the fixed-workspace GEMM takes the three base formats only
     with pytest.raises(lq.LQError):
-        lq.lq_gemm_noalloc(lq.FMT["q4_0i"], Ad, Wd, C, 2, N, K)
+        lq.lq_gemm_noalloc(lq.FMT["q4_0i"], A.to(cuda_dev), Wd, C, 2, N, K)
     torch.cuda.synchronize()
     assert torch.isnan(C).all()
 
