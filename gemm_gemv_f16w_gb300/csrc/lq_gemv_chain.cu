@@ -50,7 +50,10 @@ constexpr int kAWarp = kCW + 1;               // first of the activation warps
 constexpr int kAWarps = 3;
 constexpr int kChainThreads = (kCW + 1 + kAWarps) * 32;
 constexpr int kChainRows = 8;                 // rows per stage (at most)
-constexpr int kChainMaxStages = 16;
+constexpr int kChainMaxStages = 32;
+// Ring slots each row-group cycles through: the rows of its later slots are
+// in flight while it computes the current one.
+constexpr int kSlotsPerGroup = 1;
 
 struct ChainProblem {
   const float* A;
@@ -75,6 +78,7 @@ struct ChainParams {
   unsigned long long wait_ns;
   unsigned wait_iters;
   int a_perm;             // Q4_0 with interleaved nibbles: A reordered per block
+  int red_bytes;          // the K-groups' partials: [2 phases][stages][kChainRows][nk] floats
 };
 
 struct ChainHeader {
@@ -85,8 +89,8 @@ struct ChainHeader {
   uint64_t a_full[2], a_empty[2];  // A_j ready for the slices / every consumer warp read it
   volatile int a_go;               // the lead activation thread's verdict for the problem
   unsigned fin[kChainMax];         // finished stages of each problem on this CTA
+  int row0[kChainMax], nrows[kChainMax], nstage[kChainMax];  // each problem's rows and stages here
   volatile int abort;
-  float red[kChainMaxStages][kChainRows][kCW];
 };
 constexpr int kChainHeaderBytes = (static_cast<int>(sizeof(ChainHeader)) + 127) / 128 * 128;
 
@@ -132,7 +136,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
   ChainHeader& hd = *reinterpret_cast<ChainHeader*>(smem);
   uint8_t* slots_a = smem + kChainHeaderBytes;          // 2 x a_slots: A as the slices read it
   uint8_t* stage_a = slots_a + 2 * p.a_slots;           // A as copied (quantised formats)
-  uint8_t* ring = stage_a + p.a_stage;
+  float* red = reinterpret_cast<float*>(stage_a + p.a_stage);
+  uint8_t* ring = stage_a + p.a_stage + p.red_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int RS = p.rows_per_stage, S = p.stages, nk = p.nk, nr = p.nr, active = nk * nr;
@@ -152,6 +157,15 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     hd.abort = 0;
     fence_barrier_init();
   }
+  // this CTA's share of every problem, worked out once (the divisions would
+  // otherwise cost each consumer warp more than a row's dot per problem)
+  for (int j = threadIdx.x; j < p.count; j += blockDim.x) {
+    int r0, n;
+    cta_rows(p.pr[j], r0, n);
+    hd.row0[j] = r0;
+    hd.nrows[j] = n;
+    hd.nstage[j] = (n + RS - 1) / RS;
+  }
   __syncthreads();
 
   if (warp == kProducerWarp) {
@@ -162,9 +176,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     bool ok = true;
     for (int j = 0; j < p.count && ok; ++j) {
       const ChainProblem& q = p.pr[j];
-      int r0, nrows;
-      cta_rows(q, r0, nrows);
-      const int nst = (nrows + RS - 1) / RS;
+      const int r0 = hd.row0[j], nrows = hd.nrows[j], nst = hd.nstage[j];
       for (int st = 0; st < nst; ++st) {
         if (lap > 0 && (!mbar_wait(&hd.empty[s], static_cast<uint32_t>(lap - 1) & 1, p.wait_ns,
                                    p.wait_iters) ||
@@ -283,12 +295,17 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
 
   // ---------------- consumers ----------------
   const int kg = warp % nk, rg = warp / nk;
-  int g0 = 0;  // first global stage of problem j on this CTA
+  // this row-group's global stages are rg, rg + nr, rg + 2 nr, ... through all
+  // the problems; slot, ring phase and finisher advance with them, nr stages
+  // at a time: slot g mod S, phase (g / S) mod 2, finisher (g / nr) mod nk
+  int gw = rg;     // the warp's next global stage
+  int s = rg;      // its slot (rg < nr <= S)
+  uint32_t ph = 0;
+  int kf = 0;
+  int g0 = 0;      // first global stage of problem j on this CTA
   for (int j = 0; j < p.count; ++j) {
     const ChainProblem& q = p.pr[j];
-    int r0, nrows;
-    cta_rows(q, r0, nrows);
-    const int nst = (nrows + RS - 1) / RS;
+    const int r0 = hd.row0[j], nrows = hd.nrows[j], nst = hd.nstage[j];
     const int b = j & 1;
     if (!mbar_wait(&hd.a_full[b], static_cast<uint32_t>(j >> 1) & 1, p.wait_ns, p.wait_iters) ||
         aborted(hd)) {
@@ -300,14 +317,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     __syncwarp();
     if (lane == 0) mbar_arrive(&hd.a_empty[b]);  // this warp has read A_j
 
-    // this row-group's stages of problem j: global stages g = rg (mod nr);
-    // slot, phase and finisher advance by nr stages at a time
-    int st = rg - g0 % nr;
-    if (st < 0) st += nr;
-    int s = (g0 + st) % S;
-    uint32_t ph = static_cast<uint32_t>((g0 + st) / S) & 1;
-    int kf = ((g0 + st) / nr) % nk;
-    for (; st < nst; st += nr) {
+    for (int st = gw - g0; st < nst; st += nr) {
       if (!mbar_wait(&hd.full[s], ph, p.wait_ns, p.wait_iters) || aborted(hd)) {
         abort_all(hd, p);
         return;
@@ -324,9 +334,18 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
       }
       int r;
       const float v = transpose_reduce8(acc, lane, r);
-      if ((lane & 3) == 0) hd.red[s][r][kg] = v;
+      // partials of this use of the slot: double-buffered by the ring phase,
+      // so the slot itself is handed back as soon as its rows are read (the
+      // refill overlaps the reduction); the partials of this phase are not
+      // written again before this stage's finisher has moved on to its next
+      // stage, whose slot release the second refill waits for
+      float* red_s = red + (static_cast<size_t>(ph) * S + s) * kChainRows * nk;
+      if ((lane & 3) == 0) red_s[r * nk + kg] = v;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&hd.red_full[s]);
+      if (lane == 0) {
+        mbar_arrive(&hd.red_full[s]);
+        mbar_arrive(&hd.empty[s]);  // this warp has read the slot
+      }
       if (kg == kf) {
         // finisher: the K-groups' partials in a fixed order, then C
         if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || aborted(hd)) {
@@ -335,9 +354,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         }
         float sum = 0.f;
         if (lane < rows)
-          for (int k = 0; k < nk; ++k) sum += hd.red[s][lane][k];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&hd.empty[s]);  // slot and partials consumed
+          for (int k = 0; k < nk; ++k) sum += red_s[lane * nk + k];
         if (lane < rows) q.C[r0 + st * RS + lane] = sum;
         if (p.publish) {
           __syncwarp();
@@ -348,8 +365,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
           }
           __syncwarp();
         }
-      } else if (lane == 0) {
-        mbar_arrive(&hd.empty[s]);
       }
       s += nr;
       if (s >= S) {
@@ -357,6 +372,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         ph ^= 1u;
       }
       if (++kf == nk) kf = 0;
+      gw += nr;
     }
     if (p.publish && nst == 0 && warp == 0 && lane == 0) add_release(p.sync, 1u);  // no rows here
     g0 += nst;
@@ -472,16 +488,24 @@ lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count,
   p.a_slots = fmt == LQ_FMT_F16 ? a_linear : ((kmax / 32 + 63) / 64) * 64 * kASlotBytes;
   p.a_stage = fmt == LQ_FMT_F16 ? 0 : a_linear;
   const long long fixed = kChainHeaderBytes + 2LL * p.a_slots + p.a_stage;
-  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - fixed;
-  p.rows_per_stage = static_cast<int>(std::min<long long>(kChainRows, budget / (2LL * rb_max)));
+  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - fixed - 128;
+  // a ring slot costs its rows plus two phases of the K-groups' partials;
+  // rows per stage: the most (up to kChainRows) that still give every
+  // row-group kSlotsPerGroup slots, and the ring at least two
+  const long long red_slot = 2LL * kChainRows * p.nk * static_cast<long long>(sizeof(float));
+  const long long per_slot = budget / std::max(2, kSlotsPerGroup * p.nr);
+  p.rows_per_stage = static_cast<int>(std::min<long long>(kChainRows, (per_slot - red_slot) / rb_max));
+  if (p.rows_per_stage < 1)
+    p.rows_per_stage = static_cast<int>(std::min<long long>(kChainRows, (budget / 2 - red_slot) / rb_max));
   if (p.rows_per_stage < 1) return LQ_ERR_UNSUPPORTED;
   p.slot_bytes = static_cast<unsigned>(p.rows_per_stage * rb_max);
-  int stages = static_cast<int>(std::min<long long>(kChainMaxStages, budget / p.slot_bytes));
+  int stages = static_cast<int>(std::min<long long>(kChainMaxStages, budget / (p.slot_bytes + red_slot)));
   // every ring slot serves one row-group: S a multiple of nr
   while (p.nr > 1 && stages - stages % p.nr < 2) p.nr /= 2;
   stages -= stages % p.nr;
   if (stages < 2) return LQ_ERR_UNSUPPORTED;
   p.stages = stages;
+  p.red_bytes = static_cast<int>((stages * red_slot + 127) / 128 * 128);
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   unsigned* sync = nullptr;
@@ -490,7 +514,7 @@ lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count,
   p.sync = sync;
   cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream);
   if (e != cudaSuccess) return cuda_status(e);
-  const size_t smem = static_cast<size_t>(fixed) + static_cast<size_t>(stages) * p.slot_bytes;
+  const size_t smem = static_cast<size_t>(fixed) + p.red_bytes + static_cast<size_t>(stages) * p.slot_bytes;
   if (fmt == LQ_FMT_F16) st = launch_chain_t<LQ_FMT_F16>(p, smem, stream);
   else if (fmt == LQ_FMT_Q8_0) st = launch_chain_t<LQ_FMT_Q8_0>(p, smem, stream);
   else st = launch_chain_t<LQ_FMT_Q4_0>(p, smem, stream);
