@@ -83,6 +83,7 @@ struct Header {
   uint64_t red_full[kMaxStages];   // every consumer warp wrote its row partials
   uint64_t a_bar;                  // A landed in the staging area
   volatile int abort;
+  int row0, nrows;                 // this CTA's rows
   float red[kMaxStages][kRowsPerStage][kConsumerWarps];  // [slot][row][K-group]
 };
 constexpr int kHeaderBytes = (static_cast<int>(sizeof(Header)) + 127) / 128 * 128;
@@ -119,14 +120,9 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
   uint8_t* ring = stage_a + p.a_stage;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const int r0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.N) / G);
-  const int r1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G);
-  const int nrows = r1 - r0;
   const int RS = p.rows_per_stage, S = p.stages;
   const int nk = p.nk, nr = p.nr, active = nk * nr;
   constexpr bool AMAX = EPI == epi::kArgmax, SWIGLU = EPI == epi::kSwiglu;
-  const int nst = (nrows + RS - 1) / RS;
   const uint32_t stage_bytes = static_cast<uint32_t>(SWIGLU ? 2 * RS : RS) * p.row_bytes;
   // The host plans S as a multiple of nr (see plan_gemv); refuse anything else.
   if (S % nr != 0 || S > kMaxStages || active > kConsumerWarps || (SWIGLU && 2 * RS > kRowsPerStage)) {
@@ -142,17 +138,23 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     }
     mbar_init(&hd.a_bar, 1);
     hd.abort = 0;
+    // this CTA's rows (one thread: 64-bit divisions are long sequences)
+    const long long G = gridDim.x;
+    const int a = static_cast<int>((static_cast<long long>(blockIdx.x) * p.N) / G);
+    hd.row0 = a;
+    hd.nrows = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G) - a;
     fence_barrier_init();
   }
   __syncthreads();
   pdl_launch_dependents();
+  const int r0 = hd.row0, nrows = hd.nrows;
+  const int nst = (nrows + RS - 1) / RS;
 
   if (warp == kConsumerWarps) {
     // ---------------- producer ----------------
     const uint64_t pol = policy_evict_first();
     const uint8_t* wbase = p.W + static_cast<long long>(r0) * p.row_bytes;
-    auto issue = [&](int st) {
-      const int s = st % S;
+    auto issue = [&](int st, int s) {  // stage st into slot s
       const int rows = min(RS, nrows - st * RS);
       const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
       uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     // to L2; otherwise the prefetched lines would not survive).
     if (lane != 0) return;
     const int first = min(nst, S);
-    for (int st = 0; st < first; ++st) issue(st);
+    for (int st = 0; st < first; ++st) issue(st, st);
     if (p.l2_prefetch && nst > S) {
       const long long done = static_cast<long long>(S) * RS * p.row_bytes;
       const long long rest = static_cast<long long>(nrows) * p.row_bytes - done;
@@ -187,14 +189,20 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
              policy_evict_last());
     int issued = first;
     bool ok = true;
+    // stages past the first S (first == S here): slot s of ring lap `lap`
+    // once the consumers released the slot's previous lap
+    int s = 0, lap = 1;
     for (int st = first; st < nst; ++st) {
-      if (st >= S && (!mbar_wait(&hd.empty[st % S], ((st / S) - 1) & 1, p.wait_ns, p.wait_iters) ||
-                      hd.abort)) {
+      if (!mbar_wait(&hd.empty[s], static_cast<uint32_t>(lap - 1) & 1, p.wait_ns, p.wait_iters) || hd.abort) {
         ok = false;
         break;
       }
-      issue(st);
+      issue(st, s);
       ++issued;
+      if (++s == S) {
+        s = 0;
+        ++lap;
+      }
     }
     if (!ok) {
       record_error(kDevErrTimeout);
@@ -237,9 +245,11 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
   sl.init(smem_u32(sA), kg, nk, lane, p.K);
   const uint32_t ring_u = smem_u32(ring);
   unsigned long long best = 0ull;  // argmax variant: this lane's best row
+  // stages rg, rg + nr, ...: slot st mod S, ring phase (st / S) mod 2 and
+  // finisher (st / nr) mod nk, advanced incrementally
+  int s = rg, kf = 0;
+  uint32_t ph = 0;
   for (int st = rg; st < nst; st += nr) {
-    const int s = st % S;
-    const uint32_t ph = (st / S) & 1;
     if (!mbar_wait(&hd.full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
       record_error(kDevErrTimeout);
       hd.abort = 1;
@@ -273,7 +283,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     if ((lane & 3) == 0) hd.red[s][r][kg] = v;
     __syncwarp();
     if (lane == 0) mbar_arrive(&hd.red_full[s]);
-    if (kg == (st / nr) % nk) {
+    if (kg == kf) {
       // finisher of this stage: the K-groups' partials, in a fixed order
       // (residual: R is fetched while the other K-groups finish)
       float rres = 0.f;
@@ -305,6 +315,12 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       __syncwarp();
     }
     if (lane == 0) mbar_arrive(&hd.empty[s]);
+    s += nr;
+    if (s >= S) {
+      s -= S;
+      ph ^= 1u;
+    }
+    if (++kf == nk) kf = 0;
   }
   if constexpr (AMAX) amax::warp_done(best, p.amax, p.amax_warps, lane);
 }

@@ -76,6 +76,7 @@ struct BatchHeader {
   uint64_t a_bar;
   int last[kBMaxStages];  // last stage issued into each slot (-1: none)
   volatile int abort;
+  int row0, nrows;        // this CTA's rows
   float red[kBMaxStages][MT][kBRows][kBKGroups];
 };
 template <int MT>
@@ -104,21 +105,25 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   uint8_t* stage_a = ring + p.stage_off;          // M x K floats (quantised formats)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = gridDim.x;
-  const int r0 = static_cast<int>((static_cast<long long>(blockIdx.x) * p.N) / G);
-  const int r1 = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G);
-  const int nrows = r1 - r0;
   const int RS = p.rows_per_stage, S = p.stages, nk = p.nk, nr = p.nr, active = nk * nr;
-  const int nst = (nrows + RS - 1) / RS;
   const uint32_t stage_bytes = static_cast<uint32_t>(SWIGLU ? 2 * RS : RS) * p.row_bytes;
   if (S % nr != 0 || S > kBMaxStages || nk > kBKGroups || active > NW || (SWIGLU ? 2 * RS : RS) > kBRows ||
       p.M > MT || p.early > S) {
     if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
     return;
   }
-  const uint8_t* wbase = p.W + static_cast<long long>(r0) * p.row_bytes;
-  auto issue = [&](int st, uint64_t pol) {
-    const int s = st % S;
+  // this CTA's rows: worked out by thread 0 (64-bit divisions are long
+  // sequences), which issues the first stages, and read by the rest after
+  // the block barrier
+  int r0 = 0, nrows = 0, nst = 0;
+  const uint8_t* wbase = p.W;
+  auto set_rows = [&](int a, int n) {
+    r0 = a;
+    nrows = n;
+    nst = (n + RS - 1) / RS;
+    wbase = p.W + static_cast<long long>(a) * p.row_bytes;
+  };
+  auto issue = [&](int st, int s, uint64_t pol) {  // stage st into slot s
     const uint32_t bytes = static_cast<uint32_t>(min(RS, nrows - st * RS)) * p.row_bytes;
     uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
     const uint8_t* src = wbase + static_cast<long long>(st) * RS * p.row_bytes;
@@ -134,6 +139,12 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   };
 
   if (threadIdx.x == 0) {
+    const long long G = gridDim.x;
+    const int a = static_cast<int>((static_cast<long long>(blockIdx.x) * p.N) / G);
+    const int n = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.N) / G) - a;
+    hd.row0 = a;
+    hd.nrows = n;
+    set_rows(a, n);
     for (int s = 0; s < S; ++s) {
       mbar_init(&hd.full[s], 1);
       mbar_init(&hd.red_full[s], nk);
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
     hd.abort = 0;
     fence_barrier_init();
     const uint64_t pol = policy_evict_first();
-    for (int st = 0; st < min(nst, p.early); ++st) issue(st, pol);  // weights depend on nothing
+    for (int st = 0; st < min(nst, p.early); ++st) issue(st, st, pol);  // weights depend on nothing
     // A (M rows, contiguous) once the previous kernel on the stream completed
     pdl_wait();
     const uint32_t a_bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(p.K) * 4u;
@@ -152,6 +163,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   }
   __syncthreads();
   pdl_launch_dependents();
+  set_rows(hd.row0, hd.nrows);
 
   if (warp < active && nrows > 0) {
     // One lead thread waits for A under the time limit; the other consumers
@@ -170,30 +182,32 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
         // staging (M rows) -> block slots, token by token
         const uint32_t sa = smem_u32(sA), sg = smem_u32(stage_a);
         const int per = p.K / 4;
-        for (int c = warp * 32 + lane; c < p.M * per; c += active * 32) {
-          const int t = c / per, q = c - t * per;
-          const uint4 v = lds128(sg + 16u * c);
-          const uint32_t blk =
-              sa + static_cast<uint32_t>(t * p.a_slot) + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes;
-          if (p.a_perm)
-            q4i::store_chunk(blk, q & 7, v);
-          else
-            sts128(blk + 16u * (q & 7), v);
-        }
+        for (int t = 0; t < p.M; ++t)
+          for (int q = warp * 32 + lane; q < per; q += active * 32) {
+            const uint4 v = lds128(sg + 16u * (t * per + q));
+            const uint32_t blk =
+                sa + static_cast<uint32_t>(t * p.a_slot) + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes;
+            if (p.a_perm)
+              q4i::store_chunk(blk, q & 7, v);
+            else
+              sts128(blk + 16u * (q & 7), v);
+          }
         named_barrier(2, static_cast<uint32_t>(active) * 32u);
         if (threadIdx.x == 0) {
           // the staging area is free: the slots it covered get their stages
           fence_proxy_async_smem();
-          for (int st = p.early; st < min(nst, S); ++st) issue(st, pol);
+          for (int st = p.early; st < min(nst, S); ++st) issue(st, st, pol);
         }
       }
       const int kg = warp % nk, rg = warp / nk;
       typename SliceM<FMT, MT>::T sl;
       sl.init(smem_u32(sA), static_cast<uint32_t>(p.a_slot), kg, lane, p.K);
       const uint32_t ring_u = smem_u32(ring);
+      // stages rg, rg + nr, ...: slot st mod S, ring phase (st / S) mod 2 and
+      // finisher (st / nr) mod nk, advanced incrementally
+      int s = rg, kf = 0;
+      uint32_t ph = 0;
       for (int st = rg; st < nst; st += nr) {
-        const int s = st % S;
-        const uint32_t ph = (st / S) & 1;
         if (!mbar_wait(&hd.full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
           record_error(kDevErrTimeout);
           hd.abort = 1;
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&hd.red_full[s]);
-        if (kg == (st / nr) % nk) {
+        if (kg == kf) {
           // finisher: adds the K-groups' partials in a fixed order, one
           // output per token, then refills slot s. The refill comes last: its
           // landing releases the row-group's next stage in this slot, whose
@@ -270,8 +284,14 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
             }
           }
           __syncwarp();
-          if (lane == 0 && st + S < nst) issue(st + S, pol);
+          if (lane == 0 && st + S < nst) issue(st + S, s, pol);
         }
+        s += nr;
+        if (s >= S) {
+          s -= S;
+          ph ^= 1u;
+        }
+        if (++kf == nk) kf = 0;
       }
     }
   }
