@@ -188,14 +188,16 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 }
 
 // ---- small integer -> exact float without I2F ------------------------------
-// Byte i of w (an int8 q whose sign bit was flipped), placed as the low
-// mantissa byte of 2^23: the float equals 2^23 + 128 + q exactly.
+// Byte i of w, placed as the low mantissa byte of 2^23: the float equals
+// 2^23 + that byte exactly. For an int8 q with its sign bit flipped the byte
+// is q + 128; for a Q4_0 code masked into a byte it is the code itself.
 __device__ __forceinline__ float s8_to_magic(uint32_t w_xor80, int i) {
   // result bytes: [w.byte_i, 0x00, 0x00, 0x4B]
   const uint32_t sel = 0x7540u | static_cast<uint32_t>(i);
   return __uint_as_float(__byte_perm(w_xor80, 0x4B000000u, sel));
 }
 constexpr float kMagicS8 = 8388608.0f + 128.0f;  // 2^23 + 128
+constexpr float kMagicQ4 = 8388608.0f + 8.0f;    // 2^23 + 8: a nibble code's offset
 
 __device__ __forceinline__ float f16_lo(uint32_t w) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));

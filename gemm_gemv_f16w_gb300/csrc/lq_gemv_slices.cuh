@@ -67,14 +67,30 @@ struct F16Slice {
 __host__ __device__ __forceinline__ int a_slot_q(int b) { return (2 * (b >> 6) + (b & 1)) * 32 + ((b & 63) >> 1); }
 constexpr int kASlotBytes = 144;
 
+// Quants 4i .. 4i+3 of a Q8_0 block as two pairs of exact floats, from the
+// block's nine words w (sign bits flipped): odd blocks hold them in word
+// i + 1, even blocks in bytes 2, 3 of word i and 0, 1 of word i + 1.
+template <bool ODD>
+__device__ __forceinline__ void q8_quad(const uint32_t (&w)[9], int i, float2 mb, float2& q01, float2& q23) {
+  if (ODD) {
+    q01 = fadd2(make_float2(s8_to_magic(w[i + 1], 0), s8_to_magic(w[i + 1], 1)), mb);
+    q23 = fadd2(make_float2(s8_to_magic(w[i + 1], 2), s8_to_magic(w[i + 1], 3)), mb);
+  } else {
+    q01 = fadd2(make_float2(s8_to_magic(w[i], 2), s8_to_magic(w[i], 3)), mb);
+    q23 = fadd2(make_float2(s8_to_magic(w[i + 1], 0), s8_to_magic(w[i + 1], 1)), mb);
+  }
+}
+
 // Q8_0 (34-byte blocks): the lane's block spans nine 32-bit words starting
 // at word 17l of the segment (+8 for odd blocks, whose scale sits in the
 // upper half of that first word). 17 is odd, so for each of the nine loads
 // the 32 lanes hit 32 different banks: every byte is read once, with no bank
 // conflicts. Even blocks start with their scale, so their quants are 2 bytes
-// past a word boundary and are realigned with one byte-permute per word;
-// odd blocks' quants are word-aligned (the parity is the same for the whole
-// warp, so the two cases are separate loops, not a divergent branch).
+// past a word boundary: the byte-permute that drops each quant into the
+// 2^23 magic picks it straight out of the word it sits in (bytes 2, 3 of one
+// word and 0, 1 of the next), so no word is realigned first. Odd blocks'
+// quants are word-aligned. (The parity is the same for the whole warp, so
+// the two cases are separate code, not a divergent branch.)
 template <int CPW>
 struct Q8Slice {
   float2 a[CPW][16];       // the blocks' activations
@@ -110,11 +126,11 @@ struct Q8Slice {
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] ^= 0x80808080u;  // sign bits flipped (the scale is read above)
+#pragma unroll
     for (int i = 0; i < 8; ++i) {
-      // q_{4i..4i+3}, sign bits flipped
-      const uint32_t x = (ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u)) ^ 0x80808080u;
-      const float2 q01 = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
-      const float2 q23 = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
+      float2 q01, q23;  // q_{4i}, q_{4i+1} and q_{4i+2}, q_{4i+3}
+      q8_quad<ODD>(w, i, mb, q01, q23);
       acc[(2 * i) & 3] = ffma2(q01, a[c][2 * i], acc[(2 * i) & 3]);
       acc[(2 * i + 1) & 3] = ffma2(q23, a[c][2 * i + 1], acc[(2 * i + 1) & 3]);
     }
@@ -129,13 +145,15 @@ struct Q8Slice {
 // Q4_0 (18-byte blocks): the lane's block spans five words starting at word
 // 9l of the segment (+4 for odd blocks); 9 is odd, so again conflict-free.
 // Byte j of the 16 nibble bytes holds q_j (low nibble) and q_{j+16} (high).
-// Taking each word as two half-words of two bytes (B0, B1), the nibble at
-// bit 4p of a half-word is, for p = 0..3: B0.lo, B0.hi, B1.lo, B1.hi. A
-// nibble at bit 4p dropped into the mantissa of 2^23 gives 2^23 + q*16^p; one
-// fma with (16^-p, -(2^(23-4p)+8)) turns that into q - 8 exactly.
+// For a word of four such bytes, masking with 0x0F0F0F0F (and the same after
+// a 4-bit shift) leaves four codes as bytes, and each byte goes into the
+// mantissa of 2^23 with one byte-permute as in Q8_0; one packed add of
+// -(2^23 + 8) per pair gives q - 8 exactly. (Pulling each nibble in place
+// with its own scale, one fma per pair, needs four constant pairs per word
+// and measured about 30 % more instructions.)
 template <int CPW>
 struct Q4Slice {
-  float2 a[CPW][16];       // pair j: (a_j, a_{16+j})
+  float2 a[CPW][16];       // a[2t], a[2t+1]: elements 4t .. 4t+3; a[8+2t], a[9+2t]: 16+4t ..
   uint32_t woff[CPW];
   bool odd;
   bool ok[CPW];
@@ -153,28 +171,12 @@ struct Q4Slice {
       for (int t = 0; t < 4; ++t) {
         const float4 lo = ok[c] ? lds128f(src + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 hi = ok[c] ? lds128f(src + 64u + 16u * t) : make_float4(0.f, 0.f, 0.f, 0.f);
-        a[c][4 * t] = make_float2(lo.x, hi.x);
-        a[c][4 * t + 1] = make_float2(lo.y, hi.y);
-        a[c][4 * t + 2] = make_float2(lo.z, hi.z);
-        a[c][4 * t + 3] = make_float2(lo.w, hi.w);
+        a[c][2 * t] = make_float2(lo.x, lo.y);
+        a[c][2 * t + 1] = make_float2(lo.z, lo.w);
+        a[c][8 + 2 * t] = make_float2(hi.x, hi.y);
+        a[c][9 + 2 * t] = make_float2(hi.z, hi.w);
       }
     }
-  }
-  // One half-word (bytes j, j+1) into two f32x2 sums.
-  __device__ __forceinline__ static void halfword(uint32_t x, float2 a01, float2 a23, float2& acc0,
-                                                  float2& acc1) {
-    const float2 s01 = make_float2(1.0f, 0.0625f);
-    const float2 c01 = make_float2(-8388616.0f, -524296.0f);
-    const float2 s23 = make_float2(0.00390625f, 0.000244140625f);
-    const float2 c23 = make_float2(-32776.0f, -2056.0f);
-    float2 v01 = make_float2(__uint_as_float((x & 0x000Fu) | 0x4B000000u),
-                             __uint_as_float((x & 0x00F0u) | 0x4B000000u));
-    float2 v23 = make_float2(__uint_as_float((x & 0x0F00u) | 0x4B000000u),
-                             __uint_as_float((x & 0xF000u) | 0x4B000000u));
-    v01 = ffma2(v01, s01, c01);  // (q_j - 8, q_{16+j} - 8)
-    v23 = ffma2(v23, s23, c23);  // (q_{j+1} - 8, q_{17+j} - 8)
-    acc0 = ffma2(v01, a01, acc0);
-    acc1 = ffma2(v23, a23, acc1);
   }
   template <bool ODD>
   __device__ __forceinline__ float dot_par(uint32_t row, int c) const {
@@ -182,14 +184,22 @@ struct Q4Slice {
 #pragma unroll
     for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff[c] + 4u * i);
     const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
+    const float2 m8 = make_float2(-kMagicQ4, -kMagicQ4);
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
-      halfword(x, a[c][4 * i], a[c][4 * i + 1], acc[0], acc[1]);
-      halfword(x >> 16, a[c][4 * i + 2], a[c][4 * i + 3], acc[2], acc[3]);
+      const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+      const float2 l01 = fadd2(make_float2(s8_to_magic(lo, 0), s8_to_magic(lo, 1)), m8);
+      const float2 l23 = fadd2(make_float2(s8_to_magic(lo, 2), s8_to_magic(lo, 3)), m8);
+      const float2 h01 = fadd2(make_float2(s8_to_magic(hi, 0), s8_to_magic(hi, 1)), m8);
+      const float2 h23 = fadd2(make_float2(s8_to_magic(hi, 2), s8_to_magic(hi, 3)), m8);
+      acc[0] = ffma2(l01, a[c][2 * i], acc[0]);
+      acc[1] = ffma2(l23, a[c][2 * i + 1], acc[1]);
+      acc[2] = ffma2(h01, a[c][8 + 2 * i], acc[2]);
+      acc[3] = ffma2(h23, a[c][9 + 2 * i], acc[3]);
     }
     const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
     return d * (s.x + s.y);

@@ -85,11 +85,9 @@ struct Q8SliceM {
     const float2 mb = make_float2(-kMagicS8, -kMagicS8);
     float2 q[16];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t x = (ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u)) ^ 0x80808080u;
-      q[2 * i] = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
-      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
-    }
+    for (int i = 0; i < 9; ++i) w[i] ^= 0x80808080u;  // sign bits flipped (the scale is read above)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q8_quad<ODD>(w, i, mb, q[2 * i], q[2 * i + 1]);
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       float2 acc[4];
@@ -111,7 +109,7 @@ struct Q8SliceM {
 
 template <int MT>
 struct Q4SliceM {
-  float2 a[MT][16];  // pair j: (a_j, a_{16+j})
+  float2 a[MT][16];  // a[t][2u], a[t][2u+1]: elements 4u .. 4u+3; a[t][8+2u], a[t][9+2u]: 16+4u ..
   uint32_t woff;
   bool odd, ok;
   __device__ __forceinline__ void init(uint32_t sA, uint32_t a_stride, int kg, int lane, int K) {
@@ -127,35 +125,31 @@ struct Q4SliceM {
       for (int u = 0; u < 4; ++u) {
         const float4 lo = ok ? lds128f(src + 16u * u) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 hi = ok ? lds128f(src + 64u + 16u * u) : make_float4(0.f, 0.f, 0.f, 0.f);
-        a[t][4 * u] = make_float2(lo.x, hi.x);
-        a[t][4 * u + 1] = make_float2(lo.y, hi.y);
-        a[t][4 * u + 2] = make_float2(lo.z, hi.z);
-        a[t][4 * u + 3] = make_float2(lo.w, hi.w);
+        a[t][2 * u] = make_float2(lo.x, lo.y);
+        a[t][2 * u + 1] = make_float2(lo.z, lo.w);
+        a[t][8 + 2 * u] = make_float2(hi.x, hi.y);
+        a[t][9 + 2 * u] = make_float2(hi.z, hi.w);
       }
     }
   }
+  // the codes once (as Q4Slice: masked into bytes, each into the 2^23
+  // magic), then one set of packed fmas per token
   template <bool ODD>
   __device__ __forceinline__ void dot_par(uint32_t row, float (&out)[MT]) const {
     uint32_t w[5];
 #pragma unroll
     for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff + 4u * i);
     const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
-    const float2 s01 = make_float2(1.0f, 0.0625f), c01 = make_float2(-8388616.0f, -524296.0f);
-    const float2 s23 = make_float2(0.00390625f, 0.000244140625f), c23 = make_float2(-32776.0f, -2056.0f);
-    float2 q[16];  // pair j: (q_j - 8, q_{16+j} - 8)
+    const float2 m8 = make_float2(-kMagicQ4, -kMagicQ4);
+    float2 q[16];  // same pairing as a[t]
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t y = x >> (16 * h);
-        q[4 * i + 2 * h] = ffma2(make_float2(__uint_as_float((y & 0x000Fu) | 0x4B000000u),
-                                             __uint_as_float((y & 0x00F0u) | 0x4B000000u)),
-                                 s01, c01);
-        q[4 * i + 2 * h + 1] = ffma2(make_float2(__uint_as_float((y & 0x0F00u) | 0x4B000000u),
-                                                 __uint_as_float((y & 0xF000u) | 0x4B000000u)),
-                                     s23, c23);
-      }
+      const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+      q[2 * i] = fadd2(make_float2(s8_to_magic(lo, 0), s8_to_magic(lo, 1)), m8);
+      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(lo, 2), s8_to_magic(lo, 3)), m8);
+      q[8 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 0), s8_to_magic(hi, 1)), m8);
+      q[9 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 2), s8_to_magic(hi, 3)), m8);
     }
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
