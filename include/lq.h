@@ -74,8 +74,9 @@ typedef enum { LQ_FMT_F16 = 0, LQ_FMT_Q8_0 = 1, LQ_FMT_Q4_0 = 2, LQ_FMT_Q4_0I = 
 /* ---- decode GEMV, M == 1 (M != 1 -> LQ_ERR_INVALID_ARG) -----------------
  * One pass over W: each output C[0,n] = sum_k A[0,k] * w(n,k), accumulated
  * in f32 (Q formats: sum of q*a per block slice, times d, as gemv_q8_decode /
- * gemv_q4_decode do). Bound by HBM bandwidth, as the page notes for decode
- * (dispatch.rs, dispatch_gemm_q3: "decode is weight-bandwidth-bound"). */
+ * gemv_q4_decode do). Bound by HBM bandwidth: a decode step streams every
+ * weight once, the point the page's dispatcher makes for decode (dispatch.rs,
+ * dispatch_gemm_q3). */
 lq_status lq_gemv_f16 (const float* A, const void* W, float* C,
                        int64_t M, int64_t N, int64_t K, void* stream);
 lq_status lq_gemv_q8_0(const float* A, const void* W, float* C,
