@@ -48,8 +48,7 @@ struct F16SliceM {
       acc1 = ffma2(f3, a[t][3], acc1);
       out[t] = (acc.x + acc1.x) + (acc.y + acc1.y);
     }
-  }
-};
+  }};
 
 // Q8_0 / Q4_0: one whole block per lane (see Q8Slice / Q4Slice for the
 // mapping and the bank argument); the block's 32 values are dequantised into
@@ -76,18 +75,8 @@ struct Q8SliceM {
       }
     }
   }
-  template <bool ODD>
-  __device__ __forceinline__ void dot_par(uint32_t row, float (&out)[MT]) const {
-    uint32_t w[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) w[i] = lds32(row + woff + 4u * i);
-    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
-    const float2 mb = make_float2(-kMagicS8, -kMagicS8);
-    float2 q[16];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) w[i] ^= 0x80808080u;  // sign bits flipped (the scale is read above)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q8_quad<ODD>(w, i, mb, q[2 * i], q[2 * i + 1]);
+  // the block's codes q (paired as a[t]) times each token's activations
+  __device__ __forceinline__ void fma_tokens(const float2 (&q)[16], float d, float (&out)[MT]) const {
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       float2 acc[4];
@@ -99,11 +88,22 @@ struct Q8SliceM {
       out[t] = d * (s.x + s.y);
     }
   }
+  // one code path for both block parities (as Q8Slice::dot)
   __device__ __forceinline__ void dot(uint32_t row, float (&out)[MT]) const {
-    if (odd)
-      dot_par<true>(row, out);
-    else
-      dot_par<false>(row, out);
+    uint32_t w[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) w[i] = lds32(row + woff + 4u * i);
+    const float d = f16_lo(w[0] >> (odd ? 16 : 0));
+    const uint32_t sh = odd ? 32u : 16u;
+    const float2 mb = make_float2(-kMagicS8, -kMagicS8);
+    float2 q[16];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t x = __funnelshift_rc(w[i], w[i + 1], sh) ^ 0x80808080u;
+      q[2 * i] = fadd2(make_float2(s8_to_magic(x, 0), s8_to_magic(x, 1)), mb);
+      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(x, 2), s8_to_magic(x, 3)), mb);
+    }
+    fma_tokens(q, d, out);
   }
 };
 
@@ -134,23 +134,8 @@ struct Q4SliceM {
   }
   // the codes once (as Q4Slice: masked into bytes, each into the 2^23
   // magic), then one set of packed fmas per token
-  template <bool ODD>
-  __device__ __forceinline__ void dot_par(uint32_t row, float (&out)[MT]) const {
-    uint32_t w[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff + 4u * i);
-    const float d = f16_lo(ODD ? (w[0] >> 16) : w[0]);
-    const float2 m8 = make_float2(-kMagicQ4, -kMagicQ4);
-    float2 q[16];  // same pairing as a[t]
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t x = ODD ? w[i + 1] : __byte_perm(w[i], w[i + 1], 0x5432u);  // bytes 4i .. 4i+3
-      const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
-      q[2 * i] = fadd2(make_float2(s8_to_magic(lo, 0), s8_to_magic(lo, 1)), m8);
-      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(lo, 2), s8_to_magic(lo, 3)), m8);
-      q[8 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 0), s8_to_magic(hi, 1)), m8);
-      q[9 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 2), s8_to_magic(hi, 3)), m8);
-    }
+  // the block's codes q (paired as a[t]) times each token's activations
+  __device__ __forceinline__ void fma_tokens(const float2 (&q)[16], float d, float (&out)[MT]) const {
 #pragma unroll
     for (int t = 0; t < MT; ++t) {
       float2 acc[4];
@@ -162,11 +147,25 @@ struct Q4SliceM {
       out[t] = d * (s.x + s.y);
     }
   }
+  // one code path for both block parities (as Q8Slice::dot)
   __device__ __forceinline__ void dot(uint32_t row, float (&out)[MT]) const {
-    if (odd)
-      dot_par<true>(row, out);
-    else
-      dot_par<false>(row, out);
+    uint32_t w[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) w[i] = lds32(row + woff + 4u * i);
+    const float d = f16_lo(w[0] >> (odd ? 16 : 0));
+    const uint32_t sh = odd ? 32u : 16u;
+    const float2 m8 = make_float2(-kMagicQ4, -kMagicQ4);
+    float2 q[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t x = __funnelshift_rc(w[i], w[i + 1], sh);
+      const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+      q[2 * i] = fadd2(make_float2(s8_to_magic(lo, 0), s8_to_magic(lo, 1)), m8);
+      q[2 * i + 1] = fadd2(make_float2(s8_to_magic(lo, 2), s8_to_magic(lo, 3)), m8);
+      q[8 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 0), s8_to_magic(hi, 1)), m8);
+      q[9 + 2 * i] = fadd2(make_float2(s8_to_magic(hi, 2), s8_to_magic(hi, 3)), m8);
+    }
+    fma_tokens(q, d, out);
   }
 };
 
