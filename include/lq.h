@@ -88,8 +88,11 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
  * Counterparts: gemm_q8 / gemm_q4 / gemm_q4_tiled (metal_qwen35.rs),
  * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). Small M streams W on the
  * CUDA cores in f32 (GEMV accuracy); larger M runs on the tensor cores
- * (tcgen05, TMEM accumulators) with A rounded to bf16 and W dequantised to
- * bf16, products accumulated in f32. */
+ * (tcgen05, TMEM accumulators): each token row of A scaled by an exact power
+ * of two and rounded to f16 (11 significant bits, at least bf16's precision),
+ * W dequantised to f16, products accumulated in f32; shapes that kernel does
+ * not take use a tcgen05 kernel with bf16 operands. Tolerance: 5e-3 times
+ * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16. */
 lq_status lq_gemm_f16 (const float* A, const void* W, float* C,
                        int64_t M, int64_t N, int64_t K, void* stream);
 lq_status lq_gemm_q8_0(const float* A, const void* W, float* C,
