@@ -156,9 +156,11 @@ lq_status lq_pack_q8_0_rcp(const float* W_host, int64_t N, int64_t K, void* out_
  * call. Weights are streamed ahead of the computation in every case. One
  * cooperative launch of one CTA per SM; the problems array is read during
  * the call (host memory, caller-owned).
- *   - count in 1..64; N_j >= 0; K_j in 1..16384 with K_j % 8 == 0 (f16) or
- *     K_j % 256 == 0 (quantised); A_j and W_j 16-byte aligned. Anything else
- *     returns LQ_ERR_UNSUPPORTED without launching (use lq_gemv_<fmt>).
+ *   - count in 1..64; N_j >= 0; K_j % 8 == 0 (f16) or K_j % 256 == 0
+ *     (quantised) with the largest K_j at most 4096 (f16), 14336 (Q8_0) or
+ *     15616 (Q4_0, Q4_0I) so that A and the ring fit in shared memory;
+ *     A_j and W_j 16-byte aligned. Anything else returns
+ *     LQ_ERR_UNSUPPORTED without launching (use lq_gemv_<fmt>).
  *   - Device-side waits are bounded; lq_last_device_error reports a
  *     timeout. At most 64 calls may be in flight at once across streams. */
 typedef struct {

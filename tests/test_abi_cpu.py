@@ -204,3 +204,24 @@ def test_topk_argument_errors_return_before_launch(lq):
     assert L.lq_gemv_topk(0, x, x, None, 10, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG  # C required
     assert L.lq_gemv_topk(9, x, x, x, 10, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
     assert L.lq_gemv_topk(0, x, x, x, 0, 64, 5, v, i, w, 0) == lq.LQ_ERR_INVALID_ARG
+
+
+def test_chain_argument_errors_and_limits_return_before_launch(lq):
+    """lq_gemv_chain refuses bad problem lists before touching the device,
+    including the f16 K limit of its warp grid (16 chunks of 256 values)."""
+    L = lq.lib()
+    a, w, c = 0x10000, 0x20000, 0x30000
+
+    def call(fmt, items):
+        arr = lq.gemv_problems(items)
+        return L.lq_gemv_chain(fmt, arr, len(items), 0)
+
+    assert call(7, [(a, w, c, 8, 64, 0)]) == lq.LQ_ERR_INVALID_ARG           # format
+    assert L.lq_gemv_chain(0, None, 1, 0) == lq.LQ_ERR_INVALID_ARG            # no list
+    assert call(0, [(a, w, c, -1, 64, 0)]) == lq.LQ_ERR_INVALID_ARG          # N < 0
+    assert call(1, [(a, w, c, 8, 48, 0)]) == lq.LQ_ERR_INVALID_ARG           # K % 32
+    assert call(0, [(a, None, c, 8, 64, 0)]) == lq.LQ_ERR_INVALID_ARG        # null W
+    assert call(0, [(a + 4, w, c, 8, 64, 0)]) == lq.LQ_ERR_UNSUPPORTED       # A not 16-byte aligned
+    assert call(1, [(a, w, c, 8, 128, 0)]) == lq.LQ_ERR_UNSUPPORTED          # K % 256 (quantised)
+    assert call(0, [(a, w, c, 8, 4096 + 8, 0)]) == lq.LQ_ERR_UNSUPPORTED     # f16 K > 4096
+    assert call(0, [(a, w, c, 8, 64, 0)] * 65) == lq.LQ_ERR_UNSUPPORTED      # more than 64 problems
