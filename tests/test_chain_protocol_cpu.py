@@ -1,5 +1,6 @@
-"""A CPU model of the decode chain's weight-ring protocol (lq_gemv_chain.cu,
-consumers and producer), run under random interleavings.
+"""A CPU model of the weight-ring protocols of the decode chain
+(lq_gemv_chain.cu), the streaming GEMV (lq_gemv.cu) and the batched decode
+kernel (lq_gemv_batch.cu), run under random interleavings.
 
 The model keeps the kernel's rules: global stage g lives in ring slot g mod S
 with phase (g / S) mod 2, belongs to row-group g mod nr (S a multiple of nr)
@@ -14,9 +15,12 @@ parity P passes once the phase with parity P is the last one completed.
 
 Checked: each warp reads the stage it expects from the slot (never a refill
 or a stale copy), each finisher reads partials of its own stage only, and the
-run never deadlocks. Two planted mistakes must be caught: one partials buffer
-per slot instead of one per phase, and a ring whose slot count is not a
-multiple of the row-groups.
+run never deadlocks. The streaming GEMV differs in its release (the finisher
+hands the slot back after reading the partials, one buffer per slot), the
+batched kernel in having no producer (the finisher refills the slot after
+reading the partials). Three planted mistakes must be caught: the chain with
+one partials buffer per slot, a ring whose slot count is not a multiple of the
+row-groups, and the batched kernel's refill issued before the read.
 """
 import random
 
@@ -38,7 +42,13 @@ class Barrier:
         return (self.done & 1) != parity
 
 
-def run(S, nr, nk, stages, seed, phase_buffers=2, max_steps=200000):
+def run(S, nr, nk, stages, seed, phase_buffers=2, mode="chain", max_steps=200000):
+    """mode "chain": every warp releases the slot right after posting its
+    partial (partials double-buffered by phase); "stream" (lq_gemv.cu): the
+    finisher releases the slot after reading the partials (one buffer per
+    slot); "batch" (lq_gemv_batch.cu): no producer, the finisher issues the
+    stage S further on into the slot after reading the partials;
+    "batch-early": the same with the refill issued before the read."""
     rng = random.Random(seed)
     full = [Barrier(1) for _ in range(S)]
     empty = [Barrier(nk) for _ in range(S)]
@@ -52,6 +62,12 @@ def run(S, nr, nk, stages, seed, phase_buffers=2, max_steps=200000):
 
     def buf(g):
         return ((g // S) & 1) if phase_buffers == 2 else 0
+
+    if mode.startswith("batch"):
+        phase_buffers = 1
+        for g in range(min(S, stages)):
+            in_flight.append((g % S, g))
+        prod["g"] = stages  # no producer: the finishers refill
 
     def producer_step():
         g = prod["g"]
@@ -86,18 +102,30 @@ def run(S, nr, nk, stages, seed, phase_buffers=2, max_steps=200000):
             assert slot[s] == g, f"warp {key} read stage {slot[s]} in slot {s}, expected {g}"
             w["step"] = 1
             return True
-        if w["step"] == 1:                      # partial, red_full, early empty
+        if w["step"] == 1:                      # partial, red_full (and empty)
             red[(buf(g), s, kg)] = g
             red_full[s].arrive()
-            empty[s].arrive()
+            if mode == "chain" or (mode == "stream" and kg != kf):
+                empty[s].arrive()
             w["step"] = 2 if kg == kf else 3
             return True
         if w["step"] == 2:                      # finisher: every K-group's partial
             if not red_full[s].passed(ph):
                 return False
+            if mode == "batch-early":
+                if g + S < stages:
+                    in_flight.append((s, g + S))  # refill first (the planted mistake)
+                w["step"] = 4                   # ... and read in a later step
+                return True
+            w["step"] = 4
+        if w["step"] == 4:
             for k in range(nk):
                 got = red[(buf(g), s, k)]
                 assert got == g, f"finisher of stage {g} read K-group {k}'s partial of stage {got}"
+            if mode == "stream":
+                empty[s].arrive()
+            if mode == "batch" and g + S < stages:
+                in_flight.append((s, g + S))    # the refill, after the read
             w["step"] = 3
             return True
         w["g"] = g + nr                         # next stage of this row-group
@@ -115,12 +143,13 @@ def run(S, nr, nk, stages, seed, phase_buffers=2, max_steps=200000):
     raise AssertionError("did not finish")
 
 
+@pytest.mark.parametrize("mode", ["chain", "stream", "batch"])
 @pytest.mark.parametrize("S,nr,nk", [(4, 4, 4), (8, 4, 4), (16, 4, 4), (2, 1, 16), (8, 2, 8), (6, 2, 8),
                                      (32, 8, 2)])
-def test_ring_protocol_under_random_interleavings(S, nr, nk):
+def test_ring_protocol_under_random_interleavings(S, nr, nk, mode):
     stages = 5 * S + 3
-    for seed in range(60):
-        run(S, nr, nk, stages, seed)
+    for seed in range(40):
+        run(S, nr, nk, stages, seed, mode=mode)
 
 
 def test_single_partials_buffer_is_caught():
@@ -147,5 +176,19 @@ def test_ring_not_a_multiple_of_row_groups_is_caught():
         try:
             run(6, 4, 2, 40, seed)
         except AssertionError:
+            caught += 1
+    assert caught > 0
+
+
+def test_batch_refill_before_reading_the_partials_is_caught():
+    """The batched kernel's first version refilled the slot before its
+    finisher had read the partials, and lost parity at M = 4: the next stage
+    in the slot wrote over them. The model must find that interleaving."""
+    caught = 0
+    for seed in range(300):
+        try:
+            run(4, 4, 4, 40, seed, mode="batch-early")
+        except AssertionError as e:
+            assert "partial" in str(e)
             caught += 1
     assert caught > 0
