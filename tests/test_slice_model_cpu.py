@@ -12,7 +12,9 @@ half (odd); each word of codes is the funnel shift of words i, i+1 by 16 bits
 flipped, Q4_0 codes the bytes of (x & 0x0F0F0F0F) and ((x >> 4) & 0x0F0F0F0F);
 each goes into the low mantissa byte of 2^23 and the bias comes off with one
 exact subtraction. The products here are summed in float64: the model checks
-which codes and activations meet, not the order of the f32 sums.
+which codes and activations meet, not the order of the f32 sums. For Q4_0 with
+interleaved nibbles the same dot runs on A reordered per block as the
+kernels spread it (lq_q4i.cuh).
 """
 import numpy as np
 import pytest
@@ -115,3 +117,40 @@ def test_planted_q4_lane_stride_is_caught():
     want = _oracle_block_dots("q4_0", row, a, K)
     bad = [abs(q4_block_dot(row, a, 0, lane, woff_step=34)[1] - want[2 * lane]) > 1e-6 for lane in range(1, 32)]
     assert any(bad)
+
+
+def _q4i_store_chunks(a_block):
+    """The kernels' spread of one block's 32 activations for interleaved
+    Q4_0 (lq_q4i.cuh, store_chunk): 16-byte chunk i (elements 4i .. 4i+3)
+    puts elements 4i, 4i+2 at slots 2i, 2i+1 and 4i+1, 4i+3 at slots
+    16+2i, 17+2i."""
+    out = np.empty(32, dtype=a_block.dtype)
+    for i in range(8):
+        x, y, z, w = a_block[4 * i: 4 * i + 4]
+        out[2 * i], out[2 * i + 1] = x, z
+        out[16 + 2 * i], out[17 + 2 * i] = y, w
+    return out
+
+
+def test_q4_0i_reordered_activations_give_the_interleaved_product():
+    """Slot j of a block = element 2j, slot 16+j = element 2j+1 (slot_of);
+    the standard-order Q4_0 dot on interleaved bytes and reordered A must
+    equal the oracle's interleaved dequantisation times the original A."""
+    for e in range(32):
+        slot = (16 + (e >> 1)) if (e & 1) else (e >> 1)
+        assert _q4i_store_chunks(np.arange(32))[slot] == e
+    K = 2048
+    W, A = synthetic.draw(1, 2, K, seed=8, outlier_frac=0.1)
+    packed = O.pack("q4_0i", W.numpy())
+    a = A.numpy()[0]
+    a_perm = np.concatenate([_q4i_store_chunks(blk) for blk in a.reshape(-1, 32)])
+    for r in range(2):
+        row = packed[r]
+        want = _oracle_block_dots("q4_0i", row, a, K)
+        for kg in range(2 * ((K // 32 + 63) // 64)):
+            for lane in range(32):
+                b, got = q4_block_dot(row, a_perm, kg, lane)
+                assert abs(got - want[b]) <= 1e-9 * (1 + abs(want[b])), (r, kg, lane, b)
+        # and without the reorder the standard dot does not give it
+        b, plain = q4_block_dot(row, a, 0, 0)
+        assert abs(plain - want[b]) > 1e-6
