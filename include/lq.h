@@ -92,7 +92,12 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
  * of two and rounded to f16 (11 significant bits, at least bf16's precision),
  * W dequantised to f16, products accumulated in f32; shapes that kernel does
  * not take use a tcgen05 kernel with bf16 operands. Tolerance: 5e-3 times
- * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16. */
+ * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16.
+ * Limit: for Q8_0 and Q4_0 the tensor-core route forms 2^8 * w in f16 (to
+ * keep small weights clear of f16 subnormals), so dequantised weights must
+ * stay below 256 in magnitude there; larger ones overflow to inf. The CUDA-
+ * core routes (M = 1, and M = 2..4 where the batched kernel applies) have no
+ * such limit. */
 lq_status lq_gemm_f16 (const float* A, const void* W, float* C,
                        int64_t M, int64_t N, int64_t K, void* stream);
 lq_status lq_gemm_q8_0(const float* A, const void* W, float* C,
