@@ -192,3 +192,45 @@ def test_batch_refill_before_reading_the_partials_is_caught():
             assert "partial" in str(e)
             caught += 1
     assert caught > 0
+
+
+def _cta_rows(b, G, N):
+    r0 = (b * N) // G
+    return r0, ((b + 1) * N) // G - r0
+
+
+@pytest.mark.parametrize("S,nr,nk,RS", [(4, 4, 4, 8), (8, 4, 4, 5), (16, 4, 4, 2), (2, 1, 16, 8),
+                                        (6, 2, 8, 8), (32, 8, 2, 1)])
+def test_incremental_stage_walk_matches_the_closed_forms(S, nr, nk, RS):
+    """Each consumer warp of the chain walks its row-group's global stages
+    rg, rg + nr, ... through all problems, advancing slot, ring phase and
+    finisher incrementally (no divisions per problem). Over random problem
+    lists (CTAs with no rows of some problems included) the walk must visit
+    exactly the stages g = rg mod nr of every problem, with slot g mod S,
+    phase (g / S) mod 2 and finisher (g / nr) mod nk."""
+    rng = random.Random(S * 100 + nr * 10 + RS)
+    G = 152
+    for _ in range(20):
+        Ns = [rng.choice([0, 1, 5, 100, 151, 152, 153, 4096, 11008]) for _ in range(rng.randint(1, 12))]
+        for b in (0, 1, 75, 151):
+            nsts = [(_cta_rows(b, G, N)[1] + RS - 1) // RS for N in Ns]
+            visited = set()
+            for rg in range(nr):
+                gw, s, ph, kf, g0 = rg, rg, 0, 0, 0
+                for j, nst in enumerate(nsts):
+                    st = gw - g0
+                    assert 0 <= st < nr  # the warp's next stage is in this problem's first nr
+                    while st < nst:
+                        g = g0 + st
+                        assert (s, ph, kf) == (g % S, (g // S) & 1, (g // nr) % nk)
+                        assert g % nr == rg
+                        visited.add((j, st))
+                        s += nr
+                        if s >= S:
+                            s -= S
+                            ph ^= 1
+                        kf = kf + 1 if kf + 1 < nk else 0
+                        gw += nr
+                        st += nr
+                    g0 += nst
+            assert visited == {(j, st) for j, nst in enumerate(nsts) for st in range(nst)}
