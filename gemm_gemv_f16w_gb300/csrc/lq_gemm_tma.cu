@@ -151,6 +151,9 @@ __global__ void __launch_bounds__(kPreThreads) a_to_f16_kernel(const float* __re
   float inv = 1.f, s = 1.f;
   if (amax > 0.f && amax <= 3.4e38f) {
     frexpf(amax, &e);
+    // below 2^-112, 2^(15 - e) would overflow f32: such rows are scaled by
+    // 2^126 instead (their largest value lands below 2^14, still finite)
+    e = max(e, -111);
     s = ldexpf(1.f, e - 15);
     inv = ldexpf(1.f, 15 - e);
   }

@@ -128,3 +128,23 @@ def test_gemm_row_equals_gemv(lq, cuda_dev):
         lq.lq_gemv_q8_0(A[m:m + 1].contiguous().to(cuda_dev), Wd, g, 1, 512, 1024)
         torch.cuda.synchronize()
         assert np.all(np.abs(g.cpu().numpy()[0] - C[m]) <= tol[m])
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0"])
+def test_tiny_activation_rows_stay_finite(lq, cuda_dev, fmt):
+    """Token rows whose largest value is below 2^-112 (f32 subnormals
+    included) are scaled by 2^126 in the f16 pre-pass instead of 2^(15 - e),
+    which would overflow f32; their outputs stay finite and within the
+    tolerance."""
+    M, N, K = 64, 256, 512
+    W, A = synthetic.draw(M, N, K, seed=12)
+    A = A.clone()
+    A[3] *= 1e-36
+    A[7] = A[7] * 1e-38 * 1e-3   # f32 subnormals
+    A[11] = 0.0
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    assert lq.route_count(2) == 1
+    assert np.all(np.isfinite(C))
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} tiny rows")
