@@ -71,25 +71,7 @@ void set_use_pdl(bool on) { g_use_pdl.store(on); }
 
 lq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? LQ_OK : LQ_ERR_CUDA; }
 
-namespace {
-
 bool aligned_to(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Arguments for the launchers: LQ_FMT_Q4_0I runs the Q4_0 kernels with A
-// reordered within each block (lq_q4i.cuh).
-MatmulArgs make_args(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
-                     void* stream) {
-  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
-  if (fmt == LQ_FMT_Q4_0I) {
-    a.fmt = LQ_FMT_Q4_0;
-    a.a_perm = true;
-  }
-  return a;
-}
-
-bool known_format(int fmt) {
-  return fmt == LQ_FMT_F16 || fmt == LQ_FMT_Q8_0 || fmt == LQ_FMT_Q4_0 || fmt == LQ_FMT_Q4_0I;
-}
 
 // Shared argument checks. Returns LQ_OK to proceed, or the status to return;
 // `*noop` is set when the call is a valid no-op.
@@ -109,6 +91,24 @@ lq_status validate(int fmt, const float* A, const void* W, float* C, int64_t M, 
   // 32-bit indexing inside the kernels
   if (M > (1LL << 31) - 1 || N > (1LL << 30) || K > (1LL << 30)) return LQ_ERR_UNSUPPORTED;
   return LQ_OK;
+}
+
+namespace {
+
+// Arguments for the launchers: LQ_FMT_Q4_0I runs the Q4_0 kernels with A
+// reordered within each block (lq_q4i.cuh).
+MatmulArgs make_args(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
+                     void* stream) {
+  MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
+  if (fmt == LQ_FMT_Q4_0I) {
+    a.fmt = LQ_FMT_Q4_0;
+    a.a_perm = true;
+  }
+  return a;
+}
+
+bool known_format(int fmt) {
+  return fmt == LQ_FMT_F16 || fmt == LQ_FMT_Q8_0 || fmt == LQ_FMT_Q4_0 || fmt == LQ_FMT_Q4_0I;
 }
 
 lq_status do_gemv(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N, int64_t K,
@@ -263,6 +263,8 @@ lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, voi
     if (q.N < 0 || q.K < 1) return LQ_ERR_INVALID_ARG;
     if (fmt != LQ_FMT_F16 && q.K % 32 != 0) return LQ_ERR_INVALID_ARG;
     if (!q.A || !q.W || !q.C) return LQ_ERR_INVALID_ARG;
+    if (!aligned_to(q.A, 4) || !aligned_to(q.C, 4)) return LQ_ERR_INVALID_ARG;
+    if (fmt == LQ_FMT_F16 && !aligned_to(q.W, 2)) return LQ_ERR_INVALID_ARG;
   }
   return lq::launch_gemv_chain(fmt, problems, count, static_cast<cudaStream_t>(stream));
 }

@@ -97,4 +97,11 @@ unsigned read_clear_batch_error();
 
 lq_status cuda_status(cudaError_t e);
 
+bool aligned_to(const void* p, unsigned a);
+// The argument checks every matmul entry point makes before launching
+// anything: LQ_OK to proceed (with *noop set for M == 0 or N == 0), else the
+// status to return.
+lq_status validate(int fmt, const float* A, const void* W, float* C, int64_t M, int64_t N,
+                   int64_t K, bool* noop);
+
 }  // namespace lq

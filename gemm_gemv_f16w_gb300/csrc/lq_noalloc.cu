@@ -50,10 +50,11 @@ using namespace lq;
 extern "C" lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, float* C, int64_t M,
                                      int64_t N, int64_t K, void* stream) {
   if (fmt != LQ_FMT_F16 && fmt != LQ_FMT_Q8_0 && fmt != LQ_FMT_Q4_0) return LQ_ERR_INVALID_ARG;
-  if (M < 0 || N < 0 || K < 0) return LQ_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return LQ_OK;
-  if (!A || !W || !C) return LQ_ERR_INVALID_ARG;
-  if (fmt != LQ_FMT_F16 && K % 32 != 0) return LQ_ERR_INVALID_ARG;
+  // the same argument checks as lq_gemm_<fmt> (sizes, null pointers, the
+  // 4-byte alignment of A and C), before anything else
+  bool noop = false;
+  const lq_status vs = validate(fmt, A, W, C, M, N, K, &noop);
+  if (vs != LQ_OK || noop) return vs;
   MatmulArgs a{A, W, C, M, N, K, fmt, static_cast<cudaStream_t>(stream)};
   // Only the tensor-core kernel that needs the workspace is offered here.
   if (!gemm_tma_eligible(a)) return LQ_ERR_UNSUPPORTED;

@@ -225,3 +225,35 @@ def test_chain_argument_errors_and_limits_return_before_launch(lq):
     assert call(1, [(a, w, c, 8, 128, 0)]) == lq.LQ_ERR_UNSUPPORTED          # K % 256 (quantised)
     assert call(0, [(a, w, c, 8, 4096 + 8, 0)]) == lq.LQ_ERR_UNSUPPORTED     # f16 K > 4096
     assert call(0, [(a, w, c, 8, 64, 0)] * 65) == lq.LQ_ERR_UNSUPPORTED      # more than 64 problems
+
+
+def test_chain_refuses_misaligned_outputs_before_launch(lq):
+    """Each problem's A and C must be 4-byte aligned (f16 W 2-byte aligned),
+    as for lq_gemv_<fmt>: refused before any launch."""
+    L = lq.lib()
+    a, w, c = 0x10000, 0x20000, 0x30000
+    for fmt in (0, 1, 2, 3):
+        arr = lq.gemv_problems([(a, w, c + 2, 8, 256, 0)])
+        assert L.lq_gemv_chain(fmt, arr, 1, 0) == lq.LQ_ERR_INVALID_ARG
+        arr = lq.gemv_problems([(a, w, c, 8, 256, 0), (a + 1, w, c, 8, 256, 1)])
+        assert L.lq_gemv_chain(fmt, arr, 2, 0) == lq.LQ_ERR_INVALID_ARG
+    arr = lq.gemv_problems([(a, w + 1, c, 8, 256, 0)])
+    assert L.lq_gemv_chain(0, arr, 1, 0) == lq.LQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_noalloc_argument_errors_return_before_launch(lq, fmt):
+    """lq_gemm_noalloc makes the same argument checks as lq_gemm_<fmt> before
+    it looks at its workspace: never dereferenced here."""
+    L = lq.lib()
+    a, w, c = 0x10000, 0x20000, 0x30000
+    assert L.lq_gemm_noalloc(fmt, a, w, c, 0, 8, 256, 0) == lq.LQ_OK          # no-op
+    assert L.lq_gemm_noalloc(fmt, a, w, c, 8, 0, 256, 0) == lq.LQ_OK
+    assert L.lq_gemm_noalloc(fmt, a, w, c, 8, 8, 0, 0) == lq.LQ_ERR_INVALID_ARG   # K == 0
+    assert L.lq_gemm_noalloc(fmt, a, w, c, -1, 8, 256, 0) == lq.LQ_ERR_INVALID_ARG
+    assert L.lq_gemm_noalloc(fmt, a, w, c + 2, 8, 8, 256, 0) == lq.LQ_ERR_INVALID_ARG  # C alignment
+    assert L.lq_gemm_noalloc(fmt, a + 2, w, c, 8, 8, 256, 0) == lq.LQ_ERR_INVALID_ARG  # A alignment
+    assert L.lq_gemm_noalloc(fmt, a, w, None, 8, 8, 256, 0) == lq.LQ_ERR_INVALID_ARG
+    if fmt != 0:
+        assert L.lq_gemm_noalloc(fmt, a, w, c, 8, 8, 48, 0) == lq.LQ_ERR_INVALID_ARG  # K % 32
+    assert L.lq_gemm_noalloc(3, a, w, c, 8, 8, 256, 0) == lq.LQ_ERR_INVALID_ARG  # Q4_0I not taken

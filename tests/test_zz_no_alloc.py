@@ -1,10 +1,11 @@
 """lq_gemm_noalloc: the tensor-core GEMM for callers that must not allocate
 device memory (runtimes that own all device memory, fixed memory budgets,
 real-time paths). It runs on a fixed workspace inside the
-library; these tests check, through the C-ABI, that two calls in a row give
-the same answer as the regular lq_gemm_<fmt> entry point, within the
-tensor-core tolerance, and that a request larger than the workspace is
-refused without running anything.
+library; these tests check, through the C-ABI, on two calls in a row, that
+each output matches the CPU oracle element by element within the
+tensor-core tolerance, that it is bit-identical to the regular
+lq_gemm_<fmt> entry point (the same kernels on the same inputs), and that a
+request larger than the workspace is refused without running anything.
 
 This file is named to be collected last, so a run that stops at the first
 failure has already run every other test.
@@ -15,7 +16,7 @@ import torch
 
 import oracle as O
 import synthetic
-from helpers import nan_filled, to_dev
+from helpers import check, nan_filled, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -24,14 +25,13 @@ def _packed(lq, fmt, W, dev):
     return to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
 
 
-def _tolerance(fmt, W, A):
+def _reference(fmt, W, A):
     N, K = W.shape
-    _, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
-    return tol
+    return O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "f16", "q4_0"])
-def test_noalloc_matches_regular_gemm_on_two_calls_in_a_row(lq, cuda_dev, fmt):
+def test_noalloc_matches_oracle_and_regular_gemm_on_two_calls_in_a_row(lq, cuda_dev, fmt):
     # two different problems back to back on the shared workspace; the second
     # is smaller, so leftovers of the first would show if they were read
     cases = [(96, 384, 1024, 21), (40, 200, 512, 22)]
@@ -40,15 +40,19 @@ def test_noalloc_matches_regular_gemm_on_two_calls_in_a_row(lq, cuda_dev, fmt):
         W, A = synthetic.draw(M, N, K, seed=seed, outlier_frac=0.05)
         Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
         ref = nan_filled(M, N, cuda_dev)
+        lq.reset_counts()
         getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, ref, M, N, K)
+        assert lq.route_count(2) == 1  # the regular call took the tensor-core route
         out = nan_filled(M, N, cuda_dev)
         lq.lq_gemm_noalloc(fmt, Ad, Wd, out, M, N, K)
         torch.cuda.synchronize()
         assert lq.last_device_error() == lq.LQ_OK
         ref_h, out_h = ref.cpu().numpy(), out.cpu().numpy()
-        assert np.all(np.isfinite(out_h))
-        tol = _tolerance(fmt, W, A)
-        assert np.all(np.abs(out_h.astype(np.float64) - ref_h) <= tol), f"{fmt} {M}x{N}x{K}"
+        y, tol = _reference(fmt, W, A)
+        check(out_h, y, tol, f"noalloc {fmt} {M}x{N}x{K}")
+        check(ref_h, y, tol, f"lq_gemm_{fmt} {M}x{N}x{K}")
+        # same kernels, same inputs: the workspace must not change a bit
+        assert np.array_equal(out_h.view(np.uint32), ref_h.view(np.uint32)), f"{fmt} {M}x{N}x{K}"
 
 
 def test_noalloc_refuses_requests_beyond_its_workspace(lq, cuda_dev):
