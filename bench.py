@@ -316,13 +316,17 @@ def rate(wb: Workbench, seconds_per_launch: float):
 # ---------------------------------------------------------------- CPU oracle
 def oracle_rate(w: synthetic.Workload, seconds: float, rows=None):
     """Time the CPU oracle (dequantise + float64 matmul, as it stands) on the
-    workload's inputs, restricted to `rows` weight rows, for about `seconds`.
-    Returns (bytes/s of algorithmic traffic, sample description, calls, s)."""
+    workload's inputs, restricted to `rows` weight rows, for about `seconds`;
+    the oracle's quantisation of those rows is timed on its own. Returns
+    (bytes/s of algorithmic traffic, sample description, calls, seconds,
+    quantisation seconds)."""
     import oracle as O
     W, A = synthetic.draw_workload(w)
     Wn, An = W.numpy(), A.numpy()
     n = w.N if rows is None else min(rows, w.N)
+    tq = time.perf_counter()
     packed = O.pack(w.fmt, Wn[:n])
+    quant_s = time.perf_counter() - tq
     calls, t0 = 0, time.perf_counter()
     while True:
         O.reference(w.fmt, An, packed, n, w.K, tensor_core=w.M >= 128)
@@ -332,7 +336,37 @@ def oracle_rate(w: synthetic.Workload, seconds: float, rows=None):
     dt = time.perf_counter() - t0
     b = algorithmic_bytes(w.fmt, w.M, n, w.K)
     return (b * calls / dt, f"{calls} oracle call(s) of M={w.M}, N={n} of {w.N}, K={w.K} ({w.fmt})",
-            calls, dt)
+            calls, dt, quant_s)
+
+
+def oracle_subprocess(workload: str, seconds: float, threads):
+    """oracle_rate in a fresh interpreter whose BLAS and OpenMP pools have
+    `threads` threads (None: the library default, every core), so that the
+    thread count is fixed before numpy loads. Returns the parsed dict or an
+    {"error": ...} dict."""
+    env = dict(os.environ)
+    env["CUDA_VISIBLE_DEVICES"] = ""  # the oracle never touches the GPU
+    if threads:
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            env[k] = str(threads)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", workload,
+           "--oracle-seconds", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True,
+                           timeout=seconds * 6 + 120)
+        for line in r.stdout.splitlines()[::-1]:
+            if line.startswith("{"):
+                return json.loads(line)
+        return {"error": (r.stderr or r.stdout).strip().splitlines()[-1:] or ["no output"]}
+    except (subprocess.TimeoutExpired, OSError, ValueError) as e:
+        return {"error": str(e)}
+
+
+def workload_config(w: synthetic.Workload) -> dict:
+    """The `config` of both arms' lines: the workload itself."""
+    return {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "format": w.fmt,
+            "l2": "inputs larger than L2 (device arm: rotating weight copies, together "
+                  "more than twice the L2)"}
 
 
 def cpu_cores():
@@ -376,7 +410,7 @@ def run_reference(args, world, rank):
     import oracle as O
     w = synthetic.WORKLOADS[args.workload]
     steps, warmup = args.steps or 20, args.warmup
-    _, _, _, dt1 = oracle_rate(w, 0.0, rows=64)
+    _, _, _, dt1, _ = oracle_rate(w, 0.0, rows=64)
     per_row = dt1 / 64
     rows = int(max(8, min(w.N, args.ref_seconds / max(steps + warmup, 1) / max(per_row, 1e-9))))
     W, A = synthetic.draw_workload(w)
@@ -395,8 +429,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "GB/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": dt / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
-                                         "format": w.fmt},
+        "data": "synthetic", "config": workload_config(w),
         "cpu_baseline": {"value": val, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -426,7 +459,15 @@ def main():
                     choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused", "topk"],
                     help="how the headline step runs its matmuls (auto: chain for M = 1; argmax modes: "
                          "M = 1, the GEMV with its argmax)")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-seconds", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_sample:
+        w = synthetic.WORKLOADS[args.oracle_sample]
+        bps, sample, calls, cdt, quant_s = oracle_rate(w, args.oracle_seconds)
+        print(json.dumps({"bps": bps, "sample": sample, "calls": calls, "seconds": cdt,
+                          "quantise_s": quant_s}), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
@@ -515,18 +556,27 @@ def main():
         v, u, b = rate(xb, pl)
         pk = hbm_peak if b == "hbm" else tc_peak
         key = name if mode == "auto" else f"{name} [{mode}]"
-        extras[key] = {"value": v, "unit": u, "bound": b, "frac": v / pk, "us_per_matmul": pl * 1e6,
-                        "mode": xb.mode, "copies": xb.R, "launches": n * xb.kernels_per_step,
-                        "gb_per_s": xb.bytes_per_launch / pl / 1e9,
-                        "tflop_per_s": xb.flops_per_launch / pl / 1e12}
+        extras[key] = {"value": round(v, 1), "unit": u, "frac": round(v / pk, 4),
+                       "us": round(pl * 1e6, 3), "mode": xb.mode}
         xb.free()
 
-    # ---- CPU oracle baseline (rank 0 at N=1 only)
+    # ---- CPU oracle baseline (rank 0 at N=1 only): all threads and one
+    # thread, each in its own interpreter, quantisation timed separately
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        bps, sample, calls, cdt = oracle_rate(w, 10.0)
-        cpu = {"value": bps / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{sample}; {cdt:.1f} s; numpy float64 (BLAS matmul, multi-threaded)"}
+        full = oracle_subprocess(w.name, 10.0, None)
+        one = oracle_subprocess(w.name, 10.0, 1)
+        if "bps" in full:
+            cpu = {"value": full["bps"] / 1e9, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"{full['sample']}; {full['seconds']:.1f} s; numpy float64 "
+                             f"(dequantise + BLAS matmul, every core)",
+                   "value_1_thread": one["bps"] / 1e9 if "bps" in one else None,
+                   "quantise_s": {"all_threads": full["quantise_s"],
+                                  "1_thread": one.get("quantise_s")},
+                   "quantise_sample": f"oracle pack of the same {w.N} x {w.K} weights ({w.fmt})"}
+        else:
+            cpu = {"value": None, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                   "sample": f"oracle run failed: {full.get('error')}"}
 
     if rank == 0:
         line = {
@@ -534,12 +584,11 @@ def main():
             "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded torch.randn, recipe in synthetic.py)",
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "format": w.fmt,
-                       "launches_per_step": launches_per_step, "matmuls_per_step": wb.R,
-                       "l2": f"inputs larger than L2: {wb.R} weight copies, "
-                             f"{wb.R * wb.wbytes / 2**20:.0f} MiB > {L2_BYTES // 2**20} MiB",
-                       "step": f"one decode pass over the weight-copy stack ({wb.mode}), CUDA-graph replay",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(w),
+            "step": {"mode": wb.mode, "matmuls": wb.R, "launches": launches_per_step,
+                     "weight_copies_mib": round(wb.R * wb.wbytes / 2**20), "l2_mib": L2_BYTES // 2**20,
+                     "how": "one pass over the weight-copy stack, CUDA-graph replay",
+                     "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,

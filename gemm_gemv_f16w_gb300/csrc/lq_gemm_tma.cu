@@ -6,26 +6,27 @@
 // the tile loop) and gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs: f16
 // weights widened on load). The GB300 design:
 //
-//  1. a pre-pass turns A (f32) into f16 with an exact per-token power-of-two
-//     scale s_m, so the largest |a| of row m lands in [2^14, 2^15): no
-//     overflow, 11 significant bits (3 more than bf16), and the scale is
-//     undone exactly in the epilogue;
+//  1. a pre-pass rounds A (f32) to bf16, to nearest even: exactly the
+//     operand the tensor-core tolerance is defined on, over the whole f32
+//     range (bf16 keeps f32's exponent);
 //  2. the GEMM kernel, one CTA per SM, owns 128 rows of W and a tile of BT
 //     tokens. A producer thread moves raw W (f16 / Q8_0 / Q4_0 bytes) with
 //     one TMA box of full-width rows per stage: Q8_0 rows of 256 K are 272
 //     bytes and Q4_0 rows 144 bytes, both odd multiples of 16, so eight
 //     threads reading 16-byte chunks of eight consecutive rows hit eight
 //     different bank groups; f16 rows (64 K = 128 bytes per box) use the
-//     TMA's 128-byte swizzle for the same effect. The f16 A tile arrives the
+//     TMA's 128-byte swizzle for the same effect. The bf16 A tile arrives the
 //     same way in the swizzled K-major layout of the MMA's B operand;
 //  3. eight converter warps (thread = W row = TMEM lane) dequantise 64 K of
-//     their row at a time with half2 arithmetic (Q8_0: q*d, Q4_0: (q-8)*d,
-//     computed in f16 with W scaled by 2^8 to stay clear of f16 subnormals)
-//     and write the f16 operand into tensor memory with tcgen05.st;
-//  4. one thread issues tcgen05.mma kind::f16 with A (= W) from tensor
-//     memory and B (= tokens) from shared memory, accumulating f32 in TMEM;
-//  5. four warps read the accumulator (tcgen05.ld), multiply by s_m * 2^-8
-//     (f16 weights: s_m) and store C with coalesced stores.
+//     their row at a time: each weight is formed exactly in f32 (Q8_0: q*d,
+//     Q4_0: (q-8)*d, an 11-bit scale times a code of at most 8 bits; f16:
+//     widened) and rounded once to bf16, for any block scale, and written
+//     into tensor memory with tcgen05.st;
+//  4. one thread issues tcgen05.mma kind::f16 (bf16 x bf16) with A (= W) from
+//     tensor memory and B (= tokens) from shared memory, accumulating f32 in
+//     TMEM;
+//  5. four warps read the accumulator (tcgen05.ld) and store C with
+//     coalesced stores.
 // Every wait is bounded; on timeout the kernel records LQ_ERR_DEVICE_TIMEOUT,
 // lets its copies and MMAs finish, frees TMEM and returns.
 #include <cuda.h>
@@ -55,7 +56,6 @@ constexpr int kKS = 128;                           // K per pipeline stage (8 MM
 constexpr int kMaxStages = 4, kMaxRawStages = 8;
 constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
 constexpr uint32_t kWCol0 = 256;
-constexpr float kWScale = 256.0f;                  // Q formats: W is computed as 2^8 * w
 
 // Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
 // formats: 256 K in one box; f16: 128 K as two boxes of 64 K, each 128 rows
@@ -66,7 +66,6 @@ template <int FMT> constexpr int kRowBytes = FMT == LQ_FMT_F16 ? 256 : (FMT == L
 struct TmaGemmParams {
   float* C;
   const float* R;      // residual epilogue: added to every output
-  const float* scale;  // s_m per token (from the pre-pass)
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
   int split;           // CTAs of a cluster splitting K (1: no split)
@@ -94,89 +93,51 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 }
 
 // ---------------------------------------------------------------------------
-// Pre-pass: A f32 [M,K] -> f16 [M,K] scaled by 1/s_m, s_m = 2^(e-15) where
-// max|a_m| < 2^e (frexp), so max|a_m/s_m| lies in [2^14, 2^15). One CTA of
-// 128 threads per token row; rows of up to 4096 values stay in registers
-// between the two passes (longer rows are read twice).
+// Pre-pass: A f32 [M,K] -> bf16 [M,K], every value rounded to nearest even
+// (cvt.rn.bf16x2.f32). Elementwise: thread i converts elements 8i .. 8i+7
+// (K is a multiple of 128 on this route, so eight never straddle a row or a
+// block of 32). With perm (Q4_0 with interleaved nibbles) each block's
+// elements go to the slots of lq_q4i.cuh: element 2j to slot j, 2j+1 to
+// slot 16+j.
 // ---------------------------------------------------------------------------
-constexpr int kPreThreads = 128, kPreKeep = 8;  // float4 per thread kept in registers
+constexpr int kPreThreads = 256;
 
-// Elements 4 idx .. 4 idx + 3 of a row, scaled and rounded to f16. With perm
-// (Q4_0 with interleaved nibbles) they go to the slots of lq_q4i.cuh within
-// their block of 32: chunk i of block b puts (x, z) at halves 32b + 2i, 2i+1
-// and (y, w) at halves 32b + 16 + 2i, 17 + 2i.
-__device__ __forceinline__ void store_f16_chunk(__half2* out, int idx, float4 v, float inv, int perm) {
-  if (perm) {
-    const int b = idx >> 3, i = idx & 7;
-    out[16 * b + i] = __floats2half2_rn(v.x * inv, v.z * inv);
-    out[16 * b + 8 + i] = __floats2half2_rn(v.y * inv, v.w * inv);
-  } else {
-    out[2 * idx] = __floats2half2_rn(v.x * inv, v.y * inv);
-    out[2 * idx + 1] = __floats2half2_rn(v.z * inv, v.w * inv);
-  }
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
-__global__ void __launch_bounds__(kPreThreads) a_to_f16_kernel(const float* __restrict__ A,
-                                                               __half* __restrict__ A16,
-                                                               float* __restrict__ scale, int M, int K,
-                                                               int perm) {
+
+__global__ void __launch_bounds__(kPreThreads) a_to_bf16_kernel(const float* __restrict__ A,
+                                                                uint32_t* __restrict__ A16, long long n8,
+                                                                int perm) {
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float wmax[kPreThreads / 32];
-  const int m = blockIdx.x, t = threadIdx.x, K4 = K / 4;
-  const float4* a = reinterpret_cast<const float4*>(A + static_cast<long long>(m) * K);
-  __half2* out = reinterpret_cast<__half2*>(A16 + static_cast<long long>(m) * K);
-  float4 keep[kPreKeep];
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < kPreKeep; ++i) {
-    const int idx = t + kPreThreads * i;
-    keep[i] = idx < K4 ? __ldg(a + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(keep[i].x), fabsf(keep[i].y)), fmaxf(fabsf(keep[i].z), fabsf(keep[i].w))));
+  const long long stride = static_cast<long long>(gridDim.x) * kPreThreads;
+  for (long long i = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i < n8; i += stride) {
+    const float4 x = ldg128f(A + 8 * i), y = ldg128f(A + 8 * i + 4);
+    if (!perm) {
+      const uint4 o = make_uint4(bf16x2(x.x, x.y), bf16x2(x.z, x.w), bf16x2(y.x, y.y), bf16x2(y.z, y.w));
+      *reinterpret_cast<uint4*>(A16 + 4 * i) = o;
+    } else {
+      // chunk c of block b: even elements 8c, 8c+2, 8c+4, 8c+6 -> slots
+      // 4c .. 4c+3 (words 2c, 2c+1); odd ones -> slots 16+4c .. (words 8+2c, 9+2c)
+      uint32_t* blk = A16 + 16 * (i >> 2);
+      const int c = static_cast<int>(i & 3);
+      *reinterpret_cast<uint2*>(blk + 2 * c) = make_uint2(bf16x2(x.x, x.z), bf16x2(y.x, y.z));
+      *reinterpret_cast<uint2*>(blk + 8 + 2 * c) = make_uint2(bf16x2(x.y, x.w), bf16x2(y.y, y.w));
+    }
   }
-  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads) {
-    const float4 v = __ldg(a + idx);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 8));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  if ((t & 31) == 0) wmax[t >> 5] = amax;
-  __syncthreads();
-  amax = wmax[0];
-#pragma unroll
-  for (int w = 1; w < kPreThreads / 32; ++w) amax = fmaxf(amax, wmax[w]);
-  int e = 0;
-  float inv = 1.f, s = 1.f;
-  if (amax > 0.f && amax <= 3.4e38f) {
-    frexpf(amax, &e);
-    // below 2^-112, 2^(15 - e) would overflow f32: such rows are scaled by
-    // 2^126 instead (their largest value lands below 2^14, still finite)
-    e = max(e, -111);
-    s = ldexpf(1.f, e - 15);
-    inv = ldexpf(1.f, 15 - e);
-  }
-  // scale (exact) and round to f16
-#pragma unroll
-  for (int i = 0; i < kPreKeep; ++i) {
-    const int idx = t + kPreThreads * i;
-    if (idx < K4) store_f16_chunk(out, idx, keep[i], inv, perm);
-  }
-  for (int idx = t + kPreThreads * kPreKeep; idx < K4; idx += kPreThreads)
-    store_f16_chunk(out, idx, __ldg(a + idx), inv, perm);
-  if (t == 0) scale[m] = s;
-  (void)M;
 }
 
 // ---------------------------------------------------------------------------
 // Converters: 64 K of W row r (raw stage in shared memory at `stage`) ->
-// 32 words of packed f16 pairs (word j = elements 2j, 2j+1; low half = even
-// element).
+// 32 words of packed bf16 pairs (word j = elements 2j, 2j+1; low half = even
+// element). Each weight is formed exactly in f32 and rounded once: a code
+// byte goes into the low mantissa byte of 2^23 (one byte-permute), one
+// packed add takes the bias off exactly (q, or q - 8), and one packed
+// multiply by the f16 scale is exact too (11 x 8 significant bits); the
+// f16 weights widen exactly. cvt.rn.bf16x2.f32 then rounds to nearest even.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
-__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
-
 template <int FMT, int SUB>
 __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
   if constexpr (FMT == LQ_FMT_F16) {
@@ -185,10 +146,12 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint4 v = lds128(row + ((static_cast<uint32_t>(i) ^ (r & 7u)) << 4));
-      out[4 * i] = v.x;
-      out[4 * i + 1] = v.y;
-      out[4 * i + 2] = v.z;
-      out[4 * i + 3] = v.w;
+      const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
+        out[4 * i + j] = bf16x2(f.x, f.y);
+      }
     }
   } else if constexpr (FMT == LQ_FMT_Q8_0) {
     // two 34-byte blocks at byte 68*SUB of the row's 272 raw bytes
@@ -203,21 +166,20 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (
       w[4 * i + 2] = v.z;
       w[4 * i + 3] = v.w;
     }
-    const __half2 bias = __float2half2_rn(1152.0f);  // 1024 + 128
-    const __half2 d0 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off] & 0xFFFFu))),
-                               __float2half2_rn(kWScale));
-    const __half2 d1 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off + 8] >> 16))),
-                               __float2half2_rn(kWScale));
+    const float2 bias = make_float2(-kMagicS8, -kMagicS8);
+    const float d0 = f16_lo(w[off]), d1 = f16_lo(w[off + 8] >> 16);
+    const float2 dd0 = make_float2(d0, d0), dd1 = make_float2(d1, d1);
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
       // block 0: bytes 2+2p, 3+2p; block 1: bytes 36+2p, 37+2p
       const int b0 = 2 + 2 * p, b1 = 36 + 2 * p;
-      const uint32_t x0 = w[off + (b0 >> 2)] ^ 0x80808080u;
+      const uint32_t x0 = w[off + (b0 >> 2)] ^ 0x80808080u;  // sign bits flipped: byte = q + 128
       const uint32_t x1 = w[off + (b1 >> 2)] ^ 0x80808080u;
-      const uint32_t v0 = __byte_perm(x0, 0x64646464u, (b0 & 2) ? 0x4342u : 0x4140u);
-      const uint32_t v1 = __byte_perm(x1, 0x64646464u, (b1 & 2) ? 0x4342u : 0x4140u);
-      out[p] = h2_bits(__hmul2(__hsub2(bits_h2(v0), bias), d0));
-      out[16 + p] = h2_bits(__hmul2(__hsub2(bits_h2(v1), bias), d1));
+      const float2 q0 = fadd2(make_float2(s8_to_magic(x0, b0 & 3), s8_to_magic(x0, (b0 & 3) + 1)), bias);
+      const float2 q1 = fadd2(make_float2(s8_to_magic(x1, b1 & 3), s8_to_magic(x1, (b1 & 3) + 1)), bias);
+      const float2 v0 = fmul2(q0, dd0), v1 = fmul2(q1, dd1);
+      out[p] = bf16x2(v0.x, v0.y);
+      out[16 + p] = bf16x2(v1.x, v1.y);
     }
   } else {
     // two 18-byte blocks at byte 36*SUB of the row's 144 raw bytes
@@ -232,26 +194,26 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (
       w[4 * i + 2] = v.z;
       w[4 * i + 3] = v.w;
     }
-    const __half2 bias = __float2half2_rn(1032.0f);  // 1024 + 8
-    const __half2 d0 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off] & 0xFFFFu))),
-                               __float2half2_rn(kWScale));
-    const __half2 d1 = __hmul2(__half2half2(__ushort_as_half(static_cast<unsigned short>(w[off + 4] >> 16))),
-                               __float2half2_rn(kWScale));
+    const float2 bias = make_float2(-kMagicQ4, -kMagicQ4);
+    const float d0 = f16_lo(w[off]), d1 = f16_lo(w[off + 4] >> 16);
+    const float2 dd0 = make_float2(d0, d0), dd1 = make_float2(d1, d1);
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
       // bytes j = 2+2p, 3+2p of block 0 (and 20+2p.. of block 1) hold
       // q_{2p}, q_{2p+1} (low nibbles) and q_{16+2p}, q_{17+2p} (high)
       const int b0 = 2 + 2 * p, b1 = 20 + 2 * p;
       const uint32_t x0 = w[off + (b0 >> 2)], x1 = w[off + (b1 >> 2)];
-      const uint32_t s0sel = (b0 & 2) ? 0x4342u : 0x4140u, s1sel = (b1 & 2) ? 0x4342u : 0x4140u;
-      const uint32_t lo0 = __byte_perm(x0 & 0x0F0F0F0Fu, 0x64646464u, s0sel);
-      const uint32_t hi0 = __byte_perm((x0 >> 4) & 0x0F0F0F0Fu, 0x64646464u, s0sel);
-      const uint32_t lo1 = __byte_perm(x1 & 0x0F0F0F0Fu, 0x64646464u, s1sel);
-      const uint32_t hi1 = __byte_perm((x1 >> 4) & 0x0F0F0F0Fu, 0x64646464u, s1sel);
-      out[p] = h2_bits(__hmul2(__hsub2(bits_h2(lo0), bias), d0));
-      out[8 + p] = h2_bits(__hmul2(__hsub2(bits_h2(hi0), bias), d0));
-      out[16 + p] = h2_bits(__hmul2(__hsub2(bits_h2(lo1), bias), d1));
-      out[24 + p] = h2_bits(__hmul2(__hsub2(bits_h2(hi1), bias), d1));
+      const uint32_t lo0 = x0 & 0x0F0F0F0Fu, hi0 = (x0 >> 4) & 0x0F0F0F0Fu;
+      const uint32_t lo1 = x1 & 0x0F0F0F0Fu, hi1 = (x1 >> 4) & 0x0F0F0F0Fu;
+      const int i0 = b0 & 3, i1 = b1 & 3;
+      const float2 l0 = fmul2(fadd2(make_float2(s8_to_magic(lo0, i0), s8_to_magic(lo0, i0 + 1)), bias), dd0);
+      const float2 h0 = fmul2(fadd2(make_float2(s8_to_magic(hi0, i0), s8_to_magic(hi0, i0 + 1)), bias), dd0);
+      const float2 l1 = fmul2(fadd2(make_float2(s8_to_magic(lo1, i1), s8_to_magic(lo1, i1 + 1)), bias), dd1);
+      const float2 h1 = fmul2(fadd2(make_float2(s8_to_magic(hi1, i1), s8_to_magic(hi1, i1 + 1)), bias), dd1);
+      out[p] = bf16x2(l0.x, l0.y);
+      out[8 + p] = bf16x2(h0.x, h0.y);
+      out[16 + p] = bf16x2(l1.x, l1.y);
+      out[24 + p] = bf16x2(h1.x, h1.y);
     }
   }
 }
@@ -272,11 +234,6 @@ __device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t 
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
@@ -286,13 +243,12 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer)
 }
 
 // Epilogue of one TMEM lane (W row r of the tile): the accumulator columns
-// of 32-column chunks c0, c0 + dc, ..., plus the partial tiles of peers
+// of 32-column chunks c0, c0 + 2, ..., plus the partial tiles of peers
 // 1 .. split-1 (token-major f32 at `red` in their shared memory) when
-// split > 1, scaled by s_m (and 2^-8 for the quantised formats) and stored
-// to C[m0 + j, n0 + r].
+// split > 1, stored to C[m0 + j, n0 + r].
 template <int FMT, int EPI>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
-                                           int bt, uint32_t red, int split, int c0, const float (&scp)[4]) {
+                                           int bt, uint32_t red, int split, int c0) {
   const int n = n0 + r;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -300,7 +256,6 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
     if (c >= (bt + 31) / 32) break;
     uint32_t v[32];
     tc::ld_32x32b_x32(tcol + 32u * c, v);
-    const float sc = scp[i];  // lane j: the scale of token m0 + 32c + j
     tc::wait_ld();
 #pragma unroll 1
     for (int q = 1; q < split; ++q) {
@@ -327,13 +282,12 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const int m = m0 + 32 * c + jj;
-      const float f = __shfl_sync(0xffffffffu, sc, jj);
       if (n < p.N && 32 * c + jj < bt && m < p.M) {
         const long long o = static_cast<long long>(m) * p.N + n;
         if constexpr (EPI == epi::kResidual)
-          p.C[o] = __uint_as_float(v[jj]) * f + rv[jj];
+          p.C[o] = __uint_as_float(v[jj]) + rv[jj];
         else
-          p.C[o] = __uint_as_float(v[jj]) * f;
+          p.C[o] = __uint_as_float(v[jj]);
       }
     }
   }
@@ -391,7 +345,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int jr0 = rank * nraw_all / split;
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
   bool epi = false;  // this CTA's accumulator is complete and may be used
-  float scp[4] = {0.f, 0.f, 0.f, 0.f};  // epilogue: scales of chunks g, g + 2, g + 4, g + 6
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < RR; ++i) {
@@ -487,7 +440,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_f16_f32(kBN, static_cast<uint32_t>(bt));
+    const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
     int st = 0, lap = 0;
     auto issue_stage = [&](int ks, int sst) {
@@ -570,18 +523,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     {
       // ---------------- epilogue (both groups: 32-column chunks g, g + 2, ...) ----------------
-      // The token scales of this group's chunks, fetched while the last MMAs
-      // run (they come from the pre-pass, complete once griddepcontrol.wait
-      // returns; by now it returns at once).
+      // C (and R) are touched only once the previous kernel on the stream
+      // has completed (by now griddepcontrol.wait returns at once)
       pdl_wait();
-      {
-        const float wunscale = FMT == LQ_FMT_F16 ? 1.0f : 1.0f / kWScale;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = g + 2 * i, ml = m0 + 32 * c + lane;
-          scp[i] = (32 * c + lane < bt && ml < p.M) ? __ldg(p.scale + ml) * wunscale : 0.f;
-        }
-      }
       const bool have = warp_wait(&b.tmem_full, 0, p);
       tc::fence_after_sync();
       if (!have && lane == 0) {
@@ -590,7 +534,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       epi = have && !b.abort;
       if constexpr (SWIGLU) {
-        // gate (lanes 0-63) and up (lanes 64-127) accumulators, scaled,
+        // gate (lanes 0-63) and up (lanes 64-127) accumulators
         // -> the A ring as [token][gate 64 | up 64]; then all eight warps
         // combine (token, output) pairs in one rolled loop and store 64
         // consecutive outputs of a token together
@@ -602,13 +546,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (c >= (bt + 31) / 32) break;
             uint32_t v[32];
             tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
-            const float sc = scp[i];
             tc::wait_ld();
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const float f = __shfl_sync(0xffffffffu, sc, jj);
-              if (32 * c + jj < bt) xch[(32 * c + jj) * 128 + r] = __uint_as_float(v[jj]) * f;
-            }
+            for (int jj = 0; jj < 32; ++jj)
+              if (32 * c + jj < bt) xch[(32 * c + jj) * 128 + r] = __uint_as_float(v[jj]);
           }
         }
         named_barrier(3, 8u * 32u);  // the eight epilogue warps, whatever their outcome
@@ -623,7 +564,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           }
         }
       } else if (epi && split == 1) {
-        store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g, scp);
+        store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g);
       } else if (epi && rank != 0) {
         // this rank's partial tile -> its own shared memory (the A ring is
         // idle now), token-major so that the 32 lanes write 32 rows in a row
@@ -651,7 +592,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       tc::fence_after_sync();
       const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
       store_tile<FMT, EPI>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
-                           split, g, scp);
+                           split, g);
     }
     cluster_sync();  // the peers keep their shared memory until the leader read it
   }
@@ -919,41 +860,48 @@ cudaMemPool_t workspace_pool() {
   return pools[dev];
 }
 
-// The operands of the tensor-core kernel (f16 copy of A and its per-token
-// scales) live in a stream-ordered workspace from the library's pool for the
-// duration of the call.
+// The B operand of the tensor-core kernel (the bf16 copy of A) lives in a
+// stream-ordered workspace from the library's pool for the duration of the
+// call.
 lq_status launch_gemm_tma(const MatmulArgs& a) {
   // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
   const int bt = pick_bt(a.M, a.epi == epi::kSwiglu ? 2 * a.N : a.N);
-  const size_t a16_bytes = static_cast<size_t>(a.M) * a.K * 2;
-  const size_t ws_bytes = (a16_bytes + 255) / 256 * 256 + static_cast<size_t>(a.M) * 4;
+  const size_t ws_bytes = gemm_tma_workspace_bytes(a.M, a.K);
   void* ws = nullptr;
   cudaMemPool_t pool = workspace_pool();
   if (!pool) return LQ_ERR_CUDA;
   cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
   if (e != cudaSuccess) return LQ_ERR_CUDA;
-  __half* A16 = static_cast<__half*>(ws);
-  float* scale = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + (a16_bytes + 255) / 256 * 256);
-  lq_status st = launch_gemm_tma_ws(a, A16, scale, bt);
+  lq_status st = launch_gemm_tma_ws(a, ws, bt);
   cudaError_t ef = cudaFreeAsync(ws, a.stream);
   if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
   if (st == LQ_OK) count_route(2);
   return st;
 }
 
-// Pre-pass + GEMM given a workspace of M*K halves (A16) and M floats (scale).
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt) {
+size_t gemm_tma_workspace_bytes(int64_t M, int64_t K) {
+  return (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
+}
+
+// Pre-pass + GEMM given a workspace of M*K bf16 values (a16, 16-byte aligned).
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
-  // 1. A -> f16 with per-token power-of-two scales
-  cudaError_t e = launch_pdl(a_to_f16_kernel, dim3(static_cast<unsigned>(M)), dim3(kPreThreads), 0, a.stream, a.A,
-                             static_cast<__half*>(a16), scale, M, K, a.a_perm ? 1 : 0);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return LQ_ERR_CUDA;
+  // 1. A -> bf16 (round to nearest even)
+  {
+    const long long n8 = static_cast<long long>(M) * K / 8;
+    const long long want = (n8 + kPreThreads - 1) / kPreThreads;
+    const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1)) * 8;
+    const unsigned grid = static_cast<unsigned>(std::max<long long>(1, std::min(want, cap)));
+    cudaError_t e = launch_pdl(a_to_bf16_kernel, dim3(grid), dim3(kPreThreads), 0, a.stream, a.A,
+                               static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return LQ_ERR_CUDA;
+  }
 
   // 2. tensor maps. Q formats: raw W as [N][row_bytes/4] 32-bit words, one
   //    box = the bytes of 256 K (68 or 36 words) x 128 rows. f16: W as
-  //    [N][K] halves, boxes of 64 x 128 with the 128-byte swizzle. A16 as
-  //    [M][K] halves, boxes of 64 x bt with the 128-byte swizzle.
+  //    [N][K] halves, boxes of 64 x 128 with the 128-byte swizzle. The bf16
+  //    A as [M][K], boxes of 64 x bt with the 128-byte swizzle.
   EncodeTiled enc = encode_fn();
   if (!enc) return LQ_ERR_UNSUPPORTED;
   const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
@@ -980,7 +928,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bt)};
     cuuint32_t es[2] = {1, 1};
-    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, a16, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a16, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return LQ_ERR_UNSUPPORTED;
@@ -988,7 +936,6 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int b
   TmaGemmParams p;
   p.C = a.C;
   p.R = a.R;
-  p.scale = scale;
   p.M = M;
   p.N = N;
   p.K = K;

@@ -65,8 +65,10 @@ lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via 
 bool gemm_tc_eligible(const MatmulArgs& a);
 // tcgen05 with TMA loads and W in tensor memory; allocates its workspace
 lq_status launch_gemm_tma(const MatmulArgs& a);
-// the same given a workspace: M*K halves at a16 (16-byte aligned), M floats at scale
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, float* scale, int bt);
+// the same given a workspace of gemm_tma_workspace_bytes(M, K) bytes (the bf16
+// copy of A, 16-byte aligned)
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt);
+size_t gemm_tma_workspace_bytes(int64_t M, int64_t K);
 bool gemm_tma_eligible(const MatmulArgs& a);
 int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.

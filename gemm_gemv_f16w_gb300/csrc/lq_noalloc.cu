@@ -1,8 +1,8 @@
 // lq_gemm_noalloc: the tensor-core GEMM for callers that must not allocate
 // device memory.
 //
-// The regular tensor-core GEMM takes a short-lived workspace (an f16 copy of
-// A and one scale per token) from a stream-ordered memory pool on every call.
+// The regular tensor-core GEMM takes a short-lived workspace (a bf16 copy of
+// A) from a stream-ordered memory pool on every call.
 // Some callers cannot allow that: runtimes that own all device memory
 // themselves and give the library none, services whose memory budget is fixed
 // at start-up, and hard real-time paths where an allocation (and the pool
@@ -18,8 +18,8 @@
 namespace lq {
 namespace {
 
-// 8 MiB: enough for M*K*2 bytes of f16 activations plus M floats of scales
-// when M*K is at most about 4 million (e.g. 512 x 8192 or 2048 x 2048).
+// 8 MiB: enough for the M*K*2 bytes of bf16 activations when M*K is at most
+// 4 Mi elements (e.g. 512 x 8192 or 2048 x 2048).
 constexpr size_t kNoAllocBytes = 8u << 20;
 static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
 
@@ -59,14 +59,12 @@ extern "C" lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, flo
   // Only the tensor-core kernel that needs the workspace is offered here.
   if (!gemm_tma_eligible(a)) return LQ_ERR_UNSUPPORTED;
   // Beyond the fixed workspace: a clear refusal, never a larger allocation.
-  const size_t a16 = (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
-  if (a16 + static_cast<size_t>(M) * 4 > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
+  if (gemm_tma_workspace_bytes(M, K) > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
   const lq_status st = workspace_address(&ws);
   if (st != LQ_OK) return st;
-  // Every byte the kernels read from the workspace is written earlier in the
-  // same call (the f16 rows and scales of the M tokens), so nothing needs
-  // clearing between calls.
-  auto* base = static_cast<unsigned char*>(ws);
-  return launch_gemm_tma_ws(a, base, reinterpret_cast<float*>(base + a16), pick_gemm_bt(M, N));
+  // Every byte the kernels read from the workspace (the bf16 rows of the M
+  // tokens) is written earlier in the same call, so nothing needs clearing
+  // between calls.
+  return launch_gemm_tma_ws(a, ws, pick_gemm_bt(M, N));
 }

@@ -41,6 +41,13 @@
  *     read and cleared by lq_last_device_error().
  *   - Sub-matrices (e.g. the gate or up half of a fused weight) are addressed
  *     by pointer offsets; a W row offset is always block-aligned.
+ *   - Memory: the library allocates nothing per call and holds no workspace,
+ *     with one exception: the tensor-core route of the GEMM entry points
+ *     (lq_gemm_<fmt>, lq_matmul_<fmt> and the epilogue fusions for M > 4)
+ *     takes an M*K*2-byte stream-ordered buffer from a memory pool the
+ *     library owns (described at lq_gemm_f16); lq_gemm_noalloc runs the
+ *     same kernels on a fixed array instead. Caller-provided scratch
+ *     (lq_topk_f32's work) is named in the call.
  *   - Kernels launched on a stream may begin streaming W before the previous
  *     kernel on that stream has finished (programmatic dependent launch); A
  *     and C are touched only after it has. Do not write W on the same stream
@@ -88,16 +95,20 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
  * Counterparts: gemm_q8 / gemm_q4 / gemm_q4_tiled (metal_qwen35.rs),
  * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). Small M streams W on the
  * CUDA cores in f32 (GEMV accuracy); larger M runs on the tensor cores
- * (tcgen05, TMEM accumulators): each token row of A scaled by an exact power
- * of two and rounded to f16 (11 significant bits, at least bf16's precision),
- * W dequantised to f16, products accumulated in f32; shapes that kernel does
- * not take use a tcgen05 kernel with bf16 operands. Tolerance: 5e-3 times
- * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16.
- * Limit: for Q8_0 and Q4_0 the tensor-core route forms 2^8 * w in f16 (to
- * keep small weights clear of f16 subnormals), so dequantised weights must
- * stay below 256 in magnitude there; larger ones overflow to inf. The CUDA-
- * core routes (M = 1, and M = 2..4 where the batched kernel applies) have no
- * such limit. */
+ * (tcgen05, TMEM accumulators) with bf16 operands: A rounded to bf16 (round
+ * to nearest even, over f32's whole range), each weight formed exactly in
+ * f32 and rounded once to bf16 (any finite block scale), products
+ * accumulated in f32. Tolerance: 5e-3 times sum_k |a_k w_k| plus 1e-5,
+ * against A rounded to bf16 (the weights' rounding contributes at most
+ * 2^-8 of the sum).
+ * Workspace: the tensor-core route converts A once per call into a
+ * stream-ordered buffer of M*K*2 bytes taken from the library's own memory
+ * pool (cudaMallocFromPoolAsync; the pool keeps freed blocks, so repeated
+ * calls and CUDA-graph replays reuse the same memory without a driver
+ * call). This departs from "the library allocates nothing": every one of
+ * the N/128 tiles reads its token tile from that one copy, where converting
+ * f32 A inside the GEMM would double the bytes each SM pulls for its token
+ * tiles. Callers that may not allocate use lq_gemm_noalloc. */
 lq_status lq_gemm_f16 (const float* A, const void* W, float* C,
                        int64_t M, int64_t N, int64_t K, void* stream);
 lq_status lq_gemm_q8_0(const float* A, const void* W, float* C,
@@ -186,8 +197,8 @@ lq_status lq_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, voi
  * their memory budget at start-up, real-time paths where an allocation is a
  * stall or a failure point they cannot accept. Its
  * workspace is a fixed 8 MiB array inside this library, held on every GPU
- * that loads the library until the process exits; it needs
- * round_up(M*K*2, 256) + 4*M bytes, so M*K up to about 4 million elements.
+ * that loads the library until the process exits; it holds the bf16 copy
+ * of A, round_up(M*K*2, 256) bytes, so M*K up to 4 Mi elements.
  *   - LQ_ERR_UNSUPPORTED: larger than the fixed workspace, or a shape or
  *     alignment the tensor-core kernel does not take (K % 256 for Q8_0/Q4_0,
  *     K % 128 for f16, A and W 16-byte aligned, M >= 2). Nothing runs.

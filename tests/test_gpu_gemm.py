@@ -130,21 +130,56 @@ def test_gemm_row_equals_gemv(lq, cuda_dev):
         assert np.all(np.abs(g.cpu().numpy()[0] - C[m]) <= tol[m])
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0"])
-def test_tiny_activation_rows_stay_finite(lq, cuda_dev, fmt):
-    """Token rows whose largest value is below 2^-112 (f32 subnormals
-    included) are scaled by 2^126 in the f16 pre-pass instead of 2^(15 - e),
-    which would overflow f32; their outputs stay finite and within the
-    tolerance."""
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
+def test_tc_wide_range_token_rows(lq, cuda_dev, fmt):
+    """Token rows far wider than f16's range, against the tolerance defined on
+    A rounded to bf16: [1e6, 1e-4, 1e-4, ...] with w_0 = 0 and the other
+    weights of one sign (every small term errs the same way if it is
+    represented coarsely), rows near f32's largest and smallest values (f32
+    subnormals included), an all-zero row, and a row mixing 1e30 with 1e-30."""
     M, N, K = 64, 256, 512
     W, A = synthetic.draw(M, N, K, seed=12)
-    A = A.clone()
+    W, A = W.clone(), A.clone()
+    W[:, 0] = 0.0
+    W[:8, 1:] = 0.05 + 0.05 * torch.rand(8, K - 1, generator=torch.Generator().manual_seed(3))
+    A[0] = 1e-4
+    A[0, 0] = 1e6
+    A[1] = -1e-4
+    A[1, 0] = -3e7
     A[3] *= 1e-36
     A[7] = A[7] * 1e-38 * 1e-3   # f32 subnormals
     A[11] = 0.0
+    A[13] *= 1e30
+    A[17, ::2] *= 1e30
+    A[17, 1::2] *= 1e-30
     lq.reset_counts()
     C = _run(lq, cuda_dev, fmt, W, A)
     assert lq.route_count(2) == 1
-    assert np.all(np.isfinite(C))
     y, tol = _ref(fmt, W, A)
-    check(C, y, tol, f"{fmt} tiny rows")
+    check(C, y, tol, f"{fmt} wide rows")
+
+
+@pytest.mark.parametrize("fmt,d", [("q8_0", 4.0), ("q8_0", 300.0), ("q8_0", 60000.0),
+                                   ("q4_0", 40.0), ("q4_0", 4000.0), ("q4_0", 60000.0),
+                                   ("q4_0i", 40.0), ("f16", 60000.0 / 127)])
+def test_tc_large_block_scales(lq, cuda_dev, fmt, d):
+    """Blocks whose f16 scale d is large (Q8_0 weights up to 127 d, Q4_0 up to
+    8 d; f16 weights near f16's largest value): the dequantised weights are
+    formed exactly and rounded to bf16, so any finite block scale stays within
+    the tolerance. Here a tenth of the blocks, spread over the tiles, carry
+    the large scale; the rest are the workloads' N(0, 0.02)."""
+    M, N, K = 48, 384, 1024
+    W, A = synthetic.draw(M, N, K, seed=21)
+    W = W.clone()
+    g = torch.Generator().manual_seed(5)
+    nb = N * K // 32
+    pick = torch.randperm(nb, generator=g)[: nb // 10]
+    Wb = W.view(nb, 32)
+    amax = Wb[pick].abs().amax(dim=1, keepdim=True)
+    peak = 127.0 * d if fmt in ("q8_0", "f16") else 8.0 * d
+    Wb[pick] = Wb[pick] / amax * peak
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    assert lq.route_count(2) == 1
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} d={d}")
