@@ -20,9 +20,10 @@ import os
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "liblq.so")
+# LQ_LIBRARY=debug loads the bounds-checking build (liblq_debug.so, see build.py)
+LIB_PATH = os.path.join(_PKG, "liblq_debug.so" if os.environ.get("LQ_LIBRARY") == "debug" else "liblq.so")
 
-LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_CUDA, LQ_ERR_DEVICE_TIMEOUT = range(5)
+LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_CUDA, LQ_ERR_DEVICE_TIMEOUT, LQ_ERR_BOUNDS = range(6)
 FMT = {"f16": 0, "q8_0": 1, "q4_0": 2, "q4_0i": 3}  # q4_0i: the pages' interleaved nibbles
 ROUTE_AUTO, ROUTE_STREAM, ROUTE_TENSOR_CORE, ROUTE_GENERIC = range(4)
 

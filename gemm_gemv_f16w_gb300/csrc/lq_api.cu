@@ -138,9 +138,9 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
     case 3: return launch_gemv_generic(a);
     default: break;
   }
-  // M = 2..4: one pass over W on the CUDA cores beats the tensor-core
+  // M = 2..8: one pass over W on the CUDA cores beats the tensor-core
   // kernel's fixed latencies
-  if (M <= 4) {
+  if (M <= 8) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }
@@ -173,7 +173,7 @@ lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, fl
     default: break;
   }
   if (M == 1) return launch_gemv(a);  // falls back to the generic kernel itself
-  if (M <= 4) {
+  if (M <= 8) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }
@@ -239,6 +239,7 @@ const char* lq_status_string(lq_status s) {
     case LQ_ERR_UNSUPPORTED: return "LQ_ERR_UNSUPPORTED: no kernel for this request";
     case LQ_ERR_CUDA: return "LQ_ERR_CUDA: a CUDA call or launch failed";
     case LQ_ERR_DEVICE_TIMEOUT: return "LQ_ERR_DEVICE_TIMEOUT: a bounded device wait ran out";
+    case LQ_ERR_BOUNDS: return "LQ_ERR_BOUNDS: an index check of the debug build failed (access skipped)";
   }
   return "unknown lq_status";
 }
@@ -332,7 +333,11 @@ lq_status lq_gemv_topk(int fmt, const float* A, const void* W, float* C, int64_t
   return launch_topk_f32(C, N, k, values, indices, work, static_cast<cudaStream_t>(stream));
 }
 
-const char* lq_version(void) { return "lq 0.1.0 (sm_103a)"; }
+#ifdef LQ_DEBUG_BOUNDS
+const char* lq_version(void) { return "lq 0.2.0 (sm_103a, debug bounds checks)"; }
+#else
+const char* lq_version(void) { return "lq 0.2.0 (sm_103a)"; }
+#endif
 
 lq_status lq_debug_force_route(int route) {
   if (route < 0 || route > 3) return LQ_ERR_INVALID_ARG;

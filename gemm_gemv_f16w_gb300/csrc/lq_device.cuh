@@ -10,6 +10,23 @@ namespace lq {
 
 // Device status codes (mirror lq_status).
 constexpr unsigned kDevErrTimeout = 4u;
+constexpr unsigned kDevErrBounds = 5u;
+
+// ---- debug bounds checks ----------------------------------------------------
+// Built with -DLQ_DEBUG_BOUNDS (liblq_debug.so), each global index a kernel
+// computes for a plain load or store, and each byte range of a bulk copy of
+// W rows, is checked against its extent first: a failed check records
+// kDevErrBounds in the translation unit's status word (lq_last_device_error
+// reports LQ_ERR_BOUNDS) and the access is skipped, so nothing faults or
+// traps (a skipped copy leaves its waiters to their time limits). Release
+// builds compile the checks away. A translation unit that uses LQ_IN_BOUNDS
+// defines record_error(unsigned) first. Tensor-map copies need no check:
+// the TMA unit clips them to the tensor's extents.
+#ifdef LQ_DEBUG_BOUNDS
+#define LQ_IN_BOUNDS(cond) ((cond) ? true : (record_error(::lq::kDevErrBounds), false))
+#else
+#define LQ_IN_BOUNDS(cond) true
+#endif
 
 // Limit for draining copies that are still in flight when a kernel gives up
 // (not affected by the debugging override of the normal wait limit).

@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const TcParams p
       const uint32_t wtile = base_u + s * kStageBytes;
       const uint32_t ttile = wtile + kWTileBytes;
       float v[64];
-      if (n < p.N) {
+      if (n < p.N && LQ_IN_BOUNDS(kBK * ks + kBK <= p.K)) {
         load_w64<FMT>(wrow, ks, v);
       } else {
 #pragma unroll
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const TcParams p
         const int r = t + 128 * rr;
         if (r < BT) {
           const int m = m0 + r;
-          if (m < p.M) {
+          if (m < p.M && LQ_IN_BOUNDS(kBK * ks + kBK <= p.K)) {
             const float4* src = reinterpret_cast<const float4*>(p.A + static_cast<long long>(m) * p.K + kBK * ks);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const TcParams p
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int m = m0 + 32 * c + j;
-            if (32 * c + j < BT && m < p.M)
+            if (32 * c + j < BT && m < p.M && LQ_IN_BOUNDS(m >= 0 && nrow >= 0))
               p.C[static_cast<long long>(m) * p.N + nrow] = __uint_as_float(r[j]);
           }
         }

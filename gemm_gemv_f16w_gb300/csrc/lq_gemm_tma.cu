@@ -276,13 +276,15 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int m = m0 + 32 * c + jj;
-        rv[jj] = (n < p.N && 32 * c + jj < bt && m < p.M) ? p.R[static_cast<long long>(m) * p.N + n] : 0.f;
+        rv[jj] = (n < p.N && 32 * c + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0))
+                     ? p.R[static_cast<long long>(m) * p.N + n]
+                     : 0.f;
       }
     }
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       const int m = m0 + 32 * c + jj;
-      if (n < p.N && 32 * c + jj < bt && m < p.M) {
+      if (n < p.N && 32 * c + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0)) {
         const long long o = static_cast<long long>(m) * p.N + n;
         if constexpr (EPI == epi::kResidual)
           p.C[o] = __uint_as_float(v[jj]) + rv[jj];
@@ -559,7 +561,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll 1
           for (int idx = t0; idx < rows * 64; idx += 256) {
             const int tok = idx >> 6, j = idx & 63, n = n0 + j;
-            if (n < p.N)
+            if (n < p.N && LQ_IN_BOUNDS(m0 + tok < p.M && m0 + tok >= 0))
               p.C[static_cast<long long>(m0 + tok) * p.N + n] = epi::swiglu(xch[tok * 128 + j], xch[tok * 128 + 64 + j]);
           }
         }

@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
     const uint8_t* wbase = p.W + static_cast<long long>(r0) * p.row_bytes;
     auto issue = [&](int st, int s) {  // stage st into slot s
       const int rows = min(RS, nrows - st * RS);
+      if (!LQ_IN_BOUNDS(st >= 0 && rows > 0 && r0 + st * RS + rows <= p.N)) return;
       const uint32_t bytes = static_cast<uint32_t>(rows) * p.row_bytes;
       uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
       const uint8_t* src = wbase + static_cast<long long>(st) * RS * p.row_bytes;
@@ -288,13 +289,13 @@ __global__ void __launch_bounds__(kGemvThreads, CPW <= 2 ? 2 : 1)
       // (residual: R is fetched while the other K-groups finish)
       float rres = 0.f;
       if constexpr (EPI == epi::kResidual)
-        if (lane < rows) rres = p.R[r0 + st * RS + lane];
+        if (lane < rows && LQ_IN_BOUNDS(r0 + st * RS + lane < p.N)) rres = p.R[r0 + st * RS + lane];
       if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
         record_error(kDevErrTimeout);
         hd.abort = 1;
         return;
       }
-      if (lane < rows) {
+      if (lane < rows && LQ_IN_BOUNDS(r0 + st * RS + lane < p.N)) {
         float sum = 0.f;
         for (int g = 0; g < nk; ++g) sum += hd.red[s][lane][g];
         const int row = r0 + st * RS + lane;
@@ -382,6 +383,7 @@ __global__ void __launch_bounds__(256) generic_matmul_kernel(const float* __rest
   for (int m = blockIdx.y; m < M; m += gridDim.y) {
     const float* a = A + static_cast<long long>(m) * K;
     const long long o = static_cast<long long>(m) * N + n;
+    if (!LQ_IN_BOUNDS(o < static_cast<long long>(M) * N)) break;
     const float acc = generic_row_dot<FMT>(a, w, K, lane, il != 0);
     if constexpr (EPI == epi::kSwiglu) {
       const float up = generic_row_dot<FMT>(a, w + static_cast<long long>(N) * row_bytes, K, lane, il != 0);

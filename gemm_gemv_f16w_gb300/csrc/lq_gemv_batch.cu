@@ -1,4 +1,4 @@
-// Batched decode: C[m, n] = sum_k A[m, k] * w(n, k) for M = 2..4 rows of A
+// Batched decode: C[m, n] = sum_k A[m, k] * w(n, k) for M = 2..8 rows of A
 // (several sequences decoded together; route 1, the CUDA-core streaming
 // GEMM). The pages' counterpart is the NR x NM multi-row GEMV pattern of
 // gemm_q4 / gemm_q8 (lattice-inference 0.1.2, src/forward/metal_qwen35.rs),
@@ -16,7 +16,8 @@
 //    slots, whose weight stages are issued once A has been spread out;
 //  * the warps form the K-groups x row-groups grid of the GEMV, a row-group
 //    taking whole stages (ring depth a multiple of the row-group count);
-//    every lane holds its chunk of all M activation rows;
+//    every lane holds its chunk of all M activation rows (five to eight
+//    rows: half a quantised block per lane, lq_gemv_slices_batch.cuh);
 //  * per stage each warp reduces its row partials per token with the
 //    transposed shuffle tree; the stage's finisher adds the K-groups in a
 //    fixed order and writes the M outputs of each row.
@@ -41,13 +42,15 @@ __device__ unsigned g_batch_err;
 constexpr int kBKGroups = 8;   // K-groups at most (reduction buffer width)
 constexpr int kBRows = 8;      // rows per stage at most
 constexpr int kBMaxStages = 16;
-constexpr int kBMaxTokens = 4;
+constexpr int kBMaxTokens = 8;
 
-// Warps per CTA, all of them consumers. The f16 slices and the two-token
-// quantised slices fit in 128 registers, so 16 warps; the quantised
-// four-token slices need up to 255, so 8 (two per SM sub-partition).
+// Warps per CTA, all of them consumers. The f16 slices up to four tokens and
+// the two-token quantised slices fit in 128 registers, so 16 warps; the
+// quantised four-token slices and every eight-token slice (with eight
+// tokens' partial sums of a stage) need up to 255, so 8 (two per SM
+// sub-partition).
 __host__ __device__ constexpr int batch_warps(int fmt, int mt) {
-  return fmt == LQ_FMT_F16 || mt == 2 ? 16 : 8;
+  return mt > 4 ? 8 : (fmt == LQ_FMT_F16 || mt == 2 ? 16 : 8);
 }
 
 struct BatchParams {
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
     wbase = p.W + static_cast<long long>(a) * p.row_bytes;
   };
   auto issue = [&](int st, int s, uint64_t pol) {  // stage st into slot s
+    if (!LQ_IN_BOUNDS(st >= 0 && r0 + st * RS + min(RS, nrows - st * RS) <= p.N)) return;
     const uint32_t bytes = static_cast<uint32_t>(min(RS, nrows - st * RS)) * p.row_bytes;
     uint8_t* dst = ring + static_cast<size_t>(s) * stage_bytes;
     const uint8_t* src = wbase + static_cast<long long>(st) * RS * p.row_bytes;
@@ -249,7 +253,8 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
           float rres[MT];
 #pragma unroll
           for (int t = 0; t < MT; ++t)
-            rres[t] = EPI == epi::kResidual && lane < rows && t < p.M
+            rres[t] = EPI == epi::kResidual && lane < rows && t < p.M &&
+                              LQ_IN_BOUNDS(r0 + st * RS + lane < p.N)
                           ? p.R[static_cast<long long>(t) * p.N + r0 + st * RS + lane]
                           : 0.f;
           if (!mbar_wait(&hd.red_full[s], ph, p.wait_ns, p.wait_iters) || hd.abort) {
@@ -257,7 +262,8 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
             hd.abort = 1;
             break;
           }
-          if (SWIGLU && lane < rows) {
+          const bool row_ok = lane < rows && LQ_IN_BOUNDS(r0 + st * RS + lane < p.N);
+          if (SWIGLU && row_ok) {
             // one token at a time: a copy of silu per token would bloat the loop
 #pragma unroll 1
             for (int t = 0; t < p.M; ++t) {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
               }
               p.C[static_cast<long long>(t) * p.N + r0 + st * RS + lane] = epi::swiglu(sum, up);
             }
-          } else if (lane < rows) {
+          } else if (row_ok) {
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
               if (t < p.M) {
@@ -333,7 +339,9 @@ lq_status launch_batch_t(const MatmulArgs& a, const BatchParams& p, int G, size_
 
 template <int FMT, int EPI>
 lq_status launch_batch_mt(const MatmulArgs& a, const BatchParams& p, int G, size_t smem, int MT) {
-  return MT == 2 ? launch_batch_t<FMT, 2, EPI>(a, p, G, smem) : launch_batch_t<FMT, 4, EPI>(a, p, G, smem);
+  if (MT == 2) return launch_batch_t<FMT, 2, EPI>(a, p, G, smem);
+  if (MT == 4) return launch_batch_t<FMT, 4, EPI>(a, p, G, smem);
+  return launch_batch_t<FMT, 8, EPI>(a, p, G, smem);
 }
 
 template <int FMT>
@@ -363,6 +371,7 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   const bool shape_ok = M >= 2 && M <= kBMaxTokens && K <= 16384 && N < (1LL << 30) &&
                         (a.fmt == LQ_FMT_F16 ? (K % 8 == 0) : (K % 256 == 0));
   if (!shape_ok || !aligned16(a.A) || !aligned16(a.W)) return LQ_ERR_UNSUPPORTED;
+  const int MT = M <= 2 ? 2 : (M <= 4 ? 4 : 8);
   int nk;
   if (a.fmt == LQ_FMT_F16) {
     const int nch = static_cast<int>((K + 255) / 256);
@@ -371,10 +380,9 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
     while (nk < nch) nk *= 2;
   } else {
     const int nseg = static_cast<int>((K / 32 + 63) / 64);
-    if (2 * nseg > kBKGroups) return LQ_ERR_UNSUPPORTED;
-    nk = 2 * nseg;
+    if (kgroups_per_segment(MT) * nseg > kBKGroups) return LQ_ERR_UNSUPPORTED;
+    nk = kgroups_per_segment(MT) * nseg;
   }
-  const int MT = M <= 2 ? 2 : 4;
   const int NW = batch_warps(a.fmt, MT);
   const DeviceInfo& di = device_info();
   const int G = static_cast<int>(std::min<int64_t>(N, di.sm_count));
@@ -387,7 +395,7 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   const int a_slot = a.fmt == LQ_FMT_F16 ? static_cast<int>(K * 4)
                                          : static_cast<int>((K / 32 + 63) / 64) * 64 * kASlotBytes;
   const int a_stage = a.fmt == LQ_FMT_F16 ? 0 : static_cast<int>((M * K * 4 + 127) / 128 * 128);
-  const int hdr = MT == 2 ? batch_header_bytes<2>() : batch_header_bytes<4>();
+  const int hdr = MT == 2 ? batch_header_bytes<2>() : (MT == 4 ? batch_header_bytes<4>() : batch_header_bytes<8>());
   const int budget = std::min(di.max_smem_optin, 227 * 1024) - hdr - MT * a_slot;
   const int rows_per_cta = static_cast<int>((N + G - 1) / G);
   if (budget < 2 * rb || budget < a_stage) return LQ_ERR_UNSUPPORTED;

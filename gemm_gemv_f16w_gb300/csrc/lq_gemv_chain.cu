@@ -190,6 +190,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
           break;
         }
         const uint32_t bytes = static_cast<uint32_t>(min(RS, nrows - st * RS)) * q.row_bytes;
+        if (!LQ_IN_BOUNDS(r0 + st * RS + min(RS, nrows - st * RS) <= q.N)) {
+          ok = false;
+          break;
+        }
         mbar_arrive_expect_tx(&hd.full[s], bytes);
         bulk_g2s(ring + static_cast<size_t>(s) * p.slot_bytes,
                  q.W + (static_cast<long long>(r0) + static_cast<long long>(st) * RS) * q.row_bytes, bytes,
@@ -360,7 +364,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
         float sum = 0.f;
         if (lane < rows)
           for (int k = 0; k < nk; ++k) sum += red_s[lane * nk + k];
-        if (lane < rows) q.C[r0 + st * RS + lane] = sum;
+        if (lane < rows && LQ_IN_BOUNDS(r0 + st * RS + lane < q.N)) q.C[r0 + st * RS + lane] = sum;
         if (p.publish) {
           __syncwarp();
           if (lane == 0) {

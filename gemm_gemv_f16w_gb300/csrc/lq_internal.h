@@ -58,7 +58,7 @@ lq_status launch_gemv_generic(const MatmulArgs& a);    // any M, K, alignment
 // shared memory per CTA.
 void set_gemv_tuning(int ctas_per_sm, int rows_per_stage, int smem_cap);
 lq_status launch_gemm_stream(const MatmulArgs& a);     // CUDA-core, small M
-// CUDA-core batched decode for M = 2..4 (W streamed once, every row of A
+// CUDA-core batched decode for M = 2..8 (W streamed once, every row of A
 // multiplied with each dequantised block); LQ_ERR_UNSUPPORTED outside its shapes
 lq_status launch_gemv_batch(const MatmulArgs& a);
 lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via shared memory

@@ -68,7 +68,10 @@ typedef enum {
   LQ_ERR_INVALID_ARG = 1,    /* bad pointer, size or alignment; nothing ran   */
   LQ_ERR_UNSUPPORTED = 2,    /* no kernel exists for this request             */
   LQ_ERR_CUDA = 3,           /* a CUDA runtime call or launch failed          */
-  LQ_ERR_DEVICE_TIMEOUT = 4  /* a bounded device-side wait ran out            */
+  LQ_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out            */
+  LQ_ERR_BOUNDS = 5          /* debug build (liblq_debug.so, LQ_DEBUG_BOUNDS)
+                                only: a kernel's index check failed and the
+                                access was skipped                            */
 } lq_status;
 
 /* Weight formats. LQ_FMT_Q4_0I is Q4_0 with the nibble order the pages' own

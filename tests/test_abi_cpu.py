@@ -25,7 +25,7 @@ def test_header_declarations_are_all_exported(lq):
 
 def test_version_and_status_strings(lq):
     assert "sm_103a" in lq.version()
-    for s in range(5):
+    for s in range(6):
         assert lq.status_string(s).startswith("LQ_")
 
 

@@ -1,10 +1,12 @@
-"""The batched decode kernel (M = 2..4 rows of A, route 1) against the oracle.
+"""The batched decode kernel (M = 2..8 rows of A, route 1) against the oracle.
 
 The kernel keeps f32 activations and dequantises W exactly, so every element
 is held to the GEMV tolerance (1e-4 * sum|a*w| + 1e-6), not the tensor-core
 one. Shapes cover several stages per CTA with a ragged last stage, fewer rows
 than SMs, the K limits of the kernel and the fallbacks beyond them (shapes it
-refuses go to the tensor-core or the generic kernel and still match).
+refuses go to the tensor-core or the generic kernel and still match). Five to
+eight rows use the half-block slices (each lane holds half a quantised block
+for every row).
 """
 import numpy as np
 import pytest
@@ -34,7 +36,7 @@ def _ref(fmt, W, A):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
-@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("N,K", [(5, 512), (1000, 256), (4133, 2048), (2437, 1024)])
 def test_batch_matches_oracle(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=7 * M + N + K, outlier_frac=0.05)
@@ -47,7 +49,9 @@ def test_batch_matches_oracle(lq, cuda_dev, fmt, M, N, K):
 
 @pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 4, 20000, 2048), ("q4_0", 4, 16000, 4096),
                                        ("f16", 4, 20000, 2048), ("q8_0", 2, 8192, 8192),
-                                       ("q4_0", 3, 30000, 1024)])
+                                       ("q4_0", 3, 30000, 1024), ("q8_0", 8, 20000, 2048),
+                                       ("q4_0", 6, 16000, 2048), ("f16", 7, 20000, 2048),
+                                       ("q4_0", 5, 30000, 1024)])
 def test_batch_ring_refills(lq, cuda_dev, fmt, M, N, K):
     """More stages per CTA than ring slots: slots are refilled by the stage's
     finisher while other row-groups compute, and each refill's partials reuse
@@ -104,9 +108,58 @@ def test_batch_unaligned_a_falls_back(lq, cuda_dev):
     assert lq.route_count(1) == 0
 
 
+@pytest.mark.parametrize("fmt,K,fits", [("q8_0", 2048, True), ("q8_0", 3072, False),
+                                        ("q4_0", 2048, True), ("q4_0", 4096, False),
+                                        ("f16", 2048, True), ("f16", 2304, False)])
+def test_batch_eight_rows_k_limits(lq, cuda_dev, fmt, K, fits):
+    """Eight rows of A up to K = 2048 (the activations' block slots and the
+    staged copy share shared memory); larger K goes to the tensor cores."""
+    M, N = 8, 1536
+    W, A = synthetic.draw(M, N, K, seed=K + 8, outlier_frac=0.05)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=not fits)
+    check(C, y, tol, f"{fmt} 8x{N}x{K}")
+    assert lq.route_count(1) == (1 if fits else 0)
+
+
+@pytest.mark.parametrize("fmt", ["q4_0i", "q8_0"])
+@pytest.mark.parametrize("M", [5, 8])
+def test_batch_eight_row_slices_layouts_and_epilogues(lq, cuda_dev, fmt, M):
+    """The half-block slices with the pages' interleaved nibbles, and the
+    residual epilogue on them."""
+    N, K = 3000, 2048
+    W, A = synthetic.draw(M, N, K, seed=M + 40, outlier_frac=0.05)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, f"{fmt} {M}x{N}x{K}")
+    assert lq.route_count(1) == 1
+    R = torch.randn(M, N, generator=torch.Generator().manual_seed(9))
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), cuda_dev)
+    Cd = R.to(cuda_dev)
+    lq.reset_counts()
+    lq.lq_matmul_residual(fmt, A.to(cuda_dev), Wd, Cd, Cd, M, N, K)  # in place: C = A W^T + C
+    torch.cuda.synchronize()
+    assert lq.route_count(1) == 1
+    yr, tr = O.residual_reference(y, tol, R.numpy())
+    check(Cd.cpu().numpy(), yr, tr, f"{fmt} residual {M}x{N}x{K}")
+
+
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
 def test_batch_crossover_config_m2(lq, cuda_dev, fmt):
     w = synthetic.WORKLOADS[f"gemm_{fmt}_m2_6144x2048"]
+    W, A = synthetic.draw_workload(w)
+    lq.reset_counts()
+    C = _run(lq, cuda_dev, fmt, W, A)
+    y, tol = _ref(fmt, W, A)
+    check(C, y, tol, w.name)
+    assert lq.route_count(1) == 1
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+def test_batch_crossover_config_m8(lq, cuda_dev, fmt):
+    w = synthetic.WORKLOADS[f"gemm_{fmt}_m8_6144x2048"]
     W, A = synthetic.draw_workload(w)
     lq.reset_counts()
     C = _run(lq, cuda_dev, fmt, W, A)

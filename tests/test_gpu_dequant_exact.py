@@ -3,10 +3,11 @@
 A one-hot activation A = e_k makes every route return column k of the
 dequantised weights: the product 1 * w is w itself and every other term is
 a signed zero. On the CUDA-core routes (the decode GEMV, the batched decode
-kernel for M = 2..4 and the decode chain) the weights are dequantised
-exactly in f32 (f16 widened; Q8_0 d*q and Q4_0 d*(q-8), an 11-bit scale times
-a code of at most 8 bits), so C must equal the oracle's dequantise() of the
-same bytes bit for bit. On the tensor-core route the weight operand is that
+kernel for M = 2..8, whose five- to eight-row slices hold half a block per
+lane, and the decode chain) the weights are dequantised exactly in f32 (f16
+widened; Q8_0 d*q and Q4_0 d*(q-8), an 11-bit scale times a code of at most
+8 bits), so C must equal the oracle's dequantise() of the same bytes bit for
+bit. On the tensor-core route the weight operand is that
 exact value rounded once to bf16 (round to nearest even), so C must equal
 the oracle's bf16 rounding of it bit for bit. The only freedom is the sign
 of a zero result: a weight of -0 may come back as +0 (the sum of the other
@@ -82,7 +83,7 @@ def test_gemv_dequantises_bit_exactly(lq, cuda_dev, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
-@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("M", [2, 3, 4, 5, 8])
 def test_batched_decode_dequantises_bit_exactly(lq, cuda_dev, fmt, M):
     W = _weights(fmt, 32 + M)
     Wd = _pack(lq, fmt, W, cuda_dev)

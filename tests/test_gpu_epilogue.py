@@ -57,6 +57,8 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
     (1, 4133, 4096, ROUTE_GEMV, False),
     (2, 1000, 2048, ROUTE_BATCH, False),
     (4, 2437, 1024, ROUTE_BATCH, False),
+    (6, 1000, 2048, ROUTE_BATCH, False),
+    (8, 700, 1024, ROUTE_BATCH, False),
     (64, 1000, 2048, ROUTE_TC, True),
     (300, 777, 1024, ROUTE_TC, True),
 ]

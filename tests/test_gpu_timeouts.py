@@ -31,7 +31,8 @@ def _packed(lq, fmt, W, dev):
 
 
 @pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 3, 20000, 2048), ("f16", 2, 8000, 1024),
-                                       ("q4_0", 4, 16000, 4096)])
+                                       ("q4_0", 4, 16000, 4096), ("q8_0", 8, 20000, 2048),
+                                       ("f16", 7, 8000, 1024)])
 def test_batch_kernel_timeout(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=N)
     Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
