@@ -34,9 +34,7 @@
 
 #include <algorithm>
 #include <atomic>
-#include <map>
 #include <mutex>
-#include <tuple>
 
 #include "lq_device.cuh"
 #include "lq_epilogue.cuh"
@@ -68,7 +66,10 @@ struct TmaGemmParams {
   const float* R;      // residual epilogue: added to every output
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
-  int split;           // CTAs of a cluster splitting K (1: no split)
+  int split;           // CTAs splitting K for one output tile (1: no split)
+  int n_tiles;         // output tiles along N (the tile of CTA (x, y) is y * n_tiles + x / split)
+  float* part;         // split > 1: each rank's partial tile, [rank][tile][token][128 rows] f32
+  unsigned* cnt;       // split > 1: ranks done per tile (zeroed by the pre-pass)
   int stages;          // pipeline depth (2..kMaxStages)
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
   unsigned long long wait_ns;
@@ -82,6 +83,7 @@ struct Bars {
   uint64_t tmem_full;
   uint32_t tmem_base;
   volatile int abort;
+  volatile int last;   // split K: this CTA is the tile's last rank to finish
 };
 
 __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_tma_err, 0u, code); }
@@ -94,13 +96,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // ---------------------------------------------------------------------------
 // Pre-pass: A f32 [M,K] -> bf16 [M,K], every value rounded to nearest even
-// (cvt.rn.bf16x2.f32). Elementwise: thread i converts elements 8i .. 8i+7
-// (K is a multiple of 128 on this route, so eight never straddle a row or a
-// block of 32). With perm (Q4_0 with interleaved nibbles) each block's
-// elements go to the slots of lq_q4i.cuh: element 2j to slot j, 2j+1 to
-// slot 16+j.
+// (cvt.rn.bf16x2.f32). Elementwise over chunks of eight (K is a multiple of
+// 128 on this route, so a chunk never straddles a row or a block of 32).
+// With perm (Q4_0 with interleaved nibbles) each block's elements go to the
+// slots of lq_q4i.cuh: element 2j to slot j, 2j+1 to slot 16+j.
+// One CTA of 128 threads per SM: small enough in registers and threads that
+// the GEMM's CTAs, launched early (programmatic dependent launch), fit
+// beside it and stream their first weight stages while it runs. Each thread
+// issues the loads of up to kPreBatch chunks before converting any, so that
+// enough bytes are in flight per SM.
 // ---------------------------------------------------------------------------
-constexpr int kPreThreads = 256;
+constexpr int kPreThreads = 128, kPreBatch = 4;
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
@@ -109,22 +115,38 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kPreThreads) a_to_bf16_kernel(const float* __restrict__ A,
                                                                 uint32_t* __restrict__ A16, long long n8,
-                                                                int perm) {
+                                                                int perm, unsigned* __restrict__ cnt, int ncnt) {
   pdl_launch_dependents();
   pdl_wait();
   const long long stride = static_cast<long long>(gridDim.x) * kPreThreads;
-  for (long long i = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i < n8; i += stride) {
-    const float4 x = ldg128f(A + 8 * i), y = ldg128f(A + 8 * i + 4);
-    if (!perm) {
-      const uint4 o = make_uint4(bf16x2(x.x, x.y), bf16x2(x.z, x.w), bf16x2(y.x, y.y), bf16x2(y.z, y.w));
-      *reinterpret_cast<uint4*>(A16 + 4 * i) = o;
-    } else {
-      // chunk c of block b: even elements 8c, 8c+2, 8c+4, 8c+6 -> slots
-      // 4c .. 4c+3 (words 2c, 2c+1); odd ones -> slots 16+4c .. (words 8+2c, 9+2c)
-      uint32_t* blk = A16 + 16 * (i >> 2);
-      const int c = static_cast<int>(i & 3);
-      *reinterpret_cast<uint2*>(blk + 2 * c) = make_uint2(bf16x2(x.x, x.z), bf16x2(y.x, y.z));
-      *reinterpret_cast<uint2*>(blk + 8 + 2 * c) = make_uint2(bf16x2(x.y, x.w), bf16x2(y.y, y.w));
+  for (long long i = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i < ncnt; i += stride)
+    cnt[i] = 0u;  // split K: no rank of the GEMM has finished a tile yet
+  for (long long i0 = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i0 < n8;
+       i0 += stride * kPreBatch) {
+    float4 x[kPreBatch], y[kPreBatch];
+#pragma unroll
+    for (int u = 0; u < kPreBatch; ++u) {
+      const long long i = i0 + stride * u;
+      if (i < n8) {
+        x[u] = ldg128f(A + 8 * i);
+        y[u] = ldg128f(A + 8 * i + 4);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPreBatch; ++u) {
+      const long long i = i0 + stride * u;
+      if (i >= n8) break;
+      if (!perm) {
+        *reinterpret_cast<uint4*>(A16 + 4 * i) = make_uint4(bf16x2(x[u].x, x[u].y), bf16x2(x[u].z, x[u].w),
+                                                             bf16x2(y[u].x, y[u].y), bf16x2(y[u].z, y[u].w));
+      } else {
+        // chunk c of block b: even elements 8c, 8c+2, 8c+4, 8c+6 -> slots
+        // 4c .. 4c+3 (words 2c, 2c+1); odd ones -> slots 16+4c .. (words 8+2c, 9+2c)
+        uint32_t* blk = A16 + 16 * (i >> 2);
+        const int c = static_cast<int>(i & 3);
+        *reinterpret_cast<uint2*>(blk + 2 * c) = make_uint2(bf16x2(x[u].x, x[u].z), bf16x2(y[u].x, y[u].z));
+        *reinterpret_cast<uint2*>(blk + 8 + 2 * c) = make_uint2(bf16x2(x[u].y, x[u].w), bf16x2(y[u].y, y[u].w));
+      }
     }
   }
 }
@@ -228,27 +250,12 @@ __device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t 
   }
 }
 
-// ---------------------------------------------------------------------------
-// Split-K support: cluster barrier and loads from a peer CTA's shared memory.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-  return v;
-}
-
 // Epilogue of one TMEM lane (W row r of the tile): the accumulator columns
-// of 32-column chunks c0, c0 + 2, ..., plus the partial tiles of peers
-// 1 .. split-1 (token-major f32 at `red` in their shared memory) when
-// split > 1, stored to C[m0 + j, n0 + r].
+// of 32-column chunks c0, c0 + 2, ..., stored to C[m0 + j, n0 + r] (with R
+// added for the residual epilogue).
 template <int FMT, int EPI>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
-                                           int bt, uint32_t red, int split, int c0) {
+                                           int bt, int c0) {
   const int n = n0 + r;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -257,18 +264,6 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
     uint32_t v[32];
     tc::ld_32x32b_x32(tcol + 32u * c, v);
     tc::wait_ld();
-#pragma unroll 1
-    for (int q = 1; q < split; ++q) {
-      // all 32 loads first, so that they are in flight together
-      float t[32];
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj)
-        t[jj] = 32 * c + jj < bt ? ld_peer_f32(red + 4u * static_cast<uint32_t>((32 * c + jj) * kBN + r),
-                                               static_cast<uint32_t>(q))
-                                 : 0.f;
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + t[jj]);
-    }
     // residual: the chunk's 32 values of R first (R may be C, so no load
     // could move past a store), then the stores
     float rv[32];
@@ -295,15 +290,55 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
   }
 }
 
+// Split K, every rank: its partial tile (TMEM lane r, chunks c0, c0 + 2, ...)
+// to its slot of the workspace, token-major so that the 32 lanes of a warp
+// write 32 consecutive floats.
+__device__ __forceinline__ void store_partial(float* part, uint32_t tcol, int r, int bt, int c0) {
+#pragma unroll 1
+  for (int c = c0; c < (bt + 31) / 32; c += 2) {
+    uint32_t v[32];
+    tc::ld_32x32b_x32(tcol + 32u * c, v);
+    tc::wait_ld();
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj)
+      if (32 * c + jj < bt) part[static_cast<long long>(32 * c + jj) * kBN + r] = __uint_as_float(v[jj]);
+  }
+}
+
+// Split K, the tile's last rank: the split partial tiles of the workspace
+// added in rank order (a fixed order whichever rank finishes last), then C
+// (R added for the residual epilogue).
+template <int EPI>
+__device__ __forceinline__ void reduce_partials(const TmaGemmParams& p, const float* part0, long long rank_stride,
+                                                int split, int r, int n0, int m0, int bt, int c0) {
+  const int n = n0 + r;
+  if (n >= p.N) return;
+#pragma unroll 1
+  for (int c = c0; c < (bt + 31) / 32; c += 2) {
+#pragma unroll 4
+    for (int jj = 0; jj < 32; ++jj) {
+      const int tok = 32 * c + jj, m = m0 + tok;
+      if (tok >= bt || m >= p.M || !LQ_IN_BOUNDS(m >= 0 && n >= 0)) continue;
+      const float* src = part0 + static_cast<long long>(tok) * kBN + r;
+      float sum = 0.f;
+      for (int q = 0; q < split; ++q) sum += __ldcg(src + q * rank_stride);
+      const long long o = static_cast<long long>(m) * p.N + n;
+      if constexpr (EPI == epi::kResidual) sum += p.R[o];
+      p.C[o] = sum;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
 // Warps 2..9: converters in two groups of four (group g converts the
 // pipeline stages ks with ks % 2 == g: 128 K of its W rows into the stage's
 // 64 TMEM columns); then both groups run the epilogue, group g taking the
-// 32-column chunks g, g + 2, ... With split K (a cluster of CTAs sharing one
-// output tile), the other ranks leave their partial tiles in their own
-// shared memory and the leader adds them over distributed shared memory
-// before storing C. Per stage one barrier
+// 32-column chunks g, g + 2, ... With split K (`split` CTAs sharing one
+// output tile, each over its own range of K) every rank writes its partial
+// tile to the workspace and counts itself done on the tile's counter; the
+// rank that counts last adds the partials in rank order and stores C. No
+// rank waits for another. Per stage one barrier
 // says "A tile and W operand ready" (1 arrival with the TMA bytes + 4
 // converter warps) and one commit says "the stage's MMAs are done". The
 // producer and MMA warps run their loops with all 32 lanes (every lane
@@ -338,7 +373,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   Bars& b = *reinterpret_cast<Bars*>(w_ring + RR * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Split K: the `split` CTAs of a cluster share one output tile, rank r
+  // Split K: `split` consecutive CTAs along x share one output tile, rank r
   // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
   // the CTA, the K coordinates of its loads add ks0.
   const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
@@ -359,6 +394,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     mbar_init(&b.tmem_full, 1);
     b.abort = 0;
+    b.last = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -565,20 +601,28 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               p.C[static_cast<long long>(m0 + tok) * p.N + n] = epi::swiglu(xch[tok * 128 + j], xch[tok * 128 + 64 + j]);
           }
         }
-      } else if (epi && split == 1) {
-        store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g);
-      } else if (epi && rank != 0) {
-        // this rank's partial tile -> its own shared memory (the A ring is
-        // idle now), token-major so that the 32 lanes write 32 rows in a row
-        float* red = reinterpret_cast<float*>(a_ring);
-#pragma unroll 1
-        for (int c = g; c < (bt + 31) / 32; c += 2) {
-          uint32_t v[32];
-          tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
-          tc::wait_ld();
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj)
-            if (32 * c + jj < bt) red[(32 * c + jj) * kBN + r] = __uint_as_float(v[jj]);
+      } else if (split == 1) {
+        if (epi) store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, g);
+      } else {
+        // split K: this rank's partial tile, then one count per CTA on the
+        // tile's counter once every epilogue thread's stores are visible
+        // (fence, then the barrier of the eight epilogue warps, reached
+        // whatever their outcome); the rank that counts last reduces
+        const int tile = static_cast<int>(blockIdx.y) * p.n_tiles + static_cast<int>(blockIdx.x) / split;
+        const long long tile_floats = static_cast<long long>(bt) * kBN;
+        const long long rank_stride = tile_floats * p.n_tiles * static_cast<long long>(gridDim.y);
+        float* part0 = p.part + tile_floats * tile;
+        if (epi) store_partial(part0 + rank_stride * rank, tmem + tlane, r, bt, g);
+        __threadfence();
+        named_barrier(3, 8u * 32u);
+        if (threadIdx.x == 64) {
+          const unsigned done = atomicAdd(p.cnt + tile, 1u);
+          b.last = done == static_cast<unsigned>(split - 1) ? 1 : 0;
+        }
+        named_barrier(3, 8u * 32u);
+        if (b.last && !b.abort) {
+          __threadfence();  // the other ranks' partials, published before their counts
+          reduce_partials<EPI>(p, part0, rank_stride, split, r, n0, m0, bt, g);
         }
       }
     }
@@ -586,18 +630,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // ---------------- teardown ----------------
   tc::fence_before_sync();
   __syncthreads();
-  if (split > 1) {
-    // the peers' partial tiles are in their shared memory; the leader adds
-    // them to its own (rank order: a fixed summation order) and stores C
-    cluster_sync();
-    if (rank == 0 && epi && warp >= 2) {
-      tc::fence_after_sync();
-      const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
-      store_tile<FMT, EPI>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
-                           split, g);
-    }
-    cluster_sync();  // the peers keep their shared memory until the leader read it
-  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -626,34 +658,21 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// Launch with programmatic dependent launch and, when cluster_x > 1,
-// clusters of cluster_x CTAs along x.
+// Launch with programmatic dependent launch.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                               unsigned cluster_x, Args&&... args) {
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
   cfg.numAttrs = 1;
-  if (cluster_x > 1) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cluster_x;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-  }
   cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
-  return launch_pdl_cluster(kern, grid, block, smem, st, 1u, std::forward<Args>(args)...);
 }
 
 bool aligned(const void* p, unsigned al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
@@ -719,53 +738,14 @@ size_t tma_smem_bytes(int fmt, int bt, int a_stages, int raw_stages) {
   return std::max<size_t>(need, 116 * 1024);
 }
 
-// Clusters of `split` CTAs along K: the largest split (up to 8, the portable
-// cluster size) whose clusters all fit on the GPU at once, or 1.
-template <int FMT>
-int pick_split_query(int64_t tiles, int nraw_all, size_t smem);
-
-template <int FMT>
-int pick_split(int64_t tiles, int nraw_all, size_t smem) {
+// Split K: when the output tiles leave more than half of the SMs idle, K is
+// split so that about one CTA runs per SM (at most one raw W stage per rank
+// and at most kMaxSplit ranks).
+constexpr int kMaxSplit = 16;
+int pick_split(int64_t tiles, int nraw_all) {
   const DeviceInfo& di = device_info();
   if (2 * tiles > di.sm_count) return 1;
-  // the answer depends on (tiles, K, shared memory) only: remember it
-  static std::mutex mu;
-  static std::map<std::tuple<int, int64_t, int, size_t>, int> cache;
-  const auto key = std::make_tuple(current_device(), tiles, nraw_all, smem);
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = cache.find(key);
-    if (it != cache.end()) return it->second;
-  }
-  const int s = pick_split_query<FMT>(tiles, nraw_all, smem);
-  std::lock_guard<std::mutex> lk(mu);
-  cache[key] = s;
-  return s;
-}
-
-template <int FMT>
-int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
-  const DeviceInfo& di = device_info();
-  int s = static_cast<int>(std::min<int64_t>({8, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all}));
-  for (; s >= 2; --s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(tiles * s));
-    cfg.blockDim = dim3(kTmaThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT, epi::kPlain>, &cfg) == cudaSuccess &&
-        active >= tiles)
-      return s;
-    cudaGetLastError();  // a refused query is not an error of the call
-  }
-  return 1;
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({kMaxSplit, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all})));
 }
 
 template <int FMT, int EPI>
@@ -804,12 +784,9 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
     if (e != cudaSuccess) return cuda_status(e);
     configured[dev] = static_cast<int>(smem);
   }
-  const int64_t tiles = ((a.N + bn - 1) / bn) * ((a.M + p.bt - 1) / p.bt);
-  p.split = EPI == epi::kSwiglu ? 1 : pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
   const dim3 grid(static_cast<unsigned>((a.N + bn - 1) / bn * p.split),
                   static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
-  cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
-                                     static_cast<unsigned>(p.split), tmW, tmA, p);
+  cudaError_t e = launch_pdl(kern, grid, dim3(kTmaThreads), smem, a.stream, tmW, tmA, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
 }
@@ -823,7 +800,6 @@ unsigned read_clear_gemm_tma_error() {
   return v;
 }
 
-int pick_gemm_bt(int64_t M, int64_t N) { return pick_bt(M, N); }
 
 void set_gemm_rings(int a_stages, int raw_stages) {
   g_ring_a.store(a_stages);
@@ -866,36 +842,59 @@ cudaMemPool_t workspace_pool() {
 // stream-ordered workspace from the library's pool for the duration of the
 // call.
 lq_status launch_gemm_tma(const MatmulArgs& a) {
-  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
-  const int bt = pick_bt(a.M, a.epi == epi::kSwiglu ? 2 * a.N : a.N);
-  const size_t ws_bytes = gemm_tma_workspace_bytes(a.M, a.K);
+  const TmaPlan pl = gemm_tma_plan(a);
   void* ws = nullptr;
   cudaMemPool_t pool = workspace_pool();
   if (!pool) return LQ_ERR_CUDA;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes, pool, a.stream);
   if (e != cudaSuccess) return LQ_ERR_CUDA;
-  lq_status st = launch_gemm_tma_ws(a, ws, bt);
+  lq_status st = launch_gemm_tma_ws(a, pl, ws);
   cudaError_t ef = cudaFreeAsync(ws, a.stream);
   if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
   if (st == LQ_OK) count_route(2);
   return st;
 }
 
-size_t gemm_tma_workspace_bytes(int64_t M, int64_t K) {
-  return (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
+// Token tile, K split and workspace layout of a call: the bf16 copy of A,
+// then (split K) the ranks' partial tiles and the tiles' counters, each part
+// 256-byte aligned.
+TmaPlan gemm_tma_plan(const MatmulArgs& a) {
+  TmaPlan pl;
+  const bool sw = a.epi == epi::kSwiglu;
+  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
+  pl.bt = pick_bt(a.M, sw ? 2 * a.N : a.N);
+  const int bn = sw ? kBN / 2 : kBN;
+  pl.n_tiles = static_cast<int>((a.N + bn - 1) / bn);
+  pl.m_tiles = static_cast<int>((a.M + pl.bt - 1) / pl.bt);
+  const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles;
+  pl.split = sw ? 1 : pick_split(tiles, static_cast<int>(a.K / kstep_multiple(a.fmt)));
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  size_t off = up(static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2);
+  if (pl.split > 1) {
+    pl.part_off = off;
+    off += up(static_cast<size_t>(pl.split) * static_cast<size_t>(tiles) * pl.bt * kBN * 4);
+    pl.cnt_off = off;
+    off += up(static_cast<size_t>(tiles) * 4);
+  }
+  pl.ws_bytes = off;
+  return pl;
 }
 
-// Pre-pass + GEMM given a workspace of M*K bf16 values (a16, 16-byte aligned).
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
+// Pre-pass + GEMM given the plan's workspace (256-byte aligned).
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
-  // 1. A -> bf16 (round to nearest even)
+  const int bt = pl.bt;
+  void* a16 = ws;
+  unsigned* cnt = pl.split > 1 ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pl.cnt_off) : nullptr;
+  const int ncnt = pl.split > 1 ? pl.n_tiles * pl.m_tiles : 0;
+  // 1. A -> bf16 (round to nearest even); the split-K counters to zero
   {
     const long long n8 = static_cast<long long>(M) * K / 8;
     const long long want = (n8 + kPreThreads - 1) / kPreThreads;
-    const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1)) * 8;
+    const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1));
     const unsigned grid = static_cast<unsigned>(std::max<long long>(1, std::min(want, cap)));
     cudaError_t e = launch_pdl(a_to_bf16_kernel, dim3(grid), dim3(kPreThreads), 0, a.stream, a.A,
-                               static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0);
+                               static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0, cnt, ncnt);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return LQ_ERR_CUDA;
   }
@@ -942,7 +941,10 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
   p.N = N;
   p.K = K;
   p.bt = bt;
-  p.split = 1;  // chosen at launch (pick_split)
+  p.split = pl.split;
+  p.n_tiles = pl.n_tiles;
+  p.part = pl.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off) : nullptr;
+  p.cnt = cnt;
   {
     const RingPlan rp = ring_plan(a.fmt, bt);
     p.stages = rp.a_stages;
