@@ -307,24 +307,39 @@ __device__ __forceinline__ void store_partial(float* part, uint32_t tcol, int r,
 
 // Split K, the tile's last rank: the split partial tiles of the workspace
 // added in rank order (a fixed order whichever rank finishes last), then C
-// (R added for the residual epilogue).
+// (R added for the residual epilogue). Thread t of the 256 epilogue threads
+// takes row t % 128 and every other token from t / 128; per rank it issues
+// the loads of up to 32 tokens before adding any, so that they are in
+// flight together (a warp's loads are 128 consecutive bytes).
 template <int EPI>
 __device__ __forceinline__ void reduce_partials(const TmaGemmParams& p, const float* part0, long long rank_stride,
-                                                int split, int r, int n0, int m0, int bt, int c0) {
+                                                int split, int n0, int m0, int bt, int t) {
+  const int r = t & (kBN - 1), h = t >> 7;
   const int n = n0 + r;
   if (n >= p.N) return;
 #pragma unroll 1
-  for (int c = c0; c < (bt + 31) / 32; c += 2) {
-#pragma unroll 4
-    for (int jj = 0; jj < 32; ++jj) {
-      const int tok = 32 * c + jj, m = m0 + tok;
-      if (tok >= bt || m >= p.M || !LQ_IN_BOUNDS(m >= 0 && n >= 0)) continue;
-      const float* src = part0 + static_cast<long long>(tok) * kBN + r;
-      float sum = 0.f;
-      for (int q = 0; q < split; ++q) sum += __ldcg(src + q * rank_stride);
-      const long long o = static_cast<long long>(m) * p.N + n;
-      if constexpr (EPI == epi::kResidual) sum += p.R[o];
-      p.C[o] = sum;
+  for (int t0 = h; t0 < bt; t0 += 64) {
+    float sum[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sum[i] = 0.f;
+#pragma unroll 1
+    for (int q = 0; q < split; ++q) {
+      const float* src = part0 + q * rank_stride + r;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int tok = t0 + 2 * i;
+        if (tok < bt) sum[i] += __ldcg(src + static_cast<long long>(tok) * kBN);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tok = t0 + 2 * i, m = m0 + tok;
+      if (tok < bt && m < p.M && LQ_IN_BOUNDS(m >= 0 && n >= 0)) {
+        const long long o = static_cast<long long>(m) * p.N + n;
+        float v = sum[i];
+        if constexpr (EPI == epi::kResidual) v += p.R[o];
+        p.C[o] = v;
+      }
     }
   }
 }
@@ -622,7 +637,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         named_barrier(3, 8u * 32u);
         if (b.last && !b.abort) {
           __threadfence();  // the other ranks' partials, published before their counts
-          reduce_partials<EPI>(p, part0, rank_stride, split, r, n0, m0, bt, g);
+          reduce_partials<EPI>(p, part0, rank_stride, split, n0, m0, bt, static_cast<int>(threadIdx.x) - 64);
         }
       }
     }
