@@ -398,6 +398,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
   bool epi = false;  // this CTA's accumulator is complete and may be used
 
+  // one raw W stage into ring slot `slot` (producer lane 0)
+  auto issue_raw = [&](int j, int slot) {
+    mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
+    if (FMT == LQ_FMT_F16) {
+      for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
+        if constexpr (SWIGLU)
+          tc::tma_load_3d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
+                          &b.raw_full[slot]);
+        else
+          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
+                          &b.raw_full[slot]);
+      }
+    } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
+      if constexpr (SWIGLU)
+        tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
+                        &b.raw_full[slot]);
+      else
+        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
+                        &b.raw_full[slot]);
+    }
+  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < RR; ++i) {
       mbar_init(&b.raw_full[i], 1);
@@ -411,6 +432,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     b.abort = 0;
     b.last = 0;
     fence_barrier_init();
+    // W does not depend on the previous kernel: its first stages are on their
+    // way before the TMEM allocation and the block barrier
+    tc::prefetch_tmap(&tmW);
+    tc::prefetch_tmap(&tmA);
+    for (int j = 0; j < nraw && j < RR; ++j) issue_raw(j, j);
   }
   if (warp == 1) {
     tc::tmem_alloc(&b.tmem_base, kTmemCols);
@@ -424,36 +450,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer ----------------
-    if (lane == 0) {
-      tc::prefetch_tmap(&tmW);
-      tc::prefetch_tmap(&tmA);
-    }
-    auto issue_raw = [&](int j, int slot) {
-      mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
-      if (FMT == LQ_FMT_F16) {
-        for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
-          if constexpr (SWIGLU)
-            tc::tma_load_3d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
-                            &b.raw_full[slot]);
-          else
-            tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
-                            &b.raw_full[slot]);
-        }
-      } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
-        if constexpr (SWIGLU)
-          tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
-                          &b.raw_full[slot]);
-        else
-          tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
-                          &b.raw_full[slot]);
-      }
-    };
-    int raw_issued = 0, issued = 0;
+    int raw_issued = min(nraw, RR), issued = 0;  // the first raw stages are in flight (prologue)
     bool ok = true;
-    // W does not depend on the previous kernel: start it before waiting.
-    for (; raw_issued < nraw && raw_issued < RR; ++raw_issued)
-      if (lane == 0) issue_raw(raw_issued, raw_issued);
-    __syncwarp();
     pdl_wait();
     int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
     for (int ks = 0; ks < nk; ++ks) {
@@ -628,17 +626,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         const long long rank_stride = tile_floats * p.n_tiles * static_cast<long long>(gridDim.y);
         float* part0 = p.part + tile_floats * tile;
         if (epi) store_partial(part0 + rank_stride * rank, tmem + tlane, r, bt, g);
-        __threadfence();
+        // the CTA barrier orders every epilogue thread's stores before the
+        // count; one thread publishes them at GPU scope (the release fence
+        // is cumulative over what the barrier ordered before it) and, as
+        // the last rank, acquires the other ranks' partials for all of them
         named_barrier(3, 8u * 32u);
         if (threadIdx.x == 64) {
+          __threadfence();
           const unsigned done = atomicAdd(p.cnt + tile, 1u);
+          __threadfence();
           b.last = done == static_cast<unsigned>(split - 1) ? 1 : 0;
         }
         named_barrier(3, 8u * 32u);
-        if (b.last && !b.abort) {
-          __threadfence();  // the other ranks' partials, published before their counts
+        if (b.last && !b.abort)
           reduce_partials<EPI>(p, part0, rank_stride, split, n0, m0, bt, static_cast<int>(threadIdx.x) - 64);
-        }
       }
     }
   }

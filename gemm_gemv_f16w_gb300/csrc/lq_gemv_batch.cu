@@ -10,10 +10,11 @@
 //  * one CTA per SM owns a contiguous range of W rows, streamed in stages of
 //    up to 8 rows through a ring of shared-memory slots (one bulk copy per
 //    stage, mbarrier transaction counts);
-//  * A (all M rows) arrives with one bulk copy after the previous kernel on
-//    the stream completed; the consumers spread each row into the 144-byte
-//    block slots of the quantised slices. The copy lands in the top ring
-//    slots, whose weight stages are issued once A has been spread out;
+//  * every ring slot gets its first weight stage at kernel start (weights
+//    depend on nothing); A (all M rows) is read once the previous kernel on
+//    the stream completed: f16 with one bulk copy into place, the quantised
+//    formats by the consumers with plain loads (up to 16 in flight per
+//    thread) straight into the 144-byte block slots the slices read;
 //  * the warps form the K-groups x row-groups grid of the GEMV, a row-group
 //    taking whole stages (ring depth a multiple of the row-group count);
 //    every lane holds its chunk of all M activation rows (five to eight
@@ -61,8 +62,6 @@ struct BatchParams {
   int row_bytes;
   int rows_per_stage;     // at most kBRows
   int stages;             // ring depth, a multiple of nr
-  int early;              // slots below the A staging area (issued at once)
-  int stage_off;          // byte offset of the A staging area in the ring
   int nk, nr;             // K-groups x row-groups
   int a_slot;             // bytes of one token's A as the slices read it
   unsigned long long wait_ns;
@@ -105,13 +104,12 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   BatchHeader<MT>& hd = *reinterpret_cast<BatchHeader<MT>*>(smem);
   uint8_t* sA = smem + batch_header_bytes<MT>();  // MT x a_slot
   uint8_t* ring = sA + MT * p.a_slot;
-  uint8_t* stage_a = ring + p.stage_off;          // M x K floats (quantised formats)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int RS = p.rows_per_stage, S = p.stages, nk = p.nk, nr = p.nr, active = nk * nr;
   const uint32_t stage_bytes = static_cast<uint32_t>(SWIGLU ? 2 * RS : RS) * p.row_bytes;
   if (S % nr != 0 || S > kBMaxStages || nk > kBKGroups || active > NW || (SWIGLU ? 2 * RS : RS) > kBRows ||
-      p.M > MT || p.early > S) {
+      p.M > MT) {
     if (threadIdx.x == 0) record_error(LQ_ERR_UNSUPPORTED);
     return;
   }
@@ -158,51 +156,68 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
     hd.abort = 0;
     fence_barrier_init();
     const uint64_t pol = policy_evict_first();
-    for (int st = 0; st < min(nst, p.early); ++st) issue(st, st, pol);  // weights depend on nothing
-    // A (M rows, contiguous) once the previous kernel on the stream completed
-    pdl_wait();
-    const uint32_t a_bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(p.K) * 4u;
-    mbar_arrive_expect_tx(&hd.a_bar, a_bytes);
-    bulk_g2s(FMT == LQ_FMT_F16 ? sA : stage_a, p.A, a_bytes, &hd.a_bar, policy_evict_last());
+    for (int st = 0; st < min(nst, S); ++st) issue(st, st, pol);  // weights depend on nothing
+    if (FMT == LQ_FMT_F16) {
+      // A (M rows, contiguous, in place) once the previous kernel on the
+      // stream completed
+      pdl_wait();
+      const uint32_t a_bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(p.K) * 4u;
+      mbar_arrive_expect_tx(&hd.a_bar, a_bytes);
+      bulk_g2s(sA, p.A, a_bytes, &hd.a_bar, policy_evict_last());
+    }
   }
   __syncthreads();
   pdl_launch_dependents();
   set_rows(hd.row0, hd.nrows);
 
   if (warp < active && nrows > 0) {
-    // One lead thread waits for A under the time limit; the other consumers
-    // follow its verdict (a named barrier has no time limit, so every
-    // consumer has to reach it) and then observe the landed copy themselves.
-    if (threadIdx.x == 0 && !mbar_wait(&hd.a_bar, 0, p.wait_ns, p.wait_iters)) {
-      record_error(kDevErrTimeout);
-      hd.abort = 1;
-    }
-    named_barrier(1, static_cast<uint32_t>(active) * 32u);
-    if (!hd.abort) {
-      if (threadIdx.x != 0) mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
-      pdl_wait();  // returns at once: the previous kernel has completed
-      const uint64_t pol = policy_evict_first();
-      if (FMT != LQ_FMT_F16) {
-        // staging (M rows) -> block slots, token by token
-        const uint32_t sa = smem_u32(sA), sg = smem_u32(stage_a);
-        const int per = p.K / 4;
-        for (int t = 0; t < p.M; ++t)
-          for (int q = warp * 32 + lane; q < per; q += active * 32) {
-            const uint4 v = lds128(sg + 16u * (t * per + q));
-            const uint32_t blk =
-                sa + static_cast<uint32_t>(t * p.a_slot) + static_cast<uint32_t>(a_slot_q(q >> 3)) * kASlotBytes;
-            if (p.a_perm)
-              q4i::store_chunk(blk, q & 7, v);
-            else
-              sts128(blk + 16u * (q & 7), v);
-          }
-        named_barrier(2, static_cast<uint32_t>(active) * 32u);
-        if (threadIdx.x == 0) {
-          // the staging area is free: the slots it covered get their stages
-          fence_proxy_async_smem();
-          for (int st = p.early; st < min(nst, S); ++st) issue(st, st, pol);
+    if (FMT == LQ_FMT_F16) {
+      // One lead thread waits for the copy of A under the time limit; the
+      // other consumers follow its verdict (a named barrier has no time
+      // limit, so every consumer has to reach it) and then observe the
+      // landed copy themselves.
+      if (threadIdx.x == 0 && !mbar_wait(&hd.a_bar, 0, p.wait_ns, p.wait_iters)) {
+        record_error(kDevErrTimeout);
+        hd.abort = 1;
+      }
+      named_barrier(1, static_cast<uint32_t>(active) * 32u);
+      if (!hd.abort && threadIdx.x != 0) mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
+    } else {
+      // A (M rows) straight from global memory into the block slots the
+      // slices read, once the previous kernel on the stream completed: each
+      // thread issues up to 16 loads of 16 bytes before storing any
+      pdl_wait();
+      const uint32_t sa = smem_u32(sA);
+      const int per = p.K / 4, total = p.M * per, nthr = active * 32;
+      const float* A = p.A;
+#pragma unroll 1
+      for (int q0 = warp * 32 + lane; q0 < total; q0 += 16 * nthr) {
+        float4 v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int q = q0 + u * nthr;
+          if (q < total && LQ_IN_BOUNDS(q >= 0)) v[u] = ldg128f(A + 4LL * q);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int q = q0 + u * nthr;
+          if (q >= total) break;
+          const int t = q / per, c = q - t * per;
+          const uint32_t blk =
+              sa + static_cast<uint32_t>(t * p.a_slot) + static_cast<uint32_t>(a_slot_q(c >> 3)) * kASlotBytes;
+          const uint4 w = make_uint4(__float_as_uint(v[u].x), __float_as_uint(v[u].y), __float_as_uint(v[u].z),
+                                     __float_as_uint(v[u].w));
+          if (p.a_perm)
+            q4i::store_chunk(blk, c & 7, w);
+          else
+            sts128(blk + 16u * (c & 7), w);
         }
       }
+      named_barrier(2, static_cast<uint32_t>(active) * 32u);
+    }
+    if (!hd.abort) {
+      pdl_wait();  // returns at once: the previous kernel has completed
+      const uint64_t pol = policy_evict_first();
       const int kg = warp % nk, rg = warp / nk;
       typename SliceM<FMT, MT>::T sl;
       sl.init(smem_u32(sA), static_cast<uint32_t>(p.a_slot), kg, lane, p.K);
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s)
       if (hd.last[s] >= 0) mbar_wait(&hd.full[s], (hd.last[s] / S) & 1, kDrainWaitNs);
-    mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
+    if (FMT == LQ_FMT_F16) mbar_wait(&hd.a_bar, 0, kDrainWaitNs);
   }
 }
 
@@ -394,11 +409,10 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   const int max_rows = swiglu ? kBRows / 2 : kBRows;
   const int a_slot = a.fmt == LQ_FMT_F16 ? static_cast<int>(K * 4)
                                          : static_cast<int>((K / 32 + 63) / 64) * 64 * kASlotBytes;
-  const int a_stage = a.fmt == LQ_FMT_F16 ? 0 : static_cast<int>((M * K * 4 + 127) / 128 * 128);
   const int hdr = MT == 2 ? batch_header_bytes<2>() : (MT == 4 ? batch_header_bytes<4>() : batch_header_bytes<8>());
   const int budget = std::min(di.max_smem_optin, 227 * 1024) - hdr - MT * a_slot;
   const int rows_per_cta = static_cast<int>((N + G - 1) / G);
-  if (budget < 2 * rb || budget < a_stage) return LQ_ERR_UNSUPPORTED;
+  if (budget < 2 * rb) return LQ_ERR_UNSUPPORTED;
   // Stage height: as large as 8 rows while two stages fit; then as many
   // row-groups as there are stages (up to the warps over the K-groups), and
   // the height balanced so that every row-group gets the same number of
@@ -416,7 +430,7 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   S -= S % nr;
   S = std::min(S, nr * ((need + nr - 1) / nr));
   if (S < 1) return LQ_ERR_UNSUPPORTED;
-  const int ring = std::max(S * RS * rb, a_stage);
+  const int ring = S * RS * rb;
   BatchParams p = {};
   p.A = a.A;
   p.W = static_cast<const uint8_t*>(a.W);
@@ -433,10 +447,6 @@ lq_status launch_gemv_batch(const MatmulArgs& a) {
   p.nr = nr;
   p.stages = S;
   p.a_slot = a_slot;
-  // A staging at the top of the ring (128-byte aligned): the slots wholly
-  // below it are issued at once, the others after A has been spread out
-  p.stage_off = a_stage ? (ring - a_stage) / 128 * 128 : 0;
-  p.early = a_stage ? std::min(S, p.stage_off / (RS * rb)) : S;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   const size_t smem = static_cast<size_t>(hdr) + MT * static_cast<size_t>(a_slot) + ring;

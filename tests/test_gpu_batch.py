@@ -68,20 +68,14 @@ def test_batch_ring_refills(lq, cuda_dev, fmt, M, N, K):
 @pytest.mark.parametrize("fmt,K", [("f16", 1000), ("f16", 2048), ("q8_0", 4096), ("q4_0", 4096),
                                    ("q8_0", 8192), ("q4_0", 8192)])
 def test_batch_k_limits(lq, cuda_dev, fmt, K):
-    # M = 2 fits up to the limit; K = 8192 with four rows of A does not fit
-    # shared memory (activations kept twice) and falls back to the tensor cores
+    # two and four rows of A fit up to the largest K of the warp grid (eight
+    # K-groups: 2048 f16, 8192 quantised)
     for M in (2, 4):
         W, A = synthetic.draw(M, 1536, K, seed=K + M, outlier_frac=0.05 if K % 32 == 0 else 0.0)
         lq.reset_counts()
         C = _run(lq, cuda_dev, fmt, W, A)
-        fits = not (M == 4 and K == 8192)
-        if fits:
-            y, tol = _ref(fmt, W, A)
-            assert lq.route_count(1) == 1
-        else:
-            N = W.shape[0]
-            y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
-            assert lq.route_count(1) == 0
+        y, tol = _ref(fmt, W, A)
+        assert lq.route_count(1) == 1
         check(C, y, tol, f"{fmt} {M}x1536x{K}")
 
 
@@ -108,12 +102,13 @@ def test_batch_unaligned_a_falls_back(lq, cuda_dev):
     assert lq.route_count(1) == 0
 
 
-@pytest.mark.parametrize("fmt,K,fits", [("q8_0", 2048, True), ("q8_0", 3072, False),
-                                        ("q4_0", 2048, True), ("q4_0", 4096, False),
+@pytest.mark.parametrize("fmt,K,fits", [("q8_0", 2048, True), ("q8_0", 4096, True), ("q8_0", 8192, False),
+                                        ("q4_0", 3072, True), ("q4_0", 8192, False),
                                         ("f16", 2048, True), ("f16", 2304, False)])
 def test_batch_eight_rows_k_limits(lq, cuda_dev, fmt, K, fits):
-    """Eight rows of A up to K = 2048 (the activations' block slots and the
-    staged copy share shared memory); larger K goes to the tensor cores."""
+    """Eight rows of A up to K = 4096 quantised (half-block K-groups: four per
+    64-block segment, eight at most) and 2048 f16; larger K goes to the
+    tensor cores."""
     M, N = 8, 1536
     W, A = synthetic.draw(M, N, K, seed=K + 8, outlier_frac=0.05)
     lq.reset_counts()
