@@ -66,6 +66,7 @@ struct TmaGemmParams {
   const float* R;      // residual epilogue: added to every output
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
+  int bn;              // W rows per tile (multiple of 16, <= 128; TMEM lanes bn.. hold zeros)
   int split;           // CTAs splitting K for one output tile (1: no split)
   int n_tiles;         // output tiles along N (the tile of CTA (x, y) is y * n_tiles + x / split)
   float* part;         // split > 1: each rank's partial tile, [rank][tile][token][128 rows] f32
@@ -256,7 +257,7 @@ __device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t 
 template <int FMT, int EPI>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
                                            int bt, int c0) {
-  const int n = n0 + r;
+  const int n = r < p.bn ? n0 + r : p.N;  // lanes past the tile's rows store nothing
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int c = c0 + 2 * i;
@@ -316,7 +317,7 @@ __device__ __forceinline__ void reduce_partials(const TmaGemmParams& p, const fl
                                                 int split, int n0, int m0, int bt, int t) {
   const int r = t & (kBN - 1), h = t >> 7;
   const int n = n0 + r;
-  if (n >= p.N) return;
+  if (n >= p.N || r >= p.bn) return;
 #pragma unroll 1
   for (int t0 = h; t0 < bt; t0 += 64) {
     float sum[32];
@@ -392,7 +393,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
   // the CTA, the K coordinates of its loads add ks0.
   const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
-  const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : kBN), m0 = blockIdx.y * bt;
+  const int BN = p.bn;  // W rows of the tile (swiglu: 64 gate + 64 up rows, BN = 128)
+  const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : BN), m0 = blockIdx.y * bt;
   const int nraw_all = p.K / kKS / SUB;
   const int jr0 = rank * nraw_all / split;
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   // one raw W stage into ring slot `slot` (producer lane 0)
   auto issue_raw = [&](int j, int slot) {
-    mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
+    mbar_arrive_expect_tx(&b.raw_full[slot], static_cast<uint32_t>(kRowBytes<FMT> * BN));
     if (FMT == LQ_FMT_F16) {
       for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
         if constexpr (SWIGLU)
@@ -556,9 +558,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
       const uint32_t tcol = tmem + tlane + kWCol0 + 64u * st;
       uint32_t out[32];
-      convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
+      // lanes past the tile's BN rows feed zeros to the MMA (their raw rows
+      // were not copied)
+      if (r < BN) {
+        convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) out[i] = 0u;
+      }
       tc::st_32x32b_x32(tcol, out);
-      convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
+      if (r < BN) convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
       tc::st_32x32b_x32(tcol + 32u, out);
       tc::wait_st();
       tc::fence_before_sync();
@@ -790,7 +799,7 @@ template <int FMT, int EPI>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              TmaGemmParams p) {
   auto kern = gemm_tma_kernel<FMT, EPI>;
-  const int bn = EPI == epi::kSwiglu ? kBN / 2 : kBN;  // outputs per tile
+  const int bn = EPI == epi::kSwiglu ? kBN / 2 : p.bn;  // outputs per tile
   const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
@@ -879,9 +888,22 @@ TmaPlan gemm_tma_plan(const MatmulArgs& a) {
   const bool sw = a.epi == epi::kSwiglu;
   // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
   pl.bt = pick_bt(a.M, sw ? 2 * a.N : a.N);
-  const int bn = sw ? kBN / 2 : kBN;
-  pl.n_tiles = static_cast<int>((a.N + bn - 1) / bn);
   pl.m_tiles = static_cast<int>((a.M + pl.bt - 1) / pl.bt);
+  // W rows per tile: 128 (the MMA's M), or, while 128-row tiles would leave
+  // more than half of the SMs idle, fewer rows (a multiple of 16, at least
+  // 32) so that more SMs stream W; the MMA still runs on 128 lanes, the
+  // unused ones holding zeros. Fewer rows beat a split K there: no partial
+  // tiles, no reduction. Swiglu tiles stay at 64 gate + 64 up rows.
+  pl.bn = kBN;
+  const int sms = device_info().sm_count;
+  if (!sw && 2LL * ((a.N + kBN - 1) / kBN) * pl.m_tiles <= sms) {
+    for (int cand = kBN - 16; cand >= 32; cand -= 16) {
+      if (((a.N + cand - 1) / cand) * pl.m_tiles > sms) break;
+      pl.bn = cand;
+    }
+  }
+  const int bn = sw ? kBN / 2 : pl.bn;
+  pl.n_tiles = static_cast<int>((a.N + bn - 1) / bn);
   const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles;
   pl.split = sw ? 1 : pick_split(tiles, static_cast<int>(a.K / kstep_multiple(a.fmt)));
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
@@ -932,7 +954,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
     cuuint64_t dims[3] = {f16 ? static_cast<cuuint64_t>(K) : rb / 4, static_cast<cuuint64_t>(N), 2};
     cuuint64_t strides[2] = {rb, rb * static_cast<cuuint64_t>(N)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(f16 ? 64 : (a.fmt == LQ_FMT_Q8_0 ? 68 : 36)),
-                         static_cast<cuuint32_t>(sw ? kBN / 2 : kBN), 2};
+                         static_cast<cuuint32_t>(sw ? kBN / 2 : pl.bn), 2};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tmW, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, rank,
             const_cast<void*>(a.W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -957,6 +979,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
   p.N = N;
   p.K = K;
   p.bt = bt;
+  p.bn = a.epi == epi::kSwiglu ? kBN : pl.bn;
   p.split = pl.split;
   p.n_tiles = pl.n_tiles;
   p.part = pl.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off) : nullptr;

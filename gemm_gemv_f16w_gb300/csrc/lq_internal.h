@@ -68,7 +68,7 @@ lq_status launch_gemm_tma(const MatmulArgs& a);
 // The call's token tile, K split and workspace layout: the bf16 copy of A at
 // offset 0, then (split > 1) the ranks' partial tiles and the tiles' counters.
 struct TmaPlan {
-  int bt = 0, split = 1, n_tiles = 0, m_tiles = 0;
+  int bt = 0, bn = 128, split = 1, n_tiles = 0, m_tiles = 0;
   size_t part_off = 0, cnt_off = 0, ws_bytes = 0;
 };
 TmaPlan gemm_tma_plan(const MatmulArgs& a);
