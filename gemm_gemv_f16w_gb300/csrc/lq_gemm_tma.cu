@@ -51,8 +51,8 @@ constexpr int kNumConv = 8;                        // converter warps (2 groups 
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
-constexpr int kMaxStages = 4, kMaxRawStages = 8;
-constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
+constexpr int kMaxAStages = 16, kWStages = 4, kMaxRawStages = 8;
+constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 512)
 constexpr uint32_t kWCol0 = 256;
 
 // Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
@@ -71,7 +71,7 @@ struct TmaGemmParams {
   int n_tiles;         // output tiles along N (the tile of CTA (x, y) is y * n_tiles + x / split)
   float* part;         // split > 1: each rank's partial tile, [rank][tile][token][128 rows] f32
   unsigned* cnt;       // split > 1: ranks done per tile (zeroed by the pre-pass)
-  int stages;          // pipeline depth (2..kMaxStages)
+  int stages;          // A-tile ring depth (2..kMaxAStages)
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
@@ -79,8 +79,10 @@ struct TmaGemmParams {
 
 struct Bars {
   uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
-  uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
-  uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
+  uint64_t a_full[kMaxAStages];   // A tile landed (TMA bytes)
+  uint64_t a_empty[kMaxAStages];  // the MMAs that read it completed (commit)
+  uint64_t w_full[kWStages];      // the group's 4 converter warps wrote the W operand into TMEM
+  uint64_t w_empty[kWStages];     // the MMAs that read it completed (commit)
   uint64_t tmem_full;
   uint32_t tmem_base;
   volatile int abort;
@@ -375,17 +377,20 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     const TmaGemmParams p) {
   constexpr int SUB = kSub<FMT>;
   constexpr bool SWIGLU = EPI == epi::kSwiglu;
-  constexpr int kRawBytes = kRowBytes<FMT> * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
-  const int bt = p.bt, S = p.stages;
+  const int bt = p.bt, SA = p.stages;
   const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
-  uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
+  uint8_t* a_ring = base;                                          // SA x A tiles (swizzled)
   const int RR = p.raw_stages;
-  uint8_t* w_ring = base + S * a_stage_bytes;                      // RR x raw W stages
+  // W rows of the tile (swiglu: 64 gate + 64 up rows, BN = 128); a raw
+  // stage holds BN rows (f16: two 128-byte-swizzled boxes of BN x 128 bytes)
+  const int BN = p.bn;
+  const int kRawBytes = kRowBytes<FMT> * BN;
+  uint8_t* w_ring = base + SA * a_stage_bytes;                     // RR x raw W stages
   Bars& b = *reinterpret_cast<Bars*>(w_ring + RR * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -393,7 +398,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
   // the CTA, the K coordinates of its loads add ks0.
   const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
-  const int BN = p.bn;  // W rows of the tile (swiglu: 64 gate + 64 up rows, BN = 128)
   const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : BN), m0 = blockIdx.y * bt;
   const int nraw_all = p.K / kKS / SUB;
   const int jr0 = rank * nraw_all / split;
@@ -402,17 +406,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   // one raw W stage into ring slot `slot` (producer lane 0)
   auto issue_raw = [&](int j, int slot) {
-    mbar_arrive_expect_tx(&b.raw_full[slot], static_cast<uint32_t>(kRowBytes<FMT> * BN));
+    mbar_arrive_expect_tx(&b.raw_full[slot], static_cast<uint32_t>(kRawBytes));
     if (FMT == LQ_FMT_F16) {
-      for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
+      for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x BN rows (128B-swizzled)
         if constexpr (SWIGLU)
-          tc::tma_load_3d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
+          tc::tma_load_3d(w_ring + slot * kRawBytes + h * (BN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
                           &b.raw_full[slot]);
         else
-          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
+          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (BN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
                           &b.raw_full[slot]);
       }
-    } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
+    } else {  // one box of (row bytes of 256 K) / 4 words x BN rows
       if constexpr (SWIGLU)
         tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
                         &b.raw_full[slot]);
@@ -426,9 +430,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(&b.raw_full[i], 1);
       mbar_init(&b.raw_empty[i], 4 * SUB);
     }
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&b.full[i], 1 + 4);
-      mbar_init(&b.empty[i], 1);
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(&b.a_full[i], 1);
+      mbar_init(&b.a_empty[i], 1);
+    }
+    for (int i = 0; i < kWStages; ++i) {
+      mbar_init(&b.w_full[i], 4);
+      mbar_init(&b.w_empty[i], 1);
     }
     mbar_init(&b.tmem_full, 1);
     b.abort = 0;
@@ -455,7 +463,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     int raw_issued = min(nraw, RR), issued = 0;  // the first raw stages are in flight (prologue)
     bool ok = true;
     pdl_wait();
-    int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
+    int st = 0, lap = 0, rslot = 0, rlap = 0;  // A ring / raw ring positions
     for (int ks = 0; ks < nk; ++ks) {
       if (ks % SUB == 0 && ks / SUB >= RR) {
         const int j = ks / SUB;  // reuse raw slot j % 2 after both of its users finished
@@ -468,19 +476,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ++raw_issued;
         if (++rslot == RR) { rslot = 0; ++rlap; }
       }
-      if (ks >= S && (!warp_wait(&b.empty[st], (lap - 1) & 1, p) || b.abort)) {
+      if (ks >= SA && (!warp_wait(&b.a_empty[st], (lap - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.full[st]);
+        mbar_arrive_expect_tx(&b.a_full[st], a_stage_bytes);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.a_full[st]);
         tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, m0,
-                        &b.full[st]);
+                        &b.a_full[st]);
       }
       __syncwarp();
       ++issued;
-      if (++st == S) { st = 0; ++lap; }
+      if (++st == SA) { st = 0; ++lap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
@@ -489,48 +497,45 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // never leave copies in flight (waits for the last use of every slot)
     for (int j = max(0, raw_issued - RR); j < raw_issued; ++j)
       mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
-    for (int ks = max(0, issued - S); ks < issued; ++ks)
-      mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
+    for (int ks = max(0, issued - SA); ks < issued; ++ks)
+      mbar_wait(&b.a_full[ks % SA], (ks / SA) & 1, kDrainWaitNs);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    // stage ks: A tile in ring slot ks % SA, W operand in TMEM slot ks % 4;
+    // both slots go back to their producers with one commit each
     const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
-    int st = 0, lap = 0;
-    auto issue_stage = [&](int ks, int sst) {
-      const uint32_t abase = smem_u32(a_ring + sst * a_stage_bytes);
-      const uint32_t wcol = tmem + kWCol0 + 64u * sst;
+    auto ready = [&](int ks) {
+      return mbar_test_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1) &&
+             mbar_test_wait(&b.w_full[ks % kWStages], static_cast<uint32_t>(ks / kWStages) & 1);
+    };
+    auto issue_stage = [&](int ks) {
+      const int sa = ks % SA, sw = ks % kWStages;
+      const uint32_t abase = smem_u32(a_ring + sa * a_stage_bytes);
+      const uint32_t wcol = tmem + kWCol0 + 64u * sw;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
         tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
       }
-      tc::commit(&b.empty[sst]);
+      tc::commit(&b.a_empty[sa]);
+      tc::commit(&b.w_empty[sw]);
     };
     for (int ks = 0; ks < nk;) {
-      if (!warp_wait(&b.full[st], lap & 1, p)) {
+      if (!warp_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1, p) ||
+          !warp_wait(&b.w_full[ks % kWStages], static_cast<uint32_t>(ks / kWStages) & 1, p)) {
         ok = false;
         break;
       }
       // Issue this stage and, without a blocking wait, any following stages
-      // that are already complete (the pipeline usually runs ahead).
+      // whose operands are already in place (the pipeline usually runs ahead).
       int cnt = 1;
-      int st2 = st + 1 == S ? 0 : st + 1, lap2 = st + 1 == S ? lap + 1 : lap;
-      while (ks + cnt < nk && cnt < S - 1 && __all_sync(0xffffffffu, mbar_test_wait(&b.full[st2], lap2 & 1))) {
-        ++cnt;
-        if (++st2 == S) { st2 = 0; ++lap2; }
-      }
+      while (ks + cnt < nk && cnt < kWStages - 1 && __all_sync(0xffffffffu, ready(ks + cnt))) ++cnt;
       tc::fence_after_sync();
-      if (lane == 0) {
-        int sst = st;
-        for (int i = 0; i < cnt; ++i) {
-          issue_stage(ks + i, sst);
-          if (++sst == S) sst = 0;
-        }
-      }
+      if (lane == 0)
+        for (int i = 0; i < cnt; ++i) issue_stage(ks + i);
       __syncwarp();
       ks += cnt;
-      for (int i = 0; i < cnt; ++i)
-        if (++st == S) { st = 0; ++lap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
@@ -546,12 +551,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
     for (int ks = g; ks < nk; ks += 2) {
-      const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % RR;
+      const int j = ks / SUB, half = ks % SUB, st = ks % kWStages, rslot = j % RR;
       if (!warp_wait(&b.raw_full[rslot], (j / RR) & 1, p) || b.abort) {
         ok = false;
         break;
       }
-      if (ks >= S && (!warp_wait(&b.empty[st], ((ks / S) - 1) & 1, p) || b.abort)) {
+      if (ks >= kWStages && (!warp_wait(&b.w_empty[st], ((ks / kWStages) - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&b.full[st]);
+        mbar_arrive(&b.w_full[st]);
         mbar_arrive(&b.raw_empty[rslot]);
       }
     }
@@ -718,28 +723,31 @@ int pick_bt(int64_t M, int64_t N) {
   return static_cast<int>(std::min<int64_t>(256, (per + 15) / 16 * 16));
 }
 
-int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
+int raw_stage_bytes(int fmt, int bn) { return bn * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
 
-// Ring depths for a token tile of bt: the raw W ring first (W comes from
-// HBM: up to 6 raw stages of f16, 4 of Q8_0 / Q4_0, i.e. 6 to 8 pipeline
-// stages of lookahead), then as many A stages (bt rows x 128 K halves, from
-// L2) as fit, at least two of each; where that leaves two A stages, three A
-// stages over fewer raw stages.
+// Ring depths for a token tile of bt and W tiles of bn rows: the raw W ring
+// first (W comes from HBM: about 140 KB (Q8_0, Q4_0) to 190 KB (f16) of a
+// 128-row tile in flight, i.e. up to 4 or 6 raw stages, more of narrower
+// tiles, at most 8), then as many A stages (bt rows x 128 K bf16, from L2)
+// as fit, up to 16, at least two of each; where that leaves two A stages,
+// three A stages over fewer raw stages. The A ring is separate from the four
+// TMEM slots of the W operand, so small token tiles keep many A stages in
+// flight.
 struct RingPlan {
   int a_stages = 0, raw_stages = 0;
 };
 std::atomic<int> g_ring_a{0}, g_ring_raw{0};  // debug override (0 = automatic)
 
-RingPlan ring_plan(int fmt, int bt) {
+RingPlan ring_plan(int fmt, int bt, int bn) {
   const DeviceInfo& di = device_info();
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
                            static_cast<long long>(sizeof(Bars)) - 64;
-  const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt);
+  const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt, bn);
   RingPlan rp;
-  const int raw_cap = fmt == LQ_FMT_F16 ? 6 : 4;
+  const int raw_cap = std::min(kMaxRawStages, (fmt == LQ_FMT_F16 ? 6 : 4) * kBN / bn);
   rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 2 * a_stage) / raw));
   if (rp.raw_stages < 2) return RingPlan{};
-  rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
+  rp.a_stages = static_cast<int>(std::min<long long>(kMaxAStages, (budget - rp.raw_stages * raw) / a_stage));
   if (rp.a_stages < 2) return RingPlan{};
   // Large token tiles leave room for two A stages only: three A stages over
   // two raw stages measured about 5 % faster at M = 512 (f16 and Q8_0).
@@ -750,15 +758,15 @@ RingPlan ring_plan(int fmt, int bt) {
   const int oa = g_ring_a.load(), orr = g_ring_raw.load();
   if (oa || orr) {
     const int a2 = oa ? oa : rp.a_stages, r2 = orr ? orr : rp.raw_stages;
-    if (a2 >= 2 && a2 <= kMaxStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
+    if (a2 >= 2 && a2 <= kMaxAStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
       return RingPlan{a2, r2};
   }
   return rp;
 }
 
-size_t tma_smem_bytes(int fmt, int bt, int a_stages, int raw_stages) {
+size_t tma_smem_bytes(int fmt, int bt, int bn, int a_stages, int raw_stages) {
   const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 256 +
-                      static_cast<size_t>(raw_stages) * raw_stage_bytes(fmt) + sizeof(Bars) + 64;
+                      static_cast<size_t>(raw_stages) * raw_stage_bytes(fmt, bn) + sizeof(Bars) + 64;
   // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
   return std::max<size_t>(need, 116 * 1024);
 }
@@ -800,7 +808,7 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
                              TmaGemmParams p) {
   auto kern = gemm_tma_kernel<FMT, EPI>;
   const int bn = EPI == epi::kSwiglu ? kBN / 2 : p.bn;  // outputs per tile
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.bn, p.stages, p.raw_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -837,7 +845,7 @@ bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
   if (!encode_fn()) return false;
   const DeviceInfo& di = device_info();
-  return di.cc_major >= 10 && ring_plan(a.fmt, 256).a_stages >= 2;
+  return di.cc_major >= 10 && ring_plan(a.fmt, 256, kBN).a_stages >= 2;
 }
 
 // The library's own stream-ordered memory pool on the current device: freed
@@ -985,7 +993,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
   p.part = pl.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off) : nullptr;
   p.cnt = cnt;
   {
-    const RingPlan rp = ring_plan(a.fmt, bt);
+    const RingPlan rp = ring_plan(a.fmt, bt, p.bn);
     p.stages = rp.a_stages;
     p.raw_stages = rp.raw_stages;
   }
