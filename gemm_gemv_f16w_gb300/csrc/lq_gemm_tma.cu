@@ -164,10 +164,11 @@ __global__ void __launch_bounds__(kPreThreads) a_to_bf16_kernel(const float* __r
 // f16 weights widen exactly. cvt.rn.bf16x2.f32 then rounds to nearest even.
 // ---------------------------------------------------------------------------
 template <int FMT, int SUB>
-__device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t box_bytes, uint32_t (&out)[32]) {
   if constexpr (FMT == LQ_FMT_F16) {
-    // box SUB: 128 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)
-    const uint32_t row = stage + SUB * (kBN * 128u) + r * 128u;
+    // box SUB: BN rows x 128 bytes (box_bytes), 16-byte chunk c of row r at
+    // chunk c ^ (r % 8)
+    const uint32_t row = stage + SUB * box_bytes + r * 128u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint4 v = lds128(row + ((static_cast<uint32_t>(i) ^ (r & 7u)) << 4));
@@ -244,12 +245,13 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (
 }
 
 template <int FMT>
-__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t box_bytes,
+                                              uint32_t (&out)[32]) {
   switch (sub) {
-    case 0: convert64<FMT, 0>(stage, r, out); break;
-    case 1: convert64<FMT, 1>(stage, r, out); break;
-    case 2: convert64<FMT, 2>(stage, r, out); break;
-    default: convert64<FMT, 3>(stage, r, out); break;
+    case 0: convert64<FMT, 0>(stage, r, box_bytes, out); break;
+    case 1: convert64<FMT, 1>(stage, r, box_bytes, out); break;
+    case 2: convert64<FMT, 2>(stage, r, box_bytes, out); break;
+    default: convert64<FMT, 3>(stage, r, box_bytes, out); break;
   }
 }
 
@@ -565,14 +567,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       uint32_t out[32];
       // lanes past the tile's BN rows feed zeros to the MMA (their raw rows
       // were not copied)
+      const uint32_t box_bytes = static_cast<uint32_t>(BN) * 128u;  // f16: one 64-K box of the raw stage
       if (r < BN) {
-        convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
+        convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), box_bytes, out);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) out[i] = 0u;
       }
       tc::st_32x32b_x32(tcol, out);
-      if (r < BN) convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
+      if (r < BN) convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), box_bytes, out);
       tc::st_32x32b_x32(tcol + 32u, out);
       tc::wait_st();
       tc::fence_before_sync();
