@@ -51,9 +51,8 @@ constexpr int kNumConv = 8;                        // converter warps (2 groups 
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
-constexpr int kMaxAStages = 16, kWStages = 4, kMaxRawStages = 8;
-constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 512)
-constexpr uint32_t kWCol0 = 256;
+constexpr int kMaxAStages = 16, kMaxWStages = 7, kMaxRawStages = 8;
+constexpr uint32_t kTmemCols = 512;                // D: [0, bt), W slots: 64 columns each above it
 
 // Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
 // formats: 256 K in one box; f16: 128 K as two boxes of 64 K, each 128 rows
@@ -73,6 +72,8 @@ struct TmaGemmParams {
   unsigned* cnt;       // split > 1: ranks done per tile (zeroed by the pre-pass)
   int stages;          // A-tile ring depth (2..kMaxAStages)
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
+  int w_stages;        // TMEM slots of the W operand (2..kMaxWStages)
+  int w_col0;          // TMEM column of the first W slot (>= bt, a multiple of 64)
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
@@ -81,8 +82,8 @@ struct Bars {
   uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
   uint64_t a_full[kMaxAStages];   // A tile landed (TMA bytes)
   uint64_t a_empty[kMaxAStages];  // the MMAs that read it completed (commit)
-  uint64_t w_full[kWStages];      // the group's 4 converter warps wrote the W operand into TMEM
-  uint64_t w_empty[kWStages];     // the MMAs that read it completed (commit)
+  uint64_t w_full[kMaxWStages];   // the group's 4 converter warps wrote the W operand into TMEM
+  uint64_t w_empty[kMaxWStages];  // the MMAs that read it completed (commit)
   uint64_t tmem_full;
   uint32_t tmem_base;
   volatile int abort;
@@ -383,7 +384,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
-  const int bt = p.bt, SA = p.stages;
+  const int bt = p.bt, SA = p.stages, SW = p.w_stages;
+  const uint32_t wcol0 = static_cast<uint32_t>(p.w_col0);
   const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
   uint8_t* a_ring = base;                                          // SA x A tiles (swizzled)
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(&b.a_full[i], 1);
       mbar_init(&b.a_empty[i], 1);
     }
-    for (int i = 0; i < kWStages; ++i) {
+    for (int i = 0; i < SW; ++i) {
       mbar_init(&b.w_full[i], 4);
       mbar_init(&b.w_empty[i], 1);
     }
@@ -503,18 +505,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_wait(&b.a_full[ks % SA], (ks / SA) & 1, kDrainWaitNs);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // stage ks: A tile in ring slot ks % SA, W operand in TMEM slot ks % 4;
+    // stage ks: A tile in ring slot ks % SA, W operand in TMEM slot ks % SW;
     // both slots go back to their producers with one commit each
     const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
     auto ready = [&](int ks) {
       return mbar_test_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1) &&
-             mbar_test_wait(&b.w_full[ks % kWStages], static_cast<uint32_t>(ks / kWStages) & 1);
+             mbar_test_wait(&b.w_full[ks % SW], static_cast<uint32_t>(ks / SW) & 1);
     };
     auto issue_stage = [&](int ks) {
-      const int sa = ks % SA, sw = ks % kWStages;
+      const int sa = ks % SA, sw = ks % SW;
       const uint32_t abase = smem_u32(a_ring + sa * a_stage_bytes);
-      const uint32_t wcol = tmem + kWCol0 + 64u * sw;
+      const uint32_t wcol = tmem + wcol0 + 64u * sw;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
@@ -525,14 +527,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     };
     for (int ks = 0; ks < nk;) {
       if (!warp_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1, p) ||
-          !warp_wait(&b.w_full[ks % kWStages], static_cast<uint32_t>(ks / kWStages) & 1, p)) {
+          !warp_wait(&b.w_full[ks % SW], static_cast<uint32_t>(ks / SW) & 1, p)) {
         ok = false;
         break;
       }
       // Issue this stage and, without a blocking wait, any following stages
       // whose operands are already in place (the pipeline usually runs ahead).
       int cnt = 1;
-      while (ks + cnt < nk && cnt < kWStages - 1 && __all_sync(0xffffffffu, ready(ks + cnt))) ++cnt;
+      while (ks + cnt < nk && cnt < SW - 1 && __all_sync(0xffffffffu, ready(ks + cnt))) ++cnt;
       tc::fence_after_sync();
       if (lane == 0)
         for (int i = 0; i < cnt; ++i) issue_stage(ks + i);
@@ -553,17 +555,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
     for (int ks = g; ks < nk; ks += 2) {
-      const int j = ks / SUB, half = ks % SUB, st = ks % kWStages, rslot = j % RR;
+      const int j = ks / SUB, half = ks % SUB, st = ks % SW, rslot = j % RR;
       if (!warp_wait(&b.raw_full[rslot], (j / RR) & 1, p) || b.abort) {
         ok = false;
         break;
       }
-      if (ks >= kWStages && (!warp_wait(&b.w_empty[st], ((ks / kWStages) - 1) & 1, p) || b.abort)) {
+      if (ks >= SW && (!warp_wait(&b.w_empty[st], ((ks / SW) - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
       const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
-      const uint32_t tcol = tmem + tlane + kWCol0 + 64u * st;
+      const uint32_t tcol = tmem + tlane + wcol0 + 64u * st;
       uint32_t out[32];
       // lanes past the tile's BN rows feed zeros to the MMA (their raw rows
       // were not copied)
@@ -999,6 +1001,13 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
     const RingPlan rp = ring_plan(a.fmt, bt, p.bn);
     p.stages = rp.a_stages;
     p.raw_stages = rp.raw_stages;
+    // W slots above the accumulator's bt columns: as deep as the A ring for
+    // large token tiles (the tensor pipe is the limit there), up to seven
+    // for small ones (the converter -> MMA -> commit round trip is)
+    p.w_col0 = (bt + 63) / 64 * 64;
+    p.w_stages = std::max(2, std::min({kMaxWStages, (static_cast<int>(kTmemCols) - p.w_col0) / 64,
+                                       std::max(p.stages, bt <= 64 ? kMaxWStages : 4)}));
+    if (bt > 128) p.w_stages = std::min(p.w_stages, p.stages);
   }
   if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();
