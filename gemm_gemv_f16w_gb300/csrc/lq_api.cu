@@ -353,7 +353,7 @@ void lq_debug_reset_counts(void) {
 }
 void lq_debug_set_wait_limit_ns(uint64_t ns) { g_wait_ns.store(ns); }
 lq_status lq_debug_gemm_rings(int a_stages, int raw_stages) {
-  if (a_stages < 0 || a_stages > 16 || raw_stages < 0 || raw_stages > 8) return LQ_ERR_INVALID_ARG;
+  if (a_stages < 0 || a_stages > 4 || raw_stages < 0 || raw_stages > 8) return LQ_ERR_INVALID_ARG;
   lq::set_gemm_rings(a_stages, raw_stages);
   return LQ_OK;
 }

@@ -34,7 +34,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "lq_device.cuh"
 #include "lq_epilogue.cuh"
@@ -51,8 +53,9 @@ constexpr int kNumConv = 8;                        // converter warps (2 groups 
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
-constexpr int kMaxAStages = 16, kMaxWStages = 7, kMaxRawStages = 8;
-constexpr uint32_t kTmemCols = 512;                // D: [0, bt), W slots: 64 columns each above it
+constexpr int kMaxStages = 4, kMaxRawStages = 8;
+constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
+constexpr uint32_t kWCol0 = 256;
 
 // Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
 // formats: 256 K in one box; f16: 128 K as two boxes of 64 K, each 128 rows
@@ -65,29 +68,20 @@ struct TmaGemmParams {
   const float* R;      // residual epilogue: added to every output
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
-  int bn;              // W rows per tile (multiple of 16, <= 128; TMEM lanes bn.. hold zeros)
-  int split;           // CTAs splitting K for one output tile (1: no split)
-  int n_tiles;         // output tiles along N (the tile of CTA (x, y) is y * n_tiles + x / split)
-  float* part;         // split > 1: each rank's partial tile, [rank][tile][token][128 rows] f32
-  unsigned* cnt;       // split > 1: ranks done per tile (zeroed by the pre-pass)
-  int stages;          // A-tile ring depth (2..kMaxAStages)
+  int split;           // CTAs of a cluster splitting K (1: no split)
+  int stages;          // pipeline depth (2..kMaxStages)
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
-  int w_stages;        // TMEM slots of the W operand (2..kMaxWStages)
-  int w_col0;          // TMEM column of the first W slot (>= bt, a multiple of 64)
   unsigned long long wait_ns;
   unsigned wait_iters;
 };
 
 struct Bars {
   uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
-  uint64_t a_full[kMaxAStages];   // A tile landed (TMA bytes)
-  uint64_t a_empty[kMaxAStages];  // the MMAs that read it completed (commit)
-  uint64_t w_full[kMaxWStages];   // the group's 4 converter warps wrote the W operand into TMEM
-  uint64_t w_empty[kMaxWStages];  // the MMAs that read it completed (commit)
+  uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
+  uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
   uint64_t tmem_full;
   uint32_t tmem_base;
   volatile int abort;
-  volatile int last;   // split K: this CTA is the tile's last rank to finish
 };
 
 __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_tma_err, 0u, code); }
@@ -100,17 +94,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 
 // ---------------------------------------------------------------------------
 // Pre-pass: A f32 [M,K] -> bf16 [M,K], every value rounded to nearest even
-// (cvt.rn.bf16x2.f32). Elementwise over chunks of eight (K is a multiple of
-// 128 on this route, so a chunk never straddles a row or a block of 32).
-// With perm (Q4_0 with interleaved nibbles) each block's elements go to the
-// slots of lq_q4i.cuh: element 2j to slot j, 2j+1 to slot 16+j.
-// One CTA of 128 threads per SM: small enough in registers and threads that
-// the GEMM's CTAs, launched early (programmatic dependent launch), fit
-// beside it and stream their first weight stages while it runs. Each thread
-// issues the loads of up to kPreBatch chunks before converting any, so that
-// enough bytes are in flight per SM.
+// (cvt.rn.bf16x2.f32). Elementwise: thread i converts elements 8i .. 8i+7
+// (K is a multiple of 128 on this route, so eight never straddle a row or a
+// block of 32). With perm (Q4_0 with interleaved nibbles) each block's
+// elements go to the slots of lq_q4i.cuh: element 2j to slot j, 2j+1 to
+// slot 16+j.
 // ---------------------------------------------------------------------------
-constexpr int kPreThreads = 128, kPreBatch = 4;
+constexpr int kPreThreads = 256;
 
 __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
@@ -119,38 +109,22 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 __global__ void __launch_bounds__(kPreThreads) a_to_bf16_kernel(const float* __restrict__ A,
                                                                 uint32_t* __restrict__ A16, long long n8,
-                                                                int perm, unsigned* __restrict__ cnt, int ncnt) {
+                                                                int perm) {
   pdl_launch_dependents();
   pdl_wait();
   const long long stride = static_cast<long long>(gridDim.x) * kPreThreads;
-  for (long long i = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i < ncnt; i += stride)
-    cnt[i] = 0u;  // split K: no rank of the GEMM has finished a tile yet
-  for (long long i0 = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i0 < n8;
-       i0 += stride * kPreBatch) {
-    float4 x[kPreBatch], y[kPreBatch];
-#pragma unroll
-    for (int u = 0; u < kPreBatch; ++u) {
-      const long long i = i0 + stride * u;
-      if (i < n8) {
-        x[u] = ldg128f(A + 8 * i);
-        y[u] = ldg128f(A + 8 * i + 4);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kPreBatch; ++u) {
-      const long long i = i0 + stride * u;
-      if (i >= n8) break;
-      if (!perm) {
-        *reinterpret_cast<uint4*>(A16 + 4 * i) = make_uint4(bf16x2(x[u].x, x[u].y), bf16x2(x[u].z, x[u].w),
-                                                             bf16x2(y[u].x, y[u].y), bf16x2(y[u].z, y[u].w));
-      } else {
-        // chunk c of block b: even elements 8c, 8c+2, 8c+4, 8c+6 -> slots
-        // 4c .. 4c+3 (words 2c, 2c+1); odd ones -> slots 16+4c .. (words 8+2c, 9+2c)
-        uint32_t* blk = A16 + 16 * (i >> 2);
-        const int c = static_cast<int>(i & 3);
-        *reinterpret_cast<uint2*>(blk + 2 * c) = make_uint2(bf16x2(x[u].x, x[u].z), bf16x2(y[u].x, y[u].z));
-        *reinterpret_cast<uint2*>(blk + 8 + 2 * c) = make_uint2(bf16x2(x[u].y, x[u].w), bf16x2(y[u].y, y[u].w));
-      }
+  for (long long i = static_cast<long long>(blockIdx.x) * kPreThreads + threadIdx.x; i < n8; i += stride) {
+    const float4 x = ldg128f(A + 8 * i), y = ldg128f(A + 8 * i + 4);
+    if (!perm) {
+      const uint4 o = make_uint4(bf16x2(x.x, x.y), bf16x2(x.z, x.w), bf16x2(y.x, y.y), bf16x2(y.z, y.w));
+      *reinterpret_cast<uint4*>(A16 + 4 * i) = o;
+    } else {
+      // chunk c of block b: even elements 8c, 8c+2, 8c+4, 8c+6 -> slots
+      // 4c .. 4c+3 (words 2c, 2c+1); odd ones -> slots 16+4c .. (words 8+2c, 9+2c)
+      uint32_t* blk = A16 + 16 * (i >> 2);
+      const int c = static_cast<int>(i & 3);
+      *reinterpret_cast<uint2*>(blk + 2 * c) = make_uint2(bf16x2(x.x, x.z), bf16x2(y.x, y.z));
+      *reinterpret_cast<uint2*>(blk + 8 + 2 * c) = make_uint2(bf16x2(x.y, x.w), bf16x2(y.y, y.w));
     }
   }
 }
@@ -165,11 +139,10 @@ __global__ void __launch_bounds__(kPreThreads) a_to_bf16_kernel(const float* __r
 // f16 weights widen exactly. cvt.rn.bf16x2.f32 then rounds to nearest even.
 // ---------------------------------------------------------------------------
 template <int FMT, int SUB>
-__device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t box_bytes, uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
   if constexpr (FMT == LQ_FMT_F16) {
-    // box SUB: BN rows x 128 bytes (box_bytes), 16-byte chunk c of row r at
-    // chunk c ^ (r % 8)
-    const uint32_t row = stage + SUB * box_bytes + r * 128u;
+    // box SUB: 128 rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)
+    const uint32_t row = stage + SUB * (kBN * 128u) + r * 128u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint4 v = lds128(row + ((static_cast<uint32_t>(i) ^ (r & 7u)) << 4));
@@ -246,23 +219,37 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t b
 }
 
 template <int FMT>
-__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t box_bytes,
-                                              uint32_t (&out)[32]) {
+__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
   switch (sub) {
-    case 0: convert64<FMT, 0>(stage, r, box_bytes, out); break;
-    case 1: convert64<FMT, 1>(stage, r, box_bytes, out); break;
-    case 2: convert64<FMT, 2>(stage, r, box_bytes, out); break;
-    default: convert64<FMT, 3>(stage, r, box_bytes, out); break;
+    case 0: convert64<FMT, 0>(stage, r, out); break;
+    case 1: convert64<FMT, 1>(stage, r, out); break;
+    case 2: convert64<FMT, 2>(stage, r, out); break;
+    default: convert64<FMT, 3>(stage, r, out); break;
   }
 }
 
+// ---------------------------------------------------------------------------
+// Split-K support: cluster barrier and loads from a peer CTA's shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+  return v;
+}
+
 // Epilogue of one TMEM lane (W row r of the tile): the accumulator columns
-// of 32-column chunks c0, c0 + 2, ..., stored to C[m0 + j, n0 + r] (with R
-// added for the residual epilogue).
+// of 32-column chunks c0, c0 + 2, ..., plus the partial tiles of peers
+// 1 .. split-1 (token-major f32 at `red` in their shared memory) when
+// split > 1, stored to C[m0 + j, n0 + r].
 template <int FMT, int EPI>
 __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol, int r, int n0, int m0,
-                                           int bt, int c0) {
-  const int n = r < p.bn ? n0 + r : p.N;  // lanes past the tile's rows store nothing
+                                           int bt, uint32_t red, int split, int c0) {
+  const int n = n0 + r;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int c = c0 + 2 * i;
@@ -270,6 +257,18 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
     uint32_t v[32];
     tc::ld_32x32b_x32(tcol + 32u * c, v);
     tc::wait_ld();
+#pragma unroll 1
+    for (int q = 1; q < split; ++q) {
+      // all 32 loads first, so that they are in flight together
+      float t[32];
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj)
+        t[jj] = 32 * c + jj < bt ? ld_peer_f32(red + 4u * static_cast<uint32_t>((32 * c + jj) * kBN + r),
+                                               static_cast<uint32_t>(q))
+                                 : 0.f;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + t[jj]);
+    }
     // residual: the chunk's 32 values of R first (R may be C, so no load
     // could move past a store), then the stores
     float rv[32];
@@ -296,70 +295,15 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
   }
 }
 
-// Split K, every rank: its partial tile (TMEM lane r, chunks c0, c0 + 2, ...)
-// to its slot of the workspace, token-major so that the 32 lanes of a warp
-// write 32 consecutive floats.
-__device__ __forceinline__ void store_partial(float* part, uint32_t tcol, int r, int bt, int c0) {
-#pragma unroll 1
-  for (int c = c0; c < (bt + 31) / 32; c += 2) {
-    uint32_t v[32];
-    tc::ld_32x32b_x32(tcol + 32u * c, v);
-    tc::wait_ld();
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj)
-      if (32 * c + jj < bt) part[static_cast<long long>(32 * c + jj) * kBN + r] = __uint_as_float(v[jj]);
-  }
-}
-
-// Split K, the tile's last rank: the split partial tiles of the workspace
-// added in rank order (a fixed order whichever rank finishes last), then C
-// (R added for the residual epilogue). Thread t of the 256 epilogue threads
-// takes row t % 128 and every other token from t / 128; per rank it issues
-// the loads of up to 32 tokens before adding any, so that they are in
-// flight together (a warp's loads are 128 consecutive bytes).
-template <int EPI>
-__device__ __forceinline__ void reduce_partials(const TmaGemmParams& p, const float* part0, long long rank_stride,
-                                                int split, int n0, int m0, int bt, int t) {
-  const int r = t & (kBN - 1), h = t >> 7;
-  const int n = n0 + r;
-  if (n >= p.N || r >= p.bn) return;
-#pragma unroll 1
-  for (int t0 = h; t0 < bt; t0 += 64) {
-    float sum[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) sum[i] = 0.f;
-#pragma unroll 1
-    for (int q = 0; q < split; ++q) {
-      const float* src = part0 + q * rank_stride + r;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int tok = t0 + 2 * i;
-        if (tok < bt) sum[i] += __ldcg(src + static_cast<long long>(tok) * kBN);
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int tok = t0 + 2 * i, m = m0 + tok;
-      if (tok < bt && m < p.M && LQ_IN_BOUNDS(m >= 0 && n >= 0)) {
-        const long long o = static_cast<long long>(m) * p.N + n;
-        float v = sum[i];
-        if constexpr (EPI == epi::kResidual) v += p.R[o];
-        p.C[o] = v;
-      }
-    }
-  }
-}
-
 // ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
 // Warps 2..9: converters in two groups of four (group g converts the
 // pipeline stages ks with ks % 2 == g: 128 K of its W rows into the stage's
 // 64 TMEM columns); then both groups run the epilogue, group g taking the
-// 32-column chunks g, g + 2, ... With split K (`split` CTAs sharing one
-// output tile, each over its own range of K) every rank writes its partial
-// tile to the workspace and counts itself done on the tile's counter; the
-// rank that counts last adds the partials in rank order and stores C. No
-// rank waits for another. Per stage one barrier
+// 32-column chunks g, g + 2, ... With split K (a cluster of CTAs sharing one
+// output tile), the other ranks leave their partial tiles in their own
+// shared memory and the leader adds them over distributed shared memory
+// before storing C. Per stage one barrier
 // says "A tile and W operand ready" (1 arrival with the TMA bytes + 4
 // converter warps) and one commit says "the stage's MMAs are done". The
 // producer and MMA warps run their loops with all 32 lanes (every lane
@@ -380,77 +324,42 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     const TmaGemmParams p) {
   constexpr int SUB = kSub<FMT>;
   constexpr bool SWIGLU = EPI == epi::kSwiglu;
+  constexpr int kRawBytes = kRowBytes<FMT> * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
-  const int bt = p.bt, SA = p.stages, SW = p.w_stages;
-  const uint32_t wcol0 = static_cast<uint32_t>(p.w_col0);
+  const int bt = p.bt, S = p.stages;
   const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
-  uint8_t* a_ring = base;                                          // SA x A tiles (swizzled)
+  uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
   const int RR = p.raw_stages;
-  // W rows of the tile (swiglu: 64 gate + 64 up rows, BN = 128); a raw
-  // stage holds BN rows (f16: two 128-byte-swizzled boxes of BN x 128 bytes)
-  const int BN = p.bn;
-  const int kRawBytes = kRowBytes<FMT> * BN;
-  uint8_t* w_ring = base + SA * a_stage_bytes;                     // RR x raw W stages
+  uint8_t* w_ring = base + S * a_stage_bytes;                      // RR x raw W stages
   Bars& b = *reinterpret_cast<Bars*>(w_ring + RR * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Split K: `split` consecutive CTAs along x share one output tile, rank r
+  // Split K: the `split` CTAs of a cluster share one output tile, rank r
   // taking raw W stages [jr0, jr0 + nraw); stage indices below are local to
   // the CTA, the K coordinates of its loads add ks0.
   const int split = p.split, rank = static_cast<int>(blockIdx.x) % split;
-  const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : BN), m0 = blockIdx.y * bt;
+  const int n0 = (static_cast<int>(blockIdx.x) / split) * (SWIGLU ? kBN / 2 : kBN), m0 = blockIdx.y * bt;
   const int nraw_all = p.K / kKS / SUB;
   const int jr0 = rank * nraw_all / split;
   const int nraw = (rank + 1) * nraw_all / split - jr0, nk = nraw * SUB, ks0 = jr0 * SUB;
   bool epi = false;  // this CTA's accumulator is complete and may be used
 
-  // one raw W stage into ring slot `slot` (producer lane 0)
-  auto issue_raw = [&](int j, int slot) {
-    mbar_arrive_expect_tx(&b.raw_full[slot], static_cast<uint32_t>(kRawBytes));
-    if (FMT == LQ_FMT_F16) {
-      for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x BN rows (128B-swizzled)
-        if constexpr (SWIGLU)
-          tc::tma_load_3d(w_ring + slot * kRawBytes + h * (BN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
-                          &b.raw_full[slot]);
-        else
-          tc::tma_load_2d(w_ring + slot * kRawBytes + h * (BN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
-                          &b.raw_full[slot]);
-      }
-    } else {  // one box of (row bytes of 256 K) / 4 words x BN rows
-      if constexpr (SWIGLU)
-        tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
-                        &b.raw_full[slot]);
-      else
-        tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
-                        &b.raw_full[slot]);
-    }
-  };
   if (threadIdx.x == 0) {
     for (int i = 0; i < RR; ++i) {
       mbar_init(&b.raw_full[i], 1);
       mbar_init(&b.raw_empty[i], 4 * SUB);
     }
-    for (int i = 0; i < SA; ++i) {
-      mbar_init(&b.a_full[i], 1);
-      mbar_init(&b.a_empty[i], 1);
-    }
-    for (int i = 0; i < SW; ++i) {
-      mbar_init(&b.w_full[i], 4);
-      mbar_init(&b.w_empty[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&b.full[i], 1 + 4);
+      mbar_init(&b.empty[i], 1);
     }
     mbar_init(&b.tmem_full, 1);
     b.abort = 0;
-    b.last = 0;
     fence_barrier_init();
-    // W does not depend on the previous kernel: its first stages are on their
-    // way before the TMEM allocation and the block barrier
-    tc::prefetch_tmap(&tmW);
-    tc::prefetch_tmap(&tmA);
-    for (int j = 0; j < nraw && j < RR; ++j) issue_raw(j, j);
   }
   if (warp == 1) {
     tc::tmem_alloc(&b.tmem_base, kTmemCols);
@@ -464,10 +373,38 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
   if (warp == 0) {
     // ---------------- producer ----------------
-    int raw_issued = min(nraw, RR), issued = 0;  // the first raw stages are in flight (prologue)
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmW);
+      tc::prefetch_tmap(&tmA);
+    }
+    auto issue_raw = [&](int j, int slot) {
+      mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
+      if (FMT == LQ_FMT_F16) {
+        for (int h = 0; h < 2; ++h) {  // two boxes of 64 halves x 128 rows (128B-swizzled)
+          if constexpr (SWIGLU)
+            tc::tma_load_3d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0, 0,
+                            &b.raw_full[slot]);
+          else
+            tc::tma_load_2d(w_ring + slot * kRawBytes + h * (kBN * 128), &tmW, 128 * (jr0 + j) + 64 * h, n0,
+                            &b.raw_full[slot]);
+        }
+      } else {  // one box of (row bytes of 256 K) / 4 words x 128 rows
+        if constexpr (SWIGLU)
+          tc::tma_load_3d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0, 0,
+                          &b.raw_full[slot]);
+        else
+          tc::tma_load_2d(w_ring + slot * kRawBytes, &tmW, (kRowBytes<FMT> / 4) * (jr0 + j), n0,
+                          &b.raw_full[slot]);
+      }
+    };
+    int raw_issued = 0, issued = 0;
     bool ok = true;
+    // W does not depend on the previous kernel: start it before waiting.
+    for (; raw_issued < nraw && raw_issued < RR; ++raw_issued)
+      if (lane == 0) issue_raw(raw_issued, raw_issued);
+    __syncwarp();
     pdl_wait();
-    int st = 0, lap = 0, rslot = 0, rlap = 0;  // A ring / raw ring positions
+    int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
     for (int ks = 0; ks < nk; ++ks) {
       if (ks % SUB == 0 && ks / SUB >= RR) {
         const int j = ks / SUB;  // reuse raw slot j % 2 after both of its users finished
@@ -480,19 +417,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ++raw_issued;
         if (++rslot == RR) { rslot = 0; ++rlap; }
       }
-      if (ks >= SA && (!warp_wait(&b.a_empty[st], (lap - 1) & 1, p) || b.abort)) {
+      if (ks >= S && (!warp_wait(&b.empty[st], (lap - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(&b.a_full[st], a_stage_bytes);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.a_full[st]);
+        mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.full[st]);
         tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, m0,
-                        &b.a_full[st]);
+                        &b.full[st]);
       }
       __syncwarp();
       ++issued;
-      if (++st == SA) { st = 0; ++lap; }
+      if (++st == S) { st = 0; ++lap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
@@ -501,45 +438,48 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // never leave copies in flight (waits for the last use of every slot)
     for (int j = max(0, raw_issued - RR); j < raw_issued; ++j)
       mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
-    for (int ks = max(0, issued - SA); ks < issued; ++ks)
-      mbar_wait(&b.a_full[ks % SA], (ks / SA) & 1, kDrainWaitNs);
+    for (int ks = max(0, issued - S); ks < issued; ++ks)
+      mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    // stage ks: A tile in ring slot ks % SA, W operand in TMEM slot ks % SW;
-    // both slots go back to their producers with one commit each
     const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
-    auto ready = [&](int ks) {
-      return mbar_test_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1) &&
-             mbar_test_wait(&b.w_full[ks % SW], static_cast<uint32_t>(ks / SW) & 1);
-    };
-    auto issue_stage = [&](int ks) {
-      const int sa = ks % SA, sw = ks % SW;
-      const uint32_t abase = smem_u32(a_ring + sa * a_stage_bytes);
-      const uint32_t wcol = tmem + wcol0 + 64u * sw;
+    int st = 0, lap = 0;
+    auto issue_stage = [&](int ks, int sst) {
+      const uint32_t abase = smem_u32(a_ring + sst * a_stage_bytes);
+      const uint32_t wcol = tmem + kWCol0 + 64u * sst;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
         tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
       }
-      tc::commit(&b.a_empty[sa]);
-      tc::commit(&b.w_empty[sw]);
+      tc::commit(&b.empty[sst]);
     };
     for (int ks = 0; ks < nk;) {
-      if (!warp_wait(&b.a_full[ks % SA], static_cast<uint32_t>(ks / SA) & 1, p) ||
-          !warp_wait(&b.w_full[ks % SW], static_cast<uint32_t>(ks / SW) & 1, p)) {
+      if (!warp_wait(&b.full[st], lap & 1, p)) {
         ok = false;
         break;
       }
       // Issue this stage and, without a blocking wait, any following stages
-      // whose operands are already in place (the pipeline usually runs ahead).
+      // that are already complete (the pipeline usually runs ahead).
       int cnt = 1;
-      while (ks + cnt < nk && cnt < SW - 1 && __all_sync(0xffffffffu, ready(ks + cnt))) ++cnt;
+      int st2 = st + 1 == S ? 0 : st + 1, lap2 = st + 1 == S ? lap + 1 : lap;
+      while (ks + cnt < nk && cnt < S - 1 && __all_sync(0xffffffffu, mbar_test_wait(&b.full[st2], lap2 & 1))) {
+        ++cnt;
+        if (++st2 == S) { st2 = 0; ++lap2; }
+      }
       tc::fence_after_sync();
-      if (lane == 0)
-        for (int i = 0; i < cnt; ++i) issue_stage(ks + i);
+      if (lane == 0) {
+        int sst = st;
+        for (int i = 0; i < cnt; ++i) {
+          issue_stage(ks + i, sst);
+          if (++sst == S) sst = 0;
+        }
+      }
       __syncwarp();
       ks += cnt;
+      for (int i = 0; i < cnt; ++i)
+        if (++st == S) { st = 0; ++lap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
@@ -555,35 +495,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
     for (int ks = g; ks < nk; ks += 2) {
-      const int j = ks / SUB, half = ks % SUB, st = ks % SW, rslot = j % RR;
+      const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % RR;
       if (!warp_wait(&b.raw_full[rslot], (j / RR) & 1, p) || b.abort) {
         ok = false;
         break;
       }
-      if (ks >= SW && (!warp_wait(&b.w_empty[st], ((ks / SW) - 1) & 1, p) || b.abort)) {
+      if (ks >= S && (!warp_wait(&b.empty[st], ((ks / S) - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
       }
       const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
-      const uint32_t tcol = tmem + tlane + wcol0 + 64u * st;
+      const uint32_t tcol = tmem + tlane + kWCol0 + 64u * st;
       uint32_t out[32];
-      // lanes past the tile's BN rows feed zeros to the MMA (their raw rows
-      // were not copied)
-      const uint32_t box_bytes = static_cast<uint32_t>(BN) * 128u;  // f16: one 64-K box of the raw stage
-      if (r < BN) {
-        convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), box_bytes, out);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) out[i] = 0u;
-      }
+      convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
       tc::st_32x32b_x32(tcol, out);
-      if (r < BN) convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), box_bytes, out);
+      convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
       tc::st_32x32b_x32(tcol + 32u, out);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&b.w_full[st]);
+        mbar_arrive(&b.full[st]);
         mbar_arrive(&b.raw_empty[rslot]);
       }
     }
@@ -633,38 +565,39 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               p.C[static_cast<long long>(m0 + tok) * p.N + n] = epi::swiglu(xch[tok * 128 + j], xch[tok * 128 + 64 + j]);
           }
         }
-      } else if (split == 1) {
-        if (epi) store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, g);
-      } else {
-        // split K: this rank's partial tile, then one count per CTA on the
-        // tile's counter once every epilogue thread's stores are visible
-        // (fence, then the barrier of the eight epilogue warps, reached
-        // whatever their outcome); the rank that counts last reduces
-        const int tile = static_cast<int>(blockIdx.y) * p.n_tiles + static_cast<int>(blockIdx.x) / split;
-        const long long tile_floats = static_cast<long long>(bt) * kBN;
-        const long long rank_stride = tile_floats * p.n_tiles * static_cast<long long>(gridDim.y);
-        float* part0 = p.part + tile_floats * tile;
-        if (epi) store_partial(part0 + rank_stride * rank, tmem + tlane, r, bt, g);
-        // the CTA barrier orders every epilogue thread's stores before the
-        // count; one thread publishes them at GPU scope (the release fence
-        // is cumulative over what the barrier ordered before it) and, as
-        // the last rank, acquires the other ranks' partials for all of them
-        named_barrier(3, 8u * 32u);
-        if (threadIdx.x == 64) {
-          __threadfence();
-          const unsigned done = atomicAdd(p.cnt + tile, 1u);
-          __threadfence();
-          b.last = done == static_cast<unsigned>(split - 1) ? 1 : 0;
+      } else if (epi && split == 1) {
+        store_tile<FMT, EPI>(p, tmem + tlane, r, n0, m0, bt, 0u, 1, g);
+      } else if (epi && rank != 0) {
+        // this rank's partial tile -> its own shared memory (the A ring is
+        // idle now), token-major so that the 32 lanes write 32 rows in a row
+        float* red = reinterpret_cast<float*>(a_ring);
+#pragma unroll 1
+        for (int c = g; c < (bt + 31) / 32; c += 2) {
+          uint32_t v[32];
+          tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
+          tc::wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj)
+            if (32 * c + jj < bt) red[(32 * c + jj) * kBN + r] = __uint_as_float(v[jj]);
         }
-        named_barrier(3, 8u * 32u);
-        if (b.last && !b.abort)
-          reduce_partials<EPI>(p, part0, rank_stride, split, n0, m0, bt, static_cast<int>(threadIdx.x) - 64);
       }
     }
   }
   // ---------------- teardown ----------------
   tc::fence_before_sync();
   __syncthreads();
+  if (split > 1) {
+    // the peers' partial tiles are in their shared memory; the leader adds
+    // them to its own (rank order: a fixed summation order) and stores C
+    cluster_sync();
+    if (rank == 0 && epi && warp >= 2) {
+      tc::fence_after_sync();
+      const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
+      store_tile<FMT, EPI>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
+                           split, g);
+    }
+    cluster_sync();  // the peers keep their shared memory until the leader read it
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
@@ -693,21 +626,34 @@ EncodeTiled encode_fn() {
   return fn;
 }
 
-// Launch with programmatic dependent launch.
+// Launch with programmatic dependent launch and, when cluster_x > 1,
+// clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args&&... args) {
+cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                               unsigned cluster_x, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
   cfg.numAttrs = 1;
+  if (cluster_x > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   cfg.attrs = attr;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  return launch_pdl_cluster(kern, grid, block, smem, st, 1u, std::forward<Args>(args)...);
 }
 
 bool aligned(const void* p, unsigned al) { return (reinterpret_cast<uintptr_t>(p) % al) == 0; }
@@ -728,31 +674,28 @@ int pick_bt(int64_t M, int64_t N) {
   return static_cast<int>(std::min<int64_t>(256, (per + 15) / 16 * 16));
 }
 
-int raw_stage_bytes(int fmt, int bn) { return bn * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
+int raw_stage_bytes(int fmt) { return kBN * (fmt == LQ_FMT_F16 ? 256 : (fmt == LQ_FMT_Q8_0 ? 272 : 144)); }
 
-// Ring depths for a token tile of bt and W tiles of bn rows: the raw W ring
-// first (W comes from HBM: about 140 KB (Q8_0, Q4_0) to 190 KB (f16) of a
-// 128-row tile in flight, i.e. up to 4 or 6 raw stages, more of narrower
-// tiles, at most 8), then as many A stages (bt rows x 128 K bf16, from L2)
-// as fit, up to 16, at least two of each; where that leaves two A stages,
-// three A stages over fewer raw stages. The A ring is separate from the four
-// TMEM slots of the W operand, so small token tiles keep many A stages in
-// flight.
+// Ring depths for a token tile of bt: the raw W ring first (W comes from
+// HBM: up to 6 raw stages of f16, 4 of Q8_0 / Q4_0, i.e. 6 to 8 pipeline
+// stages of lookahead), then as many A stages (bt rows x 128 K halves, from
+// L2) as fit, at least two of each; where that leaves two A stages, three A
+// stages over fewer raw stages.
 struct RingPlan {
   int a_stages = 0, raw_stages = 0;
 };
 std::atomic<int> g_ring_a{0}, g_ring_raw{0};  // debug override (0 = automatic)
 
-RingPlan ring_plan(int fmt, int bt, int bn) {
+RingPlan ring_plan(int fmt, int bt) {
   const DeviceInfo& di = device_info();
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
                            static_cast<long long>(sizeof(Bars)) - 64;
-  const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt, bn);
+  const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt);
   RingPlan rp;
-  const int raw_cap = std::min(kMaxRawStages, (fmt == LQ_FMT_F16 ? 6 : 4) * kBN / bn);
+  const int raw_cap = fmt == LQ_FMT_F16 ? 6 : 4;
   rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 2 * a_stage) / raw));
   if (rp.raw_stages < 2) return RingPlan{};
-  rp.a_stages = static_cast<int>(std::min<long long>(kMaxAStages, (budget - rp.raw_stages * raw) / a_stage));
+  rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
   if (rp.a_stages < 2) return RingPlan{};
   // Large token tiles leave room for two A stages only: three A stages over
   // two raw stages measured about 5 % faster at M = 512 (f16 and Q8_0).
@@ -763,27 +706,66 @@ RingPlan ring_plan(int fmt, int bt, int bn) {
   const int oa = g_ring_a.load(), orr = g_ring_raw.load();
   if (oa || orr) {
     const int a2 = oa ? oa : rp.a_stages, r2 = orr ? orr : rp.raw_stages;
-    if (a2 >= 2 && a2 <= kMaxAStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
+    if (a2 >= 2 && a2 <= kMaxStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
       return RingPlan{a2, r2};
   }
   return rp;
 }
 
-size_t tma_smem_bytes(int fmt, int bt, int bn, int a_stages, int raw_stages) {
+size_t tma_smem_bytes(int fmt, int bt, int a_stages, int raw_stages) {
   const size_t need = 1024 + static_cast<size_t>(a_stages) * bt * 256 +
-                      static_cast<size_t>(raw_stages) * raw_stage_bytes(fmt, bn) + sizeof(Bars) + 64;
+                      static_cast<size_t>(raw_stages) * raw_stage_bytes(fmt) + sizeof(Bars) + 64;
   // at least 116 KB, so that no two CTAs share an SM (each holds all of TMEM)
   return std::max<size_t>(need, 116 * 1024);
 }
 
-// Split K: when the output tiles leave more than half of the SMs idle, K is
-// split so that about one CTA runs per SM (at most one raw W stage per rank
-// and at most kMaxSplit ranks).
-constexpr int kMaxSplit = 16;
-int pick_split(int64_t tiles, int nraw_all) {
+// Clusters of `split` CTAs along K: the largest split (up to 8, the portable
+// cluster size) whose clusters all fit on the GPU at once, or 1.
+template <int FMT>
+int pick_split_query(int64_t tiles, int nraw_all, size_t smem);
+
+template <int FMT>
+int pick_split(int64_t tiles, int nraw_all, size_t smem) {
   const DeviceInfo& di = device_info();
   if (2 * tiles > di.sm_count) return 1;
-  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({kMaxSplit, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all})));
+  // the answer depends on (tiles, K, shared memory) only: remember it
+  static std::mutex mu;
+  static std::map<std::tuple<int, int64_t, int, size_t>, int> cache;
+  const auto key = std::make_tuple(current_device(), tiles, nraw_all, smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  const int s = pick_split_query<FMT>(tiles, nraw_all, smem);
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = s;
+  return s;
+}
+
+template <int FMT>
+int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
+  const DeviceInfo& di = device_info();
+  int s = static_cast<int>(std::min<int64_t>({8, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all}));
+  for (; s >= 2; --s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles * s));
+    cfg.blockDim = dim3(kTmaThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(s);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT, epi::kPlain>, &cfg) == cudaSuccess &&
+        active >= tiles)
+      return s;
+    cudaGetLastError();  // a refused query is not an error of the call
+  }
+  return 1;
 }
 
 template <int FMT, int EPI>
@@ -812,8 +794,8 @@ template <int FMT, int EPI>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              TmaGemmParams p) {
   auto kern = gemm_tma_kernel<FMT, EPI>;
-  const int bn = EPI == epi::kSwiglu ? kBN / 2 : p.bn;  // outputs per tile
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.bn, p.stages, p.raw_stages);
+  const int bn = EPI == epi::kSwiglu ? kBN / 2 : kBN;  // outputs per tile
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -822,9 +804,12 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
     if (e != cudaSuccess) return cuda_status(e);
     configured[dev] = static_cast<int>(smem);
   }
+  const int64_t tiles = ((a.N + bn - 1) / bn) * ((a.M + p.bt - 1) / p.bt);
+  p.split = EPI == epi::kSwiglu ? 1 : pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
   const dim3 grid(static_cast<unsigned>((a.N + bn - 1) / bn * p.split),
                   static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
-  cudaError_t e = launch_pdl(kern, grid, dim3(kTmaThreads), smem, a.stream, tmW, tmA, p);
+  cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
+                                     static_cast<unsigned>(p.split), tmW, tmA, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
 }
@@ -838,6 +823,7 @@ unsigned read_clear_gemm_tma_error() {
   return v;
 }
 
+int pick_gemm_bt(int64_t M, int64_t N) { return pick_bt(M, N); }
 
 void set_gemm_rings(int a_stages, int raw_stages) {
   g_ring_a.store(a_stages);
@@ -850,7 +836,7 @@ bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M > (1LL << 24) || a.N > (1LL << 24)) return false;
   if (!encode_fn()) return false;
   const DeviceInfo& di = device_info();
-  return di.cc_major >= 10 && ring_plan(a.fmt, 256, kBN).a_stages >= 2;
+  return di.cc_major >= 10 && ring_plan(a.fmt, 256).a_stages >= 2;
 }
 
 // The library's own stream-ordered memory pool on the current device: freed
@@ -880,72 +866,36 @@ cudaMemPool_t workspace_pool() {
 // stream-ordered workspace from the library's pool for the duration of the
 // call.
 lq_status launch_gemm_tma(const MatmulArgs& a) {
-  const TmaPlan pl = gemm_tma_plan(a);
+  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
+  const int bt = pick_bt(a.M, a.epi == epi::kSwiglu ? 2 * a.N : a.N);
+  const size_t ws_bytes = gemm_tma_workspace_bytes(a.M, a.K);
   void* ws = nullptr;
   cudaMemPool_t pool = workspace_pool();
   if (!pool) return LQ_ERR_CUDA;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, pl.ws_bytes, pool, a.stream);
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
   if (e != cudaSuccess) return LQ_ERR_CUDA;
-  lq_status st = launch_gemm_tma_ws(a, pl, ws);
+  lq_status st = launch_gemm_tma_ws(a, ws, bt);
   cudaError_t ef = cudaFreeAsync(ws, a.stream);
   if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
   if (st == LQ_OK) count_route(2);
   return st;
 }
 
-// Token tile, K split and workspace layout of a call: the bf16 copy of A,
-// then (split K) the ranks' partial tiles and the tiles' counters, each part
-// 256-byte aligned.
-TmaPlan gemm_tma_plan(const MatmulArgs& a) {
-  TmaPlan pl;
-  const bool sw = a.epi == epi::kSwiglu;
-  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
-  pl.bt = pick_bt(a.M, sw ? 2 * a.N : a.N);
-  pl.m_tiles = static_cast<int>((a.M + pl.bt - 1) / pl.bt);
-  // W rows per tile: 128 (the MMA's M), or, while 128-row tiles would leave
-  // more than half of the SMs idle, fewer rows (a multiple of 16, at least
-  // 32) so that more SMs stream W; the MMA still runs on 128 lanes, the
-  // unused ones holding zeros. Fewer rows beat a split K there: no partial
-  // tiles, no reduction. Swiglu tiles stay at 64 gate + 64 up rows.
-  pl.bn = kBN;
-  const int sms = device_info().sm_count;
-  if (!sw && 2LL * ((a.N + kBN - 1) / kBN) * pl.m_tiles <= sms) {
-    for (int cand = kBN - 16; cand >= 32; cand -= 16) {
-      if (((a.N + cand - 1) / cand) * pl.m_tiles > sms) break;
-      pl.bn = cand;
-    }
-  }
-  const int bn = sw ? kBN / 2 : pl.bn;
-  pl.n_tiles = static_cast<int>((a.N + bn - 1) / bn);
-  const int64_t tiles = static_cast<int64_t>(pl.n_tiles) * pl.m_tiles;
-  pl.split = sw ? 1 : pick_split(tiles, static_cast<int>(a.K / kstep_multiple(a.fmt)));
-  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  size_t off = up(static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2);
-  if (pl.split > 1) {
-    pl.part_off = off;
-    off += up(static_cast<size_t>(pl.split) * static_cast<size_t>(tiles) * pl.bt * kBN * 4);
-    pl.cnt_off = off;
-    off += up(static_cast<size_t>(tiles) * 4);
-  }
-  pl.ws_bytes = off;
-  return pl;
+size_t gemm_tma_workspace_bytes(int64_t M, int64_t K) {
+  return (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
 }
 
-// Pre-pass + GEMM given the plan's workspace (256-byte aligned).
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
+// Pre-pass + GEMM given a workspace of M*K bf16 values (a16, 16-byte aligned).
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
-  const int bt = pl.bt;
-  void* a16 = ws;
-  unsigned* cnt = pl.split > 1 ? reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pl.cnt_off) : nullptr;
-  const int ncnt = pl.split > 1 ? pl.n_tiles * pl.m_tiles : 0;
-  // 1. A -> bf16 (round to nearest even); the split-K counters to zero
+  // 1. A -> bf16 (round to nearest even)
   {
     const long long n8 = static_cast<long long>(M) * K / 8;
     const long long want = (n8 + kPreThreads - 1) / kPreThreads;
-    const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1));
+    const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1)) * 8;
     const unsigned grid = static_cast<unsigned>(std::max<long long>(1, std::min(want, cap)));
     cudaError_t e = launch_pdl(a_to_bf16_kernel, dim3(grid), dim3(kPreThreads), 0, a.stream, a.A,
-                               static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0, cnt, ncnt);
+                               static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return LQ_ERR_CUDA;
   }
@@ -967,7 +917,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
     cuuint64_t dims[3] = {f16 ? static_cast<cuuint64_t>(K) : rb / 4, static_cast<cuuint64_t>(N), 2};
     cuuint64_t strides[2] = {rb, rb * static_cast<cuuint64_t>(N)};
     cuuint32_t box[3] = {static_cast<cuuint32_t>(f16 ? 64 : (a.fmt == LQ_FMT_Q8_0 ? 68 : 36)),
-                         static_cast<cuuint32_t>(sw ? kBN / 2 : pl.bn), 2};
+                         static_cast<cuuint32_t>(sw ? kBN / 2 : kBN), 2};
     cuuint32_t es[3] = {1, 1, 1};
     if (enc(&tmW, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT32, rank,
             const_cast<void*>(a.W), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -992,22 +942,11 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& pl, void* ws) {
   p.N = N;
   p.K = K;
   p.bt = bt;
-  p.bn = a.epi == epi::kSwiglu ? kBN : pl.bn;
-  p.split = pl.split;
-  p.n_tiles = pl.n_tiles;
-  p.part = pl.split > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.part_off) : nullptr;
-  p.cnt = cnt;
+  p.split = 1;  // chosen at launch (pick_split)
   {
-    const RingPlan rp = ring_plan(a.fmt, bt, p.bn);
+    const RingPlan rp = ring_plan(a.fmt, bt);
     p.stages = rp.a_stages;
     p.raw_stages = rp.raw_stages;
-    // W slots above the accumulator's bt columns: as deep as the A ring for
-    // large token tiles (the tensor pipe is the limit there), up to seven
-    // for small ones (the converter -> MMA -> commit round trip is)
-    p.w_col0 = (bt + 63) / 64 * 64;
-    p.w_stages = std::max(2, std::min({kMaxWStages, (static_cast<int>(kTmemCols) - p.w_col0) / 64,
-                                       std::max(p.stages, bt <= 64 ? kMaxWStages : 4)}));
-    if (bt > 128) p.w_stages = std::min(p.w_stages, p.stages);
   }
   if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
   p.wait_ns = wait_limit_ns();

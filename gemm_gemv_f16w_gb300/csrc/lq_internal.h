@@ -65,16 +65,12 @@ lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via 
 bool gemm_tc_eligible(const MatmulArgs& a);
 // tcgen05 with TMA loads and W in tensor memory; allocates its workspace
 lq_status launch_gemm_tma(const MatmulArgs& a);
-// The call's token tile, K split and workspace layout: the bf16 copy of A at
-// offset 0, then (split > 1) the ranks' partial tiles and the tiles' counters.
-struct TmaPlan {
-  int bt = 0, bn = 128, split = 1, n_tiles = 0, m_tiles = 0;
-  size_t part_off = 0, cnt_off = 0, ws_bytes = 0;
-};
-TmaPlan gemm_tma_plan(const MatmulArgs& a);
-// the same given a workspace of plan.ws_bytes bytes (256-byte aligned)
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, const TmaPlan& plan, void* ws);
+// the same given a workspace of gemm_tma_workspace_bytes(M, K) bytes (the bf16
+// copy of A, 16-byte aligned)
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt);
+size_t gemm_tma_workspace_bytes(int64_t M, int64_t K);
 bool gemm_tma_eligible(const MatmulArgs& a);
+int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
 void set_gemm_rings(int a_stages, int raw_stages);
 

@@ -59,14 +59,12 @@ extern "C" lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, flo
   // Only the tensor-core kernel that needs the workspace is offered here.
   if (!gemm_tma_eligible(a)) return LQ_ERR_UNSUPPORTED;
   // Beyond the fixed workspace: a clear refusal, never a larger allocation.
-  const TmaPlan pl = gemm_tma_plan(a);
-  if (pl.ws_bytes > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
+  if (gemm_tma_workspace_bytes(M, K) > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
   const lq_status st = workspace_address(&ws);
   if (st != LQ_OK) return st;
   // Every byte the kernels read from the workspace (the bf16 rows of the M
-  // tokens and, when K is split, the partial tiles) is written earlier in the
-  // same call, and the pre-pass zeroes the split's counters, so nothing
-  // carries over from the previous call.
-  return launch_gemm_tma_ws(a, pl, ws);
+  // tokens) is written earlier in the same call, so nothing needs clearing
+  // between calls.
+  return launch_gemm_tma_ws(a, ws, pick_gemm_bt(M, N));
 }

@@ -329,7 +329,7 @@ void      lq_debug_set_wait_limit_ns(uint64_t ns);
  * LQ_ERR_INVALID_ARG for values out of range. */
 lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes);
 /* Overrides the tensor-core GEMM's ring depths (0 = automatic): A-tile
- * stages (2..16) and raw-weight stages (2..8); ignored when they do not fit
+ * stages (2..4) and raw-weight stages (2..8); ignored when they do not fit
  * in shared memory. For tuning sweeps; results do not change. */
 lq_status lq_debug_gemm_rings(int a_stages, int raw_stages);
 
