@@ -158,10 +158,10 @@ class Workbench:
         over the independent copies), "chain-dependent" (every problem waits
         for the previous one), "argmax" (M = 1: one lq_gemv_argmax per copy,
         logits not stored), "argmax-unfused" (M = 1: lq_matmul into C, then
-        lq_argmax_f32 on C), "topk" (M = 1: lq_gemv_topk with k = 50), "tc"
-        (M > 1: separate calls forced onto the tensor-core route, for
-        comparison with the batched decode kernel), or "auto" (chain for
-        M = 1, else calls)."""
+        lq_argmax_f32 on C), "topk" (M = 1: lq_gemv_topk with k = 50), "tc" /
+        "batch" (M > 1: separate calls forced onto the tensor-core route or
+        the CUDA-core batched decode kernel, to compare the two where the
+        router picks one), or "auto" (chain for M = 1, else calls)."""
         self.lq, self.w, self.dev = lq, w, dev
         W, A = synthetic.draw_workload(w)
         packed = lq.pack(w.fmt, W).reshape(-1).view(np.uint8)
@@ -201,7 +201,7 @@ class Workbench:
         if mode == "topk" and w.M == 1:
             self.mode = mode
             self.topk = [lq.topk_buffers(w.N, 50, dev) for _ in range(R)]
-        if mode == "tc" and w.M > 1:
+        if mode in ("tc", "batch") and w.M > 1:
             self.mode = mode
         # kernels of ours per step
         if self.problems is not None:
@@ -228,15 +228,15 @@ class Workbench:
                 v, i, wk = self.topk[r]
                 self.lq.lq_gemv_topk(w.fmt, self.Ad[r], self.Wd[r], self.Cd[r], w.N, w.K, 50, v, i, wk, stream)
             return
-        if self.mode == "tc":
-            self.lq.force_route(self.lq.ROUTE_TENSOR_CORE)
+        if self.mode in ("tc", "batch"):
+            self.lq.force_route(self.lq.ROUTE_TENSOR_CORE if self.mode == "tc" else self.lq.ROUTE_STREAM)
         try:
             for r in range(self.R):
                 self.fn(self.Ad[r], self.Wd[r], self.Cd[r], w.M, w.N, w.K, stream)
                 if self.mode == "argmax-unfused":
                     self.lq.lq_argmax_f32(self.Cd[r], w.N, self.res[r], stream)
         finally:
-            if self.mode == "tc":
+            if self.mode in ("tc", "batch"):
                 self.lq.force_route(0)
 
     def capture(self):
@@ -449,7 +449,7 @@ def run_reference(args, world, rank):
 
 EXTRA = ["gemv_f16_256x512", "gemv_q4_0_11008x4096_outliers", "gemv_f16_lmhead_151936x2048",
          "gemm_f16_512x6144x2048", "gemm_q8_0_512x6144x2048", "gemm_q4_0_512x6144x2048"] + \
-        [f"gemm_{f}_m{m}_6144x2048" for m in (2, 8, 16, 64) for f in ("f16", "q8_0", "q4_0")]
+        [f"gemm_{f}_m{m}_6144x2048" for m in (2, 4, 8, 16, 64) for f in ("f16", "q8_0", "q4_0")]
 
 
 def main():
@@ -467,7 +467,7 @@ def main():
                     help="--impl reference: seconds of oracle work the whole run aims at")
     ap.add_argument("--mode", default="auto",
                     choices=["auto", "calls", "chain", "chain-dependent", "argmax", "argmax-unfused", "topk",
-                             "tc"],
+                             "tc", "batch"],
                     help="how the headline step runs its matmuls (auto: chain for M = 1; argmax modes: "
                          "M = 1, the GEMV with its argmax)")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
@@ -552,7 +552,8 @@ def main():
         if synthetic.WORKLOADS[name].M == 1:
             runs.append((name, "calls"))  # the decode GEMVs both as a chain and as separate calls
         if 1 < synthetic.WORKLOADS[name].M <= 8:
-            runs.append((name, "tc"))     # the batched decode kernel against the tensor-core route
+            # the batched decode kernel against the tensor-core route
+            runs.append((name, "batch" if synthetic.WORKLOADS[name].M > 4 else "tc"))
     if w.M == 1 and args.extras != "none":
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
     lmhead = "gemv_f16_lmhead_151936x2048"

@@ -38,7 +38,7 @@ EXPORTS = [
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
     "lq_gemv_argmax", "lq_argmax_f32", "lq_matmul_residual", "lq_matmul_swiglu",
     "lq_gemv_q4_0i", "lq_gemm_q4_0i", "lq_matmul_q4_0i", "lq_pack_q4_0i", "lq_pack_q8_0_rcp",
-    "lq_topk_work_bytes", "lq_topk_f32", "lq_gemv_topk",
+    "lq_topk_work_bytes", "lq_topk_f32", "lq_gemv_topk", "lq_debug_chain_waits",
 ]
 _COMPUTE = [n for n in EXPORTS if n.split("_")[1] in ("gemv", "gemm", "matmul")]
 
@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
         L.lq_gemv_chain.restype = st
         L.lq_debug_gemm_rings.argtypes = [ctypes.c_int, ctypes.c_int]
         L.lq_debug_gemm_rings.restype = st
+        L.lq_debug_chain_waits.argtypes = [ctypes.c_int]
+        L.lq_debug_chain_waits.restype = None
         L.lq_debug_gemv_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
         L.lq_debug_gemv_plan.restype = st
         L.lq_gemm_noalloc.argtypes = [st, vp, vp, vp, i64, i64, i64, vp]
@@ -346,6 +348,12 @@ def gemv_plan(ctas_per_sm: int = 0, rows_per_stage: int = 0, smem_bytes: int = 0
     """Override the decode GEMV's launch plan (0 = automatic); tuning only."""
     _check(lib().lq_debug_gemv_plan(int(ctas_per_sm), int(rows_per_stage), int(smem_bytes)),
            "lq_debug_gemv_plan")
+
+
+def chain_waits(on: bool) -> None:
+    """Dependent problems of lq_gemv_chain wait inside one launch (True) or
+    start a new launch (False, the default); for comparisons."""
+    lib().lq_debug_chain_waits(1 if on else 0)
 
 
 def gemm_rings(a_stages: int = 0, raw_stages: int = 0) -> None:

@@ -138,9 +138,12 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
     case 3: return launch_gemv_generic(a);
     default: break;
   }
-  // M = 2..8: one pass over W on the CUDA cores beats the tensor-core
-  // kernel's fixed latencies
-  if (M <= 8) {
+  // M = 2..4: one pass over W on the CUDA cores beats the tensor-core
+  // kernel's fixed latencies. From five rows the batched kernel's eight-row
+  // slices (8 warps of up to 255 registers) are slower than the tensor
+  // cores (Q8_0 M = 8, N = 6144, K = 2048: 17.2 against 13.7 us), so they
+  // run only when the route is forced (lq_debug_force_route(1)).
+  if (M <= 4) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }
@@ -173,7 +176,7 @@ lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, fl
     default: break;
   }
   if (M == 1) return launch_gemv(a);  // falls back to the generic kernel itself
-  if (M <= 8) {
+  if (M <= 4) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }
@@ -357,6 +360,7 @@ lq_status lq_debug_gemm_rings(int a_stages, int raw_stages) {
   lq::set_gemm_rings(a_stages, raw_stages);
   return LQ_OK;
 }
+void lq_debug_chain_waits(int on) { lq::set_chain_waits(on != 0); }
 lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes) {
   if (ctas_per_sm < 0 || ctas_per_sm > 2 || rows_per_stage < 0 || rows_per_stage > 8 ||
       smem_bytes < 0)

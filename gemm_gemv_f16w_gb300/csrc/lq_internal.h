@@ -89,6 +89,9 @@ lq_status launch_topk_f32(const float* x, int64_t n, int k, float* values, int32
 // Decode chain (lq_gemv_chain); LQ_ERR_UNSUPPORTED when the problems do not
 // fit its fast path.
 lq_status launch_gemv_chain(int fmt, const lq_gemv_problem* problems, int count, cudaStream_t stream);
+// Debug: dependent problems wait inside one chain launch (device-wide
+// counter) instead of starting a new launch (the default).
+void set_chain_waits(bool on);
 
 // Device status words of each translation unit (read-and-clear).
 unsigned read_clear_gemv_error();

@@ -172,14 +172,16 @@ lq_status lq_pack_q8_0_rcp(const float* W_host, int64_t N, int64_t K, void* out_
  * out as for lq_gemv_<fmt> (M = 1). If problems[j].after is non-zero,
  * problem j reads A_j only after problems 0 .. j-1 are complete, so A_j may
  * be (or depend on) an earlier C; otherwise A_j must not be written by this
- * call. Weights are streamed ahead of the computation in every case. One
- * cooperative launch of one CTA per SM; the problems array is read during
- * the call (host memory, caller-owned).
+ * call. Weights are streamed ahead of the computation in every case. Each
+ * run of problems that wait for nothing is one launch (a cooperative launch
+ * of one CTA per SM, or the streaming GEMV for a run of one problem), the
+ * runs in order on the stream; the problems array is read during the call
+ * (host memory, caller-owned).
  *   - count in 1..64; N_j >= 0; K_j % 8 == 0 (f16) or K_j % 256 == 0
  *     (quantised) with the largest K_j at most 4096 (f16), 14336 (Q8_0) or
  *     15616 (Q4_0, Q4_0I) so that A and the ring fit in shared memory;
  *     A_j and W_j 16-byte aligned. Anything else returns
- *     LQ_ERR_UNSUPPORTED without launching (use lq_gemv_<fmt>).
+ *     LQ_ERR_UNSUPPORTED without launching anything (use lq_gemv_<fmt>).
  *   - Device-side waits are bounded; lq_last_device_error reports a
  *     timeout. At most 64 calls may be in flight at once across streams. */
 typedef struct {
@@ -323,6 +325,10 @@ void      lq_debug_reset_counts(void);
  * ns/1000 polls (at least one), which exercises the LQ_ERR_DEVICE_TIMEOUT
  * path deterministically without any real hang. */
 void      lq_debug_set_wait_limit_ns(uint64_t ns);
+/* on != 0: lq_gemv_chain keeps problems that wait for earlier ones in one
+ * launch, waiting on a device-wide counter (the default starts a new launch
+ * at each such problem; both give the same results). For comparisons. */
+void      lq_debug_chain_waits(int on);
 /* Overrides the decode GEMV's launch plan (0 = automatic for each field):
  * CTAs per SM (1 or 2), rows per bulk-copy stage (1..8), shared memory per
  * CTA in bytes. For tuning sweeps; results do not change. Returns

@@ -1,5 +1,8 @@
 """The batched decode kernel (M = 2..8 rows of A, route 1) against the oracle.
 
+The router sends M = 2..4 here; five to eight rows run here when the route is
+forced (the tensor cores are faster there), which these tests do.
+
 The kernel keeps f32 activations and dequantises W exactly, so every element
 is held to the GEMV tolerance (1e-4 * sum|a*w| + 1e-6), not the tensor-core
 one. Shapes cover several stages per CTA with a ragged last stage, fewer rows
@@ -19,12 +22,19 @@ from helpers import check, nan_filled, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _run(lq, dev, fmt, W, A, A_dev=None):
+def _run(lq, dev, fmt, W, A, A_dev=None, force=None):
+    """lq_gemm_<fmt>; five to eight rows on the batched kernel (forced route)
+    unless force is False."""
     N, K = W.shape
     M = A.shape[0]
     Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
     C = nan_filled(M, N, dev)
-    getattr(lq, f"lq_gemm_{fmt}")(A.to(dev) if A_dev is None else A_dev, Wd, C, M, N, K)
+    if force if force is not None else M > 4:
+        lq.force_route(lq.ROUTE_STREAM)
+    try:
+        getattr(lq, f"lq_gemm_{fmt}")(A.to(dev) if A_dev is None else A_dev, Wd, C, M, N, K)
+    finally:
+        lq.force_route(0)
     torch.cuda.synchronize()
     assert lq.last_device_error() == lq.LQ_OK
     return C.cpu().numpy()
@@ -112,7 +122,7 @@ def test_batch_eight_rows_k_limits(lq, cuda_dev, fmt, K, fits):
     M, N = 8, 1536
     W, A = synthetic.draw(M, N, K, seed=K + 8, outlier_frac=0.05)
     lq.reset_counts()
-    C = _run(lq, cuda_dev, fmt, W, A)
+    C = _run(lq, cuda_dev, fmt, W, A, force=fits)
     y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=not fits)
     check(C, y, tol, f"{fmt} 8x{N}x{K}")
     assert lq.route_count(1) == (1 if fits else 0)
@@ -134,7 +144,11 @@ def test_batch_eight_row_slices_layouts_and_epilogues(lq, cuda_dev, fmt, M):
     Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), cuda_dev)
     Cd = R.to(cuda_dev)
     lq.reset_counts()
-    lq.lq_matmul_residual(fmt, A.to(cuda_dev), Wd, Cd, Cd, M, N, K)  # in place: C = A W^T + C
+    lq.force_route(lq.ROUTE_STREAM)
+    try:
+        lq.lq_matmul_residual(fmt, A.to(cuda_dev), Wd, Cd, Cd, M, N, K)  # in place: C = A W^T + C
+    finally:
+        lq.force_route(0)
     torch.cuda.synchronize()
     assert lq.route_count(1) == 1
     yr, tr = O.residual_reference(y, tol, R.numpy())
@@ -154,6 +168,7 @@ def test_batch_crossover_config_m2(lq, cuda_dev, fmt):
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
 def test_batch_crossover_config_m8(lq, cuda_dev, fmt):
+    """The eight-row workload on the batched kernel (forced route)."""
     w = synthetic.WORKLOADS[f"gemm_{fmt}_m8_6144x2048"]
     W, A = synthetic.draw_workload(w)
     lq.reset_counts()

@@ -2,7 +2,9 @@
 
 A dependent chain feeds every problem the previous problem's output (after
 = 1), so each C_j is checked against the oracle on the GPU's own C_{j-1}
-(read back), with the GEMV tolerance. Independent problems, CTAs that own no
+(read back), with the GEMV tolerance; both ways of running it are covered:
+a new launch at each dependent problem (the default) and the in-kernel
+device-wide wait (lq_debug_chain_waits). Independent problems, CTAs that own no
 rows (N < number of SMs), N = 0 and the refusal of shapes outside the fast
 path are covered as well.
 """
@@ -34,7 +36,8 @@ def _run_chain(lq, fmt, items):
     ("q4_0", [4096, 11008 // 256 * 256, 4096, 512]),
     ("f16", [2048, 1000 // 8 * 8, 2048, 256]),
 ])
-def test_chain_dependent_matches_oracle_step_by_step(lq, cuda_dev, fmt, dims):
+@pytest.mark.parametrize("waits", [False, True])
+def test_chain_dependent_matches_oracle_step_by_step(lq, cuda_dev, fmt, dims, waits):
     # problem j: K = dims[j], N = dims[j + 1]; A_j = C_{j-1} for j > 0
     torch.manual_seed(0)
     A0 = torch.randn(dims[0], dtype=torch.float32)
@@ -49,9 +52,16 @@ def test_chain_dependent_matches_oracle_step_by_step(lq, cuda_dev, fmt, dims):
         Cs.append(C)
         A = C
     lq.reset_counts()
-    assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    lq.chain_waits(waits)
+    try:
+        assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    finally:
+        lq.chain_waits(False)
     assert lq.last_device_error() == lq.LQ_OK
-    assert lq.route_count(4) == 1
+    if waits:
+        assert lq.route_count(4) == 1                 # one launch, in-kernel waits
+    else:
+        assert lq.route_count(0) == len(items)        # one streaming GEMV per dependent problem
     a_prev = A0.numpy()
     for j, (Wn, C) in enumerate(zip(Ws, Cs)):
         N, K = Wn.shape
@@ -82,10 +92,12 @@ def test_chain_independent_problems_and_small_n(lq, cuda_dev):
         check(C[None, :N].cpu().numpy(), y, tol, f"independent N={N} K={K}")
 
 
-def test_chain_runs_twice_in_a_row(lq, cuda_dev):
+@pytest.mark.parametrize("waits", [False, True])
+def test_chain_runs_twice_in_a_row(lq, cuda_dev, waits):
     # the completion counter is reset for every call: the second call's
     # dependent problem must wait for its own first problem again
     fmt = "q4_0"
+    lq.chain_waits(waits)
     K = N = 2048
     Wn, Wd = _weights(lq, fmt, N, K, 400, cuda_dev)
     A = torch.randn(K, generator=torch.Generator().manual_seed(401), dtype=torch.float32)
@@ -100,6 +112,28 @@ def test_chain_runs_twice_in_a_row(lq, cuda_dev):
         check(c1[None, :], y1, tol1, "first problem")
         y2, tol2 = O.reference(fmt, c1[None, :], O.pack(fmt, Wn), N, N)
         check(C2.cpu().numpy()[None, :], y2, tol2, "second problem (reads the first's output)")
+    lq.chain_waits(False)
+
+
+def test_chain_runs_of_independent_problems_between_dependent_ones(lq, cuda_dev):
+    """Runs of independent problems (one chain launch each) separated by
+    dependent ones: every output checked on the GPU's own inputs."""
+    fmt, K = "q8_0", 2048
+    Ws = [_weights(lq, fmt, K, K, 600 + j, cuda_dev) for j in range(6)]
+    A0 = torch.randn(K, generator=torch.Generator().manual_seed(7), dtype=torch.float32).to(cuda_dev)
+    Cs = [nan_filled(1, K, cuda_dev)[0] for _ in range(6)]
+    # 0, 1 independent; 2 reads C1; 3, 4 independent of each other (read C2); 5 reads C4
+    srcs = [A0, A0, Cs[1], Cs[2], Cs[2], Cs[4]]
+    after = [0, 0, 1, 1, 0, 1]
+    items = [(srcs[j], Ws[j][1], Cs[j], K, K, after[j]) for j in range(6)]
+    lq.reset_counts()
+    assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    assert lq.last_device_error() == lq.LQ_OK
+    assert lq.route_count(4) == 2 and lq.route_count(0) == 2   # runs {0, 1}, {2}, {3, 4}, {5}
+    for j in range(6):
+        a = srcs[j].cpu().numpy()
+        y, tol = O.reference(fmt, a[None, :], O.pack(fmt, Ws[j][0]), K, K)
+        check(Cs[j].cpu().numpy()[None, :], y, tol, f"problem {j}")
 
 
 def test_chain_refuses_shapes_outside_its_path(lq, cuda_dev):

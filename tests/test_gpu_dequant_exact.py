@@ -94,7 +94,12 @@ def test_batched_decode_dequantises_bit_exactly(lq, cuda_dev, fmt, M):
         A = _onehot(cols).to(cuda_dev)
         C = torch.full((M, N), float("nan"), dtype=torch.float32, device=cuda_dev)
         lq.reset_counts()
-        getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
+        if M > 4:
+            lq.force_route(lq.ROUTE_STREAM)  # the router sends five to eight rows to the tensor cores
+        try:
+            getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
+        finally:
+            lq.force_route(0)
         torch.cuda.synchronize()
         assert lq.route_count(1) == 1
         got, exp = C.cpu().numpy(), _expected(fmt, W, cols)

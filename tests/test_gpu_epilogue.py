@@ -57,8 +57,9 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
     (1, 4133, 4096, ROUTE_GEMV, False),
     (2, 1000, 2048, ROUTE_BATCH, False),
     (4, 2437, 1024, ROUTE_BATCH, False),
-    (6, 1000, 2048, ROUTE_BATCH, False),
+    (6, 1000, 2048, ROUTE_BATCH, False),   # five to eight rows: forced onto the batched kernel
     (8, 700, 1024, ROUTE_BATCH, False),
+    (6, 1000, 2048, ROUTE_TC, True),       # ... where the router picks the tensor cores
     (64, 1000, 2048, ROUTE_TC, True),
     (300, 777, 1024, ROUTE_TC, True),
 ]
@@ -66,9 +67,19 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
 @pytest.mark.parametrize("M,I,K,route,tc", CASES)
+def _forced(lq, M, route):
+    """Five to eight rows reach the batched kernel only by a forced route."""
+    if route == ROUTE_BATCH and M > 4:
+        lq.force_route(lq.ROUTE_STREAM)
+
+
 def test_swiglu_routes(lq, cuda_dev, fmt, M, I, K, route, tc):
     lq.reset_counts()
-    W, A, H = _swiglu(lq, cuda_dev, fmt, M, I, K, seed=M + I + K)
+    _forced(lq, M, route)
+    try:
+        W, A, H = _swiglu(lq, cuda_dev, fmt, M, I, K, seed=M + I + K)
+    finally:
+        lq.force_route(0)
     assert lq.route_count(route) == 1
     y, tol = _ref(fmt, A, W, tc)
     h, th = O.swiglu_reference(y, tol, I)
@@ -79,7 +90,11 @@ def test_swiglu_routes(lq, cuda_dev, fmt, M, I, K, route, tc):
 @pytest.mark.parametrize("M,N,K,route,tc", CASES)
 def test_residual_routes(lq, cuda_dev, fmt, M, N, K, route, tc):
     lq.reset_counts()
-    W, A, R, C = _residual(lq, cuda_dev, fmt, M, N, K, seed=M + N + K)
+    _forced(lq, M, route)
+    try:
+        W, A, R, C = _residual(lq, cuda_dev, fmt, M, N, K, seed=M + N + K)
+    finally:
+        lq.force_route(0)
     assert lq.route_count(route) == 1
     y, tol = _ref(fmt, A, W, tc)
     c, tc_ = O.residual_reference(y, tol, R)

@@ -38,11 +38,16 @@ def test_batch_kernel_timeout(lq, cuda_dev, fmt, M, N, K):
     Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
     C = nan_filled(M, N, cuda_dev)
     lq.reset_counts()
-    st = _with_tiny_limit(lq, lambda: getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K))
-    assert lq.route_count(1) == 1
-    assert st == lq.LQ_ERR_DEVICE_TIMEOUT
-    C = nan_filled(M, N, cuda_dev)
-    getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K)
+    if M > 4:
+        lq.force_route(lq.ROUTE_STREAM)  # five to eight rows: the batched kernel by a forced route
+    try:
+        st = _with_tiny_limit(lq, lambda: getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K))
+        assert lq.route_count(1) == 1
+        assert st == lq.LQ_ERR_DEVICE_TIMEOUT
+        C = nan_filled(M, N, cuda_dev)
+        getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K)
+    finally:
+        lq.force_route(0)
     torch.cuda.synchronize()
     assert lq.last_device_error() == lq.LQ_OK
     y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K)
