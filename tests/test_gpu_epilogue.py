@@ -65,14 +65,14 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
 ]
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
-@pytest.mark.parametrize("M,I,K,route,tc", CASES)
 def _forced(lq, M, route):
     """Five to eight rows reach the batched kernel only by a forced route."""
     if route == ROUTE_BATCH and M > 4:
         lq.force_route(lq.ROUTE_STREAM)
 
 
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
+@pytest.mark.parametrize("M,I,K,route,tc", CASES)
 def test_swiglu_routes(lq, cuda_dev, fmt, M, I, K, route, tc):
     lq.reset_counts()
     _forced(lq, M, route)
