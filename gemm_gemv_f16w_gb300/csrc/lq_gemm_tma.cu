@@ -34,6 +34,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -64,6 +65,7 @@ template <int FMT> constexpr int kSub = FMT == LQ_FMT_F16 ? 1 : 2;
 template <int FMT> constexpr int kRowBytes = FMT == LQ_FMT_F16 ? 256 : (FMT == LQ_FMT_Q8_0 ? 272 : 144);
 
 struct TmaGemmParams {
+  const float* A;      // resident-A mode: the f32 activations themselves
   float* C;
   const float* R;      // residual epilogue: added to every output
   int M, N, K;
@@ -73,6 +75,9 @@ struct TmaGemmParams {
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
+  int a_res;           // 1: the CTA rounds its whole A slice to bf16 into shared memory itself
+  int a_tiles;         // A tiles in shared memory: the ring's stages, or (resident) the K-steps of a rank
+  int a_perm;          // resident A, Q4_0 with interleaved nibbles: the slot order of lq_q4i.cuh
 };
 
 struct Bars {
@@ -80,6 +85,7 @@ struct Bars {
   uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
   uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
   uint64_t tmem_full;
+  uint64_t a_ready;            // resident A: the converter warps stored every stage's A tile
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -295,6 +301,56 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
   }
 }
 
+// Resident A: thread t of the 256 converter threads stores 16-byte chunks t,
+// t + 256, ... of the CTA's A slice: chunk q = (token r, K-step s, chunk cc
+// of 16 in the step); tokens past M are zeros. The eight bf16 values of a
+// chunk are A[m0 + r][128 (ks0 + s) + 8 cc ..] rounded to nearest even, or,
+// with perm (Q4_0 with interleaved nibbles), the slots 8u .. 8u+7 of their
+// block of 32 (u = cc % 4): elements 16 (u % 2) + 2 i + u / 2 of the block.
+__device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t* a_ring, uint32_t a_stage_bytes,
+                                                uint32_t atom_bytes, int bt, int m0, int ks0, int nk, int t) {
+  const int per_row = nk * 16, total = bt * per_row;
+  const uint32_t ring = smem_u32(a_ring);
+#pragma unroll 1
+  for (int q0 = t; q0 < total; q0 += 256 * 4) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + 256 * u;
+      const int r = q / per_row, c = q - r * per_row;
+      const int m = m0 + r;
+      if (q < total && m < p.M && LQ_IN_BOUNDS(m >= 0)) {
+        const float* row = p.A + static_cast<long long>(m) * p.K + 128LL * ks0;
+        const int kb = 8 * c;  // first K of the chunk within the slice
+        if (!p.a_perm) {
+          const float4 x = ldg128f(row + kb), y = ldg128f(row + kb + 4);
+          v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+          v[u][4] = y.x; v[u][5] = y.y; v[u][6] = y.z; v[u][7] = y.w;
+        } else {
+          const int blk = kb & ~31, w = (kb >> 3) & 3;
+          const float* src = row + blk + 16 * (w & 1) + (w >> 1);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[u][i] = __ldg(src + 2 * i);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[u][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + 256 * u;
+      if (q >= total) break;
+      const int r = q / per_row, c = q - r * per_row;
+      const int s = c >> 4, cc = c & 15;
+      const uint32_t addr = ring + static_cast<uint32_t>(s) * a_stage_bytes + static_cast<uint32_t>(cc >> 3) * atom_bytes +
+                            tc::sw128_offset(static_cast<uint32_t>(r), static_cast<uint32_t>(cc & 7));
+      sts128(addr, make_uint4(bf16x2(v[u][0], v[u][1]), bf16x2(v[u][2], v[u][3]), bf16x2(v[u][4], v[u][5]),
+                              bf16x2(v[u][6], v[u][7])));
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
 // Warps 2..9: converters in two groups of four (group g converts the
@@ -334,7 +390,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
   uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
   const int RR = p.raw_stages;
-  uint8_t* w_ring = base + S * a_stage_bytes;                      // RR x raw W stages
+  // resident A: one A tile per K-step of the CTA instead of a ring of S
+  uint8_t* w_ring = base + p.a_tiles * a_stage_bytes;              // RR x raw W stages
   Bars& b = *reinterpret_cast<Bars*>(w_ring + RR * kRawBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,6 +415,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(&b.empty[i], 1);
     }
     mbar_init(&b.tmem_full, 1);
+    mbar_init(&b.a_ready, 1);
     b.abort = 0;
     fence_barrier_init();
   }
@@ -375,7 +433,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // ---------------- producer ----------------
     if (lane == 0) {
       tc::prefetch_tmap(&tmW);
-      tc::prefetch_tmap(&tmA);
+      if (!p.a_res) tc::prefetch_tmap(&tmA);
     }
     auto issue_raw = [&](int j, int slot) {
       mbar_arrive_expect_tx(&b.raw_full[slot], kRawBytes);
@@ -421,7 +479,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ok = false;
         break;
       }
-      if (lane == 0) {
+      if (p.a_res) {
+        // resident A: every stage's tile is in place once the converter
+        // warps say so; the stage's producer arrival carries no bytes
+        if (ks == 0 && (!warp_wait(&b.a_ready, 0, p) || b.abort)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive(&b.full[st]);
+      } else if (lane == 0) {
         mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
         tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.full[st]);
         tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, m0,
@@ -438,15 +504,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // never leave copies in flight (waits for the last use of every slot)
     for (int j = max(0, raw_issued - RR); j < raw_issued; ++j)
       mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
-    for (int ks = max(0, issued - S); ks < issued; ++ks)
-      mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
+    if (!p.a_res)
+      for (int ks = max(0, issued - S); ks < issued; ++ks)
+        mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
     bool ok = true;
     int st = 0, lap = 0;
     auto issue_stage = [&](int ks, int sst) {
-      const uint32_t abase = smem_u32(a_ring + sst * a_stage_bytes);
+      const uint32_t abase = smem_u32(a_ring + (p.a_res ? ks : sst) * a_stage_bytes);
       const uint32_t wcol = tmem + kWCol0 + 64u * sst;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -494,6 +561,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int r = 32 * q4 + lane;  // W row in the tile = TMEM lane
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
+    if (p.a_res) {
+      // Resident A: the 256 converter threads round this CTA's A slice (bt
+      // tokens x its nk K-steps) to bf16 and store it in the layout the TMA
+      // would have written (per K-step two 64-K atoms of bt rows x 128
+      // bytes, 16-byte chunks swizzled by row % 8), once the previous kernel
+      // has completed; W keeps streaming meanwhile.
+      pdl_wait();
+      load_resident_a(p, a_ring, a_stage_bytes, atom_bytes, bt, m0, ks0, nk, static_cast<int>(threadIdx.x) - 64);
+      fence_proxy_async_smem();  // generic-proxy stores, read by the tensor core
+      named_barrier(4, 8u * 32u);
+      if (threadIdx.x == 64) mbar_arrive(&b.a_ready);
+    }
     for (int ks = g; ks < nk; ks += 2) {
       const int j = ks / SUB, half = ks % SUB, st = ks % S, rslot = j % RR;
       if (!warp_wait(&b.raw_full[rslot], (j / RR) & 1, p) || b.abort) {
@@ -743,9 +822,30 @@ int pick_split(int64_t tiles, int nraw_all, size_t smem) {
   return s;
 }
 
+// Lets a kernel instance use up to the per-block opt-in limit of shared
+// memory (once per device); the occupancy queries and launches below then
+// see the real request.
+template <int FMT, int EPI>
+cudaError_t allow_full_smem() {
+  static int configured[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    const int mx = std::min(device_info().max_smem_optin, 227 * 1024);
+    const cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  return cudaSuccess;
+}
+
 template <int FMT>
 int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
   const DeviceInfo& di = device_info();
+  if (allow_full_smem<FMT, epi::kPlain>() != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
   int s = static_cast<int>(std::min<int64_t>({8, di.sm_count / std::max<int64_t>(tiles, 1), nraw_all}));
   for (; s >= 2; --s) {
     cudaLaunchConfig_t cfg = {};
@@ -766,6 +866,57 @@ int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
     cudaGetLastError();  // a refused query is not an error of the call
   }
   return 1;
+}
+
+int pick_split_fmt(int fmt, int64_t tiles, int nraw_all, size_t smem) {
+  if (fmt == LQ_FMT_F16) return pick_split<LQ_FMT_F16>(tiles, nraw_all, smem);
+  if (fmt == LQ_FMT_Q8_0) return pick_split<LQ_FMT_Q8_0>(tiles, nraw_all, smem);
+  return pick_split<LQ_FMT_Q4_0>(tiles, nraw_all, smem);
+}
+
+// The launch plan of a call: token tile, K split, ring depths and whether A
+// is resident. Resident A: when the CTA's whole A slice (bt tokens x its
+// share of K, bf16) fits in shared memory beside two raw W stages, the CTA
+// rounds it itself and no pre-pass, workspace or A ring is needed (small M);
+// otherwise the pre-pass writes the bf16 copy of A to the workspace and the
+// CTAs stream its tiles with TMA.
+struct TmaLaunch {
+  int bt = 0, split = 1, stages = 0, raw_stages = 0, a_res = 0, a_tiles = 0;
+};
+
+TmaLaunch plan_tma(const MatmulArgs& a) {
+  TmaLaunch pl;
+  const bool sw = a.epi == epi::kSwiglu;
+  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
+  pl.bt = pick_bt(a.M, sw ? 2 * a.N : a.N);
+  const RingPlan rp = ring_plan(a.fmt, pl.bt);
+  if (rp.a_stages < 2) return TmaLaunch{};
+  pl.stages = rp.a_stages;
+  pl.raw_stages = rp.raw_stages;
+  pl.a_tiles = rp.a_stages;
+  const int sub = a.fmt == LQ_FMT_F16 ? 1 : 2;
+  const int nraw_all = static_cast<int>(a.K / kKS / sub);
+  const int bn = sw ? kBN / 2 : kBN;
+  const int64_t tiles = ((a.N + bn - 1) / bn) * ((a.M + pl.bt - 1) / pl.bt);
+  pl.split = sw ? 1 : pick_split_fmt(a.fmt, tiles, nraw_all, tma_smem_bytes(a.fmt, pl.bt, pl.a_tiles, pl.raw_stages));
+  const DeviceInfo& di = device_info();
+  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
+                           static_cast<long long>(sizeof(Bars)) - 64;
+  // at least two tiles: the epilogue reuses the area for bt x 128 floats
+  const int a_tiles = std::max(2, (nraw_all + pl.split - 1) / pl.split * sub);
+  const long long a_bytes = static_cast<long long>(a_tiles) * pl.bt * 256, raw = raw_stage_bytes(a.fmt);
+  // The CTA loads its slice before its first MMA, so only small slices pay:
+  // up to 64 KB of bf16 (a_tiles x bt <= 256) it saves 2 to 2.6 us per call
+  // at M = 5..16 (N = 6144, K = 2048, graph replay) and 0.3 to 0.9 us at
+  // M = 32; at M = 64 (96 KB) it cost 1.5 to 1.8 us. An explicit A-ring
+  // depth from lq_debug_gemm_rings keeps the streamed A.
+  if (a_bytes + 2 * raw <= budget && a_tiles * pl.bt <= 256 && g_ring_a.load() == 0) {
+    pl.a_res = 1;
+    pl.a_tiles = a_tiles;
+    pl.stages = kMaxStages;
+    pl.raw_stages = static_cast<int>(std::min<long long>(a.fmt == LQ_FMT_F16 ? 6 : 4, (budget - a_bytes) / raw));
+  }
+  return pl;
 }
 
 template <int FMT, int EPI>
@@ -795,17 +946,11 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
                              TmaGemmParams p) {
   auto kern = gemm_tma_kernel<FMT, EPI>;
   const int bn = EPI == epi::kSwiglu ? kBN / 2 : kBN;  // outputs per tile
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.stages, p.raw_stages);
-  static int configured[kMaxDevices] = {};
-  const int dev = current_device();
-  if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
-  if (configured[dev] < static_cast<int>(smem)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const size_t smem = tma_smem_bytes(FMT, p.bt, p.a_tiles, p.raw_stages);
+  {
+    const cudaError_t e = allow_full_smem<FMT, EPI>();
     if (e != cudaSuccess) return cuda_status(e);
-    configured[dev] = static_cast<int>(smem);
   }
-  const int64_t tiles = ((a.N + bn - 1) / bn) * ((a.M + p.bt - 1) / p.bt);
-  p.split = EPI == epi::kSwiglu ? 1 : pick_split<FMT>(tiles, p.K / kKS / kSub<FMT>, smem);
   const dim3 grid(static_cast<unsigned>((a.N + bn - 1) / bn * p.split),
                   static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
   cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
@@ -823,7 +968,6 @@ unsigned read_clear_gemm_tma_error() {
   return v;
 }
 
-int pick_gemm_bt(int64_t M, int64_t N) { return pick_bt(M, N); }
 
 void set_gemm_rings(int a_stages, int raw_stages) {
   g_ring_a.store(a_stages);
@@ -864,32 +1008,41 @@ cudaMemPool_t workspace_pool() {
 
 // The B operand of the tensor-core kernel (the bf16 copy of A) lives in a
 // stream-ordered workspace from the library's pool for the duration of the
-// call.
+// call, unless A is resident (small M: no workspace, no pre-pass).
 lq_status launch_gemm_tma(const MatmulArgs& a) {
-  // swiglu tiles hold 64 outputs (128 W rows): as many tiles as 2N rows
-  const int bt = pick_bt(a.M, a.epi == epi::kSwiglu ? 2 * a.N : a.N);
-  const size_t ws_bytes = gemm_tma_workspace_bytes(a.M, a.K);
+  const size_t ws_bytes = gemm_tma_workspace_bytes(a);
   void* ws = nullptr;
-  cudaMemPool_t pool = workspace_pool();
-  if (!pool) return LQ_ERR_CUDA;
-  cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
-  if (e != cudaSuccess) return LQ_ERR_CUDA;
-  lq_status st = launch_gemm_tma_ws(a, ws, bt);
-  cudaError_t ef = cudaFreeAsync(ws, a.stream);
-  if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
+  if (ws_bytes) {
+    cudaMemPool_t pool = workspace_pool();
+    if (!pool) return LQ_ERR_CUDA;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, ws_bytes, pool, a.stream);
+    if (e != cudaSuccess) return LQ_ERR_CUDA;
+  }
+  lq_status st = launch_gemm_tma_ws(a, ws);
+  if (ws) {
+    cudaError_t ef = cudaFreeAsync(ws, a.stream);
+    if (st == LQ_OK && ef != cudaSuccess) st = LQ_ERR_CUDA;
+  }
   if (st == LQ_OK) count_route(2);
   return st;
 }
 
-size_t gemm_tma_workspace_bytes(int64_t M, int64_t K) {
-  return (static_cast<size_t>(M) * static_cast<size_t>(K) * 2 + 255) / 256 * 256;
+size_t gemm_tma_workspace_bytes(const MatmulArgs& a) {
+  const TmaLaunch pl = plan_tma(a);
+  if (pl.a_res) return 0;
+  return (static_cast<size_t>(a.M) * static_cast<size_t>(a.K) * 2 + 255) / 256 * 256;
 }
 
-// Pre-pass + GEMM given a workspace of M*K bf16 values (a16, 16-byte aligned).
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
+// Pre-pass + GEMM given a workspace of gemm_tma_workspace_bytes(a) bytes
+// (the bf16 copy of A, 256-byte aligned); the GEMM alone when A is resident.
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16) {
   const int M = static_cast<int>(a.M), N = static_cast<int>(a.N), K = static_cast<int>(a.K);
-  // 1. A -> bf16 (round to nearest even)
-  {
+  const TmaLaunch pl = plan_tma(a);
+  if (pl.bt == 0) return LQ_ERR_UNSUPPORTED;
+  const int bt = pl.bt;
+  // 1. A -> bf16 (round to nearest even), unless the CTAs do it themselves
+  if (!pl.a_res) {
+    if (!a16) return LQ_ERR_INVALID_ARG;
     const long long n8 = static_cast<long long>(M) * K / 8;
     const long long want = (n8 + kPreThreads - 1) / kPreThreads;
     const long long cap = static_cast<long long>(std::max(device_info().sm_count, 1)) * 8;
@@ -908,6 +1061,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
   if (!enc) return LQ_ERR_UNSUPPORTED;
   const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
   CUtensorMap tmW, tmA;
+  std::memset(&tmA, 0, sizeof(tmA));  // resident A: never read
   {
     // swiglu: a third dimension of 2 (gate rows, up rows N rows further on)
     // and boxes of 64 + 64 rows; otherwise boxes of 128 rows
@@ -925,7 +1079,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return LQ_ERR_UNSUPPORTED;
   }
-  {
+  if (!pl.a_res) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bt)};
@@ -936,19 +1090,19 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt) {
       return LQ_ERR_UNSUPPORTED;
   }
   TmaGemmParams p;
+  p.A = a.A;
   p.C = a.C;
   p.R = a.R;
   p.M = M;
   p.N = N;
   p.K = K;
   p.bt = bt;
-  p.split = 1;  // chosen at launch (pick_split)
-  {
-    const RingPlan rp = ring_plan(a.fmt, bt);
-    p.stages = rp.a_stages;
-    p.raw_stages = rp.raw_stages;
-  }
-  if (p.stages < 2) return LQ_ERR_UNSUPPORTED;
+  p.split = pl.split;
+  p.stages = pl.stages;
+  p.raw_stages = pl.raw_stages;
+  p.a_res = pl.a_res;
+  p.a_tiles = pl.a_tiles;
+  p.a_perm = a.a_perm ? 1 : 0;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
   return launch_gemm_epi(a, tmW, tmA, p);

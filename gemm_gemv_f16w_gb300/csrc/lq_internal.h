@@ -63,14 +63,14 @@ lq_status launch_gemm_stream(const MatmulArgs& a);     // CUDA-core, small M
 lq_status launch_gemv_batch(const MatmulArgs& a);
 lq_status launch_gemm_tc(const MatmulArgs& a);         // tcgen05, operands via shared memory
 bool gemm_tc_eligible(const MatmulArgs& a);
-// tcgen05 with TMA loads and W in tensor memory; allocates its workspace
+// tcgen05 with TMA loads and W in tensor memory; takes its workspace (the
+// bf16 copy of A) from the library's pool unless A is resident (small M)
 lq_status launch_gemm_tma(const MatmulArgs& a);
-// the same given a workspace of gemm_tma_workspace_bytes(M, K) bytes (the bf16
-// copy of A, 16-byte aligned)
-lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16, int bt);
-size_t gemm_tma_workspace_bytes(int64_t M, int64_t K);
+// workspace bytes of a call (0: A is resident, no workspace and no pre-pass)
+size_t gemm_tma_workspace_bytes(const MatmulArgs& a);
+// the same given that workspace (256-byte aligned; may be null when 0)
+lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* ws);
 bool gemm_tma_eligible(const MatmulArgs& a);
-int pick_gemm_bt(int64_t M, int64_t N);  // token-tile width of the TMA kernel
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
 void set_gemm_rings(int a_stages, int raw_stages);
 

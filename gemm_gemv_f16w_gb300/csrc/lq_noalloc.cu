@@ -7,10 +7,11 @@
 // themselves and give the library none, services whose memory budget is fixed
 // at start-up, and hard real-time paths where an allocation (and the pool
 // growth behind it) is an unacceptable latency or failure point. For them
-// this entry point runs the same two
-// kernels on a workspace that is a fixed array in this library's device
-// memory, allocated once when the library is loaded on a device and held
-// until the process exits.
+// this entry point runs the same kernels
+// on a workspace that is a fixed array in this library's device memory,
+// allocated once when the library is loaded on a device and held until the
+// process exits. (Calls small enough for the GEMM to round A in shared
+// memory itself use no workspace on either entry point.)
 #include <mutex>
 
 #include "lq_internal.h"
@@ -59,12 +60,16 @@ extern "C" lq_status lq_gemm_noalloc(int fmt, const float* A, const void* W, flo
   // Only the tensor-core kernel that needs the workspace is offered here.
   if (!gemm_tma_eligible(a)) return LQ_ERR_UNSUPPORTED;
   // Beyond the fixed workspace: a clear refusal, never a larger allocation.
-  if (gemm_tma_workspace_bytes(M, K) > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
+  // Calls whose A is resident (small M) need no workspace at all.
+  const size_t need = gemm_tma_workspace_bytes(a);
+  if (need > kNoAllocBytes) return LQ_ERR_UNSUPPORTED;
   void* ws = nullptr;
-  const lq_status st = workspace_address(&ws);
-  if (st != LQ_OK) return st;
+  if (need) {
+    const lq_status st = workspace_address(&ws);
+    if (st != LQ_OK) return st;
+  }
   // Every byte the kernels read from the workspace (the bf16 rows of the M
   // tokens) is written earlier in the same call, so nothing needs clearing
   // between calls.
-  return launch_gemm_tma_ws(a, ws, pick_gemm_bt(M, N));
+  return launch_gemm_tma_ws(a, ws);
 }

@@ -336,7 +336,9 @@ void      lq_debug_chain_waits(int on);
 lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes);
 /* Overrides the tensor-core GEMM's ring depths (0 = automatic): A-tile
  * stages (2..4) and raw-weight stages (2..8); ignored when they do not fit
- * in shared memory. For tuning sweeps; results do not change. */
+ * in shared memory. A non-zero a_stages also keeps A streamed through the
+ * ring where it would otherwise be resident (small M), so that the two ways
+ * of staging A can be compared. For tuning sweeps; results do not change. */
 lq_status lq_debug_gemm_rings(int a_stages, int raw_stages);
 
 #ifdef __cplusplus

@@ -183,3 +183,48 @@ def test_tc_large_block_scales(lq, cuda_dev, fmt, d):
     assert lq.route_count(2) == 1
     y, tol = _ref(fmt, W, A)
     check(C, y, tol, f"{fmt} d={d}")
+
+
+@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
+@pytest.mark.parametrize("M,N,K,kind", [(5, 200, 512, "gemm"), (16, 1000, 1024, "gemm"),
+                                        (33, 384, 2048, "gemm"), (64, 2048, 2048, "gemm"),
+                                        (100, 130, 2048, "gemm"), (16, 300, 1024, "swiglu"),
+                                        (40, 520, 512, "residual")])
+def test_tc_resident_a_equals_streamed_a(lq, cuda_dev, fmt, M, N, K, kind):
+    """For small token tiles the GEMM rounds its A slice to bf16 in shared
+    memory itself (no pre-pass, no workspace); an explicit A-ring depth keeps
+    the streamed copy. Both hand the tensor cores the same bf16 operands in
+    the same order, so C must agree bit for bit, and with the oracle."""
+    rows = 2 * N if kind == "swiglu" else N
+    W, A = synthetic.draw(M, rows, K, seed=M * 7 + K, outlier_frac=0.05)
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), cuda_dev)
+    R = torch.randn(M, N, generator=torch.Generator().manual_seed(M))
+    outs = []
+    for a_stages in (0, 2):
+        lq.gemm_rings(a_stages, 0)
+        lq.force_route(lq.ROUTE_TENSOR_CORE)
+        lq.reset_counts()
+        try:
+            if kind == "swiglu":
+                C = nan_filled(M, N, cuda_dev)
+                lq.lq_matmul_swiglu(fmt, A.to(cuda_dev), Wd, C, M, N, K)
+            elif kind == "residual":
+                C = R.to(cuda_dev)
+                lq.lq_matmul_residual(fmt, A.to(cuda_dev), Wd, C, C, M, N, K)
+            else:
+                C = nan_filled(M, N, cuda_dev)
+                getattr(lq, f"lq_gemm_{fmt}")(A.to(cuda_dev), Wd, C, M, N, K)
+            torch.cuda.synchronize()
+        finally:
+            lq.gemm_rings(0, 0)
+            lq.force_route(0)
+        assert lq.route_count(2) == 1
+        assert lq.last_device_error() == lq.LQ_OK
+        outs.append(C.cpu().numpy())
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32)), f"{fmt} {M}x{N}x{K} {kind}"
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), rows, K, tensor_core=True)
+    if kind == "swiglu":
+        y, tol = O.swiglu_reference(y, tol, N)
+    elif kind == "residual":
+        y, tol = O.residual_reference(y, tol, R.numpy())
+    check(outs[0], y, tol, f"{fmt} {M}x{N}x{K} {kind}")

@@ -1,7 +1,7 @@
 """lq_gemm_noalloc: the tensor-core GEMM for callers that must not allocate
 device memory (runtimes that own all device memory, fixed memory budgets,
 real-time paths). It runs on a fixed workspace inside the
-library; these tests check, through the C-ABI, on two calls in a row, that
+library; these tests check, through the C-ABI, on calls in a row, that
 each output matches the CPU oracle element by element within the
 tensor-core tolerance, that it is bit-identical to the regular
 lq_gemm_<fmt> entry point (the same kernels on the same inputs), and that a
@@ -32,9 +32,11 @@ def _reference(fmt, W, A):
 
 @pytest.mark.parametrize("fmt", ["q8_0", "f16", "q4_0"])
 def test_noalloc_matches_oracle_and_regular_gemm_on_two_calls_in_a_row(lq, cuda_dev, fmt):
-    # two different problems back to back on the shared workspace; the second
-    # is smaller, so leftovers of the first would show if they were read
-    cases = [(96, 384, 1024, 21), (40, 200, 512, 22)]
+    # two different problems back to back on the shared workspace (token
+    # tiles whose A slice is larger than shared memory); the second is
+    # smaller, so leftovers of the first would show if they were read. Then
+    # two small problems whose A the GEMM keeps in shared memory itself.
+    cases = [(250, 1024, 4096, 20), (128, 4096, 4096, 23), (96, 384, 1024, 21), (40, 200, 512, 22)]
     lq.force_route(0)
     for M, N, K, seed in cases:
         W, A = synthetic.draw(M, N, K, seed=seed, outlier_frac=0.05)
