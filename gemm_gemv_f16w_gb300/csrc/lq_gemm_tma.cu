@@ -54,9 +54,9 @@ constexpr int kNumConv = 8;                        // converter warps (2 groups 
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
-constexpr int kMaxStages = 4, kMaxRawStages = 8;
-constexpr uint32_t kTmemCols = 512;                // D: [0, 256), W stages: [256, 256 + 64 * stages)
-constexpr uint32_t kWCol0 = 256;
+constexpr int kMaxStages = 4, kMaxRawStages = 8;  // A ring (streamed A), raw W ring
+constexpr int kMaxSlots = 7;                       // TMEM weight slots (resident A: up to 7)
+constexpr uint32_t kTmemCols = 512;                // D: [0, w_col0), W slots: [w_col0, w_col0 + 64 * stages)
 
 // Pipeline stages per raw stage, and bytes of one W row per raw stage (Q
 // formats: 256 K in one box; f16: 128 K as two boxes of 64 K, each 128 rows
@@ -71,7 +71,8 @@ struct TmaGemmParams {
   int M, N, K;
   int bt;              // tokens per CTA (multiple of 16, <= 256)
   int split;           // CTAs of a cluster splitting K (1: no split)
-  int stages;          // pipeline depth (2..kMaxStages)
+  int stages;          // pipeline depth = TMEM weight slots (2..kMaxStages, resident A up to kMaxSlots)
+  int w_col0;          // first TMEM column of the weight slots (the accumulator's bt columns lie below)
   int raw_stages;      // raw W ring depth (2..kMaxRawStages)
   unsigned long long wait_ns;
   unsigned wait_iters;
@@ -82,8 +83,8 @@ struct TmaGemmParams {
 
 struct Bars {
   uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
-  uint64_t full[kMaxStages];   // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
-  uint64_t empty[kMaxStages];  // the stage's MMAs completed (commit)
+  uint64_t full[kMaxSlots];    // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
+  uint64_t empty[kMaxSlots];   // the stage's MMAs completed (commit)
   uint64_t tmem_full;
   uint64_t a_ready;            // resident A: the converter warps stored every stage's A tile
   uint32_t tmem_base;
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     int st = 0, lap = 0;
     auto issue_stage = [&](int ks, int sst) {
       const uint32_t abase = smem_u32(a_ring + (p.a_res ? ks : sst) * a_stage_bytes);
-      const uint32_t wcol = tmem + kWCol0 + 64u * sst;
+      const uint32_t wcol = tmem + static_cast<uint32_t>(p.w_col0) + 64u * sst;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         break;
       }
       const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
-      const uint32_t tcol = tmem + tlane + kWCol0 + 64u * st;
+      const uint32_t tcol = tmem + tlane + static_cast<uint32_t>(p.w_col0) + 64u * st;
       uint32_t out[32];
       convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
       tc::st_32x32b_x32(tcol, out);
@@ -881,7 +882,7 @@ int pick_split_fmt(int fmt, int64_t tiles, int nraw_all, size_t smem) {
 // otherwise the pre-pass writes the bf16 copy of A to the workspace and the
 // CTAs stream its tiles with TMA.
 struct TmaLaunch {
-  int bt = 0, split = 1, stages = 0, raw_stages = 0, a_res = 0, a_tiles = 0;
+  int bt = 0, split = 1, stages = 0, raw_stages = 0, a_res = 0, a_tiles = 0, w_col0 = 256;
 };
 
 TmaLaunch plan_tma(const MatmulArgs& a) {
@@ -913,7 +914,10 @@ TmaLaunch plan_tma(const MatmulArgs& a) {
   if (a_bytes + 2 * raw <= budget && a_tiles * pl.bt <= 256 && g_ring_a.load() == 0) {
     pl.a_res = 1;
     pl.a_tiles = a_tiles;
-    pl.stages = kMaxStages;
+    // the accumulator needs bt columns; the weight slots take the rest of
+    // the 512 in steps of 64 (7 slots up to bt = 64, 4 at bt = 256)
+    pl.w_col0 = (pl.bt + 63) / 64 * 64;
+    pl.stages = std::min(kMaxSlots, (512 - pl.w_col0) / 64);
     pl.raw_stages = static_cast<int>(std::min<long long>(a.fmt == LQ_FMT_F16 ? 6 : 4, (budget - a_bytes) / raw));
   }
   return pl;
@@ -1099,6 +1103,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16) {
   p.bt = bt;
   p.split = pl.split;
   p.stages = pl.stages;
+  p.w_col0 = pl.w_col0;
   p.raw_stages = pl.raw_stages;
   p.a_res = pl.a_res;
   p.a_tiles = pl.a_tiles;

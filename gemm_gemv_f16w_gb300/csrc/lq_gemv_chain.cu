@@ -338,9 +338,26 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
 #pragma unroll
       for (int r = 0; r < kChainRows; ++r) acc[r] = 0.f;
       if (sl.ok[0]) {
+        if constexpr (FMT == LQ_FMT_F16) {
+          // f16 rows in pairs under one guard (their loads overlap); past
+          // the last row the pair's second half repeats the first, into a
+          // partial nobody reads. Measured on 10 independent f16
+          // 4096x4096 GEMVs: 5.85 against 6.23 us a GEMV; the quantised
+          // dots, whose dequantisation is the longer part, ran no faster
+          // (Q4_0) or slower (Q8_0 3.90 against 3.71 us) paired.
 #pragma unroll
-        for (int r = 0; r < kChainRows; ++r)
-          if (r < rows) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * q.row_bytes, 0);
+          for (int r = 0; r < kChainRows; r += 2)
+            if (r < rows) {
+              const uint32_t row0 = base + static_cast<uint32_t>(r) * q.row_bytes;
+              const uint32_t row1 = r + 1 < rows ? row0 + q.row_bytes : row0;
+              acc[r] += sl.dot(row0, 0);
+              acc[r + 1] += sl.dot(row1, 0);
+            }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kChainRows; ++r)
+            if (r < rows) acc[r] += sl.dot(base + static_cast<uint32_t>(r) * q.row_bytes, 0);
+        }
       }
       int r;
       const float v = transpose_reduce8(acc, lane, r);
