@@ -50,7 +50,9 @@ namespace {
 
 __device__ unsigned g_tma_err;
 
-constexpr int kNumConv = 8;                        // converter warps (2 groups of 4)
+constexpr int kNumConv = 8;                        // converter warps (kGroups groups of 4)
+constexpr int kGroups = kNumConv / 4;              // a group's 4 warps cover the 128 TMEM lanes
+constexpr int kConvThreads = kNumConv * 32;
 constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
@@ -225,15 +227,18 @@ __device__ __forceinline__ void convert64(uint32_t stage, uint32_t r, uint32_t (
   }
 }
 
-template <int FMT>
-__device__ __forceinline__ void convert64_dyn(int sub, uint32_t stage, uint32_t r, uint32_t (&out)[32]) {
-  switch (sub) {
-    case 0: convert64<FMT, 0>(stage, r, out); break;
-    case 1: convert64<FMT, 1>(stage, r, out); break;
-    case 2: convert64<FMT, 2>(stage, r, out); break;
-    default: convert64<FMT, 3>(stage, r, out); break;
-  }
+// One K-step of W row r: pieces P0 and P1 (compile-time, so that the two
+// conversions form one straight-line block the scheduler can interleave)
+// into the step's TMEM slot columns tcol .. tcol + 63.
+template <int FMT, int P0, int P1>
+__device__ __forceinline__ void convert_step(uint32_t stage, uint32_t r, uint32_t tcol) {
+  uint32_t out0[32], out1[32];
+  convert64<FMT, P0>(stage, r, out0);
+  convert64<FMT, P1>(stage, r, out1);
+  tc::st_32x32b_x32(tcol, out0);
+  tc::st_32x32b_x32(tcol + 32u, out1);
 }
+
 
 // ---------------------------------------------------------------------------
 // Split-K support: cluster barrier and loads from a peer CTA's shared memory.
@@ -258,8 +263,8 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
                                            int bt, uint32_t red, int split, int c0) {
   const int n = n0 + r;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int c = c0 + 2 * i;
+  for (int i = 0; i < (8 + kGroups - 1) / kGroups; ++i) {
+    const int c = c0 + kGroups * i;
     if (c >= (bt + 31) / 32) break;
     uint32_t v[32];
     tc::ld_32x32b_x32(tcol + 32u * c, v);
@@ -276,34 +281,37 @@ __device__ __forceinline__ void store_tile(const TmaGemmParams& p, uint32_t tcol
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) v[jj] = __float_as_uint(__uint_as_float(v[jj]) + t[jj]);
     }
-    // residual: the chunk's 32 values of R first (R may be C, so no load
-    // could move past a store), then the stores
-    float rv[32];
-    if constexpr (EPI == epi::kResidual) {
+    // residual: 16 values of R first (R may be C, so no load could move
+    // past a store), then their stores
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int m = m0 + 32 * c + jj;
-        rv[jj] = (n < p.N && 32 * c + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0))
-                     ? p.R[static_cast<long long>(m) * p.N + n]
-                     : 0.f;
+    for (int h = 0; h < 2; ++h) {
+      float rv[16];
+      if constexpr (EPI == epi::kResidual) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int m = m0 + 32 * c + 16 * h + jj;
+          rv[jj] = (n < p.N && 32 * c + 16 * h + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0))
+                       ? p.R[static_cast<long long>(m) * p.N + n]
+                       : 0.f;
+        }
       }
-    }
 #pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      const int m = m0 + 32 * c + jj;
-      if (n < p.N && 32 * c + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0)) {
-        const long long o = static_cast<long long>(m) * p.N + n;
-        if constexpr (EPI == epi::kResidual)
-          p.C[o] = __uint_as_float(v[jj]) + rv[jj];
-        else
-          p.C[o] = __uint_as_float(v[jj]);
+      for (int jj = 0; jj < 16; ++jj) {
+        const int m = m0 + 32 * c + 16 * h + jj;
+        if (n < p.N && 32 * c + 16 * h + jj < bt && m < p.M && LQ_IN_BOUNDS(n >= 0 && m >= 0)) {
+          const long long o = static_cast<long long>(m) * p.N + n;
+          if constexpr (EPI == epi::kResidual)
+            p.C[o] = __uint_as_float(v[16 * h + jj]) + rv[jj];
+          else
+            p.C[o] = __uint_as_float(v[16 * h + jj]);
+        }
       }
     }
   }
 }
 
-// Resident A: thread t of the 256 converter threads stores 16-byte chunks t,
-// t + 256, ... of the CTA's A slice: chunk q = (token r, K-step s, chunk cc
+// Resident A: thread t of the kConvThreads converter threads stores 16-byte
+// chunks t, t + kConvThreads, ... of the CTA's A slice: chunk q = (token r, K-step s, chunk cc
 // of 16 in the step); tokens past M are zeros. The eight bf16 values of a
 // chunk are A[m0 + r][128 (ks0 + s) + 8 cc ..] rounded to nearest even, or,
 // with perm (Q4_0 with interleaved nibbles), the slots 8u .. 8u+7 of their
@@ -313,11 +321,11 @@ __device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t*
   const int per_row = nk * 16, total = bt * per_row;
   const uint32_t ring = smem_u32(a_ring);
 #pragma unroll 1
-  for (int q0 = t; q0 < total; q0 += 256 * 4) {
+  for (int q0 = t; q0 < total; q0 += kConvThreads * 4) {
     float v[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int q = q0 + 256 * u;
+      const int q = q0 + kConvThreads * u;
       const int r = q / per_row, c = q - r * per_row;
       const int m = m0 + r;
       if (q < total && m < p.M && LQ_IN_BOUNDS(m >= 0)) {
@@ -340,7 +348,7 @@ __device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t*
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int q = q0 + 256 * u;
+      const int q = q0 + kConvThreads * u;
       if (q >= total) break;
       const int r = q / per_row, c = q - r * per_row;
       const int s = c >> 4, cc = c & 15;
@@ -354,10 +362,10 @@ __device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t*
 
 // ---------------------------------------------------------------------------
 // The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
-// Warps 2..9: converters in two groups of four (group g converts the
-// pipeline stages ks with ks % 2 == g: 128 K of its W rows into the stage's
-// 64 TMEM columns); then both groups run the epilogue, group g taking the
-// 32-column chunks g, g + 2, ... With split K (a cluster of CTAs sharing one
+// Warps 2..: converters in kGroups groups of four (group g converts the
+// pipeline stages ks with ks % kGroups == g: 128 K of its W rows into the
+// stage's 64 TMEM columns); then every group runs the epilogue, group g
+// taking the 32-column chunks g, g + kGroups, ... With split K (a cluster of CTAs sharing one
 // output tile), the other ranks leave their partial tiles in their own
 // shared memory and the leader adds them over distributed shared memory
 // before storing C. Per stage one barrier
@@ -574,7 +582,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t tlane = static_cast<uint32_t>(32 * q4) << 16;
     bool ok = true;
     if (p.a_res) {
-      // Resident A: the 256 converter threads round this CTA's A slice (bt
+      // Resident A: the converter threads round this CTA's A slice (bt
       // tokens x its nk K-steps) to bf16 and store it in the layout the TMA
       // would have written (per K-step two 64-K atoms of bt rows x 128
       // bytes, 16-byte chunks swizzled by row % 8), once the previous kernel
@@ -583,15 +591,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       pdl_wait();
       load_resident_a(p, a_ring, a_stage_bytes, atom_bytes, bt, m0, ks0, nk, static_cast<int>(threadIdx.x) - 64);
       fence_proxy_async_smem();  // generic-proxy stores, read by the tensor core
-      named_barrier(4, 8u * 32u);
+      named_barrier(4, kConvThreads);
       if (threadIdx.x == 64) mbar_arrive(&b.a_ready);
     }
     // positions advance incrementally (no runtime divisions in the loop):
-    // slot st = ks % S and its lap ks / S; raw stage j = ks / SUB (j moves
-    // by jstep), its slot j % RR and lap j / RR
-    int st = g, slap = 0, rslot = g / SUB, rlap = 0;
-    constexpr int jstep = 2 / SUB;
-    for (int ks = g; ks < nk; ks += 2) {
+    // slot st = ks % S and its lap ks / S; raw stage j = ks / SUB, its slot
+    // j % RR and lap j / RR
+    int st = g % S, slap = g / S, j = g / SUB, rslot = j % RR, rlap = j / RR;
+    for (int ks = g; ks < nk; ks += kGroups) {
       const int half = ks % SUB;
       if (!warp_wait(&b.raw_full[rslot], rlap & 1, p) || b.abort) {
         ok = false;
@@ -603,11 +610,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
       const uint32_t stage = smem_u32(w_ring + rslot * kRawBytes);
       const uint32_t tcol = tmem + tlane + static_cast<uint32_t>(p.w_col0) + 64u * st;
-      uint32_t out[32];
-      convert64_dyn<FMT>(2 * half, stage, static_cast<uint32_t>(r), out);
-      tc::st_32x32b_x32(tcol, out);
-      convert64_dyn<FMT>(2 * half + 1, stage, static_cast<uint32_t>(r), out);
-      tc::st_32x32b_x32(tcol + 32u, out);
+      if (SUB == 1 || half == 0)
+        convert_step<FMT, 0, 1>(stage, static_cast<uint32_t>(r), tcol);
+      else
+        convert_step<FMT, 2, 3>(stage, static_cast<uint32_t>(r), tcol);
       tc::wait_st();
       tc::fence_before_sync();
       __syncwarp();
@@ -615,17 +621,19 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         mbar_arrive(&b.full[st]);
         mbar_arrive(&b.raw_empty[rslot]);
       }
-      st += 2;
-      if (st >= S) { st -= S; ++slap; }
-      rslot += jstep;
-      if (rslot >= RR) { rslot -= RR; ++rlap; }
+      st += kGroups;
+      while (st >= S) { st -= S; ++slap; }
+      const int j2 = (ks + kGroups) / SUB;
+      rslot += j2 - j;
+      j = j2;
+      while (rslot >= RR) { rslot -= RR; ++rlap; }
     }
     if (!ok && lane == 0) {
       record_error(kDevErrTimeout);
       b.abort = 1;
     }
     {
-      // ---------------- epilogue (both groups: 32-column chunks g, g + 2, ...) ----------------
+      // ---------------- epilogue (every group: 32-column chunks g, g + kGroups, ...) ----------------
       // C (and R) are touched only once the previous kernel on the stream
       // has completed (by now griddepcontrol.wait returns at once)
       pdl_wait();
@@ -638,14 +646,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       epi = have && !b.abort;
       if constexpr (SWIGLU) {
         // gate (lanes 0-63) and up (lanes 64-127) accumulators
-        // -> the A ring as [token][gate 64 | up 64]; then all eight warps
+        // -> the A ring as [token][gate 64 | up 64]; then all converter warps
         // combine (token, output) pairs in one rolled loop and store 64
         // consecutive outputs of a token together
         float* xch = reinterpret_cast<float*>(a_ring);
         if (epi) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int c = g + 2 * i;
+          for (int i = 0; i < (8 + kGroups - 1) / kGroups; ++i) {
+            const int c = g + kGroups * i;
             if (c >= (bt + 31) / 32) break;
             uint32_t v[32];
             tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
@@ -655,12 +663,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
               if (32 * c + jj < bt) xch[(32 * c + jj) * 128 + r] = __uint_as_float(v[jj]);
           }
         }
-        named_barrier(3, 8u * 32u);  // the eight epilogue warps, whatever their outcome
+        named_barrier(3, kConvThreads);  // the epilogue warps, whatever their outcome
         if (epi) {
-          const int t0 = static_cast<int>(threadIdx.x) - 64;  // 0 .. 255 over warps 2..9
+          const int t0 = static_cast<int>(threadIdx.x) - 64;  // 0 .. kConvThreads - 1 over the converter warps
           const int rows = min(bt, p.M - m0);
 #pragma unroll 1
-          for (int idx = t0; idx < rows * 64; idx += 256) {
+          for (int idx = t0; idx < rows * 64; idx += kConvThreads) {
             const int tok = idx >> 6, j = idx & 63, n = n0 + j;
             if (n < p.N && LQ_IN_BOUNDS(m0 + tok < p.M && m0 + tok >= 0))
               p.C[static_cast<long long>(m0 + tok) * p.N + n] = epi::swiglu(xch[tok * 128 + j], xch[tok * 128 + 64 + j]);
@@ -673,7 +681,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         // idle now), token-major so that the 32 lanes write 32 rows in a row
         float* red = reinterpret_cast<float*>(a_ring);
 #pragma unroll 1
-        for (int c = g; c < (bt + 31) / 32; c += 2) {
+        for (int c = g; c < (bt + 31) / 32; c += kGroups) {
           uint32_t v[32];
           tc::ld_32x32b_x32(tmem + tlane + 32u * c, v);
           tc::wait_ld();
@@ -787,6 +795,17 @@ struct RingPlan {
 };
 std::atomic<int> g_ring_a{0}, g_ring_raw{0};  // debug override (0 = automatic)
 
+// Raw W ring depth from the number of stages that fit. A converter group
+// waits on a raw slot's next phase by parity, which is sound only if it has
+// itself seen the slot's previous phase complete (copies may land out of
+// order). With SUB = 2 both groups take every raw stage in order; with
+// SUB = 1 (f16) group g takes the stages j with j % kGroups == g, so the
+// depth is a multiple of kGroups and every slot has a single group.
+int raw_ring_depth(int fmt, long long fit) {
+  const long long unit = fmt == LQ_FMT_F16 ? kGroups : (kGroups + 1) / 2;
+  return static_cast<int>(fit / unit * unit);
+}
+
 RingPlan ring_plan(int fmt, int bt) {
   const DeviceInfo& di = device_info();
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 -
@@ -794,7 +813,7 @@ RingPlan ring_plan(int fmt, int bt) {
   const long long a_stage = static_cast<long long>(bt) * 256, raw = raw_stage_bytes(fmt);
   RingPlan rp;
   const int raw_cap = fmt == LQ_FMT_F16 ? 6 : 4;
-  rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 2 * a_stage) / raw));
+  rp.raw_stages = raw_ring_depth(fmt, std::min<long long>(raw_cap, (budget - 2 * a_stage) / raw));
   if (rp.raw_stages < 2) return RingPlan{};
   rp.a_stages = static_cast<int>(std::min<long long>(kMaxStages, (budget - rp.raw_stages * raw) / a_stage));
   if (rp.a_stages < 2) return RingPlan{};
@@ -802,12 +821,13 @@ RingPlan ring_plan(int fmt, int bt) {
   // two raw stages measured about 5 % faster at M = 512 (f16 and Q8_0).
   if (rp.a_stages == 2 && 3 * a_stage + 2 * raw <= budget) {
     rp.a_stages = 3;
-    rp.raw_stages = static_cast<int>(std::min<long long>(raw_cap, (budget - 3 * a_stage) / raw));
+    rp.raw_stages = raw_ring_depth(fmt, std::min<long long>(raw_cap, (budget - 3 * a_stage) / raw));
   }
   const int oa = g_ring_a.load(), orr = g_ring_raw.load();
   if (oa || orr) {
     const int a2 = oa ? oa : rp.a_stages, r2 = orr ? orr : rp.raw_stages;
-    if (a2 >= 2 && a2 <= kMaxStages && r2 >= 2 && r2 <= kMaxRawStages && a2 * a_stage + r2 * raw <= budget)
+    if (a2 >= 2 && a2 <= kMaxStages && r2 >= 2 && r2 <= kMaxRawStages && r2 == raw_ring_depth(fmt, r2) &&
+        a2 * a_stage + r2 * raw <= budget)
       return RingPlan{a2, r2};
   }
   return rp;
@@ -939,7 +959,7 @@ TmaLaunch plan_tma(const MatmulArgs& a) {
     // the 512 in steps of 64 (7 slots up to bt = 64, 4 at bt = 256)
     pl.w_col0 = (pl.bt + 63) / 64 * 64;
     pl.stages = std::min(kMaxSlots, (512 - pl.w_col0) / 64);
-    pl.raw_stages = static_cast<int>(std::min<long long>(a.fmt == LQ_FMT_F16 ? 6 : 4, (budget - a_bytes) / raw));
+    pl.raw_stages = raw_ring_depth(a.fmt, std::min<long long>(a.fmt == LQ_FMT_F16 ? 6 : 4, (budget - a_bytes) / raw));
   }
   return pl;
 }
