@@ -247,10 +247,15 @@ class Workbench:
             self.step()          # eager warm-up (sets kernel attributes)
         torch.cuda.current_stream(self.dev).wait_stream(s)
         torch.cuda.synchronize(self.dev)
-        if self.w.M >= 2 and self.lq.route_count(1) >= self.R:
-            # M = 2..4 on the batched decode kernel: one launch a matmul
-            self.route = "batch"
-            self.kernels_per_step = self.R
+        if self.w.M >= 2:
+            # launches a step, counted on the eager step: one a matmul, plus
+            # the tcgen05 route's A pre-pass where it runs
+            lq = self.lq
+            self.kernels_per_step = sum(lq.route_count(r) for r in (1, 2, lq.ROUTE_WARP_MMA, lq.COUNT_PREPASS))
+            if lq.route_count(1) >= self.R:
+                self.route = "batch"        # M = 2..4: the CUDA-core batched decode kernel
+            elif lq.route_count(lq.ROUTE_WARP_MMA) >= self.R:
+                self.route = "warp-mma"     # M = 5..16: warp-level MMAs
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step()
@@ -522,7 +527,7 @@ def main():
     if w.M == 1:
         kernel = KERNEL_OF_MODE[wb.mode]
     else:
-        kernel = "gemv_batch_kernel" if wb.route == "batch" else "gemm_tma_kernel"
+        kernel = {"batch": "gemv_batch_kernel", "warp-mma": "gemm_small_kernel"}.get(wb.route, "gemm_tma_kernel")
     launches_per_step = wb.kernels_per_step
     per_gemv = dt / (steps * wb.R)          # one matmul of the workload
     val1, unit, bound = rate(wb, per_gemv)
@@ -551,9 +556,13 @@ def main():
         runs.append((name, "auto"))
         if synthetic.WORKLOADS[name].M == 1:
             runs.append((name, "calls"))  # the decode GEMVs both as a chain and as separate calls
-        if 1 < synthetic.WORKLOADS[name].M <= 8:
-            # the batched decode kernel against the tensor-core route
-            runs.append((name, "batch" if synthetic.WORKLOADS[name].M > 4 else "tc"))
+        m = synthetic.WORKLOADS[name].M
+        if 1 < m <= 16:
+            # the router's kernel against the others: the tcgen05 kernel, and
+            # the batched decode kernel where the warp-MMA kernel is picked
+            runs.append((name, "tc"))
+            if 4 < m <= 8:
+                runs.append((name, "batch"))
     if w.M == 1 and args.extras != "none":
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs
     lmhead = "gemv_f16_lmhead_151936x2048"

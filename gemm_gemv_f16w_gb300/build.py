@@ -24,7 +24,7 @@ DEBUG_BUILD = os.path.join(PKG, "_build_debug")
 DEBUG_LIB = os.path.join(PKG, "liblq_debug.so")
 
 CUDA_SOURCES = ["lq_api.cu", "lq_gemv.cu", "lq_gemv_chain.cu", "lq_gemv_batch.cu", "lq_argmax.cu", "lq_topk.cu", "lq_gemm.cu", "lq_gemm_tma.cu",
-                "lq_noalloc.cu"]
+                "lq_noalloc.cu", "lq_gemm_small.cu"]
 CXX_SOURCES = ["lq_pack.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -17,7 +17,7 @@ namespace lq {
 
 namespace {
 std::atomic<int> g_force_route{0};
-std::atomic<uint64_t> g_route_count[5];
+std::atomic<uint64_t> g_route_count[7];
 std::atomic<unsigned long long> g_wait_ns{0};
 std::mutex g_info_mu;
 DeviceInfo g_info[kMaxDevices];
@@ -60,7 +60,7 @@ unsigned wait_limit_iters() {
 }
 
 void count_route(int route) {
-  if (route >= 0 && route < 5) g_route_count[route].fetch_add(1);
+  if (route >= 0 && route < 7) g_route_count[route].fetch_add(1);
 }
 
 namespace {
@@ -136,13 +136,24 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
       if (gemm_tma_eligible(a)) return launch_gemm_tma(a);
       return gemm_tc_eligible(a) ? launch_gemm_tc(a) : LQ_ERR_UNSUPPORTED;
     case 3: return launch_gemv_generic(a);
+    case 5: return launch_gemm_small(a);
     default: break;
   }
-  // M = 2..4: one pass over W on the CUDA cores beats the tensor-core
-  // kernel's fixed latencies. From five rows the batched kernel's eight-row
-  // slices (8 warps of up to 255 registers) are slower than the tensor
-  // cores (Q8_0 M = 8, N = 6144, K = 2048: 17.2 against 13.7 us), so they
-  // run only when the route is forced (lq_debug_force_route(1)).
+  // M = 2: one pass over W on the CUDA cores. M = 3..16: the warp-MMA
+  // tensor-core kernel (N = 6144, K = 2048 Q8_0 / f16 / Q4_0: 8.4 / 8.7 /
+  // 7.8 us at M = 4 against 11.1 / 11.5 / 10.1 on the batched kernel and
+  // 10.7 / 10.2 / 10.7 on the tcgen05 kernel; at M = 2 the batched kernel's
+  // 7.7 / 9.2 / 6.9 against 8.4 / 8.7 / 8.0). The batched kernel takes
+  // three to eight rows by a forced route (lq_debug_force_route(1)) or the
+  // shapes the warp-MMA kernel does not (up to four rows).
+  if (M <= 2) {
+    st = launch_gemv_batch(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
+  if (M <= 16) {
+    st = launch_gemm_small(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
   if (M <= 4) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
@@ -173,9 +184,20 @@ lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, fl
     case 2:
       return gemm_tma_eligible(a) ? launch_gemm_tma(a) : LQ_ERR_UNSUPPORTED;
     case 3: return launch_gemv_generic(a);
+    case 5: return launch_gemm_small(a);
     default: break;
   }
   if (M == 1) return launch_gemv(a);  // falls back to the generic kernel itself
+  // as do_gemm; the warp-MMA kernel has no SwiGLU epilogue, which keeps the
+  // batched kernel up to four rows
+  if (M <= 2) {
+    st = launch_gemv_batch(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
+  if (M <= 16) {
+    st = launch_gemm_small(a);
+    if (st != LQ_ERR_UNSUPPORTED) return st;
+  }
   if (M <= 4) {
     st = launch_gemv_batch(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
@@ -254,7 +276,8 @@ lq_status lq_last_device_error(void) {
   const unsigned c = read_clear_gemm_tma_error();
   const unsigned d = read_clear_chain_error();
   const unsigned e = read_clear_batch_error();
-  const unsigned v = a ? a : (b ? b : (c ? c : (d ? d : e)));
+  const unsigned f = read_clear_small_error();
+  const unsigned v = a ? a : (b ? b : (c ? c : (d ? d : (e ? e : f))));
   if (v == 0) return LQ_OK;
   return static_cast<lq_status>(v);
 }
@@ -343,12 +366,12 @@ const char* lq_version(void) { return "lq 0.2.0 (sm_103a)"; }
 #endif
 
 lq_status lq_debug_force_route(int route) {
-  if (route < 0 || route > 3) return LQ_ERR_INVALID_ARG;
+  if (route < 0 || route > 5 || route == 4) return LQ_ERR_INVALID_ARG;
   g_force_route.store(route);
   return LQ_OK;
 }
 uint64_t lq_debug_route_count(int route) {
-  if (route < 0 || route > 4) return 0;
+  if (route < 0 || route > 6) return 0;
   return g_route_count[route].load();
 }
 void lq_debug_reset_counts(void) {

@@ -1,0 +1,487 @@
+// The prefill GEMM for a few rows of A (M = 2..16): C = A W^T on the tensor
+// cores with warp-level MMAs, every weight read from HBM once.
+//
+// For so few tokens the weight stream sets the pace, as in the decode GEMV,
+// and the tcgen05 kernel (lq_gemm_tma.cu) spends most of a call on fixed
+// costs: the TMEM allocation, a K split over clusters of CTAs and the
+// reduction of their partial tiles, and the MMA pipeline's fill and drain.
+// This kernel keeps everything in registers instead:
+//
+//  * one CTA per SM owns a contiguous range of W rows (at most 128), streamed
+//    as stages of 256 K through a ring in shared memory by TMA tensor copies
+//    (Q8_0 / Q4_0: one box of the rows' 272 / 144 bytes of that K; f16: four
+//    128-byte-swizzled boxes of 64 halves), the first stages' weights issued
+//    at kernel start (weights depend on nothing);
+//  * each stage also holds the same 256 K of A (the M rows, f32, in one box;
+//    rows M..15 of every slot are zeroed once), copied once the previous
+//    kernel on the stream has completed; the lanes round their A values to
+//    bf16 (nearest even) as they build the MMA operands;
+//  * warp w takes block w % 8 (32 K) of every stage, for the 8-row tiles
+//    t = w / 8, w / 8 + 2, ...: each lane dequantises 8 weights of one row
+//    (lane / 4) exactly in f32 and rounds them once to bf16, the same operand
+//    as the tcgen05 kernel's, and two mma.m16n8k16 (bf16 x bf16 -> f32; A =
+//    16 tokens, B = 8 W rows) add the block to the tile's accumulator. Within
+//    a block the lanes take consecutive codes (lane % 4 takes codes 8q ..
+//    8q+7; Q4_0: the low and high nibbles of bytes 4q .. 4q+3), so the MMA's
+//    K order is a fixed permutation of the block, and each lane reads the A
+//    values of the same positions;
+//  * after the last stage the 8 block positions' partial tiles are added in a
+//    fixed order through shared memory and C (plus R with the residual
+//    epilogue) is stored.
+//
+// The tolerance is the tensor-core route's (A and W rounded to bf16, f32
+// accumulation). Every wait is bounded (LQ_ERR_DEVICE_TIMEOUT on expiry).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "lq_device.cuh"
+#include "lq_epilogue.cuh"
+#include "lq_internal.h"
+#include "lq_tcgen05.cuh"
+
+namespace lq {
+namespace {
+
+__device__ unsigned g_small_err;
+__device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_small_err, 0u, code); }
+
+constexpr int kSWarps = 16, kSThreads = kSWarps * 32;
+constexpr int kPieceK = 256;      // K of one weight stage: 8 blocks of 32
+constexpr int kSMaxStages = 8;
+constexpr int kSMaxTiles = 16;    // 8-row W tiles of a CTA (128 rows)
+constexpr int kSTokens = 16;      // the MMA's M: rows of A, zero-padded
+
+// Bytes of one W row's 256 K in a stage.
+__host__ __device__ constexpr int piece_row_bytes(int fmt) {
+  return fmt == LQ_FMT_F16 ? 512 : (fmt == LQ_FMT_Q8_0 ? 272 : 144);
+}
+
+constexpr unsigned kSABytes = kSTokens * kPieceK * 4;  // A of one stage: 16 rows x 256 f32
+
+struct SmallParams {
+  float* C;
+  const float* R;       // residual epilogue: added to every output
+  int M, N, K;
+  int rows_box;         // W rows of a stage (the copy's box), at most 128
+  int stages;           // ring depth
+  unsigned w_bytes;     // weight bytes of a stage
+  unsigned slot_bytes;  // ring slot: A (kSABytes), then the weights; a multiple of 1024
+  unsigned ring_bytes;  // ring (reused for the partial tiles at the end)
+  unsigned long long wait_ns;
+  unsigned wait_iters;
+};
+
+struct SmallBars {
+  uint64_t full[kSMaxStages];  // the stage's bytes landed
+  int done[kSMaxStages];       // warps finished with the slot's current stage
+  int last[kSMaxStages];       // last stage issued into each slot (-1: none)
+  volatile int abort;
+};
+constexpr int kSBarsBytes = 256;
+static_assert(sizeof(SmallBars) <= kSBarsBytes, "barrier block");
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The lane's 8 weights of W row `row` (of the stage), block bp, codes 8q ..
+// 8q+7 (Q4_0: low nibbles of bytes 4q .. 4q+3, then their high nibbles), as
+// four bf16 pairs in the MMA's K order. Each weight is formed exactly in f32
+// (an f16 widened; d * q, or d * (q - 8), from the code placed in the
+// mantissa of 2^23 by one byte-permute and one exact packed add) and rounded
+// once to bf16 (nearest even).
+template <int FMT>
+__device__ __forceinline__ void load_weights(uint32_t stage, int rows_box, int row, int bp, int q,
+                                             uint32_t (&bw)[4]) {
+  if constexpr (FMT == LQ_FMT_F16) {
+    // box bp / 2: rows x 128 bytes, 16-byte chunk c of row r at chunk c ^ (r % 8)
+    const uint32_t c = static_cast<uint32_t>((bp & 1) * 4 + q) ^ static_cast<uint32_t>(row & 7);
+    const uint4 v = lds128(stage + static_cast<uint32_t>((bp >> 1) * rows_box * 128 + row * 128) + (c << 4));
+    const uint32_t h[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[j]));
+      bw[j] = pack_bf16x2(f.x, f.y);
+    }
+  } else if constexpr (FMT == LQ_FMT_Q8_0) {
+    // block bp at byte 34 bp of the row's 272: scale, then 32 codes; even
+    // blocks' codes start 2 bytes into a word, odd blocks' on a word
+    const uint32_t rowa = stage + static_cast<uint32_t>(row) * 272u;
+    const bool mis = (bp & 1) == 0;
+    const uint32_t o = 34u * static_cast<uint32_t>(bp) + 2u + 8u * static_cast<uint32_t>(q);
+    const uint32_t wa = rowa + (o & ~3u);
+    const uint32_t w0 = lds32(wa), w1 = lds32(wa + 4u), w2 = mis ? lds32(wa + 8u) : 0u;
+    const uint32_t sh = mis ? 16u : 0u;
+    const uint32_t x0 = __funnelshift_r(w0, w1, sh) ^ 0x80808080u;  // codes 8q .. 8q+3, sign bits flipped
+    const uint32_t x1 = __funnelshift_r(w1, w2, sh) ^ 0x80808080u;  // codes 8q+4 .. 8q+7
+    const uint32_t dw = lds32(rowa + ((34u * static_cast<uint32_t>(bp)) & ~3u));
+    const float d = f16_lo(mis ? dw : (dw >> 16));
+    const float2 dd = make_float2(d, d), mb = make_float2(-kMagicS8, -kMagicS8);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x = j < 2 ? x0 : x1;
+      const int i = 2 * (j & 1);
+      const float2 w = fmul2(fadd2(make_float2(s8_to_magic(x, i), s8_to_magic(x, i + 1)), mb), dd);
+      bw[j] = pack_bf16x2(w.x, w.y);
+    }
+  } else {
+    // block bp at byte 18 bp of the row's 144: scale, then 16 bytes of
+    // nibbles (byte j: code j low, code j + 16 high)
+    const uint32_t rowa = stage + static_cast<uint32_t>(row) * 144u;
+    const bool mis = (bp & 1) == 0;
+    const uint32_t o = 18u * static_cast<uint32_t>(bp) + 2u + 4u * static_cast<uint32_t>(q);
+    const uint32_t wa = rowa + (o & ~3u);
+    const uint32_t w0 = lds32(wa), w1 = mis ? lds32(wa + 4u) : 0u;
+    const uint32_t x = __funnelshift_r(w0, w1, mis ? 16u : 0u);  // bytes 4q .. 4q+3
+    const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+    const uint32_t dw = lds32(rowa + ((18u * static_cast<uint32_t>(bp)) & ~3u));
+    const float d = f16_lo(mis ? dw : (dw >> 16));
+    const float2 dd = make_float2(d, d), m8 = make_float2(-kMagicQ4, -kMagicQ4);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t x2 = j < 2 ? lo : hi;
+      const int i = 2 * (j & 1);
+      const float2 w = fmul2(fadd2(make_float2(s8_to_magic(x2, i), s8_to_magic(x2, i + 1)), m8), dd);
+      bw[j] = pack_bf16x2(w.x, w.y);
+    }
+  }
+}
+
+// The lane's A values of token row `row` (0..15) for block bp of a stage, in
+// the order of its weights (Q8_0 / f16: elements 8q .. 8q+7 of the block;
+// Q4_0: 4q .. 4q+3 and 16+4q .. 19+4q), as four bf16 pairs (nearest even).
+// The stage's A is 16 rows of 256 values (1 KB each). (One box a stage:
+// eight 128-byte-swizzled boxes, free of bank conflicts, issued eight times
+// as many copies and measured slower.)
+template <int FMT>
+__device__ __forceinline__ void load_a(uint32_t sa, int row, int bp, int q, uint32_t (&a)[4]) {
+  const uint32_t rbase = sa + static_cast<uint32_t>(row * 1024 + bp * 128);
+  const uint32_t c0 = FMT == LQ_FMT_Q4_0 ? q : 2 * q, c1 = FMT == LQ_FMT_Q4_0 ? 4 + q : 2 * q + 1;
+  const float4 x = lds128f(rbase + (c0 << 4));
+  const float4 y = lds128f(rbase + (c1 << 4));
+  a[0] = pack_bf16x2(x.x, x.y);
+  a[1] = pack_bf16x2(x.z, x.w);
+  a[2] = pack_bf16x2(y.x, y.y);
+  a[3] = pack_bf16x2(y.z, y.w);
+}
+
+template <int FMT, int EPI>
+__global__ void __launch_bounds__(kSThreads, 1)
+    gemm_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                      const SmallParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u = smem_u32(smem_raw);
+  uint8_t* ring = smem_raw + (((raw_u + 1023u) & ~1023u) - raw_u);  // 1024-aligned (swizzled boxes)
+  SmallBars& b = *reinterpret_cast<SmallBars*>(ring + p.ring_bytes);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = p.stages, npieces = p.K / kPieceK;
+  const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.N / gridDim.x);
+  const int nrows = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.N / gridDim.x) - r0;
+  const int T = (nrows + 7) / 8;  // 8-row tiles
+
+  // stage `piece` into ring slot `slot`: the weights, then (once the
+  // previous kernel has completed) A; one barrier counts both
+  auto issue_w = [&](int piece, int slot) {
+    uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes + kSABytes;
+    mbar_arrive_expect_tx(&b.full[slot], p.w_bytes + static_cast<unsigned>(p.M) * kPieceK * 4u);
+    if constexpr (FMT == LQ_FMT_F16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        tc::tma_load_2d(dst + i * p.rows_box * 128, &tmW, kPieceK * piece + 64 * i, r0, &b.full[slot]);
+    } else {
+      tc::tma_load_3d(dst, &tmW, 0, piece, r0, &b.full[slot]);
+    }
+    b.last[slot] = piece;
+  };
+  auto issue_a = [&](int piece, int slot) {
+    tc::tma_load_2d(ring + static_cast<size_t>(slot) * p.slot_bytes, &tmA, kPieceK * piece, 0, &b.full[slot]);
+  };
+  const int first = min(S, npieces);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&b.full[s], 1);
+      b.done[s] = 0;
+      b.last[s] = -1;
+    }
+    b.abort = 0;
+    fence_barrier_init();
+    tc::prefetch_tmap(&tmW);
+    tc::prefetch_tmap(&tmA);
+    for (int j = 0; j < first; ++j) issue_w(j, j);  // weights depend on nothing
+  }
+  // rows M..15 of every slot's A: zeros (the copies bring rows 0..M-1)
+  for (int i = threadIdx.x; i < S * (kSTokens - p.M) * (kPieceK / 4); i += kSThreads) {
+    const int per = (kSTokens - p.M) * (kPieceK / 4), sl = i / per, j = i - sl * per;
+    sts128(smem_u32(ring) + static_cast<uint32_t>(sl) * p.slot_bytes + static_cast<uint32_t>(p.M) * kPieceK * 4u +
+               16u * static_cast<uint32_t>(j),
+           make_uint4(0u, 0u, 0u, 0u));
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // A (and C) only once the previous kernel on the stream has completed
+  pdl_wait();
+  if (threadIdx.x == 0)
+    for (int j = 0; j < first; ++j) issue_a(j, j);
+
+  // ---- main loop: warp (bp, th) takes block bp of each stage for the tiles
+  // t = th, th + 2, ...; lane (g, q): W row 8t + g, codes 8q .. 8q+7, and
+  // the A values of tokens g and g + 8 in the same order
+  const int bp = warp & 7, th = warp >> 3, g = lane >> 2, q = lane & 3;
+  float acc[kSMaxTiles / 2][4];
+#pragma unroll
+  for (int i = 0; i < kSMaxTiles / 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  int s = 0;
+  uint32_t ph = 0;
+#pragma unroll 1
+  for (int piece = 0; piece < npieces; ++piece) {
+    const bool ok = mbar_wait(&b.full[s], ph, p.wait_ns, p.wait_iters);
+    if (!__all_sync(0xffffffffu, ok) || b.abort) {
+      if (lane == 0) {
+        record_error(kDevErrTimeout);
+        b.abort = 1;
+      }
+      break;
+    }
+    const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
+    uint32_t alo[4], ahi[4];
+    load_a<FMT>(slot, g, bp, q, alo);
+    load_a<FMT>(slot, g + 8, bp, q, ahi);
+    // (every tile's weights loaded first, with two accumulators a tile,
+    // measured slower: 10.7 against 8.6 us at Q8_0 M = 16, 6144 x 2048)
+#pragma unroll
+    for (int i = 0; i < kSMaxTiles / 2; ++i) {
+      const int t = th + 2 * i;
+      if (t >= T) break;
+      uint32_t bw[4];
+      load_weights<FMT>(slot + kSABytes, p.rows_box, 8 * t + g, bp, q, bw);
+      mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], bw[0], bw[1]);  // the lane's values 0 .. 3
+      mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], bw[2], bw[3]);  // values 4 .. 7
+    }
+    // The last warp done with the slot refills it (every warp's reads of it
+    // have returned: their values went into the MMAs above).
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&b.done[s], 1) == kSWarps - 1) {
+        b.done[s] = 0;
+        if (piece + S < npieces) {
+          fence_proxy_async_smem();  // the generic reads above, before the copies' writes
+          issue_w(piece + S, s);
+          issue_a(piece + S, s);
+        }
+      }
+    }
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  __syncthreads();
+  if (b.abort) {
+    // no copy may still be in flight when the CTA exits
+    if (threadIdx.x == 0)
+      for (int k = 0; k < S; ++k)
+        if (b.last[k] >= 0) mbar_wait(&b.full[k], static_cast<uint32_t>(b.last[k] / S) & 1u, kDrainWaitNs);
+    return;
+  }
+
+  // ---- the 8 block positions' partial tiles, added in a fixed order
+  // (shared memory of the ring, every stage consumed): red[t][bp][m][n]
+  float* red = reinterpret_cast<float*>(ring);
+#pragma unroll
+  for (int i = 0; i < kSMaxTiles / 2; ++i) {
+    const int t = th + 2 * i;
+    if (t >= T) break;
+    float* tile = red + (t * 8 + bp) * 128;
+    *reinterpret_cast<float2*>(tile + g * 8 + 2 * q) = make_float2(acc[i][0], acc[i][1]);
+    *reinterpret_cast<float2*>(tile + (g + 8) * 8 + 2 * q) = make_float2(acc[i][2], acc[i][3]);
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int idx = threadIdx.x; idx < T * 128; idx += kSThreads) {
+    const int t = idx >> 7, e = idx & 127, m = e >> 3, n = 8 * t + (e & 7);
+    if (m < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum += red[(t * 8 + k) * 128 + e];
+      const long long o = static_cast<long long>(m) * p.N + r0 + n;
+      if constexpr (EPI == epi::kResidual)
+        p.C[o] = sum + p.R[o];
+      else
+        p.C[o] = sum;
+    }
+  }
+}
+
+template <int FMT, int EPI>
+lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
+                         int G, size_t smem) {
+  auto kern = gemm_small_kernel<FMT, EPI>;
+  static int configured[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
+  if (!configured[dev]) {
+    const int mx = std::min(device_info().max_smem_optin, 227 * 1024);
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e != cudaSuccess) return cuda_status(e);
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(G));
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ta, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+template <int FMT>
+lq_status launch_small_fmt(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
+                           int G, size_t smem) {
+  if (a.epi == epi::kResidual) return launch_small_t<FMT, epi::kResidual>(a, tw, ta, p, G, smem);
+  return launch_small_t<FMT, epi::kPlain>(a, tw, ta, p, G, smem);
+}
+
+struct SmallPlan {
+  int G = 0, rows_box = 0, stages = 0;
+  unsigned w_bytes = 0, slot_bytes = 0, ring_bytes = 0;
+  size_t smem = 0;
+};
+
+bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
+  if (a.fmt != LQ_FMT_F16 && a.fmt != LQ_FMT_Q8_0 && a.fmt != LQ_FMT_Q4_0) return false;
+  if (a.a_perm || (a.epi != epi::kPlain && a.epi != epi::kResidual)) return false;
+  if (a.M < 2 || a.M > kSTokens || a.K % kPieceK != 0 || a.K > (1 << 20) || a.N < 1 || a.N >= (1LL << 30))
+    return false;
+  if (!aligned_to(a.A, 16) || !aligned_to(a.W, 16)) return false;
+  if (!tma_encode_tiled()) return false;
+  const DeviceInfo& di = device_info();
+  if (di.cc_major < 10) return false;
+  const int64_t G = std::min<int64_t>(di.sm_count, (a.N + 7) / 8);
+  const int64_t rows = (a.N + G - 1) / G;
+  if (rows > 8 * kSMaxTiles) return false;
+  pl.G = static_cast<int>(G);
+  // the box covers the CTA's rows (f16: whole 8-row groups, for the
+  // swizzled boxes' 1024-byte alignment); a tile's rows past the box read
+  // other bytes of shared memory, into outputs that are not stored
+  pl.rows_box = static_cast<int>(a.fmt == LQ_FMT_F16 ? (rows + 7) / 8 * 8 : rows);
+  pl.w_bytes = static_cast<unsigned>(pl.rows_box * piece_row_bytes(a.fmt));
+  pl.slot_bytes = (kSABytes + pl.w_bytes + 1023u) / 1024u * 1024u;
+  const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - kSBarsBytes;
+  const int npieces = static_cast<int>(a.K / kPieceK);
+  const long long red = static_cast<long long>((rows + 7) / 8) * 8 * 128 * 4;  // partial tiles
+  // the last tile's rows past the box read up to 7 rows beyond the last slot
+  const long long tail = 7LL * piece_row_bytes(a.fmt);
+  const int S = static_cast<int>(std::min<long long>({kSMaxStages, npieces, (budget - tail) / pl.slot_bytes}));
+  if (S < 1) return false;
+  pl.stages = S;
+  pl.ring_bytes = static_cast<unsigned>(std::max<long long>(static_cast<long long>(S) * pl.slot_bytes + tail, red));
+  pl.ring_bytes = (pl.ring_bytes + 127u) / 128u * 128u;
+  if (static_cast<long long>(pl.ring_bytes) > budget) return false;
+  pl.smem = 1024 + pl.ring_bytes + kSBarsBytes;
+  return true;
+}
+
+}  // namespace
+
+bool gemm_small_eligible(const MatmulArgs& a) {
+  SmallPlan pl;
+  return plan_small(a, pl);
+}
+
+unsigned read_clear_small_error() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_small_err, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_small_err, &z, sizeof(z));
+  return v;
+}
+
+lq_status launch_gemm_small(const MatmulArgs& a) {
+  SmallPlan pl;
+  if (!plan_small(a, pl)) return LQ_ERR_UNSUPPORTED;
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  Encode enc = reinterpret_cast<Encode>(tma_encode_tiled());
+  CUtensorMap tw, ta;
+  const uint64_t rb = static_cast<uint64_t>(row_bytes(a.fmt, a.K));
+  if (a.fmt == LQ_FMT_F16) {
+    // W as [N][K] halves; boxes of 64 halves x rows_box rows, 128B-swizzled
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.N)};
+    cuuint64_t strides[1] = {rb};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pl.rows_box)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(a.W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  } else {
+    // W as [N][K/256][bytes of 256 K / 4] words; a box is one such piece of rows_box rows
+    const int prb = piece_row_bytes(a.fmt);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(prb / 4), static_cast<cuuint64_t>(a.K / kPieceK),
+                          static_cast<cuuint64_t>(a.N)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(prb), rb};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(prb / 4), 1, static_cast<cuuint32_t>(pl.rows_box)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(a.W), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  }
+  {
+    // A as [M][K] f32; boxes of 256 values x M rows
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(a.K), static_cast<cuuint64_t>(a.M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(a.K) * 4};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kPieceK), static_cast<cuuint32_t>(a.M)};
+    cuuint32_t es[2] = {1, 1};
+    if (enc(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(a.A), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return LQ_ERR_UNSUPPORTED;
+  }
+  SmallParams p = {};
+  p.C = a.C;
+  p.R = a.R;
+  p.M = static_cast<int>(a.M);
+  p.N = static_cast<int>(a.N);
+  p.K = static_cast<int>(a.K);
+  p.rows_box = pl.rows_box;
+  p.stages = pl.stages;
+  p.w_bytes = pl.w_bytes;
+  p.slot_bytes = pl.slot_bytes;
+  p.ring_bytes = pl.ring_bytes;
+  p.wait_ns = wait_limit_ns();
+  p.wait_iters = wait_limit_iters();
+  lq_status st;
+  if (a.fmt == LQ_FMT_F16)
+    st = launch_small_fmt<LQ_FMT_F16>(a, tw, ta, p, pl.G, pl.smem);
+  else if (a.fmt == LQ_FMT_Q8_0)
+    st = launch_small_fmt<LQ_FMT_Q8_0>(a, tw, ta, p, pl.G, pl.smem);
+  else
+    st = launch_small_fmt<LQ_FMT_Q4_0>(a, tw, ta, p, pl.G, pl.smem);
+  if (st == LQ_OK) count_route(5);
+  return st;
+}
+
+}  // namespace lq

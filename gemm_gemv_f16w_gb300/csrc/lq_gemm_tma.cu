@@ -1006,6 +1006,8 @@ lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const 
 
 }  // namespace
 
+void* tma_encode_tiled() { return reinterpret_cast<void*>(encode_fn()); }
+
 unsigned read_clear_gemm_tma_error() {
   unsigned v = 0, z = 0;
   if (cudaMemcpyFromSymbol(&v, g_tma_err, sizeof(v)) != cudaSuccess) return 0;
@@ -1096,6 +1098,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16) {
                                static_cast<uint32_t*>(a16), n8, a.a_perm ? 1 : 0);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return LQ_ERR_CUDA;
+    count_route(6);  // the pre-pass launch
   }
 
   // 2. tensor maps. Q formats: raw W as [N][row_bytes/4] 32-bit words, one

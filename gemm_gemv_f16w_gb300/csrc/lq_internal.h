@@ -71,6 +71,12 @@ size_t gemm_tma_workspace_bytes(const MatmulArgs& a);
 // the same given that workspace (256-byte aligned; may be null when 0)
 lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* ws);
 bool gemm_tma_eligible(const MatmulArgs& a);
+// cuTensorMapEncodeTiled from the driver (null when unavailable)
+void* tma_encode_tiled();
+// tensor cores with warp-level MMAs for M = 2..16 (W streamed once, every
+// operand in registers); LQ_ERR_UNSUPPORTED outside its shapes
+lq_status launch_gemm_small(const MatmulArgs& a);
+bool gemm_small_eligible(const MatmulArgs& a);
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
 void set_gemm_rings(int a_stages, int raw_stages);
 
@@ -99,6 +105,7 @@ unsigned read_clear_gemm_error();
 unsigned read_clear_gemm_tma_error();
 unsigned read_clear_chain_error();
 unsigned read_clear_batch_error();
+unsigned read_clear_small_error();
 
 lq_status cuda_status(cudaError_t e);
 

@@ -42,11 +42,13 @@
  *   - Sub-matrices (e.g. the gate or up half of a fused weight) are addressed
  *     by pointer offsets; a W row offset is always block-aligned.
  *   - Memory: the library allocates nothing per call and holds no workspace,
- *     with one exception: the tensor-core route of the GEMM entry points
- *     (lq_gemm_<fmt>, lq_matmul_<fmt> and the epilogue fusions for M > 4)
- *     takes an M*K*2-byte stream-ordered buffer from a memory pool the
- *     library owns (described at lq_gemm_f16); lq_gemm_noalloc runs the
- *     same kernels on a fixed array instead. Caller-provided scratch
+ *     with one exception: the tcgen05 route of the GEMM entry points
+ *     (lq_gemm_<fmt>, lq_matmul_<fmt> and the epilogue fusions; M > 16, or
+ *     shapes the warp-MMA kernel does not take), when a CTA's token tile is
+ *     too large to stay in its shared memory, takes an M*K*2-byte
+ *     stream-ordered buffer from a memory pool the library owns (described
+ *     at lq_gemm_f16); lq_gemm_noalloc runs the same kernels on a fixed
+ *     array instead. Caller-provided scratch
  *     (lq_topk_f32's work) is named in the call.
  *   - Kernels launched on a stream may begin streaming W before the previous
  *     kernel on that stream has finished (programmatic dependent launch); A
@@ -96,15 +98,17 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
 
 /* ---- prefill GEMM, any M >= 1 -----------------------------------------
  * Counterparts: gemm_q8 / gemm_q4 / gemm_q4_tiled (metal_qwen35.rs),
- * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). Small M streams W on the
- * CUDA cores in f32 (GEMV accuracy); larger M runs on the tensor cores
- * (tcgen05, TMEM accumulators) with bf16 operands: A rounded to bf16 (round
- * to nearest even, over f32's whole range), each weight formed exactly in
- * f32 and rounded once to bf16 (any finite block scale), products
- * accumulated in f32. Tolerance: 5e-3 times sum_k |a_k w_k| plus 1e-5,
- * against A rounded to bf16 (the weights' rounding contributes at most
- * 2^-8 of the sum).
- * Workspace: the tensor-core route converts A once per call into a
+ * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). M = 2 streams W on the
+ * CUDA cores in f32 (GEMV accuracy), as do up to four rows of the shapes
+ * the warp-MMA kernel below does not take; larger M runs on the tensor cores
+ * with bf16 operands: A rounded to bf16 (round to nearest even, over f32's
+ * whole range), each weight formed exactly in f32 and rounded once to bf16
+ * (any finite block scale), products accumulated in f32 -- up to 16 rows
+ * with warp-level MMAs on W streamed once (K a multiple of 256), beyond
+ * with tcgen05 MMAs and TMEM accumulators. Tolerance: 5e-3 times
+ * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16 (the weights'
+ * rounding contributes at most 2^-8 of the sum).
+ * Workspace: the tcgen05 route converts A once per call into a
  * stream-ordered buffer of M*K*2 bytes taken from the library's own memory
  * pool (cudaMallocFromPoolAsync; the pool keeps freed blocks, so repeated
  * calls and CUDA-graph replays reuse the same memory without a driver
@@ -314,9 +318,12 @@ const char* lq_version(void);
 /* ---- test hooks (the forced-route idea of the page's
  * force_q4_gemm_fallback_for_test and its fallback dispatch counter) ------
  * route: 0 = automatic, 1 = CUDA-core streaming GEMM (any M),
- *        2 = tensor-core GEMM, 3 = generic fallback kernels (any shape).
+ *        2 = tensor-core GEMM (tcgen05), 3 = generic fallback kernels (any
+ *        shape), 5 = tensor-core GEMM with warp-level MMAs for M = 2..16
+ *        (LQ_ERR_UNSUPPORTED outside its shapes).
  * lq_debug_route_count(r) counts launches taken by route r (r = 0 counts
- * the fast GEMV, r = 4 the decode chain); counters are process-wide. */
+ * the fast GEMV, r = 4 the decode chain, r = 6 the A pre-pass launches of
+ * route 2); counters are process-wide. */
 lq_status lq_debug_force_route(int route);
 uint64_t  lq_debug_route_count(int route);
 void      lq_debug_reset_counts(void);

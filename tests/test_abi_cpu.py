@@ -144,11 +144,14 @@ def test_argument_errors_return_before_launch(lq, kind, fmt):
 
 
 def test_route_hooks(lq):
-    with pytest.raises(lq.LQError):
-        lq.force_route(9)
+    for bad in (9, 4, -1):  # 4 counts the decode chain but is no route of its own
+        with pytest.raises(lq.LQError):
+            lq.force_route(bad)
+    lq.force_route(lq.ROUTE_WARP_MMA)
     lq.force_route(0)
     lq.reset_counts()
-    assert all(lq.route_count(r) == 0 for r in range(4))
+    assert all(lq.route_count(r) == 0 for r in range(7))
+    assert lq.route_count(7) == 0
 
 
 def test_argmax_argument_errors_return_before_launch(lq):

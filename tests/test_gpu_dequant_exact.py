@@ -94,8 +94,8 @@ def test_batched_decode_dequantises_bit_exactly(lq, cuda_dev, fmt, M):
         A = _onehot(cols).to(cuda_dev)
         C = torch.full((M, N), float("nan"), dtype=torch.float32, device=cuda_dev)
         lq.reset_counts()
-        if M > 4:
-            lq.force_route(lq.ROUTE_STREAM)  # the router sends five to eight rows to the tensor cores
+        if M > 2:
+            lq.force_route(lq.ROUTE_STREAM)  # the router sends three to eight rows to the tensor cores
         try:
             getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
         finally:
@@ -122,8 +122,10 @@ def test_chain_dequantises_bit_exactly(lq, cuda_dev, fmt):
     assert lq.last_device_error() == lq.LQ_OK
 
 
-@pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0", "q4_0i"])
-def test_tensor_core_operand_is_the_bf16_rounding_of_the_exact_weight(lq, cuda_dev, fmt):
+@pytest.mark.parametrize("fmt,route", [("f16", 2), ("q8_0", 2), ("q4_0", 2), ("q4_0i", 2),
+                                       ("f16", 5), ("q8_0", 5), ("q4_0", 5)])
+def test_tensor_core_operand_is_the_bf16_rounding_of_the_exact_weight(lq, cuda_dev, fmt, route):
+    """Both tensor-core kernels: tcgen05 (route 2) and warp-level MMAs (5)."""
     W = _weights(fmt, 34)
     Wd = _pack(lq, fmt, W, cuda_dev)
     cols = COLS + COLS[:2]        # 16 tokens: one token tile
@@ -131,8 +133,12 @@ def test_tensor_core_operand_is_the_bf16_rounding_of_the_exact_weight(lq, cuda_d
     M = len(cols)
     C = torch.full((M, N), float("nan"), dtype=torch.float32, device=cuda_dev)
     lq.reset_counts()
-    getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
+    lq.force_route(route)
+    try:
+        getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
+    finally:
+        lq.force_route(0)
     torch.cuda.synchronize()
-    assert lq.route_count(2) == 1
+    assert lq.route_count(route) == 1
     assert np.array_equal(_bits(C.cpu().numpy()), _bits(_expected(fmt, W, cols, bf16=True)))
     assert lq.last_device_error() == lq.LQ_OK

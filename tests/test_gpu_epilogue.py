@@ -16,7 +16,7 @@ from helpers import check, nan_filled, to_dev
 
 pytestmark = pytest.mark.gpu
 
-ROUTE_GEMV, ROUTE_BATCH, ROUTE_TC, ROUTE_GENERIC = 0, 1, 2, 3
+ROUTE_GEMV, ROUTE_BATCH, ROUTE_TC, ROUTE_GENERIC, ROUTE_WARP = 0, 1, 2, 3, 5
 
 
 def _pack_dev(lq, fmt, W, dev):
@@ -57,17 +57,20 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
     (1, 4133, 4096, ROUTE_GEMV, False),
     (2, 1000, 2048, ROUTE_BATCH, False),
     (4, 2437, 1024, ROUTE_BATCH, False),
-    (6, 1000, 2048, ROUTE_BATCH, False),   # five to eight rows: forced onto the batched kernel
+    (6, 1000, 2048, ROUTE_BATCH, False),   # forced onto the batched kernel (residual from three rows, SwiGLU from five)
     (8, 700, 1024, ROUTE_BATCH, False),
     (6, 1000, 2048, ROUTE_TC, True),       # ... where the router picks the tensor cores
+    (16, 1000, 2048, ROUTE_TC, True),
     (64, 1000, 2048, ROUTE_TC, True),
     (300, 777, 1024, ROUTE_TC, True),
 ]
 
 
-def _forced(lq, M, route):
-    """Five to eight rows reach the batched kernel only by a forced route."""
-    if route == ROUTE_BATCH and M > 4:
+def _forced(lq, M, route, limit=2):
+    """More rows than `limit` reach the batched kernel only by a forced route
+    (the residual epilogue: three and more; SwiGLU, which the warp-MMA kernel
+    does not take: five and more)."""
+    if route == ROUTE_BATCH and M > limit:
         lq.force_route(lq.ROUTE_STREAM)
 
 
@@ -75,7 +78,7 @@ def _forced(lq, M, route):
 @pytest.mark.parametrize("M,I,K,route,tc", CASES)
 def test_swiglu_routes(lq, cuda_dev, fmt, M, I, K, route, tc):
     lq.reset_counts()
-    _forced(lq, M, route)
+    _forced(lq, M, route, limit=4)
     try:
         W, A, H = _swiglu(lq, cuda_dev, fmt, M, I, K, seed=M + I + K)
     finally:
@@ -95,13 +98,16 @@ def test_residual_routes(lq, cuda_dev, fmt, M, N, K, route, tc):
         W, A, R, C = _residual(lq, cuda_dev, fmt, M, N, K, seed=M + N + K)
     finally:
         lq.force_route(0)
-    assert lq.route_count(route) == 1
+    # up to 16 rows the tensor cores are reached by warp-level MMAs (swiglu:
+    # by the tcgen05 kernel)
+    assert lq.route_count(ROUTE_WARP if route == ROUTE_TC and M <= 16 else route) == 1
     y, tol = _ref(fmt, A, W, tc)
     c, tc_ = O.residual_reference(y, tol, R)
     check(C, c, tc_, f"residual {fmt} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (3, ROUTE_BATCH, False), (40, ROUTE_TC, True)])
+@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (2, ROUTE_BATCH, False), (3, ROUTE_WARP, True),
+                                        (40, ROUTE_TC, True)])
 def test_residual_in_place(lq, cuda_dev, M, route, tc):
     """R and C the same buffer: the residual stream updated in place."""
     fmt, N, K = "q8_0", 3000, 2048

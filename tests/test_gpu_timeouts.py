@@ -38,8 +38,8 @@ def test_batch_kernel_timeout(lq, cuda_dev, fmt, M, N, K):
     Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
     C = nan_filled(M, N, cuda_dev)
     lq.reset_counts()
-    if M > 4:
-        lq.force_route(lq.ROUTE_STREAM)  # five to eight rows: the batched kernel by a forced route
+    if M > 2:
+        lq.force_route(lq.ROUTE_STREAM)  # three to eight rows: the batched kernel by a forced route
     try:
         st = _with_tiny_limit(lq, lambda: getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K))
         assert lq.route_count(1) == 1
@@ -66,10 +66,14 @@ def test_tensor_core_gemm_timeout(lq, cuda_dev, M, N, K, kind):
     C = nan_filled(M, N, cuda_dev)
 
     def go():
-        if kind == "swiglu":
-            lq.lq_matmul_swiglu(fmt, Ad, Wd, C, M, N, K)
-        else:
-            lq.lq_gemm_q8_0(Ad, Wd, C, M, N, K)
+        lq.force_route(lq.ROUTE_TENSOR_CORE)  # sixteen rows would take the warp-MMA kernel
+        try:
+            if kind == "swiglu":
+                lq.lq_matmul_swiglu(fmt, Ad, Wd, C, M, N, K)
+            else:
+                lq.lq_gemm_q8_0(Ad, Wd, C, M, N, K)
+        finally:
+            lq.force_route(0)
     lq.reset_counts()
     st = _with_tiny_limit(lq, go)
     assert lq.route_count(2) == 1
@@ -118,3 +122,22 @@ def test_fused_argmax_timeout_leaves_the_result_unwritten(lq, cuda_dev):
     v, i = lq.read_argmax(res)
     i_ref = O.argmax_first(y[0])
     assert i == i_ref or y[0, i_ref] - y[0, i] <= tol[0, i_ref] + tol[0, i]
+
+
+@pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 16, 6144, 2048), ("f16", 5, 3000, 1024), ("q4_0", 9, 777, 4096)])
+def test_warp_mma_gemm_timeout(lq, cuda_dev, fmt, M, N, K):
+    """The warp-MMA kernel gives up on its stage waits, drains the copies it
+    issued and leaves the context usable."""
+    W, A = synthetic.draw(M, N, K, seed=N + 1)
+    Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
+    C = nan_filled(M, N, cuda_dev)
+    lq.reset_counts()
+    st = _with_tiny_limit(lq, lambda: getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K))
+    assert lq.route_count(lq.ROUTE_WARP_MMA) == 1
+    assert st == lq.LQ_ERR_DEVICE_TIMEOUT
+    C = nan_filled(M, N, cuda_dev)
+    getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K)
+    torch.cuda.synchronize()
+    assert lq.last_device_error() == lq.LQ_OK
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+    check(C.cpu().numpy(), y, tol, "after the timeout")
