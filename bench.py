@@ -253,7 +253,7 @@ class Workbench:
             lq = self.lq
             self.kernels_per_step = sum(lq.route_count(r) for r in (1, 2, lq.ROUTE_WARP_MMA, lq.COUNT_PREPASS))
             if lq.route_count(1) >= self.R:
-                self.route = "batch"        # M = 2..4: the CUDA-core batched decode kernel
+                self.route = "batch"        # the CUDA-core batched decode kernel
             elif lq.route_count(lq.ROUTE_WARP_MMA) >= self.R:
                 self.route = "warp-mma"     # M = 5..16: warp-level MMAs
         g = torch.cuda.CUDAGraph()
@@ -558,10 +558,10 @@ def main():
             runs.append((name, "calls"))  # the decode GEMVs both as a chain and as separate calls
         m = synthetic.WORKLOADS[name].M
         if 1 < m <= 16:
-            # the router's kernel against the others: the tcgen05 kernel, and
-            # the batched decode kernel where the warp-MMA kernel is picked
+            # the router's kernel (warp-MMA) against the tcgen05 kernel and,
+            # up to eight rows, the batched decode kernel
             runs.append((name, "tc"))
-            if 4 < m <= 8:
+            if m <= 8:
                 runs.append((name, "batch"))
     if w.M == 1 and args.extras != "none":
         runs = [(w.name, "calls"), (w.name, "chain-dependent")] + runs

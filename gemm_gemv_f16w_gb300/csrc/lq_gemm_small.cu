@@ -12,10 +12,10 @@
 //    (Q8_0 / Q4_0: one box of the rows' 272 / 144 bytes of that K; f16: four
 //    128-byte-swizzled boxes of 64 halves), the first stages' weights issued
 //    at kernel start (weights depend on nothing);
-//  * each stage also holds the same 256 K of A (the M rows, f32, in one box;
-//    rows M..15 of every slot are zeroed once), copied once the previous
-//    kernel on the stream has completed; the lanes round their A values to
-//    bf16 (nearest even) as they build the MMA operands;
+//  * each stage also holds the same K of A (the M rows, f32, one box a
+//    piece), copied once the previous kernel on the stream has completed;
+//    the lanes round their A values to bf16 (nearest even) as they build the
+//    MMA operands (rows M..15 of the MMA are zeros);
 //  * warp w takes block w % 8 (32 K) of every stage, for the 8-row tiles
 //    t = w / 8, w / 8 + 2, ...: each lane dequantises 8 weights of one row
 //    (lane / 4) exactly in f32 and rounds them once to bf16, the same operand
@@ -58,7 +58,8 @@ __host__ __device__ constexpr int piece_row_bytes(int fmt) {
   return fmt == LQ_FMT_F16 ? 512 : (fmt == LQ_FMT_Q8_0 ? 272 : 144);
 }
 
-constexpr unsigned kSABytes = kSTokens * kPieceK * 4;  // A of one stage: 16 rows x 256 f32
+constexpr int kPPS = 2;           // pieces a stage (the last stage may hold one)
+constexpr unsigned kARowBytes = kPieceK * 4;  // one row of A in a piece: 256 f32
 
 struct SmallParams {
   float* C;
@@ -66,8 +67,9 @@ struct SmallParams {
   int M, N, K;
   int rows_box;         // W rows of a stage (the copy's box), at most 128
   int stages;           // ring depth
-  unsigned w_bytes;     // weight bytes of a stage
-  unsigned slot_bytes;  // ring slot: A (kSABytes), then the weights; a multiple of 1024
+  unsigned w_bytes;     // weight bytes of a piece (the copy's box)
+  unsigned w_pitch;     // their space in the slot (a multiple of 128)
+  unsigned slot_bytes;  // ring slot: A of its pieces (M rows each), then their weights; a multiple of 1024
   unsigned ring_bytes;  // ring (reused for the partial tiles at the end)
   unsigned long long wait_ns;
   unsigned wait_iters;
@@ -162,15 +164,16 @@ __device__ __forceinline__ void load_weights(uint32_t stage, int rows_box, int r
 // The lane's A values of token row `row` (0..15) for block bp of a stage, in
 // the order of its weights (Q8_0 / f16: elements 8q .. 8q+7 of the block;
 // Q4_0: 4q .. 4q+3 and 16+4q .. 19+4q), as four bf16 pairs (nearest even).
-// The stage's A is 16 rows of 256 values (1 KB each). (One box a stage:
+// The piece's A is M rows of 256 values (1 KB each). (One box a stage:
 // eight 128-byte-swizzled boxes, free of bank conflicts, issued eight times
 // as many copies and measured slower.)
 template <int FMT>
-__device__ __forceinline__ void load_a(uint32_t sa, int row, int bp, int q, uint32_t (&a)[4]) {
+__device__ __forceinline__ void load_a(uint32_t sa, int row, int M, int bp, int q, uint32_t (&a)[4]) {
   const uint32_t rbase = sa + static_cast<uint32_t>(row * 1024 + bp * 128);
   const uint32_t c0 = FMT == LQ_FMT_Q4_0 ? q : 2 * q, c1 = FMT == LQ_FMT_Q4_0 ? 4 + q : 2 * q + 1;
-  const float4 x = lds128f(rbase + (c0 << 4));
-  const float4 y = lds128f(rbase + (c1 << 4));
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 x = row < M ? lds128f(rbase + (c0 << 4)) : z;  // rows past M: zeros (not in the slot)
+  const float4 y = row < M ? lds128f(rbase + (c1 << 4)) : z;
   a[0] = pack_bf16x2(x.x, x.y);
   a[1] = pack_bf16x2(x.z, x.w);
   a[2] = pack_bf16x2(y.x, y.y);
@@ -187,47 +190,49 @@ __global__ void __launch_bounds__(kSThreads, 1)
   SmallBars& b = *reinterpret_cast<SmallBars*>(ring + p.ring_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = p.stages, npieces = p.K / kPieceK;
+  const int S = p.stages, npieces = p.K / kPieceK, nstages = (npieces + kPPS - 1) / kPPS;
   const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.N / gridDim.x);
   const int nrows = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.N / gridDim.x) - r0;
   const int T = (nrows + 7) / 8;  // 8-row tiles
 
-  // stage `piece` into ring slot `slot`: the weights, then (once the
-  // previous kernel has completed) A; one barrier counts both
-  auto issue_w = [&](int piece, int slot) {
-    uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes + kSABytes;
-    mbar_arrive_expect_tx(&b.full[slot], p.w_bytes + static_cast<unsigned>(p.M) * kPieceK * 4u);
-    if constexpr (FMT == LQ_FMT_F16) {
+  // stage st (pieces kPPS st, kPPS st + 1) into ring slot `slot`: the
+  // weights, then (once the previous kernel has completed) A; one barrier
+  // counts both. Slot layout: A of piece 0, A of piece 1, W of piece 0, W of
+  // piece 1.
+  auto issue_w = [&](int st, int slot) {
+    const int np = min(kPPS, npieces - kPPS * st);
+    mbar_arrive_expect_tx(&b.full[slot], static_cast<unsigned>(np) * (p.w_bytes + static_cast<unsigned>(p.M) * kARowBytes));
+    for (int sp = 0; sp < np; ++sp) {
+      const int piece = kPPS * st + sp;
+      uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes + kPPS * p.M * kARowBytes + sp * p.w_pitch;
+      if constexpr (FMT == LQ_FMT_F16) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        tc::tma_load_2d(dst + i * p.rows_box * 128, &tmW, kPieceK * piece + 64 * i, r0, &b.full[slot]);
-    } else {
-      tc::tma_load_3d(dst, &tmW, 0, piece, r0, &b.full[slot]);
+        for (int i = 0; i < 4; ++i)
+          tc::tma_load_2d(dst + i * p.rows_box * 128, &tmW, kPieceK * piece + 64 * i, r0, &b.full[slot]);
+      } else {
+        tc::tma_load_3d(dst, &tmW, 0, piece, r0, &b.full[slot]);
+      }
     }
-    b.last[slot] = piece;
+    b.last[slot] = st;
   };
-  auto issue_a = [&](int piece, int slot) {
-    tc::tma_load_2d(ring + static_cast<size_t>(slot) * p.slot_bytes, &tmA, kPieceK * piece, 0, &b.full[slot]);
+  auto issue_a = [&](int st, int slot) {
+    const int np = min(kPPS, npieces - kPPS * st);
+    for (int sp = 0; sp < np; ++sp)
+      tc::tma_load_2d(ring + static_cast<size_t>(slot) * p.slot_bytes + sp * p.M * kARowBytes, &tmA,
+                      kPieceK * (kPPS * st + sp), 0, &b.full[slot]);
   };
-  const int first = min(S, npieces);
+  const int first = min(S, nstages);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&b.full[s], 1);
-      b.done[s] = 0;
-      b.last[s] = -1;
+    for (int k = 0; k < S; ++k) {
+      mbar_init(&b.full[k], 1);
+      b.done[k] = 0;
+      b.last[k] = -1;
     }
     b.abort = 0;
     fence_barrier_init();
     tc::prefetch_tmap(&tmW);
     tc::prefetch_tmap(&tmA);
     for (int j = 0; j < first; ++j) issue_w(j, j);  // weights depend on nothing
-  }
-  // rows M..15 of every slot's A: zeros (the copies bring rows 0..M-1)
-  for (int i = threadIdx.x; i < S * (kSTokens - p.M) * (kPieceK / 4); i += kSThreads) {
-    const int per = (kSTokens - p.M) * (kPieceK / 4), sl = i / per, j = i - sl * per;
-    sts128(smem_u32(ring) + static_cast<uint32_t>(sl) * p.slot_bytes + static_cast<uint32_t>(p.M) * kPieceK * 4u +
-               16u * static_cast<uint32_t>(j),
-           make_uint4(0u, 0u, 0u, 0u));
   }
   __syncthreads();
   pdl_launch_dependents();
@@ -236,19 +241,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (threadIdx.x == 0)
     for (int j = 0; j < first; ++j) issue_a(j, j);
 
-  // ---- main loop: warp (bp, th) takes block bp of each stage for the tiles
-  // t = th, th + 2, ...; lane (g, q): W row 8t + g, codes 8q .. 8q+7, and
+  // ---- main loop: warp w takes block w % 8 of piece w / 8 of each stage,
+  // for every tile, two tiles at a time (independent chains of loads,
+  // conversions and MMAs); lane (g, q): W row 8t + g, codes 8q .. 8q+7, and
   // the A values of tokens g and g + 8 in the same order
-  const int bp = warp & 7, th = warp >> 3, g = lane >> 2, q = lane & 3;
-  float acc[kSMaxTiles / 2][4];
+  const int bp = warp & 7, sp = warp >> 3, g = lane >> 2, q = lane & 3;
+  float acc[kSMaxTiles][4];
 #pragma unroll
-  for (int i = 0; i < kSMaxTiles / 2; ++i)
+  for (int i = 0; i < kSMaxTiles; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   int s = 0;
   uint32_t ph = 0;
 #pragma unroll 1
-  for (int piece = 0; piece < npieces; ++piece) {
+  for (int st = 0; st < nstages; ++st) {
     const bool ok = mbar_wait(&b.full[s], ph, p.wait_ns, p.wait_iters);
     if (!__all_sync(0xffffffffu, ok) || b.abort) {
       if (lane == 0) {
@@ -257,20 +263,27 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       break;
     }
-    const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
-    uint32_t alo[4], ahi[4];
-    load_a<FMT>(slot, g, bp, q, alo);
-    load_a<FMT>(slot, g + 8, bp, q, ahi);
-    // (every tile's weights loaded first, with two accumulators a tile,
-    // measured slower: 10.7 against 8.6 us at Q8_0 M = 16, 6144 x 2048)
+    if (kPPS * st + sp < npieces) {
+      const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
+      const uint32_t sa = slot + static_cast<uint32_t>(sp * p.M) * kARowBytes;
+      const uint32_t wst = slot + static_cast<uint32_t>(kPPS * p.M) * kARowBytes + static_cast<uint32_t>(sp) * p.w_pitch;
+      uint32_t alo[4], ahi[4];
+      load_a<FMT>(sa, g, p.M, bp, q, alo);
+      load_a<FMT>(sa, g + 8, p.M, bp, q, ahi);
 #pragma unroll
-    for (int i = 0; i < kSMaxTiles / 2; ++i) {
-      const int t = th + 2 * i;
-      if (t >= T) break;
-      uint32_t bw[4];
-      load_weights<FMT>(slot + kSABytes, p.rows_box, 8 * t + g, bp, q, bw);
-      mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], bw[0], bw[1]);  // the lane's values 0 .. 3
-      mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], bw[2], bw[3]);  // values 4 .. 7
+      for (int i = 0; i < kSMaxTiles; i += 2) {
+        if (i >= T) break;
+        // with an odd tile count the last pair repeats tile i into acc[i + 1],
+        // a tile that is never stored
+        const int t1 = min(i + 1, T - 1);
+        uint32_t b0[4], b1[4];
+        load_weights<FMT>(wst, p.rows_box, 8 * i + g, bp, q, b0);
+        load_weights<FMT>(wst, p.rows_box, 8 * t1 + g, bp, q, b1);
+        mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], b0[0], b0[1]);  // the lane's values 0 .. 3
+        mma_bf16_16816(acc[i + 1], alo[0], ahi[0], alo[1], ahi[1], b1[0], b1[1]);
+        mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], b0[2], b0[3]);  // values 4 .. 7
+        mma_bf16_16816(acc[i + 1], alo[2], ahi[2], alo[3], ahi[3], b1[2], b1[3]);
+      }
     }
     // The last warp done with the slot refills it (every warp's reads of it
     // have returned: their values went into the MMAs above).
@@ -279,10 +292,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       __threadfence_block();
       if (atomicAdd(&b.done[s], 1) == kSWarps - 1) {
         b.done[s] = 0;
-        if (piece + S < npieces) {
+        if (st + S < nstages) {
           fence_proxy_async_smem();  // the generic reads above, before the copies' writes
-          issue_w(piece + S, s);
-          issue_a(piece + S, s);
+          issue_w(st + S, s);
+          issue_a(st + S, s);
         }
       }
     }
@@ -300,16 +313,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
     return;
   }
 
-  // ---- the 8 block positions' partial tiles, added in a fixed order
-  // (shared memory of the ring, every stage consumed): red[t][bp][m][n]
+  // ---- the 16 block positions' partial tiles, added in a fixed order
+  // (shared memory of the ring, every stage consumed): red[t][w][m][n]
   float* red = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int i = 0; i < kSMaxTiles / 2; ++i) {
-    const int t = th + 2 * i;
+  for (int t = 0; t < kSMaxTiles; ++t) {
     if (t >= T) break;
-    float* tile = red + (t * 8 + bp) * 128;
-    *reinterpret_cast<float2*>(tile + g * 8 + 2 * q) = make_float2(acc[i][0], acc[i][1]);
-    *reinterpret_cast<float2*>(tile + (g + 8) * 8 + 2 * q) = make_float2(acc[i][2], acc[i][3]);
+    float* tile = red + (t * kSWarps + warp) * 128;
+    *reinterpret_cast<float2*>(tile + g * 8 + 2 * q) = make_float2(acc[t][0], acc[t][1]);
+    *reinterpret_cast<float2*>(tile + (g + 8) * 8 + 2 * q) = make_float2(acc[t][2], acc[t][3]);
   }
   __syncthreads();
 #pragma unroll 1
@@ -318,7 +330,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (m < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
       float sum = 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) sum += red[(t * 8 + k) * 128 + e];
+      for (int k = 0; k < kSWarps; ++k) sum += red[(t * kSWarps + k) * 128 + e];
       const long long o = static_cast<long long>(m) * p.N + r0 + n;
       if constexpr (EPI == epi::kResidual)
         p.C[o] = sum + p.R[o];
@@ -365,7 +377,7 @@ lq_status launch_small_fmt(const MatmulArgs& a, const CUtensorMap& tw, const CUt
 
 struct SmallPlan {
   int G = 0, rows_box = 0, stages = 0;
-  unsigned w_bytes = 0, slot_bytes = 0, ring_bytes = 0;
+  unsigned w_bytes = 0, w_pitch = 0, slot_bytes = 0, ring_bytes = 0;
   size_t smem = 0;
 };
 
@@ -386,15 +398,17 @@ bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   // swizzled boxes' 1024-byte alignment); a tile's rows past the box read
   // other bytes of shared memory, into outputs that are not stored
   pl.rows_box = static_cast<int>(a.fmt == LQ_FMT_F16 ? (rows + 7) / 8 * 8 : rows);
-  pl.w_bytes = static_cast<unsigned>(pl.rows_box * piece_row_bytes(a.fmt));
-  pl.slot_bytes = (kSABytes + pl.w_bytes + 1023u) / 1024u * 1024u;
+  pl.w_bytes = static_cast<unsigned>(pl.rows_box * piece_row_bytes(a.fmt));  // f16: a multiple of 4096
+  pl.w_pitch = (pl.w_bytes + 127u) / 128u * 128u;
+  // (A's M KB a piece keeps the weights 1024-aligned, as f16's swizzled boxes need)
+  pl.slot_bytes = (kPPS * (static_cast<unsigned>(a.M) * kARowBytes + pl.w_pitch) + 1023u) / 1024u * 1024u;
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - kSBarsBytes;
-  const int npieces = static_cast<int>(a.K / kPieceK);
-  const long long red = static_cast<long long>((rows + 7) / 8) * 8 * 128 * 4;  // partial tiles
+  const int nstages = static_cast<int>((a.K / kPieceK + kPPS - 1) / kPPS);
+  const long long red = static_cast<long long>((rows + 7) / 8) * kSWarps * 128 * 4;  // partial tiles
   // the last tile's rows past the box read up to 7 rows beyond the last slot
   const long long tail = 7LL * piece_row_bytes(a.fmt);
-  const int S = static_cast<int>(std::min<long long>({kSMaxStages, npieces, (budget - tail) / pl.slot_bytes}));
-  if (S < 1) return false;
+  const int S = static_cast<int>(std::min<long long>({kSMaxStages, nstages, (budget - tail) / pl.slot_bytes}));
+  if (S < std::min(2, nstages)) return false;  // a ring of one slot would not overlap copies and MMAs
   pl.stages = S;
   pl.ring_bytes = static_cast<unsigned>(std::max<long long>(static_cast<long long>(S) * pl.slot_bytes + tail, red));
   pl.ring_bytes = (pl.ring_bytes + 127u) / 128u * 128u;
@@ -469,6 +483,7 @@ lq_status launch_gemm_small(const MatmulArgs& a) {
   p.rows_box = pl.rows_box;
   p.stages = pl.stages;
   p.w_bytes = pl.w_bytes;
+  p.w_pitch = pl.w_pitch;
   p.slot_bytes = pl.slot_bytes;
   p.ring_bytes = pl.ring_bytes;
   p.wait_ns = wait_limit_ns();

@@ -98,9 +98,9 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
 
 /* ---- prefill GEMM, any M >= 1 -----------------------------------------
  * Counterparts: gemm_q8 / gemm_q4 / gemm_q4_tiled (metal_qwen35.rs),
- * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). M = 2 streams W on the
- * CUDA cores in f32 (GEMV accuracy), as do up to four rows of the shapes
- * the warp-MMA kernel below does not take; larger M runs on the tensor cores
+ * gemm_f32a_f16w_v2 (ferrum-kernels pipelines.rs). Up to four rows of the
+ * shapes the warp-MMA kernel below does not take stream W on the CUDA cores
+ * in f32 (GEMV accuracy); everything else runs on the tensor cores
  * with bf16 operands: A rounded to bf16 (round to nearest even, over f32's
  * whole range), each weight formed exactly in f32 and rounded once to bf16
  * (any finite block scale), products accumulated in f32 -- up to 16 rows

@@ -23,13 +23,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _run(lq, dev, fmt, W, A, A_dev=None, force=None):
-    """lq_gemm_<fmt>; three to eight rows on the batched kernel (forced route)
-    unless force is False."""
+    """lq_gemm_<fmt> on the batched kernel (a forced route: the router sends
+    these shapes to the warp-MMA kernel) unless force is False."""
     N, K = W.shape
     M = A.shape[0]
     Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
     C = nan_filled(M, N, dev)
-    if force if force is not None else M > 2:
+    if force if force is not None else True:
         lq.force_route(lq.ROUTE_STREAM)
     try:
         getattr(lq, f"lq_gemm_{fmt}")(A.to(dev) if A_dev is None else A_dev, Wd, C, M, N, K)

@@ -64,7 +64,7 @@ for fmt in ("f16", "q8_0", "q4_0", "q4_0i"):
         H = nan_filled(M, N, dev)
         lq.lq_matmul_swiglu(fmt, A.to(dev), Wd, H, M, N, K)
         clean(f"swiglu {fmt} M={M}")
-        # SwiGLU on the tensor cores from five rows, the residual from three
+        # SwiGLU on the tensor cores from five rows, the residual from two
         y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), 2 * N, K, tensor_core=M > 4)
         h, th = O.swiglu_reference(y, tol, N)
         check(H.cpu().numpy(), h, th, f"swiglu {fmt} M={M}")
@@ -72,7 +72,7 @@ for fmt in ("f16", "q8_0", "q4_0", "q4_0i"):
         Cd = R.to(dev)
         lq.lq_matmul_residual(fmt, A.to(dev), Wd, Cd, Cd, M, 2 * N, K)
         clean(f"residual {fmt} M={M}")
-        y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), 2 * N, K, tensor_core=M > 2)
+        y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), 2 * N, K, tensor_core=M > 1)
         yr, tr = O.residual_reference(y, tol, R.numpy())
         check(Cd.cpu().numpy(), yr, tr, f"residual {fmt} M={M}")
         runs += 2

@@ -94,8 +94,7 @@ def test_batched_decode_dequantises_bit_exactly(lq, cuda_dev, fmt, M):
         A = _onehot(cols).to(cuda_dev)
         C = torch.full((M, N), float("nan"), dtype=torch.float32, device=cuda_dev)
         lq.reset_counts()
-        if M > 2:
-            lq.force_route(lq.ROUTE_STREAM)  # the router sends three to eight rows to the tensor cores
+        lq.force_route(lq.ROUTE_STREAM)  # the router sends these rows to the tensor cores
         try:
             getattr(lq, f"lq_gemm_{fmt}")(A, Wd, C, M, N, K)
         finally:

@@ -57,7 +57,7 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
     (1, 4133, 4096, ROUTE_GEMV, False),
     (2, 1000, 2048, ROUTE_BATCH, False),
     (4, 2437, 1024, ROUTE_BATCH, False),
-    (6, 1000, 2048, ROUTE_BATCH, False),   # forced onto the batched kernel (residual from three rows, SwiGLU from five)
+    (6, 1000, 2048, ROUTE_BATCH, False),   # forced onto the batched kernel (residual: every M > 1; SwiGLU: from five)
     (8, 700, 1024, ROUTE_BATCH, False),
     (6, 1000, 2048, ROUTE_TC, True),       # ... where the router picks the tensor cores
     (16, 1000, 2048, ROUTE_TC, True),
@@ -66,9 +66,9 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
 ]
 
 
-def _forced(lq, M, route, limit=2):
+def _forced(lq, M, route, limit=1):
     """More rows than `limit` reach the batched kernel only by a forced route
-    (the residual epilogue: three and more; SwiGLU, which the warp-MMA kernel
+    (the residual epilogue: every M > 1; SwiGLU, which the warp-MMA kernel
     does not take: five and more)."""
     if route == ROUTE_BATCH and M > limit:
         lq.force_route(lq.ROUTE_STREAM)
@@ -106,8 +106,7 @@ def test_residual_routes(lq, cuda_dev, fmt, M, N, K, route, tc):
     check(C, c, tc_, f"residual {fmt} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (2, ROUTE_BATCH, False), (3, ROUTE_WARP, True),
-                                        (40, ROUTE_TC, True)])
+@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (2, ROUTE_WARP, True), (40, ROUTE_TC, True)])
 def test_residual_in_place(lq, cuda_dev, M, route, tc):
     """R and C the same buffer: the residual stream updated in place."""
     fmt, N, K = "q8_0", 3000, 2048

@@ -38,8 +38,7 @@ def test_batch_kernel_timeout(lq, cuda_dev, fmt, M, N, K):
     Wd, Ad = _packed(lq, fmt, W, cuda_dev), A.to(cuda_dev)
     C = nan_filled(M, N, cuda_dev)
     lq.reset_counts()
-    if M > 2:
-        lq.force_route(lq.ROUTE_STREAM)  # three to eight rows: the batched kernel by a forced route
+    lq.force_route(lq.ROUTE_STREAM)  # the batched kernel, by a forced route
     try:
         st = _with_tiny_limit(lq, lambda: getattr(lq, f"lq_gemm_{fmt}")(Ad, Wd, C, M, N, K))
         assert lq.route_count(1) == 1
