@@ -11,7 +11,9 @@ lq_matmul calls, and as a chain whose every problem waits for the previous
 one, is reported under "workloads" too. Steps are captured once as a CUDA
 graph and replayed, so the GPU never waits on the host. The other workload
 families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and the
-M = 2 / 16 / 64 crossover) are timed the same way under "workloads".
+M = 2 / 16 / 64 crossover) are timed the same way under "workloads", each
+entry "name [mode]": [value, unit, fraction of the measured peak, µs a
+matmul], the prefill GEMMs last.
 
 `--impl reference` times the CPU oracle on a bounded sample of the same
 workload (rank 0 only) and prints the same JSON line with "impl": "reference".
@@ -457,6 +459,25 @@ EXTRA = ["gemv_f16_256x512", "gemv_q4_0_11008x4096_outliers", "gemv_f16_lmhead_1
         [f"gemm_{f}_m{m}_6144x2048" for m in (2, 4, 8, 16, 64) for f in ("f16", "q8_0", "q4_0")]
 
 
+def workload_rank(key: str) -> tuple:
+    """Order of the "workloads" entries in the JSON line: the tensor-core
+    and batched alternatives of the small-M GEMMs first, then the router's
+    small-M GEMMs, the decode GEMVs, the LM head's selections, and the
+    prefill GEMMs (M = 512) last, so that a reader keeping only the end of
+    the line still has the metric's prefill half and the decode families."""
+    if "512x" in key:
+        group = 4
+    elif "lmhead" in key:
+        group = 3
+    elif key.startswith("gemv_"):
+        group = 2
+    elif "[tc]" in key or "[batch]" in key:
+        group = 0
+    else:
+        group = 1
+    return (group, key)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -578,10 +599,10 @@ def main():
         pl = d / (n * xb.R)
         v, u, b = rate(xb, pl)
         pk = hbm_peak if b == "hbm" else tc_peak
-        key = name if mode == "auto" else f"{name} [{mode}]"
-        extras[key] = {"value": round(v, 1), "unit": u, "frac": round(v / pk, 4),
-                       "us": round(pl * 1e6, 3), "mode": xb.mode}
+        key = f"{name} [{xb.mode}]"
+        extras[key] = [round(v, 1), u, round(v / pk, 4), round(pl * 1e6, 3)]
         xb.free()
+    extras = dict(sorted(extras.items(), key=lambda kv: workload_rank(kv[0])))
 
     # ---- CPU oracle baseline (rank 0 at N=1 only): all threads and one
     # thread, each in its own interpreter, quantisation timed separately
@@ -619,6 +640,7 @@ def main():
             "gpu_launches": steps * launches_per_step,
             "clocks": clocks,
             "spread": spread,
+            "workloads_fields": ["value", "unit", "frac", "us"],
             "workloads": extras,
         }
         print(json.dumps(line), flush=True)

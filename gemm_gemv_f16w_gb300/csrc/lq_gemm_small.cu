@@ -8,25 +8,25 @@
 // This kernel keeps everything in registers instead:
 //
 //  * one CTA per SM owns a contiguous range of W rows (at most 128), streamed
-//    as stages of 256 K through a ring in shared memory by TMA tensor copies
-//    (Q8_0 / Q4_0: one box of the rows' 272 / 144 bytes of that K; f16: four
-//    128-byte-swizzled boxes of 64 halves), the first stages' weights issued
-//    at kernel start (weights depend on nothing);
+//    as stages of two 256-K pieces through a ring in shared memory by TMA
+//    tensor copies (a piece: Q8_0 / Q4_0 one box of the rows' 272 / 144
+//    bytes of that K; f16 four 128-byte-swizzled boxes of 64 halves), the
+//    first stages' weights issued at kernel start (weights depend on nothing);
 //  * each stage also holds the same K of A (the M rows, f32, one box a
 //    piece), copied once the previous kernel on the stream has completed;
 //    the lanes round their A values to bf16 (nearest even) as they build the
 //    MMA operands (rows M..15 of the MMA are zeros);
-//  * warp w takes block w % 8 (32 K) of every stage, for the 8-row tiles
-//    t = w / 8, w / 8 + 2, ...: each lane dequantises 8 weights of one row
-//    (lane / 4) exactly in f32 and rounds them once to bf16, the same operand
-//    as the tcgen05 kernel's, and two mma.m16n8k16 (bf16 x bf16 -> f32; A =
-//    16 tokens, B = 8 W rows) add the block to the tile's accumulator. Within
-//    a block the lanes take consecutive codes (lane % 4 takes codes 8q ..
-//    8q+7; Q4_0: the low and high nibbles of bytes 4q .. 4q+3), so the MMA's
-//    K order is a fixed permutation of the block, and each lane reads the A
-//    values of the same positions;
-//  * after the last stage the 8 block positions' partial tiles are added in a
-//    fixed order through shared memory and C (plus R with the residual
+//  * warp w takes block w % 8 (32 K) of piece w / 8 of every stage, for
+//    every 8-row tile of the CTA, two tiles at a time: each lane dequantises
+//    8 weights of one row (lane / 4) exactly in f32 and rounds them once to
+//    bf16, the same operand as the tcgen05 kernel's, and two mma.m16n8k16
+//    (bf16 x bf16 -> f32; A = 16 tokens, B = 8 W rows) add the block to the
+//    tile's accumulator. Within a block the lanes take consecutive codes
+//    (lane % 4 takes codes 8q .. 8q+7; Q4_0: the low and high nibbles of
+//    bytes 4q .. 4q+3), so the MMA's K order is a fixed permutation of the
+//    block, and each lane reads the A values of the same positions;
+//  * after the last stage the 16 block positions' partial tiles are added in
+//    a fixed order through shared memory and C (plus R with the residual
 //    epilogue) is stored.
 //
 // The tolerance is the tensor-core route's (A and W rounded to bf16, f32
