@@ -180,7 +180,9 @@ __device__ __forceinline__ void load_a(uint32_t sa, int row, int M, int bp, int 
   a[3] = pack_bf16x2(y.z, y.w);
 }
 
-template <int FMT, int EPI>
+// NP: pairs of 8-row tiles a CTA (its T tiles, 2 NP - 1 <= T <= 2 NP), so the
+// tile loop is unrolled without branches and holds 2 NP accumulators.
+template <int FMT, int EPI, int NP>
 __global__ void __launch_bounds__(kSThreads, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                       const SmallParams p) {
@@ -246,9 +248,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // conversions and MMAs); lane (g, q): W row 8t + g, codes 8q .. 8q+7, and
   // the A values of tokens g and g + 8 in the same order
   const int bp = warp & 7, sp = warp >> 3, g = lane >> 2, q = lane & 3;
-  float acc[kSMaxTiles][4];
+  float acc[2 * NP][4];
 #pragma unroll
-  for (int i = 0; i < kSMaxTiles; ++i)
+  for (int i = 0; i < 2 * NP; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   int s = 0;
@@ -271,10 +273,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
       load_a<FMT>(sa, g, p.M, bp, q, alo);
       load_a<FMT>(sa, g + 8, p.M, bp, q, ahi);
 #pragma unroll
-      for (int i = 0; i < kSMaxTiles; i += 2) {
-        if (i >= T) break;
-        // with an odd tile count the last pair repeats tile i into acc[i + 1],
-        // a tile that is never stored
+      for (int i = 0; i < 2 * NP; i += 2) {
+        // with an odd tile count the last pair repeats tile i into acc[i + 1];
+        // a CTA with fewer rows than the largest computes its pairs past T on
+        // bytes of the ring or its tail; neither is ever stored
         const int t1 = min(i + 1, T - 1);
         uint32_t b0[4], b1[4];
         load_weights<FMT>(wst, p.rows_box, 8 * i + g, bp, q, b0);
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // (shared memory of the ring, every stage consumed): red[t][w][m][n]
   float* red = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int t = 0; t < kSMaxTiles; ++t) {
+  for (int t = 0; t < 2 * NP; ++t) {
     if (t >= T) break;
     float* tile = red + (t * kSWarps + warp) * 128;
     *reinterpret_cast<float2*>(tile + g * 8 + 2 * q) = make_float2(acc[t][0], acc[t][1]);
@@ -340,10 +342,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, int NP>
 lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                          int G, size_t smem) {
-  auto kern = gemm_small_kernel<FMT, EPI>;
+  auto kern = gemm_small_kernel<FMT, EPI, NP>;
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -368,11 +370,30 @@ lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUten
   return cuda_status(e);
 }
 
+// the kernel for the CTAs' tile count: the largest CTA holds ceil(N / G)
+// rows, ceil(rows / 8) tiles, NP = ceil(tiles / 2) pairs
+template <int FMT, int EPI>
+lq_status launch_small_np(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
+                          int G, size_t smem) {
+  const int rows = static_cast<int>((static_cast<long long>(p.N) + G - 1) / G);
+  switch ((rows + 15) / 16) {
+    case 1: return launch_small_t<FMT, EPI, 1>(a, tw, ta, p, G, smem);
+    case 2: return launch_small_t<FMT, EPI, 2>(a, tw, ta, p, G, smem);
+    case 3: return launch_small_t<FMT, EPI, 3>(a, tw, ta, p, G, smem);
+    case 4: return launch_small_t<FMT, EPI, 4>(a, tw, ta, p, G, smem);
+    case 5: return launch_small_t<FMT, EPI, 5>(a, tw, ta, p, G, smem);
+    case 6: return launch_small_t<FMT, EPI, 6>(a, tw, ta, p, G, smem);
+    case 7: return launch_small_t<FMT, EPI, 7>(a, tw, ta, p, G, smem);
+    case 8: return launch_small_t<FMT, EPI, 8>(a, tw, ta, p, G, smem);
+    default: return LQ_ERR_UNSUPPORTED;
+  }
+}
+
 template <int FMT>
 lq_status launch_small_fmt(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                            int G, size_t smem) {
-  if (a.epi == epi::kResidual) return launch_small_t<FMT, epi::kResidual>(a, tw, ta, p, G, smem);
-  return launch_small_t<FMT, epi::kPlain>(a, tw, ta, p, G, smem);
+  if (a.epi == epi::kResidual) return launch_small_np<FMT, epi::kResidual>(a, tw, ta, p, G, smem);
+  return launch_small_np<FMT, epi::kPlain>(a, tw, ta, p, G, smem);
 }
 
 struct SmallPlan {
