@@ -21,10 +21,11 @@
 //    8 weights of one row (lane / 4) exactly in f32 and rounds them once to
 //    bf16, the same operand as the tcgen05 kernel's, and two mma.m16n8k16
 //    (bf16 x bf16 -> f32; A = 16 tokens, B = 8 W rows) add the block to the
-//    tile's accumulator. Within a block the lanes take consecutive codes
-//    (lane % 4 takes codes 8q .. 8q+7; Q4_0: the low and high nibbles of
-//    bytes 4q .. 4q+3), so the MMA's K order is a fixed permutation of the
-//    block, and each lane reads the A values of the same positions;
+//    tile's accumulator. Within a block lane q = lane % 4 takes 8 codes (f16
+//    elements 8q .. 8q+7; Q8_0 codes 4q .. 4q+3 and 16+4q .. 19+4q; Q4_0 the
+//    low and high nibbles of bytes 4q .. 4q+3, the same codes), so the MMA's
+//    K order is a fixed permutation of the block, and each lane reads the A
+//    values of the same positions;
 //  * after the last stage the 16 block positions' partial tiles are added in
 //    a fixed order through shared memory and C (plus R with the residual
 //    epilogue) is stored.
@@ -98,13 +99,18 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// The lane's 8 weights of W row `row` (of the stage), block bp, codes 8q ..
-// 8q+7 (Q4_0: low nibbles of bytes 4q .. 4q+3, then their high nibbles), as
-// four bf16 pairs in the MMA's K order. Each weight is formed exactly in f32
+// The lane's 8 weights of W row `row` (of the stage), block bp, as four bf16
+// pairs in the MMA's K order: f16 elements 8q .. 8q+7; Q8_0 codes 8q ..
+// 8q+7, or with BIG (more than 8 rows of A) codes 4q .. 4q+3 and 16+4q ..
+// 19+4q; Q4_0 the low nibbles of bytes 4q .. 4q+3 (the same codes), then
+// their high nibbles. Reading words q (and q + 4) of a row's codes, the 32
+// lanes hit 32 different banks (rows 68 or 36 words apart, 4 banks); BIG
+// Q8_0 does so at the cost of a fourth load for unaligned blocks, which only
+// pays when the A loads are conflict-free too. Each weight is formed exactly in f32
 // (an f16 widened; d * q, or d * (q - 8), from the code placed in the
 // mantissa of 2^23 by one byte-permute and one exact packed add) and rounded
 // once to bf16 (nearest even).
-template <int FMT>
+template <int FMT, bool BIG>
 __device__ __forceinline__ void load_weights(uint32_t stage, int rows_box, int row, int bp, int q,
                                              uint32_t (&bw)[4]) {
   if constexpr (FMT == LQ_FMT_F16) {
@@ -122,12 +128,25 @@ __device__ __forceinline__ void load_weights(uint32_t stage, int rows_box, int r
     // blocks' codes start 2 bytes into a word, odd blocks' on a word
     const uint32_t rowa = stage + static_cast<uint32_t>(row) * 272u;
     const bool mis = (bp & 1) == 0;
-    const uint32_t o = 34u * static_cast<uint32_t>(bp) + 2u + 8u * static_cast<uint32_t>(q);
-    const uint32_t wa = rowa + (o & ~3u);
-    const uint32_t w0 = lds32(wa), w1 = lds32(wa + 4u), w2 = mis ? lds32(wa + 8u) : 0u;
     const uint32_t sh = mis ? 16u : 0u;
-    const uint32_t x0 = __funnelshift_r(w0, w1, sh) ^ 0x80808080u;  // codes 8q .. 8q+3, sign bits flipped
-    const uint32_t x1 = __funnelshift_r(w1, w2, sh) ^ 0x80808080u;  // codes 8q+4 .. 8q+7
+    uint32_t x0, x1;  // four codes each, sign bits flipped
+    if constexpr (BIG) {
+      // codes 4q .. 4q+3 and 16+4q .. 19+4q: words q (and q + 1) and q + 4
+      // (q + 5) of the codes, one bank each (four loads when unaligned)
+      const uint32_t o = 34u * static_cast<uint32_t>(bp) + 2u + 4u * static_cast<uint32_t>(q);
+      const uint32_t wa = rowa + (o & ~3u);
+      const uint32_t w0 = lds32(wa), w1 = mis ? lds32(wa + 4u) : 0u;
+      const uint32_t w4 = lds32(wa + 16u), w5 = mis ? lds32(wa + 20u) : 0u;
+      x0 = __funnelshift_r(w0, w1, sh) ^ 0x80808080u;
+      x1 = __funnelshift_r(w4, w5, sh) ^ 0x80808080u;
+    } else {
+      // codes 8q .. 8q+7: three words (two when aligned), two lanes a bank
+      const uint32_t o = 34u * static_cast<uint32_t>(bp) + 2u + 8u * static_cast<uint32_t>(q);
+      const uint32_t wa = rowa + (o & ~3u);
+      const uint32_t w0 = lds32(wa), w1 = lds32(wa + 4u), w2 = mis ? lds32(wa + 8u) : 0u;
+      x0 = __funnelshift_r(w0, w1, sh) ^ 0x80808080u;
+      x1 = __funnelshift_r(w1, w2, sh) ^ 0x80808080u;
+    }
     const uint32_t dw = lds32(rowa + ((34u * static_cast<uint32_t>(bp)) & ~3u));
     const float d = f16_lo(mis ? dw : (dw >> 16));
     const float2 dd = make_float2(d, d), mb = make_float2(-kMagicS8, -kMagicS8);
@@ -162,27 +181,38 @@ __device__ __forceinline__ void load_weights(uint32_t stage, int rows_box, int r
 }
 
 // The lane's A values of token row `row` (0..15) for block bp of a stage, in
-// the order of its weights (Q8_0 / f16: elements 8q .. 8q+7 of the block;
-// Q4_0: 4q .. 4q+3 and 16+4q .. 19+4q), as four bf16 pairs (nearest even).
-// The piece's A is M rows of 256 values (1 KB each). (One box a stage:
-// eight 128-byte-swizzled boxes, free of bank conflicts, issued eight times
-// as many copies and measured slower.)
-template <int FMT>
+// the order of its weights (elements 8q .. 8q+7 of the block, 16-byte
+// chunks 2q and 2q+1; Q4_0, and Q8_0 with BIG: 4q .. 4q+3 and 16+4q ..
+// 19+4q, chunks q and 4+q), as four bf16 pairs (nearest even). The piece's
+// A is M rows of 256 values (1 KB each), so every row's chunk c sits in the
+// same banks and a quarter-warp's eight lanes, two rows, read each bank
+// twice. With BIG the odd row reads its two chunks in the other order (the
+// first load of all eight lanes then covers the 32 banks once); with 8 rows
+// or fewer the swap measured slower (Q8_0 M=8 2048x2048 4.24 against 3.73
+// us). (One box a stage: eight 128-byte-swizzled boxes issued eight times as
+// many copies and measured slower.)
+template <int FMT, bool BIG>
 __device__ __forceinline__ void load_a(uint32_t sa, int row, int M, int bp, int q, uint32_t (&a)[4]) {
   const uint32_t rbase = sa + static_cast<uint32_t>(row * 1024 + bp * 128);
-  const uint32_t c0 = FMT == LQ_FMT_Q4_0 ? q : 2 * q, c1 = FMT == LQ_FMT_Q4_0 ? 4 + q : 2 * q + 1;
+  const bool quarters = FMT == LQ_FMT_Q4_0 || (FMT == LQ_FMT_Q8_0 && BIG);
+  const uint32_t c0 = quarters ? q : 2 * q, c1 = quarters ? 4 + q : 2 * q + 1;
+  const bool odd = BIG && (row & 1) != 0;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 x = row < M ? lds128f(rbase + (c0 << 4)) : z;  // rows past M: zeros (not in the slot)
-  const float4 y = row < M ? lds128f(rbase + (c1 << 4)) : z;
-  a[0] = pack_bf16x2(x.x, x.y);
-  a[1] = pack_bf16x2(x.z, x.w);
-  a[2] = pack_bf16x2(y.x, y.y);
-  a[3] = pack_bf16x2(y.z, y.w);
+  const float4 x = row < M ? lds128f(rbase + ((odd ? c1 : c0) << 4)) : z;  // rows past M: zeros (not in the slot)
+  const float4 y = row < M ? lds128f(rbase + ((odd ? c0 : c1) << 4)) : z;
+  const uint32_t p0 = pack_bf16x2(x.x, x.y), p1 = pack_bf16x2(x.z, x.w);
+  const uint32_t p2 = pack_bf16x2(y.x, y.y), p3 = pack_bf16x2(y.z, y.w);
+  a[0] = odd ? p2 : p0;
+  a[1] = odd ? p3 : p1;
+  a[2] = odd ? p0 : p2;
+  a[3] = odd ? p1 : p3;
 }
 
 // NP: pairs of 8-row tiles a CTA (its T tiles, 2 NP - 1 <= T <= 2 NP), so the
-// tile loop is unrolled without branches and holds 2 NP accumulators.
-template <int FMT, int EPI, int NP>
+// tile loop is unrolled without branches and holds 2 NP accumulators. BIG:
+// more than 8 rows of A (otherwise the MMA's rows 8..15 are zeros, never
+// loaded).
+template <int FMT, int EPI, int NP, bool BIG>
 __global__ void __launch_bounds__(kSThreads, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                       const SmallParams p) {
@@ -245,7 +275,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   // ---- main loop: warp w takes block w % 8 of piece w / 8 of each stage,
   // for every tile, two tiles at a time (independent chains of loads,
-  // conversions and MMAs); lane (g, q): W row 8t + g, codes 8q .. 8q+7, and
+  // conversions and MMAs); lane (g, q): W row 8t + g, its 8 codes, and
   // the A values of tokens g and g + 8 in the same order
   const int bp = warp & 7, sp = warp >> 3, g = lane >> 2, q = lane & 3;
   float acc[2 * NP][4];
@@ -269,9 +299,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
       const uint32_t sa = slot + static_cast<uint32_t>(sp * p.M) * kARowBytes;
       const uint32_t wst = slot + static_cast<uint32_t>(kPPS * p.M) * kARowBytes + static_cast<uint32_t>(sp) * p.w_pitch;
-      uint32_t alo[4], ahi[4];
-      load_a<FMT>(sa, g, p.M, bp, q, alo);
-      load_a<FMT>(sa, g + 8, p.M, bp, q, ahi);
+      uint32_t alo[4], ahi[4] = {0u, 0u, 0u, 0u};
+      load_a<FMT, BIG>(sa, g, p.M, bp, q, alo);
+      if constexpr (BIG) load_a<FMT, BIG>(sa, g + 8, p.M, bp, q, ahi);
 #pragma unroll
       for (int i = 0; i < 2 * NP; i += 2) {
         // with an odd tile count the last pair repeats tile i into acc[i + 1];
@@ -279,8 +309,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // bytes of the ring or its tail; neither is ever stored
         const int t1 = min(i + 1, T - 1);
         uint32_t b0[4], b1[4];
-        load_weights<FMT>(wst, p.rows_box, 8 * i + g, bp, q, b0);
-        load_weights<FMT>(wst, p.rows_box, 8 * t1 + g, bp, q, b1);
+        load_weights<FMT, BIG>(wst, p.rows_box, 8 * i + g, bp, q, b0);
+        load_weights<FMT, BIG>(wst, p.rows_box, 8 * t1 + g, bp, q, b1);
         mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], b0[0], b0[1]);  // the lane's values 0 .. 3
         mma_bf16_16816(acc[i + 1], alo[0], ahi[0], alo[1], ahi[1], b1[0], b1[1]);
         mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], b0[2], b0[3]);  // values 4 .. 7
@@ -342,10 +372,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 }
 
-template <int FMT, int EPI, int NP>
-lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
+template <int FMT, int EPI, int NP, bool BIG>
+lq_status launch_small_k(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                          int G, size_t smem) {
-  auto kern = gemm_small_kernel<FMT, EPI, NP>;
+  auto kern = gemm_small_kernel<FMT, EPI, NP, BIG>;
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -368,6 +398,13 @@ lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUten
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tw, ta, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
+}
+
+template <int FMT, int EPI, int NP>
+lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
+                         int G, size_t smem) {
+  return p.M > 8 ? launch_small_k<FMT, EPI, NP, true>(a, tw, ta, p, G, smem)
+                 : launch_small_k<FMT, EPI, NP, false>(a, tw, ta, p, G, smem);
 }
 
 // the kernel for the CTAs' tile count: the largest CTA holds ceil(N / G)
