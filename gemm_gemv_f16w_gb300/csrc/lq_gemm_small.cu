@@ -275,9 +275,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
   // ---- main loop: warp w takes block w % 8 of piece w / 8 of each stage,
   // for every tile, two tiles at a time (independent chains of loads,
-  // conversions and MMAs); lane (g, q): W row 8t + g, its 8 codes, and
+  // conversions and MMAs); lane (g, q): W row 8t + wr, its 8 codes, and
   // the A values of tokens g and g + 8 in the same order
   const int bp = warp & 7, sp = warp >> 3, g = lane >> 2, q = lane & 3;
+  // f16: MMA column g of a tile is W row wr = g / 2 + 4 (g % 2) of it, so
+  // the two rows a quarter-warp reads sit in different halves of the boxes'
+  // 128-byte swizzle (conflict-free 16-byte loads: f16 M=16 6144x2048 6.89
+  // -> 6.66 us; the block formats keep column g = row g, measured 1 % ahead)
+  const int wr = FMT == LQ_FMT_F16 ? (g >> 1) + 4 * (g & 1) : g;
   float acc[2 * NP][4];
 #pragma unroll
   for (int i = 0; i < 2 * NP; ++i)
@@ -309,8 +314,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         // bytes of the ring or its tail; neither is ever stored
         const int t1 = min(i + 1, T - 1);
         uint32_t b0[4], b1[4];
-        load_weights<FMT, BIG>(wst, p.rows_box, 8 * i + g, bp, q, b0);
-        load_weights<FMT, BIG>(wst, p.rows_box, 8 * t1 + g, bp, q, b1);
+        load_weights<FMT, BIG>(wst, p.rows_box, 8 * i + wr, bp, q, b0);
+        load_weights<FMT, BIG>(wst, p.rows_box, 8 * t1 + wr, bp, q, b1);
         mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], b0[0], b0[1]);  // the lane's values 0 .. 3
         mma_bf16_16816(acc[i + 1], alo[0], ahi[0], alo[1], ahi[1], b1[0], b1[1]);
         mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], b0[2], b0[3]);  // values 4 .. 7
@@ -358,7 +363,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
 #pragma unroll 1
   for (int idx = threadIdx.x; idx < T * 128; idx += kSThreads) {
-    const int t = idx >> 7, e = idx & 127, m = e >> 3, n = 8 * t + (e & 7);
+    const int t = idx >> 7, e = idx & 127, m = e >> 3, c = e & 7;  // c: MMA column
+    const int n = 8 * t + (FMT == LQ_FMT_F16 ? (c >> 1) + 4 * (c & 1) : c);
     if (m < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
       float sum = 0.f;
 #pragma unroll
