@@ -262,16 +262,23 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     b.abort = 0;
     fence_barrier_init();
-    tc::prefetch_tmap(&tmW);
-    tc::prefetch_tmap(&tmA);
-    for (int j = 0; j < first; ++j) issue_w(j, j);  // weights depend on nothing
   }
   __syncthreads();
   pdl_launch_dependents();
-  // A (and C) only once the previous kernel on the stream has completed
-  pdl_wait();
-  if (threadIdx.x == 0)
+  // the first stages' copies from two threads at once: the weights (they
+  // depend on nothing) and, once the previous kernel on the stream has
+  // completed, A (a slot's barrier may see A's bytes land before the
+  // weights' thread has announced them: the transaction count dips below
+  // zero and the phase still completes only after that announcement)
+  if (threadIdx.x == 0) {
+    tc::prefetch_tmap(&tmW);
+    for (int j = 0; j < first; ++j) issue_w(j, j);
+  } else if (threadIdx.x == 32) {
+    tc::prefetch_tmap(&tmA);
+    pdl_wait();
     for (int j = 0; j < first; ++j) issue_a(j, j);
+  }
+  pdl_wait();  // (C and R)
 
   // ---- main loop: warp w takes block w % 8 of piece w / 8 of each stage,
   // for every tile, two tiles at a time (independent chains of loads,
