@@ -8,8 +8,10 @@ HBM peak). One step is one decode pass over a stack of R such weight matrices
 activation row. For M = 1 the pass is one lq_gemv_chain call (the R GEMVs are
 independent: each has its own A and C); the same pass as R separate
 lq_matmul calls, and as a chain whose every problem waits for the previous
-one, is reported under "workloads" too. Steps are captured once as a CUDA
-graph and replayed, so the GPU never waits on the host. The other workload
+one, is reported under "workloads" too. Steps are captured as CUDA graphs
+(eight steps back to back, and one for a remainder) and replayed, so the GPU
+never waits on the host and, as in a decode loop, a step's kernels may start
+streaming their weights while the previous step finishes. The other workload
 families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and the
 M = 2 / 16 / 64 crossover) are timed the same way under "workloads", each
 entry "name [mode]": [value, unit, fraction of the measured peak, µs a
@@ -44,6 +46,8 @@ import torch  # noqa: E402
 import synthetic  # noqa: E402
 
 HEADLINE = "gemv_q8_0_4096x4096"
+GRAPH_STEPS = 8  # steps captured in one CUDA graph for the timed replays
+
 KERNEL_OF_MODE = {"chain": "gemv_chain_kernel", "chain-dependent": "gemv_chain_kernel",
                   "calls": "gemv_stream_kernel", "argmax": "gemv_stream_kernel",
                   "argmax-unfused": "gemv_stream_kernel", "topk": "gemv_stream_kernel"}
@@ -263,23 +267,40 @@ class Workbench:
             self.step()
         torch.cuda.synchronize(self.dev)
         self.graph = g
+        # GRAPH_STEPS steps back to back in one graph, as a decode loop issues
+        # them: each step's kernels may start streaming their weights while
+        # the previous step finishes (programmatic dependent launch works
+        # within a graph, not across two graph launches)
+        gn = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gn):
+            for _ in range(GRAPH_STEPS):
+                self.step()
+        torch.cuda.synchronize(self.dev)
+        self.graph_n = gn
         st = self.lq.last_device_error()
         if st != self.lq.LQ_OK:
             raise RuntimeError(f"device status after warm-up: {self.lq.status_string(st)}")
 
-    def time_graph(self, steps: int, warmup: int, barrier=None):
-        """Device time in seconds of `steps` graph replays (CUDA events on
-        the replay stream), after `warmup` replays."""
-        stream = torch.cuda.current_stream(self.dev)
-        for _ in range(warmup):
+    def replay(self, steps: int):
+        """Exactly `steps` steps: whole GRAPH_STEPS-step graphs, then
+        single-step ones."""
+        full, rest = divmod(steps, GRAPH_STEPS)
+        for _ in range(full):
+            self.graph_n.replay()
+        for _ in range(rest):
             self.graph.replay()
+
+    def time_graph(self, steps: int, warmup: int, barrier=None):
+        """Device time in seconds of `steps` steps replayed from the graphs
+        (CUDA events on the replay stream), after `warmup` steps."""
+        stream = torch.cuda.current_stream(self.dev)
+        self.replay(warmup)
         torch.cuda.synchronize(self.dev)
         if barrier:
             barrier()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for _ in range(steps):
-            self.graph.replay()
+        self.replay(steps)
         t1.record(stream)
         torch.cuda.synchronize(self.dev)
         if barrier:
@@ -318,7 +339,7 @@ class Workbench:
         return dt, self.A_host.numel() * 4, self.C_host.numel() * 4, checksum
 
     def free(self):
-        self.graph = None
+        self.graph = self.graph_n = None
         self.Wd = self.Ad = self.Cd = None
         torch.cuda.empty_cache()
 
@@ -631,7 +652,8 @@ def main():
             "config": workload_config(w),
             "step": {"mode": wb.mode, "matmuls": wb.R, "launches": launches_per_step,
                      "weight_copies_mib": round(wb.R * wb.wbytes / 2**20), "l2_mib": L2_BYTES // 2**20,
-                     "how": "one pass over the weight-copy stack, CUDA-graph replay",
+                     "how": f"one pass over the weight-copy stack; K steps back to back on one stream, "
+                            f"replayed from CUDA graphs of {GRAPH_STEPS} steps (and of 1 for the remainder)",
                      "parallelism": f"replicas x{world}"},
             "roofline": roofline,
             "cpu_baseline": cpu,

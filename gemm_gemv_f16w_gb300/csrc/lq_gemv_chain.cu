@@ -5,8 +5,11 @@
 // earlier one (q/k/v and o projections, gate/up and down, the LM head). As
 // separate launches, every GEMV pays its launch, the release of the
 // dependent kernel after the previous one drained, and a cold start of its
-// weight stream. Here one CTA per SM (a cooperative launch, so all CTAs are
-// resident together) walks the whole list:
+// weight stream. Here one CTA per SM walks the whole list (a launch of
+// independent problems starts early after the previous kernel on the
+// stream, its weights streaming at once and its A read once that kernel has
+// completed; with the in-kernel waits below it is a cooperative launch, so
+// that all CTAs are resident together):
 //
 //  * the producer warp streams every problem's weight rows through one ring
 //    of shared-memory slots, running ahead into later problems as soon as
@@ -173,6 +176,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     hd.nstage[j] = (n + RS - 1) / RS;
   }
   __syncthreads();
+  // the next kernel on the stream may start streaming its weights as this
+  // one's CTAs leave; A is read only once the previous kernel has completed
+  // (below)
+  pdl_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ---------------- weight stream ----------------
@@ -223,6 +230,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) gemv_chain_kernel(const __gr
     const int at = (warp - kAWarp) * 32 + lane;  // 0 .. 32 * kAWarps - 1
     int issued = 0, landed = 0;
     bool ok = true;
+    // every A (and, after it, every C) only once the previous kernel on the
+    // stream has completed (at once in a cooperative launch, which never
+    // starts early); the weight stream above does not wait
+    if (lead) pdl_wait();
     for (int j = 0; j < p.count; ++j) {
       const ChainProblem& q = p.pr[j];
       const int b = j & 1;
@@ -430,6 +441,10 @@ lq_status sync_slot(unsigned** out) {
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+// A launch whose problems wait for earlier ones inside it (the in-kernel
+// device-wide wait) is cooperative: every CTA resident at once. Otherwise
+// the CTAs never wait for each other and the launch may start early after
+// the previous kernel on the stream (programmatic dependent launch).
 template <int FMT>
 lq_status launch_chain_t(const ChainParams& p, size_t smem, cudaStream_t stream) {
   auto kern = gemv_chain_kernel<FMT>;
@@ -447,8 +462,13 @@ lq_status launch_chain_t(const ChainParams& p, size_t smem, cudaStream_t stream)
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once
-  attr[0].val.cooperative = 1;
+  if (p.publish) {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = use_pdl() ? 1 : 0;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, p);
@@ -548,8 +568,10 @@ lq_status launch_planned_chain(int fmt, ChainParams& p, size_t smem, cudaStream_
   lq_status st = sync_slot(&sync);
   if (st != LQ_OK) return st;
   p.sync = sync;
-  cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream);
-  if (e != cudaSuccess) return cuda_status(e);
+  if (p.publish) {  // the completion count and the abort word, read only by the in-kernel waits
+    const cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   if (fmt == LQ_FMT_F16) st = launch_chain_t<LQ_FMT_F16>(p, smem, stream);
   else if (fmt == LQ_FMT_Q8_0) st = launch_chain_t<LQ_FMT_Q8_0>(p, smem, stream);
   else st = launch_chain_t<LQ_FMT_Q4_0>(p, smem, stream);

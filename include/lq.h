@@ -177,10 +177,11 @@ lq_status lq_pack_q8_0_rcp(const float* W_host, int64_t N, int64_t K, void* out_
  * problem j reads A_j only after problems 0 .. j-1 are complete, so A_j may
  * be (or depend on) an earlier C; otherwise A_j must not be written by this
  * call. Weights are streamed ahead of the computation in every case. Each
- * run of problems that wait for nothing is one launch (a cooperative launch
- * of one CTA per SM, or the streaming GEMV for a run of one problem), the
- * runs in order on the stream; the problems array is read during the call
- * (host memory, caller-owned).
+ * run of problems that wait for nothing is one launch (one CTA per SM, or
+ * the streaming GEMV for a run of one problem), the runs in order on the
+ * stream, each streaming its weights while the previous kernel finishes and
+ * reading A after it; the problems array is read during the call (host
+ * memory, caller-owned).
  *   - count in 1..64; N_j >= 0; K_j % 8 == 0 (f16) or K_j % 256 == 0
  *     (quantised) with the largest K_j at most 4096 (f16), 14336 (Q8_0) or
  *     15616 (Q4_0, Q4_0I) so that A and the ring fit in shared memory;

@@ -136,6 +136,49 @@ def test_chain_runs_of_independent_problems_between_dependent_ones(lq, cuda_dev)
         check(Cs[j].cpu().numpy()[None, :], y, tol, f"problem {j}")
 
 
+def test_chain_calls_back_to_back_read_and_overwrite_earlier_data(lq, cuda_dev):
+    """A launch of independent problems may start while the previous kernel
+    on the stream runs (its weights stream at once; A is read, and C
+    written, after that kernel has completed). Three calls with no
+    synchronisation between them: the second reads the first's outputs, the
+    third overwrites what the second read, and a streaming GEMV then reads
+    the third's output. The kernels are deterministic, so every output must
+    equal, bit for bit, the same calls run with a synchronisation after
+    each; that run is checked against the oracle."""
+    fmt, K = "q8_0", 4096
+    Ws = [_weights(lq, fmt, K, K, 700 + j, cuda_dev) for j in range(4)]
+    A0 = torch.randn(K, generator=torch.Generator().manual_seed(9), dtype=torch.float32).to(cuda_dev)
+
+    def run(sync):
+        C = [nan_filled(1, K, cuda_dev)[0] for _ in range(5)]
+        calls = [
+            [(A0, Ws[0][1], C[0], K, K, 0), (A0, Ws[1][1], C[1], K, K, 0)],
+            [(C[0], Ws[2][1], C[2], K, K, 0), (C[1], Ws[3][1], C[3], K, K, 0)],
+            [(C[2], Ws[0][1], C[0], K, K, 0), (C[3], Ws[1][1], C[1], K, K, 0)],
+        ]
+        seen = []
+        for items in calls:
+            assert lq.lq_gemv_chain(fmt, items) == lq.LQ_OK
+            if sync:
+                torch.cuda.synchronize()
+                seen.append([c.clone() for c in C])
+        lq.lq_gemv_q8_0(C[0], Ws[3][1], C[4], 1, K, K)
+        torch.cuda.synchronize()
+        assert lq.last_device_error() == lq.LQ_OK
+        return [c.cpu() for c in C], seen
+
+    ref, seen = run(True)
+    out, _ = run(False)
+    for j in range(5):
+        assert torch.equal(out[j].view(torch.int32), ref[j].view(torch.int32)), f"output {j}"
+    # the synchronised run against the oracle, call by call on its own inputs
+    after1, after2 = seen[0], seen[1]
+    for src, w, dst, tag in [(A0.cpu(), 0, after1[0].cpu(), "C0"), (after1[0].cpu(), 2, after2[2].cpu(), "C2"),
+                             (after2[2].cpu(), 0, ref[0], "C0 again"), (ref[0], 3, ref[4], "GEMV")]:
+        y, tol = O.reference(fmt, src.numpy()[None, :], O.pack(fmt, Ws[w][0]), K, K)
+        check(dst.numpy()[None, :], y, tol, tag)
+
+
 def test_chain_refuses_shapes_outside_its_path(lq, cuda_dev):
     fmt = "q8_0"
     K, N = 96, 64  # K % 256 != 0
