@@ -10,8 +10,9 @@
 //     operand the tensor-core tolerance is defined on, over the whole f32
 //     range (bf16 keeps f32's exponent);
 //  2. the GEMM kernel, one CTA per SM, owns 128 rows of W and a tile of BT
-//     tokens. A producer thread moves raw W (f16 / Q8_0 / Q4_0 bytes) with
-//     one TMA box of full-width rows per stage: Q8_0 rows of 256 K are 272
+//     tokens. Raw W (f16 / Q8_0 / Q4_0 bytes) arrives by TMA, one box of
+//     full-width rows per stage, each slot refilled by a warp of its own as
+//     soon as the converters have read it: Q8_0 rows of 256 K are 272
 //     bytes and Q4_0 rows 144 bytes, both odd multiples of 16, so eight
 //     threads reading 16-byte chunks of eight consecutive rows hit eight
 //     different bank groups; f16 rows (64 K = 128 bytes per box) use the
@@ -53,7 +54,8 @@ __device__ unsigned g_tma_err;
 constexpr int kNumConv = 8;                        // converter warps (kGroups groups of 4)
 constexpr int kGroups = kNumConv / 4;              // a group's 4 warps cover the 128 TMEM lanes
 constexpr int kConvThreads = kNumConv * 32;
-constexpr int kTmaThreads = (2 + kNumConv) * 32;   // producer, MMA, converters
+constexpr int kRawWarp = 2 + kNumConv;             // raw W refills
+constexpr int kTmaThreads = (3 + kNumConv) * 32;   // producer, MMA, converters, raw W
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
 constexpr int kMaxStages = 4, kMaxRawStages = 8;  // A ring (streamed A), raw W ring
@@ -361,7 +363,9 @@ __device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t*
 }
 
 // ---------------------------------------------------------------------------
-// The GEMM kernel. Warp 0: TMA producer. Warp 1: TMEM owner and MMA issuer.
+// The GEMM kernel. Warp 0: TMA producer of the A stages (and of the first
+// raw W stages). Warp 1: TMEM owner and MMA issuer. Warp 2 + kNumConv: the
+// raw W refills.
 // Warps 2..: converters in kGroups groups of four (group g converts the
 // pipeline stages ks with ks % kGroups == g: 128 K of its W rows into the
 // stage's 64 TMEM columns); then every group runs the epilogue, group g
@@ -479,22 +483,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       }
     }
     __syncwarp();
-    int raw_issued = raw_first, issued = 0;  // the first raw stages are out
+    int issued = 0;
     bool ok = true;
     pdl_wait();
-    int st = 0, lap = 0, rslot = 0, rlap = 0;  // stage ring / raw ring positions
+    int st = 0, lap = 0;  // stage ring position
     for (int ks = 0; ks < nk; ++ks) {
-      if (ks % SUB == 0 && ks / SUB >= RR) {
-        const int j = ks / SUB;  // reuse raw slot j % 2 after both of its users finished
-        if (!warp_wait(&b.raw_empty[rslot], rlap & 1, p) || b.abort) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) issue_raw(j, rslot);
-        __syncwarp();
-        ++raw_issued;
-        if (++rslot == RR) { rslot = 0; ++rlap; }
-      }
       if (ks >= S && (!warp_wait(&b.empty[st], (lap - 1) & 1, p) || b.abort)) {
         ok = false;
         break;
@@ -522,8 +515,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       b.abort = 1;
     }
     // never leave copies in flight (waits for the last use of every slot)
-    for (int j = max(0, raw_issued - RR); j < raw_issued; ++j)
-      mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
     if (!p.a_res)
       for (int ks = max(0, issued - S); ks < issued; ++ks)
         mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
@@ -575,6 +566,34 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (lane == 0) tc::commit(&b.tmem_full);
     __syncwarp();
     if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
+  } else if (warp == kRawWarp) {
+    // ---------------- raw W refills ----------------
+    // slot j % RR gets raw stage j once its 4 SUB converter warps have read
+    // stage j - RR. A warp of its own: in the producer's loop a refill
+    // waited behind the A stages, which wait for the MMAs (Q8_0 M = 512
+    // 18.1 -> 17.5 us on taking it out of that loop); issued by the last
+    // converter warp instead it stalled that warp's conversions (f16 17.5 ->
+    // 18.1 us).
+    int issued = raw_first;
+    bool ok = true;
+    int rslot = 0, rlap = 0;
+    for (int j = RR; j < nraw; ++j) {
+      if (!warp_wait(&b.raw_empty[rslot], rlap & 1, p) || b.abort) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) issue_raw(j, rslot);
+      __syncwarp();
+      ++issued;
+      if (++rslot == RR) { rslot = 0; ++rlap; }
+    }
+    if (!ok && lane == 0) {
+      record_error(kDevErrTimeout);
+      b.abort = 1;
+    }
+    // never leave copies in flight
+    for (int j = max(0, issued - RR); j < issued; ++j)
+      mbar_wait(&b.raw_full[j % RR], (j / RR) & 1, kDrainWaitNs);
   } else {
     // ---------------- converters ----------------
     const int cw = warp - 2, g = cw >> 2, q4 = warp & 3;
@@ -699,7 +718,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // the peers' partial tiles are in their shared memory; the leader adds
     // them to its own (rank order: a fixed summation order) and stores C
     cluster_sync();
-    if (rank == 0 && epi && warp >= 2) {
+    if (rank == 0 && epi && warp >= 2 && warp < kRawWarp) {
       tc::fence_after_sync();
       const int q4 = warp & 3, r = 32 * q4 + lane, g = (warp - 2) >> 2;
       store_tile<FMT, EPI>(p, tmem + (static_cast<uint32_t>(32 * q4) << 16), r, n0, m0, bt, smem_u32(a_ring),
