@@ -13,7 +13,7 @@ one, is reported under "workloads" too. Steps are captured as CUDA graphs
 never waits on the host and, as in a decode loop, a step's kernels may start
 streaming their weights while the previous step finishes. The other workload
 families (the f16 / Q4_0 GEMVs, the LM head, the prefill GEMMs and the
-M = 2 / 16 / 64 crossover) are timed the same way under "workloads", each
+M = 2 .. 64 crossover) are timed the same way under "workloads", each
 entry "name [mode]": [value, unit, fraction of the measured peak, µs a
 matmul], the prefill GEMMs last.
 
@@ -477,7 +477,7 @@ def run_reference(args, world, rank):
 
 EXTRA = ["gemv_f16_256x512", "gemv_q4_0_11008x4096_outliers", "gemv_f16_lmhead_151936x2048",
          "gemm_f16_512x6144x2048", "gemm_q8_0_512x6144x2048", "gemm_q4_0_512x6144x2048"] + \
-        [f"gemm_{f}_m{m}_6144x2048" for m in (2, 4, 8, 16, 64) for f in ("f16", "q8_0", "q4_0")]
+        [f"gemm_{f}_m{m}_6144x2048" for m in (2, 4, 8, 16, 32, 64) for f in ("f16", "q8_0", "q4_0")]
 
 
 def workload_rank(key: str) -> tuple:
@@ -599,7 +599,7 @@ def main():
         if synthetic.WORKLOADS[name].M == 1:
             runs.append((name, "calls"))  # the decode GEMVs both as a chain and as separate calls
         m = synthetic.WORKLOADS[name].M
-        if 1 < m <= 16:
+        if 1 < m <= 32:
             # the router's kernel (warp-MMA) against the tcgen05 kernel and,
             # up to eight rows, the batched decode kernel
             runs.append((name, "tc"))

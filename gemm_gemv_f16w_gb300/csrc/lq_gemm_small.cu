@@ -1,4 +1,4 @@
-// The prefill GEMM for a few rows of A (M = 2..16): C = A W^T on the tensor
+// The prefill GEMM for a few rows of A (M = 2..32): C = A W^T on the tensor
 // cores with warp-level MMAs, every weight read from HBM once.
 //
 // For so few tokens the weight stream sets the pace, as in the decode GEMV,
@@ -15,13 +15,16 @@
 //  * each stage also holds the same K of A (the M rows, f32, one box a
 //    piece), copied once the previous kernel on the stream has completed;
 //    the lanes round their A values to bf16 (nearest even) as they build the
-//    MMA operands (rows M..15 of the MMA are zeros);
+//    MMA operands (rows of the MMA past M are zeros);
 //  * warp w takes block w % 8 (32 K) of piece w / 8 of every stage, for
 //    every 8-row tile of the CTA, two tiles at a time: each lane dequantises
 //    8 weights of one row (lane / 4) exactly in f32 and rounds them once to
 //    bf16, the same operand as the tcgen05 kernel's, and two mma.m16n8k16
 //    (bf16 x bf16 -> f32; A = 16 tokens, B = 8 W rows) add the block to the
-//    tile's accumulator. Within a block lane q = lane % 4 takes 8 codes (f16
+//    tile's accumulator, for each group of 16 tokens (more than 16 rows of
+//    A: two groups share every converted weight, for CTAs of at most 64 W
+//    rows, whose accumulators fit in registers). Within a block lane q =
+//    lane % 4 takes 8 codes (f16
 //    elements 8q .. 8q+7; Q8_0 codes 4q .. 4q+3 and 16+4q .. 19+4q; Q4_0 the
 //    low and high nibbles of bytes 4q .. 4q+3, the same codes), so the MMA's
 //    K order is a fixed permutation of the block, and each lane reads the A
@@ -53,6 +56,8 @@ constexpr int kPieceK = 256;      // K of one weight stage: 8 blocks of 32
 constexpr int kSMaxStages = 8;
 constexpr int kSMaxTiles = 16;    // 8-row W tiles of a CTA (128 rows)
 constexpr int kSTokens = 16;      // the MMA's M: rows of A, zero-padded
+constexpr int kSMaxM = 32;        // two token groups of 16 share every converted weight
+constexpr int kSMaxPairs2 = 4;    // tile pairs a CTA with two token groups (64 W rows)
 
 // Bytes of one W row's 256 K in a stage.
 __host__ __device__ constexpr int piece_row_bytes(int fmt) {
@@ -211,8 +216,9 @@ __device__ __forceinline__ void load_a(uint32_t sa, int row, int M, int bp, int 
 // NP: pairs of 8-row tiles a CTA (its T tiles, 2 NP - 1 <= T <= 2 NP), so the
 // tile loop is unrolled without branches and holds 2 NP accumulators. BIG:
 // more than 8 rows of A (otherwise the MMA's rows 8..15 are zeros, never
-// loaded).
-template <int FMT, int EPI, int NP, bool BIG>
+// loaded). TG: groups of 16 tokens (rows 16 tg ..), each weight pair
+// converted once and multiplied with every group.
+template <int FMT, int EPI, int NP, bool BIG, int TG>
 __global__ void __launch_bounds__(kSThreads, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                       const SmallParams p) {
@@ -290,11 +296,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // 128-byte swizzle (conflict-free 16-byte loads: f16 M=16 6144x2048 6.89
   // -> 6.66 us; the block formats keep column g = row g, measured 1 % ahead)
   const int wr = FMT == LQ_FMT_F16 ? (g >> 1) + 4 * (g & 1) : g;
-  float acc[2 * NP][4];
+  float acc[2 * NP][TG][4];
 #pragma unroll
   for (int i = 0; i < 2 * NP; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    for (int j = 0; j < 4 * TG; ++j) acc[i][j >> 2][j & 3] = 0.f;
   int s = 0;
   uint32_t ph = 0;
 #pragma unroll 1
@@ -311,9 +317,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
       const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
       const uint32_t sa = slot + static_cast<uint32_t>(sp * p.M) * kARowBytes;
       const uint32_t wst = slot + static_cast<uint32_t>(kPPS * p.M) * kARowBytes + static_cast<uint32_t>(sp) * p.w_pitch;
-      uint32_t alo[4], ahi[4] = {0u, 0u, 0u, 0u};
-      load_a<FMT, BIG>(sa, g, p.M, bp, q, alo);
-      if constexpr (BIG) load_a<FMT, BIG>(sa, g + 8, p.M, bp, q, ahi);
+      uint32_t alo[TG][4], ahi[TG][4];
+#pragma unroll
+      for (int tg = 0; tg < TG; ++tg) {
+        load_a<FMT, BIG>(sa, 16 * tg + g, p.M, bp, q, alo[tg]);
+        if constexpr (BIG)
+          load_a<FMT, BIG>(sa, 16 * tg + g + 8, p.M, bp, q, ahi[tg]);
+        else
+          ahi[tg][0] = ahi[tg][1] = ahi[tg][2] = ahi[tg][3] = 0u;
+      }
 #pragma unroll
       for (int i = 0; i < 2 * NP; i += 2) {
         // with an odd tile count the last pair repeats tile i into acc[i + 1];
@@ -323,10 +335,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         uint32_t b0[4], b1[4];
         load_weights<FMT, BIG>(wst, p.rows_box, 8 * i + wr, bp, q, b0);
         load_weights<FMT, BIG>(wst, p.rows_box, 8 * t1 + wr, bp, q, b1);
-        mma_bf16_16816(acc[i], alo[0], ahi[0], alo[1], ahi[1], b0[0], b0[1]);  // the lane's values 0 .. 3
-        mma_bf16_16816(acc[i + 1], alo[0], ahi[0], alo[1], ahi[1], b1[0], b1[1]);
-        mma_bf16_16816(acc[i], alo[2], ahi[2], alo[3], ahi[3], b0[2], b0[3]);  // values 4 .. 7
-        mma_bf16_16816(acc[i + 1], alo[2], ahi[2], alo[3], ahi[3], b1[2], b1[3]);
+#pragma unroll
+        for (int tg = 0; tg < TG; ++tg) {
+          const uint32_t* al = alo[tg];
+          const uint32_t* ah = ahi[tg];
+          mma_bf16_16816(acc[i][tg], al[0], ah[0], al[1], ah[1], b0[0], b0[1]);  // the lane's values 0 .. 3
+          mma_bf16_16816(acc[i + 1][tg], al[0], ah[0], al[1], ah[1], b1[0], b1[1]);
+          mma_bf16_16816(acc[i][tg], al[2], ah[2], al[3], ah[3], b0[2], b0[3]);  // values 4 .. 7
+          mma_bf16_16816(acc[i + 1][tg], al[2], ah[2], al[3], ah[3], b1[2], b1[3]);
+        }
       }
     }
     // The last warp done with the slot refills it (every warp's reads of it
@@ -358,24 +375,29 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 
   // ---- the 16 block positions' partial tiles, added in a fixed order
-  // (shared memory of the ring, every stage consumed): red[t][w][m][n]
+  // (shared memory of the ring, every stage consumed): red[t][w][m][n],
+  // 16 TG tokens x 8 columns a tile
+  constexpr int kTileF = 128 * TG;
   float* red = reinterpret_cast<float*>(ring);
 #pragma unroll
   for (int t = 0; t < 2 * NP; ++t) {
     if (t >= T) break;
-    float* tile = red + (t * kSWarps + warp) * 128;
-    *reinterpret_cast<float2*>(tile + g * 8 + 2 * q) = make_float2(acc[t][0], acc[t][1]);
-    *reinterpret_cast<float2*>(tile + (g + 8) * 8 + 2 * q) = make_float2(acc[t][2], acc[t][3]);
+    float* tile = red + (t * kSWarps + warp) * kTileF;
+#pragma unroll
+    for (int tg = 0; tg < TG; ++tg) {
+      *reinterpret_cast<float2*>(tile + (16 * tg + g) * 8 + 2 * q) = make_float2(acc[t][tg][0], acc[t][tg][1]);
+      *reinterpret_cast<float2*>(tile + (16 * tg + g + 8) * 8 + 2 * q) = make_float2(acc[t][tg][2], acc[t][tg][3]);
+    }
   }
   __syncthreads();
 #pragma unroll 1
-  for (int idx = threadIdx.x; idx < T * 128; idx += kSThreads) {
-    const int t = idx >> 7, e = idx & 127, m = e >> 3, c = e & 7;  // c: MMA column
+  for (int idx = threadIdx.x; idx < T * kTileF; idx += kSThreads) {
+    const int t = idx / kTileF, e = idx - t * kTileF, m = e >> 3, c = e & 7;  // c: MMA column
     const int n = 8 * t + (FMT == LQ_FMT_F16 ? (c >> 1) + 4 * (c & 1) : c);
     if (m < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
       float sum = 0.f;
 #pragma unroll
-      for (int k = 0; k < kSWarps; ++k) sum += red[(t * kSWarps + k) * 128 + e];
+      for (int k = 0; k < kSWarps; ++k) sum += red[(t * kSWarps + k) * kTileF + e];
       const long long o = static_cast<long long>(m) * p.N + r0 + n;
       if constexpr (EPI == epi::kResidual)
         p.C[o] = sum + p.R[o];
@@ -385,10 +407,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 }
 
-template <int FMT, int EPI, int NP, bool BIG>
+template <int FMT, int EPI, int NP, bool BIG, int TG>
 lq_status launch_small_k(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                          int G, size_t smem) {
-  auto kern = gemm_small_kernel<FMT, EPI, NP, BIG>;
+  auto kern = gemm_small_kernel<FMT, EPI, NP, BIG, TG>;
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -416,8 +438,14 @@ lq_status launch_small_k(const MatmulArgs& a, const CUtensorMap& tw, const CUten
 template <int FMT, int EPI, int NP>
 lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                          int G, size_t smem) {
-  return p.M > 8 ? launch_small_k<FMT, EPI, NP, true>(a, tw, ta, p, G, smem)
-                 : launch_small_k<FMT, EPI, NP, false>(a, tw, ta, p, G, smem);
+  if (p.M > kSTokens) {
+    // two token groups: the accumulators of up to 4 tile pairs fit the 128
+    // registers of 512 threads (the plan refuses more)
+    if constexpr (NP <= kSMaxPairs2) return launch_small_k<FMT, EPI, NP, true, 2>(a, tw, ta, p, G, smem);
+    return LQ_ERR_UNSUPPORTED;
+  }
+  return p.M > 8 ? launch_small_k<FMT, EPI, NP, true, 1>(a, tw, ta, p, G, smem)
+                 : launch_small_k<FMT, EPI, NP, false, 1>(a, tw, ta, p, G, smem);
 }
 
 // the kernel for the CTAs' tile count: the largest CTA holds ceil(N / G)
@@ -455,7 +483,7 @@ struct SmallPlan {
 bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   if (a.fmt != LQ_FMT_F16 && a.fmt != LQ_FMT_Q8_0 && a.fmt != LQ_FMT_Q4_0) return false;
   if (a.a_perm || (a.epi != epi::kPlain && a.epi != epi::kResidual)) return false;
-  if (a.M < 2 || a.M > kSTokens || a.K % kPieceK != 0 || a.K > (1 << 20) || a.N < 1 || a.N >= (1LL << 30))
+  if (a.M < 2 || a.M > kSMaxM || a.K % kPieceK != 0 || a.K > (1 << 20) || a.N < 1 || a.N >= (1LL << 30))
     return false;
   if (!aligned_to(a.A, 16) || !aligned_to(a.W, 16)) return false;
   if (!tma_encode_tiled()) return false;
@@ -464,6 +492,8 @@ bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   const int64_t G = std::min<int64_t>(di.sm_count, (a.N + 7) / 8);
   const int64_t rows = (a.N + G - 1) / G;
   if (rows > 8 * kSMaxTiles) return false;
+  const int tg = (a.M + kSTokens - 1) / kSTokens;
+  if (tg > 1 && rows > 16 * kSMaxPairs2) return false;
   pl.G = static_cast<int>(G);
   // the box covers the CTA's rows (f16: whole 8-row groups, for the
   // swizzled boxes' 1024-byte alignment); a tile's rows past the box read
@@ -475,7 +505,7 @@ bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   pl.slot_bytes = (kPPS * (static_cast<unsigned>(a.M) * kARowBytes + pl.w_pitch) + 1023u) / 1024u * 1024u;
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - kSBarsBytes;
   const int nstages = static_cast<int>((a.K / kPieceK + kPPS - 1) / kPPS);
-  const long long red = static_cast<long long>((rows + 7) / 8) * kSWarps * 128 * 4;  // partial tiles
+  const long long red = static_cast<long long>((rows + 7) / 8) * kSWarps * 128 * tg * 4;  // partial tiles
   // the last tile's rows past the box read up to 7 rows beyond the last slot
   const long long tail = 7LL * piece_row_bytes(a.fmt);
   const int S = static_cast<int>(std::min<long long>({kSMaxStages, nstages, (budget - tail) / pl.slot_bytes}));

@@ -62,7 +62,7 @@ WORKLOADS = {
     ]
     + [_wl(f"gemm_{f}_512x6144x2048", f, 512, 6144, 2048) for f in FORMATS]
     + [_wl(f"gemm_{f}_m{m}_6144x2048", f, m, 6144, 2048)
-       for m in (2, 4, 8, 16, 64) for f in FORMATS]
+       for m in (2, 4, 8, 16, 32, 64) for f in FORMATS]
 }
 
 

@@ -47,7 +47,7 @@ def test_tc_single_tile_single_kstep(lq, cuda_dev, fmt):
 def test_tc_shapes(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=M + N + K, outlier_frac=0.05)
     lq.reset_counts()
-    lq.force_route(lq.ROUTE_TENSOR_CORE)  # M <= 16 would take the warp-MMA or batched kernel
+    lq.force_route(lq.ROUTE_TENSOR_CORE)  # M <= 32 would take the warp-MMA or batched kernel
     try:
         C = _run(lq, cuda_dev, fmt, W, A)
     finally:
