@@ -1,4 +1,5 @@
-"""lq_topk_f32 and lq_gemv_topk against the oracle's topk_first.
+"""lq_topk_f32 and lq_gemv_topk against the oracle's topk_first (inputs up to
+4 Mi entries take the radix selection, larger ones the sorting passes).
 
 The order is decided in f32 on both sides: the oracle ranks the GPU's own
 float32 inputs (or logits), so indices must agree exactly and values bit for
@@ -30,7 +31,8 @@ def _expect(x, k):
 
 
 @pytest.mark.parametrize("n,k", [(1, 1), (5, 9), (1000, 1), (1000, 64), (151936, 50), (1 << 20, 40),
-                                 (3_000_001, 64), (1985, 17), (3968, 64)])
+                                 (3_000_001, 64), (1985, 17), (3968, 64), (4096, 64), (4097, 33),
+                                 ((1 << 22) + 1, 50)])  # past 4 Mi entries: the sorting passes
 def test_topk_random_with_ties_and_nan(lq, cuda_dev, n, k):
     rng = np.random.default_rng(n + k)
     x = rng.standard_normal(n).astype(np.float32)
