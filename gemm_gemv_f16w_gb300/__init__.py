@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_PKG, "liblq_debug.so" if os.environ.get("LQ_LIBRARY") =
 LQ_OK, LQ_ERR_INVALID_ARG, LQ_ERR_UNSUPPORTED, LQ_ERR_CUDA, LQ_ERR_DEVICE_TIMEOUT, LQ_ERR_BOUNDS = range(6)
 FMT = {"f16": 0, "q8_0": 1, "q4_0": 2, "q4_0i": 3}  # q4_0i: the pages' interleaved nibbles
 ROUTE_AUTO, ROUTE_STREAM, ROUTE_TENSOR_CORE, ROUTE_GENERIC = range(4)
-ROUTE_WARP_MMA = 5         # tensor cores, warp-level MMAs, M = 2..32
+ROUTE_WARP_MMA = 5         # tensor cores, warp-level MMAs, M = 2..48
 COUNT_CHAIN, COUNT_PREPASS = 4, 6  # route_count(): decode-chain launches, route 2's A pre-pass launches
 
 # every symbol include/lq.h declares

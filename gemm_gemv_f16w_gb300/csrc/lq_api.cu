@@ -139,15 +139,16 @@ lq_status do_gemm(int fmt, const float* A, const void* W, float* C, int64_t M, i
     case 5: return launch_gemm_small(a);
     default: break;
   }
-  // M = 2..32: the warp-MMA tensor-core kernel (N = 6144, K = 2048, Q8_0 /
+  // M = 2..48: the warp-MMA tensor-core kernel (N = 6144, K = 2048, Q8_0 /
   // f16 / Q4_0: 7.1 / 6.8 / 6.4 us at M = 2 against 7.7 / 9.2 / 7.0 on the
   // batched CUDA-core kernel and 10.6 / 10.1 / 10.6 on the tcgen05 kernel;
   // at M = 16 7.7 / 7.2 / 7.2 against 11.4 / 10.8 / 11.3 on tcgen05; from 17
-  // rows two token groups share each converted weight, for CTAs of up to 64
-  // W rows). The batched kernel takes the shapes the warp-MMA kernel does
-  // not (up to four rows), and two to eight rows by a forced route
-  // (lq_debug_force_route(1)).
-  if (M <= 32) {
+  // rows two or three token groups share each converted weight, for CTAs of
+  // up to 64 / 48 W rows: M = 32 8.3 / 9.9 / 7.7 against 12.9 / 12.3 / 12.7,
+  // M = 48 12.1 / 11.9 / 12.2 against 14.0 / 13.2 / 13.3). The batched kernel
+  // takes the shapes the warp-MMA kernel does not (up to four rows), and two
+  // to eight rows by a forced route (lq_debug_force_route(1)).
+  if (M <= 48) {
     st = launch_gemm_small(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }
@@ -187,7 +188,7 @@ lq_status do_epilogue(int fmt, const float* A, const void* W, const float* R, fl
   if (M == 1) return launch_gemv(a);  // falls back to the generic kernel itself
   // as do_gemm; the warp-MMA kernel has no SwiGLU epilogue, which keeps the
   // batched kernel up to four rows
-  if (M <= 32) {
+  if (M <= 48) {
     st = launch_gemm_small(a);
     if (st != LQ_ERR_UNSUPPORTED) return st;
   }

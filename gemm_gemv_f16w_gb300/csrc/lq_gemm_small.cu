@@ -1,4 +1,4 @@
-// The prefill GEMM for a few rows of A (M = 2..32): C = A W^T on the tensor
+// The prefill GEMM for a few rows of A (M = 2..48): C = A W^T on the tensor
 // cores with warp-level MMAs, every weight read from HBM once.
 //
 // For so few tokens the weight stream sets the pace, as in the decode GEMV,
@@ -22,8 +22,11 @@
 //    bf16, the same operand as the tcgen05 kernel's, and two mma.m16n8k16
 //    (bf16 x bf16 -> f32; A = 16 tokens, B = 8 W rows) add the block to the
 //    tile's accumulator, for each group of 16 tokens (more than 16 rows of
-//    A: two groups share every converted weight, for CTAs of at most 64 W
-//    rows, whose accumulators fit in registers). Within a block lane q =
+//    A: two or three groups share every converted weight, for CTAs of at
+//    most 64 or 48 W rows, whose accumulators fit in registers; where two
+//    pieces' A rows and weights do not fit twice in shared memory, stages of
+//    one piece, its 8 block positions shared by the warps' two halves, each
+//    taking every other tile pair). Within a block lane q =
 //    lane % 4 takes 8 codes (f16
 //    elements 8q .. 8q+7; Q8_0 codes 4q .. 4q+3 and 16+4q .. 19+4q; Q4_0 the
 //    low and high nibbles of bytes 4q .. 4q+3, the same codes), so the MMA's
@@ -52,19 +55,23 @@ __device__ unsigned g_small_err;
 __device__ __forceinline__ void record_error(unsigned code) { atomicCAS(&g_small_err, 0u, code); }
 
 constexpr int kSWarps = 16, kSThreads = kSWarps * 32;
+constexpr int kSPos = 16;  // block positions of a two-piece stage (8 blocks x 2 pieces)
 constexpr int kPieceK = 256;      // K of one weight stage: 8 blocks of 32
 constexpr int kSMaxStages = 8;
 constexpr int kSMaxTiles = 16;    // 8-row W tiles of a CTA (128 rows)
 constexpr int kSTokens = 16;      // the MMA's M: rows of A, zero-padded
-constexpr int kSMaxM = 32;        // two token groups of 16 share every converted weight
+constexpr int kSMaxM = 48;        // up to three token groups of 16 share every converted weight
 constexpr int kSMaxPairs2 = 4;    // tile pairs a CTA with two token groups (64 W rows)
+constexpr int kSMaxPairs3 = 3;    // with three (48 W rows: more lost to the tcgen05 kernel)
 
 // Bytes of one W row's 256 K in a stage.
 __host__ __device__ constexpr int piece_row_bytes(int fmt) {
   return fmt == LQ_FMT_F16 ? 512 : (fmt == LQ_FMT_Q8_0 ? 272 : 144);
 }
 
-constexpr int kPPS = 2;           // pieces a stage (the last stage may hold one)
+// pieces a stage (the last stage may hold fewer): 2, or 1 where two pieces'
+// A rows and weights would not fit twice in shared memory (M > 32; f16 at
+// M = 25..32 on wide CTAs)
 constexpr unsigned kARowBytes = kPieceK * 4;  // one row of A in a piece: 256 f32
 
 struct SmallParams {
@@ -214,11 +221,14 @@ __device__ __forceinline__ void load_a(uint32_t sa, int row, int M, int bp, int 
 }
 
 // NP: pairs of 8-row tiles a CTA (its T tiles, 2 NP - 1 <= T <= 2 NP), so the
-// tile loop is unrolled without branches and holds 2 NP accumulators. BIG:
-// more than 8 rows of A (otherwise the MMA's rows 8..15 are zeros, never
-// loaded). TG: groups of 16 tokens (rows 16 tg ..), each weight pair
-// converted once and multiplied with every group.
-template <int FMT, int EPI, int NP, bool BIG, int TG>
+// tile loop is unrolled without branches. BIG: more than 8 rows of A
+// (otherwise the MMA's rows 8..15 are zeros, never loaded). TG: groups of 16
+// tokens (rows 16 tg ..), each weight pair converted once and multiplied with
+// every group. PPS: pieces a stage. With 2, warp w takes block w % 8 of piece
+// w / 8 for every pair; with 1, block w % 8 of the piece for the pairs w / 8,
+// w / 8 + 2, ... (half of them: fewer accumulators, A loaded a group at a
+// time), and a tile's partial sums come from 8 positions instead of 16.
+template <int FMT, int EPI, int NP, bool BIG, int TG, int PPS>
 __global__ void __launch_bounds__(kSThreads, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                       const SmallParams p) {
@@ -228,21 +238,21 @@ __global__ void __launch_bounds__(kSThreads, 1)
   SmallBars& b = *reinterpret_cast<SmallBars*>(ring + p.ring_bytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = p.stages, npieces = p.K / kPieceK, nstages = (npieces + kPPS - 1) / kPPS;
+  const int S = p.stages, npieces = p.K / kPieceK, nstages = (npieces + PPS - 1) / PPS;
   const int r0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.N / gridDim.x);
   const int nrows = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.N / gridDim.x) - r0;
   const int T = (nrows + 7) / 8;  // 8-row tiles
 
-  // stage st (pieces kPPS st, kPPS st + 1) into ring slot `slot`: the
+  // stage st (pieces PPS st .. PPS st + PPS - 1) into ring slot `slot`: the
   // weights, then (once the previous kernel has completed) A; one barrier
   // counts both. Slot layout: A of piece 0, A of piece 1, W of piece 0, W of
   // piece 1.
   auto issue_w = [&](int st, int slot) {
-    const int np = min(kPPS, npieces - kPPS * st);
+    const int np = min(PPS, npieces - PPS * st);
     mbar_arrive_expect_tx(&b.full[slot], static_cast<unsigned>(np) * (p.w_bytes + static_cast<unsigned>(p.M) * kARowBytes));
     for (int sp = 0; sp < np; ++sp) {
-      const int piece = kPPS * st + sp;
-      uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes + kPPS * p.M * kARowBytes + sp * p.w_pitch;
+      const int piece = PPS * st + sp;
+      uint8_t* dst = ring + static_cast<size_t>(slot) * p.slot_bytes + PPS * p.M * kARowBytes + sp * p.w_pitch;
       if constexpr (FMT == LQ_FMT_F16) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -254,10 +264,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     b.last[slot] = st;
   };
   auto issue_a = [&](int st, int slot) {
-    const int np = min(kPPS, npieces - kPPS * st);
+    const int np = min(PPS, npieces - PPS * st);
     for (int sp = 0; sp < np; ++sp)
       tc::tma_load_2d(ring + static_cast<size_t>(slot) * p.slot_bytes + sp * p.M * kARowBytes, &tmA,
-                      kPieceK * (kPPS * st + sp), 0, &b.full[slot]);
+                      kPieceK * (PPS * st + sp), 0, &b.full[slot]);
   };
   const int first = min(S, nstages);
   if (threadIdx.x == 0) {
@@ -287,18 +297,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
   pdl_wait();  // (C and R)
 
   // ---- main loop: warp w takes block w % 8 of piece w / 8 of each stage,
-  // for every tile, two tiles at a time (independent chains of loads,
-  // conversions and MMAs); lane (g, q): W row 8t + wr, its 8 codes, and
-  // the A values of tokens g and g + 8 in the same order
-  const int bp = warp & 7, sp = warp >> 3, g = lane >> 2, q = lane & 3;
+  // for every tile, two tiles at a time (PPS 2; PPS 1: block w % 8 of the
+  // piece, pairs w / 8, w / 8 + 2, ...), each pair an independent chain of
+  // loads, conversions and MMAs; lane (g, q): W row 8t + wr, its 8 codes,
+  // and the A values of tokens 16 tg + g and 16 tg + g + 8 in the same order
+  const int bp = warp & 7, sp = PPS == 2 ? warp >> 3 : 0, half = warp >> 3, g = lane >> 2, q = lane & 3;
   // f16: MMA column g of a tile is W row wr = g / 2 + 4 (g % 2) of it, so
   // the two rows a quarter-warp reads sit in different halves of the boxes'
   // 128-byte swizzle (conflict-free 16-byte loads: f16 M=16 6144x2048 6.89
   // -> 6.66 us; the block formats keep column g = row g, measured 1 % ahead)
   const int wr = FMT == LQ_FMT_F16 ? (g >> 1) + 4 * (g & 1) : g;
-  float acc[2 * NP][TG][4];
+  constexpr int NPA = PPS == 2 ? NP : (NP + 1) / 2;  // pairs a warp
+  float acc[2 * NPA][TG][4];
 #pragma unroll
-  for (int i = 0; i < 2 * NP; ++i)
+  for (int i = 0; i < 2 * NPA; ++i)
 #pragma unroll
     for (int j = 0; j < 4 * TG; ++j) acc[i][j >> 2][j & 3] = 0.f;
   int s = 0;
@@ -313,36 +325,53 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       break;
     }
-    if (kPPS * st + sp < npieces) {
+    if (PPS * st + sp < npieces) {
       const uint32_t slot = smem_u32(ring) + static_cast<uint32_t>(s) * p.slot_bytes;
       const uint32_t sa = slot + static_cast<uint32_t>(sp * p.M) * kARowBytes;
-      const uint32_t wst = slot + static_cast<uint32_t>(kPPS * p.M) * kARowBytes + static_cast<uint32_t>(sp) * p.w_pitch;
-      uint32_t alo[TG][4], ahi[TG][4];
+      const uint32_t wst = slot + static_cast<uint32_t>(PPS * p.M) * kARowBytes + static_cast<uint32_t>(sp) * p.w_pitch;
+      uint32_t alo[PPS == 2 ? TG : 1][4], ahi[PPS == 2 ? TG : 1][4];
+      if constexpr (PPS == 2) {
 #pragma unroll
-      for (int tg = 0; tg < TG; ++tg) {
-        load_a<FMT, BIG>(sa, 16 * tg + g, p.M, bp, q, alo[tg]);
-        if constexpr (BIG)
-          load_a<FMT, BIG>(sa, 16 * tg + g + 8, p.M, bp, q, ahi[tg]);
-        else
-          ahi[tg][0] = ahi[tg][1] = ahi[tg][2] = ahi[tg][3] = 0u;
+        for (int tg = 0; tg < TG; ++tg) {
+          load_a<FMT, BIG>(sa, 16 * tg + g, p.M, bp, q, alo[tg]);
+          if constexpr (BIG)
+            load_a<FMT, BIG>(sa, 16 * tg + g + 8, p.M, bp, q, ahi[tg]);
+          else
+            ahi[tg][0] = ahi[tg][1] = ahi[tg][2] = ahi[tg][3] = 0u;
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 2 * NP; i += 2) {
-        // with an odd tile count the last pair repeats tile i into acc[i + 1];
-        // a CTA with fewer rows than the largest computes its pairs past T on
-        // bytes of the ring or its tail; neither is ever stored
-        const int t1 = min(i + 1, T - 1);
+      for (int m = 0; m < NPA; ++m) {
+        const int pr = PPS == 2 ? m : half + 2 * m;  // the pair
+        if (PPS == 1 && pr >= NP) break;
+        // with an odd tile count the last pair repeats its first tile into
+        // the second accumulator; a CTA with fewer rows than the largest
+        // computes its pairs past T on bytes of the ring or its tail;
+        // neither is ever stored
+        const int t0 = 2 * pr, t1 = min(t0 + 1, T - 1);
         uint32_t b0[4], b1[4];
-        load_weights<FMT, BIG>(wst, p.rows_box, 8 * i + wr, bp, q, b0);
+        load_weights<FMT, BIG>(wst, p.rows_box, 8 * t0 + wr, bp, q, b0);
         load_weights<FMT, BIG>(wst, p.rows_box, 8 * t1 + wr, bp, q, b1);
 #pragma unroll
         for (int tg = 0; tg < TG; ++tg) {
-          const uint32_t* al = alo[tg];
-          const uint32_t* ah = ahi[tg];
-          mma_bf16_16816(acc[i][tg], al[0], ah[0], al[1], ah[1], b0[0], b0[1]);  // the lane's values 0 .. 3
-          mma_bf16_16816(acc[i + 1][tg], al[0], ah[0], al[1], ah[1], b1[0], b1[1]);
-          mma_bf16_16816(acc[i][tg], al[2], ah[2], al[3], ah[3], b0[2], b0[3]);  // values 4 .. 7
-          mma_bf16_16816(acc[i + 1][tg], al[2], ah[2], al[3], ah[3], b1[2], b1[3]);
+          uint32_t al[4], ah[4];
+          if constexpr (PPS == 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              al[j] = alo[tg][j];
+              ah[j] = ahi[tg][j];
+            }
+          } else {
+            load_a<FMT, BIG>(sa, 16 * tg + g, p.M, bp, q, al);
+            if constexpr (BIG)
+              load_a<FMT, BIG>(sa, 16 * tg + g + 8, p.M, bp, q, ah);
+            else
+              ah[0] = ah[1] = ah[2] = ah[3] = 0u;
+          }
+          mma_bf16_16816(acc[2 * m][tg], al[0], ah[0], al[1], ah[1], b0[0], b0[1]);  // the lane's values 0 .. 3
+          mma_bf16_16816(acc[2 * m + 1][tg], al[0], ah[0], al[1], ah[1], b1[0], b1[1]);
+          mma_bf16_16816(acc[2 * m][tg], al[2], ah[2], al[3], ah[3], b0[2], b0[3]);  // values 4 .. 7
+          mma_bf16_16816(acc[2 * m + 1][tg], al[2], ah[2], al[3], ah[3], b1[2], b1[3]);
         }
       }
     }
@@ -374,31 +403,42 @@ __global__ void __launch_bounds__(kSThreads, 1)
     return;
   }
 
-  // ---- the 16 block positions' partial tiles, added in a fixed order
-  // (shared memory of the ring, every stage consumed): red[t][w][m][n],
-  // 16 TG tokens x 8 columns a tile
+  // ---- the block positions' partial tiles (16, or 8 with PPS 1), added in
+  // a fixed order (shared memory of the ring, every stage consumed):
+  // red[t][position][m][n], 16 TG tokens x 8 columns a tile
   constexpr int kTileF = 128 * TG;
+  constexpr int kNPos = 8 * PPS;
+  const int pos = PPS == 2 ? warp : bp;
   float* red = reinterpret_cast<float*>(ring);
 #pragma unroll
-  for (int t = 0; t < 2 * NP; ++t) {
-    if (t >= T) break;
-    float* tile = red + (t * kSWarps + warp) * kTileF;
+  for (int m = 0; m < NPA; ++m) {
+    const int pr = PPS == 2 ? m : half + 2 * m;
+    if (PPS == 1 && pr >= NP) break;
 #pragma unroll
-    for (int tg = 0; tg < TG; ++tg) {
-      *reinterpret_cast<float2*>(tile + (16 * tg + g) * 8 + 2 * q) = make_float2(acc[t][tg][0], acc[t][tg][1]);
-      *reinterpret_cast<float2*>(tile + (16 * tg + g + 8) * 8 + 2 * q) = make_float2(acc[t][tg][2], acc[t][tg][3]);
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int t = 2 * pr + h2;
+      if (t < T) {
+        float* tile = red + (t * kNPos + pos) * kTileF;
+        const int a = 2 * m + h2;
+#pragma unroll
+        for (int tg = 0; tg < TG; ++tg) {
+          *reinterpret_cast<float2*>(tile + (16 * tg + g) * 8 + 2 * q) = make_float2(acc[a][tg][0], acc[a][tg][1]);
+          *reinterpret_cast<float2*>(tile + (16 * tg + g + 8) * 8 + 2 * q) =
+              make_float2(acc[a][tg][2], acc[a][tg][3]);
+        }
+      }
     }
   }
   __syncthreads();
 #pragma unroll 1
   for (int idx = threadIdx.x; idx < T * kTileF; idx += kSThreads) {
-    const int t = idx / kTileF, e = idx - t * kTileF, m = e >> 3, c = e & 7;  // c: MMA column
+    const int t = idx / kTileF, e = idx - t * kTileF, mrow = e >> 3, c = e & 7;  // c: MMA column
     const int n = 8 * t + (FMT == LQ_FMT_F16 ? (c >> 1) + 4 * (c & 1) : c);
-    if (m < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
+    if (mrow < p.M && n < nrows && LQ_IN_BOUNDS(r0 + n < p.N)) {
       float sum = 0.f;
 #pragma unroll
-      for (int k = 0; k < kSWarps; ++k) sum += red[(t * kSWarps + k) * kTileF + e];
-      const long long o = static_cast<long long>(m) * p.N + r0 + n;
+      for (int k = 0; k < kNPos; ++k) sum += red[(t * kNPos + k) * kTileF + e];
+      const long long o = static_cast<long long>(mrow) * p.N + r0 + n;
       if constexpr (EPI == epi::kResidual)
         p.C[o] = sum + p.R[o];
       else
@@ -407,10 +447,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   }
 }
 
-template <int FMT, int EPI, int NP, bool BIG, int TG>
+template <int FMT, int EPI, int NP, bool BIG, int TG, int PPS>
 lq_status launch_small_k(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
                          int G, size_t smem) {
-  auto kern = gemm_small_kernel<FMT, EPI, NP, BIG, TG>;
+  auto kern = gemm_small_kernel<FMT, EPI, NP, BIG, TG, PPS>;
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return LQ_ERR_CUDA;
@@ -437,45 +477,57 @@ lq_status launch_small_k(const MatmulArgs& a, const CUtensorMap& tw, const CUten
 
 template <int FMT, int EPI, int NP>
 lq_status launch_small_t(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
-                         int G, size_t smem) {
-  if (p.M > kSTokens) {
-    // two token groups: the accumulators of up to 4 tile pairs fit the 128
-    // registers of 512 threads (the plan refuses more)
-    if constexpr (NP <= kSMaxPairs2) return launch_small_k<FMT, EPI, NP, true, 2>(a, tw, ta, p, G, smem);
+                         int G, size_t smem, int pps) {
+  const int tg = (p.M + kSTokens - 1) / kSTokens;
+  if (tg > 1) {
+    // two or three token groups: the accumulators of up to 4 tile pairs
+    // (3 with three groups; half of them a warp with single-piece stages)
+    // fit the 128 registers of 512 threads (the plan refuses more). Four
+    // groups spilled and lost to the tcgen05 kernel (Q8_0 6144x2048 M = 64
+    // 14.9 against 14.2 us); three on 64-row CTAs too (8192x2048 M = 33
+    // 14.7 against 14.2).
+    if constexpr (NP <= kSMaxPairs2) {
+      if (pps == 2) return tg == 2 ? launch_small_k<FMT, EPI, NP, true, 2, 2>(a, tw, ta, p, G, smem) : LQ_ERR_UNSUPPORTED;
+      if (tg == 2) return launch_small_k<FMT, EPI, NP, true, 2, 1>(a, tw, ta, p, G, smem);
+      if constexpr (NP <= kSMaxPairs3)
+        if (tg == 3) return launch_small_k<FMT, EPI, NP, true, 3, 1>(a, tw, ta, p, G, smem);
+      return LQ_ERR_UNSUPPORTED;
+    }
     return LQ_ERR_UNSUPPORTED;
   }
-  return p.M > 8 ? launch_small_k<FMT, EPI, NP, true, 1>(a, tw, ta, p, G, smem)
-                 : launch_small_k<FMT, EPI, NP, false, 1>(a, tw, ta, p, G, smem);
+  if (pps != 2) return LQ_ERR_UNSUPPORTED;
+  return p.M > 8 ? launch_small_k<FMT, EPI, NP, true, 1, 2>(a, tw, ta, p, G, smem)
+                 : launch_small_k<FMT, EPI, NP, false, 1, 2>(a, tw, ta, p, G, smem);
 }
 
 // the kernel for the CTAs' tile count: the largest CTA holds ceil(N / G)
 // rows, ceil(rows / 8) tiles, NP = ceil(tiles / 2) pairs
 template <int FMT, int EPI>
 lq_status launch_small_np(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
-                          int G, size_t smem) {
+                          int G, size_t smem, int pps) {
   const int rows = static_cast<int>((static_cast<long long>(p.N) + G - 1) / G);
   switch ((rows + 15) / 16) {
-    case 1: return launch_small_t<FMT, EPI, 1>(a, tw, ta, p, G, smem);
-    case 2: return launch_small_t<FMT, EPI, 2>(a, tw, ta, p, G, smem);
-    case 3: return launch_small_t<FMT, EPI, 3>(a, tw, ta, p, G, smem);
-    case 4: return launch_small_t<FMT, EPI, 4>(a, tw, ta, p, G, smem);
-    case 5: return launch_small_t<FMT, EPI, 5>(a, tw, ta, p, G, smem);
-    case 6: return launch_small_t<FMT, EPI, 6>(a, tw, ta, p, G, smem);
-    case 7: return launch_small_t<FMT, EPI, 7>(a, tw, ta, p, G, smem);
-    case 8: return launch_small_t<FMT, EPI, 8>(a, tw, ta, p, G, smem);
+    case 1: return launch_small_t<FMT, EPI, 1>(a, tw, ta, p, G, smem, pps);
+    case 2: return launch_small_t<FMT, EPI, 2>(a, tw, ta, p, G, smem, pps);
+    case 3: return launch_small_t<FMT, EPI, 3>(a, tw, ta, p, G, smem, pps);
+    case 4: return launch_small_t<FMT, EPI, 4>(a, tw, ta, p, G, smem, pps);
+    case 5: return launch_small_t<FMT, EPI, 5>(a, tw, ta, p, G, smem, pps);
+    case 6: return launch_small_t<FMT, EPI, 6>(a, tw, ta, p, G, smem, pps);
+    case 7: return launch_small_t<FMT, EPI, 7>(a, tw, ta, p, G, smem, pps);
+    case 8: return launch_small_t<FMT, EPI, 8>(a, tw, ta, p, G, smem, pps);
     default: return LQ_ERR_UNSUPPORTED;
   }
 }
 
 template <int FMT>
 lq_status launch_small_fmt(const MatmulArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, const SmallParams& p,
-                           int G, size_t smem) {
-  if (a.epi == epi::kResidual) return launch_small_np<FMT, epi::kResidual>(a, tw, ta, p, G, smem);
-  return launch_small_np<FMT, epi::kPlain>(a, tw, ta, p, G, smem);
+                           int G, size_t smem, int pps) {
+  if (a.epi == epi::kResidual) return launch_small_np<FMT, epi::kResidual>(a, tw, ta, p, G, smem, pps);
+  return launch_small_np<FMT, epi::kPlain>(a, tw, ta, p, G, smem, pps);
 }
 
 struct SmallPlan {
-  int G = 0, rows_box = 0, stages = 0;
+  int G = 0, rows_box = 0, stages = 0, pps = 0;
   unsigned w_bytes = 0, w_pitch = 0, slot_bytes = 0, ring_bytes = 0;
   size_t smem = 0;
 };
@@ -494,6 +546,7 @@ bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   if (rows > 8 * kSMaxTiles) return false;
   const int tg = (a.M + kSTokens - 1) / kSTokens;
   if (tg > 1 && rows > 16 * kSMaxPairs2) return false;
+  if (tg > 2 && rows > 16 * kSMaxPairs3) return false;
   pl.G = static_cast<int>(G);
   // the box covers the CTA's rows (f16: whole 8-row groups, for the
   // swizzled boxes' 1024-byte alignment); a tile's rows past the box read
@@ -501,16 +554,32 @@ bool plan_small(const MatmulArgs& a, SmallPlan& pl) {
   pl.rows_box = static_cast<int>(a.fmt == LQ_FMT_F16 ? (rows + 7) / 8 * 8 : rows);
   pl.w_bytes = static_cast<unsigned>(pl.rows_box * piece_row_bytes(a.fmt));  // f16: a multiple of 4096
   pl.w_pitch = (pl.w_bytes + 127u) / 128u * 128u;
-  // (A's M KB a piece keeps the weights 1024-aligned, as f16's swizzled boxes need)
-  pl.slot_bytes = (kPPS * (static_cast<unsigned>(a.M) * kARowBytes + pl.w_pitch) + 1023u) / 1024u * 1024u;
   const long long budget = std::min(di.max_smem_optin, 227 * 1024) - 1024 - kSBarsBytes;
-  const int nstages = static_cast<int>((a.K / kPieceK + kPPS - 1) / kPPS);
-  const long long red = static_cast<long long>((rows + 7) / 8) * kSWarps * 128 * tg * 4;  // partial tiles
   // the last tile's rows past the box read up to 7 rows beyond the last slot
   const long long tail = 7LL * piece_row_bytes(a.fmt);
-  const int S = static_cast<int>(std::min<long long>({kSMaxStages, nstages, (budget - tail) / pl.slot_bytes}));
-  if (S < std::min(2, nstages)) return false;  // a ring of one slot would not overlap copies and MMAs
+  // two pieces a stage where they fit twice (one or two token groups), else
+  // one (two or three token groups); a ring of one slot would not overlap
+  // copies and MMAs
+  int S = 0, pps = 0, nstages = 0;
+  for (const int cand : {2, 1}) {
+    if ((cand == 2 && tg > 2) || (cand == 1 && tg < 2)) continue;  // (one group: two pieces or nothing)
+    // (A's M KB a piece keeps the weights 1024-aligned, as f16's swizzled boxes need)
+    const unsigned slot = (cand * (static_cast<unsigned>(a.M) * kARowBytes + pl.w_pitch) + 1023u) / 1024u * 1024u;
+    const int ns = static_cast<int>((a.K / kPieceK + cand - 1) / cand);
+    const int s = static_cast<int>(std::min<long long>({kSMaxStages, ns, (budget - tail) / slot}));
+    if (s >= std::min(2, ns)) {
+      S = s;
+      pps = cand;
+      nstages = ns;
+      pl.slot_bytes = slot;
+      break;
+    }
+  }
+  if (!pps) return false;
+  (void)nstages;
+  const long long red = static_cast<long long>((rows + 7) / 8) * (8 * pps) * 128 * tg * 4;  // partial tiles
   pl.stages = S;
+  pl.pps = pps;
   pl.ring_bytes = static_cast<unsigned>(std::max<long long>(static_cast<long long>(S) * pl.slot_bytes + tail, red));
   pl.ring_bytes = (pl.ring_bytes + 127u) / 128u * 128u;
   if (static_cast<long long>(pl.ring_bytes) > budget) return false;
@@ -591,11 +660,11 @@ lq_status launch_gemm_small(const MatmulArgs& a) {
   p.wait_iters = wait_limit_iters();
   lq_status st;
   if (a.fmt == LQ_FMT_F16)
-    st = launch_small_fmt<LQ_FMT_F16>(a, tw, ta, p, pl.G, pl.smem);
+    st = launch_small_fmt<LQ_FMT_F16>(a, tw, ta, p, pl.G, pl.smem, pl.pps);
   else if (a.fmt == LQ_FMT_Q8_0)
-    st = launch_small_fmt<LQ_FMT_Q8_0>(a, tw, ta, p, pl.G, pl.smem);
+    st = launch_small_fmt<LQ_FMT_Q8_0>(a, tw, ta, p, pl.G, pl.smem, pl.pps);
   else
-    st = launch_small_fmt<LQ_FMT_Q4_0>(a, tw, ta, p, pl.G, pl.smem);
+    st = launch_small_fmt<LQ_FMT_Q4_0>(a, tw, ta, p, pl.G, pl.smem, pl.pps);
   if (st == LQ_OK) count_route(5);
   return st;
 }

@@ -73,7 +73,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* ws);
 bool gemm_tma_eligible(const MatmulArgs& a);
 // cuTensorMapEncodeTiled from the driver (null when unavailable)
 void* tma_encode_tiled();
-// tensor cores with warp-level MMAs for M = 2..32 (W streamed once, every
+// tensor cores with warp-level MMAs for M = 2..48 (W streamed once, every
 // operand in registers); LQ_ERR_UNSUPPORTED outside its shapes
 lq_status launch_gemm_small(const MatmulArgs& a);
 bool gemm_small_eligible(const MatmulArgs& a);

@@ -43,7 +43,7 @@
  *     by pointer offsets; a W row offset is always block-aligned.
  *   - Memory: the library allocates nothing per call and holds no workspace,
  *     with one exception: the tcgen05 route of the GEMM entry points
- *     (lq_gemm_<fmt>, lq_matmul_<fmt> and the epilogue fusions; M > 32, or
+ *     (lq_gemm_<fmt>, lq_matmul_<fmt> and the epilogue fusions; M > 48, or
  *     shapes the warp-MMA kernel does not take), when a CTA's token tile is
  *     too large to stay in its shared memory, takes an M*K*2-byte
  *     stream-ordered buffer from a memory pool the library owns (described
@@ -103,10 +103,10 @@ lq_status lq_gemv_q4_0(const float* A, const void* W, float* C,
  * in f32 (GEMV accuracy); everything else runs on the tensor cores
  * with bf16 operands: A rounded to bf16 (round to nearest even, over f32's
  * whole range), each weight formed exactly in f32 and rounded once to bf16
- * (any finite block scale), products accumulated in f32 -- up to 32 rows
+ * (any finite block scale), products accumulated in f32 -- up to 48 rows
  * with warp-level MMAs on W streamed once (K a multiple of 256; up to 128
- * W rows per SM, 64 beyond 16 rows of A, and stages that fit twice in
- * shared memory), beyond with tcgen05 MMAs and TMEM accumulators. Tolerance: 5e-3 times
+ * W rows per SM, 64 beyond 16 rows of A, 48 beyond 32, and stages that fit
+ * twice in shared memory), beyond with tcgen05 MMAs and TMEM accumulators. Tolerance: 5e-3 times
  * sum_k |a_k w_k| plus 1e-5, against A rounded to bf16 (the weights'
  * rounding contributes at most 2^-8 of the sum).
  * Workspace: the tcgen05 route converts A once per call into a
@@ -321,7 +321,7 @@ const char* lq_version(void);
  * force_q4_gemm_fallback_for_test and its fallback dispatch counter) ------
  * route: 0 = automatic, 1 = CUDA-core streaming GEMM (any M),
  *        2 = tensor-core GEMM (tcgen05), 3 = generic fallback kernels (any
- *        shape), 5 = tensor-core GEMM with warp-level MMAs for M = 2..32
+ *        shape), 5 = tensor-core GEMM with warp-level MMAs for M = 2..48
  *        (LQ_ERR_UNSUPPORTED outside its shapes).
  * lq_debug_route_count(r) counts launches taken by route r (r = 0 counts
  * the fast GEMV, r = 4 the decode chain, r = 6 the A pre-pass launches of

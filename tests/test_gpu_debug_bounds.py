@@ -39,7 +39,7 @@ for fmt in ("f16", "q8_0", "q4_0", "q4_0i"):
                              (2, 519, 256, 0), (3, 1003, 1024, 0), (5, 777, 512, 0), (8, 130, 2048, 0),
                              (16, 200, 512, 0), (37, 129, 768, 0), (300, 515, 256, 0), (6, 77, 96, 0),
                              (24, 192, 320, 2), (7, 100, 160, 1), (9, 300, 512, 3), (6, 300, 512, 1),
-                             (3, 257, 2048, 1), (11, 1000, 768, 5), (2, 19, 256, 5)]:
+                             (3, 257, 2048, 1), (11, 1000, 768, 5), (2, 19, 256, 5), (40, 300, 512, 5)]:
         if fmt == "f16" or K % 32 == 0:
             W, A = synthetic.draw(M, N, K, seed=M + N + K, outlier_frac=0.05 if K % 32 == 0 else 0.0)
             Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)

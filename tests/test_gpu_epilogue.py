@@ -62,6 +62,7 @@ CASES = [  # (M, rows, K, route, tensor-core tolerance)
     (6, 1000, 2048, ROUTE_TC, True),       # ... where the router picks the tensor cores
     (16, 1000, 2048, ROUTE_TC, True),
     (24, 1000, 2048, ROUTE_TC, True),
+    (40, 1000, 2048, ROUTE_TC, True),
     (64, 1000, 2048, ROUTE_TC, True),
     (300, 777, 1024, ROUTE_TC, True),
 ]
@@ -99,15 +100,16 @@ def test_residual_routes(lq, cuda_dev, fmt, M, N, K, route, tc):
         W, A, R, C = _residual(lq, cuda_dev, fmt, M, N, K, seed=M + N + K)
     finally:
         lq.force_route(0)
-    # up to 32 rows the tensor cores are reached by warp-level MMAs (swiglu:
+    # up to 48 rows the tensor cores are reached by warp-level MMAs (swiglu:
     # by the tcgen05 kernel)
-    assert lq.route_count(ROUTE_WARP if route == ROUTE_TC and M <= 32 else route) == 1
+    assert lq.route_count(ROUTE_WARP if route == ROUTE_TC and M <= 48 else route) == 1
     y, tol = _ref(fmt, A, W, tc)
     c, tc_ = O.residual_reference(y, tol, R)
     check(C, c, tc_, f"residual {fmt} M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (2, ROUTE_WARP, True), (40, ROUTE_TC, True)])
+@pytest.mark.parametrize("M,route,tc", [(1, ROUTE_GEMV, False), (2, ROUTE_WARP, True), (40, ROUTE_WARP, True),
+                                        (56, ROUTE_TC, True)])
 def test_residual_in_place(lq, cuda_dev, M, route, tc):
     """R and C the same buffer: the residual stream updated in place."""
     fmt, N, K = "q8_0", 3000, 2048

@@ -47,7 +47,7 @@ def test_tc_single_tile_single_kstep(lq, cuda_dev, fmt):
 def test_tc_shapes(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=M + N + K, outlier_frac=0.05)
     lq.reset_counts()
-    lq.force_route(lq.ROUTE_TENSOR_CORE)  # M <= 32 would take the warp-MMA or batched kernel
+    lq.force_route(lq.ROUTE_TENSOR_CORE)  # M <= 48 would take the warp-MMA or batched kernel
     try:
         C = _run(lq, cuda_dev, fmt, W, A)
     finally:
@@ -162,13 +162,16 @@ def test_tc_wide_range_token_rows(lq, cuda_dev, fmt):
 @pytest.mark.parametrize("fmt,d", [("q8_0", 4.0), ("q8_0", 300.0), ("q8_0", 60000.0),
                                    ("q4_0", 40.0), ("q4_0", 4000.0), ("q4_0", 60000.0),
                                    ("q4_0i", 40.0), ("f16", 60000.0 / 127)])
-def test_tc_large_block_scales(lq, cuda_dev, fmt, d):
+@pytest.mark.parametrize("M,route", [(48, 5), (64, 2)])
+def test_tc_large_block_scales(lq, cuda_dev, fmt, d, M, route):
     """Blocks whose f16 scale d is large (Q8_0 weights up to 127 d, Q4_0 up to
     8 d; f16 weights near f16's largest value): the dequantised weights are
     formed exactly and rounded to bf16, so any finite block scale stays within
     the tolerance. Here a tenth of the blocks, spread over the tiles, carry
-    the large scale; the rest are the workloads' N(0, 0.02)."""
-    M, N, K = 48, 384, 1024
+    the large scale; the rest are the workloads' N(0, 0.02). Both tensor-core
+    routes: 48 rows take the warp MMAs (Q4_0I, which reorders A, the tcgen05
+    GEMM), 64 the tcgen05 GEMM."""
+    N, K = 384, 1024
     W, A = synthetic.draw(M, N, K, seed=21)
     W = W.clone()
     g = torch.Generator().manual_seed(5)
@@ -180,7 +183,7 @@ def test_tc_large_block_scales(lq, cuda_dev, fmt, d):
     Wb[pick] = Wb[pick] / amax * peak
     lq.reset_counts()
     C = _run(lq, cuda_dev, fmt, W, A)
-    assert lq.route_count(2) == 1
+    assert lq.route_count(2 if fmt == "q4_0i" else route) == 1
     y, tol = _ref(fmt, W, A)
     check(C, y, tol, f"{fmt} d={d}")
 

@@ -1,12 +1,13 @@
-"""The warp-MMA tensor-core GEMM for M = 2..32 (route 5) against the oracle.
+"""The warp-MMA tensor-core GEMM for M = 2..48 (route 5) against the oracle.
 
 W is streamed once as stages of 256 K; each lane dequantises 8 weights of a
 row exactly and rounds them to bf16, A is rounded to bf16, mma.m16n8k16
 accumulates in f32: the tensor-core tolerance (5e-3 * sum|a*w| + 1e-5)
 applies. Shapes: ragged row counts per CTA (N not a multiple of 8 or of the
 SM count), a single stage (K = 256), more stages than ring slots (K = 4096),
-one to sixteen tokens (padding rows of the 16-token MMA), 17 to 32 tokens
-(two token groups sharing each converted weight, CTAs of up to 64 W rows), the router's
+one to sixteen tokens (padding rows of the 16-token MMA), 17 to 48 tokens
+(two or three token groups sharing each converted weight, CTAs of up to 64 or
+48 W rows; single-piece stages where two pieces would not fit twice), the router's
 choice, the residual epilogue (in place too), and the shapes the kernel
 refuses. Output buffers start as NaN.
 """
@@ -48,7 +49,8 @@ def _ref(fmt, W, A):
 @pytest.mark.parametrize("M,N,K", [(2, 1, 256), (5, 7, 256), (8, 300, 512), (9, 1000, 2048), (16, 6144, 2048),
                                    (16, 777, 4096), (3, 4097, 1024), (12, 19000, 256), (16, 153, 768),
                                    (7, 300, 16384), (17, 6144, 2048), (24, 1000, 768), (32, 4096, 4096),
-                                   (31, 9727, 512), (20, 5, 256)])
+                                   (31, 9727, 512), (20, 5, 256), (33, 6144, 2048), (48, 1000, 768),
+                                   (48, 4096, 4096), (40, 7296, 512), (40, 300, 4096), (28, 6144, 2048)])
 def test_warp_mma_gemm_matches_oracle(lq, cuda_dev, fmt, M, N, K):
     W, A = synthetic.draw(M, N, K, seed=M * 31 + N + K, outlier_frac=0.05)
     C = _run(lq, cuda_dev, fmt, W, A)
@@ -57,8 +59,8 @@ def test_warp_mma_gemm_matches_oracle(lq, cuda_dev, fmt, M, N, K):
 
 
 @pytest.mark.parametrize("fmt", ["f16", "q8_0", "q4_0"])
-@pytest.mark.parametrize("M", [2, 3, 8, 16, 17, 24])
-def test_router_sends_two_to_thirty_two_rows_to_warp_mmas(lq, cuda_dev, fmt, M):
+@pytest.mark.parametrize("M", [2, 3, 8, 16, 17, 24, 40])
+def test_router_sends_two_to_forty_eight_rows_to_warp_mmas(lq, cuda_dev, fmt, M):
     # (f16 at 6144 x 2048 with more than 24 rows needs stages larger than
     # half the shared memory, so the plan refuses and the tcgen05 kernel
     # takes it)
@@ -109,7 +111,8 @@ def test_warp_mma_residual(lq, cuda_dev, fmt, in_place, M):
     check(C.cpu().numpy(), c, t, f"residual {fmt} in_place={in_place}")
 
 
-@pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 33, 512, 512),   # more than 32 rows
+@pytest.mark.parametrize("fmt,M,N,K", [("q8_0", 49, 512, 512),   # more than 48 rows
+                                       ("q8_0", 33, 7297, 512),  # three token groups, more than 48 rows per SM
                                        ("q8_0", 17, 9729, 512),  # two token groups, more than 64 rows per SM
                                        ("q8_0", 8, 512, 320),    # K not a multiple of 256
                                        ("q4_0i", 8, 512, 512),   # interleaved nibbles

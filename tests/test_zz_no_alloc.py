@@ -36,7 +36,7 @@ def test_noalloc_matches_oracle_and_regular_gemm_on_two_calls_in_a_row(lq, cuda_
     # tiles whose A slice is larger than shared memory); the second is
     # smaller, so leftovers of the first would show if they were read. Then
     # two small problems whose A the GEMM keeps in shared memory itself.
-    cases = [(250, 1024, 4096, 20), (128, 4096, 4096, 23), (96, 384, 1024, 21), (40, 200, 512, 22)]
+    cases = [(250, 1024, 4096, 20), (128, 4096, 4096, 23), (96, 384, 1024, 21), (56, 200, 512, 22)]
     lq.force_route(0)
     for M, N, K, seed in cases:
         W, A = synthetic.draw(M, N, K, seed=seed, outlier_frac=0.05)
