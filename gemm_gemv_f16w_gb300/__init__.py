@@ -38,6 +38,7 @@ EXPORTS = [
     "lq_status_string", "lq_last_device_error", "lq_version",
     "lq_debug_force_route", "lq_debug_route_count", "lq_debug_reset_counts",
     "lq_debug_set_wait_limit_ns", "lq_gemm_noalloc", "lq_debug_gemv_plan", "lq_gemv_chain", "lq_debug_gemm_rings",
+    "lq_debug_gemm_pairs",
     "lq_gemv_argmax", "lq_argmax_f32", "lq_matmul_residual", "lq_matmul_swiglu",
     "lq_gemv_q4_0i", "lq_gemm_q4_0i", "lq_matmul_q4_0i", "lq_pack_q4_0i", "lq_pack_q8_0_rcp",
     "lq_topk_work_bytes", "lq_topk_f32", "lq_gemv_topk", "lq_debug_chain_waits",
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.lq_gemv_chain.restype = st
         L.lq_debug_gemm_rings.argtypes = [ctypes.c_int, ctypes.c_int]
         L.lq_debug_gemm_rings.restype = st
+        L.lq_debug_gemm_pairs.argtypes = [ctypes.c_int]
+        L.lq_debug_gemm_pairs.restype = None
         L.lq_debug_chain_waits.argtypes = [ctypes.c_int]
         L.lq_debug_chain_waits.restype = None
         L.lq_debug_gemv_plan.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
@@ -356,6 +359,12 @@ def chain_waits(on: bool) -> None:
     """Dependent problems of lq_gemv_chain wait inside one launch (True) or
     start a new launch (False, the default); for comparisons."""
     lib().lq_debug_chain_waits(1 if on else 0)
+
+
+def gemm_pairs(on: bool) -> None:
+    """Let the tensor-core GEMM pair CTAs on 256-row MMAs where they fit
+    (True) or never (False, the default); for comparisons."""
+    lib().lq_debug_gemm_pairs(1 if on else 0)
 
 
 def gemm_rings(a_stages: int = 0, raw_stages: int = 0) -> None:

@@ -17,7 +17,7 @@ namespace lq {
 
 namespace {
 std::atomic<int> g_force_route{0};
-std::atomic<uint64_t> g_route_count[7];
+std::atomic<uint64_t> g_route_count[8];
 std::atomic<unsigned long long> g_wait_ns{0};
 std::mutex g_info_mu;
 DeviceInfo g_info[kMaxDevices];
@@ -60,7 +60,7 @@ unsigned wait_limit_iters() {
 }
 
 void count_route(int route) {
-  if (route >= 0 && route < 7) g_route_count[route].fetch_add(1);
+  if (route >= 0 && route < 8) g_route_count[route].fetch_add(1);
 }
 
 namespace {
@@ -365,7 +365,7 @@ lq_status lq_debug_force_route(int route) {
   return LQ_OK;
 }
 uint64_t lq_debug_route_count(int route) {
-  if (route < 0 || route > 6) return 0;
+  if (route < 0 || route > 7) return 0;
   return g_route_count[route].load();
 }
 void lq_debug_reset_counts(void) {
@@ -378,6 +378,7 @@ lq_status lq_debug_gemm_rings(int a_stages, int raw_stages) {
   return LQ_OK;
 }
 void lq_debug_chain_waits(int on) { lq::set_chain_waits(on != 0); }
+void lq_debug_gemm_pairs(int on) { lq::set_gemm_pairs(on != 0); }
 lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes) {
   if (ctas_per_sm < 0 || ctas_per_sm > 2 || rows_per_stage < 0 || rows_per_stage > 8 ||
       smem_bytes < 0)

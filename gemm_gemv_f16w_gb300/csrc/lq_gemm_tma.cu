@@ -56,6 +56,8 @@ constexpr int kGroups = kNumConv / 4;              // a group's 4 warps cover th
 constexpr int kConvThreads = kNumConv * 32;
 constexpr int kRawWarp = 2 + kNumConv;             // raw W refills
 constexpr int kTmaThreads = (3 + kNumConv) * 32;   // producer, MMA, converters, raw W
+constexpr int kGateWarp = 3 + kNumConv;            // CTA pairs: the stage relay (rank 1) / gate (rank 0)
+constexpr int kPairThreads = kTmaThreads + 32;
 constexpr int kBN = 128;                           // W rows per CTA
 constexpr int kKS = 128;                           // K per pipeline stage (8 MMAs of K=16)
 constexpr int kMaxStages = 4, kMaxRawStages = 8;  // A ring (streamed A), raw W ring
@@ -88,6 +90,7 @@ struct TmaGemmParams {
 struct Bars {
   uint64_t raw_full[kMaxRawStages], raw_empty[kMaxRawStages];
   uint64_t full[kMaxSlots];    // A tile landed (TMA bytes) + the group's 4 converter warps wrote W
+  uint64_t pfull[kMaxSlots];   // CTA pairs, rank 0: rank 1's half of the stage is ready (its relay warp)
   uint64_t empty[kMaxSlots];   // the stage's MMAs completed (commit)
   uint64_t tmem_full;
   uint64_t a_ready;            // resident A: the converter warps stored every stage's A tile
@@ -248,6 +251,53 @@ __device__ __forceinline__ void convert_step(uint32_t stage, uint32_t r, uint32_
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local_addr, uint32_t peer) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
+  return remote;
+}
+// Arrive on a barrier of another CTA of the cluster (address from peer_addr),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+// Polls of a barrier that another CTA arrives on (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_test_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait as mbar_wait with acquire at cluster scope, by all 32 lanes,
+// with one outcome for the warp.
+__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity, const TmaGemmParams& p) {
+  bool ok = false;
+  if (p.wait_iters < 1024u) {
+    for (uint32_t it = 0; it < p.wait_iters && !ok; ++it) ok = mbar_test_wait_cl(bar, parity);
+  } else {
+    ok = mbar_try_wait_cl(bar, parity);
+    const long long t0 = clock64(), limit = static_cast<long long>(p.wait_ns) * 4;
+    for (uint32_t it = 1; !ok && it < p.wait_iters; ++it) {
+      ok = mbar_try_wait_cl(bar, parity);
+      if (!ok && (it & 15u) == 15u && clock64() - t0 > limit) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
 __device__ __forceinline__ float ld_peer_f32(uint32_t local_addr, uint32_t peer) {
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(peer));
@@ -387,19 +437,39 @@ __device__ __forceinline__ void load_resident_a(const TmaGemmParams& p, uint8_t*
 // put the scaled accumulators into the idle A ring and then combine gate and
 // up pairs in one short loop (a fully unrolled combine made the kernel's
 // code large enough to stall on instruction fetch). No K split with kSwiglu.
-template <int FMT, int EPI>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+//
+// PAIR (opt-in, lq_debug_gemm_pairs): the two CTAs of a cluster of two (W
+// row tiles 2i and 2i + 1, the same tokens) run as one CTA pair. Each loads
+// half of the token tile (bt / 2 rows) and converts its own 128 W rows into
+// its own tensor memory; rank 0's MMA thread issues M = 256 MMAs over both
+// (cta_group::2), so each SM pulls half the token bytes per MMA FLOP. A warp
+// of its own (kGateWarp) carries each stage's readiness across: in rank 1 it
+// waits for its own full barrier and arrives on rank 0's pfull (release at
+// cluster scope); in rank 0 it waits for pfull (acquire at cluster scope)
+// and arrives on rank 0's full, which then counts six arrivals, so that the
+// MMA thread only waits at CTA scope. Rank 0's commits arrive on both CTAs'
+// barriers. No K split, streamed A only. Slower than single CTAs on every
+// shape measured (Q8_0 512 x 6144 x 2048: 23.2 against 17.6 us): in a
+// %globaltimer timeline the half tiles land no sooner than whole ones
+// (about 1.4 us after issue), the hop from rank 1 to rank 0 adds about
+// 0.8 us to every stage and the setup's cluster barrier about 2.5 us, while
+// the pair's MMAs alone run at the single CTAs' rate.
+template <int FMT, int EPI, bool PAIR = false>
+__global__ void __launch_bounds__(PAIR ? kPairThreads : kTmaThreads, 1)
     gemm_tma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
                     const TmaGemmParams p) {
   constexpr int SUB = kSub<FMT>;
   constexpr bool SWIGLU = EPI == epi::kSwiglu;
+  static_assert(!(PAIR && SWIGLU), "no CTA pairs with the SwiGLU epilogue");
   constexpr int kRawBytes = kRowBytes<FMT> * kBN;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u = smem_u32(smem_raw);
   const uint32_t base_u = (raw_u + 1023u) & ~1023u;
   uint8_t* base = smem_raw + (base_u - raw_u);
   const int bt = p.bt, S = p.stages;
-  const uint32_t atom_bytes = static_cast<uint32_t>(bt) * 128u;   // 64 K of the A tile
+  const int prank = PAIR ? static_cast<int>(blockIdx.x & 1u) : 0;  // rank in the CTA pair
+  const int bta = PAIR ? bt / 2 : bt;                               // token rows of this CTA's A tiles
+  const uint32_t atom_bytes = static_cast<uint32_t>(bta) * 128u;  // 64 K of the A tile
   const uint32_t a_stage_bytes = 2u * atom_bytes;                  // 128 K
   uint8_t* a_ring = base;                                          // S x A tiles (swizzled)
   const int RR = p.raw_stages;
@@ -450,8 +520,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       mbar_init(&b.raw_empty[i], 4 * SUB);
     }
     for (int i = 0; i < S; ++i) {
-      mbar_init(&b.full[i], 1 + 4);
+      mbar_init(&b.full[i], 1 + 4 + (PAIR && prank == 0 ? 1 : 0));
       mbar_init(&b.empty[i], 1);
+      mbar_init(&b.pfull[i], 1);
     }
     mbar_init(&b.tmem_full, 1);
     mbar_init(&b.a_ready, 1);
@@ -463,11 +534,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
   }
   if (warp == 1) {
-    tc::tmem_alloc(&b.tmem_base, kTmemCols);
-    tc::tmem_relinquish();
+    if constexpr (PAIR) {
+      tc::tmem_alloc_pair(&b.tmem_base, kTmemCols);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(&b.tmem_base, kTmemCols);
+      tc::tmem_relinquish();
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // both CTAs' barriers exist before any remote arrive or commit
   tc::fence_after_sync();
   const uint32_t tmem = b.tmem_base;
   pdl_launch_dependents();
@@ -501,9 +578,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         if (lane == 0) mbar_arrive(&b.full[st]);
       } else if (lane == 0) {
+        const int ma = m0 + prank * bta;  // CTA pairs: this CTA's half of the token tile
         mbar_arrive_expect_tx(&b.full[st], a_stage_bytes);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), m0, &b.full[st]);
-        tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, m0,
+        tc::tma_load_2d(a_ring + st * a_stage_bytes, &tmA, kKS * (ks0 + ks), ma, &b.full[st]);
+        tc::tma_load_2d(a_ring + st * a_stage_bytes + atom_bytes, &tmA, kKS * (ks0 + ks) + 64, ma,
                         &b.full[st]);
       }
       __syncwarp();
@@ -518,9 +596,43 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     if (!p.a_res)
       for (int ks = max(0, issued - S); ks < issued; ++ks)
         mbar_wait(&b.full[ks % S], (ks / S) & 1, kDrainWaitNs);
+  } else if (PAIR && warp == kGateWarp) {
+    // ---------------- CTA pair: stage readiness across the pair ----------------
+    // rank 1: full[st] (its A half landed, its converters wrote its W rows)
+    // -> one arrival on rank 0's pfull[st]; rank 0: pfull[st] -> one
+    // arrival on its own full[st]. Phases advance in order: rank 1's next
+    // phase of full[st] needs the commit of this one's MMAs, which rank 0
+    // issues only after its full[st] completed.
+    bool ok = true;
+    int st = 0, lap = 0;
+    const uint32_t pfull0 = peer_addr(smem_u32(&b.pfull[0]), 0u);
+    for (int ks = 0; ks < nk; ++ks) {
+      if (prank == 1 ? !warp_wait(&b.full[st], lap & 1, p) : !warp_wait_cl(&b.pfull[st], lap & 1, p)) {
+        ok = false;
+        break;
+      }
+      if (b.abort) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        if (prank == 1)
+          mbar_arrive_remote(pfull0 + 8u * static_cast<uint32_t>(st));
+        else
+          mbar_arrive(&b.full[st]);
+      }
+      __syncwarp();
+      if (++st == S) { st = 0; ++lap; }
+    }
+    if (!ok && lane == 0) {
+      record_error(kDevErrTimeout);
+      b.abort = 1;
+    }
+  } else if (warp == 1 && PAIR && prank == 1) {
+    // rank 1 issues no MMAs
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    const uint32_t idesc = tc::idesc_bf16_f32(kBN, static_cast<uint32_t>(bt));
+    const uint32_t idesc = tc::idesc_bf16_f32(PAIR ? 2 * kBN : kBN, static_cast<uint32_t>(bt));
     bool ok = true;
     int st = 0, lap = 0;
     auto issue_stage = [&](int ks, int sst) {
@@ -529,9 +641,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint64_t bdesc = tc::desc_sw128_kmajor(abase + (kk >> 2) * atom_bytes) + 2u * (kk & 3);
-        tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        if constexpr (PAIR)
+          tc::mma_f16_ts_pair(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        else
+          tc::mma_f16_ts(tmem, wcol + 8u * kk, bdesc, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
       }
-      tc::commit(&b.empty[sst]);
+      if constexpr (PAIR)
+        tc::commit_pair(&b.empty[sst], 0x3);
+      else
+        tc::commit(&b.empty[sst]);
     };
     for (int ks = 0; ks < nk;) {
       if (!warp_wait(&b.full[st], lap & 1, p)) {
@@ -563,7 +681,12 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
       record_error(kDevErrTimeout);
       b.abort = 1;
     }
-    if (lane == 0) tc::commit(&b.tmem_full);
+    if (lane == 0) {
+      if constexpr (PAIR)
+        tc::commit_pair(&b.tmem_full, 0x3);
+      else
+        tc::commit(&b.tmem_full);
+    }
     __syncwarp();
     if (b.abort) mbar_wait(&b.tmem_full, 0, kDrainWaitNs);
   } else if (warp == kRawWarp) {
@@ -726,9 +849,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     cluster_sync();  // the peers keep their shared memory until the leader read it
   }
+  // CTA pairs: rank 0's MMAs read both CTAs' shared and tensor memory, and
+  // both free the pair's columns together
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR)
+      tc::tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      tc::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -813,6 +942,7 @@ struct RingPlan {
   int a_stages = 0, raw_stages = 0;
 };
 std::atomic<int> g_ring_a{0}, g_ring_raw{0};  // debug override (0 = automatic)
+std::atomic<int> g_pair{0};                    // CTA pairs: 1 = where they fit, 0 = never (the default)
 
 // Raw W ring depth from the number of stages that fit. A converter group
 // waits on a raw slot's next phase by parity, which is sound only if it has
@@ -886,14 +1016,15 @@ int pick_split(int64_t tiles, int nraw_all, size_t smem) {
 // Lets a kernel instance use up to the per-block opt-in limit of shared
 // memory (once per device); the occupancy queries and launches below then
 // see the real request.
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool PAIR = false>
 cudaError_t allow_full_smem() {
   static int configured[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
     const int mx = std::min(device_info().max_smem_optin, 227 * 1024);
-    const cudaError_t e = cudaFuncSetAttribute(gemm_tma_kernel<FMT, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    const cudaError_t e =
+        cudaFuncSetAttribute(gemm_tma_kernel<FMT, EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -929,6 +1060,47 @@ int pick_split_query(int64_t tiles, int nraw_all, size_t smem) {
   return 1;
 }
 
+// CTA pairs: how many clusters of two CTAs with `smem` bytes each are
+// resident at once (a GPC with an odd number of free SMs leaves one idle).
+// Remembered per (device, shared memory).
+template <int FMT>
+int pair_slots(size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, size_t>, int> cache;
+  const auto key = std::make_tuple(current_device(), smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int active = 0;
+  if (allow_full_smem<FMT, epi::kPlain, true>() == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(device_info().sm_count));
+    cfg.blockDim = dim3(kPairThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&active, gemm_tma_kernel<FMT, epi::kPlain, true>, &cfg) != cudaSuccess)
+      active = 0;
+  }
+  cudaGetLastError();  // a refused query is not an error of the call
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = active;
+  return active;
+}
+
+int pair_slots_fmt(int fmt, size_t smem) {
+  if (fmt == LQ_FMT_F16) return pair_slots<LQ_FMT_F16>(smem);
+  if (fmt == LQ_FMT_Q8_0) return pair_slots<LQ_FMT_Q8_0>(smem);
+  return pair_slots<LQ_FMT_Q4_0>(smem);
+}
+
 int pick_split_fmt(int fmt, int64_t tiles, int nraw_all, size_t smem) {
   if (fmt == LQ_FMT_F16) return pick_split<LQ_FMT_F16>(tiles, nraw_all, smem);
   if (fmt == LQ_FMT_Q8_0) return pick_split<LQ_FMT_Q8_0>(tiles, nraw_all, smem);
@@ -943,6 +1115,7 @@ int pick_split_fmt(int fmt, int64_t tiles, int nraw_all, size_t smem) {
 // CTAs stream its tiles with TMA.
 struct TmaLaunch {
   int bt = 0, split = 1, stages = 0, raw_stages = 0, a_res = 0, a_tiles = 0, w_col0 = 256;
+  int pair = 0;  // CTA pairs (each CTA's A tiles hold bt / 2 token rows)
 };
 
 TmaLaunch plan_tma(const MatmulArgs& a) {
@@ -980,45 +1153,66 @@ TmaLaunch plan_tma(const MatmulArgs& a) {
     pl.stages = std::min(kMaxSlots, (512 - pl.w_col0) / 64);
     pl.raw_stages = raw_ring_depth(a.fmt, std::min<long long>(a.fmt == LQ_FMT_F16 ? 6 : 4, (budget - a_bytes) / raw));
   }
+  // CTA pairs: streamed A without a K split, an even number of W row tiles
+  // (tiles 2i and 2i + 1 pair up), and no more waves of pairs than of
+  // single CTAs (one an SM). Each CTA's A tiles then hold bt / 2 rows, so
+  // the rings are planned for that.
+  const int64_t row_tiles = (a.N + bn - 1) / bn;
+  if (!sw && !pl.a_res && pl.split == 1 && row_tiles % 2 == 0 && g_pair.load() != 0) {
+    const RingPlan hp = ring_plan(a.fmt, pl.bt / 2);
+    const int slots =
+        hp.a_stages >= 2 ? pair_slots_fmt(a.fmt, tma_smem_bytes(a.fmt, pl.bt / 2, hp.a_stages, hp.raw_stages)) : 0;
+    const int64_t sms = std::max(di.sm_count, 1);
+    if (slots > 0 && (tiles / 2 + slots - 1) / slots <= (tiles + sms - 1) / sms) {
+      pl.pair = 1;
+      pl.stages = hp.a_stages;
+      pl.raw_stages = hp.raw_stages;
+      pl.a_tiles = hp.a_stages;
+    }
+  }
   return pl;
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool PAIR = false>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              TmaGemmParams p);
 
 template <int FMT>
 lq_status launch_gemm_fmt(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
-                          const TmaGemmParams& p) {
+                          const TmaGemmParams& p, bool pair) {
   switch (a.epi) {
-    case epi::kPlain: return launch_gemm_kernel<FMT, epi::kPlain>(a, tmW, tmA, p);
-    case epi::kResidual: return launch_gemm_kernel<FMT, epi::kResidual>(a, tmW, tmA, p);
+    case epi::kPlain:
+      return pair ? launch_gemm_kernel<FMT, epi::kPlain, true>(a, tmW, tmA, p)
+                  : launch_gemm_kernel<FMT, epi::kPlain>(a, tmW, tmA, p);
+    case epi::kResidual:
+      return pair ? launch_gemm_kernel<FMT, epi::kResidual, true>(a, tmW, tmA, p)
+                  : launch_gemm_kernel<FMT, epi::kResidual>(a, tmW, tmA, p);
     case epi::kSwiglu: return launch_gemm_kernel<FMT, epi::kSwiglu>(a, tmW, tmA, p);
     default: return LQ_ERR_UNSUPPORTED;
   }
 }
 
 lq_status launch_gemm_epi(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
-                          const TmaGemmParams& p) {
-  if (a.fmt == LQ_FMT_F16) return launch_gemm_fmt<LQ_FMT_F16>(a, tmW, tmA, p);
-  if (a.fmt == LQ_FMT_Q8_0) return launch_gemm_fmt<LQ_FMT_Q8_0>(a, tmW, tmA, p);
-  return launch_gemm_fmt<LQ_FMT_Q4_0>(a, tmW, tmA, p);
+                          const TmaGemmParams& p, bool pair) {
+  if (a.fmt == LQ_FMT_F16) return launch_gemm_fmt<LQ_FMT_F16>(a, tmW, tmA, p, pair);
+  if (a.fmt == LQ_FMT_Q8_0) return launch_gemm_fmt<LQ_FMT_Q8_0>(a, tmW, tmA, p, pair);
+  return launch_gemm_fmt<LQ_FMT_Q4_0>(a, tmW, tmA, p, pair);
 }
 
-template <int FMT, int EPI>
+template <int FMT, int EPI, bool PAIR>
 lq_status launch_gemm_kernel(const MatmulArgs& a, const CUtensorMap& tmW, const CUtensorMap& tmA,
                              TmaGemmParams p) {
-  auto kern = gemm_tma_kernel<FMT, EPI>;
+  auto kern = gemm_tma_kernel<FMT, EPI, PAIR>;
   const int bn = EPI == epi::kSwiglu ? kBN / 2 : kBN;  // outputs per tile
-  const size_t smem = tma_smem_bytes(FMT, p.bt, p.a_tiles, p.raw_stages);
+  const size_t smem = tma_smem_bytes(FMT, PAIR ? p.bt / 2 : p.bt, p.a_tiles, p.raw_stages);
   {
-    const cudaError_t e = allow_full_smem<FMT, EPI>();
+    const cudaError_t e = allow_full_smem<FMT, EPI, PAIR>();
     if (e != cudaSuccess) return cuda_status(e);
   }
   const dim3 grid(static_cast<unsigned>((a.N + bn - 1) / bn * p.split),
                   static_cast<unsigned>((a.M + p.bt - 1) / p.bt));
-  cudaError_t e = launch_pdl_cluster(kern, grid, dim3(kTmaThreads), smem, a.stream,
-                                     static_cast<unsigned>(p.split), tmW, tmA, p);
+  cudaError_t e = launch_pdl_cluster(kern, grid, dim3(PAIR ? kPairThreads : kTmaThreads), smem, a.stream,
+                                     PAIR ? 2u : static_cast<unsigned>(p.split), tmW, tmA, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   return cuda_status(e);
 }
@@ -1039,6 +1233,8 @@ void set_gemm_rings(int a_stages, int raw_stages) {
   g_ring_a.store(a_stages);
   g_ring_raw.store(raw_stages);
 }
+
+void set_gemm_pairs(bool on) { g_pair.store(on ? 1 : 0); }
 
 bool gemm_tma_eligible(const MatmulArgs& a) {
   if (a.M < 2 || a.K % kstep_multiple(a.fmt) != 0) return false;
@@ -1149,7 +1345,7 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16) {
   if (!pl.a_res) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(bt)};
+    cuuint32_t box[2] = {64, static_cast<cuuint32_t>(pl.pair ? bt / 2 : bt)};
     cuuint32_t es[2] = {1, 1};
     if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a16, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1173,7 +1369,9 @@ lq_status launch_gemm_tma_ws(const MatmulArgs& a, void* a16) {
   p.a_perm = a.a_perm ? 1 : 0;
   p.wait_ns = wait_limit_ns();
   p.wait_iters = wait_limit_iters();
-  return launch_gemm_epi(a, tmW, tmA, p);
+  const lq_status st = launch_gemm_epi(a, tmW, tmA, p, pl.pair != 0);
+  if (st == LQ_OK && pl.pair) count_route(7);
+  return st;
 }
 
 }  // namespace lq

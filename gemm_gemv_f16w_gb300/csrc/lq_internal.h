@@ -79,6 +79,7 @@ lq_status launch_gemm_small(const MatmulArgs& a);
 bool gemm_small_eligible(const MatmulArgs& a);
 // TMA GEMM ring-depth override (0 = automatic): A stages, raw W stages.
 void set_gemm_rings(int a_stages, int raw_stages);
+void set_gemm_pairs(bool on);
 
 // Argmax (lq_gemv_argmax, lq_argmax_f32). launch_gemv_argmax returns
 // LQ_ERR_UNSUPPORTED, launching nothing, outside the streaming GEMV's fast

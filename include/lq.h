@@ -325,7 +325,8 @@ const char* lq_version(void);
  *        (LQ_ERR_UNSUPPORTED outside its shapes).
  * lq_debug_route_count(r) counts launches taken by route r (r = 0 counts
  * the fast GEMV, r = 4 the decode chain, r = 6 the A pre-pass launches of
- * route 2); counters are process-wide. */
+ * route 2, r = 7 the route-2 GEMMs run as CTA pairs); counters are
+ * process-wide. */
 lq_status lq_debug_force_route(int route);
 uint64_t  lq_debug_route_count(int route);
 void      lq_debug_reset_counts(void);
@@ -349,6 +350,13 @@ lq_status lq_debug_gemv_plan(int ctas_per_sm, int rows_per_stage, int smem_bytes
  * ring where it would otherwise be resident (small M), so that the two ways
  * of staging A can be compared. For tuning sweeps; results do not change. */
 lq_status lq_debug_gemm_rings(int a_stages, int raw_stages);
+/* on != 0: the tensor-core GEMM runs its CTAs in pairs (W row tiles 2i and
+ * 2i + 1 on one 256-row cta_group::2 MMA, each CTA holding half of the
+ * token tile) wherever A is streamed without a K split, the tile count is
+ * even and the pairs need no more waves than single CTAs; on = 0 (the
+ * default): never. Both give the same results; pairs measured slower, so
+ * this is for comparisons. */
+void      lq_debug_gemm_pairs(int on);
 
 #ifdef __cplusplus
 }
