@@ -128,13 +128,20 @@ struct Q8Slice {
 // Q4_0 (18-byte blocks): the lane's block spans five words starting at word
 // 9l of the segment (+4 for odd blocks); 9 is odd, so again conflict-free.
 // Byte j of the 16 nibble bytes holds q_j (low nibble) and q_{j+16} (high).
-// For a word of four such bytes, masking with 0x0F0F0F0F (and the same after
-// a 4-bit shift) leaves four codes as bytes, and each byte goes into the
-// mantissa of 2^23 with one byte-permute as in Q8_0; one packed add of
-// -(2^23 + 8) per pair gives q - 8 exactly. (Pulling each nibble in place
-// with its own scale, one fma per pair, needs four constant pairs per word
-// and measured about 30 % more instructions.) The words are aligned by the
-// same funnel shift as Q8_0's, one code path for both parities.
+// For a word of four such bytes, masking with 0x0F0F0F0F leaves the four low
+// codes as bytes and masking with 0xF0F0F0F0 the four high codes times 16
+// (no shift); each byte goes into the mantissa of 2^23 with one byte-permute
+// as in Q8_0, and one packed add per pair gives q - 8 exactly, or 16 (q - 8)
+// with Q8_0's bias of 2^23 + 128. The high half's partial sums are thus 16
+// times the products' and come back at the block's end with one exact
+// packed multiply-add by 1/16 in place of the add: scaling by 16 commutes
+// with rounding, so the sums are the same bits as with the codes themselves
+// (outside f32's subnormal range, where they are closer), for activations
+// below about 2^119 in magnitude (2^123 with the codes themselves). (Pulling
+// each nibble in place with its own scale, one fma per pair, needs four
+// constant pairs per word and measured about 30 % more instructions.) The
+// words are aligned by the same funnel shift as Q8_0's, one code path for
+// both parities.
 template <int CPW>
 struct Q4Slice {
   float2 a[CPW][16];       // a[2t], a[2t+1]: elements 4t .. 4t+3; a[8+2t], a[9+2t]: 16+4t ..
@@ -169,23 +176,24 @@ struct Q4Slice {
     const float d = f16_lo(w[0] >> (odd ? 16 : 0));
     const uint32_t sh = odd ? 32u : 16u;
     const float2 m8 = make_float2(-kMagicQ4, -kMagicQ4);
+    const float2 m128 = make_float2(-kMagicS8, -kMagicS8);  // 2^23 + 16 q - (2^23 + 128) = 16 (q - 8)
     float2 acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t x = __funnelshift_rc(w[i], w[i + 1], sh);  // bytes 4i .. 4i+3
-      const uint32_t lo = x & 0x0F0F0F0Fu, hi = (x >> 4) & 0x0F0F0F0Fu;
+      const uint32_t lo = x & 0x0F0F0F0Fu, hi16 = x & 0xF0F0F0F0u;
       const float2 l01 = fadd2(make_float2(s8_to_magic(lo, 0), s8_to_magic(lo, 1)), m8);
       const float2 l23 = fadd2(make_float2(s8_to_magic(lo, 2), s8_to_magic(lo, 3)), m8);
-      const float2 h01 = fadd2(make_float2(s8_to_magic(hi, 0), s8_to_magic(hi, 1)), m8);
-      const float2 h23 = fadd2(make_float2(s8_to_magic(hi, 2), s8_to_magic(hi, 3)), m8);
+      const float2 h01 = fadd2(make_float2(s8_to_magic(hi16, 0), s8_to_magic(hi16, 1)), m128);
+      const float2 h23 = fadd2(make_float2(s8_to_magic(hi16, 2), s8_to_magic(hi16, 3)), m128);
       acc[0] = ffma2(l01, a[c][2 * i], acc[0]);
       acc[1] = ffma2(l23, a[c][2 * i + 1], acc[1]);
-      acc[2] = ffma2(h01, a[c][8 + 2 * i], acc[2]);
+      acc[2] = ffma2(h01, a[c][8 + 2 * i], acc[2]);  // 16 x the high codes' products
       acc[3] = ffma2(h23, a[c][9 + 2 * i], acc[3]);
     }
-    const float2 s = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+    const float2 s = ffma2(fadd2(acc[2], acc[3]), make_float2(0.0625f, 0.0625f), fadd2(acc[0], acc[1]));
     return d * (s.x + s.y);
   }
 };
