@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(batch_warps(FMT, MT) * 32, 1) gemv_batch_kerne
   if (warp < active && nrows > 0) {
     if (FMT == LQ_FMT_F16) {
       // One lead thread waits for the copy of A under the time limit; the
-      // other consumers follow its verdict (a named barrier has no time
+      // other consumers follow its outcome (a named barrier has no time
       // limit, so every consumer has to reach it) and then observe the
       // landed copy themselves.
       if (threadIdx.x == 0 && !mbar_wait(&hd.a_bar, 0, p.wait_ns, p.wait_iters)) {

@@ -96,7 +96,7 @@ struct ChainHeader {
   uint64_t red_full[kChainMaxStages];
   uint64_t a_landed;               // A_j in the staging area (quantised formats)
   uint64_t a_full[2], a_empty[2];  // A_j ready for the slices / every consumer warp read it
-  volatile int a_go;               // the lead activation thread's verdict for the problem
+  volatile int a_go;               // the lead activation thread's outcome for the problem
   unsigned fin[kChainMax];         // finished stages of each problem on this CTA
   int row0[kChainMax], nrows[kChainMax], nstage[kChainMax];  // each problem's rows and stages here
   volatile int abort;
