@@ -5,8 +5,9 @@ row ranges of its bulk weight copies) before the access; a failed check
 records LQ_ERR_BOUNDS and skips the access instead of faulting. This test
 builds it and, in a child process that loads only the debug library
 (LQ_LIBRARY=debug), runs every route on small odd shapes (ragged row counts,
-partial tiles and stages, K not a multiple of the fast paths' steps): each
-call must leave the status word clean and match the CPU oracle.
+partial tiles and stages, K not a multiple of the fast paths' steps), and the
+opt-in CTA pairs of the tensor-core GEMM on one ragged shape: each call must
+leave the status word clean and match the CPU oracle.
 """
 import os
 import subprocess
@@ -115,6 +116,23 @@ for fmt in ("f16", "q8_0", "q4_0", "q4_0i"):
         y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
         check(C.cpu().numpy(), y, tol, f"noalloc {fmt}")
         runs += 1
+# the tensor-core GEMM as CTA pairs (opt-in): ragged token and W tiles
+for fmt in ("f16", "q8_0", "q4_0"):
+    M, N, K = 1000, 1000, 1024
+    W, A = synthetic.draw(M, N, K, seed=11)
+    Wd = to_dev(lq.pack(fmt, W).reshape(-1).view(np.uint8), dev)
+    C = nan_filled(M, N, dev)
+    lq.reset_counts()
+    lq.gemm_pairs(True)
+    try:
+        getattr(lq, f"lq_gemm_{fmt}")(A.to(dev), Wd, C, M, N, K)
+    finally:
+        lq.gemm_pairs(False)
+    clean(f"pairs {fmt}")
+    assert lq.route_count(7) == 1
+    y, tol = O.reference(fmt, A.numpy(), O.pack(fmt, W.numpy()), N, K, tensor_core=True)
+    check(C.cpu().numpy(), y, tol, f"pairs {fmt}")
+    runs += 1
 x = torch.randn(5003).to(dev)
 v, i, w = lq.topk_buffers(5003, 17, dev)
 lq.lq_topk_f32(x, 5003, 17, v, i, w)
