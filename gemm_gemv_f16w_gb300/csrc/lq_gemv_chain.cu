@@ -543,7 +543,12 @@ lq_status plan_chain(int fmt, const lq_gemv_problem* problems, int count, ChainP
   // row-group its slots, and the ring at least two
   const long long red_slot = 2LL * kChainRows * p.nk * static_cast<long long>(sizeof(float));
   const int slots_per_group = p.publish ? kSlotsDependent : kSlotsIndependent;
-  const long long per_slot = budget / std::max(2, slots_per_group * p.nr);
+  // independent problems keep at least three slots in the ring: with a single
+  // row-group (f16 beyond K = 2048) two slots per group meant two stages of
+  // eight rows; three of seven measured 5.10 against 5.55 us a 4096 x 4096
+  // f16 GEMV (the quantised plans, four row-groups, are unchanged)
+  const int min_slots = p.publish ? 2 : 3;
+  const long long per_slot = budget / std::max(min_slots, slots_per_group * p.nr);
   p.rows_per_stage = static_cast<int>(std::min<long long>(kChainRows, (per_slot - red_slot) / rb_max));
   if (p.rows_per_stage < 1)
     p.rows_per_stage = static_cast<int>(std::min<long long>(kChainRows, (budget / 2 - red_slot) / rb_max));
