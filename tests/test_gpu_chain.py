@@ -188,3 +188,38 @@ def test_chain_refuses_shapes_outside_its_path(lq, cuda_dev):
     assert lq.lq_gemv_chain(fmt, [(A, Wd, C, N, K, 0)]) == lq.LQ_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert torch.isnan(C).all()
+
+
+@pytest.mark.parametrize("K", [2304, 4096])
+def test_chain_f16_single_row_group(lq, cuda_dev, K):
+    """f16 beyond K = 2048 (up to 4096, the chain's f16 limit): one row-group
+    of consumer warps, whose ring the plan keeps at three slots or more for
+    independent problems; every problem against the oracle. Then a dependent
+    pair (its second problem starts a new launch)."""
+    fmt = "f16"
+    items, refs = [], []
+    for j, N in enumerate([4096, 1000, 152, 2048]):
+        Wn, Wd = _weights(lq, fmt, N, K, 300 + j, cuda_dev)
+        A = torch.randn(K, generator=torch.Generator().manual_seed(j))
+        C = nan_filled(1, N, cuda_dev)[0]
+        items.append((A.to(cuda_dev), Wd, C, N, K, 0))
+        refs.append((Wn, A.numpy(), C))
+    lq.reset_counts()
+    assert _run_chain(lq, fmt, items) == lq.LQ_OK
+    assert lq.last_device_error() == lq.LQ_OK and lq.route_count(4) == 1
+    for Wn, a, C in refs:
+        N = Wn.shape[0]
+        y, tol = O.reference(fmt, a[None, :], O.pack(fmt, Wn), N, K)
+        check(torch.from_numpy(C.cpu().numpy()[None, :]), y, tol, f"f16 chain N={N} K={K}")
+    # a dependent pair: the second problem reads the first one's output
+    Wn0, Wd0 = _weights(lq, fmt, K, K, 400, cuda_dev)
+    Wn1, Wd1 = _weights(lq, fmt, 512, K, 401, cuda_dev)
+    A = torch.randn(K, generator=torch.Generator().manual_seed(9))
+    C0, C1 = nan_filled(1, K, cuda_dev)[0], nan_filled(1, 512, cuda_dev)[0]
+    assert _run_chain(lq, fmt, [(A.to(cuda_dev), Wd0, C0, K, K, 0), (C0, Wd1, C1, 512, K, 1)]) == lq.LQ_OK
+    assert lq.last_device_error() == lq.LQ_OK
+    c0 = C0.cpu().numpy()
+    y0, t0 = O.reference(fmt, A.numpy()[None, :], O.pack(fmt, Wn0), K, K)
+    check(torch.from_numpy(c0[None, :]), y0, t0, "f16 dependent step 0")
+    y1, t1 = O.reference(fmt, c0[None, :], O.pack(fmt, Wn1), 512, K)
+    check(torch.from_numpy(C1.cpu().numpy()[None, :]), y1, t1, "f16 dependent step 1")
